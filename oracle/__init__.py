@@ -1,0 +1,188 @@
+"""fp64 CPU oracle for paged decode/verify attention, KV append and
+speculative acceptance.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the product package
+(``spec_verify_paged_gb300``) never does, and this package never imports it.
+The arithmetic lives in ``oracle.c`` (plain single-threaded C, fp64); this
+module only builds it with gcc and marshals numpy arrays into it.
+
+Which page passage each function follows is stated in ``oracle.c``:
+exact attention from the lesson "KV cache & Flash Attention" (section
+"FlashAttention -- the tiling trick") and the StreamingLLM page (section "The
+softmax problem"); masks from "How speculative decoding doubles LLM speed"
+(step 2, verification) and the StreamingLLM page (section "The StreamingLLM
+solution"); acceptance from "How speculative decoding doubles LLM speed"
+(step 3, sampling).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+BOUNDARY_EPS = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so in place with gcc (-O2, no fast-math, no threads)."""
+    stale = (not os.path.exists(_LIB)) or any(
+        os.path.getmtime(s) > os.path.getmtime(_LIB) for s in (_SRC, _HDR))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+            lib.oracle_paged_attention.argtypes = (
+                [i32] * 8 + [vp] * 5 + [i32, i32, i32, f32, vp, i64, vp, vp])
+            lib.oracle_paged_attention.restype = i32
+            lib.oracle_paged_attention_tiled.argtypes = (
+                [i32] * 8 + [vp] * 5 + [i32, i32, i32, f32, i32, i32, vp, vp])
+            lib.oracle_paged_attention_tiled.restype = i32
+            lib.oracle_kv_append.argtypes = [i32] * 7 + [vp] * 6 + [i32]
+            lib.oracle_kv_append.restype = i32
+            lib.oracle_spec_accept.argtypes = (
+                [i32] * 3 + [vp] * 8 + [ctypes.c_double])
+            lib.oracle_spec_accept.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(arr):
+    if arr.dtype == np.float32:
+        return F32
+    if arr.dtype == np.uint16:  # raw bfloat16 bit patterns
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+def paged_attention(q, k_cache, v_cache, block_table, seq_lens, q_len,
+                    n_sink=0, window=0, scale=None, rows=None, tiled=None):
+    """Exact attention over the paged cache, in fp64.
+
+    q: [B, q_len, Hq, D]; k_cache/v_cache: [num_blocks, Hkv, block_size, D]
+    (float32 or uint16 bf16 bits, same dtype as q); block_table [B, max_blocks]
+    int32; seq_lens [B] int32 (including the q_len new rows).
+    rows: optional flat row ids (b*q_len + i)*Hq + h; then returns
+    (out [n, D], lse [n]).  Otherwise returns out [B, q_len, Hq, D] and
+    lse [B, q_len, Hq] (float64).
+    tiled=(tile, n_splits) runs the tiled/split online-softmax variant.
+    """
+    lib = _load()
+    B, ql, Hq, D = q.shape
+    assert ql == q_len
+    nb, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    code = _dtype_code(q)
+    assert _dtype_code(k_cache) == code and _dtype_code(v_cache) == code
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    q = _c(q, q.dtype)
+    kc = _c(k_cache, k_cache.dtype)
+    vc = _c(v_cache, v_cache.dtype)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    if tiled is not None:
+        out = np.zeros((B, q_len, Hq, D), np.float64)
+        lse = np.zeros((B, q_len, Hq), np.float64)
+        st = lib.oracle_paged_attention_tiled(
+            B, Hq, Hkv, D, bs, mb, nb, code, _ptr(q), _ptr(kc), _ptr(vc),
+            _ptr(bt), _ptr(sl), q_len, n_sink, window, float(scale),
+            int(tiled[0]), int(tiled[1]), _ptr(out), _ptr(lse))
+    elif rows is None:
+        out = np.zeros((B, q_len, Hq, D), np.float64)
+        lse = np.zeros((B, q_len, Hq), np.float64)
+        st = lib.oracle_paged_attention(
+            B, Hq, Hkv, D, bs, mb, nb, code, _ptr(q), _ptr(kc), _ptr(vc),
+            _ptr(bt), _ptr(sl), q_len, n_sink, window, float(scale), None, 0,
+            _ptr(out), _ptr(lse))
+    else:
+        r = _c(rows, np.int64)
+        out = np.zeros((r.size, D), np.float64)
+        lse = np.zeros((r.size,), np.float64)
+        st = lib.oracle_paged_attention(
+            B, Hq, Hkv, D, bs, mb, nb, code, _ptr(q), _ptr(kc), _ptr(vc),
+            _ptr(bt), _ptr(sl), q_len, n_sink, window, float(scale), _ptr(r),
+            r.size, _ptr(out), _ptr(lse))
+    if st != 0:
+        raise ValueError(f"oracle_paged_attention failed with status {st}")
+    return out, lse
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens):
+    """Scatter k_new/v_new [B, n_new, Hkv, D] into copies of the caches.
+    Returns the updated (k_cache, v_cache); the inputs are not modified."""
+    lib = _load()
+    B, n_new, Hkv, D = k_new.shape
+    nb, Hkv2, bs, D2 = k_cache.shape
+    assert Hkv2 == Hkv and D2 == D and k_new.dtype == k_cache.dtype
+    kc = np.array(k_cache, copy=True, order="C")
+    vc = np.array(v_cache, copy=True, order="C")
+    kn = _c(k_new, k_new.dtype)
+    vn = _c(v_new, v_new.dtype)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    st = lib.oracle_kv_append(B, Hkv, D, bs, bt.shape[1], nb, kc.itemsize,
+                              _ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(bt),
+                              _ptr(sl), n_new)
+    if st != 0:
+        raise ValueError(f"oracle_kv_append failed with status {st}")
+    return kc, vc
+
+
+def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
+                eps=BOUNDARY_EPS):
+    """Literal rejection-sampling loop in fp64.
+
+    Returns dict(out_tokens [B, K+1] int32 (-1 padded), n_accepted [B] int32,
+    near_boundary [B] int32, residual_fallback [B] int32)."""
+    lib = _load()
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    assert draft_logits.shape == (B, K, V)
+    assert draft_tokens.shape == (B, K) and uniforms.shape == (B, K + 1)
+    tl = _c(target_logits, np.float32)
+    dl = _c(draft_logits, np.float32)
+    dt = _c(draft_tokens, np.int32)
+    un = _c(uniforms, np.float32)
+    out = np.full((B, K + 1), -1, np.int32)
+    nacc = np.zeros((B,), np.int32)
+    near = np.zeros((B,), np.int32)
+    fb = np.zeros((B,), np.int32)
+    st = lib.oracle_spec_accept(B, K, V, _ptr(tl), _ptr(dl), _ptr(dt), _ptr(un),
+                                _ptr(out), _ptr(nacc), _ptr(near), _ptr(fb),
+                                float(eps))
+    if st != 0:
+        raise ValueError(f"oracle_spec_accept failed with status {st}")
+    return {"out_tokens": out, "n_accepted": nacc, "near_boundary": near,
+            "residual_fallback": fb}

@@ -1,0 +1,417 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the product path.  It shares no
+ * code with the CUDA library.  Single-threaded, no vectorisation tricks,
+ * no blocking or reordering beyond what the definitions below state.
+ *
+ * Sources (web pages; quoted by title and section):
+ *  [SD]  "How speculative decoding doubles LLM speed without quality loss"
+ *        (dothoosh.com): sections "The speculative execution cycle"
+ *        (step 2 verification, step 3 sampling) and "Absolute mathematical
+ *        exactness".
+ *  [KV]  "KV cache & Flash Attention" lesson (nextadmin.net): sections
+ *        "KV-cache math", "FlashAttention -- the tiling trick",
+ *        "PagedAttention -- the KV cache as virtual memory",
+ *        "Implementation, step 2: tiled softmax".
+ *  [SL]  "How StreamingLLM stabilizes million-token streams via attention
+ *        sinks" (dothoosh.com): sections "The softmax problem",
+ *        "Why sliding windows fail", "The StreamingLLM solution".
+ *  [SP]  "Speculative decoding: how AI models get faster without getting
+ *        bigger" (aioapex.com): section "What speculative decoding does".
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes): query i of a q_len-row verify block sits at absolute position
+ * t_i = seq_len - q_len + i and sees keys j <= t_i (causal inside the draft,
+ * [SD] step 2); with window > 0 a key is visible iff j < n_sink or
+ * j > t_i - window (sinks plus the last `window` keys, the query's own key
+ * included, [SL] "The StreamingLLM solution"); window == 0 disables both;
+ * GQA maps query head h to kv head floor(h / (Hq/Hkv)); lse is the natural
+ * log-sum-exp of the scaled scores over the visible set.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- element access: the stored bits widened to fp64 ------------------ */
+
+static double widen(const void *base, size_t idx, int dtype) {
+  if (dtype == 0) return (double)((const float *)base)[idx];
+  /* bfloat16: the upper 16 bits of an IEEE fp32 pattern. */
+  uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* ---- mask: [SD] step 2 (causal) and [SL] (sinks + sliding window) ------ */
+
+static int key_visible(long j, long t, int n_sink, int window) {
+  if (j < 0 || j > t) return 0;
+  if (window == 0) return 1;
+  return (j < n_sink) || (j > t - window);
+}
+
+/* Flat element offset of row `pos` of the logical sequence b, kv head g.
+ * [KV] "PagedAttention": logical position -> (block_table[b][pos/bs], pos%bs).
+ * Returns -1 if the physical block id is out of range. */
+static long kv_offset(const int32_t *block_table, int max_blocks, int b,
+                      long pos, int block_size, int num_kv_heads, int g,
+                      int head_dim, int num_blocks) {
+  long lb = pos / block_size;
+  if (lb >= max_blocks) return -1;
+  int32_t phys = block_table[(long)b * max_blocks + lb];
+  if (phys < 0 || phys >= num_blocks) return -1;
+  long row = pos % block_size;
+  return (((long)phys * num_kv_heads + g) * block_size + row) * head_dim;
+}
+
+static int check_sizes(int batch, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, int max_blocks,
+                       int num_blocks, int dtype, int q_len, int n_sink,
+                       int window) {
+  if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
+      block_size < 1 || max_blocks < 0 || num_blocks < 0 || q_len < 1 ||
+      n_sink < 0 || window < 0 || (dtype != 0 && dtype != 1))
+    return -1;
+  if (num_q_heads % num_kv_heads != 0) return -1;
+  return 0;
+}
+
+/* ---- exact attention: [KV] "FlashAttention" (S = QK^T, P = softmax(S),
+ * O = PV) and [SL] "The softmax problem" (softmax(QK^T/sqrt(d))V) -------- */
+
+int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int max_blocks_per_seq,
+                           int num_blocks, int dtype, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           const int64_t *rows, int64_t n_rows, double *out,
+                           double *lse) {
+  if (check_sizes(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                  max_blocks_per_seq, num_blocks, dtype, q_len, n_sink,
+                  window))
+    return -1;
+  const int64_t total_rows = (int64_t)batch * q_len * num_q_heads;
+  if (rows == NULL) n_rows = total_rows;
+  const int group = num_q_heads / num_kv_heads;
+  const double sc = (double)scale;
+
+  long max_len = 0;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] > max_len) max_len = seq_lens[b];
+  double *s = (double *)malloc(sizeof(double) * (size_t)(max_len + 1));
+  long *koff = (long *)malloc(sizeof(long) * (size_t)(max_len + 1));
+  if (!s || !koff) {
+    free(s);
+    free(koff);
+    return -1;
+  }
+  int status = 0;
+
+  for (int64_t n = 0; n < n_rows && status == 0; ++n) {
+    const int64_t row = rows ? rows[n] : n;
+    if (row < 0 || row >= total_rows) {
+      status = -1;
+      break;
+    }
+    const int h = (int)(row % num_q_heads);
+    const int i = (int)((row / num_q_heads) % q_len);
+    const int b = (int)(row / ((int64_t)num_q_heads * q_len));
+    const int g = h / group; /* GQA: contiguous head groups */
+    const long L = seq_lens[b];
+    if (L < q_len) {
+      status = -3;
+      break;
+    }
+    const long t = L - q_len + i; /* absolute position of query i */
+
+    /* 1. gather the visible keys and their scores */
+    long nv = 0;
+    for (long j = 0; j <= t; ++j) {
+      if (!key_visible(j, t, n_sink, window)) continue;
+      long off = kv_offset(block_table, max_blocks_per_seq, b, j, block_size,
+                           num_kv_heads, g, head_dim, num_blocks);
+      if (off < 0) {
+        status = -2;
+        break;
+      }
+      double dot = 0.0;
+      for (int d = 0; d < head_dim; ++d)
+        dot += widen(q, (size_t)row * head_dim + d, dtype) *
+               widen(k_cache, (size_t)off + d, dtype);
+      s[nv] = sc * dot;
+      koff[nv] = off;
+      ++nv;
+    }
+    if (status) break;
+
+    /* 2. softmax over the visible set, max-subtracted */
+    double m = -INFINITY;
+    for (long k = 0; k < nv; ++k)
+      if (s[k] > m) m = s[k];
+    double z = 0.0;
+    for (long k = 0; k < nv; ++k) z += exp(s[k] - m);
+
+    /* 3. O = P V */
+    double *o = out + (size_t)n * head_dim;
+    for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+    for (long k = 0; k < nv; ++k) {
+      double p = exp(s[k] - m) / z;
+      for (int d = 0; d < head_dim; ++d)
+        o[d] += p * widen(v_cache, (size_t)koff[k] + d, dtype);
+    }
+    lse[n] = m + log(z);
+  }
+  free(s);
+  free(koff);
+  return status;
+}
+
+/* ---- tiled variant: [KV] "FlashAttention -- the tiling trick" and
+ * "Implementation, step 2": a running (max, sum, accumulator) folded over
+ * blocks of keys, rescaled by exp(m_old - m_new); parts merged by LSE. ---- */
+
+int oracle_paged_attention_tiled(int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size,
+                                 int max_blocks_per_seq, int num_blocks,
+                                 int dtype, const void *q, const void *k_cache,
+                                 const void *v_cache,
+                                 const int32_t *block_table,
+                                 const int32_t *seq_lens, int q_len, int n_sink,
+                                 int window, float scale, int tile,
+                                 int n_splits, double *out, double *lse) {
+  if (check_sizes(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                  max_blocks_per_seq, num_blocks, dtype, q_len, n_sink,
+                  window) ||
+      tile < 1 || n_splits < 1)
+    return -1;
+  const int group = num_q_heads / num_kv_heads;
+  const double sc = (double)scale;
+  long max_len = 0;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] > max_len) max_len = seq_lens[b];
+  long *keys = (long *)malloc(sizeof(long) * (size_t)(max_len + 1));
+  double *part_o = (double *)malloc(sizeof(double) * (size_t)n_splits * head_dim);
+  double *part_lse = (double *)malloc(sizeof(double) * (size_t)n_splits);
+  double *acc = (double *)malloc(sizeof(double) * (size_t)head_dim);
+  double *sblk = (double *)malloc(sizeof(double) * (size_t)tile);
+  if (!keys || !part_o || !part_lse || !acc || !sblk) {
+    free(keys); free(part_o); free(part_lse); free(acc); free(sblk);
+    return -1;
+  }
+  int status = 0;
+  const int64_t total_rows = (int64_t)batch * q_len * num_q_heads;
+  for (int64_t row = 0; row < total_rows && status == 0; ++row) {
+    const int h = (int)(row % num_q_heads);
+    const int i = (int)((row / num_q_heads) % q_len);
+    const int b = (int)(row / ((int64_t)num_q_heads * q_len));
+    const int g = h / group;
+    const long L = seq_lens[b];
+    if (L < q_len) { status = -3; break; }
+    const long t = L - q_len + i;
+    long nv = 0;
+    for (long j = 0; j <= t; ++j) {
+      if (!key_visible(j, t, n_sink, window)) continue;
+      long off = kv_offset(block_table, max_blocks_per_seq, b, j, block_size,
+                           num_kv_heads, g, head_dim, num_blocks);
+      if (off < 0) { status = -2; break; }
+      keys[nv++] = off;
+    }
+    if (status) break;
+
+    for (int part = 0; part < n_splits; ++part) {
+      long lo = nv * part / n_splits, hi = nv * (part + 1) / n_splits;
+      double m = -INFINITY, ssum = 0.0;
+      for (int d = 0; d < head_dim; ++d) acc[d] = 0.0;
+      for (long start = lo; start < hi; start += tile) {
+        long cnt = (hi - start < tile) ? hi - start : tile;
+        double new_m = m;
+        for (long k = 0; k < cnt; ++k) {
+          double dot = 0.0;
+          for (int d = 0; d < head_dim; ++d)
+            dot += widen(q, (size_t)row * head_dim + d, dtype) *
+                   widen(k_cache, (size_t)keys[start + k] + d, dtype);
+          sblk[k] = sc * dot;
+          if (sblk[k] > new_m) new_m = sblk[k];
+        }
+        double exp_old = (m == -INFINITY) ? 0.0 : exp(m - new_m);
+        ssum *= exp_old;
+        for (int d = 0; d < head_dim; ++d) acc[d] *= exp_old;
+        for (long k = 0; k < cnt; ++k) {
+          double e = exp(sblk[k] - new_m);
+          ssum += e;
+          for (int d = 0; d < head_dim; ++d)
+            acc[d] += e * widen(v_cache, (size_t)keys[start + k] + d, dtype);
+        }
+        m = new_m;
+      }
+      if (hi > lo) {
+        for (int d = 0; d < head_dim; ++d)
+          part_o[(size_t)part * head_dim + d] = acc[d] / ssum;
+        part_lse[part] = m + log(ssum);
+      } else { /* an empty part carries zero weight */
+        for (int d = 0; d < head_dim; ++d) part_o[(size_t)part * head_dim + d] = 0.0;
+        part_lse[part] = -INFINITY;
+      }
+    }
+    /* merge the parts: weights exp(lse_part - lse_total) */
+    double mx = -INFINITY;
+    for (int part = 0; part < n_splits; ++part)
+      if (part_lse[part] > mx) mx = part_lse[part];
+    double wsum = 0.0;
+    for (int part = 0; part < n_splits; ++part)
+      if (part_lse[part] != -INFINITY) wsum += exp(part_lse[part] - mx);
+    double total = mx + log(wsum);
+    double *o = out + (size_t)row * head_dim;
+    for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+    for (int part = 0; part < n_splits; ++part) {
+      if (part_lse[part] == -INFINITY) continue;
+      double w = exp(part_lse[part] - total);
+      for (int d = 0; d < head_dim; ++d) o[d] += w * part_o[(size_t)part * head_dim + d];
+    }
+    lse[row] = total;
+  }
+  free(keys); free(part_o); free(part_lse); free(acc); free(sblk);
+  return status;
+}
+
+/* ---- KV append: [KV] "KV cache" (store K and V of every new token) and
+ * "PagedAttention" (logical position -> physical block, row) ------------ */
+
+int oracle_kv_append(int batch, int num_kv_heads, int head_dim, int block_size,
+                     int max_blocks_per_seq, int num_blocks, int elem_bytes,
+                     const void *k_new, const void *v_new, void *k_cache,
+                     void *v_cache, const int32_t *block_table,
+                     const int32_t *seq_lens, int n_new) {
+  if (batch < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 ||
+      n_new < 0 || (elem_bytes != 2 && elem_bytes != 4))
+    return -1;
+  const size_t row_bytes = (size_t)head_dim * elem_bytes;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens[b] < n_new) return -1;
+    for (int k = 0; k < n_new; ++k) {
+      long pos = (long)seq_lens[b] - n_new + k;
+      for (int g = 0; g < num_kv_heads; ++g) {
+        long off = kv_offset(block_table, max_blocks_per_seq, b, pos,
+                             block_size, num_kv_heads, g, head_dim, num_blocks);
+        if (off < 0) return -2;
+        size_t src = ((((size_t)b * n_new + k) * num_kv_heads) + g) * row_bytes;
+        memcpy((char *)k_cache + (size_t)off * elem_bytes,
+               (const char *)k_new + src, row_bytes);
+        memcpy((char *)v_cache + (size_t)off * elem_bytes,
+               (const char *)v_new + src, row_bytes);
+      }
+    }
+  }
+  return 0;
+}
+
+/* ---- speculative acceptance: [SD] "The speculative execution cycle",
+ * step 3, and [SP] "What speculative decoding does" ---------------------- */
+
+/* softmax of one logit row in fp64, max-subtracted */
+static void softmax_row(const float *logits, int vocab, double *p) {
+  double m = -INFINITY;
+  for (int x = 0; x < vocab; ++x)
+    if ((double)logits[x] > m) m = (double)logits[x];
+  double z = 0.0;
+  for (int x = 0; x < vocab; ++x) {
+    p[x] = exp((double)logits[x] - m);
+    z += p[x];
+  }
+  for (int x = 0; x < vocab; ++x) p[x] /= z;
+}
+
+/* Inverse-CDF draw in token-index order: the smallest x whose running sum of
+ * w exceeds u * sum(w); if rounding leaves none, the last x with w_x > 0.
+ * Sets *near when u*W lies within eps*W of the running sum at the chosen x or
+ * at the one before it. */
+static int inverse_cdf(const double *w, int vocab, double u, double eps,
+                       int *near) {
+  double total = 0.0;
+  for (int x = 0; x < vocab; ++x) total += w[x];
+  const double target = u * total;
+  double c = 0.0;
+  for (int x = 0; x < vocab; ++x) {
+    double prev = c;
+    c += w[x];
+    if (c > target) {
+      if (fabs(c - target) < eps * total || fabs(prev - target) < eps * total)
+        *near = 1;
+      return x;
+    }
+  }
+  *near = 1; /* the draw fell off the end by rounding */
+  for (int x = vocab - 1; x >= 0; --x)
+    if (w[x] > 0.0) return x;
+  return vocab - 1;
+}
+
+int oracle_spec_accept(int batch, int num_draft, int vocab,
+                       const float *target_logits, const float *draft_logits,
+                       const int32_t *draft_tokens, const float *uniforms,
+                       int32_t *out_tokens, int32_t *n_accepted,
+                       int32_t *near_boundary, int32_t *residual_fallback,
+                       double eps) {
+  if (batch < 0 || num_draft < 1 || vocab < 2) return -1;
+  const int K = num_draft;
+  double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *w = (double *)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !qd || !w) { free(p); free(qd); free(w); return -1; }
+  int status = 0;
+  for (int b = 0; b < batch && status == 0; ++b) {
+    int32_t *emit = out_tokens + (size_t)b * (K + 1);
+    const float *u = uniforms + (size_t)b * (K + 1);
+    int near = 0, fallback = 0, n_out = 0, accepted_all = 1;
+    for (int k = 0; k <= K; ++k) emit[k] = -1;
+    for (int i = 0; i < K; ++i) { /* every draft token must be a token id */
+      const int x = draft_tokens[(size_t)b * K + i];
+      if (x < 0 || x >= vocab) status = -4;
+    }
+    if (status) break;
+    for (int i = 0; i < K; ++i) {
+      const int x = draft_tokens[(size_t)b * K + i];
+      softmax_row(target_logits + ((size_t)b * (K + 1) + i) * vocab, vocab, p);
+      softmax_row(draft_logits + ((size_t)b * K + i) * vocab, vocab, qd);
+      /* accept iff r <= min(1, p(x)/q(x)); q(x) = 0 reads as ratio +inf */
+      const double r = (double)u[i];
+      const double ratio = (qd[x] > 0.0) ? p[x] / qd[x] : INFINITY;
+      if (fabs(r - ratio) < eps) near = 1;
+      if (r <= ratio) {
+        emit[n_out++] = x;
+        continue;
+      }
+      /* rejected at position i: resample from max(0, p - q) normalised */
+      double mass = 0.0;
+      for (int y = 0; y < vocab; ++y) {
+        w[y] = (p[y] - qd[y] > 0.0) ? p[y] - qd[y] : 0.0;
+        mass += w[y];
+      }
+      if (mass == 0.0) { /* impossible in exact arithmetic: sample p */
+        fallback = 1;
+        for (int y = 0; y < vocab; ++y) w[y] = p[y];
+      }
+      emit[n_out++] = inverse_cdf(w, vocab, (double)u[K], eps, &near);
+      n_accepted[b] = i;
+      accepted_all = 0;
+      break;
+    }
+    if (status) break;
+    if (accepted_all) {
+      /* every draft accepted: the bonus token from the last target row */
+      softmax_row(target_logits + ((size_t)b * (K + 1) + K) * vocab, vocab, p);
+      emit[n_out++] = inverse_cdf(p, vocab, (double)u[K], eps, &near);
+      n_accepted[b] = K;
+    }
+    if (near_boundary) near_boundary[b] = near;
+    if (residual_fallback) residual_fallback[b] = fallback;
+  }
+  free(p); free(qd); free(w);
+  return status;
+}

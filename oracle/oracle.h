@@ -1,0 +1,85 @@
+/*
+ * oracle.h -- plain, slow, single-threaded fp64 CPU oracle for paged
+ * decode/verify attention, KV append and speculative acceptance.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link
+ * or call this code: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no source, header, table or helper with
+ * the CUDA library; the two meet only through the seeded input arrays.
+ *
+ * Layouts (row-major, element counts):
+ *   q, out          [batch, q_len, num_q_heads, head_dim]   (q in `dtype`)
+ *   lse             [batch, q_len, num_q_heads]              natural log
+ *   k_cache,v_cache [num_blocks, num_kv_heads, block_size, head_dim]
+ *   block_table     [batch, max_blocks_per_seq]  int32
+ *   seq_lens        [batch] int32, logical length INCLUDING the q_len new rows
+ * dtype: 0 = IEEE fp32, 1 = bfloat16 given as raw 16-bit patterns.
+ */
+#ifndef SVP_ORACLE_H
+#define SVP_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exact attention by full materialisation over the logically gathered cache.
+ * rows (optional): flat query-row ids (b*q_len + i)*num_q_heads + h to
+ * compute; NULL computes every row in order.  out gets n_rows*head_dim
+ * doubles, lse n_rows doubles.  Returns 0, or -1 for bad sizes, -2 if a
+ * visible key maps to a block id outside [0, num_blocks), -3 if
+ * seq_len < q_len. */
+int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int max_blocks_per_seq,
+                           int num_blocks, int dtype, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           const int64_t *rows, int64_t n_rows, double *out,
+                           double *lse);
+
+/* The same quantity computed the tiled way: the visible keys of each row are
+ * cut into n_splits contiguous parts, each part is folded in `tile`-key
+ * blocks with a running (max, sum, accumulator), and the parts are merged by
+ * their log-sum-exp.  Self-check of the online-softmax algebra only. */
+int oracle_paged_attention_tiled(int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size,
+                                 int max_blocks_per_seq, int num_blocks,
+                                 int dtype, const void *q, const void *k_cache,
+                                 const void *v_cache,
+                                 const int32_t *block_table,
+                                 const int32_t *seq_lens, int q_len, int n_sink,
+                                 int window, float scale, int tile,
+                                 int n_splits, double *out, double *lse);
+
+/* Writes the n_new new K/V rows of every sequence at logical positions
+ * seq_lens[b]-n_new .. seq_lens[b]-1 into the paged caches (byte copy).
+ * k_new, v_new: [batch, n_new, num_kv_heads, head_dim] of elem_bytes each.
+ * Returns 0, -1 for bad sizes, -2 for a block id out of range. */
+int oracle_kv_append(int batch, int num_kv_heads, int head_dim, int block_size,
+                     int max_blocks_per_seq, int num_blocks, int elem_bytes,
+                     const void *k_new, const void *v_new, void *k_cache,
+                     void *v_cache, const int32_t *block_table,
+                     const int32_t *seq_lens, int n_new);
+
+/* Speculative acceptance, literal rejection-sampling loop.
+ *   target_logits [batch, K+1, vocab] fp32, draft_logits [batch, K, vocab]
+ *   draft_tokens [batch, K], uniforms [batch, K+1] in [0,1)
+ *   out_tokens [batch, K+1] (-1 padded), n_accepted [batch]
+ *   near_boundary [batch] (may be NULL): 1 if a decision of that sequence
+ *     fell within eps of its boundary (accept test: |r - p/q| < eps;
+ *     sampling: |u*W - C(x)| < eps*W at the chosen or preceding x).
+ *   residual_fallback [batch] (may be NULL): 1 if a rejection met a residual
+ *     of zero mass and p itself was sampled instead.
+ * Returns 0, -1 for bad sizes, -4 for a draft token outside [0, vocab). */
+int oracle_spec_accept(int batch, int num_draft, int vocab,
+                       const float *target_logits, const float *draft_logits,
+                       const int32_t *draft_tokens, const float *uniforms,
+                       int32_t *out_tokens, int32_t *n_accepted,
+                       int32_t *near_boundary, int32_t *residual_fallback,
+                       double eps);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
