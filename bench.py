@@ -1,0 +1,456 @@
+"""Benchmark: paged decode attention step on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--split-pages P]
+
+A step is one pass of the decode hot path over one batch: kv_append of the
+batch's new K/V rows into the paged cache, then paged_decode_attention of
+the new query rows over every cached row (decode-7b: 32 sequences, 32/32
+heads, head_dim 128, context U[512, 4096], bf16 16-token pages in a shuffled
+block table).  `value` is query tokens per second over the whole job; the
+KV-read bandwidth and its fraction of the measured HBM peak are in
+`roofline`.  Inputs are resident in HBM before the timed region; each step
+reads ~1.2 GB of KV, far more than the 129 MB L2, so no flush is needed.
+`e2e` repeats the step through the same public calls with the step's inputs
+copied from pinned host memory and its outputs copied back inside the timed
+region.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+
+--impl reference times that CPU oracle alone (the slow, obviously correct
+program the GPU results are checked against) on the same workload.
+
+Multi-GPU: one process per GPU under torchrun; each rank runs an
+independent replica of the workload (the path shards by sequence with no
+exchange), timing is the max over ranks, value is the sum of the work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from spec_verify_paged_gb300 import accounting as A  # noqa: E402
+from spec_verify_paged_gb300 import workloads as W  # noqa: E402
+
+METRIC = ("decode-attention query-tokens/s and achieved KV-read HBM GB/s "
+          "(% of GB300 peak)")
+UNIT = "query-tokens/s"
+PROFILE = os.path.join(ROOT, "profiles", "ncu_paged_attention_decode-7b.md")
+ATTN_SRC = os.path.join(ROOT, "spec_verify_paged_gb300", "csrc", "attention.cu")
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current attention kernel source; else None."""
+    if not os.path.exists(PROFILE):
+        return None
+    sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("attention.cu sha256[:16]") != sha:
+        return None
+    try:
+        return int(vals["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        if not rows:  # a very short region: the nearest samples around it
+            near = sorted(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))
+            rows = [s for _, s in near[:3]]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def to_dev(a, dev):
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def to_pinned(a):
+    import torch
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.pin_memory()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time (all ranks must call this)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------
+
+def oracle_sample(wl, n_seqs, start=0):
+    """Run the fp64 oracle on n_seqs sequences of the workload (all heads,
+    all query rows); returns (seconds, query tokens)."""
+    import oracle
+    oracle.build()
+    B = wl.cfg.batch
+    per = wl.q_len * wl.cfg.num_q_heads
+    seqs = [(start + i) % B for i in range(n_seqs)]
+    rows = np.concatenate([np.arange(b * per, (b + 1) * per) for b in seqs])
+    t = time.perf_counter()
+    oracle.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                           wl.seq_lens, wl.q_len, wl.cfg.n_sink, wl.cfg.window,
+                           wl.scale, rows=rows.astype(np.int64))
+    return time.perf_counter() - t, n_seqs * wl.q_len
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The oracle as it stands, single-threaded, on sequences of the workload
+    until about budget_s seconds of CPU work."""
+    total_t, total_tok, n = 0.0, 0, 0
+    while total_t < budget_s and n < wl.cfg.batch:
+        dt, tok = oracle_sample(wl, 1, start=n)
+        total_t += dt
+        total_tok += tok
+        n += 1
+    return {"value": total_tok / total_t, "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} of {wl.cfg.batch} sequences of {wl.cfg.name} "
+                      f"(all {wl.cfg.num_q_heads} heads, fp64, one thread), "
+                      f"{total_t:.1f} s"}
+
+
+def workload_config(wl, split_pages=None):
+    cfg = wl.cfg
+    tr = A.attention_traffic(wl.seq_lens, cfg.q_len, cfg.num_q_heads,
+                             cfg.num_kv_heads, cfg.head_dim,
+                             4 if cfg.dtype == "f32" else 2, cfg.n_sink,
+                             cfg.window)
+    c = {"workload": cfg.name, "batch": cfg.batch,
+         "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
+         "head_dim": cfg.head_dim, "q_len": cfg.q_len, "kv_dtype": cfg.dtype,
+         "page_tokens": W.BLOCK_SIZE,
+         "context": (f"U[{cfg.ctx_min},{cfg.ctx_max}]"
+                     if cfg.ctx_min != cfg.ctx_max else cfg.ctx_min),
+         "n_sink": cfg.n_sink, "window": cfg.window,
+         "kv_bytes_per_step": tr["kv_bytes"], "seed": cfg.seed,
+         "l2": "no flush: each step reads %.2f GB of KV, > 129 MB L2"
+               % (tr["kv_bytes"] / 1e9)}
+    if split_pages is not None:
+        c["split_pages"] = split_pages
+    return c, tr
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import spec_verify_paged_gb300 as svp
+    from spec_verify_paged_gb300 import build as svp_build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        svp_build.build()
+    if world > 1:
+        dist.barrier()
+    svp.load_library()
+
+    cfg = W.CONFIGS[args.workload]
+    wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
+    conf, tr = workload_config(wl, args.split_pages or None)
+
+    q = to_dev(wl.q, dev)
+    kc, vc = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
+    bt, sl = to_dev(wl.block_table, dev), to_dev(wl.seq_lens, dev)
+    kn, vn = to_dev(wl.k_new, dev), to_dev(wl.v_new, dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((cfg.batch, cfg.q_len, cfg.num_q_heads),
+                      dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = float(wl.scale)
+    kw = dict(q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
+              scale=scale, out=out, lse=lse, split_pages=args.split_pages)
+    launches = [0]
+
+    def step(ev=None):
+        svp.kv_append(kn, vn, kc, vc, bt, sl)
+        n = svp.last_launch_count()
+        if ev is not None:
+            ev[0].record(stream)
+        svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
+        if ev is not None:
+            ev[1].record(stream)
+        launches[0] += n + svp.last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert svp.read_device_status() == 0, "device status flags raised"
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start producing lines
+    attn_ev = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches[0] = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(attn_ev[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    gpu_launches = launches[0]
+    ms = start.elapsed_time(end)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    ms_max = max_over_ranks(ms, world)
+
+    # ---- end to end through the public calls, host buffers ----
+    h_q, h_kn, h_vn = to_pinned(wl.q), to_pinned(wl.k_new), to_pinned(wl.v_new)
+    h_bt, h_sl = to_pinned(wl.block_table), to_pinned(wl.seq_lens)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    d_bt, d_sl = torch.empty_like(bt), torch.empty_like(sl)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        svp.kv_append(d_kn, d_vn, kc, vc, d_bt, d_sl)
+        svp.paged_decode_attention(d_q, kc, vc, d_bt, d_sl, q_len=cfg.q_len,
+                                   n_sink=cfg.n_sink, window=cfg.window,
+                                   scale=scale, out=out, lse=lse,
+                                   split_pages=args.split_pages)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(1, min(args.steps, 200))
+    if world > 1:
+        dist.barrier()
+    e0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+        stream.synchronize()           # the host reads the result every step
+    e_ms = (time.perf_counter() - e0) * 1e3 / e_steps
+    e_ms = max_over_ranks(e_ms, world)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    # ---- report ----
+    tokens_per_step = cfg.batch * cfg.q_len
+    value = world * tokens_per_step * args.steps / (ms_max / 1e3)
+    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = tr["kv_bytes"] / attn_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) Q/K/V, shuffled 16-token pages)",
+        "config": conf,
+        "kv_read_gbs": round(tr["kv_bytes"] * args.steps / (ms / 1e3) / 1e9, 1),
+        "attention_us": round(attn_avg_s * 1e6, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": "paged_attention_kernel",
+                     "traffic": kernel_traffic()},
+        "e2e": {"value": round(world * tokens_per_step / (e_ms / 1e3), 1),
+                "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(gpu_launches),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = W.CONFIGS[args.workload]
+    wl = W.make_attention(cfg, poison=False)
+    conf, _ = workload_config(wl)
+    seqs_per_step = 1
+    for i in range(args.warmup):
+        oracle_sample(wl, seqs_per_step, start=i)
+    t_tot, tok = 0.0, 0
+    for i in range(args.steps):
+        dt, n = oracle_sample(wl, seqs_per_step, start=args.warmup + i)
+        t_tot += dt
+        tok += n
+    value = tok / t_tot
+    sample = (f"each step: {seqs_per_step} of {cfg.batch} sequences of "
+              f"{cfg.name}, all heads, fp64 oracle, one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_tot * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": conf,
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT,
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode-7b", choices=sorted(W.CONFIGS))
+    ap.add_argument("--split-pages", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * svp.h -- C ABI of libsvp.so: paged decode/verify attention, KV append and
+ * speculative acceptance on one GB300 GPU (sm_103a).
+ *
+ * The three calls are the step of a speculative decoding loop that runs on
+ * the GPU's memory: store the new tokens' K/V in the paged cache
+ * (kv_append), let the new query rows attend to their sequence's cached
+ * rows (paged_decode_attention), and accept or resample the draft tokens
+ * (spec_accept).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a caller-owned DEVICE pointer, row-major and
+ *    densely packed.  The library never frees or keeps a pointer beyond
+ *    the call.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream),
+ *    does not synchronise the host, and allocates nothing when the caller
+ *    passes the workspace it asks for (paged_decode_attention with
+ *    dims->workspace == NULL falls back to a library-owned buffer, see
+ *    below).
+ *  - Return value: SVP_OK or a negative svp_status.  Arguments are checked
+ *    on the host BEFORE anything is launched; a failed check launches
+ *    nothing and writes nothing.  SVP_ERR_CUDA reports a launch error.
+ *  - Data that can only be checked on the device (block ids, sequence
+ *    lengths, token ids) never faults or traps: the kernel skips the bad
+ *    item, records a flag in a device status word and carries on;
+ *    svp_read_device_status() returns and clears the flags.
+ *  - bf16 tensors hold IEEE bfloat16 bit patterns (uint16).
+ */
+#ifndef SVP_H
+#define SVP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SVP_OK = 0,
+  SVP_ERR_INVALID_ARG = -1, /* null pointer, bad size or bad combination */
+  SVP_ERR_UNSUPPORTED = -2, /* valid request outside what is built      */
+  SVP_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed      */
+  SVP_ERR_WORKSPACE = -4    /* caller workspace smaller than required    */
+} svp_status;
+
+typedef enum { SVP_F32 = 0, SVP_BF16 = 1 } svp_dtype;
+
+/* Flags returned by svp_read_device_status(). */
+enum {
+  SVP_DEV_BAD_BLOCK_ID = 1,  /* a visible page maps outside [0,num_blocks) */
+  SVP_DEV_BAD_SEQ_LEN = 2,   /* seq_len < q_len or > max_blocks_per_seq*16 */
+  SVP_DEV_BAD_TOKEN = 4,     /* a draft token outside [0, vocab)           */
+  SVP_DEV_TIMEOUT = 8        /* a bounded device-side wait gave up         */
+};
+
+/* Shapes shared by kv_append and paged_decode_attention.
+ *   q, out           [batch, q_len, num_q_heads, head_dim]        dtype
+ *   k_cache, v_cache [num_blocks, num_kv_heads, block_size, head_dim] dtype
+ *                    (one head's page is one contiguous run)
+ *   block_table      [batch, max_blocks_per_seq] int32; entry lb of row b
+ *                    is the physical page of logical block lb of sequence b
+ *                    (positions lb*16 .. lb*16+15).  Entries of pages that
+ *                    the call does not need may hold anything (e.g. -1).
+ *   seq_lens         [batch] int32, logical length of each sequence
+ *                    INCLUDING its q_len new rows.
+ * num_q_heads must be a multiple of num_kv_heads; query head h reads kv
+ * head h / (num_q_heads / num_kv_heads).  head_dim is 64 or 128; block_size
+ * is 16 (the page size of the lesson "KV cache & Flash Attention", section
+ * "PagedAttention"). */
+typedef struct {
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int dtype;              /* svp_dtype of q, out and both caches           */
+  void *workspace;        /* device scratch for split partials, or NULL    */
+  size_t workspace_bytes; /* size of `workspace`                           */
+  int split_pages;        /* pages per split-K unit; 0 = automatic         */
+} svp_dims;
+
+/* Paged decode / speculative-verify attention.
+ *
+ * Defines (pages: "KV cache & Flash Attention", sections "FlashAttention --
+ * the tiling trick" and "PagedAttention"; "How speculative decoding doubles
+ * LLM speed", step 2 (verification); "How StreamingLLM stabilizes
+ * million-token streams via attention sinks", section "The StreamingLLM
+ * solution"):
+ *   query row i in [0, q_len) of sequence b sits at absolute position
+ *   t_i = seq_lens[b] - q_len + i.  Key j is visible to it iff j <= t_i
+ *   and (window == 0 or j < n_sink or j > t_i - window).
+ *   out[b,i,h]  = sum_j softmax_j(scale * <q[b,i,h], K_j>) V_j over the
+ *                 visible keys of kv head h / (Hq/Hkv), written in dtype;
+ *   lse[b,i,h]  = natural log of sum_j exp(scale * <q, K_j>), fp32.
+ *   window == 0 disables the window (n_sink is then ignored); n_sink
+ *   counts from position 0; window counts the query's own key.  Only pages
+ *   holding visible keys are read; other block_table entries are not read.
+ * q_len: 1 (decode) .. 16 (verify of q_len-1 drafts + bonus position).
+ * Work is split along the key axis into units of dims->split_pages pages;
+ * partial results are merged by log-sum-exp inside the same launch.
+ * Workspace: paged_decode_workspace_size() bytes.  Pass it in dims (the
+ * region must be zero-filled before its first use; every call leaves its
+ * counters at zero again).  With dims->workspace == NULL the library uses
+ * a buffer of its own per device, (re)allocated and zeroed inside the call
+ * when it is too small -- that first call is then not capturable in a CUDA
+ * graph.  Calls that share a workspace must not overlap on the GPU.
+ * Errors: SVP_ERR_INVALID_ARG for null pointers, sizes < 0, num_q_heads not
+ * a multiple of num_kv_heads, q_len < 1, n_sink < 0, window < 0 or a
+ * non-finite scale; SVP_ERR_UNSUPPORTED for head_dim not in {64,128},
+ * block_size != 16, q_len > 16, batch > 65535; SVP_ERR_WORKSPACE for a
+ * caller workspace that is too small.  batch == 0 returns SVP_OK at once. */
+int paged_decode_attention(const svp_dims *dims, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           void *out, float *lse, cudaStream_t stream);
+
+/* Bytes of workspace paged_decode_attention needs for these dims and this
+ * (q_len, n_sink, window).  Returns 0 for invalid dims. */
+size_t paged_decode_workspace_size(const svp_dims *dims, int q_len,
+                                   int n_sink, int window);
+
+/* KV append: writes the n_new new K/V rows of every sequence, k_new/v_new
+ * [batch, n_new, num_kv_heads, head_dim] (dtype of dims), at logical
+ * positions seq_lens[b]-n_new .. seq_lens[b]-1 of the paged caches, i.e.
+ * page block_table[b][pos/16], row pos%16 (pages: "KV cache & Flash
+ * Attention", sections "KV cache" and "PagedAttention").  seq_lens are the
+ * lengths AFTER the append.  A pure byte copy.  Uses no workspace.
+ * Errors as for paged_decode_attention; n_new in [0, 64]. */
+int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
+              void *k_cache, void *v_cache, const int32_t *block_table,
+              const int32_t *seq_lens, int n_new, cudaStream_t stream);
+
+/* Speculative acceptance (pages: "How speculative decoding doubles LLM
+ * speed", step 3 (sampling) and section "Absolute mathematical exactness";
+ * "Speculative decoding: how AI models get faster without getting bigger").
+ *   target_logits [batch, num_draft+1, vocab] fp32 (rows p_0 .. p_K)
+ *   draft_logits  [batch, num_draft, vocab]   fp32 (rows q_0 .. q_{K-1})
+ *   draft_tokens  [batch, num_draft] int32
+ *   uniforms      [batch, num_draft+1] fp32 in [0,1): entry i < K decides
+ *                 draft i, entry K drives the one resample or bonus draw
+ *   out_tokens    [batch, num_draft+1] int32, written: accepted drafts,
+ *                 then the resampled or bonus token, then -1 padding
+ *   n_accepted    [batch] int32: number of accepted drafts (0..K)
+ * With p = softmax(target row), q = softmax(draft row): draft i is accepted
+ * iff u_i * q_i(x_i) <= p_i(x_i), i.e. u_i <= min(1, p/q); at the first
+ * rejection j the replacement is drawn from max(0, p_j - q_j) normalised;
+ * if all K are accepted the bonus token is drawn from p_K.  A draw takes
+ * the smallest token index whose running sum (token order) exceeds
+ * u_K * total.  A residual of zero mass (impossible in exact arithmetic)
+ * falls back to p_j.  A sequence with a draft token outside [0, vocab) gets
+ * n_accepted = -1 and all-(-1) tokens and sets SVP_DEV_BAD_TOKEN.
+ * Softmax normalisers are sums of fp32 exponentials with compensated
+ * (Kahan) fp32 partial sums combined in fp64.  Uses no workspace.
+ * Errors: SVP_ERR_INVALID_ARG for null pointers, batch < 0, num_draft < 1,
+ * vocab < 2; SVP_ERR_UNSUPPORTED for num_draft > 15 or batch > 65535. */
+int spec_accept(int batch, int num_draft, int vocab,
+                const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tokens, const float *uniforms,
+                int32_t *out_tokens, int32_t *n_accepted, cudaStream_t stream);
+
+/* Synchronises `stream`, returns SVP_OK and stores in *flags the OR of the
+ * SVP_DEV_* flags raised by kernels since the last read, then clears them.
+ * flags may be NULL. */
+int svp_read_device_status(cudaStream_t stream, int *flags);
+
+/* Human-readable name of an svp_status value (static string). */
+const char *svp_status_string(int status);
+
+/* Number of kernels the last successful call of each entry point launched
+ * on the calling thread (for launch accounting). */
+int svp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SVP_H */

@@ -1,1 +1,17 @@
-"""Paged decode/verify attention and speculative acceptance for GB300."""
+"""Paged decode/verify attention, KV append and speculative acceptance for
+one GB300 GPU (sm_103a).
+
+The computation lives in libsvp.so (CUDA kernels behind the C ABI declared in
+include/svp.h); this package is its thin Python binding.  Importing it loads
+nothing; the first call loads the library and raises if it is not built.
+"""
+from .binding import (  # noqa: F401
+    SvpError,
+    kv_append,
+    last_launch_count,
+    load_library,
+    paged_decode_attention,
+    read_device_status,
+    spec_accept,
+    workspace_for,
+)

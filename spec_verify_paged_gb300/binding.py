@@ -1,0 +1,255 @@
+"""Thin ctypes binding of libsvp.so (include/svp.h).
+
+Argument marshalling only: shape/dtype/device checks, raw device pointers,
+the current CUDA stream, and a zero-filled workspace tensor kept per device.
+Every step of the computation runs in the library's CUDA kernels; there is
+no fallback of any kind -- if libsvp.so is missing or no GPU is present the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsvp.so")
+
+SVP_OK, SVP_ERR_INVALID_ARG, SVP_ERR_UNSUPPORTED, SVP_ERR_CUDA, SVP_ERR_WORKSPACE = (
+    0, -1, -2, -3, -4)
+SVP_F32, SVP_BF16 = 0, 1
+DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
+EXPORTED = ("paged_decode_attention", "paged_decode_workspace_size",
+            "kv_append", "spec_accept", "svp_read_device_status",
+            "svp_status_string", "svp_last_launch_count")
+
+
+class SvpDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("block_size", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t),
+                ("split_pages", ctypes.c_int)]
+
+
+class SvpError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} returned {status} ({msg})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libsvp.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        dims_p = ctypes.POINTER(SvpDims)
+        lib.paged_decode_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, i32,
+                                               i32, i32, f32, vp, vp, vp]
+        lib.paged_decode_attention.restype = i32
+        lib.paged_decode_workspace_size.argtypes = [dims_p, i32, i32, i32]
+        lib.paged_decode_workspace_size.restype = sz
+        lib.kv_append.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, vp]
+        lib.kv_append.restype = i32
+        lib.spec_accept.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.spec_accept.restype = i32
+        lib.svp_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        lib.svp_read_device_status.restype = i32
+        lib.svp_status_string.argtypes = [i32]
+        lib.svp_status_string.restype = ctypes.c_char_p
+        lib.svp_last_launch_count.argtypes = []
+        lib.svp_last_launch_count.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(fn, status):
+    if status != SVP_OK:
+        msg = _lib.svp_status_string(status).decode()
+        raise SvpError(fn, status, msg)
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SVP_F32
+    if t.dtype == torch.bfloat16:
+        return SVP_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(cond, what):
+    if not cond:
+        raise ValueError(what)
+
+
+def _cuda_contig(t, name):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def make_dims(q_shape, k_cache, block_table, dtype_code, workspace=None,
+              split_pages=0):
+    B, _, Hq, D = q_shape
+    nb, Hkv, bs, D2 = k_cache.shape
+    d = SvpDims()
+    d.batch, d.num_q_heads, d.num_kv_heads, d.head_dim = B, Hq, Hkv, D
+    d.block_size, d.max_blocks_per_seq, d.num_blocks = bs, block_table.shape[1], nb
+    d.dtype = dtype_code
+    d.split_pages = int(split_pages)
+    if workspace is not None:
+        d.workspace = ctypes.c_void_p(workspace.data_ptr())
+        d.workspace_bytes = workspace.numel() * workspace.element_size()
+    return d
+
+
+_ws_cache: dict = {}
+
+
+def workspace_for(dims: SvpDims, q_len: int, n_sink: int, window: int,
+                  device) -> torch.Tensor:
+    """A zero-filled workspace of at least the required size, kept per
+    device and reused (calls that share it must not overlap on the GPU)."""
+    lib = load_library()
+    need = int(lib.paged_decode_workspace_size(ctypes.byref(dims), q_len,
+                                               n_sink, window))
+    _need(need > 0, "invalid attention dims")
+    key = torch.device(device).index or 0
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
+                           q_len=None, n_sink=0, window=0, scale=None,
+                           out=None, lse=None, workspace=None, split_pages=0,
+                           stream=None):
+    """out [B, q_len, Hq, D] (q's dtype) and lse [B, q_len, Hq] fp32 of paged
+    decode/verify attention (include/svp.h: paged_decode_attention)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _cuda_contig(t, n)
+    code = _dtype_code(q)
+    _need(k_cache.dtype == q.dtype and v_cache.dtype == q.dtype,
+          "q, k_cache and v_cache must share a dtype")
+    _need(k_cache.shape == v_cache.shape and k_cache.dim() == 4,
+          "k_cache/v_cache must be [num_blocks, Hkv, block_size, D]")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2,
+          "block_table must be int32 [B, max_blocks]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.dim() == 1,
+          "seq_lens must be int32 [B]")
+    B, ql, Hq, D = q.shape
+    q_len = ql if q_len is None else q_len
+    _need(ql == q_len, "q.shape[1] must equal q_len")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    _cuda_contig(out, "out")
+    _cuda_contig(lse, "lse")
+    dims = make_dims(q.shape, k_cache, block_table, code, None, split_pages)
+    if workspace is None:
+        workspace = workspace_for(dims, q_len, n_sink, window, q.device)
+    dims.workspace = ctypes.c_void_p(workspace.data_ptr())
+    dims.workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib.paged_decode_attention(
+        ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+        int(q_len), int(n_sink), int(window), float(scale), out.data_ptr(),
+        lse.data_ptr(), _stream_handle(stream, q.device))
+    _check("paged_decode_attention", st)
+    return out, lse
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens,
+              stream=None):
+    """Scatter k_new/v_new [B, n_new, Hkv, D] into the paged caches in place
+    (include/svp.h: kv_append).  seq_lens are the lengths after the append."""
+    lib = load_library()
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache"), (block_table, "block_table"),
+                 (seq_lens, "seq_lens")):
+        _cuda_contig(t, n)
+    code = _dtype_code(k_cache)
+    _need(k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype,
+          "k_new/v_new must have the cache dtype")
+    B, n_new, Hkv, D = k_new.shape
+    dims = make_dims((B, n_new, Hkv, D), k_cache, block_table, code)
+    st = lib.kv_append(ctypes.byref(dims), k_new.data_ptr(), v_new.data_ptr(),
+                       k_cache.data_ptr(), v_cache.data_ptr(),
+                       block_table.data_ptr(), seq_lens.data_ptr(), int(n_new),
+                       _stream_handle(stream, k_cache.device))
+    _check("kv_append", st)
+
+
+def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
+                out_tokens=None, n_accepted=None, stream=None):
+    """Speculative acceptance (include/svp.h: spec_accept).  Returns
+    (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+    lib = load_library()
+    for t, n in ((target_logits, "target_logits"),
+                 (draft_logits, "draft_logits"), (draft_tokens, "draft_tokens"),
+                 (uniforms, "uniforms")):
+        _cuda_contig(t, n)
+    _need(target_logits.dtype == torch.float32 and
+          draft_logits.dtype == torch.float32 and
+          uniforms.dtype == torch.float32, "logits/uniforms must be float32")
+    _need(draft_tokens.dtype == torch.int32, "draft_tokens must be int32")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    _need(tuple(draft_logits.shape) == (B, K, V), "draft_logits must be [B, K, V]")
+    _need(tuple(draft_tokens.shape) == (B, K), "draft_tokens must be [B, K]")
+    _need(tuple(uniforms.shape) == (B, K + 1), "uniforms must be [B, K+1]")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib.spec_accept(B, K, V, target_logits.data_ptr(),
+                         draft_logits.data_ptr(), draft_tokens.data_ptr(),
+                         uniforms.data_ptr(), out_tokens.data_ptr(),
+                         n_accepted.data_ptr(), _stream_handle(stream, dev))
+    _check("spec_accept", st)
+    return out_tokens, n_accepted
+
+
+def read_device_status(stream=None, device=None) -> int:
+    """Synchronise and return (and clear) the device-side SVP_DEV_* flags."""
+    lib = load_library()
+    flags = ctypes.c_int(0)
+    st = lib.svp_read_device_status(_stream_handle(stream, device),
+                                    ctypes.byref(flags))
+    _check("svp_read_device_status", st)
+    return flags.value
+
+
+def last_launch_count() -> int:
+    """Kernels launched by the last successful library call on this thread."""
+    return int(load_library().svp_last_launch_count())

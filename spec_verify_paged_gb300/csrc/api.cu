@@ -1,0 +1,327 @@
+// api.cu -- the C ABI of libsvp.so: argument checks, split planning,
+// workspace handling and kernel launches.  Declarations and the full
+// contract of every entry point are in include/svp.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "svp.h"
+#include "svp_internal.h"
+
+namespace svp {
+
+static thread_local int t_last_launches = 0;
+
+// ---- per-device facts, queried once ----
+struct DeviceInfo {
+  int sms = 0;
+};
+static std::mutex g_mu;
+static std::vector<DeviceInfo> g_dev;
+
+static int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+  if (g_dev[dev].sms == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return -1;
+    g_dev[dev].sms = n;
+  }
+  return g_dev[dev].sms;
+}
+
+// ---- library-owned workspace (only when the caller passes none) ----
+struct OwnedWs {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+};
+static std::vector<OwnedWs> g_ws;
+
+static int owned_workspace(size_t need, cudaStream_t stream, void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SVP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if ((int)g_ws.size() <= dev) g_ws.resize(dev + 1);
+  OwnedWs &w = g_ws[dev];
+  if (w.bytes < need) {
+    if (w.ptr) {
+      if (cudaDeviceSynchronize() != cudaSuccess) return SVP_ERR_CUDA;
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    if (cudaMalloc(&w.ptr, need) != cudaSuccess) return SVP_ERR_CUDA;
+    if (cudaMemsetAsync(w.ptr, 0, need, stream) != cudaSuccess)
+      return SVP_ERR_CUDA;
+    w.bytes = need;
+  }
+  *out = w.ptr;
+  return SVP_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static int check_dims(const svp_dims *d) {
+  if (!d) return SVP_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->num_q_heads < 1 || d->num_kv_heads < 1 ||
+      d->head_dim < 1 || d->block_size < 1 || d->max_blocks_per_seq < 0 ||
+      d->num_blocks < 0 || d->split_pages < 0)
+    return SVP_ERR_INVALID_ARG;
+  if (d->num_q_heads % d->num_kv_heads != 0) return SVP_ERR_INVALID_ARG;
+  if (d->dtype != SVP_F32 && d->dtype != SVP_BF16) return SVP_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return SVP_ERR_UNSUPPORTED;
+  if (d->block_size != kBlockSize) return SVP_ERR_UNSUPPORTED;
+  if (d->batch > kMaxBatch) return SVP_ERR_UNSUPPORTED;
+  return SVP_OK;
+}
+
+// Upper bound of the pages one sequence's visible set can span.
+static int max_visible_pages(int max_blocks, int q_len, int n_sink,
+                             int window) {
+  if (window == 0) return max_blocks;
+  const long long sink_pages = (n_sink + kBlockSize - 1) / kBlockSize;
+  const long long win_pages =
+      ((long long)window + q_len - 1 + kBlockSize - 1) / kBlockSize + 1;
+  const long long b = sink_pages + win_pages;
+  return (int)(b < max_blocks ? b : max_blocks);
+}
+
+int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                   int dtype, int max_blocks, int q_len, int n_sink,
+                   int window, int split_pages, int num_sms, AttnPlan *plan) {
+  const int group = num_q_heads / num_kv_heads;
+  const int rows = group * q_len;
+  int rb = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  const int n_rg = (rows + rb - 1) / rb;
+  const int mvp = max_visible_pages(max_blocks, q_len, n_sink, window);
+  const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, batch);
+  const long long slots = (long long)num_sms * ctas;
+  int pps = split_pages;
+  if (pps <= 0) {
+    // aim for ~16 units per CTA slot at the worst-case lengths
+    const long long groups = (long long)batch * num_kv_heads * n_rg;
+    const long long bound = groups * (long long)(mvp > 0 ? mvp : 1);
+    long long want = bound / (slots * 16 > 0 ? slots * 16 : 1);
+    pps = 8;
+    while (pps < 64 && pps * 2 <= want) pps *= 2;
+  }
+  if (pps > 128) pps = 128;
+  const int max_splits = mvp > 0 ? (mvp + pps - 1) / pps : 1;
+  const long long groups = (long long)batch * num_kv_heads * n_rg;
+  const long long units_bound = groups * max_splits;
+  long long grid = slots;
+  if (grid > units_bound) grid = units_bound;
+  if (grid < 1) grid = 1;
+  plan->rb = rb;
+  plan->n_rg = n_rg;
+  plan->split_pages = pps;
+  plan->max_splits = max_splits;
+  plan->grid = (int)grid;
+  plan->ctas_per_sm = ctas;
+  plan->ws_counters = 256;
+  plan->ws_tickets = align256((size_t)groups * sizeof(int));
+  plan->ws_part_o = align256((size_t)groups * max_splits * rb * head_dim * 4);
+  plan->ws_part_lse = align256((size_t)groups * max_splits * rb * 4);
+  plan->ws_total =
+      plan->ws_counters + plan->ws_tickets + plan->ws_part_o + plan->ws_part_lse;
+  return SVP_OK;
+}
+
+constexpr int kBatchPerLaunch = 4096;
+
+}  // namespace svp
+
+using namespace svp;
+
+extern "C" {
+
+const char *svp_status_string(int s) {
+  switch (s) {
+    case SVP_OK: return "SVP_OK";
+    case SVP_ERR_INVALID_ARG: return "SVP_ERR_INVALID_ARG";
+    case SVP_ERR_UNSUPPORTED: return "SVP_ERR_UNSUPPORTED";
+    case SVP_ERR_CUDA: return "SVP_ERR_CUDA";
+    case SVP_ERR_WORKSPACE: return "SVP_ERR_WORKSPACE";
+    default: return "SVP_UNKNOWN_STATUS";
+  }
+}
+
+int svp_last_launch_count(void) { return t_last_launches; }
+
+static int check_attention_args(const svp_dims *dims, int q_len, int n_sink,
+                                int window, float scale) {
+  int st = check_dims(dims);
+  if (st != SVP_OK) return st;
+  if (q_len < 1 || n_sink < 0 || window < 0 || !std::isfinite(scale))
+    return SVP_ERR_INVALID_ARG;
+  if (q_len > kMaxQLen) return SVP_ERR_UNSUPPORTED;
+  return SVP_OK;
+}
+
+size_t paged_decode_workspace_size(const svp_dims *dims, int q_len, int n_sink,
+                                   int window) {
+  if (check_attention_args(dims, q_len, n_sink, window, 1.0f) != SVP_OK)
+    return 0;
+  const int sms = device_sms();
+  AttnPlan plan;
+  const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
+  plan_attention(bl > 0 ? bl : 1, dims->num_q_heads, dims->num_kv_heads,
+                 dims->head_dim, dims->dtype, dims->max_blocks_per_seq, q_len,
+                 n_sink, window, dims->split_pages, sms > 0 ? sms : 1, &plan);
+  return plan.ws_total;
+}
+
+int paged_decode_attention(const svp_dims *dims, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           void *out, float *lse, cudaStream_t stream) {
+  t_last_launches = 0;
+  int st = check_attention_args(dims, q_len, n_sink, window, scale);
+  if (st != SVP_OK) return st;
+  if (dims->batch == 0) return SVP_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse)
+    return SVP_ERR_INVALID_ARG;
+  if (dims->num_blocks == 0 || dims->max_blocks_per_seq == 0)
+    return SVP_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return SVP_ERR_CUDA;
+
+  const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
+  AttnPlan plan;
+  plan_attention(bl, dims->num_q_heads, dims->num_kv_heads, dims->head_dim,
+                 dims->dtype, dims->max_blocks_per_seq, q_len, n_sink, window,
+                 dims->split_pages, sms, &plan);
+  void *ws = dims->workspace;
+  if (ws) {
+    if (dims->workspace_bytes < plan.ws_total) return SVP_ERR_WORKSPACE;
+  } else {
+    st = owned_workspace(plan.ws_total, stream, &ws);
+    if (st != SVP_OK) return st;
+  }
+  char *wp = static_cast<char *>(ws);
+  const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
+  const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
+  int launches = 0;
+  for (int b0 = 0; b0 < dims->batch; b0 += kBatchPerLaunch) {
+    const int nb = dims->batch - b0 < kBatchPerLaunch ? dims->batch - b0
+                                                      : kBatchPerLaunch;
+    AttnParams p;
+    p.q = static_cast<const char *>(q) + (size_t)b0 * q_len * row_elems * eb;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table + (size_t)b0 * dims->max_blocks_per_seq;
+    p.seq_lens = seq_lens + b0;
+    p.out = static_cast<char *>(out) + (size_t)b0 * q_len * row_elems * eb;
+    p.lse = lse + (size_t)b0 * q_len * dims->num_q_heads;
+    p.counters = reinterpret_cast<int *>(wp);
+    p.tickets = reinterpret_cast<int *>(wp + plan.ws_counters);
+    p.part_o = reinterpret_cast<float *>(wp + plan.ws_counters + plan.ws_tickets);
+    p.part_lse = reinterpret_cast<float *>(wp + plan.ws_counters +
+                                           plan.ws_tickets + plan.ws_part_o);
+    p.batch = nb;
+    p.num_q_heads = dims->num_q_heads;
+    p.num_kv_heads = dims->num_kv_heads;
+    p.head_dim = dims->head_dim;
+    p.group = dims->num_q_heads / dims->num_kv_heads;
+    p.q_len = q_len;
+    p.n_sink = n_sink;
+    p.window = window;
+    p.max_blocks = dims->max_blocks_per_seq;
+    p.num_blocks = dims->num_blocks;
+    p.rows = p.group * q_len;
+    p.rb = plan.rb;
+    p.n_rg = plan.n_rg;
+    p.split_pages = plan.split_pages;
+    p.max_splits = plan.max_splits;
+    p.qscale = scale * 1.4426950408889634f;
+    AttnPlan sub = plan;
+    if (nb != bl) {
+      plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
+                     dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
+                     q_len, n_sink, window, plan.split_pages, sms, &sub);
+    }
+    cudaError_t e = launch_attention(p, dims->dtype, sub.grid, stream);
+    if (e != cudaSuccess) return SVP_ERR_CUDA;
+    ++launches;
+  }
+  t_last_launches = launches;
+  return SVP_OK;
+}
+
+int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
+              void *k_cache, void *v_cache, const int32_t *block_table,
+              const int32_t *seq_lens, int n_new, cudaStream_t stream) {
+  t_last_launches = 0;
+  int st = check_dims(dims);
+  if (st != SVP_OK) return st;
+  if (n_new < 0) return SVP_ERR_INVALID_ARG;
+  if (n_new > 64) return SVP_ERR_UNSUPPORTED;
+  if (dims->batch == 0 || n_new == 0) return SVP_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens)
+    return SVP_ERR_INVALID_ARG;
+  if (dims->num_blocks == 0 || dims->max_blocks_per_seq == 0)
+    return SVP_ERR_INVALID_ARG;
+  AppendParams p;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.batch = dims->batch;
+  p.num_kv_heads = dims->num_kv_heads;
+  p.head_dim = dims->head_dim;
+  p.n_new = n_new;
+  p.max_blocks = dims->max_blocks_per_seq;
+  p.num_blocks = dims->num_blocks;
+  p.elem_bytes = dims->dtype == SVP_F32 ? 4 : 2;
+  if (launch_kv_append(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
+  t_last_launches = 1;
+  return SVP_OK;
+}
+
+int spec_accept(int batch, int num_draft, int vocab,
+                const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tokens, const float *uniforms,
+                int32_t *out_tokens, int32_t *n_accepted,
+                cudaStream_t stream) {
+  t_last_launches = 0;
+  if (batch < 0 || num_draft < 1 || vocab < 2) return SVP_ERR_INVALID_ARG;
+  if (num_draft > kMaxDraft || batch > kMaxBatch) return SVP_ERR_UNSUPPORTED;
+  if ((long long)vocab > 8LL * 40000) return SVP_ERR_UNSUPPORTED;
+  if (batch == 0) return SVP_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !uniforms ||
+      !out_tokens || !n_accepted)
+    return SVP_ERR_INVALID_ARG;
+  AcceptParams p;
+  p.target_logits = target_logits;
+  p.draft_logits = draft_logits;
+  p.draft_tokens = draft_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.n_accepted = n_accepted;
+  p.batch = batch;
+  p.num_draft = num_draft;
+  p.vocab = vocab;
+  if (launch_spec_accept(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
+  t_last_launches = 1;
+  return SVP_OK;
+}
+
+int svp_read_device_status(cudaStream_t stream, int *flags) {
+  unsigned f = 0;
+  if (read_status_attention(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
+  if (read_status_append(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
+  if (read_status_accept(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
+  if (flags) *flags = (int)f;
+  return SVP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// svp_internal.h -- parameter blocks and launchers shared between the C-ABI
+// host layer (api.cu) and the kernel translation units.  Not installed.
+#pragma once
+#include <cuda_runtime_api.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace svp {
+
+constexpr int kBlockSize = 16;     // tokens per KV page
+constexpr int kMaxQLen = 16;
+constexpr int kMaxBatch = 65535;
+constexpr int kMaxDraft = 15;
+
+// One paged_decode_attention launch.
+struct AttnParams {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  void *out;
+  float *lse;
+  // workspace pieces
+  int *counters;       // [0] work queue head, [1] finished CTAs
+  int *tickets;        // [batch * Hkv * n_rg] split arrival counters
+  float *part_o;       // [batch*Hkv*n_rg][max_splits][RB][D] normalised partials
+  float *part_lse;     // [batch*Hkv*n_rg][max_splits][RB] log2-domain LSE
+  int batch, num_q_heads, num_kv_heads, head_dim, group;
+  int q_len, n_sink, window;
+  int max_blocks, num_blocks;
+  int rows;            // group * q_len query rows per (sequence, kv head)
+  int rb;              // rows per CTA work unit (row-group size)
+  int n_rg;            // ceil(rows / rb)
+  int split_pages;     // pages per split unit
+  int max_splits;      // upper bound of splits per sequence (workspace stride)
+  float qscale;        // scale * log2(e)
+};
+
+struct AttnPlan {
+  int rb, n_rg, split_pages, max_splits, grid, ctas_per_sm;
+  size_t ws_counters, ws_tickets, ws_part_o, ws_part_lse, ws_total;
+};
+
+// Fills the plan (no CUDA launches).  dtype 0 = f32, 1 = bf16.  Returns 0 or
+// a negative svp_status.
+int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                   int dtype, int max_blocks, int q_len, int n_sink,
+                   int window, int split_pages, int num_sms, AttnPlan *plan);
+
+// Occupancy-derived CTAs per SM for the attention kernel of this shape
+// (queried once per device and shape, cached).
+int attention_ctas_per_sm(int dtype, int head_dim, int rb, int batch);
+
+cudaError_t launch_attention(const AttnParams &p, int dtype, int grid,
+                             cudaStream_t stream);
+
+struct AppendParams {
+  const void *k_new;
+  const void *v_new;
+  void *k_cache;
+  void *v_cache;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  int batch, num_kv_heads, head_dim, n_new, max_blocks, num_blocks;
+  int elem_bytes;
+};
+cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream);
+
+struct AcceptParams {
+  const float *target_logits;
+  const float *draft_logits;
+  const int32_t *draft_tokens;
+  const float *uniforms;
+  int32_t *out_tokens;
+  int32_t *n_accepted;
+  int batch, num_draft, vocab;
+};
+cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream);
+
+// Device status words (one per translation unit): read-and-clear.
+cudaError_t read_status_attention(cudaStream_t s, unsigned *flags);
+cudaError_t read_status_append(cudaStream_t s, unsigned *flags);
+cudaError_t read_status_accept(cudaStream_t s, unsigned *flags);
+
+}  // namespace svp

@@ -50,3 +50,24 @@ def permute_pages(rng, k, v, table):
     v2[pi] = v
     t2 = np.where(table >= 0, pi[np.maximum(table, 0)], -1).astype(np.int32)
     return k2, v2, t2
+
+
+def to_dev(a, device="cuda:0"):
+    """numpy -> torch on the GPU; uint16 arrays become bfloat16 (same bits)."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_host(t):
+    """torch (GPU) -> numpy; bfloat16 comes back as uint16 bit patterns."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def out_as_f64(t):
+    """GPU attention output widened to float64."""
+    return widen(to_host(t))

@@ -1,0 +1,161 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/svp.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from spec_verify_paged_gb300 import binding, build
+    build.build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "svp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", src)
+    return sorted(set(n for n in names if n not in ("sizeof",)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"paged_decode_attention", "spec_accept", "kv_append"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} missing from libsvp.so"
+
+
+def test_binding_covers_the_header():
+    from spec_verify_paged_gb300 import binding
+    assert set(_declared_functions()) == set(binding.EXPORTED)
+
+
+def _dims(**kw):
+    from spec_verify_paged_gb300.binding import SvpDims
+    d = SvpDims()
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                block_size=16, max_blocks_per_seq=4, num_blocks=8, dtype=1,
+                split_pages=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+P = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails its checks
+
+
+@pytest.mark.parametrize("kw,q_len,n_sink,window,scale,expect", [
+    (dict(head_dim=96), 1, 0, 0, 0.1, -2),
+    (dict(block_size=32), 1, 0, 0, 0.1, -2),
+    (dict(num_q_heads=6, num_kv_heads=4), 1, 0, 0, 0.1, -1),
+    (dict(dtype=7), 1, 0, 0, 0.1, -1),
+    (dict(batch=-1), 1, 0, 0, 0.1, -1),
+    (dict(batch=70000), 1, 0, 0, 0.1, -2),
+    ({}, 0, 0, 0, 0.1, -1),
+    ({}, 17, 0, 0, 0.1, -2),
+    ({}, 1, -1, 0, 0.1, -1),
+    ({}, 1, 0, -3, 0.1, -1),
+    ({}, 1, 0, 0, float("nan"), -1),
+    ({}, 1, 0, 0, float("inf"), -1),
+])
+def test_attention_rejects_bad_arguments(lib, kw, q_len, n_sink, window, scale,
+                                         expect):
+    d = _dims(**kw)
+    st = lib.paged_decode_attention(ctypes.byref(d), P, P, P, P, P, q_len,
+                                    n_sink, window, scale, P, P, None)
+    assert st == expect
+    assert lib.svp_last_launch_count() == 0
+
+
+def test_attention_null_pointers(lib):
+    d = _dims()
+    assert lib.paged_decode_attention(None, P, P, P, P, P, 1, 0, 0, 0.1, P, P,
+                                      None) == -1
+    assert lib.paged_decode_attention(ctypes.byref(d), None, P, P, P, P, 1, 0,
+                                      0, 0.1, P, P, None) == -1
+    assert lib.paged_decode_attention(ctypes.byref(d), P, P, P, P, P, 1, 0, 0,
+                                      0.1, P, None, None) == -1
+
+
+def test_attention_empty_batch_is_a_no_op(lib):
+    d = _dims(batch=0)
+    assert lib.paged_decode_attention(ctypes.byref(d), None, None, None, None,
+                                      None, 1, 0, 0, 0.1, None, None, None) == 0
+    assert lib.svp_last_launch_count() == 0
+
+
+def test_workspace_too_small(lib):
+    d = _dims()
+    d.workspace = P
+    d.workspace_bytes = 16
+    # the plan is made before any launch; a short workspace is refused
+    st = lib.paged_decode_attention(ctypes.byref(d), P, P, P, P, P, 1, 0, 0,
+                                    0.1, P, P, None)
+    assert st in (-4, -3)  # -3 only where no device can be queried
+
+
+def test_workspace_size_grows_with_work(lib):
+    small = lib.paged_decode_workspace_size(ctypes.byref(_dims()), 1, 0, 0)
+    big = lib.paged_decode_workspace_size(
+        ctypes.byref(_dims(batch=64, max_blocks_per_seq=512)), 1, 0, 0)
+    win = lib.paged_decode_workspace_size(
+        ctypes.byref(_dims(batch=64, max_blocks_per_seq=512)), 1, 4, 64)
+    assert 0 < small < big and win < big
+    assert lib.paged_decode_workspace_size(None, 1, 0, 0) == 0
+    assert lib.paged_decode_workspace_size(ctypes.byref(_dims(head_dim=80)),
+                                           1, 0, 0) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((2, 0, 100), -1), ((2, 4, 1), -1), ((-1, 4, 100), -1),
+    ((2, 16, 100), -2), ((70000, 4, 100), -2), ((2, 4, 8 * 40000 + 1), -2),
+])
+def test_accept_rejects_bad_sizes(lib, args, expect):
+    assert lib.spec_accept(*args, P, P, P, P, P, P, None) == expect
+
+
+def test_accept_null_pointer(lib):
+    assert lib.spec_accept(2, 4, 100, P, None, P, P, P, P, None) == -1
+    assert lib.spec_accept(0, 4, 100, None, None, None, None, None, None,
+                           None) == 0
+
+
+def test_append_rejects_bad_arguments(lib):
+    d = _dims()
+    assert lib.kv_append(ctypes.byref(d), P, P, P, P, P, P, -1, None) == -1
+    assert lib.kv_append(ctypes.byref(d), P, P, P, P, P, P, 65, None) == -2
+    assert lib.kv_append(ctypes.byref(_dims(head_dim=32)), P, P, P, P, P, P, 1,
+                         None) == -2
+    assert lib.kv_append(ctypes.byref(d), None, P, P, P, P, P, 1, None) == -1
+    assert lib.kv_append(ctypes.byref(d), P, P, P, P, P, P, 0, None) == 0
+
+
+def test_status_strings(lib):
+    assert lib.svp_status_string(0) == b"SVP_OK"
+    assert lib.svp_status_string(-4) == b"SVP_ERR_WORKSPACE"
+    assert lib.svp_status_string(5) == b"SVP_UNKNOWN_STATUS"
+
+
+def test_product_path_fails_loudly_without_the_library(tmp_path):
+    """No CPU fallback: a missing library is an error, not a slow path."""
+    from spec_verify_paged_gb300 import binding
+    with pytest.raises(RuntimeError):
+        binding.load_library.__wrapped__(str(tmp_path / "nope.so")) \
+            if hasattr(binding.load_library, "__wrapped__") else \
+            _load_missing(binding, tmp_path)
+
+
+def _load_missing(binding, tmp_path):
+    saved = binding._lib
+    binding._lib = None
+    try:
+        binding.load_library(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved
