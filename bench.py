@@ -76,7 +76,7 @@ def kernel_traffic():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("attention.cu sha256[:16]") != sha:
+    if vals.get("attention.cu sha256 prefix") != sha:
         return None
     try:
         return int(vals["dram bytes per launch"])
