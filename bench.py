@@ -268,6 +268,8 @@ def run_ours(args):
     cfg = W.CONFIGS[args.workload]
     wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
     conf, tr = workload_config(wl, args.split_pages or None)
+    if args.kernel_path:
+        conf["kernel_path"] = {1: "cuda_cores", 2: "tensor_cores"}[args.kernel_path]
 
     q = to_dev(wl.q, dev)
     kc, vc = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
@@ -279,7 +281,8 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     scale = float(wl.scale)
     kw = dict(q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
-              scale=scale, out=out, lse=lse, split_pages=args.split_pages)
+              scale=scale, out=out, lse=lse, split_pages=args.split_pages,
+              kernel_path=args.kernel_path)
     launches = [0]
 
     def step(ev=None):
@@ -342,7 +345,8 @@ def run_ours(args):
         svp.paged_decode_attention(d_q, kc, vc, d_bt, d_sl, q_len=cfg.q_len,
                                    n_sink=cfg.n_sink, window=cfg.window,
                                    scale=scale, out=out, lse=lse,
-                                   split_pages=args.split_pages)
+                                   split_pages=args.split_pages,
+                                   kernel_path=args.kernel_path)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -441,7 +445,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode-7b", choices=sorted(W.CONFIGS))
-    ap.add_argument("--split-pages", type=int, default=0)
+    ap.add_argument("--split-pages", type=int, default=0,
+                    help="pages per split-K unit (0: automatic)")
+    ap.add_argument("--kernel-path", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

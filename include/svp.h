@@ -82,7 +82,19 @@ typedef struct {
   void *workspace;        /* device scratch for split partials, or NULL    */
   size_t workspace_bytes; /* size of `workspace`                           */
   int split_pages;        /* pages per split-K unit; 0 = automatic         */
+  int kernel_path;        /* svp_kernel_path; SVP_PATH_AUTO by default     */
 } svp_dims;
+
+/* Which attention kernel variant runs.  AUTO picks tensor cores (bf16 only)
+ * when a kv head serves at least 3 query rows (GQA group x q_len), CUDA
+ * cores otherwise.  Both compute the same quantity; forcing a path exists
+ * for testing and tuning.  TENSOR_CORES with fp32 data is
+ * SVP_ERR_UNSUPPORTED. */
+typedef enum {
+  SVP_PATH_AUTO = 0,
+  SVP_PATH_CUDA_CORES = 1,
+  SVP_PATH_TENSOR_CORES = 2
+} svp_kernel_path;
 
 /* Paged decode / speculative-verify attention.
  *
@@ -103,17 +115,21 @@ typedef struct {
  * q_len: 1 (decode) .. 16 (verify of q_len-1 drafts + bonus position).
  * Work is split along the key axis into units of dims->split_pages pages;
  * partial results are merged by log-sum-exp inside the same launch.
- * Workspace: paged_decode_workspace_size() bytes.  Pass it in dims (the
- * region must be zero-filled before its first use; every call leaves its
- * counters at zero again).  With dims->workspace == NULL the library uses
- * a buffer of its own per device, (re)allocated and zeroed inside the call
- * when it is too small -- that first call is then not capturable in a CUDA
- * graph.  Calls that share a workspace must not overlap on the GPU.
- * Errors: SVP_ERR_INVALID_ARG for null pointers, sizes < 0, num_q_heads not
- * a multiple of num_kv_heads, q_len < 1, n_sink < 0, window < 0 or a
- * non-finite scale; SVP_ERR_UNSUPPORTED for head_dim not in {64,128},
- * block_size != 16, q_len > 16, batch > 65535; SVP_ERR_WORKSPACE for a
- * caller workspace that is too small.  batch == 0 returns SVP_OK at once. */
+ * Workspace: paged_decode_workspace_size() bytes, passed in dims; it needs
+ * no initialisation (each call clears the few KB of counters it uses with
+ * one cudaMemsetAsync on `stream`, then launches one kernel).  With
+ * dims->workspace == NULL the library uses a buffer of its own per device,
+ * (re)allocated inside the call when it is too small -- that first call is
+ * then not capturable in a CUDA graph.  Calls that share a workspace must
+ * not overlap on the GPU.
+ * q, k_cache and v_cache must be 16-byte aligned.
+ * Errors: SVP_ERR_INVALID_ARG for null or misaligned pointers, sizes < 0,
+ * num_q_heads not a multiple of num_kv_heads, q_len < 1, n_sink < 0,
+ * window < 0, a non-finite scale or an unknown kernel_path;
+ * SVP_ERR_UNSUPPORTED for head_dim not in {64,128}, block_size != 16,
+ * q_len > 16, batch > 65535, or a forced tensor-core path on fp32 data;
+ * SVP_ERR_WORKSPACE for a caller workspace that is too small.  batch == 0
+ * returns SVP_OK at once. */
 int paged_decode_attention(const svp_dims *dims, const void *q,
                            const void *k_cache, const void *v_cache,
                            const int32_t *block_table, const int32_t *seq_lens,

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libsvp.so")
 SVP_OK, SVP_ERR_INVALID_ARG, SVP_ERR_UNSUPPORTED, SVP_ERR_CUDA, SVP_ERR_WORKSPACE = (
     0, -1, -2, -3, -4)
 SVP_F32, SVP_BF16 = 0, 1
+PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES = 0, 1, 2
 DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("paged_decode_attention", "paged_decode_workspace_size",
             "kv_append", "spec_accept", "svp_read_device_status",
@@ -35,7 +36,8 @@ class SvpDims(ctypes.Structure):
                 ("num_blocks", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t),
-                ("split_pages", ctypes.c_int)]
+                ("split_pages", ctypes.c_int),
+                ("kernel_path", ctypes.c_int)]
 
 
 class SvpError(RuntimeError):
@@ -111,7 +113,7 @@ def _cuda_contig(t, name):
 
 
 def make_dims(q_shape, k_cache, block_table, dtype_code, workspace=None,
-              split_pages=0):
+              split_pages=0, kernel_path=0):
     B, _, Hq, D = q_shape
     nb, Hkv, bs, D2 = k_cache.shape
     d = SvpDims()
@@ -119,6 +121,7 @@ def make_dims(q_shape, k_cache, block_table, dtype_code, workspace=None,
     d.block_size, d.max_blocks_per_seq, d.num_blocks = bs, block_table.shape[1], nb
     d.dtype = dtype_code
     d.split_pages = int(split_pages)
+    d.kernel_path = int(kernel_path)
     if workspace is not None:
         d.workspace = ctypes.c_void_p(workspace.data_ptr())
         d.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -130,12 +133,14 @@ _ws_cache: dict = {}
 
 def workspace_for(dims: SvpDims, q_len: int, n_sink: int, window: int,
                   device) -> torch.Tensor:
-    """A zero-filled workspace of at least the required size, kept per
-    device and reused (calls that share it must not overlap on the GPU)."""
+    """A workspace of at least the required size, kept per device and
+    reused (calls that share it must not overlap on the GPU).  None for a
+    request the library rejects."""
     lib = load_library()
     need = int(lib.paged_decode_workspace_size(ctypes.byref(dims), q_len,
                                                n_sink, window))
-    _need(need > 0, "invalid attention dims")
+    if need == 0:  # an invalid request: the call itself reports the status
+        return None
     key = torch.device(device).index or 0
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
@@ -147,7 +152,7 @@ def workspace_for(dims: SvpDims, q_len: int, n_sink: int, window: int,
 def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
                            q_len=None, n_sink=0, window=0, scale=None,
                            out=None, lse=None, workspace=None, split_pages=0,
-                           stream=None):
+                           kernel_path=PATH_AUTO, stream=None):
     """out [B, q_len, Hq, D] (q's dtype) and lse [B, q_len, Hq] fp32 of paged
     decode/verify attention (include/svp.h: paged_decode_attention)."""
     lib = load_library()
@@ -174,11 +179,13 @@ def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
         lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
     _cuda_contig(out, "out")
     _cuda_contig(lse, "lse")
-    dims = make_dims(q.shape, k_cache, block_table, code, None, split_pages)
+    dims = make_dims(q.shape, k_cache, block_table, code, None, split_pages,
+                     kernel_path)
     if workspace is None:
         workspace = workspace_for(dims, q_len, n_sink, window, q.device)
-    dims.workspace = ctypes.c_void_p(workspace.data_ptr())
-    dims.workspace_bytes = workspace.numel() * workspace.element_size()
+    if workspace is not None:
+        dims.workspace = ctypes.c_void_p(workspace.data_ptr())
+        dims.workspace_bytes = workspace.numel() * workspace.element_size()
     st = lib.paged_decode_attention(
         ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(),
         v_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),

@@ -71,7 +71,8 @@ static int check_dims(const svp_dims *d) {
   if (!d) return SVP_ERR_INVALID_ARG;
   if (d->batch < 0 || d->num_q_heads < 1 || d->num_kv_heads < 1 ||
       d->head_dim < 1 || d->block_size < 1 || d->max_blocks_per_seq < 0 ||
-      d->num_blocks < 0 || d->split_pages < 0)
+      d->num_blocks < 0 || d->split_pages < 0 || d->kernel_path < 0 ||
+      d->kernel_path > SVP_PATH_TENSOR_CORES)
     return SVP_ERR_INVALID_ARG;
   if (d->num_q_heads % d->num_kv_heads != 0) return SVP_ERR_INVALID_ARG;
   if (d->dtype != SVP_F32 && d->dtype != SVP_BF16) return SVP_ERR_INVALID_ARG;
@@ -94,32 +95,43 @@ static int max_visible_pages(int max_blocks, int q_len, int n_sink,
 
 int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    int dtype, int max_blocks, int q_len, int n_sink,
-                   int window, int split_pages, int num_sms, AttnPlan *plan) {
+                   int window, int split_pages, int kernel_path, int num_sms,
+                   long long num_blocks, AttnPlan *plan) {
   const int group = num_q_heads / num_kv_heads;
   const int rows = group * q_len;
-  int rb = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  // the tensor path addresses the cache as a 2-D tensor with int32 rows
+  const bool tma_ok = tensor_maps_available() &&
+                      num_blocks * num_kv_heads * kBlockSize < (1LL << 31);
+  bool mma = false;
+  if (kernel_path == SVP_PATH_TENSOR_CORES) {
+    if (dtype != SVP_BF16 || !tma_ok) return SVP_ERR_UNSUPPORTED;
+    mma = true;
+  } else if (kernel_path == SVP_PATH_AUTO) {
+    mma = dtype == SVP_BF16 && rows >= kMmaMinRows && tma_ok;
+  }
+  int rb = mma ? 16 : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
   const int n_rg = (rows + rb - 1) / rb;
   const int mvp = max_visible_pages(max_blocks, q_len, n_sink, window);
-  const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, batch);
+  const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);
   const long long slots = (long long)num_sms * ctas;
+  const long long groups = (long long)batch * num_kv_heads * n_rg;
   int pps = split_pages;
   if (pps <= 0) {
-    // aim for ~16 units per CTA slot at the worst-case lengths
-    const long long groups = (long long)batch * num_kv_heads * n_rg;
+    // aim for ~8 units per CTA slot at the worst-case lengths
     const long long bound = groups * (long long)(mvp > 0 ? mvp : 1);
-    long long want = bound / (slots * 16 > 0 ? slots * 16 : 1);
+    const long long want = bound / (slots * 8 > 0 ? slots * 8 : 1);
     pps = 8;
     while (pps < 64 && pps * 2 <= want) pps *= 2;
   }
   if (pps > 128) pps = 128;
   const int max_splits = mvp > 0 ? (mvp + pps - 1) / pps : 1;
-  const long long groups = (long long)batch * num_kv_heads * n_rg;
   const long long units_bound = groups * max_splits;
   long long grid = slots;
   if (grid > units_bound) grid = units_bound;
   if (grid < 1) grid = 1;
   plan->rb = rb;
   plan->n_rg = n_rg;
+  plan->mma = mma;
   plan->split_pages = pps;
   plan->max_splits = max_splits;
   plan->grid = (int)grid;
@@ -171,9 +183,12 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len, int n_sink,
   const int sms = device_sms();
   AttnPlan plan;
   const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
-  plan_attention(bl > 0 ? bl : 1, dims->num_q_heads, dims->num_kv_heads,
-                 dims->head_dim, dims->dtype, dims->max_blocks_per_seq, q_len,
-                 n_sink, window, dims->split_pages, sms > 0 ? sms : 1, &plan);
+  if (plan_attention(bl > 0 ? bl : 1, dims->num_q_heads, dims->num_kv_heads,
+                     dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
+                     q_len, n_sink, window, dims->split_pages,
+                     dims->kernel_path, sms > 0 ? sms : 1, dims->num_blocks,
+                     &plan) != SVP_OK)
+    return 0;
   return plan.ws_total;
 }
 
@@ -190,14 +205,20 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     return SVP_ERR_INVALID_ARG;
   if (dims->num_blocks == 0 || dims->max_blocks_per_seq == 0)
     return SVP_ERR_INVALID_ARG;
+  // pages move with 16-byte bulk copies and q with vector loads
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) % 16 != 0)
+    return SVP_ERR_INVALID_ARG;
   const int sms = device_sms();
   if (sms <= 0) return SVP_ERR_CUDA;
 
   const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
   AttnPlan plan;
-  plan_attention(bl, dims->num_q_heads, dims->num_kv_heads, dims->head_dim,
-                 dims->dtype, dims->max_blocks_per_seq, q_len, n_sink, window,
-                 dims->split_pages, sms, &plan);
+  st = plan_attention(bl, dims->num_q_heads, dims->num_kv_heads,
+                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
+                      q_len, n_sink, window, dims->split_pages,
+                      dims->kernel_path, sms, dims->num_blocks, &plan);
+  if (st != SVP_OK) return st;
   void *ws = dims->workspace;
   if (ws) {
     if (dims->workspace_bytes < plan.ws_total) return SVP_ERR_WORKSPACE;
@@ -206,6 +227,12 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     if (st != SVP_OK) return st;
   }
   char *wp = static_cast<char *>(ws);
+  // The workspace layout depends on the call's shape, so an earlier call
+  // may have left split partials where this call keeps its counters and
+  // tickets: clear that (small) region on the stream first.
+  if (cudaMemsetAsync(wp, 0, plan.ws_counters + plan.ws_tickets, stream) !=
+      cudaSuccess)
+    return SVP_ERR_CUDA;
   const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
   const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
   int launches = 0;
@@ -245,9 +272,11 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     if (nb != bl) {
       plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
-                     q_len, n_sink, window, plan.split_pages, sms, &sub);
+                     q_len, n_sink, window, plan.split_pages,
+                     plan.mma ? SVP_PATH_TENSOR_CORES : SVP_PATH_CUDA_CORES,
+                     sms, dims->num_blocks, &sub);
     }
-    cudaError_t e = launch_attention(p, dims->dtype, sub.grid, stream);
+    cudaError_t e = launch_attention(p, dims->dtype, plan.mma, sub.grid, stream);
     if (e != cudaSuccess) return SVP_ERR_CUDA;
     ++launches;
   }

@@ -8,34 +8,48 @@
 // scaled scores over the keys visible to it, times V, plus the log-sum-exp.
 //
 // How (GB300 design):
-//  * Work unit = (sequence b, kv head g, row group rg, split s).  The rows of
+//  * Work unit = (sequence b, kv head g, split s, row group rg).  The rows of
 //    a unit are up to RB query rows (i, h) that share kv head g (GQA group x
 //    q_len), so each K/V page fetched serves all of them.  Only pages that
 //    hold visible keys are enumerated (sink pages, then window pages), so
 //    masked-out pages are never read.
-//  * Persistent CTAs pull units from a global work queue (atomic counter).
-//    One producer warp streams the unit's pages: it reads the block table
-//    once per unit (one coalesced load per 32 pages) and issues one 1-D bulk
-//    copy (TMA engine, cp.async.bulk) per 16-row K page and V page into an
-//    NSTAGES-deep shared-memory ring guarded by mbarriers.  The producer runs
-//    ahead across unit boundaries.
-//  * Four consumer warps take pages round-robin.  Lane l owns D/32
-//    contiguous dims; a page's 16 partial dot products are reduced with a
-//    transposing butterfly (16 shuffles per row) so that lane l ends with the
-//    score of key l/2.  Scores are in the log2 domain (q prescaled by
-//    scale*log2 e) and folded into a running (max, sum, acc) per row with
-//    exp2; the four warps' states are merged by log-sum-exp at unit end.
-//  * Split-K: a unit covers split_pages pages.  If a sequence needs more
-//    than one split, each writes its normalised partial (o, lse2) to the
-//    workspace and takes an atomic ticket; the CTA that takes the last
-//    ticket merges all partials in split order (deterministic) and resets
-//    the ticket.  No CTA ever waits for another.
+//  * Persistent CTAs pull units from a global work queue (atomic counter,
+//    next unit claimed one unit ahead).  One producer warp streams the
+//    unit's pages: it reads the block table once per unit (one coalesced
+//    load per 32 pages) and fills an NSTAGES-deep shared-memory ring guarded
+//    by mbarriers, running ahead across unit boundaries.
+//  * CUDA-core path (few rows per kv head): one 1-D bulk copy (TMA engine,
+//    cp.async.bulk) per 16-row K page and V page.  Four consumer warps take
+//    pages round-robin; lane l owns D/32 dims; a page's 16 partial dot
+//    products are reduced with a transposing butterfly so lane l ends with
+//    the score of key l/2; online softmax in the log2 domain with exp2.
+//  * Tensor-core path (bf16, many rows: GQA groups x verify positions): each
+//    page arrives as 2-D tensor copies (cp.async.bulk.tensor, 128-byte
+//    swizzle, 64-element boxes) so ldmatrix reads are bank-conflict free.
+//    A consumer warp owns whole pages for a 16-row group: S = Q K^T with
+//    mma.sync m16n8k16 (keys as N), the S accumulators are re-used in
+//    registers as the A operand of P V (no shared-memory round trip), V is
+//    read with ldmatrix.trans.  The running row sums stay per lane and are
+//    reduced once per unit.
+//  * The warps' states are merged by log-sum-exp at unit end.  Split-K: if a
+//    sequence needs more than one split, each writes its normalised partial
+//    (o, lse2) to the workspace and takes an atomic ticket; the CTA that
+//    takes the last ticket merges all partials in split order
+//    (deterministic) and resets the ticket.  No CTA ever waits for another.
+//  * Rows of a page that hold no valid data (positions >= seq_len, evicted
+//    stream rows) are zeroed in shared memory before P V, because p = 0
+//    times a NaN left in unused cache memory is still NaN.
 //  * Every wait is bounded (mbar_wait); a timeout raises SVP_DEV_TIMEOUT and
 //    the CTA drains its outstanding copies and exits.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "ptx.cuh"
 #include "svp.h"
@@ -51,11 +65,18 @@ constexpr int kUnitRing = 4;
 constexpr int kMaxSplitPages = 128;  // 4 block-table entries per producer lane
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBoxElems = 64;        // 128-byte swizzle box: 64 bf16 columns
+constexpr int kBoxBytes = kBlockSize * 128;
 
 struct UnitInfo {
   int b, g, rg, split;
   int n_splits, page0, n_pages, seq_len;
   int n_a, b_start, valid, pad;
+};
+
+struct TensorMaps {
+  CUtensorMap k;
+  CUtensorMap v;
 };
 
 // Visible logical blocks of a sequence: [0, n_a) followed by
@@ -84,7 +105,6 @@ struct Vec;
 // lane owns VEC = D/32 consecutive elements; load them as fp32
 template <>
 struct Vec<float, 64> {
-  static constexpr int N = 2;
   __device__ static void load(const float *p, float (&f)[2]) {
     float2 v = *reinterpret_cast<const float2 *>(p);
     f[0] = v.x; f[1] = v.y;
@@ -92,7 +112,6 @@ struct Vec<float, 64> {
 };
 template <>
 struct Vec<float, 128> {
-  static constexpr int N = 4;
   __device__ static void load(const float *p, float (&f)[4]) {
     float4 v = *reinterpret_cast<const float4 *>(p);
     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
@@ -100,7 +119,6 @@ struct Vec<float, 128> {
 };
 template <>
 struct Vec<uint16_t, 64> {
-  static constexpr int N = 2;
   __device__ static void load(const uint16_t *p, float (&f)[2]) {
     uint32_t v = *reinterpret_cast<const uint32_t *>(p);
     f[0] = __uint_as_float(v << 16);
@@ -109,7 +127,6 @@ struct Vec<uint16_t, 64> {
 };
 template <>
 struct Vec<uint16_t, 128> {
-  static constexpr int N = 4;
   __device__ static void load(const uint16_t *p, float (&f)[4]) {
     uint2 v = *reinterpret_cast<const uint2 *>(p);
     f[0] = __uint_as_float(v.x << 16);
@@ -125,9 +142,8 @@ __device__ __forceinline__ void store_out(uint16_t *p, float v) {
   *p = *reinterpret_cast<uint16_t *>(&h);
 }
 
-template <typename T, int D, int RB>
+template <typename T, int D>
 struct Cfg {
-  static constexpr int VEC = D / 32;
   static constexpr int PAGE_ELEMS = kBlockSize * D;
   static constexpr int PAGE_BYTES = PAGE_ELEMS * (int)sizeof(T);
   static constexpr int STAGES = (65536 / (2 * PAGE_BYTES)) < 4
@@ -138,9 +154,9 @@ struct Cfg {
 };
 
 template <typename T, int D, int RB>
-struct __align__(128) Smem {
-  using C = Cfg<T, D, RB>;
-  T kv[C::STAGES][2][C::PAGE_ELEMS];               // K page, V page
+struct Smem {
+  using C = Cfg<T, D>;
+  alignas(1024) unsigned char kv[C::STAGES][2][C::PAGE_BYTES];  // K, V page
   float red_o[kConsumerWarps][RB][D];
   float red_m[kConsumerWarps][RB];
   float red_l[kConsumerWarps][RB];
@@ -159,7 +175,8 @@ struct __align__(128) Smem {
 
 template <typename T, int D, int RB>
 constexpr size_t smem_bytes(int batch) {
-  return sizeof(Smem<T, D, RB>) + sizeof(int) * (size_t)batch + 16;
+  // + 1024 so the ring can be aligned to 1024 bytes (the swizzle atom)
+  return sizeof(Smem<T, D, RB>) + sizeof(int) * (size_t)batch + 1024;
 }
 
 __device__ __forceinline__ void raise_flag(unsigned f) {
@@ -178,10 +195,51 @@ __device__ __forceinline__ bool epi_sync(S &sm, uint32_t &phase, int lane) {
 }
 
 // --------------------------------------------------------------------------
-// per-page consumer work
+// tensor-core helpers (warp-level MMA, bf16 in, fp32 accumulate)
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0,
+                                        uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0,
+                                          uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// two fp32 -> bf16x2 (round to nearest even); `lo` goes to the low half
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Byte offset of 16-byte chunk `chunk` of row `key` in a page stored as
+// D/64 boxes of [16 rows][128 B] with the TMA 128-byte swizzle (the chunk
+// index within a 128-byte row is XOR-ed with the row index mod 8).
+__device__ __forceinline__ uint32_t swz(int key, int chunk) {
+  return (uint32_t)((chunk >> 3) * kBoxBytes + key * 128 +
+                    (((chunk & 7) ^ (key & 7)) << 4));
+}
+
+// --------------------------------------------------------------------------
+// CUDA-core consumer work on one page
 // --------------------------------------------------------------------------
 template <typename T, int D, int RB>
-__device__ __forceinline__ void process_page(
+__device__ __forceinline__ void process_page_fma(
     const T *__restrict__ kp, const T *__restrict__ vp,
     const float (&q)[RB][D / 32], float (&o)[RB][D / 32], float (&m)[RB],
     float (&l)[RB], float *pbuf /* [RB][16] of this warp */, int lane, int j0,
@@ -290,37 +348,138 @@ __device__ __forceinline__ void process_page(
   __syncwarp();
 }
 
-// Zero the V rows of a page that lie outside the union of the visible sets
-// (positions >= seq_len or evicted stream positions): their storage may hold
-// anything, and p = 0 times a NaN is still NaN.
-template <typename T, int D>
-__device__ __forceinline__ void zero_invalid_rows(T *vp, int lane, int j0,
-                                                  int L, int t0, int n_sink,
-                                                  int window) {
-  constexpr int CHUNKS = D * (int)sizeof(T) / 16;  // 16-B chunks per row
+// --------------------------------------------------------------------------
+// tensor-core consumer work on one page (16 query rows x 16 keys)
+// Lane layout of m16n8k16: g = lane/4 (rows g, g+8), t = lane%4.
+// --------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void process_page_mma(
+    uint32_t kbase, uint32_t vbase, const uint32_t (&qa)[D / 16][4],
+    float (&o)[D / 8][4], float (&m)[2], float (&lp)[2], int lane, int j0,
+    bool all_visible, const int (&t)[2], int n_sink, int window,
+    float qscale) {
+  const int tq = lane & 3;
+  const int mi = lane >> 3, mrow = lane & 7;
+  // S = Q K^T : two n8 tiles (keys 0-7, 8-15), k over D
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  {
+    const int key = (mi >> 1) * 8 + mrow;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + swz(key, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+      mma16816(s[0], qa[ks], b0, b1);
+      mma16816(s[1], qa[ks], b2, b3);
+    }
+  }
+  // scale into the log2 domain, mask, running max per row (rows g, g+8)
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = s[nt][e] * qscale;
+      if (!all_visible) {
+        const int j = j0 + nt * 8 + 2 * tq + (e & 1);
+        const int tr = t[e >> 1];
+        const bool vis = (j <= tr) &&
+                         (window == 0 || j < n_sink || j > tr - window);
+        v = vis ? v : -INFINITY;
+      }
+      s[nt][e] = v;
+      mx[e >> 1] = fmaxf(mx[e >> 1], v);
+    }
+  float alpha[2], mu[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
+    const float m_new = fmaxf(m[r], mx[r]);
+    mu[r] = (m_new == -INFINITY) ? 0.f : m_new;
+    alpha[r] = ex2(m[r] - mu[r]);
+    m[r] = m_new;
+  }
+  float ps[2] = {0.f, 0.f};
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float pv = ex2(s[nt][e] - mu[e >> 1]);
+      s[nt][e] = pv;
+      ps[e >> 1] += pv;
+    }
+  lp[0] = lp[0] * alpha[0] + ps[0];
+  lp[1] = lp[1] * alpha[1] + ps[1];
+  if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      o[dn][0] *= alpha[0];
+      o[dn][1] *= alpha[0];
+      o[dn][2] *= alpha[1];
+      o[dn][3] *= alpha[1];
+    }
+  }
+  // P as the A operand (the S accumulator layout is the A fragment layout)
+  const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
+                          pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
+  {
+    const int key = (mi & 1) * 8 + mrow;
+#pragma unroll
+    for (int d2 = 0; d2 < D / 16; ++d2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vbase + swz(key, 2 * d2 + (mi >> 1)), b0, b1, b2, b3);
+      mma16816(o[2 * d2], pa, b0, b1);
+      mma16816(o[2 * d2 + 1], pa, b2, b3);
+    }
+  }
+}
+
+// Zero the V rows of a page that lie outside the union of the visible sets.
+template <typename T, int D, bool MMA>
+__device__ __forceinline__ void zero_invalid_rows(unsigned char *vp, int lane,
+                                                  int j0, int L, int t0,
+                                                  int n_sink, int window) {
+  constexpr int ROWB = D * (int)sizeof(T);
+  constexpr int CHUNKS = ROWB / 16;  // 16-B chunks per row
   for (int idx = lane; idx < kBlockSize * CHUNKS; idx += 32) {
     const int r = idx / CHUNKS, c = idx % CHUNKS;
     const int j = j0 + r;
     const bool valid = (j < L) &&
                        (window == 0 || j < n_sink || j > t0 - window);
-    if (!valid)
-      reinterpret_cast<uint4 *>(vp + r * D)[c] = make_uint4(0, 0, 0, 0);
+    if (!valid) {
+      // every chunk of the row is cleared, so the swizzle does not matter
+      const int off = MMA ? (c >> 3) * kBoxBytes + r * 128 + (c & 7) * 16
+                          : r * ROWB + c * 16;
+      *reinterpret_cast<uint4 *>(vp + off) = make_uint4(0, 0, 0, 0);
+    }
   }
   fence_proxy_async_smem();
   __syncwarp();
 }
 
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
+                                            int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <typename T, int D, int RB>
+template <typename T, int D, int RB, bool MMA>
 __global__ void __launch_bounds__(kThreads, 2)
-    paged_attention_kernel(const AttnParams p) {
-  using C = Cfg<T, D, RB>;
-  constexpr int VEC = C::VEC;
+    paged_attention_kernel(const AttnParams p,
+                           const __grid_constant__ TensorMaps tm) {
+  using C = Cfg<T, D>;
+  constexpr int VEC = D / 32;
   constexpr int STAGES = C::STAGES;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem<T, D, RB> &sm = *reinterpret_cast<Smem<T, D, RB> *>(smem_raw);
+  extern __shared__ unsigned char smem_raw[];
+  Smem<T, D, RB> &sm = *reinterpret_cast<Smem<T, D, RB> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -377,10 +536,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     int c = 0;   // pages issued so far
     int us = 0;  // units taken so far
     bool ok = true;
+    int u = 0;
+    if (lane == 0) u = atomicAdd(&p.counters[0], 1);
+    u = __shfl_sync(kFull, u, 0);
     while (true) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(&p.counters[0], 1);
-      u = __shfl_sync(kFull, u, 0);
+      // claim the next unit now; its latency hides behind this unit's work
+      int u_next = 0;
+      if (lane == 0 && u < total_units) u_next = atomicAdd(&p.counters[0], 1);
       const int slot = us % kUnitRing;
       if (lane == 0)
         ok = mbar_wait(&sm.uempty[slot], ((us / kUnitRing) & 1) ^ 1);
@@ -407,18 +569,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int t2 = ub / p.n_rg;
       const int split = t2 % n_splits;
       const int g = t2 / n_splits;
-      const int L = p.seq_lens[b];
+      const int L = __ldg(p.seq_lens + b);
       int na, bs, np;
       visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
       const int page0 = split * p.split_pages;
       const int n_pages = min(p.split_pages, np - page0);
-      if (lane == 0) {
-        UnitInfo &ui = sm.unit[slot];
-        ui.b = b; ui.g = g; ui.rg = rg; ui.split = split;
-        ui.n_splits = n_splits; ui.page0 = page0; ui.n_pages = n_pages;
-        ui.seq_len = L; ui.n_a = na; ui.b_start = bs; ui.valid = 1;
-        mbar_arrive(&sm.ufull[slot]);
-      }
       // block-table entries of this unit's pages, one coalesced load each
       int phys[kMaxSplitPages / 32];
 #pragma unroll
@@ -431,7 +586,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           phys[k4] = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
         }
       }
-      const size_t head_off = (size_t)g * C::PAGE_ELEMS;
+      if (lane == 0) {
+        UnitInfo &ui = sm.unit[slot];
+        ui.b = b; ui.g = g; ui.rg = rg; ui.split = split;
+        ui.n_splits = n_splits; ui.page0 = page0; ui.n_pages = n_pages;
+        ui.seq_len = L; ui.n_a = na; ui.b_start = bs; ui.valid = 1;
+        mbar_arrive(&sm.ufull[slot]);
+      }
 #pragma unroll
       for (int k4 = 0; k4 < kMaxSplitPages / 32; ++k4) {
         for (int kk = 0; kk < 32; ++kk) {
@@ -448,12 +609,24 @@ __global__ void __launch_bounds__(kThreads, 2)
               mbar_arrive(&sm.full[s]);
             } else {
               sm.stage_ok[s] = 1;
-              const size_t off = (size_t)ph * p.num_kv_heads * C::PAGE_ELEMS + head_off;
               mbar_arrive_expect_tx(&sm.full[s], 2 * C::PAGE_BYTES);
-              bulk_g2s(sm.kv[s][0], static_cast<const T *>(p.k_cache) + off,
-                       C::PAGE_BYTES, &sm.full[s]);
-              bulk_g2s(sm.kv[s][1], static_cast<const T *>(p.v_cache) + off,
-                       C::PAGE_BYTES, &sm.full[s]);
+              if constexpr (MMA) {
+                const int y = (ph * p.num_kv_heads + g) * kBlockSize;
+#pragma unroll
+                for (int bx = 0; bx < D / kBoxElems; ++bx) {
+                  tma_load_2d(sm.kv[s][0] + bx * kBoxBytes, &tm.k,
+                              bx * kBoxElems, y, &sm.full[s]);
+                  tma_load_2d(sm.kv[s][1] + bx * kBoxBytes, &tm.v,
+                              bx * kBoxElems, y, &sm.full[s]);
+                }
+              } else {
+                const size_t off =
+                    ((size_t)ph * p.num_kv_heads + g) * C::PAGE_ELEMS;
+                bulk_g2s(sm.kv[s][0], static_cast<const T *>(p.k_cache) + off,
+                         C::PAGE_BYTES, &sm.full[s]);
+                bulk_g2s(sm.kv[s][1], static_cast<const T *>(p.v_cache) + off,
+                         C::PAGE_BYTES, &sm.full[s]);
+              }
             }
           }
           ok = __shfl_sync(kFull, ok, 0);
@@ -464,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (!ok) break;
       ++us;
+      u = __shfl_sync(kFull, u_next, 0);
     }
     if (!ok) {
       // give up: flag it, then wait (bounded) for copies still in flight
@@ -494,79 +668,169 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       const int b = ui.b, g = ui.g, rg = ui.rg, L = ui.seq_len;
       const int t0 = L - p.q_len;
-      // this unit's query rows
-      float q[RB][VEC], o[RB][VEC], m[RB], l[RB];
-      int t[RB];
-      int t_min = 0x7fffffff, t_max = -1;
-#pragma unroll
+      const int first =
+          ((warp - c) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+      bool aborted = false;
+      int t_min = 0x7fffffff, t_max = -1;  // positions of the unit's rows
       for (int r = 0; r < RB; ++r) {
         const int gr = rg * RB + r;
-        m[r] = -INFINITY;
-        l[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) { o[r][e] = 0.f; q[r][e] = 0.f; }
-        t[r] = -1;
         if (gr < p.rows) {
-          const int i = gr / p.group;
-          const int h = g * p.group + gr % p.group;
-          const T *qp = static_cast<const T *>(p.q) +
-                        (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
-                        lane * VEC;
-          Vec<T, D>::load(qp, q[r]);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
-          t[r] = t0 + i;
-          t_min = min(t_min, t[r]);
-          t_max = max(t_max, t[r]);
+          const int tt = t0 + gr / p.group;
+          t_min = min(t_min, tt);
+          t_max = max(t_max, tt);
         }
       }
-      // pages of this unit owned by this warp: global page index == warp mod 4
-      const int first = ((warp - c) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-      bool aborted = false;
-      for (int k = first; k < ui.n_pages; k += kConsumerWarps) {
-        const int cc = c + k;
-        const int s = cc % STAGES;
-        const bool got =
-            __all_sync(kFull, mbar_wait(&sm.full[s], (cc / STAGES) & 1));
-        if (!got) {
-          if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
-          aborted = true;
-          break;
+
+      if constexpr (MMA) {
+        // ---- tensor-core path: 16 rows, lane rows g and g+8 ----
+        const int gq = lane >> 2, tq = lane & 3;
+        uint32_t qa[D / 16][4];
+        float o[D / 8][4];
+        float m[2] = {-INFINITY, -INFINITY}, lp[2] = {0.f, 0.f};
+        int t[2] = {-1, -1};
+        const uint16_t *qrow[2] = {nullptr, nullptr};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int gr = rg * RB + gq + 8 * r;
+          if (gr < p.rows) {
+            const int i = gr / p.group;
+            const int h = g * p.group + gr % p.group;
+            qrow[r] = static_cast<const uint16_t *>(p.q) +
+                      (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D;
+            t[r] = t0 + i;
+          }
         }
-        if (sm.stage_ok[s]) {
-          const int pidx = ui.page0 + k;
-          const int lb = (pidx < ui.n_a) ? pidx : ui.b_start + (pidx - ui.n_a);
-          const int j0 = lb * kBlockSize;
-          const int j1 = j0 + kBlockSize - 1;
-          // rows of this page outside the union of visible sets?
-          const bool union_full =
-              (j1 < L) && (p.window == 0 || j1 < p.n_sink ||
-                           j0 > t0 - p.window);
-          if (!union_full)
-            zero_invalid_rows<T, D>(sm.kv[s][1], lane, j0, L, t0, p.n_sink,
-                                    p.window);
-          const bool all_vis =
-              (j1 <= t_min) && (p.window == 0 || j1 < p.n_sink ||
-                                j0 > t_max - p.window);
-          process_page<T, D, RB>(sm.kv[s][0], sm.kv[s][1], q, o, m, l, pbuf,
-                                 lane, j0, all_vis, t, p.n_sink, p.window);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int d0 = ks * 16 + 2 * tq;
+          qa[ks][0] = qrow[0] ? *reinterpret_cast<const uint32_t *>(qrow[0] + d0) : 0u;
+          qa[ks][1] = qrow[1] ? *reinterpret_cast<const uint32_t *>(qrow[1] + d0) : 0u;
+          qa[ks][2] = qrow[0] ? *reinterpret_cast<const uint32_t *>(qrow[0] + d0 + 8) : 0u;
+          qa[ks][3] = qrow[1] ? *reinterpret_cast<const uint32_t *>(qrow[1] + d0 + 8) : 0u;
         }
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn)
+          o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+
+        for (int k = first; k < ui.n_pages; k += kConsumerWarps) {
+          const int cc = c + k;
+          const int s = cc % STAGES;
+          const bool got =
+              __all_sync(kFull, mbar_wait(&sm.full[s], (cc / STAGES) & 1));
+          if (!got) {
+            if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
+            aborted = true;
+            break;
+          }
+          if (sm.stage_ok[s]) {
+            const int pidx = ui.page0 + k;
+            const int lb = (pidx < ui.n_a) ? pidx : ui.b_start + (pidx - ui.n_a);
+            const int j0 = lb * kBlockSize;
+            const int j1 = j0 + kBlockSize - 1;
+            const bool union_full = (j1 < L) && (p.window == 0 || j1 < p.n_sink ||
+                                                 j0 > t0 - p.window);
+            if (!union_full)
+              zero_invalid_rows<T, D, true>(sm.kv[s][1], lane, j0, L, t0,
+                                            p.n_sink, p.window);
+            const bool all_vis = (j1 <= t_min) &&
+                                 (p.window == 0 || j1 < p.n_sink ||
+                                  j0 > t_max - p.window);
+            process_page_mma<D>(smem_u32(sm.kv[s][0]), smem_u32(sm.kv[s][1]),
+                                qa, o, m, lp, lane, j0, all_vis, t, p.n_sink,
+                                p.window, p.qscale);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[s]);
+        }
+        // per-lane partial row sums -> the quad (same g) total
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          lp[r] += __shfl_xor_sync(kFull, lp[r], 1);
+          lp[r] += __shfl_xor_sync(kFull, lp[r], 2);
+        }
+        if (tq == 0) {
+          sm.red_m[warp][gq] = m[0];
+          sm.red_m[warp][gq + 8] = m[1];
+          sm.red_l[warp][gq] = lp[0];
+          sm.red_l[warp][gq + 8] = lp[1];
+        }
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          const int d = dn * 8 + 2 * tq;
+          *reinterpret_cast<float2 *>(&sm.red_o[warp][gq][d]) =
+              make_float2(o[dn][0], o[dn][1]);
+          *reinterpret_cast<float2 *>(&sm.red_o[warp][gq + 8][d]) =
+              make_float2(o[dn][2], o[dn][3]);
+        }
+      } else {
+        // ---- CUDA-core path ----
+        float q[RB][VEC], o[RB][VEC], m[RB], l[RB];
+        int t[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const int gr = rg * RB + r;
+          m[r] = -INFINITY;
+          l[r] = 0.f;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) { o[r][e] = 0.f; q[r][e] = 0.f; }
+          t[r] = -1;
+          if (gr < p.rows) {
+            const int i = gr / p.group;
+            const int h = g * p.group + gr % p.group;
+            const T *qp = static_cast<const T *>(p.q) +
+                          (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
+                          lane * VEC;
+            Vec<T, D>::load(qp, q[r]);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
+            t[r] = t0 + i;
+          }
+        }
+        for (int k = first; k < ui.n_pages; k += kConsumerWarps) {
+          const int cc = c + k;
+          const int s = cc % STAGES;
+          const bool got =
+              __all_sync(kFull, mbar_wait(&sm.full[s], (cc / STAGES) & 1));
+          if (!got) {
+            if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
+            aborted = true;
+            break;
+          }
+          if (sm.stage_ok[s]) {
+            const int pidx = ui.page0 + k;
+            const int lb = (pidx < ui.n_a) ? pidx : ui.b_start + (pidx - ui.n_a);
+            const int j0 = lb * kBlockSize;
+            const int j1 = j0 + kBlockSize - 1;
+            const bool union_full = (j1 < L) && (p.window == 0 || j1 < p.n_sink ||
+                                                 j0 > t0 - p.window);
+            if (!union_full)
+              zero_invalid_rows<T, D, false>(sm.kv[s][1], lane, j0, L, t0,
+                                             p.n_sink, p.window);
+            const bool all_vis = (j1 <= t_min) &&
+                                 (p.window == 0 || j1 < p.n_sink ||
+                                  j0 > t_max - p.window);
+            process_page_fma<T, D, RB>(
+                reinterpret_cast<const T *>(sm.kv[s][0]),
+                reinterpret_cast<const T *>(sm.kv[s][1]), q, o, m, l, pbuf,
+                lane, j0, all_vis, t, p.n_sink, p.window);
+          }
+          if (lane == 0) mbar_arrive(&sm.empty[s]);
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int r = 0; r < RB; ++r) {
+            sm.red_m[warp][r] = m[r];
+            sm.red_l[warp][r] = l[r];
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) sm.red_o[warp][r][lane * VEC + e] = o[r][e];
       }
       c += ui.n_pages;
 
       // ---- epilogue: merge the 4 warps' states ----
-      if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-          sm.red_m[warp][r] = m[r];
-          sm.red_l[warp][r] = l[r];
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < RB; ++r)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) sm.red_o[warp][r][lane * VEC + e] = o[r][e];
       if (!epi_sync(sm, epi_phase, lane) || aborted) {
         if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
         break;
@@ -584,7 +848,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (M != -INFINITY) {
 #pragma unroll
           for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = ex2(sm.red_m[w][r] - M);
+            const float mw = sm.red_m[w][r];
+            if (mw == -INFINITY) continue;
+            const float f = ex2(mw - M);
             Lsum = fmaf(f, sm.red_l[w][r], Lsum);
             O = fmaf(f, sm.red_o[w][r][d], O);
           }
@@ -689,67 +955,143 @@ __global__ void __launch_bounds__(kThreads, 2)
 // --------------------------------------------------------------------------
 // host side
 // --------------------------------------------------------------------------
-template <typename T, int D, int RB>
-static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
-  const size_t smem = smem_bytes<T, D, RB>(p.batch);
-  auto kern = paged_attention_kernel<T, D, RB>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+
+// cuTensorMapEncodeTiled, fetched once through the runtime (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
 }
 
-template <typename T, int D, int RB>
-static int occupancy_t(int batch) {
-  const size_t smem = smem_bytes<T, D, RB>(batch);
-  auto kern = paged_attention_kernel<T, D, RB>;
+// The cache as a 2-D bf16 tensor [num_blocks*Hkv*16 rows, D], 128-byte
+// swizzled boxes of 16 rows x 64 columns.
+static bool make_kv_map(CUtensorMap *map, const void *base, int num_blocks,
+                        int hkv, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d,
+                              (cuuint64_t)num_blocks * hkv * kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBoxElems, (cuuint32_t)kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// per (device, instantiation, shared-memory size): attribute set + occupancy
+static std::mutex g_occ_mu;
+static std::map<std::tuple<int, const void *, size_t>, int> g_occ;
+
+static size_t batch_bucket(int batch) { return (size_t)(batch + 255) / 256 * 256; }
+
+template <typename T, int D, int RB, bool MMA>
+static int prepare_t(int batch) {
+  const size_t smem = smem_bytes<T, D, RB>((int)batch_bucket(batch));
+  auto kern = paged_attention_kernel<T, D, RB, MMA>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  const auto key = std::make_tuple(dev, (const void *)kern, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
-    return 1;
+    return -1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) !=
       cudaSuccess)
-    return 1;
-  return n > 0 ? n : 1;
+    return -1;
+  n = n > 0 ? n : 1;
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  g_occ[key] = n;
+  return n;
 }
 
-#define SVP_DISPATCH_RB(T, D, RB, CALL) \
-  switch (RB) {                         \
-    case 1: CALL(T, D, 1); break;       \
-    case 2: CALL(T, D, 2); break;       \
-    case 4: CALL(T, D, 4); break;       \
-    default: CALL(T, D, 8); break;      \
+template <typename T, int D, int RB, bool MMA>
+static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
+  if (prepare_t<T, D, RB, MMA>(p.batch) < 0) return cudaErrorInvalidValue;
+  const size_t smem = smem_bytes<T, D, RB>((int)batch_bucket(p.batch));
+  TensorMaps tm;
+  memset(&tm, 0, sizeof tm);
+  if constexpr (MMA) {
+    if (!make_kv_map(&tm.k, p.k_cache, p.num_blocks, p.num_kv_heads, D) ||
+        !make_kv_map(&tm.v, p.v_cache, p.num_blocks, p.num_kv_heads, D))
+      return cudaErrorInvalidValue;
   }
+  paged_attention_kernel<T, D, RB, MMA><<<grid, kThreads, smem, st>>>(p, tm);
+  return cudaGetLastError();
+}
 
-cudaError_t launch_attention(const AttnParams &p, int dtype, int grid,
-                             cudaStream_t stream) {
+#define SVP_DISPATCH(DTYPE, HD, RB, MMA, CALL)                        \
+  do {                                                                \
+    if (MMA) {                                                        \
+      if (HD == 64) CALL(uint16_t, 64, 16, true);                     \
+      else CALL(uint16_t, 128, 16, true);                             \
+    } else if (DTYPE == 0) {                                          \
+      if (HD == 64) {                                                 \
+        switch (RB) { case 1: CALL(float, 64, 1, false); break;       \
+                      case 2: CALL(float, 64, 2, false); break;       \
+                      case 4: CALL(float, 64, 4, false); break;       \
+                      default: CALL(float, 64, 8, false); }           \
+      } else {                                                        \
+        switch (RB) { case 1: CALL(float, 128, 1, false); break;      \
+                      case 2: CALL(float, 128, 2, false); break;      \
+                      case 4: CALL(float, 128, 4, false); break;      \
+                      default: CALL(float, 128, 8, false); }          \
+      }                                                               \
+    } else {                                                          \
+      if (HD == 64) {                                                 \
+        switch (RB) { case 1: CALL(uint16_t, 64, 1, false); break;    \
+                      case 2: CALL(uint16_t, 64, 2, false); break;    \
+                      case 4: CALL(uint16_t, 64, 4, false); break;    \
+                      default: CALL(uint16_t, 64, 8, false); }        \
+      } else {                                                        \
+        switch (RB) { case 1: CALL(uint16_t, 128, 1, false); break;   \
+                      case 2: CALL(uint16_t, 128, 2, false); break;   \
+                      case 4: CALL(uint16_t, 128, 4, false); break;   \
+                      default: CALL(uint16_t, 128, 8, false); }       \
+      }                                                               \
+    }                                                                 \
+  } while (0)
+
+cudaError_t launch_attention(const AttnParams &p, int dtype, bool mma,
+                             int grid, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
-#define SVP_CALL(T, D, RB) e = launch_t<T, D, RB>(p, grid, stream)
-  if (dtype == 0) {
-    if (p.head_dim == 64) { SVP_DISPATCH_RB(float, 64, p.rb, SVP_CALL) }
-    else { SVP_DISPATCH_RB(float, 128, p.rb, SVP_CALL) }
-  } else {
-    if (p.head_dim == 64) { SVP_DISPATCH_RB(uint16_t, 64, p.rb, SVP_CALL) }
-    else { SVP_DISPATCH_RB(uint16_t, 128, p.rb, SVP_CALL) }
-  }
+#define SVP_CALL(T, D, RB, M) e = launch_t<T, D, RB, M>(p, grid, stream)
+  SVP_DISPATCH(dtype, p.head_dim, p.rb, mma, SVP_CALL);
 #undef SVP_CALL
   return e;
 }
 
-int attention_ctas_per_sm(int dtype, int head_dim, int rb, int batch) {
+int attention_ctas_per_sm(int dtype, int head_dim, int rb, bool mma,
+                          int batch) {
   int n = 1;
-#define SVP_CALL(T, D, RB) n = occupancy_t<T, D, RB>(batch)
-  if (dtype == 0) {
-    if (head_dim == 64) { SVP_DISPATCH_RB(float, 64, rb, SVP_CALL) }
-    else { SVP_DISPATCH_RB(float, 128, rb, SVP_CALL) }
-  } else {
-    if (head_dim == 64) { SVP_DISPATCH_RB(uint16_t, 64, rb, SVP_CALL) }
-    else { SVP_DISPATCH_RB(uint16_t, 128, rb, SVP_CALL) }
-  }
+#define SVP_CALL(T, D, RB, M) n = prepare_t<T, D, RB, M>(batch)
+  SVP_DISPATCH(dtype, head_dim, rb, mma, SVP_CALL);
 #undef SVP_CALL
-  return n;
+  return n > 0 ? n : 1;
 }
+
+bool tensor_maps_available() { return encode_fn() != nullptr; }
 
 cudaError_t read_status_attention(cudaStream_t s, unsigned *flags) {
   unsigned v = 0;

@@ -39,6 +39,7 @@ struct AttnParams {
 
 struct AttnPlan {
   int rb, n_rg, split_pages, max_splits, grid, ctas_per_sm;
+  bool mma;            // tensor-core path
   size_t ws_counters, ws_tickets, ws_part_o, ws_part_lse, ws_total;
 };
 
@@ -46,14 +47,23 @@ struct AttnPlan {
 // a negative svp_status.
 int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    int dtype, int max_blocks, int q_len, int n_sink,
-                   int window, int split_pages, int num_sms, AttnPlan *plan);
+                   int window, int split_pages, int kernel_path, int num_sms,
+                   long long num_blocks, AttnPlan *plan);
+
+// Query rows per kv head (GQA group x q_len) from which the automatic path
+// choice uses tensor cores (bf16 only).
+constexpr int kMmaMinRows = 3;
 
 // Occupancy-derived CTAs per SM for the attention kernel of this shape
 // (queried once per device and shape, cached).
-int attention_ctas_per_sm(int dtype, int head_dim, int rb, int batch);
+int attention_ctas_per_sm(int dtype, int head_dim, int rb, bool mma,
+                          int batch);
 
-cudaError_t launch_attention(const AttnParams &p, int dtype, int grid,
-                             cudaStream_t stream);
+cudaError_t launch_attention(const AttnParams &p, int dtype, bool mma,
+                             int grid, cudaStream_t stream);
+
+// True when the driver provides cuTensorMapEncodeTiled.
+bool tensor_maps_available();
 
 struct AppendParams {
   const void *k_new;

@@ -25,7 +25,8 @@ def svp():
     return m
 
 
-def _run_gpu(svp, wl, n_sink, window, split_pages=0, append=True):
+def _run_gpu(svp, wl, n_sink, window, split_pages=0, append=True,
+             kernel_path=0):
     import torch
     kc, vc = to_dev(wl.k_cache), to_dev(wl.v_cache)
     bt, sl = to_dev(wl.block_table), to_dev(wl.seq_lens)
@@ -33,7 +34,8 @@ def _run_gpu(svp, wl, n_sink, window, split_pages=0, append=True):
         svp.kv_append(to_dev(wl.k_new), to_dev(wl.v_new), kc, vc, bt, sl)
     out, lse = svp.paged_decode_attention(
         to_dev(wl.q), kc, vc, bt, sl, q_len=wl.q_len, n_sink=n_sink,
-        window=window, scale=float(wl.scale), split_pages=split_pages)
+        window=window, scale=float(wl.scale), split_pages=split_pages,
+        kernel_path=kernel_path)
     torch.cuda.synchronize()
     assert svp.read_device_status() == 0
     return out_as_f64(out), lse.cpu().numpy().astype(np.float64)
@@ -83,37 +85,52 @@ SWEEP = [
 ]
 
 
+PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("case", SWEEP, ids=[str(i) for i in range(len(SWEEP))])
-def test_parity_sweep(svp, oracle_mod, case):
+def test_parity_sweep(svp, oracle_mod, case, path):
+    """Every case through each kernel path (automatic choice, CUDA cores,
+    tensor cores); fp32 data has no tensor-core path and must say so."""
     dtype, D, Hq, Hkv, q_len, lo, hi, n_sink, window, sp = case
     cfg = W.small_config(batch=5, num_q_heads=Hq, num_kv_heads=Hkv,
                          head_dim=D, q_len=q_len, dtype=dtype, ctx_min=lo,
                          ctx_max=hi, seed=100 + D + q_len + Hq)
     wl = W.make_attention(cfg, n_new=min(q_len, 2))
-    got = _run_gpu(svp, wl, n_sink, window, split_pages=sp)
+    if dtype == "f32" and path == "tensor_cores":
+        with pytest.raises(svp.SvpError) as e:
+            _run_gpu(svp, wl, n_sink, window, split_pages=sp,
+                     kernel_path=PATHS[path])
+        assert e.value.status == -2
+        return
+    got = _run_gpu(svp, wl, n_sink, window, split_pages=sp,
+                   kernel_path=PATHS[path])
     _compare(wl, got, _oracle(oracle_mod, wl, n_sink, window))
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("sp", [1, 2, 7, 128])
-def test_split_counts_agree(svp, oracle_mod, sp):
+def test_split_counts_agree(svp, oracle_mod, sp, path):
     """The same inputs under different split sizes (1 page per split up to
     128) all match the oracle: the log-sum-exp merge is exact."""
     cfg = W.small_config(batch=4, num_q_heads=8, num_kv_heads=2, head_dim=128,
                          q_len=2, ctx_min=2, ctx_max=900, seed=17)
     wl = W.make_attention(cfg)
-    got = _run_gpu(svp, wl, 0, 0, split_pages=sp)
+    got = _run_gpu(svp, wl, 0, 0, split_pages=sp, kernel_path=path)
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
 
 
-def test_ring_layout_small(svp, oracle_mod):
+@pytest.mark.parametrize("path,q_len,Hq", [(1, 1, 4), (2, 1, 4), (2, 3, 8)])
+def test_ring_layout_small(svp, oracle_mod, path, q_len, Hq):
     """A streaming cache in a ring of pages with NaN in every non-resident
     row: only sink and window rows may be read."""
-    cfg = W.small_config(batch=3, num_q_heads=4, num_kv_heads=4,
-                         head_dim=128, q_len=1, ctx_min=5000, ctx_max=9000,
-                         n_sink=4, window=100, ring=True, sink_key_scale=4.0,
-                         seed=23)
+    cfg = W.small_config(batch=3, num_q_heads=Hq, num_kv_heads=4,
+                         head_dim=128, q_len=q_len, ctx_min=5000,
+                         ctx_max=9000, n_sink=4, window=100, ring=True,
+                         sink_key_scale=4.0, seed=23)
     wl = W.make_attention(cfg)
-    got = _run_gpu(svp, wl, 4, 100)
+    got = _run_gpu(svp, wl, 4, 100, kernel_path=path)
     _compare(wl, got, _oracle(oracle_mod, wl, 4, 100))
 
 
@@ -143,7 +160,7 @@ def _sampled_rows(wl, n, seed):
     ("long-context-128k-verify", 0, 0, 24),
 ])
 def test_full_size_configs_sampled(svp, oracle_mod, name, n_sink, window,
-                                   n_rows):
+                                   n_rows):  # automatic path, as benchmarked
     """Each workload at full size, in the launch configuration the benchmark
     uses (automatic split size), compared on sampled rows."""
     wl = W.make_attention(W.CONFIGS[name], n_new=W.CONFIGS[name].q_len)
@@ -215,3 +232,24 @@ def test_repeated_calls_reuse_workspace(svp, oracle_mod):
         assert torch.equal(first[0], cur[0]) and torch.equal(first[1], cur[1])
     _compare(wl, (out_as_f64(first[0]), first[1].cpu().numpy().astype(np.float64)),
              _oracle(oracle_mod, wl, 0, 0))
+
+
+def test_workspace_shared_across_shapes(svp, oracle_mod):
+    """One workspace serves calls of different shapes in any order: a small
+    call, a call with many more split tickets, then the small call again."""
+    import torch
+    ws = torch.full((64 << 20,), 0x5A, dtype=torch.uint8, device="cuda:0")
+    shapes = [dict(batch=2, num_q_heads=8, num_kv_heads=2, q_len=2, ctx_max=900),
+              dict(batch=24, num_q_heads=16, num_kv_heads=16, q_len=1, ctx_max=700),
+              dict(batch=2, num_q_heads=8, num_kv_heads=2, q_len=2, ctx_max=900)]
+    for i, kw in enumerate(shapes):
+        cfg = W.small_config(head_dim=128, ctx_min=kw["q_len"], seed=40 + i,
+                             **kw)
+        wl = W.make_attention(cfg)
+        out, lse = svp.paged_decode_attention(
+            to_dev(wl.q), to_dev(wl.k_cache), to_dev(wl.v_cache),
+            to_dev(wl.block_table), to_dev(wl.seq_lens), q_len=wl.q_len,
+            scale=float(wl.scale), split_pages=3, workspace=ws)
+        torch.cuda.synchronize()
+        _compare(wl, (out_as_f64(out), lse.cpu().numpy().astype(np.float64)),
+                 _oracle(oracle_mod, wl, 0, 0))
