@@ -136,6 +136,43 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
                            int q_len, int n_sink, int window, float scale,
                            void *out, float *lse, cudaStream_t stream);
 
+/* Size of the fixed device scratch used by paged_decode_attention_noalloc. */
+#define SVP_STATIC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
+
+/* paged_decode_attention for callers that cannot allocate device memory.
+ *
+ * No counterpart in the source pages: this entry point exists for callers
+ * that must not call cudaMalloc when they run attention -- code executing
+ * while a CUDA graph is being captured (allocation is not capturable),
+ * plug-ins whose host framework owns every device allocation through its
+ * own pool, and latency-critical loops where cudaMalloc/cudaFree would
+ * synchronise the device.
+ *
+ * Same arguments, layouts and results as paged_decode_attention, except
+ * that dims->workspace and dims->workspace_bytes are ignored: the split-K
+ * scratch is a fixed SVP_STATIC_SCRATCH_BYTES array inside the library's
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.  Nothing is allocated by this call.  The caller still
+ * passes q, the caches, block_table, seq_lens, out and lse.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, with that device current);
+ *     make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; the
+ *     call clears the counters it relies on before launching, so calls in
+ *     sequence on one stream are independent.  Calls that overlap on the
+ *     GPU (other streams, other host threads) race on the array.
+ *   - With dims->split_pages == 0 the automatic split size is enlarged (up
+ *     to 128 pages) when the default plan would not fit the array.
+ * Errors: those of paged_decode_attention, plus SVP_ERR_WORKSPACE when the
+ * scratch this request needs exceeds SVP_STATIC_SCRATCH_BYTES (use fewer
+ * sequences per call or longer splits). */
+int paged_decode_attention_noalloc(const svp_dims *dims, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_table,
+                                   const int32_t *seq_lens, int q_len,
+                                   int n_sink, int window, float scale,
+                                   void *out, float *lse, cudaStream_t stream);
+
 /* Bytes of workspace paged_decode_attention needs for these dims and this
  * (q_len, n_sink, window).  Returns 0 for invalid dims. */
 size_t paged_decode_workspace_size(const svp_dims *dims, int q_len,

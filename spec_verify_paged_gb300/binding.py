@@ -23,7 +23,8 @@ SVP_OK, SVP_ERR_INVALID_ARG, SVP_ERR_UNSUPPORTED, SVP_ERR_CUDA, SVP_ERR_WORKSPAC
 SVP_F32, SVP_BF16 = 0, 1
 PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES = 0, 1, 2
 DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
-EXPORTED = ("paged_decode_attention", "paged_decode_workspace_size",
+EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
+            "paged_decode_workspace_size",
             "kv_append", "spec_accept", "svp_read_device_status",
             "svp_status_string", "svp_last_launch_count")
 
@@ -66,6 +67,10 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, i32,
                                                i32, i32, f32, vp, vp, vp]
         lib.paged_decode_attention.restype = i32
+        lib.paged_decode_attention_noalloc.argtypes = [dims_p, vp, vp, vp, vp,
+                                                       vp, i32, i32, i32, f32,
+                                                       vp, vp, vp]
+        lib.paged_decode_attention_noalloc.restype = i32
         lib.paged_decode_workspace_size.argtypes = [dims_p, i32, i32, i32]
         lib.paged_decode_workspace_size.restype = sz
         lib.kv_append.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, vp]

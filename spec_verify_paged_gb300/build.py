@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsvp.so")
-SOURCES = ["attention.cu", "accept.cu", "kv_append.cu", "api.cu"]
+SOURCES = ["attention.cu", "accept.cu", "kv_append.cu", "api.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "svp_internal.h")] + [
     os.path.join(INCLUDE, "svp.h")]
 
