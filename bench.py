@@ -25,6 +25,7 @@ exchange), timing is the max over ranks, value is the sum of the work.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -167,6 +168,34 @@ def to_pinned(a):
     return t.pin_memory()
 
 
+def pack_buffers(parts, dev):
+    """One pinned host buffer and one device buffer holding the given
+    tensors back to back (256-byte aligned); returns (host, device, views of
+    the device buffer shaped like the parts)."""
+    import torch
+    offs, total = [], 0
+    for _, t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    devb = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = {}
+    for (name, t), o in zip(parts, offs):
+        n = t.numel() * t.element_size()
+        views[name] = devb[o:o + n].view(t.dtype).view(t.shape)
+    views["_offsets"] = dict(zip([n for n, _ in parts], offs))
+    views["_host"] = host
+    return host, devb, views
+
+
+def host_view(host, dview):
+    """The host-buffer slice that mirrors a device view from pack_buffers."""
+    base = dview.untyped_storage().data_ptr()
+    off = dview.data_ptr() - base
+    n = dview.numel() * dview.element_size()
+    return host[off:off + n].view(dview.dtype).view(dview.shape)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -206,20 +235,21 @@ def oracle_sample(wl, n_seqs, start=0):
     return time.perf_counter() - t, n_seqs * wl.q_len
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """The oracle as it stands, single-threaded, on sequences of the workload
-    until about budget_s seconds of CPU work."""
+def cpu_baseline(wl, budget_s=10.0, max_passes=20):
+    """The oracle as it stands, single-threaded, on whole sequences of the
+    workload (cycling through them) until about budget_s seconds of CPU
+    work."""
     total_t, total_tok, n = 0.0, 0, 0
-    while total_t < budget_s and n < wl.cfg.batch:
+    while total_t < budget_s and n < max_passes * wl.cfg.batch:
         dt, tok = oracle_sample(wl, 1, start=n)
         total_t += dt
         total_tok += tok
         n += 1
     return {"value": total_tok / total_t, "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": f"{n} of {wl.cfg.batch} sequences of {wl.cfg.name} "
-                      f"(all {wl.cfg.num_q_heads} heads, fp64, one thread), "
-                      f"{total_t:.1f} s"}
+            "sample": f"{n} sequence passes over the {wl.cfg.batch} sequences "
+                      f"of {wl.cfg.name} (all {wl.cfg.num_q_heads} heads, "
+                      f"fp64, one thread), {total_t:.1f} s"}
 
 
 def workload_config(wl, split_pages=None):
@@ -266,6 +296,8 @@ def run_ours(args):
     svp.load_library()
 
     cfg = W.CONFIGS[args.workload]
+    if args.batch:
+        cfg = dataclasses.replace(cfg, batch=args.batch)
     wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
     conf, tr = workload_config(wl, args.split_pages or None)
     if args.kernel_path:
@@ -328,27 +360,27 @@ def run_ours(args):
     ms_max = max_over_ranks(ms, world)
 
     # ---- end to end through the public calls, host buffers ----
-    h_q, h_kn, h_vn = to_pinned(wl.q), to_pinned(wl.k_new), to_pinned(wl.v_new)
-    h_bt, h_sl = to_pinned(wl.block_table), to_pinned(wl.seq_lens)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
-    d_bt, d_sl = torch.empty_like(bt), torch.empty_like(sl)
+    # The step's inputs (q, new K/V rows, block table, lengths) travel in one
+    # pinned buffer and one host-to-device copy; out and lse come back in
+    # one device-to-host copy that the host waits for every step.
+    in_parts = [("q", q), ("k_new", kn), ("v_new", vn), ("block_table", bt),
+                ("seq_lens", sl)]
+    h_in, d_in, d_views = pack_buffers(in_parts, dev)
+    for name, t in in_parts:
+        host_view(h_in, d_views[name]).copy_(t.cpu())
+    out_parts = [("out", out), ("lse", lse)]
+    h_res, d_res, r_views = pack_buffers(out_parts, dev)
 
     def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_kn.copy_(h_kn, non_blocking=True)
-        d_vn.copy_(h_vn, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        svp.kv_append(d_kn, d_vn, kc, vc, d_bt, d_sl)
-        svp.paged_decode_attention(d_q, kc, vc, d_bt, d_sl, q_len=cfg.q_len,
-                                   n_sink=cfg.n_sink, window=cfg.window,
-                                   scale=scale, out=out, lse=lse,
-                                   split_pages=args.split_pages,
-                                   kernel_path=args.kernel_path)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        svp.kv_append(d_views["k_new"], d_views["v_new"], kc, vc,
+                      d_views["block_table"], d_views["seq_lens"])
+        svp.paged_decode_attention(
+            d_views["q"], kc, vc, d_views["block_table"], d_views["seq_lens"],
+            q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
+            scale=scale, out=r_views["out"], lse=r_views["lse"],
+            split_pages=args.split_pages, kernel_path=args.kernel_path)
+        h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -362,8 +394,8 @@ def run_ours(args):
         stream.synchronize()           # the host reads the result every step
     e_ms = (time.perf_counter() - e0) * 1e3 / e_steps
     e_ms = max_over_ranks(e_ms, world)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_sl))
-    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    h2d = sum(t.numel() * t.element_size() for _, t in in_parts)
+    d2h = sum(t.numel() * t.element_size() for _, t in out_parts)
 
     # ---- report ----
     tokens_per_step = cfg.batch * cfg.q_len
@@ -449,6 +481,9 @@ def main(argv=None):
                     help="pages per split-K unit (0: automatic)")
     ap.add_argument("--kernel-path", type=int, default=0, choices=[0, 1, 2],
                     help="0 automatic, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's sequence count (smaller "
+                         "cases for profiling; reported in config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

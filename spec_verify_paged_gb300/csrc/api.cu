@@ -109,7 +109,9 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   } else if (kernel_path == SVP_PATH_AUTO) {
     mma = dtype == SVP_BF16 && rows >= kMmaMinRows && tma_ok;
   }
-  int rb = mma ? 16 : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  // tensor path: one m16 tile per warp, two warps share a page beyond 16
+  int rb = mma ? (rows <= 16 ? 16 : 32)
+               : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
   const int n_rg = (rows + rb - 1) / rb;
   const int mvp = max_visible_pages(max_blocks, q_len, n_sink, window);
   const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);
@@ -122,6 +124,8 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
     const long long want = bound / (slots * 8 > 0 ? slots * 8 : 1);
     pps = 8;
     while (pps < 64 && pps * 2 <= want) pps *= 2;
+    // keep the final log-sum-exp merge cheap: at most 64 splits per sequence
+    while (pps < 128 && (mvp + pps - 1) / pps > 64) pps *= 2;
   }
   if (pps > 128) pps = 128;
   const int max_splits = mvp > 0 ? (mvp + pps - 1) / pps : 1;

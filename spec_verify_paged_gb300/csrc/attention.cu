@@ -153,15 +153,19 @@ struct Cfg {
                                           : (65536 / (2 * PAGE_BYTES));
 };
 
-template <typename T, int D, int RB>
+// RW = rows one consumer warp accumulates: RB on the CUDA-core path, one
+// m16 tile (16) on the tensor-core path, where a unit of 32 rows is shared
+// by warp pairs.
+template <typename T, int D, int RB, int RW>
 struct Smem {
   using C = Cfg<T, D>;
   alignas(1024) unsigned char kv[C::STAGES][2][C::PAGE_BYTES];  // K, V page
-  float red_o[kConsumerWarps][RB][D];
-  float red_m[kConsumerWarps][RB];
-  float red_l[kConsumerWarps][RB];
-  float pbuf[kConsumerWarps][RB][kBlockSize];
+  float red_o[kConsumerWarps][RW][D];
+  float red_m[kConsumerWarps][RW];
+  float red_l[kConsumerWarps][RW];
+  float pbuf[kConsumerWarps][RW][kBlockSize];
   float row_m[RB], row_w[RB];
+  float wf[kConsumerWarps][RB];                    // per-warp row weights
   UnitInfo unit[kUnitRing];
   int stage_ok[C::STAGES];
   uint64_t full[C::STAGES], empty[C::STAGES];
@@ -173,10 +177,11 @@ struct Smem {
   int prefix[1];                                   // [batch + 1], dynamic
 };
 
-template <typename T, int D, int RB>
+template <typename T, int D, int RB, bool MMA>
 constexpr size_t smem_bytes(int batch) {
   // + 1024 so the ring can be aligned to 1024 bytes (the swizzle atom)
-  return sizeof(Smem<T, D, RB>) + sizeof(int) * (size_t)batch + 1024;
+  return sizeof(Smem<T, D, RB, MMA ? 16 : RB>) + sizeof(int) * (size_t)batch +
+         1024;
 }
 
 __device__ __forceinline__ void raise_flag(unsigned f) {
@@ -352,25 +357,50 @@ __device__ __forceinline__ void process_page_fma(
 // tensor-core consumer work on one page (16 query rows x 16 keys)
 // Lane layout of m16n8k16: g = lane/4 (rows g, g+8), t = lane%4.
 // --------------------------------------------------------------------------
+// All MMA operand fragments of one page: K as the B operand of S = Q K^T
+// (ldmatrix) and V as the B operand of P V (ldmatrix.trans), so the ring
+// stage can be released before any arithmetic.
+template <int D>
+__device__ __forceinline__ void load_page_frags(uint32_t kbase, uint32_t vbase,
+                                                uint32_t (&kb)[D / 16][4],
+                                                uint32_t (&vb)[D / 16][4],
+                                                int lane) {
+  const int mi = lane >> 3, mrow = lane & 7;
+  const int kkey = (mi >> 1) * 8 + mrow;
+  const int vkey = (mi & 1) * 8 + mrow;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks)
+    ldsm_x4(kbase + swz(kkey, 2 * ks + (mi & 1)), kb[ks][0], kb[ks][1],
+            kb[ks][2], kb[ks][3]);
+#pragma unroll
+  for (int d2 = 0; d2 < D / 16; ++d2)
+    ldsm_x4_t(vbase + swz(vkey, 2 * d2 + (mi >> 1)), vb[d2][0], vb[d2][1],
+              vb[d2][2], vb[d2][3]);
+}
+
 template <int D>
 __device__ __forceinline__ void process_page_mma(
-    uint32_t kbase, uint32_t vbase, const uint32_t (&qa)[D / 16][4],
-    float (&o)[D / 8][4], float (&m)[2], float (&lp)[2], int lane, int j0,
-    bool all_visible, const int (&t)[2], int n_sink, int window,
-    float qscale) {
+    const uint32_t (&kb)[D / 16][4], const uint32_t (&vb)[D / 16][4],
+    const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4], float (&m)[2],
+    float (&lp)[2], int lane, int j0, bool all_visible, const int (&t)[2],
+    int n_sink, int window, float qscale) {
   const int tq = lane & 3;
-  const int mi = lane >> 3, mrow = lane & 7;
-  // S = Q K^T : two n8 tiles (keys 0-7, 8-15), k over D
+  // S = Q K^T : two n8 tiles (keys 0-7, 8-15), k over D, accumulated in two
+  // independent chains (even / odd k steps) to halve the dependent depth
   float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   {
-    const int key = (mi >> 1) * 8 + mrow;
+    float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kbase + swz(key, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-      mma16816(s[0], qa[ks], b0, b1);
-      mma16816(s[1], qa[ks], b2, b3);
+    for (int ks = 0; ks < D / 16; ks += 2) {
+      mma16816(s[0], qa[ks], kb[ks][0], kb[ks][1]);
+      mma16816(s[1], qa[ks], kb[ks][2], kb[ks][3]);
+      mma16816(s2[0], qa[ks + 1], kb[ks + 1][0], kb[ks + 1][1]);
+      mma16816(s2[1], qa[ks + 1], kb[ks + 1][2], kb[ks + 1][3]);
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
   }
   // scale into the log2 domain, mask, running max per row (rows g, g+8)
   float mx[2] = {-INFINITY, -INFINITY};
@@ -422,15 +452,10 @@ __device__ __forceinline__ void process_page_mma(
   // P as the A operand (the S accumulator layout is the A fragment layout)
   const uint32_t pa[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[0][2], s[0][3]),
                           pack_bf16(s[1][0], s[1][1]), pack_bf16(s[1][2], s[1][3])};
-  {
-    const int key = (mi & 1) * 8 + mrow;
 #pragma unroll
-    for (int d2 = 0; d2 < D / 16; ++d2) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vbase + swz(key, 2 * d2 + (mi >> 1)), b0, b1, b2, b3);
-      mma16816(o[2 * d2], pa, b0, b1);
-      mma16816(o[2 * d2 + 1], pa, b2, b3);
-    }
+  for (int d2 = 0; d2 < D / 16; ++d2) {
+    mma16816(o[2 * d2], pa, vb[d2][0], vb[d2][1]);
+    mma16816(o[2 * d2 + 1], pa, vb[d2][2], vb[d2][3]);
   }
 }
 
@@ -478,7 +503,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int VEC = D / 32;
   constexpr int STAGES = C::STAGES;
   extern __shared__ unsigned char smem_raw[];
-  Smem<T, D, RB> &sm = *reinterpret_cast<Smem<T, D, RB> *>(
+  // tensor path: MT m16 tiles per unit, one per warp of a warp group that
+  // shares each page; NSTREAM groups take pages round-robin
+  constexpr int MT = MMA ? RB / 16 : 1;
+  constexpr int RW = MMA ? 16 : RB;
+  constexpr int NSTREAM = kConsumerWarps / MT;
+  Smem<T, D, RB, RW> &sm = *reinterpret_cast<Smem<T, D, RB, RW> *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x;
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], MT);  // every warp of the owning group
     }
     for (int u = 0; u < kUnitRing; ++u) {
       mbar_init(&sm.ufull[u], 1);
@@ -668,8 +698,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
       const int b = ui.b, g = ui.g, rg = ui.rg, L = ui.seq_len;
       const int t0 = L - p.q_len;
-      const int first =
-          ((warp - c) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+      const int stream = warp / MT, mt = warp % MT;
+      const int first = ((stream - c) % NSTREAM + NSTREAM) % NSTREAM;
       bool aborted = false;
       int t_min = 0x7fffffff, t_max = -1;  // positions of the unit's rows
       for (int r = 0; r < RB; ++r) {
@@ -691,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint16_t *qrow[2] = {nullptr, nullptr};
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const int gr = rg * RB + gq + 8 * r;
+          const int gr = rg * RB + mt * 16 + gq + 8 * r;
           if (gr < p.rows) {
             const int i = gr / p.group;
             const int h = g * p.group + gr % p.group;
@@ -712,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int dn = 0; dn < D / 8; ++dn)
           o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
 
-        for (int k = first; k < ui.n_pages; k += kConsumerWarps) {
+        for (int k = first; k < ui.n_pages; k += NSTREAM) {
           const int cc = c + k;
           const int s = cc % STAGES;
           const bool got =
@@ -735,12 +765,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool all_vis = (j1 <= t_min) &&
                                  (p.window == 0 || j1 < p.n_sink ||
                                   j0 > t_max - p.window);
-            process_page_mma<D>(smem_u32(sm.kv[s][0]), smem_u32(sm.kv[s][1]),
-                                qa, o, m, lp, lane, j0, all_vis, t, p.n_sink,
-                                p.window, p.qscale);
+            uint32_t kb[D / 16][4], vb[D / 16][4];
+            load_page_frags<D>(smem_u32(sm.kv[s][0]), smem_u32(sm.kv[s][1]),
+                               kb, vb, lane);
+            // the page is in registers: hand the stage back to the producer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            process_page_mma<D>(kb, vb, qa, o, m, lp, lane, j0, all_vis, t,
+                                p.n_sink, p.window, p.qscale);
+          } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
         // per-lane partial row sums -> the quad (same g) total
 #pragma unroll
@@ -786,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             t[r] = t0 + i;
           }
         }
-        for (int k = first; k < ui.n_pages; k += kConsumerWarps) {
+        for (int k = first; k < ui.n_pages; k += NSTREAM) {
           const int cc = c + k;
           const int s = cc % STAGES;
           const bool got =
@@ -837,36 +873,68 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const int grp = (b * p.num_kv_heads + g) * p.n_rg + rg;
       const bool single = ui.n_splits == 1;
-      for (int e = ctid; e < RB * D; e += kConsumerWarps * 32) {
-        const int r = e / D, d = e % D;
-        const int gr = rg * RB + r;
-        if (gr >= p.rows) continue;
+      const int vrows = min(RB, p.rows - rg * RB);  // valid rows of the unit
+      // per-row statistics, once per row: row r lives in local row lr of
+      // the warps w with w % MT == r / RW; their states are weighted by
+      // exp2(m_w - M) / L so that the elements below only multiply-add
+      if (ctid < vrows) {
+        const int r = ctid, w0 = r / RW, lr = r % RW;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.red_m[w][r]);
-        float Lsum = 0.f, O = 0.f;
-        if (M != -INFINITY) {
+        for (int w = w0; w < kConsumerWarps; w += MT)
+          M = fmaxf(M, sm.red_m[w][lr]);
+        float Lsum = 0.f;
+        float f[kConsumerWarps];
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = sm.red_m[w][r];
-            if (mw == -INFINITY) continue;
-            const float f = ex2(mw - M);
-            Lsum = fmaf(f, sm.red_l[w][r], Lsum);
-            O = fmaf(f, sm.red_o[w][r][d], O);
-          }
+        for (int w = w0, k = 0; w < kConsumerWarps; w += MT, ++k) {
+          const float mw = sm.red_m[w][lr];
+          f[k] = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+          Lsum = fmaf(f[k], sm.red_l[w][lr], Lsum);
         }
-        const float on = Lsum > 0.f ? O / Lsum : 0.f;
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+        for (int w = w0, k = 0; w < kConsumerWarps; w += MT, ++k)
+          sm.wf[w][r] = f[k] * inv;
         const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : -INFINITY;
+        const int gr = rg * RB + r;
         if (single) {
           const int i = gr / p.group;
           const int h = g * p.group + gr % p.group;
-          const size_t row = ((size_t)b * p.q_len + i) * p.num_q_heads + h;
-          store_out(static_cast<T *>(p.out) + row * D + d, on);
-          if (d == 0) p.lse[row] = lse2 * kLn2;
+          p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
+        } else {
+          p.part_lse[((size_t)grp * p.max_splits + ui.split) * RB + r] = lse2;
+        }
+      }
+      if (!epi_sync(sm, epi_phase, lane)) {
+        if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
+        break;
+      }
+      for (int e4 = ctid; e4 < vrows * (D / 4); e4 += kConsumerWarps * 32) {
+        const int r = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
+        const int w0 = r / RW, lr = r % RW;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = w0; w < kConsumerWarps; w += MT) {
+          const float f = sm.wf[w][r];
+          const float4 v = *reinterpret_cast<const float4 *>(&sm.red_o[w][lr][d]);
+          a.x = fmaf(f, v.x, a.x);
+          a.y = fmaf(f, v.y, a.y);
+          a.z = fmaf(f, v.z, a.z);
+          a.w = fmaf(f, v.w, a.w);
+        }
+        const int gr = rg * RB + r;
+        if (single) {
+          const int i = gr / p.group;
+          const int h = g * p.group + gr % p.group;
+          T *dst = static_cast<T *>(p.out) +
+                   (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D + d;
+          store_out(dst + 0, a.x);
+          store_out(dst + 1, a.y);
+          store_out(dst + 2, a.z);
+          store_out(dst + 3, a.w);
         } else {
           const size_t prow = ((size_t)grp * p.max_splits + ui.split) * RB + r;
-          p.part_o[prow * D + d] = on;
-          if (d == 0) p.part_lse[prow] = lse2;
+          *reinterpret_cast<float4 *>(p.part_o + prow * D + d) = a;
         }
       }
       if (!single) {
@@ -887,8 +955,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           __threadfence();
           const int ns = ui.n_splits;
           const size_t base = (size_t)grp * p.max_splits;
+          const int vrows = min(RB, p.rows - rg * RB);  // valid rows here
           // per-row max and weight sum over the splits (warp w: rows w, w+4..)
-          for (int r = warp; r < RB; r += kConsumerWarps) {
+          for (int r = warp; r < vrows; r += kConsumerWarps) {
             float M = -INFINITY;
             for (int s = lane; s < ns; s += 32)
               M = fmaxf(M, __ldcg(p.part_lse + (base + s) * RB + r));
@@ -908,23 +977,69 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
             break;
           }
-          for (int e = ctid; e < RB * D; e += kConsumerWarps * 32) {
-            const int r = e / D, d = e % D;
-            const int gr = rg * RB + r;
-            if (gr >= p.rows) continue;
-            const float M = sm.row_m[r], W = sm.row_w[r];
-            float acc = 0.f;
-            for (int s = 0; s < ns; ++s) {
+          // normalised split weights go to shared memory (red_o is free now),
+          // CH splits at a time; each thread then sums float4 slices of the
+          // partial outputs with independent loads.
+          constexpr int CH = kConsumerWarps * RW * D / RB;  // splits per chunk
+          constexpr int NE4 = RB * D / 4;          // float4 slices per unit
+          constexpr int EPT = (NE4 + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+          float *wts = &sm.red_o[0][0][0];
+          const float4 *po4 = reinterpret_cast<const float4 *>(p.part_o);
+          float4 acc[EPT];
+#pragma unroll
+          for (int k = 0; k < EPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          bool merged = true;
+          for (int s0 = 0; s0 < ns; s0 += CH) {
+            const int cn = min(CH, ns - s0);
+            // (branch free: an empty split has lse2 = -inf and weight 0)
+#pragma unroll 4
+            for (int idx = ctid; idx < cn * RB; idx += kConsumerWarps * 32) {
+              const int s = s0 + idx / RB, r = idx % RB;
               const float ls = __ldcg(p.part_lse + (base + s) * RB + r);
-              if (ls == -INFINITY) continue;
-              acc = fmaf(ex2(ls - M),
-                         __ldcg(p.part_o + ((base + s) * RB + r) * D + d), acc);
+              const float w = ex2(ls - sm.row_m[r]) / sm.row_w[r];
+              wts[idx] = r < vrows ? w : 0.f;
             }
+            if (!epi_sync(sm, epi_phase, lane)) { merged = false; break; }
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+              const int e4 = ctid + k * kConsumerWarps * 32;
+              if (e4 >= vrows * (D / 4)) continue;
+              const int r = e4 / (D / 4), d4 = e4 % (D / 4);
+              const float4 *src = po4 + ((base + s0) * RB + r) * (D / 4) + d4;
+              float4 a = acc[k];
+#pragma unroll 8
+              for (int s = 0; s < cn; ++s) {
+                const float w = wts[s * RB + r];
+                const float4 v = __ldcg(src + (size_t)s * RB * (D / 4));
+                a.x = fmaf(w, v.x, a.x);
+                a.y = fmaf(w, v.y, a.y);
+                a.z = fmaf(w, v.z, a.z);
+                a.w = fmaf(w, v.w, a.w);
+              }
+              acc[k] = a;
+            }
+            if (!epi_sync(sm, epi_phase, lane)) { merged = false; break; }
+          }
+          if (!merged) {
+            if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
+            break;
+          }
+#pragma unroll
+          for (int k = 0; k < EPT; ++k) {
+            const int e4 = ctid + k * kConsumerWarps * 32;
+            if (e4 >= vrows * (D / 4)) continue;
+            const int r = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
+            const int gr = rg * RB + r;
             const int i = gr / p.group;
             const int h = g * p.group + gr % p.group;
             const size_t row = ((size_t)b * p.q_len + i) * p.num_q_heads + h;
-            store_out(static_cast<T *>(p.out) + row * D + d, W > 0.f ? acc / W : 0.f);
-            if (d == 0) p.lse[row] = (M + log2f(W)) * kLn2;
+            T *dst = static_cast<T *>(p.out) + row * D + d;
+            store_out(dst + 0, acc[k].x);
+            store_out(dst + 1, acc[k].y);
+            store_out(dst + 2, acc[k].z);
+            store_out(dst + 3, acc[k].w);
+            if (d == 0)
+              p.lse[row] = (sm.row_m[r] + log2f(sm.row_w[r])) * kLn2;
           }
           if (ctid == 0) p.tickets[grp] = 0;
         }
@@ -1003,7 +1118,7 @@ static size_t batch_bucket(int batch) { return (size_t)(batch + 255) / 256 * 256
 
 template <typename T, int D, int RB, bool MMA>
 static int prepare_t(int batch) {
-  const size_t smem = smem_bytes<T, D, RB>((int)batch_bucket(batch));
+  const size_t smem = smem_bytes<T, D, RB, MMA>((int)batch_bucket(batch));
   auto kern = paged_attention_kernel<T, D, RB, MMA>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -1029,7 +1144,7 @@ static int prepare_t(int batch) {
 template <typename T, int D, int RB, bool MMA>
 static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
   if (prepare_t<T, D, RB, MMA>(p.batch) < 0) return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes<T, D, RB>((int)batch_bucket(p.batch));
+  const size_t smem = smem_bytes<T, D, RB, MMA>((int)batch_bucket(p.batch));
   TensorMaps tm;
   memset(&tm, 0, sizeof tm);
   if constexpr (MMA) {
@@ -1044,8 +1159,13 @@ static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
 #define SVP_DISPATCH(DTYPE, HD, RB, MMA, CALL)                        \
   do {                                                                \
     if (MMA) {                                                        \
-      if (HD == 64) CALL(uint16_t, 64, 16, true);                     \
-      else CALL(uint16_t, 128, 16, true);                             \
+      if (HD == 64) {                                                 \
+        if (RB == 16) CALL(uint16_t, 64, 16, true);                   \
+        else CALL(uint16_t, 64, 32, true);                            \
+      } else {                                                        \
+        if (RB == 16) CALL(uint16_t, 128, 16, true);                  \
+        else CALL(uint16_t, 128, 32, true);                           \
+      }                                                               \
     } else if (DTYPE == 0) {                                          \
       if (HD == 64) {                                                 \
         switch (RB) { case 1: CALL(float, 64, 1, false); break;       \
