@@ -81,7 +81,7 @@ typedef struct {
   int dtype;              /* svp_dtype of q, out and both caches           */
   void *workspace;        /* device scratch for split partials, or NULL    */
   size_t workspace_bytes; /* size of `workspace`                           */
-  int split_pages;        /* pages per split-K unit; 0 = automatic         */
+  int split_pages;        /* fewest pages per CTA slice; 0 = automatic (8) */
   int kernel_path;        /* svp_kernel_path; SVP_PATH_AUTO by default     */
 } svp_dims;
 
@@ -113,11 +113,17 @@ typedef enum {
  *   counts from position 0; window counts the query's own key.  Only pages
  *   holding visible keys are read; other block_table entries are not read.
  * q_len: 1 (decode) .. 16 (verify of q_len-1 drafts + bonus position).
- * Work is split along the key axis into units of dims->split_pages pages;
- * partial results are merged by log-sum-exp inside the same launch.
+ * Work: every CTA of one persistent launch takes an equal slice of all
+ * visible pages of all (sequence, kv head) groups (at least
+ * dims->split_pages pages each); a group that spans several slices is
+ * finished by merging their partial results by log-sum-exp inside the same
+ * launch.
  * Workspace: paged_decode_workspace_size() bytes, passed in dims; it needs
- * no initialisation (each call clears the few KB of counters it uses with
- * one cudaMemsetAsync on `stream`, then launches one kernel).  With
+ * no initialisation: split arrivals are counted in 64-bit tickets tagged
+ * with a per-call number, so whatever a ticket holds from earlier calls
+ * counts as zero (a call with more than 65536 sequence x kv-head groups
+ * also clears its tickets with one cudaMemsetAsync).  One kernel launch per
+ * 4096 sequences.  With
  * dims->workspace == NULL the library uses a buffer of its own per device,
  * (re)allocated inside the call when it is too small -- that first call is
  * then not capturable in a CUDA graph.  Calls that share a workspace must
@@ -161,8 +167,9 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
  *     call clears the counters it relies on before launching, so calls in
  *     sequence on one stream are independent.  Calls that overlap on the
  *     GPU (other streams, other host threads) race on the array.
- *   - With dims->split_pages == 0 the automatic split size is enlarged (up
- *     to 128 pages) when the default plan would not fit the array.
+ *   - With dims->split_pages == 0 the automatic slice size is enlarged (64,
+ *     then 128 pages per CTA: fewer partial slots) when the default plan
+ *     would not fit the array.
  * Errors: those of paged_decode_attention, plus SVP_ERR_WORKSPACE when the
  * scratch this request needs exceeds SVP_STATIC_SCRATCH_BYTES (use fewer
  * sequences per call or longer splits). */

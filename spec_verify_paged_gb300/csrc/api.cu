@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libsvp.so: argument checks, split planning,
 // workspace handling and kernel launches.  Declarations and the full
 // contract of every entry point are in include/svp.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -13,6 +14,7 @@
 namespace svp {
 
 static thread_local int t_last_launches = 0;
+static std::atomic<unsigned int> g_epoch{0};  // per-call ticket tags
 
 // ---- per-device facts, queried once ----
 struct DeviceInfo {
@@ -113,43 +115,47 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   int rb = mma ? (rows <= 16 ? 16 : 32)
                : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
   const int n_rg = (rows + rb - 1) / rb;
-  const int mvp = max_visible_pages(max_blocks, q_len, n_sink, window);
   const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);
-  const long long slots = (long long)num_sms * ctas;
   const long long groups = (long long)batch * num_kv_heads * n_rg;
-  int pps = split_pages;
-  if (pps <= 0) {
-    // aim for ~8 units per CTA slot at the worst-case lengths
-    const long long bound = groups * (long long)(mvp > 0 ? mvp : 1);
-    const long long want = bound / (slots * 8 > 0 ? slots * 8 : 1);
-    pps = 8;
-    while (pps < 64 && pps * 2 <= want) pps *= 2;
-    // keep the final log-sum-exp merge cheap: at most 64 splits per sequence
-    while (pps < 128 && (mvp + pps - 1) / pps > 64) pps *= 2;
-  }
-  if (pps > 128) pps = 128;
-  const int max_splits = mvp > 0 ? (mvp + pps - 1) / pps : 1;
-  const long long units_bound = groups * max_splits;
-  long long grid = slots;
-  if (grid > units_bound) grid = units_bound;
+  // Every CTA of the persistent grid takes an equal slice of all pages;
+  // a slice holds at least min_pages pages (fewer CTAs for small calls).
+  int min_pages = split_pages > 0 ? split_pages : 8;
+  long long grid = (long long)num_sms * ctas;
+  const long long page_bound =
+      groups * (long long)max_visible_pages(max_blocks, q_len, n_sink, window);
+  if (grid > page_bound / min_pages) grid = page_bound / min_pages;
   if (grid < 1) grid = 1;
   plan->rb = rb;
   plan->n_rg = n_rg;
   plan->mma = mma;
-  plan->split_pages = pps;
-  plan->max_splits = max_splits;
+  plan->min_pages = min_pages;
   plan->grid = (int)grid;
   plan->ctas_per_sm = ctas;
-  plan->ws_counters = 256;
-  plan->ws_tickets = align256((size_t)groups * sizeof(int));
-  plan->ws_part_o = align256((size_t)groups * max_splits * rb * head_dim * 4);
-  plan->ws_part_lse = align256((size_t)groups * max_splits * rb * 4);
+  plan->ws_head = 256;
+  plan->clear_tickets = groups > kTicketCap;
+  plan->ws_tickets = (size_t)(groups > kTicketCap ? groups : kTicketCap) * 8;
+  plan->ws_part_o = align256((size_t)2 * grid * rb * head_dim * 4);
+  plan->ws_part_lse = align256((size_t)2 * grid * rb * 4);
   plan->ws_total =
-      plan->ws_counters + plan->ws_tickets + plan->ws_part_o + plan->ws_part_lse;
+      plan->ws_head + plan->ws_tickets + plan->ws_part_o + plan->ws_part_lse;
   return SVP_OK;
 }
 
 constexpr int kBatchPerLaunch = 4096;
+
+// Sequences per launch: at most 4096 (the in-kernel prefix lives in shared
+// memory) and few enough that the flattened page count fits in 32 bits.
+static int batch_per_launch(const svp_dims *d, int q_len, int n_sink,
+                            int window) {
+  const long long rows = (long long)(d->num_q_heads / d->num_kv_heads) * q_len;
+  const long long per_seq =
+      (long long)d->num_kv_heads * rows *
+      max_visible_pages(d->max_blocks_per_seq, q_len, n_sink, window);
+  long long bl = per_seq > 0 ? ((1LL << 31) - 1) / per_seq : kBatchPerLaunch;
+  if (bl > kBatchPerLaunch) bl = kBatchPerLaunch;
+  if (bl > d->batch) bl = d->batch;
+  return bl < 1 ? 1 : (int)bl;
+}
 
 }  // namespace svp
 
@@ -186,8 +192,8 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len, int n_sink,
     return 0;
   const int sms = device_sms();
   AttnPlan plan;
-  const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
-  if (plan_attention(bl > 0 ? bl : 1, dims->num_q_heads, dims->num_kv_heads,
+  const int bl = batch_per_launch(dims, q_len, n_sink, window);
+  if (plan_attention(bl, dims->num_q_heads, dims->num_kv_heads,
                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
                      q_len, n_sink, window, dims->split_pages,
                      dims->kernel_path, sms > 0 ? sms : 1, dims->num_blocks,
@@ -216,7 +222,7 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
   const int sms = device_sms();
   if (sms <= 0) return SVP_ERR_CUDA;
 
-  const int bl = dims->batch < kBatchPerLaunch ? dims->batch : kBatchPerLaunch;
+  const int bl = batch_per_launch(dims, q_len, n_sink, window);
   AttnPlan plan;
   st = plan_attention(bl, dims->num_q_heads, dims->num_kv_heads,
                       dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
@@ -231,18 +237,20 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     if (st != SVP_OK) return st;
   }
   char *wp = static_cast<char *>(ws);
-  // The workspace layout depends on the call's shape, so an earlier call
-  // may have left split partials where this call keeps its counters and
-  // tickets: clear that (small) region on the stream first.
-  if (cudaMemsetAsync(wp, 0, plan.ws_counters + plan.ws_tickets, stream) !=
-      cudaSuccess)
+  // Ticket arrivals carry this call's epoch, so stale tickets need no reset.
+  // Only a call with more groups than the fixed ticket region clears its
+  // (larger) region, which other shapes' partials may have overwritten.
+  if (plan.clear_tickets &&
+      cudaMemsetAsync(wp + plan.ws_head, 0, plan.ws_tickets, stream) !=
+          cudaSuccess)
     return SVP_ERR_CUDA;
+  unsigned int epoch = g_epoch.fetch_add(1) + 1;
+  if (epoch == 0) epoch = g_epoch.fetch_add(1) + 1;
   const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
   const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
   int launches = 0;
-  for (int b0 = 0; b0 < dims->batch; b0 += kBatchPerLaunch) {
-    const int nb = dims->batch - b0 < kBatchPerLaunch ? dims->batch - b0
-                                                      : kBatchPerLaunch;
+  for (int b0 = 0; b0 < dims->batch; b0 += bl) {
+    const int nb = dims->batch - b0 < bl ? dims->batch - b0 : bl;
     AttnParams p;
     p.q = static_cast<const char *>(q) + (size_t)b0 * q_len * row_elems * eb;
     p.k_cache = k_cache;
@@ -251,10 +259,10 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.seq_lens = seq_lens + b0;
     p.out = static_cast<char *>(out) + (size_t)b0 * q_len * row_elems * eb;
     p.lse = lse + (size_t)b0 * q_len * dims->num_q_heads;
-    p.counters = reinterpret_cast<int *>(wp);
-    p.tickets = reinterpret_cast<int *>(wp + plan.ws_counters);
-    p.part_o = reinterpret_cast<float *>(wp + plan.ws_counters + plan.ws_tickets);
-    p.part_lse = reinterpret_cast<float *>(wp + plan.ws_counters +
+    p.tickets = reinterpret_cast<unsigned long long *>(wp + plan.ws_head);
+    p.epoch = epoch;
+    p.part_o = reinterpret_cast<float *>(wp + plan.ws_head + plan.ws_tickets);
+    p.part_lse = reinterpret_cast<float *>(wp + plan.ws_head +
                                            plan.ws_tickets + plan.ws_part_o);
     p.batch = nb;
     p.num_q_heads = dims->num_q_heads;
@@ -269,14 +277,13 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.rows = p.group * q_len;
     p.rb = plan.rb;
     p.n_rg = plan.n_rg;
-    p.split_pages = plan.split_pages;
-    p.max_splits = plan.max_splits;
+    p.min_pages = plan.min_pages;
     p.qscale = scale * 1.4426950408889634f;
     AttnPlan sub = plan;
     if (nb != bl) {
       plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
-                     q_len, n_sink, window, plan.split_pages,
+                     q_len, n_sink, window, plan.min_pages,
                      plan.mma ? SVP_PATH_TENSOR_CORES : SVP_PATH_CUDA_CORES,
                      sms, dims->num_blocks, &sub);
     }

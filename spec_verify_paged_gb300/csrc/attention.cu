@@ -62,16 +62,20 @@ static __device__ unsigned int g_status_attn;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kUnitRing = 4;
-constexpr int kMaxSplitPages = 128;  // 4 block-table entries per producer lane
+constexpr int kTableChunk = 128;     // block-table entries loaded per round
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBoxElems = 64;        // 128-byte swizzle box: 64 bf16 columns
 constexpr int kBoxBytes = kBlockSize * 128;
 
+// One segment of a CTA's slice: pages [page0, page0 + n_pages) of group
+// (b, g, rg).  CTAs f..l own the group's pages; `slot` says whether this is
+// the CTA's first (0) or last (1) segment, which is where its partial goes.
 struct UnitInfo {
-  int b, g, rg, split;
-  int n_splits, page0, n_pages, seq_len;
-  int n_a, b_start, valid, pad;
+  int b, g, rg, slot;
+  int f, l, gstart, page0;
+  int n_pages, seq_len, n_a, b_start;
+  int valid, pad0, pad1, pad2;
 };
 
 struct TensorMaps {
@@ -173,7 +177,8 @@ struct Smem {
   uint64_t epi;                                    // consumer-only barrier
   int abort_flag;
   int is_last;
-  int total_units;
+  int total_pages;                                 // flattened pages
+  int n_ctas;                                      // CTAs sharing them
   int prefix[1];                                   // [batch + 1], dynamic
 };
 
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int B = p.batch;
-  const int units_per_split = p.num_kv_heads * p.n_rg;
+  const int groups_per_seq = p.num_kv_heads * p.n_rg;
 
   // ---- set-up: barriers and the per-sequence unit prefix ----
   if (tid == 0) {
@@ -532,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_mbar_init();
   }
   if (warp == 0) {
+    // pages of every sequence, times its groups (kv heads x row groups)
     int run = 0;
     if (lane == 0) sm.prefix[0] = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
@@ -544,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
           int na, bs, np;
           visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
-          n = (np + p.split_pages - 1) / p.split_pages * units_per_split;
+          n = np * groups_per_seq;
         }
       }
       int incl = n;
@@ -556,118 +562,135 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (b < B) sm.prefix[b + 1] = run + incl;
       run += __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 0) sm.total_units = run;
+    if (lane == 0) {
+      sm.total_pages = run;
+      // CTAs that share the pages: at least min_pages each
+      long long ce = run / (p.min_pages > 0 ? p.min_pages : 1);
+      if (ce > (long long)gridDim.x) ce = gridDim.x;
+      if (ce < 1) ce = 1;
+      sm.n_ctas = (int)ce;
+    }
   }
   __syncthreads();
-  const int total_units = sm.total_units;
+  const int total_pages = sm.total_pages;
+  const int n_ctas = sm.n_ctas;
+  // this CTA's slice of the flattened (sequence, group, page) space
+  const int range_begin =
+      blockIdx.x < n_ctas ? (int)((long long)blockIdx.x * total_pages / n_ctas)
+                          : total_pages;
+  const int range_end =
+      blockIdx.x < n_ctas
+          ? (int)((long long)(blockIdx.x + 1) * total_pages / n_ctas)
+          : total_pages;
 
   if (warp == kConsumerWarps) {
     // ======================= producer warp =======================
     int c = 0;   // pages issued so far
-    int us = 0;  // units taken so far
+    int us = 0;  // segments published so far
     bool ok = true;
-    int u = 0;
-    if (lane == 0) u = atomicAdd(&p.counters[0], 1);
-    u = __shfl_sync(kFull, u, 0);
+    int pos = range_begin;
     while (true) {
-      // claim the next unit now; its latency hides behind this unit's work
-      int u_next = 0;
-      if (lane == 0 && u < total_units) u_next = atomicAdd(&p.counters[0], 1);
       const int slot = us % kUnitRing;
       if (lane == 0)
         ok = mbar_wait(&sm.uempty[slot], ((us / kUnitRing) & 1) ^ 1);
       ok = __shfl_sync(kFull, ok, 0) && !sm.abort_flag;
       if (!ok) break;
-      if (u >= total_units) {
+      if (pos >= range_end) {
         if (lane == 0) {
           sm.unit[slot].valid = 0;
           mbar_arrive(&sm.ufull[slot]);
         }
         break;
       }
-      // decode unit u -> (b, g, split, rg): binary search in the prefix
-      int lo = 0, hi = B;  // find b with prefix[b] <= u < prefix[b+1]
+      // decode pos -> (b, group, page): binary search in the prefix
+      int lo = 0, hi = B;  // find b with prefix[b] <= pos < prefix[b+1]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (sm.prefix[mid] <= u) lo = mid; else hi = mid;
+        if (sm.prefix[mid] <= pos) lo = mid; else hi = mid;
       }
       const int b = lo;
-      const int ub = u - sm.prefix[b];
-      const int n_units_b = sm.prefix[b + 1] - sm.prefix[b];
-      const int n_splits = n_units_b / units_per_split;
-      const int rg = ub % p.n_rg;
-      const int t2 = ub / p.n_rg;
-      const int split = t2 % n_splits;
-      const int g = t2 / n_splits;
+      const int np = (sm.prefix[b + 1] - sm.prefix[b]) / groups_per_seq;
+      const int qoff = pos - sm.prefix[b];
+      const int gi = qoff / np;              // group within the sequence
+      const int page0 = qoff - gi * np;      // first page of this segment
+      const int g = gi / p.n_rg, rg = gi - g * p.n_rg;
+      const int n_pages = min(range_end - pos, np - page0);
+      const int gstart = pos - page0;        // the group's first flat page
+      // CTAs that own the group's first and last pages
+      const int f = (int)(((long long)(gstart + 1) * n_ctas - 1) / total_pages);
+      const int l = (int)(((long long)(gstart + np) * n_ctas - 1) / total_pages);
       const int L = __ldg(p.seq_lens + b);
-      int na, bs, np;
-      visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
-      const int page0 = split * p.split_pages;
-      const int n_pages = min(p.split_pages, np - page0);
-      // block-table entries of this unit's pages, one coalesced load each
-      int phys[kMaxSplitPages / 32];
-#pragma unroll
-      for (int k4 = 0; k4 < kMaxSplitPages / 32; ++k4) {
-        const int k = k4 * 32 + lane;
-        phys[k4] = -1;
-        if (k < n_pages) {
-          const int pidx = page0 + k;
-          const int lb = (pidx < na) ? pidx : bs + (pidx - na);
-          phys[k4] = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
-        }
-      }
+      int na, bs, np2;
+      visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np2);
       if (lane == 0) {
         UnitInfo &ui = sm.unit[slot];
-        ui.b = b; ui.g = g; ui.rg = rg; ui.split = split;
-        ui.n_splits = n_splits; ui.page0 = page0; ui.n_pages = n_pages;
+        ui.b = b; ui.g = g; ui.rg = rg;
+        ui.slot = (pos == range_begin) ? 0 : 1;  // first or last segment
+        ui.f = f; ui.l = l; ui.gstart = gstart;
+        ui.page0 = page0; ui.n_pages = n_pages;
         ui.seq_len = L; ui.n_a = na; ui.b_start = bs; ui.valid = 1;
         mbar_arrive(&sm.ufull[slot]);
       }
+      const size_t head_off = (size_t)g * C::PAGE_ELEMS;
+      for (int k0 = 0; k0 < n_pages && ok; k0 += kTableChunk) {
+        // block-table entries of the next chunk, one coalesced load each
+        int phys[kTableChunk / 32];
 #pragma unroll
-      for (int k4 = 0; k4 < kMaxSplitPages / 32; ++k4) {
-        for (int kk = 0; kk < 32; ++kk) {
-          const int k = k4 * 32 + kk;
-          if (k >= n_pages) break;
-          const int ph = __shfl_sync(kFull, phys[k4], kk);
-          if (lane == 0) {
-            const int s = c % STAGES;
-            if (!mbar_wait(&sm.empty[s], ((c / STAGES) & 1) ^ 1)) {
-              ok = false;
-            } else if (ph < 0 || ph >= p.num_blocks) {
-              raise_flag(SVP_DEV_BAD_BLOCK_ID);
-              sm.stage_ok[s] = 0;
-              mbar_arrive(&sm.full[s]);
-            } else {
-              sm.stage_ok[s] = 1;
-              mbar_arrive_expect_tx(&sm.full[s], 2 * C::PAGE_BYTES);
-              if constexpr (MMA) {
-                const int y = (ph * p.num_kv_heads + g) * kBlockSize;
+        for (int k4 = 0; k4 < kTableChunk / 32; ++k4) {
+          const int k = k0 + k4 * 32 + lane;
+          phys[k4] = -1;
+          if (k < n_pages) {
+            const int pidx = page0 + k;
+            const int lb = (pidx < na) ? pidx : bs + (pidx - na);
+            phys[k4] = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
+          }
+        }
 #pragma unroll
-                for (int bx = 0; bx < D / kBoxElems; ++bx) {
-                  tma_load_2d(sm.kv[s][0] + bx * kBoxBytes, &tm.k,
-                              bx * kBoxElems, y, &sm.full[s]);
-                  tma_load_2d(sm.kv[s][1] + bx * kBoxBytes, &tm.v,
-                              bx * kBoxElems, y, &sm.full[s]);
-                }
+        for (int k4 = 0; k4 < kTableChunk / 32; ++k4) {
+          for (int kk = 0; kk < 32; ++kk) {
+            const int k = k0 + k4 * 32 + kk;
+            if (k >= n_pages) break;
+            const int ph = __shfl_sync(kFull, phys[k4], kk);
+            if (lane == 0) {
+              const int s = c % STAGES;
+              if (!mbar_wait(&sm.empty[s], ((c / STAGES) & 1) ^ 1)) {
+                ok = false;
+              } else if (ph < 0 || ph >= p.num_blocks) {
+                raise_flag(SVP_DEV_BAD_BLOCK_ID);
+                sm.stage_ok[s] = 0;
+                mbar_arrive(&sm.full[s]);
               } else {
-                const size_t off =
-                    ((size_t)ph * p.num_kv_heads + g) * C::PAGE_ELEMS;
-                bulk_g2s(sm.kv[s][0], static_cast<const T *>(p.k_cache) + off,
-                         C::PAGE_BYTES, &sm.full[s]);
-                bulk_g2s(sm.kv[s][1], static_cast<const T *>(p.v_cache) + off,
-                         C::PAGE_BYTES, &sm.full[s]);
+                sm.stage_ok[s] = 1;
+                mbar_arrive_expect_tx(&sm.full[s], 2 * C::PAGE_BYTES);
+                if constexpr (MMA) {
+                  const int y = (ph * p.num_kv_heads + g) * kBlockSize;
+#pragma unroll
+                  for (int bx = 0; bx < D / kBoxElems; ++bx) {
+                    tma_load_2d(sm.kv[s][0] + bx * kBoxBytes, &tm.k,
+                                bx * kBoxElems, y, &sm.full[s]);
+                    tma_load_2d(sm.kv[s][1] + bx * kBoxBytes, &tm.v,
+                                bx * kBoxElems, y, &sm.full[s]);
+                  }
+                } else {
+                  const size_t off = (size_t)ph * p.num_kv_heads * C::PAGE_ELEMS +
+                                     head_off;
+                  bulk_g2s(sm.kv[s][0], static_cast<const T *>(p.k_cache) + off,
+                           C::PAGE_BYTES, &sm.full[s]);
+                  bulk_g2s(sm.kv[s][1], static_cast<const T *>(p.v_cache) + off,
+                           C::PAGE_BYTES, &sm.full[s]);
+                }
               }
             }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) break;
+            ++c;
           }
-          ok = __shfl_sync(kFull, ok, 0);
           if (!ok) break;
-          ++c;
         }
-        if (!ok) break;
       }
       if (!ok) break;
+      pos += n_pages;
       ++us;
-      u = __shfl_sync(kFull, u_next, 0);
     }
     if (!ok) {
       // give up: flag it, then wait (bounded) for copies still in flight
@@ -718,25 +741,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         float o[D / 8][4];
         float m[2] = {-INFINITY, -INFINITY}, lp[2] = {0.f, 0.f};
         int t[2] = {-1, -1};
-        const uint16_t *qrow[2] = {nullptr, nullptr};
+        // Q fragments straight from global memory: rows past the unit's
+        // last row read row 0 of the group and are masked to zero, so all
+        // loads are unconditional and issue back to back.
+        const uint32_t *qrow[2];
+        uint32_t qmask[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int gr = rg * RB + mt * 16 + gq + 8 * r;
-          if (gr < p.rows) {
-            const int i = gr / p.group;
-            const int h = g * p.group + gr % p.group;
-            qrow[r] = static_cast<const uint16_t *>(p.q) +
-                      (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D;
-            t[r] = t0 + i;
-          }
+          const bool valid = gr < p.rows;
+          const int grc = valid ? gr : 0;
+          const int i = grc / p.group;
+          const int h = g * p.group + grc % p.group;
+          qrow[r] = reinterpret_cast<const uint32_t *>(
+              static_cast<const uint16_t *>(p.q) +
+              (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D);
+          qmask[r] = valid ? 0xffffffffu : 0u;
+          t[r] = valid ? t0 + i : -1;
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int d0 = ks * 16 + 2 * tq;
-          qa[ks][0] = qrow[0] ? *reinterpret_cast<const uint32_t *>(qrow[0] + d0) : 0u;
-          qa[ks][1] = qrow[1] ? *reinterpret_cast<const uint32_t *>(qrow[1] + d0) : 0u;
-          qa[ks][2] = qrow[0] ? *reinterpret_cast<const uint32_t *>(qrow[0] + d0 + 8) : 0u;
-          qa[ks][3] = qrow[1] ? *reinterpret_cast<const uint32_t *>(qrow[1] + d0 + 8) : 0u;
+          const int w0 = ks * 8 + tq;  // 32-bit word of columns 16ks+2tq, +1
+          qa[ks][0] = __ldg(qrow[0] + w0);
+          qa[ks][1] = __ldg(qrow[1] + w0);
+          qa[ks][2] = __ldg(qrow[0] + w0 + 4);
+          qa[ks][3] = __ldg(qrow[1] + w0 + 4);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qa[ks][0] &= qmask[0];
+          qa[ks][1] &= qmask[1];
+          qa[ks][2] &= qmask[0];
+          qa[ks][3] &= qmask[1];
         }
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn)
@@ -872,7 +908,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       const int grp = (b * p.num_kv_heads + g) * p.n_rg + rg;
-      const bool single = ui.n_splits == 1;
+      // a group owned by one CTA is finished here; else a partial goes to
+      // this CTA's first- or last-segment slot
+      const bool single = ui.f == ui.l;
+      const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
       const int vrows = min(RB, p.rows - rg * RB);  // valid rows of the unit
       // per-row statistics, once per row: row r lives in local row lr of
       // the warps w with w % MT == r / RW; their states are weighted by
@@ -902,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int h = g * p.group + gr % p.group;
           p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
         } else {
-          p.part_lse[((size_t)grp * p.max_splits + ui.split) * RB + r] = lse2;
+          p.part_lse[pslot * RB + r] = lse2;
         }
       }
       if (!epi_sync(sm, epi_phase, lane)) {
@@ -933,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           store_out(dst + 2, a.z);
           store_out(dst + 3, a.w);
         } else {
-          const size_t prow = ((size_t)grp * p.max_splits + ui.split) * RB + r;
+          const size_t prow = pslot * RB + r;
           *reinterpret_cast<float4 *>(p.part_o + prow * D + d) = a;
         }
       }
@@ -944,8 +983,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         if (ctid == 0) {
-          const int ticket = atomicAdd(&p.tickets[grp], 1);
-          sm.is_last = (ticket == ui.n_splits - 1);
+          // arrivals of this call are tagged with its epoch in the high word;
+          // a ticket left by another call (or never written) counts as zero
+          unsigned long long *tk = p.tickets + grp;
+          unsigned long long seen = __ldcg(tk), want;
+          unsigned int before;
+          while (true) {
+            before = (unsigned int)(seen >> 32) == p.epoch ? (unsigned int)seen : 0u;
+            want = ((unsigned long long)p.epoch << 32) | (before + 1u);
+            const unsigned long long got = atomicCAS(tk, seen, want);
+            if (got == seen) break;
+            seen = got;
+          }
+          sm.is_last = (before == (unsigned int)(ui.l - ui.f));
         }
         if (!epi_sync(sm, epi_phase, lane)) {
           if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
@@ -953,21 +1003,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (sm.is_last) {
           __threadfence();
-          const int ns = ui.n_splits;
-          const size_t base = (size_t)grp * p.max_splits;
+          // contributors are CTAs f..l in order; CTA f's partial sits in its
+          // last-segment slot when its slice began before this group
+          const int ns = ui.l - ui.f + 1;
+          const int f_begin = (int)((long long)ui.f * total_pages / n_ctas);
+          const int f_tail = f_begin < ui.gstart ? 1 : 0;
+          auto prow_of = [&](int sidx) -> size_t {
+            return (size_t)(2 * (ui.f + sidx) + (sidx == 0 ? f_tail : 0));
+          };
           const int vrows = min(RB, p.rows - rg * RB);  // valid rows here
           // per-row max and weight sum over the splits (warp w: rows w, w+4..)
           for (int r = warp; r < vrows; r += kConsumerWarps) {
             float M = -INFINITY;
             for (int s = lane; s < ns; s += 32)
-              M = fmaxf(M, __ldcg(p.part_lse + (base + s) * RB + r));
+              M = fmaxf(M, __ldcg(p.part_lse + prow_of(s) * RB + r));
 #pragma unroll
             for (int off = 16; off; off >>= 1)
               M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
             float W = 0.f;
             if (M != -INFINITY)
               for (int s = lane; s < ns; s += 32)
-                W += ex2(__ldcg(p.part_lse + (base + s) * RB + r) - M);
+                W += ex2(__ldcg(p.part_lse + prow_of(s) * RB + r) - M);
 #pragma unroll
             for (int off = 16; off; off >>= 1)
               W += __shfl_xor_sync(kFull, W, off);
@@ -995,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 4
             for (int idx = ctid; idx < cn * RB; idx += kConsumerWarps * 32) {
               const int s = s0 + idx / RB, r = idx % RB;
-              const float ls = __ldcg(p.part_lse + (base + s) * RB + r);
+              const float ls = __ldcg(p.part_lse + prow_of(s) * RB + r);
               const float w = ex2(ls - sm.row_m[r]) / sm.row_w[r];
               wts[idx] = r < vrows ? w : 0.f;
             }
@@ -1005,12 +1061,11 @@ __global__ void __launch_bounds__(kThreads, 2)
               const int e4 = ctid + k * kConsumerWarps * 32;
               if (e4 >= vrows * (D / 4)) continue;
               const int r = e4 / (D / 4), d4 = e4 % (D / 4);
-              const float4 *src = po4 + ((base + s0) * RB + r) * (D / 4) + d4;
               float4 a = acc[k];
 #pragma unroll 8
               for (int s = 0; s < cn; ++s) {
                 const float w = wts[s * RB + r];
-                const float4 v = __ldcg(src + (size_t)s * RB * (D / 4));
+                const float4 v = __ldcg(po4 + (prow_of(s0 + s) * RB + r) * (D / 4) + d4);
                 a.x = fmaf(w, v.x, a.x);
                 a.y = fmaf(w, v.y, a.y);
                 a.z = fmaf(w, v.z, a.z);
@@ -1041,7 +1096,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (d == 0)
               p.lse[row] = (sm.row_m[r] + log2f(sm.row_w[r])) * kLn2;
           }
-          if (ctid == 0) p.tickets[grp] = 0;
         }
       }
       // all consumers are done with this unit's info and scratch
@@ -1054,17 +1108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
-  // ---- tear-down: the last CTA out resets the work queue ----
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int done = atomicAdd(&p.counters[1], 1);
-    if (done == (int)gridDim.x - 1) {
-      p.counters[0] = 0;
-      p.counters[1] = 0;
-      __threadfence();
-    }
-  }
+  __syncthreads();  // no warp leaves while the others may use the barriers
 }
 
 // --------------------------------------------------------------------------

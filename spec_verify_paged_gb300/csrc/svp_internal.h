@@ -22,25 +22,31 @@ struct AttnParams {
   void *out;
   float *lse;
   // workspace pieces
-  int *counters;       // [0] work queue head, [1] finished CTAs
-  int *tickets;        // [batch * Hkv * n_rg] split arrival counters
-  float *part_o;       // [batch*Hkv*n_rg][max_splits][RB][D] normalised partials
-  float *part_lse;     // [batch*Hkv*n_rg][max_splits][RB] log2-domain LSE
+  unsigned long long *tickets;  // [batch * Hkv * n_rg] arrivals per group:
+                                // (epoch << 32) | count
+  float *part_o;       // [2 * grid][RB][D] normalised partials: each CTA's
+                       // first- and last-segment slot
+  float *part_lse;     // [2 * grid][RB] log2-domain LSE of the partials
   int batch, num_q_heads, num_kv_heads, head_dim, group;
   int q_len, n_sink, window;
   int max_blocks, num_blocks;
   int rows;            // group * q_len query rows per (sequence, kv head)
-  int rb;              // rows per CTA work unit (row-group size)
+  int rb;              // rows per work unit (row-group size)
   int n_rg;            // ceil(rows / rb)
-  int split_pages;     // pages per split unit
-  int max_splits;      // upper bound of splits per sequence (workspace stride)
+  int min_pages;       // fewest pages a CTA's slice may hold
+  unsigned int epoch;  // this call's tag for ticket arrivals (never 0)
   float qscale;        // scale * log2(e)
 };
 
+// Tickets of calls with at most this many groups live at a fixed offset, so
+// no other call's partials ever land on them; bigger calls clear theirs.
+constexpr long long kTicketCap = 65536;
+
 struct AttnPlan {
-  int rb, n_rg, split_pages, max_splits, grid, ctas_per_sm;
+  int rb, n_rg, min_pages, grid, ctas_per_sm;
   bool mma;            // tensor-core path
-  size_t ws_counters, ws_tickets, ws_part_o, ws_part_lse, ws_total;
+  bool clear_tickets;  // more groups than the fixed ticket region holds
+  size_t ws_head, ws_tickets, ws_part_o, ws_part_lse, ws_total;
 };
 
 // Fills the plan (no CUDA launches).  dtype 0 = f32, 1 = bf16.  Returns 0 or

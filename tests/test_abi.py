@@ -102,12 +102,16 @@ def test_workspace_too_small(lib):
 
 
 def test_workspace_size_grows_with_work(lib):
+    """Header + one ticket per (sequence, kv head, row group) + two partial
+    slots per CTA: more sequences need more, a window never needs more."""
     small = lib.paged_decode_workspace_size(ctypes.byref(_dims()), 1, 0, 0)
-    big = lib.paged_decode_workspace_size(
-        ctypes.byref(_dims(batch=64, max_blocks_per_seq=512)), 1, 0, 0)
-    win = lib.paged_decode_workspace_size(
-        ctypes.byref(_dims(batch=64, max_blocks_per_seq=512)), 1, 4, 64)
-    assert 0 < small < big and win < big
+    many = dict(batch=4096, num_q_heads=64, num_kv_heads=64,
+                max_blocks_per_seq=512)     # 262144 groups > fixed tickets
+    big = lib.paged_decode_workspace_size(ctypes.byref(_dims(**many)), 1, 0, 0)
+    win = lib.paged_decode_workspace_size(ctypes.byref(_dims(**many)), 1, 4, 64)
+    assert 0 < small < big and win <= big
+    # the fixed ticket region (65536 x 8 bytes) is always there
+    assert small >= 256 + 65536 * 8
     assert lib.paged_decode_workspace_size(None, 1, 0, 0) == 0
     assert lib.paged_decode_workspace_size(ctypes.byref(_dims(head_dim=80)),
                                            1, 0, 0) == 0

@@ -84,8 +84,9 @@ def test_noalloc_rejects_requests_beyond_the_scratch(lib):
     with SVP_ERR_WORKSPACE before anything is launched."""
     from spec_verify_paged_gb300 import binding
     d = binding.SvpDims()
-    d.batch, d.num_q_heads, d.num_kv_heads, d.head_dim = 4096, 64, 64, 128
-    d.block_size, d.max_blocks_per_seq, d.num_blocks = 16, 8192, 1 << 20
+    # 4096 sequences x 4096 kv heads: 16.8M split tickets (67 MB) alone
+    d.batch, d.num_q_heads, d.num_kv_heads, d.head_dim = 4096, 4096, 4096, 128
+    d.block_size, d.max_blocks_per_seq, d.num_blocks = 16, 1, 1 << 20
     d.dtype, d.split_pages, d.kernel_path = 1, 8, 1
     p = ctypes.c_void_p(0x1000)  # never dereferenced: the size check fails first
     st = lib.paged_decode_attention_noalloc(ctypes.byref(d), p, p, p, p, p, 1,
