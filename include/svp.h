@@ -86,14 +86,23 @@ typedef struct {
 } svp_dims;
 
 /* Which attention kernel variant runs.  AUTO picks tensor cores (bf16 only)
- * when a kv head serves at least 3 query rows (GQA group x q_len), CUDA
- * cores otherwise.  Both compute the same quantity; forcing a path exists
- * for testing and tuning.  TENSOR_CORES with fp32 data is
- * SVP_ERR_UNSUPPORTED. */
+ * when a kv head serves at least 3 query rows (GQA group x q_len): TCGEN05
+ * for head_dim 128, TENSOR_CORES for head_dim 64; CUDA cores otherwise.
+ * All compute the same quantity; forcing a path exists for testing and
+ * tuning.
+ *   CUDA_CORES    fp32 FMA dot products, any dtype.
+ *   TENSOR_CORES  warp-level mma.sync (bf16 in, fp32 accumulate).
+ *   TCGEN05       fifth-generation tensor cores: tcgen05.mma with fp32
+ *                 accumulators in tensor memory, keys as the 128-row M
+ *                 dimension (bf16, head_dim 128, 1024 sequences per
+ *                 kernel launch).
+ * A forced tensor path on data it cannot take (fp32; head_dim 64 for
+ * TCGEN05) is SVP_ERR_UNSUPPORTED. */
 typedef enum {
   SVP_PATH_AUTO = 0,
   SVP_PATH_CUDA_CORES = 1,
-  SVP_PATH_TENSOR_CORES = 2
+  SVP_PATH_TENSOR_CORES = 2,
+  SVP_PATH_TCGEN05 = 3
 } svp_kernel_path;
 
 /* Paged decode / speculative-verify attention.
@@ -120,10 +129,10 @@ typedef enum {
  * launch.
  * Workspace: paged_decode_workspace_size() bytes, passed in dims; it needs
  * no initialisation: split arrivals are counted in 64-bit tickets tagged
- * with a per-call number, so whatever a ticket holds from earlier calls
- * counts as zero (a call with more than 65536 sequence x kv-head groups
- * also clears its tickets with one cudaMemsetAsync).  One kernel launch per
- * 4096 sequences.  With
+ * with a per-launch number, so whatever a ticket holds from earlier
+ * launches counts as zero (a call with more than 65536 sequence x kv-head
+ * groups also clears its tickets with one cudaMemsetAsync).  One kernel
+ * launch per 4096 sequences (1024 on the TCGEN05 path).  With
  * dims->workspace == NULL the library uses a buffer of its own per device,
  * (re)allocated inside the call when it is too small -- that first call is
  * then not capturable in a CUDA graph.  Calls that share a workspace must
@@ -133,7 +142,8 @@ typedef enum {
  * num_q_heads not a multiple of num_kv_heads, q_len < 1, n_sink < 0,
  * window < 0, a non-finite scale or an unknown kernel_path;
  * SVP_ERR_UNSUPPORTED for head_dim not in {64,128}, block_size != 16,
- * q_len > 16, batch > 65535, or a forced tensor-core path on fp32 data;
+ * q_len > 16, batch > 65535, or a forced tensor-core path on data it cannot
+ * take;
  * SVP_ERR_WORKSPACE for a caller workspace that is too small.  batch == 0
  * returns SVP_OK at once. */
 int paged_decode_attention(const svp_dims *dims, const void *q,
@@ -163,10 +173,11 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device, with that device current);
  *     make that first call before any stream capture.
- *   - Every call shares the one array and leaves its contents behind; the
- *     call clears the counters it relies on before launching, so calls in
- *     sequence on one stream are independent.  Calls that overlap on the
- *     GPU (other streams, other host threads) race on the array.
+ *   - Every call shares the one array and leaves its contents behind;
+ *     nothing in it needs to start at zero (split counters are tagged with
+ *     a per-launch number), so calls in sequence on one stream are
+ *     independent.  Calls that overlap on the GPU (other streams, other
+ *     host threads) race on the array.
  *   - With dims->split_pages == 0 the automatic slice size is enlarged (64,
  *     then 128 pages per CTA: fewer partial slots) when the default plan
  *     would not fit the array.

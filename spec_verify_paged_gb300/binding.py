@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libsvp.so")
 SVP_OK, SVP_ERR_INVALID_ARG, SVP_ERR_UNSUPPORTED, SVP_ERR_CUDA, SVP_ERR_WORKSPACE = (
     0, -1, -2, -3, -4)
 SVP_F32, SVP_BF16 = 0, 1
-PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES, PATH_TCGEN05 = 0, 1, 2, 3
 DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
             "paged_decode_workspace_size",

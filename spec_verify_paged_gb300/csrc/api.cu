@@ -74,7 +74,7 @@ static int check_dims(const svp_dims *d) {
   if (d->batch < 0 || d->num_q_heads < 1 || d->num_kv_heads < 1 ||
       d->head_dim < 1 || d->block_size < 1 || d->max_blocks_per_seq < 0 ||
       d->num_blocks < 0 || d->split_pages < 0 || d->kernel_path < 0 ||
-      d->kernel_path > SVP_PATH_TENSOR_CORES)
+      d->kernel_path > SVP_PATH_TCGEN05)
     return SVP_ERR_INVALID_ARG;
   if (d->num_q_heads % d->num_kv_heads != 0) return SVP_ERR_INVALID_ARG;
   if (d->dtype != SVP_F32 && d->dtype != SVP_BF16) return SVP_ERR_INVALID_ARG;
@@ -95,27 +95,50 @@ static int max_visible_pages(int max_blocks, int q_len, int n_sink,
   return (int)(b < max_blocks ? b : max_blocks);
 }
 
+constexpr int kBatchPerLaunch = 4096;
+
+// The kernel variant for this shape (a svp_kernel_path other than AUTO), or
+// SVP_ERR_UNSUPPORTED for a forced path the shape cannot take.
+static int select_path(int dtype, int head_dim, int rows, int kernel_path,
+                       long long num_blocks, int num_kv_heads) {
+  // the tensor paths address the cache as a 2-D tensor with int32 rows
+  const bool tma_ok = tensor_maps_available() &&
+                      num_blocks * num_kv_heads * kBlockSize < (1LL << 31);
+  switch (kernel_path) {
+    case SVP_PATH_CUDA_CORES:
+      return SVP_PATH_CUDA_CORES;
+    case SVP_PATH_TENSOR_CORES:
+      if (dtype != SVP_BF16 || !tma_ok) return SVP_ERR_UNSUPPORTED;
+      return SVP_PATH_TENSOR_CORES;
+    case SVP_PATH_TCGEN05:
+      if (dtype != SVP_BF16 || head_dim != 128 || !tma_ok)
+        return SVP_ERR_UNSUPPORTED;
+      return SVP_PATH_TCGEN05;
+    default:
+      if (dtype != SVP_BF16 || rows < kMmaMinRows || !tma_ok)
+        return SVP_PATH_CUDA_CORES;
+      return head_dim == 128 ? SVP_PATH_TCGEN05 : SVP_PATH_TENSOR_CORES;
+  }
+}
+
 int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    int dtype, int max_blocks, int q_len, int n_sink,
                    int window, int split_pages, int kernel_path, int num_sms,
                    long long num_blocks, AttnPlan *plan) {
   const int group = num_q_heads / num_kv_heads;
   const int rows = group * q_len;
-  // the tensor path addresses the cache as a 2-D tensor with int32 rows
-  const bool tma_ok = tensor_maps_available() &&
-                      num_blocks * num_kv_heads * kBlockSize < (1LL << 31);
-  bool mma = false;
-  if (kernel_path == SVP_PATH_TENSOR_CORES) {
-    if (dtype != SVP_BF16 || !tma_ok) return SVP_ERR_UNSUPPORTED;
-    mma = true;
-  } else if (kernel_path == SVP_PATH_AUTO) {
-    mma = dtype == SVP_BF16 && rows >= kMmaMinRows && tma_ok;
-  }
-  // tensor path: one m16 tile per warp, two warps share a page beyond 16
-  int rb = mma ? (rows <= 16 ? 16 : 32)
-               : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  int path = select_path(dtype, head_dim, rows, kernel_path, num_blocks,
+                         num_kv_heads);
+  if (path < 0) return path;
+  const bool mma = path == SVP_PATH_TENSOR_CORES;
+  const bool tc = path == SVP_PATH_TCGEN05;
+  // mma.sync: one m16 tile per warp, two warps share a page beyond 16 rows;
+  // tcgen05: the rows are the MMA's N (16 or 32)
+  int rb = (mma || tc) ? (rows <= 16 ? 16 : 32)
+                       : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
   const int n_rg = (rows + rb - 1) / rb;
-  const int ctas = attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);
+  const int ctas = tc ? attention_tc_ctas_per_sm(rb, batch)
+                      : attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);
   const long long groups = (long long)batch * num_kv_heads * n_rg;
   // Every CTA of the persistent grid takes an equal slice of all pages;
   // a slice holds at least min_pages pages (fewer CTAs for small calls).
@@ -128,6 +151,8 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   plan->rb = rb;
   plan->n_rg = n_rg;
   plan->mma = mma;
+  plan->tc = tc;
+  plan->batch_cap = tc ? tc_batch_cap() : kBatchPerLaunch;
   plan->min_pages = min_pages;
   plan->grid = (int)grid;
   plan->ctas_per_sm = ctas;
@@ -141,20 +166,38 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   return SVP_OK;
 }
 
-constexpr int kBatchPerLaunch = 4096;
-
-// Sequences per launch: at most 4096 (the in-kernel prefix lives in shared
-// memory) and few enough that the flattened page count fits in 32 bits.
+// Sequences per launch: at most the path's cap (the in-kernel prefix lives
+// in shared memory) and few enough that the flattened page count fits in
+// 32 bits.
 static int batch_per_launch(const svp_dims *d, int q_len, int n_sink,
-                            int window) {
+                            int window, int cap) {
   const long long rows = (long long)(d->num_q_heads / d->num_kv_heads) * q_len;
   const long long per_seq =
       (long long)d->num_kv_heads * rows *
       max_visible_pages(d->max_blocks_per_seq, q_len, n_sink, window);
-  long long bl = per_seq > 0 ? ((1LL << 31) - 1) / per_seq : kBatchPerLaunch;
-  if (bl > kBatchPerLaunch) bl = kBatchPerLaunch;
+  long long bl = per_seq > 0 ? ((1LL << 31) - 1) / per_seq : cap;
+  if (bl > cap) bl = cap;
   if (bl > d->batch) bl = d->batch;
   return bl < 1 ? 1 : (int)bl;
+}
+
+// The plan of one launch of a call: its path fixes the sequences per
+// launch, which fix the grid and workspace.  plan->batch_cap is then the
+// call's sequences per launch.
+static int plan_call(const svp_dims *d, int q_len, int n_sink, int window,
+                     int sms, AttnPlan *plan) {
+  const int rows = (d->num_q_heads / d->num_kv_heads) * q_len;
+  const int path = select_path(d->dtype, d->head_dim, rows, d->kernel_path,
+                               d->num_blocks, d->num_kv_heads);
+  if (path < 0) return path;
+  const int cap = path == SVP_PATH_TCGEN05 ? tc_batch_cap() : kBatchPerLaunch;
+  const int bl = batch_per_launch(d, q_len, n_sink, window, cap);
+  const int st = plan_attention(bl, d->num_q_heads, d->num_kv_heads,
+                                d->head_dim, d->dtype, d->max_blocks_per_seq,
+                                q_len, n_sink, window, d->split_pages, path,
+                                sms, d->num_blocks, plan);
+  plan->batch_cap = bl;
+  return st;
 }
 
 }  // namespace svp
@@ -192,12 +235,8 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len, int n_sink,
     return 0;
   const int sms = device_sms();
   AttnPlan plan;
-  const int bl = batch_per_launch(dims, q_len, n_sink, window);
-  if (plan_attention(bl, dims->num_q_heads, dims->num_kv_heads,
-                     dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
-                     q_len, n_sink, window, dims->split_pages,
-                     dims->kernel_path, sms > 0 ? sms : 1, dims->num_blocks,
-                     &plan) != SVP_OK)
+  if (plan_call(dims, q_len, n_sink, window, sms > 0 ? sms : 1, &plan) !=
+      SVP_OK)
     return 0;
   return plan.ws_total;
 }
@@ -222,13 +261,10 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
   const int sms = device_sms();
   if (sms <= 0) return SVP_ERR_CUDA;
 
-  const int bl = batch_per_launch(dims, q_len, n_sink, window);
   AttnPlan plan;
-  st = plan_attention(bl, dims->num_q_heads, dims->num_kv_heads,
-                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
-                      q_len, n_sink, window, dims->split_pages,
-                      dims->kernel_path, sms, dims->num_blocks, &plan);
+  st = plan_call(dims, q_len, n_sink, window, sms, &plan);
   if (st != SVP_OK) return st;
+  const int bl = plan.batch_cap;
   void *ws = dims->workspace;
   if (ws) {
     if (dims->workspace_bytes < plan.ws_total) return SVP_ERR_WORKSPACE;
@@ -237,15 +273,13 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     if (st != SVP_OK) return st;
   }
   char *wp = static_cast<char *>(ws);
-  // Ticket arrivals carry this call's epoch, so stale tickets need no reset.
-  // Only a call with more groups than the fixed ticket region clears its
-  // (larger) region, which other shapes' partials may have overwritten.
+  // Ticket arrivals carry their launch's epoch, so stale tickets need no
+  // reset.  Only a call with more groups than the fixed ticket region clears
+  // its (larger) region, which other shapes' partials may have overwritten.
   if (plan.clear_tickets &&
       cudaMemsetAsync(wp + plan.ws_head, 0, plan.ws_tickets, stream) !=
           cudaSuccess)
     return SVP_ERR_CUDA;
-  unsigned int epoch = g_epoch.fetch_add(1) + 1;
-  if (epoch == 0) epoch = g_epoch.fetch_add(1) + 1;
   const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
   const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
   int launches = 0;
@@ -260,6 +294,9 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.out = static_cast<char *>(out) + (size_t)b0 * q_len * row_elems * eb;
     p.lse = lse + (size_t)b0 * q_len * dims->num_q_heads;
     p.tickets = reinterpret_cast<unsigned long long *>(wp + plan.ws_head);
+    // every launch has its own epoch: sub-launches index the same tickets
+    unsigned int epoch = g_epoch.fetch_add(1) + 1;
+    if (epoch == 0) epoch = g_epoch.fetch_add(1) + 1;
     p.epoch = epoch;
     p.part_o = reinterpret_cast<float *>(wp + plan.ws_head + plan.ws_tickets);
     p.part_lse = reinterpret_cast<float *>(wp + plan.ws_head +
@@ -284,10 +321,14 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
       plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
                      dims->head_dim, dims->dtype, dims->max_blocks_per_seq,
                      q_len, n_sink, window, plan.min_pages,
-                     plan.mma ? SVP_PATH_TENSOR_CORES : SVP_PATH_CUDA_CORES,
+                     plan.tc    ? SVP_PATH_TCGEN05
+                     : plan.mma ? SVP_PATH_TENSOR_CORES
+                                : SVP_PATH_CUDA_CORES,
                      sms, dims->num_blocks, &sub);
     }
-    cudaError_t e = launch_attention(p, dims->dtype, plan.mma, sub.grid, stream);
+    cudaError_t e =
+        plan.tc ? launch_attention_tc(p, sub.grid, stream)
+                : launch_attention(p, dims->dtype, plan.mma, sub.grid, stream);
     if (e != cudaSuccess) return SVP_ERR_CUDA;
     ++launches;
   }
@@ -358,6 +399,7 @@ int spec_accept(int batch, int num_draft, int vocab,
 int svp_read_device_status(cudaStream_t stream, int *flags) {
   unsigned f = 0;
   if (read_status_attention(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
+  if (read_status_attention_tc(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
   if (read_status_append(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
   if (read_status_accept(stream, &f) != cudaSuccess) return SVP_ERR_CUDA;
   if (flags) *flags = (int)f;

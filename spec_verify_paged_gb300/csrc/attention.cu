@@ -8,16 +8,16 @@
 // scaled scores over the keys visible to it, times V, plus the log-sum-exp.
 //
 // How (GB300 design):
-//  * Work unit = (sequence b, kv head g, split s, row group rg).  The rows of
-//    a unit are up to RB query rows (i, h) that share kv head g (GQA group x
-//    q_len), so each K/V page fetched serves all of them.  Only pages that
-//    hold visible keys are enumerated (sink pages, then window pages), so
-//    masked-out pages are never read.
-//  * Persistent CTAs pull units from a global work queue (atomic counter,
-//    next unit claimed one unit ahead).  One producer warp streams the
-//    unit's pages: it reads the block table once per unit (one coalesced
-//    load per 32 pages) and fills an NSTAGES-deep shared-memory ring guarded
-//    by mbarriers, running ahead across unit boundaries.
+//  * A group = (sequence b, kv head g, row group rg): up to RB query rows
+//    (i, h) that share kv head g (GQA group x q_len), so each K/V page
+//    fetched serves all of them.  Only pages that hold visible keys are
+//    enumerated (sink pages, then window pages), so masked-out pages are
+//    never read.
+//  * Persistent CTAs take equal slices of the flattened (group, page) list
+//    (stream-K, attn_common.cuh).  One producer warp walks the slice's
+//    segments: it reads the block table once per 128 pages (coalesced) and
+//    fills an NSTAGES-deep shared-memory ring guarded by mbarriers, running
+//    ahead across segment boundaries.
 //  * CUDA-core path (few rows per kv head): one 1-D bulk copy (TMA engine,
 //    cp.async.bulk) per 16-row K page and V page.  Four consumer warps take
 //    pages round-robin; lane l owns D/32 dims; a page's 16 partial dot
@@ -31,11 +31,10 @@
 //    registers as the A operand of P V (no shared-memory round trip), V is
 //    read with ldmatrix.trans.  The running row sums stay per lane and are
 //    reduced once per unit.
-//  * The warps' states are merged by log-sum-exp at unit end.  Split-K: if a
-//    sequence needs more than one split, each writes its normalised partial
-//    (o, lse2) to the workspace and takes an atomic ticket; the CTA that
-//    takes the last ticket merges all partials in split order
-//    (deterministic) and resets the ticket.  No CTA ever waits for another.
+//  * The warps' states are merged by log-sum-exp at segment end.  A group
+//    split over several slices is finished by the CTA whose ticket arrives
+//    last; it merges all partials in slice order (deterministic).  No CTA
+//    ever waits for another.
 //  * Rows of a page that hold no valid data (positions >= seq_len, evicted
 //    stream rows) are zeroed in shared memory before P V, because p = 0
 //    times a NaN left in unused cache memory is still NaN.
@@ -51,9 +50,7 @@
 #include <mutex>
 #include <tuple>
 
-#include "ptx.cuh"
-#include "svp.h"
-#include "svp_internal.h"
+#include "attn_common.cuh"
 
 namespace svp {
 
@@ -61,49 +58,6 @@ static __device__ unsigned int g_status_attn;
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kUnitRing = 4;
-constexpr int kTableChunk = 128;     // block-table entries loaded per round
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kBoxElems = 64;        // 128-byte swizzle box: 64 bf16 columns
-constexpr int kBoxBytes = kBlockSize * 128;
-
-// One segment of a CTA's slice: pages [page0, page0 + n_pages) of group
-// (b, g, rg).  CTAs f..l own the group's pages; `slot` says whether this is
-// the CTA's first (0) or last (1) segment, which is where its partial goes.
-struct UnitInfo {
-  int b, g, rg, slot;
-  int f, l, gstart, page0;
-  int n_pages, seq_len, n_a, b_start;
-  int valid, pad0, pad1, pad2;
-};
-
-struct TensorMaps {
-  CUtensorMap k;
-  CUtensorMap v;
-};
-
-// Visible logical blocks of a sequence: [0, n_a) followed by
-// [b_start, b_start + n_pages - n_a).  (window == 0: all blocks.)
-__device__ __forceinline__ void visible_pages(int L, int q_len, int n_sink,
-                                              int window, int &n_a,
-                                              int &b_start, int &n_pages) {
-  const int nblk = (L + kBlockSize - 1) / kBlockSize;
-  n_a = 0;
-  b_start = 0;
-  n_pages = nblk;
-  if (window == 0) return;
-  const int t0 = L - q_len;                     // first query position
-  const int lo = max(0, t0 - window + 1);       // first window key (union)
-  const int sink_end = min(n_sink, L);
-  const int na = (sink_end + kBlockSize - 1) / kBlockSize;
-  const int bs = lo / kBlockSize;
-  if (bs <= na) return;                         // ranges touch: all blocks
-  n_a = na;
-  b_start = bs;
-  n_pages = na + (nblk - bs);
-}
-
 template <typename T, int D>
 struct Vec;
 // lane owns VEC = D/32 consecutive elements; load them as fp32
@@ -139,12 +93,6 @@ struct Vec<uint16_t, 128> {
     f[3] = __uint_as_float(v.y & 0xffff0000u);
   }
 };
-
-__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
-__device__ __forceinline__ void store_out(uint16_t *p, float v) {
-  __nv_bfloat16 h = __float2bfloat16_rn(v);
-  *p = *reinterpret_cast<uint16_t *>(&h);
-}
 
 template <typename T, int D>
 struct Cfg {
@@ -487,16 +435,6 @@ __device__ __forceinline__ void zero_invalid_rows(unsigned char *vp, int lane,
   __syncwarp();
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
-                                            int x, int y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
@@ -519,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int B = p.batch;
   const int groups_per_seq = p.num_kv_heads * p.n_rg;
 
   // ---- set-up: barriers and the per-sequence unit prefix ----
@@ -538,50 +475,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (warp == 0) {
     // pages of every sequence, times its groups (kv heads x row groups)
-    int run = 0;
-    if (lane == 0) sm.prefix[0] = 0;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      const int b = b0 + lane;
-      int n = 0;
-      if (b < B) {
-        const int L = p.seq_lens[b];
-        if (L < p.q_len || L > p.max_blocks * kBlockSize) {
-          if (blockIdx.x == 0) raise_flag(SVP_DEV_BAD_SEQ_LEN);
-        } else {
-          int na, bs, np;
-          visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
-          n = np * groups_per_seq;
-        }
-      }
-      int incl = n;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        int y = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += y;
-      }
-      if (b < B) sm.prefix[b + 1] = run + incl;
-      run += __shfl_sync(kFull, incl, 31);
-    }
+    const int run = build_prefix(p, sm.prefix, groups_per_seq, lane,
+                                 &g_status_attn);
     if (lane == 0) {
       sm.total_pages = run;
-      // CTAs that share the pages: at least min_pages each
-      long long ce = run / (p.min_pages > 0 ? p.min_pages : 1);
-      if (ce > (long long)gridDim.x) ce = gridDim.x;
-      if (ce < 1) ce = 1;
-      sm.n_ctas = (int)ce;
+      sm.n_ctas = working_ctas(run, p.min_pages);
     }
   }
   __syncthreads();
   const int total_pages = sm.total_pages;
   const int n_ctas = sm.n_ctas;
   // this CTA's slice of the flattened (sequence, group, page) space
-  const int range_begin =
-      blockIdx.x < n_ctas ? (int)((long long)blockIdx.x * total_pages / n_ctas)
-                          : total_pages;
-  const int range_end =
-      blockIdx.x < n_ctas
-          ? (int)((long long)(blockIdx.x + 1) * total_pages / n_ctas)
-          : total_pages;
+  const int range_begin = slice_begin(blockIdx.x, total_pages, n_ctas);
+  const int range_end = blockIdx.x < n_ctas
+                            ? slice_begin(blockIdx.x + 1, total_pages, n_ctas)
+                            : total_pages;
 
   if (warp == kConsumerWarps) {
     // ======================= producer warp =======================
@@ -602,33 +510,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         break;
       }
-      // decode pos -> (b, group, page): binary search in the prefix
-      int lo = 0, hi = B;  // find b with prefix[b] <= pos < prefix[b+1]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (sm.prefix[mid] <= pos) lo = mid; else hi = mid;
-      }
-      const int b = lo;
-      const int np = (sm.prefix[b + 1] - sm.prefix[b]) / groups_per_seq;
-      const int qoff = pos - sm.prefix[b];
-      const int gi = qoff / np;              // group within the sequence
-      const int page0 = qoff - gi * np;      // first page of this segment
-      const int g = gi / p.n_rg, rg = gi - g * p.n_rg;
-      const int n_pages = min(range_end - pos, np - page0);
-      const int gstart = pos - page0;        // the group's first flat page
-      // CTAs that own the group's first and last pages
-      const int f = (int)(((long long)(gstart + 1) * n_ctas - 1) / total_pages);
-      const int l = (int)(((long long)(gstart + np) * n_ctas - 1) / total_pages);
-      const int L = __ldg(p.seq_lens + b);
-      int na, bs, np2;
-      visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np2);
+      const UnitInfo seg =
+          decode_segment(p, sm.prefix, groups_per_seq, pos, range_begin,
+                         range_end, total_pages, n_ctas);
+      const int b = seg.b, g = seg.g, n_pages = seg.n_pages;
+      const int page0 = seg.page0, na = seg.n_a, bs = seg.b_start;
       if (lane == 0) {
-        UnitInfo &ui = sm.unit[slot];
-        ui.b = b; ui.g = g; ui.rg = rg;
-        ui.slot = (pos == range_begin) ? 0 : 1;  // first or last segment
-        ui.f = f; ui.l = l; ui.gstart = gstart;
-        ui.page0 = page0; ui.n_pages = n_pages;
-        ui.seq_len = L; ui.n_a = na; ui.b_start = bs; ui.valid = 1;
+        sm.unit[slot] = seg;
         mbar_arrive(&sm.ufull[slot]);
       }
       const size_t head_off = (size_t)g * C::PAGE_ELEMS;
@@ -982,119 +870,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
           break;
         }
-        if (ctid == 0) {
-          // arrivals of this call are tagged with its epoch in the high word;
-          // a ticket left by another call (or never written) counts as zero
-          unsigned long long *tk = p.tickets + grp;
-          unsigned long long seen = __ldcg(tk), want;
-          unsigned int before;
-          while (true) {
-            before = (unsigned int)(seen >> 32) == p.epoch ? (unsigned int)seen : 0u;
-            want = ((unsigned long long)p.epoch << 32) | (before + 1u);
-            const unsigned long long got = atomicCAS(tk, seen, want);
-            if (got == seen) break;
-            seen = got;
-          }
-          sm.is_last = (before == (unsigned int)(ui.l - ui.f));
-        }
+        if (ctid == 0) sm.is_last = take_ticket(p, grp, ui.l - ui.f + 1);
         if (!epi_sync(sm, epi_phase, lane)) {
           if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
           break;
         }
         if (sm.is_last) {
           __threadfence();
-          // contributors are CTAs f..l in order; CTA f's partial sits in its
-          // last-segment slot when its slice began before this group
-          const int ns = ui.l - ui.f + 1;
-          const int f_begin = (int)((long long)ui.f * total_pages / n_ctas);
-          const int f_tail = f_begin < ui.gstart ? 1 : 0;
-          auto prow_of = [&](int sidx) -> size_t {
-            return (size_t)(2 * (ui.f + sidx) + (sidx == 0 ? f_tail : 0));
-          };
-          const int vrows = min(RB, p.rows - rg * RB);  // valid rows here
-          // per-row max and weight sum over the splits (warp w: rows w, w+4..)
-          for (int r = warp; r < vrows; r += kConsumerWarps) {
-            float M = -INFINITY;
-            for (int s = lane; s < ns; s += 32)
-              M = fmaxf(M, __ldcg(p.part_lse + prow_of(s) * RB + r));
-#pragma unroll
-            for (int off = 16; off; off >>= 1)
-              M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-            float W = 0.f;
-            if (M != -INFINITY)
-              for (int s = lane; s < ns; s += 32)
-                W += ex2(__ldcg(p.part_lse + prow_of(s) * RB + r) - M);
-#pragma unroll
-            for (int off = 16; off; off >>= 1)
-              W += __shfl_xor_sync(kFull, W, off);
-            if (lane == 0) { sm.row_m[r] = M; sm.row_w[r] = W; }
-          }
-          if (!epi_sync(sm, epi_phase, lane)) {
+          if (!merge_partials<T, D, RB, kConsumerWarps * 32>(
+                  p, ui, total_pages, n_ctas, &sm.red_o[0][0][0],
+                  kConsumerWarps * RW * D, sm.row_m, sm.row_w, &sm.epi,
+                  epi_phase, ctid)) {
             if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
             break;
-          }
-          // normalised split weights go to shared memory (red_o is free now),
-          // CH splits at a time; each thread then sums float4 slices of the
-          // partial outputs with independent loads.
-          constexpr int CH = kConsumerWarps * RW * D / RB;  // splits per chunk
-          constexpr int NE4 = RB * D / 4;          // float4 slices per unit
-          constexpr int EPT = (NE4 + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
-          float *wts = &sm.red_o[0][0][0];
-          const float4 *po4 = reinterpret_cast<const float4 *>(p.part_o);
-          float4 acc[EPT];
-#pragma unroll
-          for (int k = 0; k < EPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          bool merged = true;
-          for (int s0 = 0; s0 < ns; s0 += CH) {
-            const int cn = min(CH, ns - s0);
-            // (branch free: an empty split has lse2 = -inf and weight 0)
-#pragma unroll 4
-            for (int idx = ctid; idx < cn * RB; idx += kConsumerWarps * 32) {
-              const int s = s0 + idx / RB, r = idx % RB;
-              const float ls = __ldcg(p.part_lse + prow_of(s) * RB + r);
-              const float w = ex2(ls - sm.row_m[r]) / sm.row_w[r];
-              wts[idx] = r < vrows ? w : 0.f;
-            }
-            if (!epi_sync(sm, epi_phase, lane)) { merged = false; break; }
-#pragma unroll
-            for (int k = 0; k < EPT; ++k) {
-              const int e4 = ctid + k * kConsumerWarps * 32;
-              if (e4 >= vrows * (D / 4)) continue;
-              const int r = e4 / (D / 4), d4 = e4 % (D / 4);
-              float4 a = acc[k];
-#pragma unroll 8
-              for (int s = 0; s < cn; ++s) {
-                const float w = wts[s * RB + r];
-                const float4 v = __ldcg(po4 + (prow_of(s0 + s) * RB + r) * (D / 4) + d4);
-                a.x = fmaf(w, v.x, a.x);
-                a.y = fmaf(w, v.y, a.y);
-                a.z = fmaf(w, v.z, a.z);
-                a.w = fmaf(w, v.w, a.w);
-              }
-              acc[k] = a;
-            }
-            if (!epi_sync(sm, epi_phase, lane)) { merged = false; break; }
-          }
-          if (!merged) {
-            if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
-            break;
-          }
-#pragma unroll
-          for (int k = 0; k < EPT; ++k) {
-            const int e4 = ctid + k * kConsumerWarps * 32;
-            if (e4 >= vrows * (D / 4)) continue;
-            const int r = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
-            const int gr = rg * RB + r;
-            const int i = gr / p.group;
-            const int h = g * p.group + gr % p.group;
-            const size_t row = ((size_t)b * p.q_len + i) * p.num_q_heads + h;
-            T *dst = static_cast<T *>(p.out) + row * D + d;
-            store_out(dst + 0, acc[k].x);
-            store_out(dst + 1, acc[k].y);
-            store_out(dst + 2, acc[k].z);
-            store_out(dst + 3, acc[k].w);
-            if (d == 0)
-              p.lse[row] = (sm.row_m[r] + log2f(sm.row_w[r])) * kLn2;
           }
         }
       }
@@ -1114,45 +902,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 // --------------------------------------------------------------------------
 // host side
 // --------------------------------------------------------------------------
-
-// cuTensorMapEncodeTiled, fetched once through the runtime (no -lcuda).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
-                                  void *, const cuuint64_t *, const cuuint64_t *,
-                                  const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// The cache as a 2-D bf16 tensor [num_blocks*Hkv*16 rows, D], 128-byte
-// swizzled boxes of 16 rows x 64 columns.
-static bool make_kv_map(CUtensorMap *map, const void *base, int num_blocks,
-                        int hkv, int d) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)d,
-                              (cuuint64_t)num_blocks * hkv * kBlockSize};
-  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBoxElems, (cuuint32_t)kBlockSize};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // per (device, instantiation, shared-memory size): attribute set + occupancy
 static std::mutex g_occ_mu;

@@ -11,9 +11,9 @@
 //
 // The array lives in every GPU that loads the library, from module load
 // until process exit.  Every call shares it, and it keeps the last call's
-// contents; the attention entry point clears the counters it relies on
-// before each launch, so nothing else must start at zero.  Calls that
-// overlap on the GPU race on it.
+// contents.  Nothing in it must start at zero: the split counters carry a
+// per-launch tag, so counts left by earlier launches read as zero.  Calls
+// that overlap on the GPU race on it.
 #include <mutex>
 
 #include "svp.h"

@@ -34,7 +34,7 @@ struct AttnParams {
   int rb;              // rows per work unit (row-group size)
   int n_rg;            // ceil(rows / rb)
   int min_pages;       // fewest pages a CTA's slice may hold
-  unsigned int epoch;  // this call's tag for ticket arrivals (never 0)
+  unsigned int epoch;  // this launch's tag for ticket arrivals (never 0)
   float qscale;        // scale * log2(e)
 };
 
@@ -44,7 +44,9 @@ constexpr long long kTicketCap = 65536;
 
 struct AttnPlan {
   int rb, n_rg, min_pages, grid, ctas_per_sm;
-  bool mma;            // tensor-core path
+  bool mma;            // warp-level mma.sync path
+  bool tc;             // tcgen05 path (tensor-memory accumulators)
+  int batch_cap;       // sequences per launch
   bool clear_tickets;  // more groups than the fixed ticket region holds
   size_t ws_head, ws_tickets, ws_part_o, ws_part_lse, ws_total;
 };
@@ -57,7 +59,8 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    long long num_blocks, AttnPlan *plan);
 
 // Query rows per kv head (GQA group x q_len) from which the automatic path
-// choice uses tensor cores (bf16 only).
+// choice uses tensor cores (bf16 only): tcgen05 for head_dim 128, warp-level
+// mma.sync for head_dim 64.
 constexpr int kMmaMinRows = 3;
 
 // Occupancy-derived CTAs per SM for the attention kernel of this shape
@@ -70,6 +73,13 @@ cudaError_t launch_attention(const AttnParams &p, int dtype, bool mma,
 
 // True when the driver provides cuTensorMapEncodeTiled.
 bool tensor_maps_available();
+
+// The tcgen05 kernel (attention_tc.cu): bf16, head_dim 128, 16 or 32 rows
+// per group, at most tc_batch_cap() sequences per launch.
+int tc_batch_cap();
+int attention_tc_ctas_per_sm(int rb, int batch);
+cudaError_t launch_attention_tc(const AttnParams &p, int grid,
+                                cudaStream_t stream);
 
 struct AppendParams {
   const void *k_new;
@@ -96,6 +106,7 @@ cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream);
 
 // Device status words (one per translation unit): read-and-clear.
 cudaError_t read_status_attention(cudaStream_t s, unsigned *flags);
+cudaError_t read_status_attention_tc(cudaStream_t s, unsigned *flags);
 cudaError_t read_status_append(cudaStream_t s, unsigned *flags);
 cudaError_t read_status_accept(cudaStream_t s, unsigned *flags);
 

@@ -85,20 +85,30 @@ SWEEP = [
 ]
 
 
-PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "tcgen05": 3}
+
+
+def _unsupported(path, dtype, D):
+    """Forced tensor paths refuse data they cannot take."""
+    if path == "tensor_cores":
+        return dtype == "f32"
+    if path == "tcgen05":
+        return dtype == "f32" or D != 128
+    return False
 
 
 @pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("case", SWEEP, ids=[str(i) for i in range(len(SWEEP))])
 def test_parity_sweep(svp, oracle_mod, case, path):
     """Every case through each kernel path (automatic choice, CUDA cores,
-    tensor cores); fp32 data has no tensor-core path and must say so."""
+    warp-level tensor cores, tcgen05); a forced tensor path on data it cannot
+    take must say so."""
     dtype, D, Hq, Hkv, q_len, lo, hi, n_sink, window, sp = case
     cfg = W.small_config(batch=5, num_q_heads=Hq, num_kv_heads=Hkv,
                          head_dim=D, q_len=q_len, dtype=dtype, ctx_min=lo,
                          ctx_max=hi, seed=100 + D + q_len + Hq)
     wl = W.make_attention(cfg, n_new=min(q_len, 2))
-    if dtype == "f32" and path == "tensor_cores":
+    if _unsupported(path, dtype, D):
         with pytest.raises(svp.SvpError) as e:
             _run_gpu(svp, wl, n_sink, window, split_pages=sp,
                      kernel_path=PATHS[path])
@@ -109,7 +119,7 @@ def test_parity_sweep(svp, oracle_mod, case, path):
     _compare(wl, got, _oracle(oracle_mod, wl, n_sink, window))
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 @pytest.mark.parametrize("sp", [1, 2, 7, 128])
 def test_split_counts_agree(svp, oracle_mod, sp, path):
     """The same inputs under different split sizes (1 page per split up to
@@ -121,7 +131,8 @@ def test_split_counts_agree(svp, oracle_mod, sp, path):
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
 
 
-@pytest.mark.parametrize("path,q_len,Hq", [(1, 1, 4), (2, 1, 4), (2, 3, 8)])
+@pytest.mark.parametrize("path,q_len,Hq", [(1, 1, 4), (2, 1, 4), (2, 3, 8),
+                                           (3, 1, 4), (3, 3, 8)])
 def test_ring_layout_small(svp, oracle_mod, path, q_len, Hq):
     """A streaming cache in a ring of pages with NaN in every non-resident
     row: only sink and window rows may be read."""
@@ -182,7 +193,8 @@ def test_empty_batch(svp):
     assert out.shape == (0, 1, 4, 64) and svp.last_launch_count() == 0
 
 
-def test_bad_block_id_is_flagged_not_read(svp):
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_bad_block_id_is_flagged_not_read(svp, path):
     """A block-table entry outside [0, num_blocks) is caught before any load:
     the device status reports it and nothing faults."""
     import torch
@@ -191,12 +203,13 @@ def test_bad_block_id_is_flagged_not_read(svp):
     wl = W.make_attention(cfg)
     bt = wl.block_table.copy()
     bt[1, 1] = wl.num_blocks + 1000
-    svp.paged_decode_attention(to_dev(wl.q), to_dev(wl.k_cache),
-                               to_dev(wl.v_cache), to_dev(bt),
-                               to_dev(wl.seq_lens), q_len=1)
+    out, _ = svp.paged_decode_attention(
+        to_dev(wl.q), to_dev(wl.k_cache), to_dev(wl.v_cache), to_dev(bt),
+        to_dev(wl.seq_lens), q_len=1, kernel_path=path)
     torch.cuda.synchronize()
     assert svp.read_device_status() & 1
     assert svp.read_device_status() == 0  # read clears
+    assert torch.isfinite(out.float()).all()
 
 
 def test_bad_seq_len_is_flagged(svp):
@@ -253,3 +266,17 @@ def test_workspace_shared_across_shapes(svp, oracle_mod):
         torch.cuda.synchronize()
         _compare(wl, (out_as_f64(out), lse.cpu().numpy().astype(np.float64)),
                  _oracle(oracle_mod, wl, 0, 0))
+
+
+@pytest.mark.parametrize("path,batch", [(1, 4100), (3, 1030)])
+def test_many_sequences_span_launches(svp, oracle_mod, path, batch):
+    """More sequences than one launch takes (4096 on CUDA cores, 1024 on
+    tcgen05): the call makes two launches on one workspace, with groups
+    split over several CTAs in both; every output matches the oracle."""
+    cfg = W.small_config(batch=batch, num_q_heads=4, num_kv_heads=1,
+                         head_dim=128, q_len=2, ctx_min=2, ctx_max=70,
+                         seed=61)
+    wl = W.make_attention(cfg)
+    got = _run_gpu(svp, wl, 0, 0, split_pages=1, kernel_path=path)
+    assert svp.last_launch_count() == 2
+    _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
