@@ -49,8 +49,7 @@ from spec_verify_paged_gb300 import workloads as W  # noqa: E402
 METRIC = ("decode-attention query-tokens/s and achieved KV-read HBM GB/s "
           "(% of GB300 peak)")
 UNIT = "query-tokens/s"
-PROFILE = os.path.join(ROOT, "profiles", "ncu_paged_attention_decode-7b.md")
-ATTN_SRC = os.path.join(ROOT, "spec_verify_paged_gb300", "csrc", "attention.cu")
+CSRC = os.path.join(ROOT, "spec_verify_paged_gb300", "csrc")
 
 
 # --------------------------------------------------------------------------
@@ -66,18 +65,32 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_traffic():
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current attention kernel source; else None."""
-    if not os.path.exists(PROFILE):
+def attention_kernel(cfg, kernel_path):
+    """(kernel name, its source file) for the path the library takes: the
+    tcgen05 kernel for bf16 head_dim-128 groups of 3+ query rows, the
+    CUDA-core / mma.sync kernel otherwise."""
+    rows = cfg.q_len * (cfg.num_q_heads // cfg.num_kv_heads)
+    tc = (kernel_path == 3 or
+          (kernel_path == 0 and cfg.dtype == "bf16" and cfg.head_dim == 128
+           and rows >= 3))
+    if tc:
+        return "paged_attention_tc_kernel", "attention_tc.cu"
+    return "paged_attention_kernel", "attention.cu"
+
+
+def kernel_traffic(kernel, src, workload):
+    """dram bytes per launch from the committed ncu summary of this kernel
+    on this workload, if it was taken on the current source; else None."""
+    prof = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
+    if not os.path.exists(prof):
         return None
-    sha = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    sha = hashlib.sha256(open(os.path.join(CSRC, src), "rb").read()).hexdigest()[:16]
     vals = {}
-    for line in open(PROFILE):
+    for line in open(prof):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("attention.cu sha256 prefix") != sha:
+    if vals.get(f"{src} sha256 prefix") != sha:
         return None
     try:
         return int(vals["dram bytes per launch"])
@@ -301,7 +314,10 @@ def run_ours(args):
     wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
     conf, tr = workload_config(wl, args.split_pages or None)
     if args.kernel_path:
-        conf["kernel_path"] = {1: "cuda_cores", 2: "tensor_cores"}[args.kernel_path]
+        conf["kernel_path"] = {1: "cuda_cores", 2: "tensor_cores",
+                               3: "tcgen05"}[args.kernel_path]
+    conf["timing"] = ("plain calls" if args.no_graph else
+                      "CUDA-graph replays of the step")
 
     q = to_dev(wl.q, dev)
     kc, vc = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
@@ -331,6 +347,36 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
     assert svp.read_device_status() == 0, "device status flags raised"
+
+    # The timed loop replays the step as two CUDA graphs (the KV append,
+    # then the attention call) captured once here: a step of tens of
+    # microseconds would otherwise be paced by the host's Python and launch
+    # overhead, not by the GPU.  The library keeps no per-call state, so a
+    # replay does exactly the work of a call.  The end-to-end figure below
+    # still goes through the plain public calls every step.
+    g_app, g_attn = None, None
+    if not args.no_graph:
+        g_app, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_app):
+            svp.kv_append(kn, vn, kc, vc, bt, sl)
+        n_app = svp.last_launch_count()
+        with torch.cuda.graph(g_attn):
+            svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
+        n_attn = svp.last_launch_count()
+        torch.cuda.synchronize(dev)
+
+        def step(ev=None):  # noqa: F811 -- the replayed form of the step
+            g_app.replay()
+            if ev is not None:
+                ev[0].record(stream)
+            g_attn.replay()
+            if ev is not None:
+                ev[1].record(stream)
+            launches[0] += n_app + n_attn
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -398,6 +444,7 @@ def run_ours(args):
     d2h = sum(t.numel() * t.element_size() for _, t in out_parts)
 
     # ---- report ----
+    kname, ksrc = attention_kernel(cfg, args.kernel_path)
     tokens_per_step = cfg.batch * cfg.q_len
     value = world * tokens_per_step * args.steps / (ms_max / 1e3)
     attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
@@ -417,8 +464,8 @@ def run_ours(args):
                      "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "kernel": "paged_attention_kernel",
-                     "traffic": kernel_traffic()},
+                     "kernel": kname,
+                     "traffic": kernel_traffic(kname, ksrc, cfg.name)},
         "e2e": {"value": round(world * tokens_per_step / (e_ms / 1e3), 1),
                 "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
@@ -479,12 +526,15 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode-7b", choices=sorted(W.CONFIGS))
     ap.add_argument("--split-pages", type=int, default=0,
                     help="pages per split-K unit (0: automatic)")
-    ap.add_argument("--kernel-path", type=int, default=0, choices=[0, 1, 2],
-                    help="0 automatic, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--kernel-path", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="0 automatic, 1 CUDA cores, 2 warp-level tensor "
+                         "cores (mma.sync), 3 tcgen05")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's sequence count (smaller "
                          "cases for profiling; reported in config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time plain API calls instead of CUDA-graph replays")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

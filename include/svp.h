@@ -137,7 +137,7 @@ typedef enum {
  * (re)allocated inside the call when it is too small -- that first call is
  * then not capturable in a CUDA graph.  Calls that share a workspace must
  * not overlap on the GPU.
- * q, k_cache and v_cache must be 16-byte aligned.
+ * q, k_cache, v_cache and out must be 16-byte aligned.
  * Errors: SVP_ERR_INVALID_ARG for null or misaligned pointers, sizes < 0,
  * num_q_heads not a multiple of num_kv_heads, q_len < 1, n_sink < 0,
  * window < 0, a non-finite scale or an unknown kernel_path;

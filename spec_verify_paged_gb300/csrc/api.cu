@@ -1,7 +1,6 @@
 // api.cu -- the C ABI of libsvp.so: argument checks, split planning,
 // workspace handling and kernel launches.  Declarations and the full
 // contract of every entry point are in include/svp.h.
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -14,7 +13,6 @@
 namespace svp {
 
 static thread_local int t_last_launches = 0;
-static std::atomic<unsigned int> g_epoch{0};  // per-call ticket tags
 
 // ---- per-device facts, queried once ----
 struct DeviceInfo {
@@ -157,12 +155,11 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   plan->grid = (int)grid;
   plan->ctas_per_sm = ctas;
   plan->ws_head = 256;
-  plan->clear_tickets = groups > kTicketCap;
-  plan->ws_tickets = (size_t)(groups > kTicketCap ? groups : kTicketCap) * 8;
+  plan->ws_desc = align256((size_t)grid * 32);  // one SplitDesc per CTA
   plan->ws_part_o = align256((size_t)2 * grid * rb * head_dim * 4);
   plan->ws_part_lse = align256((size_t)2 * grid * rb * 4);
   plan->ws_total =
-      plan->ws_head + plan->ws_tickets + plan->ws_part_o + plan->ws_part_lse;
+      plan->ws_head + plan->ws_desc + plan->ws_part_o + plan->ws_part_lse;
   return SVP_OK;
 }
 
@@ -254,9 +251,10 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     return SVP_ERR_INVALID_ARG;
   if (dims->num_blocks == 0 || dims->max_blocks_per_seq == 0)
     return SVP_ERR_INVALID_ARG;
-  // pages move with 16-byte bulk copies and q with vector loads
+  // pages, q and out move with 16-byte bulk copies
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-       reinterpret_cast<uintptr_t>(v_cache)) % 16 != 0)
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) %
+          16 != 0)
     return SVP_ERR_INVALID_ARG;
   const int sms = device_sms();
   if (sms <= 0) return SVP_ERR_CUDA;
@@ -272,14 +270,9 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     st = owned_workspace(plan.ws_total, stream, &ws);
     if (st != SVP_OK) return st;
   }
+  // every CTA rewrites its split descriptor, so the workspace needs no
+  // clearing between calls
   char *wp = static_cast<char *>(ws);
-  // Ticket arrivals carry their launch's epoch, so stale tickets need no
-  // reset.  Only a call with more groups than the fixed ticket region clears
-  // its (larger) region, which other shapes' partials may have overwritten.
-  if (plan.clear_tickets &&
-      cudaMemsetAsync(wp + plan.ws_head, 0, plan.ws_tickets, stream) !=
-          cudaSuccess)
-    return SVP_ERR_CUDA;
   const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
   const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
   int launches = 0;
@@ -293,14 +286,10 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.seq_lens = seq_lens + b0;
     p.out = static_cast<char *>(out) + (size_t)b0 * q_len * row_elems * eb;
     p.lse = lse + (size_t)b0 * q_len * dims->num_q_heads;
-    p.tickets = reinterpret_cast<unsigned long long *>(wp + plan.ws_head);
-    // every launch has its own epoch: sub-launches index the same tickets
-    unsigned int epoch = g_epoch.fetch_add(1) + 1;
-    if (epoch == 0) epoch = g_epoch.fetch_add(1) + 1;
-    p.epoch = epoch;
-    p.part_o = reinterpret_cast<float *>(wp + plan.ws_head + plan.ws_tickets);
-    p.part_lse = reinterpret_cast<float *>(wp + plan.ws_head +
-                                           plan.ws_tickets + plan.ws_part_o);
+    p.desc = reinterpret_cast<SplitDesc *>(wp + plan.ws_head);
+    p.part_o = reinterpret_cast<float *>(wp + plan.ws_head + plan.ws_desc);
+    p.part_lse = reinterpret_cast<float *>(wp + plan.ws_head + plan.ws_desc +
+                                           plan.ws_part_o);
     p.batch = nb;
     p.num_q_heads = dims->num_q_heads;
     p.num_kv_heads = dims->num_kv_heads;
@@ -330,7 +319,10 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
         plan.tc ? launch_attention_tc(p, sub.grid, stream)
                 : launch_attention(p, dims->dtype, plan.mma, sub.grid, stream);
     if (e != cudaSuccess) return SVP_ERR_CUDA;
-    ++launches;
+    // groups split over several CTAs are finished by the merge kernel
+    if (launch_merge(p, dims->dtype, sub.grid, stream) != cudaSuccess)
+      return SVP_ERR_CUDA;
+    launches += 2;
   }
   t_last_launches = launches;
   return SVP_OK;

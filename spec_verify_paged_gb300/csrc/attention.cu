@@ -32,9 +32,9 @@
 //    read with ldmatrix.trans.  The running row sums stay per lane and are
 //    reduced once per unit.
 //  * The warps' states are merged by log-sum-exp at segment end.  A group
-//    split over several slices is finished by the CTA whose ticket arrives
-//    last; it merges all partials in slice order (deterministic).  No CTA
-//    ever waits for another.
+//    split over several slices leaves one partial per slice; the merge
+//    kernel (attn_common.cuh) combines them in slice order
+//    (deterministic).  No CTA ever waits for another.
 //  * Rows of a page that hold no valid data (positions >= seq_len, evicted
 //    stream rows) are zeroed in shared memory before P V, because p = 0
 //    times a NaN left in unused cache memory is still NaN.
@@ -116,7 +116,6 @@ struct Smem {
   float red_m[kConsumerWarps][RW];
   float red_l[kConsumerWarps][RW];
   float pbuf[kConsumerWarps][RW][kBlockSize];
-  float row_m[RB], row_w[RB];
   float wf[kConsumerWarps][RB];                    // per-warp row weights
   UnitInfo unit[kUnitRing];
   int stage_ok[C::STAGES];
@@ -124,7 +123,6 @@ struct Smem {
   uint64_t ufull[kUnitRing], uempty[kUnitRing];
   uint64_t epi;                                    // consumer-only barrier
   int abort_flag;
-  int is_last;
   int total_pages;                                 // flattened pages
   int n_ctas;                                      // CTAs sharing them
   int prefix[1];                                   // [batch + 1], dynamic
@@ -141,15 +139,10 @@ __device__ __forceinline__ void raise_flag(unsigned f) {
   atomicOr(&g_status_attn, f);
 }
 
-// Consumer-only barrier (4 warps) on an mbarrier: bounded.
+// Consumer-only barrier (4 warps) on an mbarrier: bounded, warp-uniform.
 template <typename S>
 __device__ __forceinline__ bool epi_sync(S &sm, uint32_t &phase, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&sm.epi);
-  bool ok = mbar_wait(&sm.epi, phase);
-  phase ^= 1u;
-  __syncwarp();
-  return ok;
+  return consumer_sync(&sm.epi, phase, lane);
 }
 
 // --------------------------------------------------------------------------
@@ -472,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&sm.epi, kConsumerWarps);
     sm.abort_flag = 0;
     fence_mbar_init();
+    p.desc[blockIdx.x].valid = 0;  // until this CTA starts a split group
   }
   if (warp == 0) {
     // pages of every sequence, times its groups (kv heads x row groups)
@@ -795,7 +789,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
         break;
       }
-      const int grp = (b * p.num_kv_heads + g) * p.n_rg + rg;
       // a group owned by one CTA is finished here; else a partial goes to
       // this CTA's first- or last-segment slot
       const bool single = ui.f == ui.l;
@@ -864,28 +857,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<float4 *>(p.part_o + prow * D + d) = a;
         }
       }
-      if (!single) {
-        __threadfence();
-        if (!epi_sync(sm, epi_phase, lane)) {
-          if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
-          break;
-        }
-        if (ctid == 0) sm.is_last = take_ticket(p, grp, ui.l - ui.f + 1);
-        if (!epi_sync(sm, epi_phase, lane)) {
-          if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
-          break;
-        }
-        if (sm.is_last) {
-          __threadfence();
-          if (!merge_partials<T, D, RB, kConsumerWarps * 32>(
-                  p, ui, total_pages, n_ctas, &sm.red_o[0][0][0],
-                  kConsumerWarps * RW * D, sm.row_m, sm.row_w, &sm.epi,
-                  epi_phase, ctid)) {
-            if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
-            break;
-          }
-        }
-      }
+      if (!single && ctid == 0) record_split(p, ui, blockIdx.x);
       // all consumers are done with this unit's info and scratch
       if (!epi_sync(sm, epi_phase, lane)) {
         if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
@@ -941,8 +913,8 @@ static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
   TensorMaps tm;
   memset(&tm, 0, sizeof tm);
   if constexpr (MMA) {
-    if (!make_kv_map(&tm.k, p.k_cache, p.num_blocks, p.num_kv_heads, D) ||
-        !make_kv_map(&tm.v, p.v_cache, p.num_blocks, p.num_kv_heads, D))
+    if (!cached_map(&tm.k, 0, p.k_cache, p.num_blocks, p.num_kv_heads, D) ||
+        !cached_map(&tm.v, 0, p.v_cache, p.num_blocks, p.num_kv_heads, D))
       return cudaErrorInvalidValue;
   }
   paged_attention_kernel<T, D, RB, MMA><<<grid, kThreads, smem, st>>>(p, tm);
@@ -1005,6 +977,32 @@ int attention_ctas_per_sm(int dtype, int head_dim, int rb, bool mma,
 }
 
 bool tensor_maps_available() { return encode_fn() != nullptr; }
+
+cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
+                         cudaStream_t stream) {
+#define SVP_MERGE(T, D, RB)                                            \
+  merge_splits_kernel<T, D, RB><<<grid, kMergeThreads, 0, stream>>>(p)
+  const bool f32 = dtype == 0;
+  const int D = p.head_dim;
+  switch (p.rb) {
+#define SVP_MERGE_RB(RB)                                             \
+  case RB:                                                           \
+    if (f32) { if (D == 64) SVP_MERGE(float, 64, RB); else SVP_MERGE(float, 128, RB); } \
+    else { if (D == 64) SVP_MERGE(uint16_t, 64, RB); else SVP_MERGE(uint16_t, 128, RB); } \
+    break;
+    SVP_MERGE_RB(1)
+    SVP_MERGE_RB(2)
+    SVP_MERGE_RB(4)
+    SVP_MERGE_RB(8)
+    SVP_MERGE_RB(16)
+    SVP_MERGE_RB(32)
+#undef SVP_MERGE_RB
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef SVP_MERGE
+  return cudaGetLastError();
+}
 
 cudaError_t read_status_attention(cudaStream_t s, unsigned *flags) {
   unsigned v = 0;

@@ -20,21 +20,33 @@
 // 128-byte-swizzled tiles.  Accumulators live in tensor memory (TMEM):
 // two S buffers and two O buffers of N columns, double-buffered by tile.
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warps 0-3  softmax and epilogue.  Thread k reads TMEM lane k: key k of
-//              the tile for S, head dim k for O.  Column statistics (row
-//              max and sum over the tile's keys) use a transposing warp
-//              butterfly and four-warp exchange in shared memory; P goes
-//              back to shared memory as bf16 in the MMA's swizzled layout.
-//              Each tile's O_t is folded into registers (o = o * alpha +
-//              O_t) while the tensor core works on the next tile.
-//   warp 4     producer: block table, 2-D TMA copies of 8 pages' K and V
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-7  softmax and epilogue, as two groups of four warps that take
+//              alternate tiles (group = tile parity), so one group's
+//              shuffles, exponentials and barriers overlap the other's.
+//              Thread k of a group reads TMEM lane k: key k of the tile for
+//              S, head dim k for O.  Column statistics (row max and sum
+//              over the tile's keys) use a transposing warp butterfly and a
+//              four-warp exchange in shared memory; P goes back to shared
+//              memory as bf16 in the MMA's swizzled layout.  Each group
+//              folds its tiles' O into registers (o = o * alpha + O_t) and
+//              keeps its own running max and sum; the two states are merged
+//              by log-sum-exp at the end of a segment.
+//   warp 8     producer: block table, 2-D TMA copies of 8 pages' K and V
 //              into a 3-stage ring.
-//   warp 5     one thread issues tcgen05.mma / tcgen05.commit.
-// Scheduling, split tickets and the merge are shared with attention.cu
-// (attn_common.cuh).  Every wait is bounded; a timeout raises
-// SVP_DEV_TIMEOUT and every role drains what it started before the CTA
-// frees its tensor memory.
+//   warp 9     one thread issues tcgen05.mma / tcgen05.commit, event
+//              driven: S of a tile as soon as its data and S buffer are
+//              free, P V as soon as its P is written, so stages go back to
+//              the producer without waiting for later tiles.
+// Synchronisation: mbarriers between roles (all waits bounded); named
+// barriers inside the softmax warps, where every timeout decision is made
+// uniform by an AND-reducing barrier (bar.red.and) before anyone acts on
+// it, so no warp can be left waiting at a barrier another warp has left.
+// A segment's Q is loaded before the previous segment's epilogue, so the
+// tensor core starts on the new segment while the softmax warps write the
+// old one out.  Scheduling and the merge of split groups are shared with
+// attention.cu (attn_common.cuh).  A timeout raises SVP_DEV_TIMEOUT and every role
+// drains what it started before the CTA frees its tensor memory.
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -54,10 +66,13 @@ constexpr int kTileKeys = kTilePages * kBlockSize;  // the MMA's M
 constexpr int kHalfBytes = kTileKeys * 128;  // 64 columns x 128 keys, bf16
 constexpr int kTileBytes = 2 * kHalfBytes;   // one K (or V) tile: 32 KB
 constexpr int kStages = 3;
-constexpr int kSoftWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kTcThreads = 32 * 6;
+constexpr int kGroups = 2;                  // softmax groups, by tile parity
+constexpr int kGroupThreads = 128;          // four warps: TMEM lanes 0-127
+constexpr int kSoftWarps = 4 * kGroups;
+constexpr int kProducerWarp = kSoftWarps;
+constexpr int kMmaWarp = kSoftWarps + 1;
+constexpr int kTcThreads = 32 * (kSoftWarps + 2);
+// named barriers (0 is __syncthreads): 1 + g for group g
 constexpr int kPageTxBytes = 2 * 2 * kBoxBytes;  // K and V, two boxes each
 constexpr int kTcBatchCap = 1024;  // sequences per launch (prefix in smem)
 
@@ -66,23 +81,25 @@ struct TcSmem {
   alignas(1024) unsigned char k[kStages][kTileBytes];
   alignas(1024) unsigned char v[kStages][kTileBytes];
   alignas(1024) unsigned char q[N * kD * 2];
-  alignas(1024) unsigned char pb[2][N * kTileKeys * 2];
-  alignas(16) float red_m[kSoftWarps][N];
-  alignas(16) float red_l[2][kSoftWarps][N];
-  alignas(16) float mu[N];        // the max each tile's p was taken against
-  alignas(16) float alpha[2][N];  // rescale of the running state by a tile
-  float row_inv[N];
-  float row_m[N], row_w[N];
+  alignas(1024) unsigned char pb[kGroups][N * kTileKeys * 2];  // P per group
+  alignas(16) float red_m[kGroups][4][N];
+  alignas(16) float red_l[kGroups][4][N];
+  alignas(16) float mu[kGroups][N];        // the max a tile's p was taken at
+  alignas(16) float alpha[kGroups][2][N];  // rescale of the state by a tile
+  alignas(16) float xs_m[2][N], xs_l[2][N];  // group 1's state per segment
+  alignas(16) float f0[N], f1[N];          // combine weights of the groups
+  alignas(16) float lse_st[N];             // a split partial's LSEs
   UnitInfo unit[kUnitRing];
   int stage_mask[kStages];  // bit k: page k of the tile was copied
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-  uint64_t q_full;
+  uint64_t s_full[kGroups], p_full[kGroups], o_full[kGroups];
+  uint64_t q_full, q_empty;
+  uint64_t x_full[2], x_empty[2];  // group 1 -> group 0 state hand-over
+  uint64_t stg_free;               // a segment's output left the P buffers
   uint64_t ufull[kUnitRing], uempty[kUnitRing];
-  uint64_t epi;
   uint64_t drain;
   uint32_t tmem_base;
-  int abort_flag, is_last, total_pages, n_ctas;
+  int abort_flag, total_pages, n_ctas;
   int prefix[1];  // [batch + 1], dynamic
 };
 
@@ -148,6 +165,34 @@ __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Non-blocking test of a phase's completion.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Named barrier over `count` threads that returns the AND of `ok` over
+// them: every participant leaves with the same answer.
+__device__ __forceinline__ bool bar_and(int id, int count, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // N consecutive 32-bit columns of this thread's TMEM lane.
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t addr, float (&v)[N]);
@@ -184,6 +229,42 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t addr, float (&v)[32]) {
       : "r"(addr));
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// N consecutive 32-bit columns into this thread's TMEM lane.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t addr, const float (&v)[N]);
+
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t addr,
+                                            const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,"
+      "%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(addr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+      "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]),
+      "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+      : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t addr,
+                                            const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,"
+      "%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,"
+      "%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+      "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]),
+      "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]),
+      "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]),
+      "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]),
+      "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Column reduction over the 32 keys (lanes) of a warp: each lane holds N
@@ -227,6 +308,13 @@ __device__ __forceinline__ uint32_t kmajor_off(int n, int k) {
                     ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2);
 }
 
+// K and V caches as 2-D tensors of 16-row pages; Q as rows of 128 dims.
+struct TcMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+  CUtensorMap q;
+};
+
 }  // namespace
 
 // --------------------------------------------------------------------------
@@ -235,11 +323,12 @@ __device__ __forceinline__ uint32_t kmajor_off(int n, int k) {
 template <int N>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_attention_tc_kernel(const AttnParams p,
-                              const __grid_constant__ TensorMaps tm) {
+                              const __grid_constant__ TcMaps tm) {
   extern __shared__ unsigned char smem_raw[];
   TcSmem<N> &sm = *reinterpret_cast<TcSmem<N> *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr uint32_t kTmemCols = 4 * N;  // S[2], O[2]
+  // S[group], O[group], X[2] (group 1's o handed to group 0), N columns each
+  constexpr uint32_t kTmemCols = 6 * N <= 128 ? 128 : 256;
   constexpr uint32_t kIdescS = idesc_bf16(kTileKeys, N, 0, 0);
   constexpr uint32_t kIdescO = idesc_bf16(kD, N, 1, 0);
 
@@ -253,21 +342,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int b2 = 0; b2 < 2; ++b2) {
-      mbar_init(&sm.s_full[b2], 1);
-      mbar_init(&sm.p_full[b2], kSoftWarps);
-      mbar_init(&sm.o_full[b2], 1);
-      mbar_init(&sm.o_free[b2], kSoftWarps);
+    for (int gi = 0; gi < kGroups; ++gi) {
+      mbar_init(&sm.s_full[gi], 1);
+      mbar_init(&sm.p_full[gi], 4);  // the group's warps
+      mbar_init(&sm.o_full[gi], 1);
     }
-    mbar_init(&sm.q_full, kSoftWarps);
+    mbar_init(&sm.q_full, 1);        // the producer's expect_tx + Q copies
+    mbar_init(&sm.q_empty, 1);       // the segment's last S MMA completed
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sm.x_full[k], 4);   // group 1's warps
+      mbar_init(&sm.x_empty[k], 4);  // group 0's warps
+    }
     for (int u = 0; u < kUnitRing; ++u) {
       mbar_init(&sm.ufull[u], 1);
-      mbar_init(&sm.uempty[u], 2);  // softmax warps and the MMA thread
+      mbar_init(&sm.uempty[u], 3);   // both softmax groups and the MMA thread
     }
-    mbar_init(&sm.epi, kSoftWarps);
+    mbar_init(&sm.stg_free, 1);      // group 0's storing thread
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
+    p.desc[blockIdx.x].valid = 0;    // until this CTA starts a split group
+  }
+  if (warp < kSoftWarps) {
+    // Q rows past a segment's valid rows are never copied: keep them zero
+    for (int i = tid; i < N * kD * 2 / 16; i += kSoftWarps * 32)
+      reinterpret_cast<uint4 *>(sm.q)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == kMmaWarp) {
     asm volatile(
@@ -301,6 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ======================= producer warp =======================
     int c = 0;   // tiles issued so far
     int us = 0;  // segments published so far
+    int q_issued = -1;  // last segment whose Q copies were issued
     bool ok = true;
     int pos = range_begin;
     while (true) {
@@ -323,6 +424,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sm.unit[slot] = seg;
         mbar_arrive(&sm.ufull[slot]);
       }
+      // Q of the segment's rows, one 128-byte box per half row, once the
+      // previous segment's last S MMA has read the old Q; tiles of this
+      // segment are issued meanwhile
+      bool q_pending = true;
+      auto issue_q = [&]() {
+        q_issued = us;
+        const int vr = min(N, p.rows - seg.rg * N);
+        if (lane == 0) mbar_arrive_expect_tx(&sm.q_full, vr * kD * 2);
+        __syncwarp();
+        if (lane < vr) {
+          const int gr = seg.rg * N + lane;
+          const int i = gr / p.group, h = seg.g * p.group + gr % p.group;
+          const int y = (seg.b * p.q_len + i) * p.num_q_heads + h;
+          tma_load_2d(sm.q + lane * 128, &tm.q, 0, y, &sm.q_full);
+          tma_load_2d(sm.q + N * 128 + lane * 128, &tm.q, kBoxElems, y,
+                      &sm.q_full);
+        }
+        q_pending = false;
+      };
       const int n_pages = seg.n_pages;
       for (int k0 = 0; k0 < n_pages && ok; k0 += kTableChunk) {
         // block-table entries of the next 128 pages, one coalesced load each
@@ -337,6 +457,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const int kend = min(k0 + kTableChunk, n_pages);
         for (int t0 = k0; t0 < kend; t0 += kTilePages) {
+          if (q_pending) {
+            const bool r = __shfl_sync(
+                kFull, lane == 0 && mbar_test(&sm.q_empty, (us & 1) ^ 1), 0);
+            if (r) issue_q();
+          }
           // tiles start at multiples of 8 pages of the segment; lane kk < 8
           // copies page t0 + kk, whose entry sits in lane (t0-k0)%32 + kk
           const int npg = min(kTilePages, n_pages - t0);
@@ -375,6 +500,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++c;
         }
       }
+      if (ok && q_pending) {
+        if (lane == 0) ok = mbar_wait(&sm.q_empty, (us & 1) ^ 1);
+        ok = __shfl_sync(kFull, ok, 0);
+        if (ok) issue_q();
+      }
       if (!ok) break;
       pos += n_pages;
       ++us;
@@ -385,72 +515,97 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       sm.abort_flag = 1;
       for (int k = max(0, c - kStages); k < c; ++k)
         (void)mbar_wait(&sm.full[k % kStages], (k / kStages) & 1);
+      if (q_issued >= 0) (void)mbar_wait(&sm.q_full, q_issued & 1);
     }
   } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer =======================
+    // ======================= MMA issuer (event driven) =======================
     if (lane == 0) {
       bool ok = true;
-      int c = 0, us = 0;
-      int pend = -1, pend_npg = 0;  // the tile whose P V is not issued yet
-      // O_t^T = V^T P^T over the tile's npg pages (16 keys per k-step)
-      auto issue_pv = [&](int t, int npg) -> bool {
-        const int b2 = t & 1;
-        if (!mbar_wait(&sm.p_full[b2], (t >> 1) & 1)) return false;
-        if (t >= 2 && !mbar_wait(&sm.o_free[b2], ((t - 2) >> 1) & 1))
-          return false;
-        tc_fence_after();
-        const int s = t % kStages;
-        const uint32_t va = smem_u32(sm.v[s]), pa = smem_u32(sm.pb[b2]);
-        for (int ks = 0; ks < npg; ++ks) {
-          // V as MN-major A: 64-dim halves kHalfBytes apart (leading byte
-          // offset), 8-key groups 1024 B apart (stride byte offset)
-          const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
-          const uint64_t b =
-              sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-          tc_mma(tmem + 2 * N + b2 * N, a, b, kIdescO, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(&sm.empty[s]);
-        tc_commit(&sm.o_full[b2]);
-        return true;
-      };
-      while (ok) {
-        const int slot = us % kUnitRing;
-        if (!mbar_wait(&sm.ufull[slot], (us / kUnitRing) & 1)) {
-          ok = false;
-          break;
-        }
-        const UnitInfo ui = sm.unit[slot];
-        mbar_arrive(&sm.uempty[slot]);
-        if (!ui.valid || sm.abort_flag) break;
-        const int tiles = (ui.n_pages + kTilePages - 1) / kTilePages;
-        for (int tau = 0; tau < tiles; ++tau, ++c) {
-          const int s = c % kStages, b2 = c & 1;
-          if (!mbar_wait(&sm.full[s], (c / kStages) & 1)) { ok = false; break; }
-          if (tau == 0) {
-            // finish the previous segment before waiting for this one's Q
-            if (pend >= 0 && !issue_pv(pend, pend_npg)) { ok = false; break; }
-            pend = -1;
-            if (!mbar_wait(&sm.q_full, us & 1)) { ok = false; break; }
+      int c_s = 0;    // next tile whose S is issued
+      int c_p = 0;    // next tile whose P V is issued
+      int p_obs = 0;  // tiles whose P is known to be written
+      int us = 0;     // segments taken from the ring
+      int left = 0, tau = 0, cur_pages = 0;
+      bool first = false, no_more = false;
+      int npg_ring[8];  // pages of tiles c_p .. c_s - 1 (at most 3)
+      uint64_t last = globaltimer();
+      while (true) {
+        bool prog = false;
+        // a new segment for the S side
+        if (left == 0 && !no_more &&
+            mbar_test(&sm.ufull[us % kUnitRing], (us / kUnitRing) & 1)) {
+          const UnitInfo ui = sm.unit[us % kUnitRing];
+          mbar_arrive(&sm.uempty[us % kUnitRing]);
+          ++us;
+          if (!ui.valid) {
+            no_more = true;
+          } else {
+            cur_pages = ui.n_pages;
+            left = (ui.n_pages + kTilePages - 1) / kTilePages;
+            tau = 0;
+            first = true;
           }
+          prog = true;
+        }
+        // S^T = K Q^T of tile c_s: its data is in, its group's S buffer was
+        // read (P of tile c_s - 2 written), its segment's Q is in
+        if (left > 0 && p_obs >= c_s - 1 &&
+            mbar_test(&sm.full[c_s % kStages], (c_s / kStages) & 1) &&
+            (!first || mbar_test(&sm.q_full, (us - 1) & 1))) {
           tc_fence_after();
-          // S^T = K Q^T: 8 k-steps of 16 head dims (32 B inside a 128-B row)
+          const int s = c_s % kStages, gi = c_s & 1;
           const uint32_t ka = smem_u32(sm.k[s]), qa = smem_u32(sm.q);
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ++ks) {
+            // 16 head dims per k-step: 32 B inside the 128-B swizzled rows
             const uint64_t a =
                 sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
             const uint64_t b =
                 sw128_desc(qa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-            tc_mma(tmem + b2 * N, a, b, kIdescS, ks > 0 ? 1u : 0u);
+            tc_mma(tmem + gi * N, a, b, kIdescS, ks > 0 ? 1u : 0u);
           }
-          tc_commit(&sm.s_full[b2]);
-          if (pend >= 0 && !issue_pv(pend, pend_npg)) { ok = false; break; }
-          pend = c;
-          pend_npg = min(kTilePages, ui.n_pages - tau * kTilePages);
+          tc_commit(&sm.s_full[gi]);
+          npg_ring[c_s & 7] = min(kTilePages, cur_pages - tau * kTilePages);
+          ++c_s;
+          ++tau;
+          --left;
+          first = false;
+          // the segment's last S: its Q may be replaced once this completes
+          if (left == 0) tc_commit(&sm.q_empty);
+          prog = true;
         }
-        ++us;
+        if (p_obs < c_s && mbar_test(&sm.p_full[p_obs & 1], (p_obs >> 1) & 1)) {
+          ++p_obs;
+          prog = true;
+        }
+        // O_t^T = V^T P^T of tile c_p over its pages (16 keys per k-step);
+        // the group read the previous O of this buffer before writing P
+        if (c_p < p_obs) {
+          tc_fence_after();
+          const int s = c_p % kStages, gi = c_p & 1;
+          const uint32_t va = smem_u32(sm.v[s]), pa = smem_u32(sm.pb[gi]);
+          const int npg = npg_ring[c_p & 7];
+          for (int ks = 0; ks < npg; ++ks) {
+            // V as MN-major A: 64-dim halves kHalfBytes apart (leading byte
+            // offset), 8-key groups 1024 B apart (stride byte offset)
+            const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
+            const uint64_t b =
+                sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+            tc_mma(tmem + (2 + gi) * N, a, b, kIdescO, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&sm.empty[s]);
+          tc_commit(&sm.o_full[gi]);
+          ++c_p;
+          prog = true;
+        }
+        if (no_more && left == 0 && c_p == c_s) break;
+        if (prog) {
+          last = globaltimer();
+        } else if (sm.abort_flag || globaltimer() - last > SVP_WAIT_NS) {
+          ok = false;
+          break;
+        }
       }
-      if (ok && pend >= 0) ok = issue_pv(pend, pend_npg);
       if (!ok) {
         raise_tc(SVP_DEV_TIMEOUT);
         sm.abort_flag = 1;
@@ -461,25 +616,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax warps =======================
-    const int ctid = tid;  // key of the tile (S), head dim (O)
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t epi_phase = 0;
-    int c = 0, us = 0;
-    bool aborted = false;
-    // O of tile t: wait, read, release the buffer, fold into o
+    // ======================= softmax groups =======================
+    // The two groups run independently: each takes the tiles of its parity
+    // in every segment; at a segment's end group 1 parks its state in
+    // tensor memory (X[segment & 1]) and moves on, group 0 merges it with
+    // its own and writes the segment out.
+    const int gi = warp >> 2;          // group: tiles of this parity
+    const int gw = warp & 3;           // warp in the group = TMEM lane quadrant
+    const int gt = tid & 127;          // key of the tile (S), head dim (O)
+    const int gbar = 1 + gi;
+    const uint32_t lane_base = (uint32_t)(gw * 32) << 16;
+    const uint32_t tS = tmem + lane_base + gi * N;
+    const uint32_t tO = tmem + lane_base + (2 + gi) * N;
+    int c0 = 0, us = 0;
+    bool ok = true;
+    // O of this group's tile t: wait, read, fold into o with alpha(t).
+    // Returns a warp-uniform success flag.
     auto fold_o = [&](int t, float (&o)[N]) -> bool {
-      const int b2 = t & 1;
-      const bool got = mbar_wait(&sm.o_full[b2], (t >> 1) & 1);
-      if (!__all_sync(kFull, got)) return false;
+      const bool got =
+          __all_sync(kFull, mbar_wait(&sm.o_full[gi], (t >> 1) & 1));
       tc_fence_after();
       float ov[N];
-      tmem_ld<N>(tmem + lane_base + 2 * N + b2 * N, ov);
+      tmem_ld<N>(tO, ov);
       tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[b2]);
-      const float4 *al = reinterpret_cast<const float4 *>(sm.alpha[b2]);
+      const float4 *al =
+          reinterpret_cast<const float4 *>(sm.alpha[gi][(t >> 1) & 1]);
 #pragma unroll
       for (int n4 = 0; n4 < N / 4; ++n4) {
         const float4 a = al[n4];
@@ -488,57 +649,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         o[4 * n4 + 2] = fmaf(o[4 * n4 + 2], a.z, ov[4 * n4 + 2]);
         o[4 * n4 + 3] = fmaf(o[4 * n4 + 3], a.w, ov[4 * n4 + 3]);
       }
-      return true;
+      return got;
     };
     while (true) {
       const int slot = us % kUnitRing;
-      const bool got =
-          __all_sync(kFull, mbar_wait(&sm.ufull[slot], (us / kUnitRing) & 1));
-      if (!got) { aborted = true; break; }
+      ok = mbar_wait(&sm.ufull[slot], (us / kUnitRing) & 1);
+      ok = bar_and(gbar, kGroupThreads, ok && !sm.abort_flag);
+      if (!ok) break;
       const UnitInfo ui = sm.unit[slot];
-      if (!ui.valid || sm.abort_flag) break;
+      if (!ui.valid) break;
       const int b = ui.b, g = ui.g, rg = ui.rg, L = ui.seq_len;
       const int t0 = L - p.q_len;
       const int vrows = min(N, p.rows - rg * N);
-
-      // ---- Q of the group -> shared memory (rows past vrows are zero) ----
-      for (int idx = ctid; idx < N * 16; idx += kSoftWarps * 32) {
-        const int n = idx >> 4, ch = idx & 15;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (n < vrows) {
-          const int gr = rg * N + n;
-          const int i = gr / p.group, h = g * p.group + gr % p.group;
-          val = __ldg(reinterpret_cast<const uint4 *>(
-                          static_cast<const uint16_t *>(p.q) +
-                          (((size_t)b * p.q_len + i) * p.num_q_heads + h) * kD) +
-                      ch);
-        }
-        *reinterpret_cast<uint4 *>(sm.q + kmajor_off<N>(n, ch * 8)) = val;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.q_full);
+      const int row0 = rg * N;  // first global row of the group's N rows
 
       float o[N];
 #pragma unroll
       for (int n = 0; n < N; ++n) o[n] = 0.f;
-      // running column statistics, kept by thread n < N for row n
+      // running statistics of column gt (thread gt < N of the group)
       float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
+      int prev = -1;  // this group's previous tile in the segment
       const int tiles = (ui.n_pages + kTilePages - 1) / kTilePages;
-      // first global row of this group: visibility bounds are row indices
-      const int row0 = rg * N;
-      for (int tau = 0; tau < tiles; ++tau, ++c) {
-        const int s = c % kStages, b2 = c & 1;
-        bool ok = mbar_wait(&sm.s_full[b2], (c >> 1) & 1);
-        ok = ok && mbar_wait(&sm.full[s], (c / kStages) & 1);
-        if (!__all_sync(kFull, ok)) { aborted = true; break; }
+      for (int tau = (c0 & 1) == gi ? 0 : 1; tau < tiles; tau += 2) {
+        const int c = c0 + tau;
+        const int s = c % kStages;
+        bool got = mbar_wait(&sm.s_full[gi], (c >> 1) & 1);
+        got = got && mbar_wait(&sm.full[s], (c / kStages) & 1);
         tc_fence_after();
         float sv[N];
-        tmem_ld<N>(tmem + lane_base + b2 * N, sv);
+        tmem_ld<N>(tS, sv);
         tc_wait_ld();
 
         // ---- this thread's key ----
-        const int kslot = ctid >> 4, r = ctid & 15;
+        const int kslot = gt >> 4, r = gt & 15;
         const int npg = min(kTilePages, ui.n_pages - tau * kTilePages);
         const bool loaded = ((sm.stage_mask[s] >> kslot) & 1) != 0;
         const int j =
@@ -546,17 +689,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // visible to some row of the call: holds real data
         const bool in_union = loaded && j < L &&
                               (p.window == 0 || j < p.n_sink || j > t0 - p.window);
-        if (kslot < npg && !in_union) {
+        if (got && kslot < npg && !in_union) {
           // p = 0 here, but 0 * NaN left in unused cache rows is still NaN
 #pragma unroll
           for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4 *>(sm.v[s] + bx * kHalfBytes + ctid * 128 +
+              *reinterpret_cast<uint4 *>(sm.v[s] + bx * kHalfBytes + gt * 128 +
                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
-        // rows n (of this group) that see key j: n in [nlo, nhi).  Row n is
-        // query position i = (row0 + n) / group, at t0 + i.
+        // rows n that see key j: n in [nlo, nhi); row n is query position
+        // i = (row0 + n) / group, at t0 + i
         int nlo = 0, nhi = N;
         if (!in_union) {
           nlo = N;
@@ -576,29 +719,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
         // ---- column max over the tile's 128 keys ----
         const float cm = col_reduce<N, true>(sv, lane);
-        if (N == 32 || (lane & 1) == 0) sm.red_m[warp][col_of<N>(lane)] = cm;
-        if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
-        if (ctid < N) {
-          const float mt = fmaxf(fmaxf(sm.red_m[0][ctid], sm.red_m[1][ctid]),
-                                 fmaxf(sm.red_m[2][ctid], sm.red_m[3][ctid]));
-          if (tau > 0) {
-            const int pb2 = b2 ^ 1;
+        if (N == 32 || (lane & 1) == 0) sm.red_m[gi][gw][col_of<N>(lane)] = cm;
+        ok = bar_and(gbar, kGroupThreads, ok && got);
+        if (!ok) break;
+        if (gt < N) {
+          const float mt = fmaxf(fmaxf(sm.red_m[gi][0][gt], sm.red_m[gi][1][gt]),
+                                 fmaxf(sm.red_m[gi][2][gt], sm.red_m[gi][3][gt]));
+          if (prev >= 0)
             l_run = fmaf(l_run, alpha_prev,
-                         (sm.red_l[pb2][0][ctid] + sm.red_l[pb2][1][ctid]) +
-                             (sm.red_l[pb2][2][ctid] + sm.red_l[pb2][3][ctid]));
-          }
+                         (sm.red_l[gi][0][gt] + sm.red_l[gi][1][gt]) +
+                             (sm.red_l[gi][2][gt] + sm.red_l[gi][3][gt]));
           const float m_new = fmaxf(m_run, mt);
           const float mu = m_new == -INFINITY ? 0.f : m_new;
           alpha_prev = ex2(m_run - mu);  // 0 while nothing was visible
           m_run = m_new;
-          sm.mu[ctid] = mu;
-          sm.alpha[b2][ctid] = alpha_prev;
+          sm.mu[gi][gt] = mu;
+          sm.alpha[gi][(c >> 1) & 1][gt] = alpha_prev;
         }
-        if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
+        named_bar(gbar, kGroupThreads);
 
-        // ---- p = exp2(s - mu), column sums, P -> shared memory (bf16) ----
+        // ---- p = exp2(s - mu) and the column sums ----
         {
-          const float4 *mu4 = reinterpret_cast<const float4 *>(sm.mu);
+          const float4 *mu4 = reinterpret_cast<const float4 *>(sm.mu[gi]);
 #pragma unroll
           for (int n4 = 0; n4 < N / 4; ++n4) {
             const float4 m4 = mu4[n4];
@@ -609,93 +751,137 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         const float cs = col_reduce<N, false>(sv, lane);
-        if (N == 32 || (lane & 1) == 0) sm.red_l[b2][warp][col_of<N>(lane)] = cs;
-        unsigned char *pbuf = sm.pb[b2];
+        if (N == 32 || (lane & 1) == 0) sm.red_l[gi][gw][col_of<N>(lane)] = cs;
+        // ---- the previous tile's O leaves the buffer before P is written:
+        // its P V has then finished reading this group's P buffer too ----
+        if (prev >= 0) ok = fold_o(prev, o) && ok;
+        // group 0 stages the previous segment's output in both P buffers:
+        // group 1 writes P again once the TMA engine has read it
+        if (gi == 1 && prev < 0 && us > 0)
+          ok = __all_sync(kFull, mbar_wait(&sm.stg_free, (us - 1) & 1)) && ok;
+        unsigned char *pbuf = sm.pb[gi];
 #pragma unroll
         for (int n = 0; n < N; ++n) {
           const __nv_bfloat16 h = __float2bfloat16_rn(sv[n]);
-          *reinterpret_cast<__nv_bfloat16 *>(pbuf + kmajor_off<N>(n, ctid)) = h;
+          *reinterpret_cast<__nv_bfloat16 *>(pbuf + kmajor_off<N>(n, gt)) = h;
         }
         fence_proxy_async_smem();  // P and zeroed V rows -> tensor core
-        tc_fence_before();         // S reads done before S is rewritten
+        tc_fence_before();         // S and O reads done before they are rewritten
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[b2]);
-
-        // ---- fold the previous tile's O while this tile's P V runs ----
-        if (tau > 0 && !fold_o(c - 1, o)) { aborted = true; break; }
+        if (lane == 0) mbar_arrive(&sm.p_full[gi]);
+        prev = c;
       }
-      if (aborted) break;
-      if (!fold_o(c - 1, o)) { aborted = true; break; }
-      // last tile's sums: every warp wrote them before its p_full arrival;
-      // a barrier makes them visible to the row threads
-      if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
-
-      // ---- epilogue ----
-      const bool single = ui.f == ui.l;
-      const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
-      if (ctid < N) {
-        const int lb2 = (c - 1) & 1;
+      // ---- the group's last tile (a warp whose last fold failed skips it;
+      // the vote below makes the outcome the group's) ----
+      if (ok && prev >= 0) ok = fold_o(prev, o);
+      // (also makes the last tile's column sums visible)
+      ok = bar_and(gbar, kGroupThreads, ok);
+      if (!ok) break;
+      if (gt < N && prev >= 0)
         l_run = fmaf(l_run, alpha_prev,
-                     (sm.red_l[lb2][0][ctid] + sm.red_l[lb2][1][ctid]) +
-                         (sm.red_l[lb2][2][ctid] + sm.red_l[lb2][3][ctid]));
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        sm.row_inv[ctid] = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse2 = l_run > 0.f ? mu + log2f(l_run) : -INFINITY;
-        if (ctid < vrows) {
-          const int gr = row0 + ctid;
+                     (sm.red_l[gi][0][gt] + sm.red_l[gi][1][gt]) +
+                         (sm.red_l[gi][2][gt] + sm.red_l[gi][3][gt]));
+      const int xk = us & 1;
+      const uint32_t tX = tmem + lane_base + (4 + xk) * N;
+      if (gi == 1) {
+        // ---- hand the state to group 0 (its copy of segment us - 2 must
+        // have been taken) and go on with the next segment ----
+        bool got = us < 2 || mbar_wait(&sm.x_empty[xk], ((us >> 1) - 1) & 1);
+        ok = bar_and(gbar, kGroupThreads, got);
+        if (!ok) break;
+        tc_fence_after();
+        tmem_st<N>(tX, o);
+        if (gt < N) { sm.xs_m[xk][gt] = m_run; sm.xs_l[xk][gt] = l_run; }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.x_full[xk]);
+      } else {
+        // ---- epilogue (group 0): merge the two groups' states; a group
+        // owned by one CTA is finished here, else a partial goes to this
+        // CTA's first- or last-segment slot ----
+        bool got = mbar_wait(&sm.x_full[xk], (us >> 1) & 1);
+        ok = bar_and(gbar, kGroupThreads, got);
+        if (!ok) break;
+        tc_fence_after();
+        float o1[N];
+        tmem_ld<N>(tX, o1);
+        tc_wait_ld();
+        const bool single = ui.f == ui.l;
+        const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
+        if (gt < N) {
+          const float m1 = sm.xs_m[xk][gt], l1 = sm.xs_l[xk][gt];
+          const float M = fmaxf(m_run, m1);
+          const float mr = M == -INFINITY ? 0.f : M;
+          const float w0 = ex2(m_run - mr), w1 = ex2(m1 - mr);
+          const float lt = w0 * l_run + w1 * l1;
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          sm.f0[gt] = w0 * inv;
+          sm.f1[gt] = w1 * inv;
+          const float lse2 = lt > 0.f ? mr + log2f(lt) : -INFINITY;
           if (single) {
-            const int i = gr / p.group, h = g * p.group + gr % p.group;
-            p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
+            if (gt < vrows) {
+              const int gr = row0 + gt;
+              const int i = gr / p.group, h = g * p.group + gr % p.group;
+              p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
+            }
           } else {
-            p.part_lse[pslot * N + ctid] = lse2;
+            sm.lse_st[gt] = lse2;
           }
         }
-      }
-      if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
+        // group 1's state is read: its slot may be reused
+        tc_fence_before();
+        named_bar(gbar, kGroupThreads);
+        if (lane == 0) mbar_arrive(&sm.x_empty[xk]);
+        // ---- the rows go out through the TMA engine, staged in the P
+        // buffers (every P V of the segment is done; group 1 writes P again
+        // after stg_free): plain stores would queue behind the KV stream of
+        // all SMs and stall this group for microseconds ----
+        float *stg32 = reinterpret_cast<float *>(&sm.pb[0][0]);  // [N][128]
+        __nv_bfloat16 *stg16 = reinterpret_cast<__nv_bfloat16 *>(&sm.pb[0][0]);
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
-        if (n < vrows) {
-          const float val = o[n] * sm.row_inv[n];
+        for (int n = 0; n < N; ++n) {
+          const float val = o[n] * sm.f0[n] + o1[n] * sm.f1[n];
+          if (single)
+            stg16[n * kD + gt] = __float2bfloat16_rn(val);
+          else
+            stg32[n * kD + gt] = val;
+        }
+        fence_proxy_async_smem();
+        named_bar(gbar, kGroupThreads);
+        if (gt == 0) {
           if (single) {
-            const int gr = row0 + n;
-            const int i = gr / p.group, h = g * p.group + gr % p.group;
-            store_out(static_cast<uint16_t *>(p.out) +
-                          (((size_t)b * p.q_len + i) * p.num_q_heads + h) * kD +
-                          ctid,
-                      val);
+            // one copy per query position: its rows are consecutive heads
+            for (int n = 0; n < vrows;) {
+              const int gr = row0 + n, i = gr / p.group;
+              const int n_end = min(vrows, (i + 1) * p.group - row0);
+              const int h = g * p.group + gr % p.group;
+              bulk_s2g(static_cast<uint16_t *>(p.out) +
+                           (((size_t)b * p.q_len + i) * p.num_q_heads + h) * kD,
+                       stg16 + n * kD, (uint32_t)(n_end - n) * kD * 2);
+              n = n_end;
+            }
           } else {
-            p.part_o[(pslot * N + n) * kD + ctid] = val;
+            bulk_s2g(p.part_o + pslot * N * kD, stg32, N * kD * 4);
+            bulk_s2g(p.part_lse + pslot * N, sm.lse_st, N * 4);
+            record_split(p, ui, blockIdx.x);
           }
+          bulk_commit();
+          bulk_wait_read();  // the staging area may be written again
+          mbar_arrive(&sm.stg_free);
         }
+        // f0 / f1 / the staging area are rewritten only after this barrier
+        named_bar(gbar, kGroupThreads);
       }
-      if (!single) {
-        __threadfence();
-        if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
-        if (ctid == 0)
-          sm.is_last = take_ticket(p, (b * p.num_kv_heads + g) * p.n_rg + rg,
-                                   ui.l - ui.f + 1);
-        if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
-        if (sm.is_last) {
-          __threadfence();
-          // the P buffers are idle between segments: merge scratch
-          if (!merge_partials<uint16_t, kD, N, kSoftWarps * 32>(
-                  p, ui, total_pages, n_ctas,
-                  reinterpret_cast<float *>(&sm.pb[0][0]),
-                  (int)(sizeof(sm.pb) / sizeof(float)), sm.row_m, sm.row_w,
-                  &sm.epi, epi_phase, ctid)) {
-            aborted = true;
-            break;
-          }
-        }
-      }
-      if (!consumer_sync(&sm.epi, epi_phase, lane)) { aborted = true; break; }
-      if (ctid == 0) mbar_arrive(&sm.uempty[slot]);
+      if (gt == 0) mbar_arrive(&sm.uempty[slot]);
+      c0 += tiles;
       ++us;
     }
-    if (aborted && lane == 0) {
+    if (!ok && gt == 0) {
       raise_tc(SVP_DEV_TIMEOUT);
       sm.abort_flag = 1;
     }
+    if (gi == 0 && gt == 0) bulk_wait();  // the output stores have landed
   }
 
   // no warp leaves while others may use the barriers; tensor memory is
@@ -749,10 +935,12 @@ template <int N>
 static cudaError_t launch_tc(const AttnParams &p, int grid, cudaStream_t st) {
   if (prepare_tc<N>(p.batch) < 0) return cudaErrorInvalidValue;
   const size_t smem = tc_smem_bytes<N>((int)tc_batch_bucket(p.batch));
-  TensorMaps tm;
+  TcMaps tm;
   memset(&tm, 0, sizeof tm);
-  if (!make_kv_map(&tm.k, p.k_cache, p.num_blocks, p.num_kv_heads, kD) ||
-      !make_kv_map(&tm.v, p.v_cache, p.num_blocks, p.num_kv_heads, kD))
+  if (!cached_map(&tm.k, 0, p.k_cache, p.num_blocks, p.num_kv_heads, kD) ||
+      !cached_map(&tm.v, 0, p.v_cache, p.num_blocks, p.num_kv_heads, kD) ||
+      !cached_map(&tm.q, 1, p.q, (long long)p.batch * p.q_len * p.num_q_heads,
+                  0, kD))
     return cudaErrorInvalidValue;
   paged_attention_tc_kernel<N><<<grid, kTcThreads, smem, st>>>(p, tm);
   return cudaGetLastError();

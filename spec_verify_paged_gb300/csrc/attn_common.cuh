@@ -6,13 +6,16 @@
 // (sequence b, kv head g, row group rg, visible page) items, sequence-major.
 // CTA c of the n_ctas working CTAs takes the slice [c*P/n, (c+1)*P/n) of the
 // P items ("stream-K"): every CTA reads the same number of pages whatever the
-// length mix.  A slice cut into one or more segments, each a run of pages of
-// a single group.  A group whose pages lie in several slices is finished by
-// the CTA whose ticket arrives last: each contributor writes a normalised
-// partial (o, log2-LSE) to its first- or last-segment slot, and the last one
-// merges them by log-sum-exp in slice order ("KV cache & Flash Attention",
-// section "FlashAttention -- the tiling trick": partial softmax states
-// combine exactly by rescaling with exp(m_i - m)).
+// length mix.  A slice cuts into one or more segments, each a run of pages
+// of a single group.  A group whose pages lie in several slices ("split")
+// is finished by a second, small kernel: each contributor writes a
+// normalised partial (o, log2-LSE) to its first- or last-segment slot, the
+// CTA that owns the group's first page records the group in its split
+// descriptor, and merge_splits_kernel combines the partials by log-sum-exp
+// in slice order ("KV cache & Flash Attention", section "FlashAttention --
+// the tiling trick": partial softmax states combine exactly by rescaling
+// with exp(m_i - m)).  No CTA waits for another and nothing in the
+// workspace has to start at zero: every CTA rewrites its descriptor.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,6 +50,13 @@ struct UnitInfo {
 struct TensorMaps {
   CUtensorMap k;
   CUtensorMap v;
+};
+
+// A split group whose first page this CTA owns: its partials sit in slot
+// f_slot of this CTA and slot 0 of CTAs blockIdx.x+1 .. l.
+struct SplitDesc {
+  int valid, b, g, rg;
+  int l, f_slot, pad0, pad1;
 };
 
 // Visible logical blocks of a sequence: [0, n_a) followed by
@@ -92,15 +102,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
 }
 
 // Barrier of the consumer warps on an mbarrier initialised with their
-// count: bounded, unlike bar.sync.
+// count: bounded, unlike bar.sync.  The result is the same in every lane of
+// the warp, so warp-wide operations after it never see a partial warp.
 __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &phase,
                                               int lane) {
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
-  bool ok = mbar_wait(bar, phase);
+  const bool ok = mbar_wait(bar, phase);
   phase ^= 1u;
-  __syncwarp();
-  return ok;
+  return __all_sync(kFull, ok);
 }
 
 // Warp 0: prefix[b + 1] = items of sequences 0..b (visible pages x groups
@@ -184,118 +194,111 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   return ui;
 }
 
-// One arrival on the group's ticket; true for the last contributor.  The
-// ticket's high word holds the epoch of the launch that last wrote it; a
-// ticket of another launch (or never written) counts as zero arrivals.
-__device__ __forceinline__ bool take_ticket(const AttnParams &p, int grp,
-                                            int n_contrib) {
-  unsigned long long *tk = p.tickets + grp;
-  unsigned long long seen = __ldcg(tk), want;
-  unsigned int before;
-  while (true) {
-    before = (unsigned int)(seen >> 32) == p.epoch ? (unsigned int)seen : 0u;
-    want = ((unsigned long long)p.epoch << 32) | (before + 1u);
-    const unsigned long long got = atomicCAS(tk, seen, want);
-    if (got == seen) break;
-    seen = got;
-  }
-  return before + 1u == (unsigned int)n_contrib;
+// The end of a segment on the split path: CTA `cta` wrote its partial; if
+// it owns the group's first page, it records the group for the merge.
+__device__ __forceinline__ void record_split(const AttnParams &p,
+                                             const UnitInfo &ui, int cta) {
+  if (ui.f != cta) return;
+  SplitDesc d;
+  d.valid = 1;
+  d.b = ui.b;
+  d.g = ui.g;
+  d.rg = ui.rg;
+  d.l = ui.l;
+  d.f_slot = ui.slot;
+  d.pad0 = d.pad1 = 0;
+  p.desc[cta] = d;
 }
 
-// The last contributor's merge of a group's partials, by NT consumer
-// threads (ctid 0..NT-1, NT/32 warps).  wts: shared scratch of wcap floats;
-// row_m / row_w: RB floats each.  Returns false if a barrier timed out.
-template <typename T, int D, int RB, int NT>
-__device__ __forceinline__ bool merge_partials(
-    const AttnParams &p, const UnitInfo &ui, int total, int n_ctas, float *wts,
-    int wcap, float *row_m, float *row_w, uint64_t *bar, uint32_t &phase,
-    int ctid) {
-  constexpr int NW = NT / 32;
-  const int lane = ctid & 31, warp = ctid >> 5;
-  const int rg = ui.rg, g = ui.g, b = ui.b;
-  // contributors are CTAs f..l in order; CTA f's partial sits in its
-  // last-segment slot when its slice began before this group
-  const int ns = ui.l - ui.f + 1;
-  const int f_begin = (int)((long long)ui.f * total / n_ctas);
-  const int f_tail = f_begin < ui.gstart ? 1 : 0;
-  auto prow_of = [&](int sidx) -> size_t {
-    return (size_t)(2 * (ui.f + sidx) + (sidx == 0 ? f_tail : 0));
-  };
-  const int vrows = min(RB, p.rows - rg * RB);
-  // per-row max and weight sum over the splits (warp w: rows w, w+NW, ...)
-  for (int r = warp; r < vrows; r += NW) {
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32)
-      M = fmaxf(M, __ldcg(p.part_lse + prow_of(s) * RB + r));
-#pragma unroll
-    for (int off = 16; off; off >>= 1)
-      M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    float W = 0.f;
-    if (M != -INFINITY)
-      for (int s = lane; s < ns; s += 32)
-        W += ex2(__ldcg(p.part_lse + prow_of(s) * RB + r) - M);
-#pragma unroll
-    for (int off = 16; off; off >>= 1)
-      W += __shfl_xor_sync(kFull, W, off);
-    if (lane == 0) { row_m[r] = M; row_w[r] = W; }
-  }
-  if (!consumer_sync(bar, phase, lane)) return false;
-  // normalised split weights go to shared memory, CH splits at a time; each
-  // thread then sums float4 slices of the partial outputs with independent
-  // loads (an empty split has lse2 = -inf and weight 0)
-  const int CH = wcap / RB;
-  constexpr int NE4 = RB * D / 4;
-  constexpr int EPT = (NE4 + NT - 1) / NT;
+// Merge of split groups: CTA c finishes the group recorded in desc[c] (if
+// any) from the partials of CTAs c..l.  Each thread owns float4 slices of
+// a few rows and folds the splits in with an online log-sum-exp, kMergeUnroll
+// splits at a time: all their loads are issued together, so a typical group
+// (two to four splits) costs one memory round trip.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeUnroll = 4;
+
+template <typename T, int D, int RB>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_splits_kernel(const AttnParams p) {
+  const SplitDesc dsc = p.desc[blockIdx.x];
+  if (!dsc.valid) return;
+  const int tid = threadIdx.x;
+  const int f = blockIdx.x;
+  const int ns = dsc.l - f + 1;
+  const int vrows = min(RB, p.rows - dsc.rg * RB);
+  constexpr int NE4 = RB * D / 4;  // float4 slices of the group's rows
+  constexpr int EPT = (NE4 + kMergeThreads - 1) / kMergeThreads;
   const float4 *po4 = reinterpret_cast<const float4 *>(p.part_o);
+  float m[EPT], w_sum[EPT];
   float4 acc[EPT];
 #pragma unroll
-  for (int k = 0; k < EPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += CH) {
-    const int cn = min(CH, ns - s0);
-#pragma unroll 4
-    for (int idx = ctid; idx < cn * RB; idx += NT) {
-      const int s = s0 + idx / RB, r = idx % RB;
-      const float ls = __ldcg(p.part_lse + prow_of(s) * RB + r);
-      const float w = r < vrows ? ex2(ls - row_m[r]) / row_w[r] : 0.f;
-      wts[idx] = w;
-    }
-    if (!consumer_sync(bar, phase, lane)) return false;
+  for (int k = 0; k < EPT; ++k) {
+    m[k] = -INFINITY;
+    w_sum[k] = 0.f;
+    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s0 = 0; s0 < ns; s0 += kMergeUnroll) {
+    float ls[EPT][kMergeUnroll];
+    float4 v[EPT][kMergeUnroll];
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
-      const int e4 = ctid + k * NT;
-      if (e4 >= vrows * (D / 4)) continue;
+      const int e4 = tid + k * kMergeThreads;
       const int r = e4 / (D / 4), d4 = e4 % (D / 4);
+#pragma unroll
+      for (int j = 0; j < kMergeUnroll; ++j) {
+        const int s = s0 + j;
+        ls[k][j] = -INFINITY;
+        v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e4 < NE4 && r < vrows && s < ns) {
+          // CTA f's partial sits in its f_slot; later CTAs' in slot 0
+          const size_t prow = (size_t)(2 * (f + s) + (s == 0 ? dsc.f_slot : 0));
+          ls[k][j] = p.part_lse[prow * RB + r];
+          v[k][j] = po4[(prow * RB + r) * (D / 4) + d4];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      float mn = m[k];
+#pragma unroll
+      for (int j = 0; j < kMergeUnroll; ++j) mn = fmaxf(mn, ls[k][j]);
+      if (mn == -INFINITY) continue;  // nothing visible yet (or padding)
+      const float sc = ex2(m[k] - mn);  // 0 while m[k] is -inf
       float4 a = acc[k];
-#pragma unroll 8
-      for (int s = 0; s < cn; ++s) {
-        const float w = wts[s * RB + r];
-        const float4 v = __ldcg(po4 + (prow_of(s0 + s) * RB + r) * (D / 4) + d4);
-        a.x = fmaf(w, v.x, a.x);
-        a.y = fmaf(w, v.y, a.y);
-        a.z = fmaf(w, v.z, a.z);
-        a.w = fmaf(w, v.w, a.w);
+      a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+      float ws = w_sum[k] * sc;
+#pragma unroll
+      for (int j = 0; j < kMergeUnroll; ++j) {
+        const float w = ex2(ls[k][j] - mn);  // 0 for an empty split
+        ws += w;
+        a.x = fmaf(w, v[k][j].x, a.x);
+        a.y = fmaf(w, v[k][j].y, a.y);
+        a.z = fmaf(w, v[k][j].z, a.z);
+        a.w = fmaf(w, v[k][j].w, a.w);
       }
       acc[k] = a;
+      w_sum[k] = ws;
+      m[k] = mn;
     }
-    if (!consumer_sync(bar, phase, lane)) return false;
   }
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
-    const int e4 = ctid + k * NT;
-    if (e4 >= vrows * (D / 4)) continue;
+    const int e4 = tid + k * kMergeThreads;
     const int r = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
-    const int gr = rg * RB + r;
+    if (e4 >= NE4 || r >= vrows) continue;
+    const float inv = w_sum[k] > 0.f ? 1.f / w_sum[k] : 0.f;
+    const int gr = dsc.rg * RB + r;
     const int i = gr / p.group;
-    const int h = g * p.group + gr % p.group;
-    const size_t row = ((size_t)b * p.q_len + i) * p.num_q_heads + h;
+    const int h = dsc.g * p.group + gr % p.group;
+    const size_t row = ((size_t)dsc.b * p.q_len + i) * p.num_q_heads + h;
     T *dst = static_cast<T *>(p.out) + row * D + d;
-    store_out(dst + 0, acc[k].x);
-    store_out(dst + 1, acc[k].y);
-    store_out(dst + 2, acc[k].z);
-    store_out(dst + 3, acc[k].w);
-    if (d == 0) p.lse[row] = (row_m[r] + log2f(row_w[r])) * kLn2;
+    store_out(dst + 0, acc[k].x * inv);
+    store_out(dst + 1, acc[k].y * inv);
+    store_out(dst + 2, acc[k].z * inv);
+    store_out(dst + 3, acc[k].w * inv);
+    if (d == 0) p.lse[row] = (m[k] + log2f(w_sum[k])) * kLn2;
   }
-  return true;
 }
 
 // ---- host side ----
@@ -337,6 +340,64 @@ inline bool make_kv_map(CUtensorMap *map, const void *base, int num_blocks,
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A row-major bf16 matrix [rows, d] as a 2-D tensor copied one row (of
+// 64-column, 128-byte-swizzled halves) per box.
+inline bool make_row_map(CUtensorMap *map, const void *base, long long rows,
+                         int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBoxElems, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoded tensor maps of recent calls, keyed by everything they encode
+// (kind 0: make_kv_map(base, a = num_blocks, b = hkv, d); kind 1:
+// make_row_map(base, a = rows, d)), so repeated calls on the same buffers
+// skip the driver's encoder.
+inline bool cached_map(CUtensorMap *map, int kind, const void *base,
+                       long long a, int b, int d) {
+  struct Entry {
+    int kind, b, d;
+    const void *base;
+    long long a;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static std::mutex mu;
+  static Entry cache[kEntries];
+  static int filled = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < filled; ++i) {
+      const Entry &e = cache[i];
+      if (e.kind == kind && e.base == base && e.a == a && e.b == b && e.d == d) {
+        *map = e.map;
+        return true;
+      }
+    }
+  }
+  const bool ok = kind == 0 ? make_kv_map(map, base, (int)a, b, d)
+                            : make_row_map(map, base, a, d);
+  if (!ok) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  Entry &e = cache[next];
+  e.kind = kind;
+  e.b = b;
+  e.d = d;
+  e.base = base;
+  e.a = a;
+  e.map = *map;
+  next = (next + 1) % kEntries;
+  if (filled < kEntries) ++filled;
+  return true;
 }
 
 }  // namespace svp

@@ -103,6 +103,27 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src,
       : "memory");
 }
 
+// 1-D bulk copy shared -> global (TMA engine), tracked in the issuing
+// thread's bulk group; both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem,
+                                         uint32_t bytes) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+      "r"(smem_u32(src_smem)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory sources of this thread's bulk stores have been read.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"

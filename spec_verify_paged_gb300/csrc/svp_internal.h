@@ -7,6 +7,8 @@
 
 namespace svp {
 
+struct SplitDesc;
+
 constexpr int kBlockSize = 16;     // tokens per KV page
 constexpr int kMaxQLen = 16;
 constexpr int kMaxBatch = 65535;
@@ -22,8 +24,7 @@ struct AttnParams {
   void *out;
   float *lse;
   // workspace pieces
-  unsigned long long *tickets;  // [batch * Hkv * n_rg] arrivals per group:
-                                // (epoch << 32) | count
+  struct SplitDesc *desc;  // [grid] split group whose first page a CTA owns
   float *part_o;       // [2 * grid][RB][D] normalised partials: each CTA's
                        // first- and last-segment slot
   float *part_lse;     // [2 * grid][RB] log2-domain LSE of the partials
@@ -34,21 +35,15 @@ struct AttnParams {
   int rb;              // rows per work unit (row-group size)
   int n_rg;            // ceil(rows / rb)
   int min_pages;       // fewest pages a CTA's slice may hold
-  unsigned int epoch;  // this launch's tag for ticket arrivals (never 0)
   float qscale;        // scale * log2(e)
 };
-
-// Tickets of calls with at most this many groups live at a fixed offset, so
-// no other call's partials ever land on them; bigger calls clear theirs.
-constexpr long long kTicketCap = 65536;
 
 struct AttnPlan {
   int rb, n_rg, min_pages, grid, ctas_per_sm;
   bool mma;            // warp-level mma.sync path
   bool tc;             // tcgen05 path (tensor-memory accumulators)
   int batch_cap;       // sequences per launch
-  bool clear_tickets;  // more groups than the fixed ticket region holds
-  size_t ws_head, ws_tickets, ws_part_o, ws_part_lse, ws_total;
+  size_t ws_head, ws_desc, ws_part_o, ws_part_lse, ws_total;
 };
 
 // Fills the plan (no CUDA launches).  dtype 0 = f32, 1 = bf16.  Returns 0 or
@@ -70,6 +65,10 @@ int attention_ctas_per_sm(int dtype, int head_dim, int rb, bool mma,
 
 cudaError_t launch_attention(const AttnParams &p, int dtype, bool mma,
                              int grid, cudaStream_t stream);
+
+// The merge of split groups after either attention kernel (same grid).
+cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
+                         cudaStream_t stream);
 
 // True when the driver provides cuTensorMapEncodeTiled.
 bool tensor_maps_available();

@@ -102,16 +102,15 @@ def test_workspace_too_small(lib):
 
 
 def test_workspace_size_grows_with_work(lib):
-    """Header + one ticket per (sequence, kv head, row group) + two partial
-    slots per CTA: more sequences need more, a window never needs more."""
+    """Header + one split descriptor and two partial slots per CTA of the
+    grid: more work never needs less, a window never needs more."""
     small = lib.paged_decode_workspace_size(ctypes.byref(_dims()), 1, 0, 0)
-    many = dict(batch=4096, num_q_heads=64, num_kv_heads=64,
-                max_blocks_per_seq=512)     # 262144 groups > fixed tickets
+    many = dict(batch=4096, max_blocks_per_seq=512)  # same heads and rows
     big = lib.paged_decode_workspace_size(ctypes.byref(_dims(**many)), 1, 0, 0)
     win = lib.paged_decode_workspace_size(ctypes.byref(_dims(**many)), 1, 4, 64)
-    assert 0 < small < big and win <= big
-    # the fixed ticket region (65536 x 8 bytes) is always there
-    assert small >= 256 + 65536 * 8
+    assert 0 < small <= big and win <= big
+    # header (256) + descriptors (256-aligned) + one slot pair of head_dim
+    assert small >= 256 + 256 + 2 * 128 * 4
     assert lib.paged_decode_workspace_size(None, 1, 0, 0) == 0
     assert lib.paged_decode_workspace_size(ctypes.byref(_dims(head_dim=80)),
                                            1, 0, 0) == 0

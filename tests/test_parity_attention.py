@@ -227,8 +227,8 @@ def test_bad_seq_len_is_flagged(svp):
 
 
 def test_repeated_calls_reuse_workspace(svp, oracle_mod):
-    """Counters in the workspace return to zero after every call: ten calls in
-    a row on the same workspace give identical results."""
+    """Nothing in the workspace carries over between calls: ten calls in a
+    row on the same workspace give identical results."""
     import torch
     cfg = W.small_config(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=128,
                          q_len=2, ctx_min=100, ctx_max=800, seed=5)
@@ -248,8 +248,9 @@ def test_repeated_calls_reuse_workspace(svp, oracle_mod):
 
 
 def test_workspace_shared_across_shapes(svp, oracle_mod):
-    """One workspace serves calls of different shapes in any order: a small
-    call, a call with many more split tickets, then the small call again."""
+    """One workspace, filled with junk first, serves calls of different
+    shapes in any order: a small call, a call with many more split groups,
+    then the small call again."""
     import torch
     ws = torch.full((64 << 20,), 0x5A, dtype=torch.uint8, device="cuda:0")
     shapes = [dict(batch=2, num_q_heads=8, num_kv_heads=2, q_len=2, ctx_max=900),
@@ -271,12 +272,13 @@ def test_workspace_shared_across_shapes(svp, oracle_mod):
 @pytest.mark.parametrize("path,batch", [(1, 4100), (3, 1030)])
 def test_many_sequences_span_launches(svp, oracle_mod, path, batch):
     """More sequences than one launch takes (4096 on CUDA cores, 1024 on
-    tcgen05): the call makes two launches on one workspace, with groups
-    split over several CTAs in both; every output matches the oracle."""
+    tcgen05): the call makes two attention launches on one workspace, each
+    followed by its merge, with groups split over several CTAs in both;
+    every output matches the oracle."""
     cfg = W.small_config(batch=batch, num_q_heads=4, num_kv_heads=1,
                          head_dim=128, q_len=2, ctx_min=2, ctx_max=70,
                          seed=61)
     wl = W.make_attention(cfg)
     got = _run_gpu(svp, wl, 0, 0, split_pages=1, kernel_path=path)
-    assert svp.last_launch_count() == 2
+    assert svp.last_launch_count() == 4  # two attention + two merge launches
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
