@@ -152,6 +152,7 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   plan->tc = tc;
   plan->batch_cap = tc ? tc_batch_cap() : kBatchPerLaunch;
   plan->min_pages = min_pages;
+  plan->seg_items = tc ? kSegItemsTc : 0;
   plan->grid = (int)grid;
   plan->ctas_per_sm = ctas;
   plan->ws_head = 256;
@@ -167,11 +168,12 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
 // in shared memory) and few enough that the flattened page count fits in
 // 32 bits.
 static int batch_per_launch(const svp_dims *d, int q_len, int n_sink,
-                            int window, int cap) {
+                            int window, int cap, int seg_items) {
   const long long rows = (long long)(d->num_q_heads / d->num_kv_heads) * q_len;
   const long long per_seq =
       (long long)d->num_kv_heads * rows *
-      max_visible_pages(d->max_blocks_per_seq, q_len, n_sink, window);
+      (max_visible_pages(d->max_blocks_per_seq, q_len, n_sink, window) +
+       seg_items);
   long long bl = per_seq > 0 ? ((1LL << 31) - 1) / per_seq : cap;
   if (bl > cap) bl = cap;
   if (bl > d->batch) bl = d->batch;
@@ -188,7 +190,8 @@ static int plan_call(const svp_dims *d, int q_len, int n_sink, int window,
                                d->num_blocks, d->num_kv_heads);
   if (path < 0) return path;
   const int cap = path == SVP_PATH_TCGEN05 ? tc_batch_cap() : kBatchPerLaunch;
-  const int bl = batch_per_launch(d, q_len, n_sink, window, cap);
+  const int bl = batch_per_launch(d, q_len, n_sink, window, cap,
+                                  path == SVP_PATH_TCGEN05 ? kSegItemsTc : 0);
   const int st = plan_attention(bl, d->num_q_heads, d->num_kv_heads,
                                 d->head_dim, d->dtype, d->max_blocks_per_seq,
                                 q_len, n_sink, window, d->split_pages, path,
@@ -304,6 +307,7 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.rb = plan.rb;
     p.n_rg = plan.n_rg;
     p.min_pages = plan.min_pages;
+    p.seg_items = plan.seg_items;
     p.qscale = scale * 1.4426950408889634f;
     AttnPlan sub = plan;
     if (nb != bl) {

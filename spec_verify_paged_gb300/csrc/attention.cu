@@ -465,8 +465,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&sm.epi, kConsumerWarps);
     sm.abort_flag = 0;
     fence_mbar_init();
-    p.desc[blockIdx.x].valid = 0;  // until this CTA starts a split group
   }
+  // launched early (programmatic dependent launch): nothing in global
+  // memory is touched before the previous kernel on the stream is done
+  pdl_wait();
+  if (tid == 0) p.desc[blockIdx.x].valid = 0;  // until a split group starts
   if (warp == 0) {
     // pages of every sequence, times its groups (kv heads x row groups)
     const int run = build_prefix(p, sm.prefix, groups_per_seq, lane,
@@ -477,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   __syncthreads();
+  if (tid == 0) pdl_launch_dependents();  // the merge may be scheduled
   const int total_pages = sm.total_pages;
   const int n_ctas = sm.n_ctas;
   // this CTA's slice of the flattened (sequence, group, page) space
@@ -497,16 +501,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         ok = mbar_wait(&sm.uempty[slot], ((us / kUnitRing) & 1) ^ 1);
       ok = __shfl_sync(kFull, ok, 0) && !sm.abort_flag;
       if (!ok) break;
-      if (pos >= range_end) {
+      const UnitInfo seg =
+          pos < range_end
+              ? decode_segment(p, sm.prefix, groups_per_seq, pos, us == 0,
+                               range_end, total_pages, n_ctas)
+              : UnitInfo{};
+      if (!seg.valid) {
         if (lane == 0) {
           sm.unit[slot].valid = 0;
           mbar_arrive(&sm.ufull[slot]);
         }
         break;
       }
-      const UnitInfo seg =
-          decode_segment(p, sm.prefix, groups_per_seq, pos, range_begin,
-                         range_end, total_pages, n_ctas);
       const int b = seg.b, g = seg.g, n_pages = seg.n_pages;
       const int page0 = seg.page0, na = seg.n_a, bs = seg.b_start;
       if (lane == 0) {
@@ -571,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (!ok) break;
-      pos += n_pages;
+      pos = seg.item0 + seg.n_pages;
       ++us;
     }
     if (!ok) {
@@ -917,8 +923,8 @@ static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
         !cached_map(&tm.v, 0, p.v_cache, p.num_blocks, p.num_kv_heads, D))
       return cudaErrorInvalidValue;
   }
-  paged_attention_kernel<T, D, RB, MMA><<<grid, kThreads, smem, st>>>(p, tm);
-  return cudaGetLastError();
+  return launch_pdl(paged_attention_kernel<T, D, RB, MMA>, (unsigned)grid,
+                    (unsigned)kThreads, smem, st, p, tm);
 }
 
 #define SVP_DISPATCH(DTYPE, HD, RB, MMA, CALL)                        \
@@ -981,9 +987,11 @@ bool tensor_maps_available() { return encode_fn() != nullptr; }
 cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
                          cudaStream_t stream) {
 #define SVP_MERGE(T, D, RB)                                            \
-  merge_splits_kernel<T, D, RB><<<grid, kMergeThreads, 0, stream>>>(p)
+  e = launch_pdl(merge_splits_kernel<T, D, RB>, (unsigned)grid,         \
+                 (unsigned)kMergeThreads, 0, stream, p)
   const bool f32 = dtype == 0;
   const int D = p.head_dim;
+  cudaError_t e = cudaSuccess;
   switch (p.rb) {
 #define SVP_MERGE_RB(RB)                                             \
   case RB:                                                           \
@@ -1001,7 +1009,7 @@ cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
       return cudaErrorInvalidValue;
   }
 #undef SVP_MERGE
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t read_status_attention(cudaStream_t s, unsigned *flags) {

@@ -361,7 +361,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    p.desc[blockIdx.x].valid = 0;    // until this CTA starts a split group
   }
   if (warp < kSoftWarps) {
     // Q rows past a segment's valid rows are never copied: keep them zero
@@ -378,6 +377,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
                      : "memory");
   }
+  // launched early (programmatic dependent launch): nothing in global
+  // memory is touched before the previous kernel on the stream is done
+  pdl_wait();
+  if (tid == 0) p.desc[blockIdx.x].valid = 0;  // until a split group starts
   if (warp == 0) {
     const int run = build_prefix(p, sm.prefix, groups_per_seq, lane,
                                  &g_status_attn_tc);
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) pdl_launch_dependents();  // the merge may be scheduled
   const uint32_t tmem = sm.tmem_base;
   const int total_pages = sm.total_pages;
   const int n_ctas = sm.n_ctas;
@@ -410,16 +414,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = mbar_wait(&sm.uempty[slot], ((us / kUnitRing) & 1) ^ 1);
       ok = __shfl_sync(kFull, ok, 0) && !sm.abort_flag;
       if (!ok) break;
-      if (pos >= range_end) {
+      const UnitInfo seg =
+          pos < range_end
+              ? decode_segment(p, sm.prefix, groups_per_seq, pos, us == 0,
+                               range_end, total_pages, n_ctas)
+              : UnitInfo{};
+      if (!seg.valid) {
         if (lane == 0) {
           sm.unit[slot].valid = 0;
           mbar_arrive(&sm.ufull[slot]);
         }
         break;
       }
-      const UnitInfo seg =
-          decode_segment(p, sm.prefix, groups_per_seq, pos, range_begin,
-                         range_end, total_pages, n_ctas);
       if (lane == 0) {
         sm.unit[slot] = seg;
         mbar_arrive(&sm.ufull[slot]);
@@ -506,7 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok) issue_q();
       }
       if (!ok) break;
-      pos += n_pages;
+      pos = seg.item0 + seg.n_pages;
       ++us;
     }
     if (!ok && lane == 0) {
@@ -942,8 +948,8 @@ static cudaError_t launch_tc(const AttnParams &p, int grid, cudaStream_t st) {
       !cached_map(&tm.q, 1, p.q, (long long)p.batch * p.q_len * p.num_q_heads,
                   0, kD))
     return cudaErrorInvalidValue;
-  paged_attention_tc_kernel<N><<<grid, kTcThreads, smem, st>>>(p, tm);
-  return cudaGetLastError();
+  return launch_pdl(paged_attention_tc_kernel<N>, (unsigned)grid,
+                    (unsigned)kTcThreads, smem, st, p, tm);
 }
 
 int tc_batch_cap() { return kTcBatchCap; }

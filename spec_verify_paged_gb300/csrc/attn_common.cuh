@@ -3,10 +3,12 @@
 // attention_tc.cu: tcgen05 consumers with tensor-memory accumulators).
 //
 // Scheduling (both kernels): the work of a call is the flattened list of
-// (sequence b, kv head g, row group rg, visible page) items, sequence-major.
-// CTA c of the n_ctas working CTAs takes the slice [c*P/n, (c+1)*P/n) of the
-// P items ("stream-K"): every CTA reads the same number of pages whatever the
-// length mix.  A slice cuts into one or more segments, each a run of pages
+// (sequence b, kv head g, row group rg, visible page) items, sequence-major,
+// where every group starts with p.seg_items items that stand for the fixed
+// cost of a segment (they hold no page).  CTA c of the n_ctas working CTAs
+// takes the slice [c*P/n, (c+1)*P/n) of the P items ("stream-K"): every CTA
+// gets the same amount of work whatever the length mix, a CTA that cuts
+// through many groups a few pages less.  A slice cuts into one or more segments, each a run of pages
 // of a single group.  A group whose pages lie in several slices ("split")
 // is finished by a second, small kernel: each contributor writes a
 // normalised partial (o, log2-LSE) to its first- or last-segment slot, the
@@ -42,7 +44,7 @@ constexpr int kBoxBytes = kBlockSize * 128;
 // the CTA's first (0) or last (1) segment, which is where its partial goes.
 struct UnitInfo {
   int b, g, rg, slot;
-  int f, l, gstart, page0;
+  int f, l, item0, page0;  // item0: flat item of page0
   int n_pages, seq_len, n_a, b_start;
   int valid, pad0, pad1, pad2;
 };
@@ -131,7 +133,7 @@ __device__ __forceinline__ int build_prefix(const AttnParams &p, int *prefix,
       } else {
         int na, bs, np;
         visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
-        n = np * groups_per_seq;
+        n = (np + p.seg_items) * groups_per_seq;
       }
     }
     int incl = n;
@@ -158,13 +160,15 @@ __device__ __forceinline__ int slice_begin(int cta, int total, int n_ctas) {
   return cta < n_ctas ? (int)((long long)cta * total / n_ctas) : total;
 }
 
-// The segment that starts at flat item `pos` of this CTA's slice.
+// The first segment with pages at or after flat item `pos` of this CTA's
+// slice (valid = 0 if the rest of the slice holds none); the next segment
+// starts at item0 + n_pages.  `first`: no segment of this slice came
+// before (its partial goes to slot 0, any later one to slot 1).
 __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
                                                    const int *prefix,
                                                    int groups_per_seq, int pos,
-                                                   int range_begin,
-                                                   int range_end, int total,
-                                                   int n_ctas) {
+                                                   bool first, int range_end,
+                                                   int total, int n_ctas) {
   int lo = 0, hi = p.batch;  // b with prefix[b] <= pos < prefix[b + 1]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -172,25 +176,28 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   }
   UnitInfo ui;
   const int b = lo;
-  const int np = (prefix[b + 1] - prefix[b]) / groups_per_seq;
+  const int per = (prefix[b + 1] - prefix[b]) / groups_per_seq;  // np + X
+  const int np = per - p.seg_items;
   const int qoff = pos - prefix[b];
-  const int gi = qoff / np;              // group within the sequence
-  ui.page0 = qoff - gi * np;             // first page of this segment
+  const int gi = qoff / per;              // group within the sequence
+  const int off = qoff - gi * per;        // item within the group
+  const int gfirst = prefix[b] + gi * per + p.seg_items;  // its first page
+  ui.page0 = off < p.seg_items ? 0 : off - p.seg_items;
+  ui.item0 = gfirst + ui.page0;
   ui.b = b;
   ui.g = gi / p.n_rg;
   ui.rg = gi - ui.g * p.n_rg;
-  ui.n_pages = min(range_end - pos, np - ui.page0);
-  ui.gstart = pos - ui.page0;            // the group's first flat item
+  ui.n_pages = min(range_end - ui.item0, np - ui.page0);
   // CTAs that own the group's first and last pages
-  ui.f = (int)(((long long)(ui.gstart + 1) * n_ctas - 1) / total);
-  ui.l = (int)(((long long)(ui.gstart + np) * n_ctas - 1) / total);
-  ui.slot = (pos == range_begin) ? 0 : 1;
+  ui.f = (int)(((long long)(gfirst + 1) * n_ctas - 1) / total);
+  ui.l = (int)(((long long)(gfirst + np) * n_ctas - 1) / total);
+  ui.slot = first ? 0 : 1;
   ui.seq_len = __ldg(p.seq_lens + b);
   int np_seq;
   visible_pages(ui.seq_len, p.q_len, p.n_sink, p.window, ui.n_a, ui.b_start,
                 np_seq);
   ui.pad0 = ui.pad1 = ui.pad2 = 0;
-  ui.valid = 1;
+  ui.valid = ui.n_pages > 0;
   return ui;
 }
 
@@ -221,6 +228,7 @@ constexpr int kMergeUnroll = 4;
 template <typename T, int D, int RB>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_splits_kernel(const AttnParams p) {
+  pdl_wait();  // launched early: the attention grid must have finished
   const SplitDesc dsc = p.desc[blockIdx.x];
   if (!dsc.valid) return;
   const int tid = threadIdx.x;

@@ -8,6 +8,7 @@
 // row with 16-byte vector accesses.
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "svp.h"
 #include "svp_internal.h"
 
@@ -19,6 +20,9 @@ constexpr int kAppendWarps = 8;
 
 __global__ void __launch_bounds__(32 * kAppendWarps)
     kv_append_kernel(const AppendParams p) {
+  // the attention kernel that usually follows may set itself up meanwhile;
+  // it reads the caches only after this grid has completed
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   const long long n_rows = (long long)p.batch * p.n_new * p.num_kv_heads;

@@ -131,6 +131,18 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Programmatic dependent launch: the grid launched after this one on the
+// stream may start (and run up to its own pdl_wait) once every CTA of this
+// grid has signalled or exited.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grid this one depends on has completed and its memory
+// writes are visible (returns at once without such a grid).
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

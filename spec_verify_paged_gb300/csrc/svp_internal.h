@@ -34,12 +34,13 @@ struct AttnParams {
   int rows;            // group * q_len query rows per (sequence, kv head)
   int rb;              // rows per work unit (row-group size)
   int n_rg;            // ceil(rows / rb)
-  int min_pages;       // fewest pages a CTA's slice may hold
+  int min_pages;       // fewest items a CTA's slice may hold
+  int seg_items;       // items that stand for a segment's fixed cost
   float qscale;        // scale * log2(e)
 };
 
 struct AttnPlan {
-  int rb, n_rg, min_pages, grid, ctas_per_sm;
+  int rb, n_rg, min_pages, seg_items, grid, ctas_per_sm;
   bool mma;            // warp-level mma.sync path
   bool tc;             // tcgen05 path (tensor-memory accumulators)
   int batch_cap;       // sequences per launch
@@ -52,6 +53,10 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    int dtype, int max_blocks, int q_len, int n_sink,
                    int window, int split_pages, int kernel_path, int num_sms,
                    long long num_blocks, AttnPlan *plan);
+
+// Pages' worth of time a segment's fixed cost takes on the tcgen05 kernel
+// (epilogue, partial tiles at its ends): the stream-K split counts it.
+constexpr int kSegItemsTc = 12;
 
 // Query rows per kv head (GQA group x q_len) from which the automatic path
 // choice uses tensor cores (bf16 only): tcgen05 for head_dim 128, warp-level
@@ -108,5 +113,27 @@ cudaError_t read_status_attention(cudaStream_t s, unsigned *flags);
 cudaError_t read_status_attention_tc(cudaStream_t s, unsigned *flags);
 cudaError_t read_status_append(cudaStream_t s, unsigned *flags);
 cudaError_t read_status_accept(cudaStream_t s, unsigned *flags);
+
+#ifdef __CUDACC__
+// A launch that may start while the previous kernel on the stream is still
+// running (programmatic dependent launch); the kernel itself waits for that
+// kernel's results (pdl_wait) before it reads anything it could have
+// written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block,
+                       size_t smem, cudaStream_t stream, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+#endif
 
 }  // namespace svp
