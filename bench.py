@@ -1,19 +1,25 @@
 """Benchmark: paged decode attention step on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--split-pages P]
+                    [--workload NAME] [--split-pages P] [--kernel-path 0-3]
+                    [--no-graph]
 
-A step is one pass of the decode hot path over one batch: kv_append of the
+A step is one pass of the hot path over one batch: kv_append of the
 batch's new K/V rows into the paged cache, then paged_decode_attention of
 the new query rows over every cached row (decode-7b: 32 sequences, 32/32
 heads, head_dim 128, context U[512, 4096], bf16 16-token pages in a shuffled
-block table).  `value` is query tokens per second over the whole job; the
-KV-read bandwidth and its fraction of the measured HBM peak are in
-`roofline`.  Inputs are resident in HBM before the timed region; each step
-reads ~1.2 GB of KV, far more than the 129 MB L2, so no flush is needed.
-`e2e` repeats the step through the same public calls with the step's inputs
-copied from pinned host memory and its outputs copied back inside the timed
-region.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+block table); on the verify workloads (q_len > 1) the step ends with
+spec_accept of the q_len - 1 drafts per sequence over a 32,000-token
+vocabulary (its time is reported as `accept_us`).  After the warm-up the
+step is captured as CUDA graphs and the timed loop replays them, so the
+host's launch overhead does not pace the GPU.  `value` is query tokens per
+second over the whole job; the KV-read bandwidth of the attention call and
+its fraction of the measured HBM peak are in `roofline`.  Inputs are
+resident in HBM before the timed region; each step reads 0.27-2.2 GB of
+KV, more than the 129 MB L2, so no flush is needed.  `e2e` repeats the
+step through the plain public calls with the step's inputs copied from
+pinned host memory and its outputs copied back inside the timed region.
+`cpu_baseline` times the fp64 CPU oracle on a bounded sample.
 
 --impl reference times that CPU oracle alone (the slow, obviously correct
 program the GPU results are checked against) on the same workload.
@@ -326,6 +332,21 @@ def run_ours(args):
     out = torch.empty_like(q)
     lse = torch.empty((cfg.batch, cfg.q_len, cfg.num_q_heads),
                       dtype=torch.float32, device=dev)
+    # verify workloads (q_len > 1) end with the acceptance step on K =
+    # q_len - 1 drafts per sequence, vocab 32,000 (the acceptance workload's
+    # recipe, same seed as the attention inputs)
+    acc = None
+    if cfg.q_len > 1:
+        awl = W.make_accept(batch=cfg.batch, num_draft=cfg.q_len - 1,
+                            vocab=W.ACCEPT_CONFIG["vocab"], seed=cfg.seed)
+        acc_in = [to_dev(x, dev) for x in (awl.target_logits, awl.draft_logits,
+                                           awl.draft_tokens, awl.uniforms)]
+        acc_out = (torch.empty((cfg.batch, cfg.q_len), dtype=torch.int32,
+                               device=dev),
+                   torch.empty((cfg.batch,), dtype=torch.int32, device=dev))
+        acc = (acc_in, acc_out)
+        conf["accept"] = {"batch": cfg.batch, "num_draft": cfg.q_len - 1,
+                          "vocab": W.ACCEPT_CONFIG["vocab"]}
     stream = torch.cuda.current_stream(dev)
     scale = float(wl.scale)
     kw = dict(q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
@@ -333,15 +354,24 @@ def run_ours(args):
               kernel_path=args.kernel_path)
     launches = [0]
 
+    def accept_call():
+        svp.spec_accept(*acc[0], out_tokens=acc[1][0], n_accepted=acc[1][1])
+        return svp.last_launch_count()
+
     def step(ev=None):
         svp.kv_append(kn, vn, kc, vc, bt, sl)
         n = svp.last_launch_count()
         if ev is not None:
             ev[0].record(stream)
         svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
+        n += svp.last_launch_count()
         if ev is not None:
             ev[1].record(stream)
-        launches[0] += n + svp.last_launch_count()
+        if acc is not None:
+            n += accept_call()
+            if ev is not None:
+                ev[2].record(stream)
+        launches[0] += n
 
     for _ in range(args.warmup):
         step()
@@ -354,15 +384,19 @@ def run_ours(args):
     # overhead, not by the GPU.  The library keeps no per-call state, so a
     # replay does exactly the work of a call.  The end-to-end figure below
     # still goes through the plain public calls every step.
-    g_app, g_attn = None, None
     if not args.no_graph:
-        g_app, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_app, g_attn, g_acc = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_app):
             svp.kv_append(kn, vn, kc, vc, bt, sl)
         n_app = svp.last_launch_count()
         with torch.cuda.graph(g_attn):
             svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
         n_attn = svp.last_launch_count()
+        n_acc = 0
+        if acc is not None:
+            with torch.cuda.graph(g_acc):
+                n_acc = accept_call()
         torch.cuda.synchronize(dev)
 
         def step(ev=None):  # noqa: F811 -- the replayed form of the step
@@ -372,7 +406,11 @@ def run_ours(args):
             g_attn.replay()
             if ev is not None:
                 ev[1].record(stream)
-            launches[0] += n_app + n_attn
+            if acc is not None:
+                g_acc.replay()
+                if ev is not None:
+                    ev[2].record(stream)
+            launches[0] += n_app + n_attn + n_acc
 
         for _ in range(3):
             step()
@@ -381,8 +419,8 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)  # let the sampler start producing lines
-    attn_ev = [(torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+               for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches[0] = 0
     if world > 1:
@@ -399,7 +437,9 @@ def run_ours(args):
         dist.barrier()
     gpu_launches = launches[0]
     ms = start.elapsed_time(end)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms = [e[0].elapsed_time(e[1]) for e in attn_ev]
+    acc_ms = ([e[1].elapsed_time(e[2]) for e in attn_ev] if acc is not None
+              else None)
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
@@ -411,10 +451,15 @@ def run_ours(args):
     # one device-to-host copy that the host waits for every step.
     in_parts = [("q", q), ("k_new", kn), ("v_new", vn), ("block_table", bt),
                 ("seq_lens", sl)]
+    if acc is not None:
+        in_parts += list(zip(("target_logits", "draft_logits", "draft_tokens",
+                              "uniforms"), acc[0]))
     h_in, d_in, d_views = pack_buffers(in_parts, dev)
     for name, t in in_parts:
         host_view(h_in, d_views[name]).copy_(t.cpu())
     out_parts = [("out", out), ("lse", lse)]
+    if acc is not None:
+        out_parts += list(zip(("out_tokens", "n_accepted"), acc[1]))
     h_res, d_res, r_views = pack_buffers(out_parts, dev)
 
     def e2e_step():
@@ -426,6 +471,11 @@ def run_ours(args):
             q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
             scale=scale, out=r_views["out"], lse=r_views["lse"],
             split_pages=args.split_pages, kernel_path=args.kernel_path)
+        if acc is not None:
+            svp.spec_accept(d_views["target_logits"], d_views["draft_logits"],
+                            d_views["draft_tokens"], d_views["uniforms"],
+                            out_tokens=r_views["out_tokens"],
+                            n_accepted=r_views["n_accepted"])
         h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -470,6 +520,8 @@ def run_ours(args):
                 "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(gpu_launches),
+        **({"accept_us": round(sum(acc_ms) / len(acc_ms) * 1e3, 2)}
+           if acc is not None else {}),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
