@@ -228,8 +228,10 @@ int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
  * n_accepted = -1 and all-(-1) tokens and sets SVP_DEV_BAD_TOKEN.
  * Softmax normalisers are sums of fp32 exponentials relative to integer
  * power-of-two references, accumulated in compensated fp32 pairs and
- * combined by exact power-of-two scaling; the accept ratio is formed in
- * fp64.  One 8-CTA thread-block cluster per sequence.  Uses no workspace.
+ * combined by exact power-of-two scaling; the accept ratio and the draw's
+ * prefix sums use error-free fp32 transformations (no fp64).  One
+ * thread-block cluster per sequence: 16 CTAs when the whole batch fits one
+ * wave of such clusters, else 8.  Uses no workspace.
  * Errors: SVP_ERR_INVALID_ARG for null pointers, batch < 0, num_draft < 1,
  * vocab < 2; SVP_ERR_UNSUPPORTED for num_draft > 15 or batch > 65535. */
 int spec_accept(int batch, int num_draft, int vocab,
