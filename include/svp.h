@@ -125,14 +125,13 @@ typedef enum {
  * Work: every CTA of one persistent launch takes an equal slice of all
  * visible pages of all (sequence, kv head) groups (at least
  * dims->split_pages pages each); a group that spans several slices is
- * finished by merging their partial results by log-sum-exp inside the same
- * launch.
+ * finished by a second kernel, launched as a programmatic dependent of the
+ * first, which merges the slices' partial results by log-sum-exp.
  * Workspace: paged_decode_workspace_size() bytes, passed in dims; it needs
- * no initialisation: split arrivals are counted in 64-bit tickets tagged
- * with a per-launch number, so whatever a ticket holds from earlier
- * launches counts as zero (a call with more than 65536 sequence x kv-head
- * groups also clears its tickets with one cudaMemsetAsync).  One kernel
- * launch per 4096 sequences (1024 on the TCGEN05 path).  With
+ * no initialisation: each CTA rewrites the split record it owns in every
+ * launch, and the merge kernel reads partials only where a record of the
+ * same launch points.  Two kernel launches (attention, merge) per 4096
+ * sequences (1024 on the TCGEN05 path).  With
  * dims->workspace == NULL the library uses a buffer of its own per device,
  * (re)allocated inside the call when it is too small -- that first call is
  * then not capturable in a CUDA graph.  Calls that share a workspace must
@@ -174,8 +173,8 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
  *     (cudaGetSymbolAddress, once per device, with that device current);
  *     make that first call before any stream capture.
  *   - Every call shares the one array and leaves its contents behind;
- *     nothing in it needs to start at zero (split counters are tagged with
- *     a per-launch number), so calls in sequence on one stream are
+ *     nothing in it needs to start at zero (every launch rewrites the
+ *     split records it reads), so calls in sequence on one stream are
  *     independent.  Calls that overlap on the GPU (other streams, other
  *     host threads) race on the array.
  *   - With dims->split_pages == 0 the automatic slice size is enlarged (64,
