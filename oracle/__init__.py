@@ -13,7 +13,10 @@ exact attention from the lesson "KV cache & Flash Attention" (section
 softmax problem"); masks from "How speculative decoding doubles LLM speed"
 (step 2, verification) and the StreamingLLM page (section "The StreamingLLM
 solution"); acceptance from "How speculative decoding doubles LLM speed"
-(step 3, sampling).
+(step 3, sampling); the draft-tree mask and tree acceptance from the same
+page (section "Modern architecture variants", SpecInfer) and "Speculative
+decoding: how AI models get faster without getting bigger" (section on
+real-world adoption).
 """
 from __future__ import annotations
 
@@ -65,6 +68,12 @@ def _load():
             lib.oracle_spec_accept.argtypes = (
                 [i32] * 3 + [vp] * 8 + [ctypes.c_double])
             lib.oracle_spec_accept.restype = i32
+            lib.oracle_paged_tree_attention.argtypes = (
+                [i32] * 8 + [vp] * 5 + [i32, vp, f32, vp, i64, vp, vp])
+            lib.oracle_paged_tree_attention.restype = i32
+            lib.oracle_spec_accept_tree.argtypes = (
+                [i32] * 3 + [vp] * 10 + [ctypes.c_double])
+            lib.oracle_spec_accept_tree.restype = i32
             _lib = lib
     return _lib
 
@@ -186,3 +195,77 @@ def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
         raise ValueError(f"oracle_spec_accept failed with status {st}")
     return {"out_tokens": out, "n_accepted": nacc, "near_boundary": near,
             "residual_fallback": fb}
+
+
+def paged_tree_attention(q, k_cache, v_cache, block_table, seq_lens, q_len,
+                         tree_mask, scale=None, rows=None):
+    """Exact attention with a draft-tree mask, in fp64.
+
+    tree_mask [B, q_len] uint32: bit k of entry (b, i) set iff node k is an
+    ancestor of node i or i itself (keys of the q_len new rows); every key
+    before them is visible.  Returns like paged_attention."""
+    lib = _load()
+    B, ql, Hq, D = q.shape
+    assert ql == q_len and tree_mask.shape == (B, q_len)
+    nb, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    code = _dtype_code(q)
+    assert _dtype_code(k_cache) == code and _dtype_code(v_cache) == code
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    q = _c(q, q.dtype)
+    kc = _c(k_cache, k_cache.dtype)
+    vc = _c(v_cache, v_cache.dtype)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    tm = _c(tree_mask, np.uint32)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    if rows is None:
+        out = np.zeros((B, q_len, Hq, D), np.float64)
+        lse = np.zeros((B, q_len, Hq), np.float64)
+        r, n = None, 0
+    else:
+        r = _c(rows, np.int64)
+        out = np.zeros((r.size, D), np.float64)
+        lse = np.zeros((r.size,), np.float64)
+        n = r.size
+    st = lib.oracle_paged_tree_attention(
+        B, Hq, Hkv, D, bs, mb, nb, code, _ptr(q), _ptr(kc), _ptr(vc),
+        _ptr(bt), _ptr(sl), q_len, _ptr(tm), float(scale), _ptr(r), n,
+        _ptr(out), _ptr(lse))
+    if st != 0:
+        raise ValueError(f"oracle_paged_tree_attention failed with status {st}")
+    return out, lse
+
+
+def spec_accept_tree(target_logits, draft_logits, parents, node_tokens,
+                     uniforms, eps=BOUNDARY_EPS):
+    """Literal tree walk in fp64 (see oracle.h).
+
+    target_logits, draft_logits [B, N, V] fp32; parents, node_tokens [B, N]
+    int32; uniforms [B, N] fp32.  Returns dict(out_tokens [B, N],
+    out_nodes [B, N], n_accepted [B], near_boundary [B],
+    residual_fallback [B])."""
+    lib = _load()
+    B, N, V = target_logits.shape
+    assert draft_logits.shape == (B, N, V)
+    assert parents.shape == (B, N) and node_tokens.shape == (B, N)
+    assert uniforms.shape == (B, N)
+    tl = _c(target_logits, np.float32)
+    dl = _c(draft_logits, np.float32)
+    pa = _c(parents, np.int32)
+    tk = _c(node_tokens, np.int32)
+    un = _c(uniforms, np.float32)
+    out = np.full((B, N), -1, np.int32)
+    nodes = np.full((B, N), -1, np.int32)
+    nacc = np.zeros((B,), np.int32)
+    near = np.zeros((B,), np.int32)
+    fb = np.zeros((B,), np.int32)
+    st = lib.oracle_spec_accept_tree(B, N, V, _ptr(tl), _ptr(dl), _ptr(pa),
+                                     _ptr(tk), _ptr(un), _ptr(out), _ptr(nodes),
+                                     _ptr(nacc), _ptr(near), _ptr(fb),
+                                     float(eps))
+    if st != 0:
+        raise ValueError(f"oracle_spec_accept_tree failed with status {st}")
+    return {"out_tokens": out, "out_nodes": nodes, "n_accepted": nacc,
+            "near_boundary": near, "residual_fallback": fb}

@@ -9,8 +9,9 @@
  * Sources (web pages; quoted by title and section):
  *  [SD]  "How speculative decoding doubles LLM speed without quality loss"
  *        (dothoosh.com): sections "The speculative execution cycle"
- *        (step 2 verification, step 3 sampling) and "Absolute mathematical
- *        exactness".
+ *        (step 2 verification, step 3 sampling), "Absolute mathematical
+ *        exactness" and "Modern architecture variants" (SpecInfer's draft
+ *        tree).
  *  [KV]  "KV cache & Flash Attention" lesson (nextadmin.net): sections
  *        "KV-cache math", "FlashAttention -- the tiling trick",
  *        "PagedAttention -- the KV cache as virtual memory",
@@ -19,7 +20,8 @@
  *        sinks" (dothoosh.com): sections "The softmax problem",
  *        "Why sliding windows fail", "The StreamingLLM solution".
  *  [SP]  "Speculative decoding: how AI models get faster without getting
- *        bigger" (aioapex.com): section "What speculative decoding does".
+ *        bigger" (aioapex.com): sections "What speculative decoding does" and
+ *        "Real-world adoption" (tree speculation, longest accepted path).
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes): query i of a q_len-row verify block sits at absolute position
@@ -55,6 +57,17 @@ static int key_visible(long j, long t, int n_sink, int window) {
   return (j < n_sink) || (j > t - window);
 }
 
+/* The draft-tree mask ([SD] "Modern architecture variants": SpecInfer checks
+ * every branch of a draft tree in one pass with a two-dimensional attention
+ * mask).  The q_len new rows of a sequence are the tree's nodes, node k at
+ * position base + k; query node i sees every key before base and the node
+ * keys whose bit is set in its mask word (its ancestors and itself). */
+static int key_visible_tree(long j, long t, long base, uint32_t mask) {
+  if (j < 0 || j > t) return 0;
+  if (j < base) return 1;
+  return (int)((mask >> (j - base)) & 1u);
+}
+
 /* Flat element offset of row `pos` of the logical sequence b, kv head g.
  * [KV] "PagedAttention": logical position -> (block_table[b][pos/bs], pos%bs).
  * Returns -1 if the physical block id is out of range. */
@@ -84,18 +97,20 @@ static int check_sizes(int batch, int num_q_heads, int num_kv_heads,
 /* ---- exact attention: [KV] "FlashAttention" (S = QK^T, P = softmax(S),
  * O = PV) and [SL] "The softmax problem" (softmax(QK^T/sqrt(d))V) -------- */
 
-int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
-                           int head_dim, int block_size, int max_blocks_per_seq,
-                           int num_blocks, int dtype, const void *q,
-                           const void *k_cache, const void *v_cache,
-                           const int32_t *block_table, const int32_t *seq_lens,
-                           int q_len, int n_sink, int window, float scale,
-                           const int64_t *rows, int64_t n_rows, double *out,
-                           double *lse) {
+static int attention_rows(int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq,
+                          int num_blocks, int dtype, const void *q,
+                          const void *k_cache, const void *v_cache,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          int q_len, int n_sink, int window,
+                          const uint32_t *tree_mask, float scale,
+                          const int64_t *rows, int64_t n_rows, double *out,
+                          double *lse) {
   if (check_sizes(batch, num_q_heads, num_kv_heads, head_dim, block_size,
                   max_blocks_per_seq, num_blocks, dtype, q_len, n_sink,
                   window))
     return -1;
+  if (tree_mask && (window != 0 || q_len > 32)) return -1;
   const int64_t total_rows = (int64_t)batch * q_len * num_q_heads;
   if (rows == NULL) n_rows = total_rows;
   const int group = num_q_heads / num_kv_heads;
@@ -133,7 +148,10 @@ int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
     /* 1. gather the visible keys and their scores */
     long nv = 0;
     for (long j = 0; j <= t; ++j) {
-      if (!key_visible(j, t, n_sink, window)) continue;
+      if (tree_mask ? !key_visible_tree(j, t, L - q_len,
+                                        tree_mask[(size_t)b * q_len + i])
+                    : !key_visible(j, t, n_sink, window))
+        continue;
       long off = kv_offset(block_table, max_blocks_per_seq, b, j, block_size,
                            num_kv_heads, g, head_dim, num_blocks);
       if (off < 0) {
@@ -170,6 +188,37 @@ int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
   free(s);
   free(koff);
   return status;
+}
+
+int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int max_blocks_per_seq,
+                           int num_blocks, int dtype, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           const int64_t *rows, int64_t n_rows, double *out,
+                           double *lse) {
+  return attention_rows(batch, num_q_heads, num_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, dtype, q,
+                        k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
+                        window, NULL, scale, rows, n_rows, out, lse);
+}
+
+int oracle_paged_tree_attention(int batch, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size,
+                                int max_blocks_per_seq, int num_blocks,
+                                int dtype, const void *q, const void *k_cache,
+                                const void *v_cache,
+                                const int32_t *block_table,
+                                const int32_t *seq_lens, int q_len,
+                                const uint32_t *tree_mask, float scale,
+                                const int64_t *rows, int64_t n_rows,
+                                double *out, double *lse) {
+  if (!tree_mask) return -1;
+  return attention_rows(batch, num_q_heads, num_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, dtype, q,
+                        k_cache, v_cache, block_table, seq_lens, q_len, 0, 0,
+                        tree_mask, scale, rows, n_rows, out, lse);
 }
 
 /* ---- tiled variant: [KV] "FlashAttention -- the tiling trick" and
@@ -413,5 +462,86 @@ int oracle_spec_accept(int batch, int num_draft, int vocab,
     if (residual_fallback) residual_fallback[b] = fallback;
   }
   free(p); free(qd); free(w);
+  return status;
+}
+
+/* ---- tree acceptance: [SD] "Modern architecture variants" (SpecInfer: a
+ * tree of speculative branches checked in one pass) and [SP] "Real-world
+ * adoption" (the verifier keeps the longest accepted path).  Reading: the
+ * walk starts at the root; a node's children are tried in index order with
+ * the linear rule of [SD] step 3, u_c <= r(x_c)/q(x_c), where r starts as
+ * the target distribution after the node and, after each rejected child,
+ * becomes the normalised residual max(0, r - q) -- the distribution the
+ * linear rule resamples from; an accepted child becomes the next node; when
+ * every child is rejected (or the node is a leaf) one token is drawn from r
+ * with u_0.  On a chain this is exactly the linear rule. ---------------- */
+
+int oracle_spec_accept_tree(int batch, int num_nodes, int vocab,
+                            const float *target_logits,
+                            const float *draft_logits, const int32_t *parents,
+                            const int32_t *node_tokens, const float *uniforms,
+                            int32_t *out_tokens, int32_t *out_nodes,
+                            int32_t *n_accepted, int32_t *near_boundary,
+                            int32_t *residual_fallback, double eps) {
+  if (batch < 0 || num_nodes < 1 || vocab < 2) return -1;
+  const int N = num_nodes;
+  double *r = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
+  if (!r || !qd) { free(r); free(qd); return -1; }
+  int status = 0;
+  for (int b = 0; b < batch && status == 0; ++b) {
+    const int32_t *par = parents + (size_t)b * N;
+    const int32_t *tok = node_tokens + (size_t)b * N;
+    const float *u = uniforms + (size_t)b * N;
+    int32_t *emit = out_tokens + (size_t)b * N;
+    int32_t *nodes = out_nodes + (size_t)b * N;
+    for (int k = 0; k < N; ++k) { emit[k] = -1; nodes[k] = -1; }
+    /* a tree: node 0 is the root, every other node's parent comes first */
+    if (par[0] != -1) status = -1;
+    for (int c = 1; c < N; ++c) {
+      if (par[c] < 0 || par[c] >= c) status = -1;
+      if (tok[c] < 0 || tok[c] >= vocab) status = status ? status : -4;
+    }
+    if (status) break;
+    int near = 0, fallback = 0, n_out = 0, cur = 0;
+    for (;;) {
+      softmax_row(target_logits + ((size_t)b * N + cur) * vocab, vocab, r);
+      softmax_row(draft_logits + ((size_t)b * N + cur) * vocab, vocab, qd);
+      int next = -1;
+      for (int c = cur + 1; c < N && next < 0; ++c) {
+        if (par[c] != cur) continue;
+        const int x = tok[c];
+        const double ur = (double)u[c];
+        const double ratio = (qd[x] > 0.0) ? r[x] / qd[x] : INFINITY;
+        if (fabs(ur - ratio) < eps) near = 1;
+        if (ur <= ratio) {
+          next = c;
+          break;
+        }
+        /* child rejected: continue with the normalised residual */
+        double mass = 0.0;
+        for (int y = 0; y < vocab; ++y)
+          mass += (r[y] - qd[y] > 0.0) ? r[y] - qd[y] : 0.0;
+        if (mass == 0.0) { /* impossible in exact arithmetic: keep r */
+          fallback = 1;
+          continue;
+        }
+        for (int y = 0; y < vocab; ++y)
+          r[y] = ((r[y] - qd[y] > 0.0) ? r[y] - qd[y] : 0.0) / mass;
+      }
+      if (next < 0) {
+        emit[n_out] = inverse_cdf(r, vocab, (double)u[0], eps, &near);
+        break;
+      }
+      emit[n_out] = tok[next];
+      nodes[n_out] = next;
+      ++n_out;
+      cur = next;
+    }
+    n_accepted[b] = n_out;
+    if (near_boundary) near_boundary[b] = near;
+    if (residual_fallback) residual_fallback[b] = fallback;
+  }
+  free(r); free(qd);
   return status;
 }

@@ -38,6 +38,23 @@ int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
                            const int64_t *rows, int64_t n_rows, double *out,
                            double *lse);
 
+/* The same definition with a draft-tree mask instead of the causal verify
+ * mask: the q_len new rows of a sequence are the tree's nodes (node k at
+ * position seq_len - q_len + k) and query node i sees every earlier key plus
+ * the node keys k <= i whose bit k is set in tree_mask[b*q_len + i]
+ * (uint32, its ancestors and itself).  No sinks or window.  q_len <= 32.
+ * Same returns as oracle_paged_attention. */
+int oracle_paged_tree_attention(int batch, int num_q_heads, int num_kv_heads,
+                                int head_dim, int block_size,
+                                int max_blocks_per_seq, int num_blocks,
+                                int dtype, const void *q, const void *k_cache,
+                                const void *v_cache,
+                                const int32_t *block_table,
+                                const int32_t *seq_lens, int q_len,
+                                const uint32_t *tree_mask, float scale,
+                                const int64_t *rows, int64_t n_rows,
+                                double *out, double *lse);
+
 /* The same quantity computed the tiled way: the visible keys of each row are
  * cut into n_splits contiguous parts, each part is folded in `tile`-key
  * blocks with a running (max, sum, accumulator), and the parts are merged by
@@ -78,6 +95,31 @@ int oracle_spec_accept(int batch, int num_draft, int vocab,
                        int32_t *out_tokens, int32_t *n_accepted,
                        int32_t *near_boundary, int32_t *residual_fallback,
                        double eps);
+
+/* Tree acceptance (draft tree of num_nodes nodes; node 0 is the root, the
+ * last token already accepted; parents[c] < c for c >= 1, parents[0] = -1).
+ *   target_logits [batch, N, vocab]: row i = target distribution after node i
+ *   draft_logits  [batch, N, vocab]: row i = draft distribution node i's
+ *                 children were drawn from
+ *   node_tokens   [batch, N] (entry 0 unused), uniforms [batch, N]: entry
+ *                 c >= 1 decides node c, entry 0 drives the final draw
+ *   out_tokens    [batch, N]: accepted path tokens, then the drawn token,
+ *                 -1 padded; out_nodes [batch, N]: node of each accepted
+ *                 path token, -1 padded; n_accepted [batch]: path length
+ * At each node the children are tried in index order: child c is accepted
+ * iff u_c <= r(x_c)/q(x_c), r being the target distribution after the node,
+ * replaced by the normalised residual max(0, r - q) after each rejected
+ * child; when no child is accepted one token is drawn from r with u_0.
+ * near_boundary / residual_fallback as for oracle_spec_accept.
+ * Returns 0, -1 for bad sizes or a malformed tree, -4 for a node token
+ * outside [0, vocab). */
+int oracle_spec_accept_tree(int batch, int num_nodes, int vocab,
+                            const float *target_logits,
+                            const float *draft_logits, const int32_t *parents,
+                            const int32_t *node_tokens, const float *uniforms,
+                            int32_t *out_tokens, int32_t *out_nodes,
+                            int32_t *n_accepted, int32_t *near_boundary,
+                            int32_t *residual_fallback, double eps);
 
 #ifdef __cplusplus
 }

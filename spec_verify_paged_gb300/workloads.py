@@ -93,6 +93,8 @@ class AttnConfig:
     ring: bool = False         # ring-buffered resident pages (streaming)
     sink_key_scale: float = 1.0
     seed: int = 0
+    tree_depth: int = 0        # > 0: the q_len new rows are a complete
+                               # binary draft tree of this depth
 
 
 CONFIGS = {
@@ -111,10 +113,43 @@ CONFIGS = {
     "long-context-128k-verify": AttnConfig("long-context-128k-verify", 4, 64,
                                            8, 128, 4, "bf16", 131072, 131072,
                                            seed=5),
+    # SpecInfer-style draft tree: 2 candidates per depth, 3 levels, so
+    # 1 + 2 + 4 + 8 = 15 new rows (the root and 14 draft nodes)
+    "tree-verify": AttnConfig("tree-verify", 16, 32, 8, 128, 15, "bf16", 2048,
+                              8192, seed=6, tree_depth=3),
 }
 
 ACCEPT_CONFIG = dict(name="verify-gqa-accept", batch=16, num_draft=4,
                      vocab=32000, target_std=2.0, noise_std=0.5, seed=3)
+TREE_ACCEPT_CONFIG = dict(name="tree-verify-accept", batch=16, depth=3,
+                          vocab=32000, target_std=2.0, noise_std=0.5, seed=6)
+
+
+def binary_tree_parents(depth: int) -> np.ndarray:
+    """Parents of a complete binary tree in breadth-first numbering: node 0
+    is the root, node c >= 1 hangs below (c - 1) // 2; 2^(depth+1) - 1
+    nodes."""
+    n = (1 << (depth + 1)) - 1
+    par = np.array([-1] + [(c - 1) // 2 for c in range(1, n)], np.int32)
+    return par
+
+
+def tree_mask_from_parents(parents: np.ndarray) -> np.ndarray:
+    """Ancestor-or-self bit masks: bit k of entry i is set iff node k lies
+    on the path from the root to node i (parents[..., c] < c).  Works on
+    [N] or [B, N] arrays; returns uint32 of the same shape."""
+    par = np.asarray(parents)
+    mask = np.zeros(par.shape, np.uint32)
+    for c in range(par.shape[-1]):
+        own = np.uint32(1 << c)
+        pc = par[..., c]
+        if par.ndim == 1:
+            mask[c] = own | (mask[pc] if pc >= 0 else np.uint32(0))
+        else:
+            up = np.where(pc >= 0, np.take_along_axis(
+                mask, np.maximum(pc, 0)[:, None], axis=1)[:, 0], 0)
+            mask[:, c] = own | up.astype(np.uint32)
+    return mask
 
 
 @dataclasses.dataclass
@@ -129,6 +164,8 @@ class AttnWorkload:
     # rows to append before attending (kv_append inputs), may be None
     k_new: Optional[np.ndarray] = None
     v_new: Optional[np.ndarray] = None
+    # [B, q_len] uint32 ancestor masks of a draft tree, or None (causal)
+    tree_mask: Optional[np.ndarray] = None
 
     @property
     def q_len(self):
@@ -265,8 +302,14 @@ def make_attention(cfg: AttnConfig, seed: Optional[int] = None,
                 v_cache[blk, :, pos % BLOCK_SIZE, :] = nan
 
     scale = np.float32(1.0 / math.sqrt(D))
+    tree_mask = None
+    if cfg.tree_depth > 0:
+        par = binary_tree_parents(cfg.tree_depth)
+        assert par.size == ql, "q_len must be the tree's node count"
+        tree_mask = np.tile(tree_mask_from_parents(par), (B, 1))
     return AttnWorkload(cfg, q, k_cache, v_cache, table,
-                        seq_lens.astype(np.int32), scale, k_new, v_new)
+                        seq_lens.astype(np.int32), scale, k_new, v_new,
+                        tree_mask)
 
 
 def small_config(name="small", batch=3, num_q_heads=8, num_kv_heads=2,
@@ -311,3 +354,38 @@ def make_accept(batch=16, num_draft=4, vocab=32000, target_std=2.0,
     tokens = np.argmax(draft.astype(np.float64) + gumbel, axis=-1).astype(np.int32)
     u = uniforms01(rng, (B, K + 1))
     return AcceptWorkload(target.astype(np.float32), draft, tokens, u)
+
+
+@dataclasses.dataclass
+class TreeAcceptWorkload:
+    target_logits: np.ndarray   # [B, N, V] fp32: row i = target after node i
+    draft_logits: np.ndarray    # [B, N, V] fp32: row i = draft after node i
+    parents: np.ndarray         # [B, N] int32, parents[:, 0] = -1
+    node_tokens: np.ndarray     # [B, N] int32 (entry 0 unused: -1)
+    uniforms: np.ndarray        # [B, N] fp32 in [0, 1)
+
+
+def make_tree_accept(batch=16, depth=3, vocab=32000, target_std=2.0,
+                     noise_std=0.5, seed=6, parents=None,
+                     **_unused) -> TreeAcceptWorkload:
+    """A draft tree per sequence (complete binary of `depth` levels unless
+    `parents` [N] is given).  Target logits ~ N(0, target_std^2) per node;
+    draft logits = target + N(0, noise_std^2); the children of node i are
+    drawn independently from softmax(draft row i) by the Gumbel-max trick
+    (the draft model sampling several continuations); uniforms in [0, 1)."""
+    rng = np.random.default_rng(seed)
+    par = binary_tree_parents(depth) if parents is None else np.asarray(
+        parents, np.int32)
+    B, N, V = batch, par.size, vocab
+    target = (rng.standard_normal((B, N, V), dtype=np.float32)
+              * np.float32(target_std))
+    draft = (target + rng.standard_normal((B, N, V), dtype=np.float32)
+             * np.float32(noise_std)).astype(np.float32)
+    tokens = np.full((B, N), -1, np.int32)
+    for c in range(1, N):
+        g = rng.gumbel(size=(B, V))
+        tokens[:, c] = np.argmax(draft[:, par[c], :].astype(np.float64) + g,
+                                 axis=-1)
+    u = uniforms01(rng, (B, N))
+    return TreeAcceptWorkload(target.astype(np.float32), draft,
+                              np.tile(par, (B, 1)).astype(np.int32), tokens, u)
