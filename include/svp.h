@@ -151,6 +151,28 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
                            int q_len, int n_sink, int window, float scale,
                            void *out, float *lse, cudaStream_t stream);
 
+/* Draft-tree verify attention (pages: "How speculative decoding doubles LLM
+ * speed", section "Modern architecture variants" -- SpecInfer verifies a
+ * tree of draft branches in one pass with a two-dimensional attention mask;
+ * "Speculative decoding: how AI models get faster without getting bigger",
+ * on tree speculation).
+ * The q_len new rows of sequence b are the nodes of its draft tree, node k
+ * at position seq_lens[b] - q_len + k (node 0 the root: the last accepted
+ * token).  tree_mask [batch, q_len] uint32 (DEVICE, 4-byte aligned): bit k
+ * of entry (b, i) is set iff node k is an ancestor of node i or i itself
+ * (so only bits k <= i matter; higher bits are ignored).  Query node i
+ * attends to every cached key before the tree and to the node keys its
+ * bits select; otherwise exactly paged_decode_attention with n_sink = 0 and
+ * window = 0 (same layouts, workspace, alignment and errors).  A chain
+ * (bits 0..i for node i) reproduces the causal verify block.  q_len
+ * <= 16.  Errors: those of paged_decode_attention, plus SVP_ERR_INVALID_ARG
+ * for a null or misaligned tree_mask. */
+int paged_tree_attention(const svp_dims *dims, const void *q,
+                         const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         int q_len, const uint32_t *tree_mask, float scale,
+                         void *out, float *lse, cudaStream_t stream);
+
 /* Size of the fixed device scratch used by paged_decode_attention_noalloc. */
 #define SVP_STATIC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
 
@@ -237,6 +259,46 @@ int spec_accept(int batch, int num_draft, int vocab,
                 const float *target_logits, const float *draft_logits,
                 const int32_t *draft_tokens, const float *uniforms,
                 int32_t *out_tokens, int32_t *n_accepted, cudaStream_t stream);
+
+/* Tree acceptance (pages: "How speculative decoding doubles LLM speed",
+ * sections "Modern architecture variants" -- SpecInfer's draft tree -- and
+ * step 3 (sampling); "Speculative decoding: how AI models get faster without
+ * getting bigger": the verifier keeps the longest accepted path).
+ * A draft tree of num_nodes = N nodes per sequence; node 0 is the root (the
+ * last accepted token), every other node c has parents[b][c] < c.
+ *   target_logits [batch, N, vocab] fp32: row i = target logits after node i
+ *   draft_logits  [batch, N, vocab] fp32: row i = draft logits the children
+ *                 of node i were drawn from (rows of leaves are not read)
+ *   parents       [batch, N] int32 (parents[b][0] = -1)
+ *   node_tokens   [batch, N] int32 (entry 0 unused)
+ *   uniforms      [batch, N] fp32 in [0,1): entry c >= 1 decides node c,
+ *                 entry 0 drives the one final draw
+ *   out_tokens    [batch, N] int32, written: the accepted path's tokens,
+ *                 then the drawn token, then -1 padding
+ *   out_nodes     [batch, N] int32: the node of each accepted path token
+ *                 (for compacting the KV cache), then -1
+ *   n_accepted    [batch] int32: length of the accepted path
+ * The walk starts at the root; a node's children are tried in index order,
+ * child c being accepted iff u_c <= r(x_c) / q(x_c), where q is the draft
+ * distribution of the node and r starts as its target distribution p and,
+ * after each rejected child, becomes the normalised residual max(0, r - q).
+ * An accepted child becomes the current node; when no child is accepted
+ * (or the node is a leaf) one token is drawn from r with u_0 (inverse CDF
+ * in token order, as in spec_accept).  On a chain this is spec_accept with
+ * uniforms (u_1 .. u_K, u_0).  With the children of a node drawn
+ * independently from its q, the emitted tokens follow the target model.
+ * A malformed tree or a token outside [0, vocab) gives n_accepted = -1 and
+ * all -1 outputs and sets SVP_DEV_BAD_TOKEN.  Numerics as spec_accept; one
+ * rejected child costs one more pass over the node's two rows.  Uses no
+ * workspace.
+ * Errors: SVP_ERR_INVALID_ARG for null pointers, batch < 0, num_nodes < 1,
+ * vocab < 2; SVP_ERR_UNSUPPORTED for num_nodes > 16 or batch > 65535. */
+int spec_accept_tree(int batch, int num_nodes, int vocab,
+                     const float *target_logits, const float *draft_logits,
+                     const int32_t *parents, const int32_t *node_tokens,
+                     const float *uniforms, int32_t *out_tokens,
+                     int32_t *out_nodes, int32_t *n_accepted,
+                     cudaStream_t stream);
 
 /* Synchronises `stream`, returns SVP_OK and stores in *flags the OR of the
  * SVP_DEV_* flags raised by kernels since the last read, then clears them.

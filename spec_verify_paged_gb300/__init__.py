@@ -11,7 +11,9 @@ from .binding import (  # noqa: F401
     last_launch_count,
     load_library,
     paged_decode_attention,
+    paged_tree_attention,
     read_device_status,
     spec_accept,
+    spec_accept_tree,
     workspace_for,
 )

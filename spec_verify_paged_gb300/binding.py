@@ -24,8 +24,10 @@ SVP_F32, SVP_BF16 = 0, 1
 PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES, PATH_TCGEN05 = 0, 1, 2, 3
 DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
+            "paged_tree_attention",
             "paged_decode_workspace_size",
-            "kv_append", "spec_accept", "svp_read_device_status",
+            "kv_append", "spec_accept", "spec_accept_tree",
+            "svp_read_device_status",
             "svp_status_string", "svp_last_launch_count")
 
 
@@ -71,12 +73,17 @@ def load_library(path: str = LIB_PATH):
                                                        vp, i32, i32, i32, f32,
                                                        vp, vp, vp]
         lib.paged_decode_attention_noalloc.restype = i32
+        lib.paged_tree_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, i32,
+                                             vp, f32, vp, vp, vp]
+        lib.paged_tree_attention.restype = i32
         lib.paged_decode_workspace_size.argtypes = [dims_p, i32, i32, i32]
         lib.paged_decode_workspace_size.restype = sz
         lib.kv_append.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, vp]
         lib.kv_append.restype = i32
         lib.spec_accept.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.spec_accept.restype = i32
+        lib.spec_accept_tree.argtypes = [i32, i32, i32] + [vp] * 9
+        lib.spec_accept_tree.restype = i32
         lib.svp_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
         lib.svp_read_device_status.restype = i32
         lib.svp_status_string.argtypes = [i32]
@@ -160,6 +167,30 @@ def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
                            kernel_path=PATH_AUTO, stream=None):
     """out [B, q_len, Hq, D] (q's dtype) and lse [B, q_len, Hq] fp32 of paged
     decode/verify attention (include/svp.h: paged_decode_attention)."""
+    return _attention(q, k_cache, v_cache, block_table, seq_lens, q_len,
+                      n_sink, window, None, scale, out, lse, workspace,
+                      split_pages, kernel_path, stream)
+
+
+def paged_tree_attention(q, k_cache, v_cache, block_table, seq_lens,
+                         tree_mask, scale=None, out=None, lse=None,
+                         workspace=None, split_pages=0, kernel_path=PATH_AUTO,
+                         stream=None):
+    """Draft-tree verify attention (include/svp.h: paged_tree_attention).
+    tree_mask: int32 (or uint32) [B, q_len] on the GPU, bit k of entry
+    (b, i) set iff node k is an ancestor of node i or i itself."""
+    _cuda_contig(tree_mask, "tree_mask")
+    _need(tree_mask.dtype in (torch.int32, getattr(torch, "uint32", torch.int32))
+          and tuple(tree_mask.shape) == tuple(q.shape[:2]),
+          "tree_mask must be int32/uint32 [B, q_len]")
+    return _attention(q, k_cache, v_cache, block_table, seq_lens, None, 0, 0,
+                      tree_mask, scale, out, lse, workspace, split_pages,
+                      kernel_path, stream)
+
+
+def _attention(q, k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
+               window, tree_mask, scale, out, lse, workspace, split_pages,
+               kernel_path, stream):
     lib = load_library()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
                  (block_table, "block_table"), (seq_lens, "seq_lens")):
@@ -191,12 +222,20 @@ def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
     if workspace is not None:
         dims.workspace = ctypes.c_void_p(workspace.data_ptr())
         dims.workspace_bytes = workspace.numel() * workspace.element_size()
-    st = lib.paged_decode_attention(
-        ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(),
-        v_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
-        int(q_len), int(n_sink), int(window), float(scale), out.data_ptr(),
-        lse.data_ptr(), _stream_handle(stream, q.device))
-    _check("paged_decode_attention", st)
+    if tree_mask is None:
+        st = lib.paged_decode_attention(
+            ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(),
+            v_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+            int(q_len), int(n_sink), int(window), float(scale),
+            out.data_ptr(), lse.data_ptr(), _stream_handle(stream, q.device))
+        _check("paged_decode_attention", st)
+    else:
+        st = lib.paged_tree_attention(
+            ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(),
+            v_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(),
+            int(q_len), tree_mask.data_ptr(), float(scale), out.data_ptr(),
+            lse.data_ptr(), _stream_handle(stream, q.device))
+        _check("paged_tree_attention", st)
     return out, lse
 
 
@@ -250,6 +289,42 @@ def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
                          n_accepted.data_ptr(), _stream_handle(stream, dev))
     _check("spec_accept", st)
     return out_tokens, n_accepted
+
+
+def spec_accept_tree(target_logits, draft_logits, parents, node_tokens,
+                     uniforms, out_tokens=None, out_nodes=None,
+                     n_accepted=None, stream=None):
+    """Tree acceptance (include/svp.h: spec_accept_tree).  Returns
+    (out_tokens [B, N] int32, out_nodes [B, N] int32, n_accepted [B] int32)."""
+    lib = load_library()
+    for t, n in ((target_logits, "target_logits"),
+                 (draft_logits, "draft_logits"), (parents, "parents"),
+                 (node_tokens, "node_tokens"), (uniforms, "uniforms")):
+        _cuda_contig(t, n)
+    _need(target_logits.dtype == torch.float32 and
+          draft_logits.dtype == torch.float32 and
+          uniforms.dtype == torch.float32, "logits/uniforms must be float32")
+    _need(parents.dtype == torch.int32 and node_tokens.dtype == torch.int32,
+          "parents/node_tokens must be int32")
+    B, N, V = target_logits.shape
+    _need(tuple(draft_logits.shape) == (B, N, V), "draft_logits must be [B, N, V]")
+    for t, n in ((parents, "parents"), (node_tokens, "node_tokens"),
+                 (uniforms, "uniforms")):
+        _need(tuple(t.shape) == (B, N), f"{n} must be [B, N]")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_nodes is None:
+        out_nodes = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib.spec_accept_tree(B, N, V, target_logits.data_ptr(),
+                              draft_logits.data_ptr(), parents.data_ptr(),
+                              node_tokens.data_ptr(), uniforms.data_ptr(),
+                              out_tokens.data_ptr(), out_nodes.data_ptr(),
+                              n_accepted.data_ptr(), _stream_handle(stream, dev))
+    _check("spec_accept_tree", st)
+    return out_tokens, out_nodes, n_accepted
 
 
 def read_device_status(stream=None, device=None) -> int:

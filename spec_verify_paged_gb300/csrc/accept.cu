@@ -1,31 +1,36 @@
-// accept.cu -- speculative acceptance (rejection sampling) for sm_103a.
+// accept.cu -- speculative acceptance (rejection sampling) for sm_103a:
+// the linear draft (spec_accept) and the draft tree (spec_accept_tree).
 //
-// Pages: "How speculative decoding doubles LLM speed", step 3 (sampling)
-// and section "Absolute mathematical exactness"; "Speculative decoding: how
-// AI models get faster without getting bigger", section "What speculative
-// decoding does".  For one sequence: p_i = softmax(target row i), q_i =
-// softmax(draft row i); draft i is accepted iff u_i <= p_i(x_i)/q_i(x_i);
-// at the first rejection j a replacement is drawn from max(0, p_j - q_j)
-// normalised, and if all K drafts pass the bonus is drawn from p_K.
+// Pages: "How speculative decoding doubles LLM speed", step 3 (sampling),
+// sections "Absolute mathematical exactness" and "Modern architecture
+// variants" (SpecInfer's draft tree); "Speculative decoding: how AI models
+// get faster without getting bigger", sections "What speculative decoding
+// does" and on real-world adoption (the verifier keeps the longest accepted
+// path of the tree).  For one sequence: p = softmax(target row), q =
+// softmax(draft row); a draft token x is accepted iff u <= p(x)/q(x); at a
+// rejection the replacement is drawn from max(0, p - q) normalised, and if
+// every draft passes the bonus is drawn from the last target row.  On a
+// tree, a node's children are tried in index order and each rejected child
+// replaces p by that normalised residual before the next is tried.
 //
 // GB300 design: one thread-block cluster of NC CTAs per sequence (16 when
 // the whole batch fits one wave of 16-CTA clusters, else 8); CTA c owns
 // vocab slice c of every logit row.
-//  * At kernel start each CTA issues 1-D bulk copies of its slice of all
-//    2K+1 rows into shared memory (about 72 KB for K = 4 and vocab 32,000
-//    with 16-CTA clusters, three CTAs per SM); larger K x vocab cycle through
-//    a ring of slots.  The loops stay rolled: the kernel's code has to fit
-//    the instruction cache, since every warp runs it once.
-//  * Pass 1: per row, a thread keeps an integer reference exponent
-//    E >= max(x * log2 e) and the sum of exp2(x * log2 e - E) as a
-//    compensated fp32 pair, in one pass: when E grows the sum is rescaled by
-//    an exact power of two.  Warps, CTAs and the cluster merge partial sums
-//    the same way, so no rounding enters the merges (GB300's fp64 rate is
-//    low: fp64 appears only in a few scalar steps).
+//  * At kernel start each CTA issues 1-D bulk copies of its slice of the
+//    rows it needs into shared memory (about 72 KB for K = 4 and vocab
+//    32,000 with 16-CTA clusters, three CTAs per SM); more rows cycle
+//    through a ring of slots.  The loops stay rolled: the kernel's code has
+//    to fit the instruction cache, since every warp runs it once.
+//  * Pass 1: one warp per staged piece; a sweep for the piece's maximum
+//    fixes an integer reference exponent E >= max(x * log2 e), a second
+//    sweep sums exp2(x * log2 e - E) as a compensated fp32 pair.  Warps,
+//    CTAs and the cluster merge partial sums by exact power-of-two scaling,
+//    so no rounding enters the merges (GB300's fp64 rate is low: no fp64 on
+//    this path).
 //  * The CTAs exchange slice statistics through distributed shared memory;
 //    every CTA then takes the accept decisions itself (they are scalar).
-//  * Pass 2 weighs only the one or two rows the draw needs, from shared
-//    memory when they stayed resident.  Thread t owns a contiguous run of
+//  * Draws and residual masses weigh only the rows they need, from shared
+//    memory when those stayed resident.  Thread t owns a contiguous run of
 //    its CTA's slice, so (CTA, thread, element) is token order; the CTA
 //    holding the crossing of u * W finds the run by a block scan and that
 //    thread walks its run once more to find the token.
@@ -52,11 +57,12 @@ namespace {
 
 constexpr int kAThreads = 256;
 constexpr int kAWarps = kAThreads / 32;
-constexpr int kMaxRows = 2 * kMaxDraft + 1;
+constexpr int kMaxRows = 2 * kMaxDraft + 1;  // also 2 * kMaxNodes - 1
 constexpr int kStageBytes = 72000;  // staged logits per CTA (3 CTAs per SM)
 constexpr int kMaxSlots = 32;
 constexpr float kL2E = 1.4426950408889634f;
 constexpr int kNoExp = INT_MIN / 4;  // reference exponent of an empty sum
+static_assert(2 * kMaxNodes - 1 <= kMaxRows, "tree rows exceed the row arrays");
 
 // A sum of exp2 terms relative to 2^e, as a compensated fp32 pair.
 struct ESum {
@@ -112,32 +118,375 @@ __device__ __forceinline__ ESum esum_merge(ESum a, ESum b) {
   return r;
 }
 
-struct AcceptShared {
+// p(x) / q(x) for logits a (target) and c (draft) and row normalisers
+// 2^ep * Sp, 2^eq * Sq: 2^d * Sq / Sp with d = (a - c) log2e - (ep - eq)
+// (the same fp32 log2 e as the sums' terms), split as 2^k * 2^frac with
+// a - c and its product with log2 e carried as unevaluated pairs
+// (error-free transformations).  q(x) = 0 gives +inf.
+__device__ __forceinline__ float accept_ratio(float a, float c, int ep,
+                                              float Sp, int eq, float Sq) {
+  const float s = a - c;
+  const float bv = s - a;
+  const float err = (a - (s - bv)) + (-c - bv);
+  const float xh = s * kL2E;
+  const float xl = fmaf(s, kL2E, -xh) + err * kL2E;
+  const float kf = floorf(xh);
+  const float m = exp2f((xh - kf) + xl) * (Sq / Sp);
+  const float k = kf - ((float)ep - (float)eq);
+  return ldexpf(m, (int)fmaxf(fminf(k, 400.f), -400.f));
+}
+
+// Slice statistics of every staged row (read cluster-wide).
+struct StageShared {
   ESum warp_s[kAWarps][kMaxRows];  // pass 1: per-warp partials
-  ESum slice_s[kMaxRows];          // this CTA's slice (read cluster-wide)
+  ESum slice_s[kMaxRows];          // this CTA's slice
   int row_e[kMaxRows];             // row normaliser 2^row_e * row_s
   float row_s[kMaxRows];
-  float mass_hi, mass_lo;          // pass 2: this slice's mass (cluster-wide)
-  int last;                        // pass 2: its last token with w > 0
+  uint64_t full[kMaxSlots];        // staging slots' arrival barriers
+};
+
+// Exchange state of cluster-wide sums and draws (read cluster-wide).
+struct DrawShared {
+  float mass_hi, mass_lo;  // draw: this slice's total weight
+  int last;                // draw: its last token of positive weight
+  float zh[2], zl[2];      // cluster sums, by parity of the sum
   float red_hi[kAWarps], red_lo[kAWarps];
   int red_i[kAWarps];
-  float logit_x[2 * kMaxDraft];    // target / draft logits at the drafts
-  int acc[kMaxDraft];
+  int sel_t;
+};
+
+// Staging of this CTA's slice [s0, s0 + n) of rows 0 .. R-1: item
+// it = (row it / np, piece it % np), psz floats per piece, goes to slot
+// it % slots of the dynamic shared memory xs.  With bulk (16-byte aligned
+// rows) thread 0 moves items with 1-D bulk copies, a wave of `slots` at a
+// time; otherwise all threads copy with plain loads.  When every row is one
+// piece and has a slot, the rows stay resident after pass 1.
+template <class RowPtr>
+struct SliceStage {
+  RowPtr row_ptr;
+  int R, s0, n, psz, np, slots, bulk;
+  float *xs;
+  StageShared *st;
+
+  __device__ int items() const { return R * np; }
+  __device__ int piece_len(int pc) const { return min(psz, n - pc * psz); }
+  __device__ bool resident() const { return np == 1 && slots >= R; }
+  // row r of the slice: shared memory when resident, else global memory
+  __device__ const float *row(int r) const {
+    return resident() ? xs + (size_t)r * psz : row_ptr(r) + s0;
+  }
+
+  __device__ void issue(int it) const {  // thread 0, bulk mode
+    const int r = it / np, pc = it - r * np;
+    const int len = piece_len(pc);
+    const int s = it % slots;
+    if (len <= 0) {  // nothing to copy: the slot's phase still completes
+      mbar_arrive(&st->full[s]);
+      return;
+    }
+    mbar_arrive_expect_tx(&st->full[s], (uint32_t)len * 4u);
+    bulk_g2s(xs + (size_t)s * psz, row_ptr(r) + s0 + pc * psz,
+             (uint32_t)len * 4u, &st->full[s]);
+  }
+
+  // Thread 0 initialises the slot barriers and issues the first wave; the
+  // caller synchronises the block before pass1.
+  __device__ void begin(int tid) const {
+    if (tid == 0 && bulk) {
+      for (int s = 0; s < slots; ++s) mbar_init(&st->full[s], 1);
+      fence_mbar_init();
+      for (int it = 0; it < min(slots, items()); ++it) issue(it);
+    }
+  }
+
+  // Pass 1: one warp per staged piece, in waves of `slots` pieces: a sweep
+  // for the piece's maximum fixes E = ceil(max * log2 e), a second sweep
+  // sums exp2(x * log2 e - E); the warp's partial sums per row (warp_s) are
+  // merged by exact power-of-two scaling.  Returns false if a wait timed
+  // out.  finish() then forms slice_s.
+  __device__ bool pass1(int tid, int lane, int warp) const {
+    bool ok = true;
+    if (lane == 0)
+      for (int r = 0; r < R; ++r) st->warp_s[warp][r] = ESum{kNoExp, 0.f, 0.f};
+    for (int w0 = 0; w0 < items(); w0 += slots) {
+      const int w1 = min(items(), w0 + slots);
+      if (!bulk) {  // plain loads into the wave's slots
+        for (int it = w0; it < w1; ++it) {
+          const int r = it / np, pc = it - r * np;
+          const int len = piece_len(pc);
+          float *x = xs + (size_t)(it - w0) * psz;
+          const float *src = row_ptr(r) + s0 + pc * psz;
+          for (int e = tid; e < ((len + 3) & ~3); e += kAThreads)
+            x[e] = e < len ? __ldg(src + e) : -INFINITY;
+        }
+        __syncthreads();
+      }
+      for (int it = w0 + warp; it < w1; it += kAWarps) {
+        const int r = it / np, pc = it - r * np;
+        const int len = piece_len(pc);
+        if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
+        if (len <= 0) continue;
+        const float4 *x4 =
+            reinterpret_cast<const float4 *>(xs + (size_t)(it - w0) * psz);
+        const int ng = (len + 3) >> 2;
+        float m = -INFINITY;
+#pragma unroll 4
+        for (int g = lane; g < ng; g += 32) {
+          const float4 v = x4[g];
+          m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (!(m > -INFINITY)) continue;  // nothing but -inf (warp-uniform)
+        const int e = (int)ceilf(fminf(m * kL2E, 1.0e9f));
+        const float eb = (float)e;
+        float hi = 0.f, lo = 0.f;
+#pragma unroll 4
+        for (int g = lane; g < ng; g += 32) {
+          const float4 v = x4[g];
+          const float t =
+              (ex2(fmaf(v.x, kL2E, -eb)) + ex2(fmaf(v.y, kL2E, -eb))) +
+              (ex2(fmaf(v.z, kL2E, -eb)) + ex2(fmaf(v.w, kL2E, -eb)));
+          kahan_add(hi, lo, t);
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+          const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+          pair_add(hi, lo, oh, ol);
+        }
+        if (lane == 0)
+          st->warp_s[warp][r] = esum_merge(st->warp_s[warp][r], ESum{e, hi, lo});
+      }
+      if (w1 < items()) {  // ring: the next wave into the same slots
+        __syncthreads();
+        if (tid == 0 && bulk)
+          for (int it = w1; it < min(items(), w1 + slots); ++it) issue(it);
+      }
+    }
+    return ok;
+  }
+
+  __device__ void finish(int tid) const {
+    __syncthreads();
+    if (tid < R) {
+      ESum s{kNoExp, 0.f, 0.f};
+      for (int w = 0; w < kAWarps; ++w) s = esum_merge(s, st->warp_s[w][tid]);
+      st->slice_s[tid] = s;
+    }
+  }
+};
+
+// Warp 0, after the cluster barrier that follows finish(): lane r < R
+// combines row r's slice statistics of all NC CTAs into its normaliser
+// 2^e * S (kept in registers and in row_e / row_s).
+template <int NC>
+__device__ __forceinline__ void row_normalisers(cg::cluster_group &cluster,
+                                                StageShared &st, int R,
+                                                int lane, int &e, float &S) {
+  e = kNoExp;
+  S = 0.f;
+  if (lane < R) {
+    ESum o[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      o[c] = cluster.map_shared_rank(&st, c)->slice_s[lane];
+      e = max(e, o[c].e);
+    }
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (o[c].e != kNoExp) {
+        const float f = pow2i(o[c].e - e);  // exact
+        pair_add(hi, lo, o[c].hi * f, o[c].lo * f);
+      }
+    S = hi + lo;
+    st.row_e[lane] = e;
+    st.row_s[lane] = S;
+  }
+}
+
+// Sum of weight(e) over every CTA's slice (thread runs [e0, e1)), the same
+// compensated pair in every CTA.  One cluster barrier; `parity` alternates
+// between consecutive sums so a slot is rewritten only after a barrier.
+template <int NC, class Weight>
+__device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
+                            const Weight &weight, int e0, int e1, int tid,
+                            int lane, int warp, int parity, float &h,
+                            float &l) {
+  float hi = 0.f, lo = 0.f;
+#pragma unroll 4
+  for (int e = e0; e < e1; ++e) kahan_add(hi, lo, weight(e));
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+    pair_add(hi, lo, oh, ol);
+  }
+  if (lane == 0) {
+    ds.red_hi[warp] = hi;
+    ds.red_lo[warp] = lo;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float h2 = 0.f, l2 = 0.f;
+    for (int w = 0; w < kAWarps; ++w) pair_add(h2, l2, ds.red_hi[w], ds.red_lo[w]);
+    ds.zh[parity] = h2;
+    ds.zl[parity] = l2;
+  }
+  cluster.sync();
+  h = 0.f;
+  l = 0.f;
+  for (int c = 0; c < NC; ++c) {
+    const DrawShared *o = cluster.map_shared_rank(&ds, c);
+    pair_add(h, l, o->zh[parity], o->zl[parity]);
+  }
+}
+
+// Inverse-CDF draw over weight(e) of every CTA's slice: the smallest token
+// whose running sum (token order) exceeds u * total.  Returns false, after a
+// cluster barrier, if the total is zero (nothing written); otherwise one
+// thread of one CTA writes the token to *dst and this CTA has arrived at
+// the exit barrier (no further reads of other CTAs' shared memory).
+template <int NC, class Weight>
+__device__ bool draw_token(cg::cluster_group &cluster, DrawShared &ds,
+                           const Weight &weight, int e0, int e1, float u,
+                           int s0, int crank, int tid, int lane, int warp,
+                           int32_t *dst) {
+  // visit(e, w) sees this thread's run in token order; false stops it
+  auto for_run = [&](auto visit) {
+#pragma unroll 4
+    for (int e = e0; e < e1; ++e)
+      if (!visit(e, weight(e))) return;
+  };
+  float hi = 0.f, lo = 0.f;  // my run's mass
+  int my_last = -1;          // my last slice index with w > 0
+  for_run([&](int e, float w) {
+    if (w > 0.f) my_last = e;
+    kahan_add(hi, lo, w);
+    return true;
+  });
+  // this slice's mass and last positive token; the inclusive warp scan of
+  // the run masses is kept for the draw
+  float ih = hi, il = lo;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float oh = __shfl_up_sync(0xffffffffu, ih, off);
+    const float ol = __shfl_up_sync(0xffffffffu, il, off);
+    if (lane >= off) pair_add(ih, il, oh, ol);
+  }
+  int lst = my_last;
+#pragma unroll
+  for (int off = 16; off; off >>= 1)
+    lst = max(lst, __shfl_xor_sync(0xffffffffu, lst, off));
+  if (lane == 31) {
+    ds.red_hi[warp] = ih;
+    ds.red_lo[warp] = il;
+  }
+  if (lane == 0) ds.red_i[warp] = lst;
+  __syncthreads();
+  if (tid == 0) {
+    float h2 = 0.f, l2 = 0.f;
+    int l = -1;
+    for (int w = 0; w < kAWarps; ++w) {
+      pair_add(h2, l2, ds.red_hi[w], ds.red_lo[w]);
+      l = max(l, ds.red_i[w]);
+    }
+    ds.mass_hi = h2;
+    ds.mass_lo = l2;
+    ds.last = l < 0 ? -1 : s0 + l;
+  }
+  cluster.sync();  // slice masses visible cluster-wide
+  // cumulative masses in CTA order: the same operations in every CTA
+  float Ph = 0.f, Pl = 0.f, loh = 0.f, lol = 0.f, hih = 0.f, hil = 0.f;
+  int last_tok = -1;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const DrawShared *o = cluster.map_shared_rank(&ds, c);
+    const float mh = o->mass_hi, ml = o->mass_lo;
+    const int lt = o->last;
+    if (c == crank) { loh = Ph; lol = Pl; }
+    pair_add(Ph, Pl, mh, ml);
+    if (c == crank) { hih = Ph; hil = Pl; }
+    if (lt >= 0) last_tok = lt;
+  }
+  if (!(Ph > 0.f)) {  // cluster-uniform
+    cluster.sync();   // nobody rewrites ds while it may still be read
+    return false;
+  }
+  cluster_arrive();
+  float Th = u * Ph;  // T = u * W
+  float Tl = fmaf(u, Ph, -Th) + u * Pl;
+  const bool mine_cta = ds.mass_hi > 0.f && !pair_less(Th, Tl, loh, lol) &&
+                        pair_less(Th, Tl, hih, hil);  // CTA-uniform
+  if (mine_cta) {
+    pair_add(Th, Tl, -loh, -lol);  // T within this slice
+    // exclusive prefix of my run: the warp scan, shifted, plus the earlier
+    // warps' totals
+    float xh = __shfl_up_sync(0xffffffffu, ih, 1);
+    float xl = __shfl_up_sync(0xffffffffu, il, 1);
+    if (lane == 0) xh = xl = 0.f;
+    for (int w = 0; w < warp; ++w) pair_add(xh, xl, ds.red_hi[w], ds.red_lo[w]);
+    float nh = xh, nl = xl;  // ... and its inclusive end
+    pair_add(nh, nl, hi, lo);
+    if (tid == 0) ds.sel_t = -1;
+    __syncthreads();
+    if (hi > 0.f && !pair_less(Th, Tl, xh, xl) && pair_less(Th, Tl, nh, nl))
+      ds.sel_t = tid;
+    __syncthreads();
+    if (ds.sel_t < 0) {
+      // rounding left T outside every run: this slice's last token
+      if (tid == 0) *dst = ds.last;
+    } else if (tid == ds.sel_t) {
+      // the run once more, to the first token whose prefix passes T
+      pair_add(Th, Tl, -xh, -xl);  // T within this run
+      float h2 = 0.f, l2 = 0.f;
+      int found = -1, lastpos = -1;
+      for_run([&](int e, float w) {
+        if (w > 0.f) lastpos = e;
+        kahan_add(h2, l2, w);
+        if (w > 0.f && pair_less(Th, Tl, h2, l2)) {
+          found = e;
+          return false;
+        }
+        return true;
+      });
+      if (found < 0) found = lastpos;  // rounding: stay inside this run
+      *dst = s0 + found;
+    }
+  }
+  if (!pair_less(Th, Tl, Ph, Pl) && !mine_cta && crank == NC - 1 && tid == 0)
+    *dst = last_tok;  // rounded past the end
+  return true;
+}
+
+struct AcceptShared {
+  StageShared st;
+  DrawShared ds;
+  float logit_x[2 * kMaxDraft];  // target / draft logits at the drafts
   int tok[kMaxDraft];
   int accept_upto;
   int bad;
-  int sel_t;
-  uint64_t full[kMaxSlots];        // staging slots' arrival barriers
+};
+
+struct TreeShared {
+  StageShared st;
+  DrawShared ds;
+  int par[kMaxNodes], tok[kMaxNodes];
+  int drow[kMaxNodes];     // staged draft row of an inner node, else -1
+  int rowsrc[kMaxRows];    // node whose draft row a staged row r >= N is
+  int path[kMaxNodes];     // accepted nodes
+  float lx_t[kMaxNodes];   // target / draft logits of node c's token in the
+  float lx_d[kMaxNodes];   // rows of its parent
+  float zinv[kMaxNodes];   // 1 / residual mass after each rejected child
+  int R;
+  int bad;
 };
 
 }  // namespace
 
-// Staging: item it = (row it / np, piece it % np) of this CTA's slice, psz
-// floats per piece, goes to slot it % slots of the dynamic shared memory.
-// With bulk != 0 (16-byte aligned rows) thread 0 moves items with 1-D bulk
-// copies, the first `slots` at once; otherwise all threads copy with plain
-// loads.  When every row is one piece and every row has a slot, the rows
-// stay resident for pass 2.
+// ---- linear draft: spec_accept ----
 template <int NC>
 __global__ void __launch_bounds__(kAThreads, 3)
     spec_accept_kernel(const AcceptParams p, int chunk, int psz, int np,
@@ -152,158 +501,44 @@ __global__ void __launch_bounds__(kAThreads, 3)
 
   const int s0 = min(V, crank * chunk);
   const int n = min(V, s0 + chunk) - s0;  // slice length (may be 0)
-  const int items = R2 * np;
 
   // logit row r of this sequence: r <= K target row r, else draft row r-K-1
-  auto row_ptr = [&](int r) -> const float * {
+  auto row_ptr = [=](int r) -> const float * {
     return r <= K ? p.target_logits + ((size_t)b * (K + 1) + r) * V
                   : p.draft_logits + ((size_t)b * K + (r - K - 1)) * V;
   };
-  auto piece_len = [&](int pc) { return min(psz, n - pc * psz); };
-  auto issue = [&](int it) {  // thread 0, bulk mode
-    const int r = it / np, pc = it - r * np;
-    const int len = piece_len(pc);
-    const int s = it % slots;
-    if (len <= 0) {  // nothing to copy: the slot's phase still completes
-      mbar_arrive(&sh.full[s]);
-      return;
-    }
-    mbar_arrive_expect_tx(&sh.full[s], (uint32_t)len * 4u);
-    bulk_g2s(xs + (size_t)s * psz, row_ptr(r) + s0 + pc * psz,
-             (uint32_t)len * 4u, &sh.full[s]);
-  };
-
-  if (tid == 0 && bulk) {
-    for (int s = 0; s < slots; ++s) mbar_init(&sh.full[s], 1);
-    fence_mbar_init();
-    for (int it = 0; it < min(slots, items); ++it) issue(it);
-  }
+  const SliceStage<decltype(row_ptr)> stage{row_ptr, R2, s0, n, psz, np,
+                                            slots, bulk, xs, &sh.st};
+  stage.begin(tid);
   // the draft tokens, read by the last warp (it has the fewest pieces)
   const bool tok_lane = warp == kAWarps - 1 && lane < K;
   const int xtok = tok_lane ? p.draft_tokens[(size_t)b * K + lane] : 0;
   __syncthreads();  // barriers initialised
 
-  // ---- pass 1: every row's slice sum of exp2(x log2e - E) ----
-  // One warp per staged piece, in waves of `slots` pieces: a sweep for the
-  // piece's maximum fixes E = ceil(max * log2 e), a second sweep sums
-  // exp2(x * log2 e - E); the warp's partial sums per row (warp_s) are
-  // merged by exact power-of-two scaling.
-  bool ok = true;
-  if (lane == 0)
-    for (int r = 0; r < R2; ++r) sh.warp_s[warp][r] = ESum{kNoExp, 0.f, 0.f};
-  for (int w0 = 0; w0 < items; w0 += slots) {
-    const int w1 = min(items, w0 + slots);
-    if (!bulk) {  // plain loads into the wave's slots
-      for (int it = w0; it < w1; ++it) {
-        const int r = it / np, pc = it - r * np;
-        const int len = piece_len(pc);
-        float *x = xs + (size_t)(it - w0) * psz;
-        const float *src = row_ptr(r) + s0 + pc * psz;
-        for (int e = tid; e < ((len + 3) & ~3); e += kAThreads)
-          x[e] = e < len ? __ldg(src + e) : -INFINITY;
-      }
-      __syncthreads();
-    }
-    for (int it = w0 + warp; it < w1; it += kAWarps) {
-      const int r = it / np, pc = it - r * np;
-      const int len = piece_len(pc);
-      if (bulk) ok = mbar_wait(&sh.full[it - w0], (it / slots) & 1) && ok;
-      if (len <= 0) continue;
-      const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)(it - w0) * psz);
-      const int ng = (len + 3) >> 2;
-      float m = -INFINITY;
-#pragma unroll 4
-      for (int g = lane; g < ng; g += 32) {
-        const float4 v = x4[g];
-        m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (!(m > -INFINITY)) continue;  // nothing but -inf (warp-uniform)
-      const int e = (int)ceilf(fminf(m * kL2E, 1.0e9f));
-      const float eb = (float)e;
-      float hi = 0.f, lo = 0.f;
-#pragma unroll 4
-      for (int g = lane; g < ng; g += 32) {
-        const float4 v = x4[g];
-        const float t = (ex2(fmaf(v.x, kL2E, -eb)) + ex2(fmaf(v.y, kL2E, -eb))) +
-                        (ex2(fmaf(v.z, kL2E, -eb)) + ex2(fmaf(v.w, kL2E, -eb)));
-        kahan_add(hi, lo, t);
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
-        const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
-        pair_add(hi, lo, oh, ol);
-      }
-      if (lane == 0)
-        sh.warp_s[warp][r] = esum_merge(sh.warp_s[warp][r], ESum{e, hi, lo});
-    }
-    if (w1 < items) {  // ring: the next wave into the same slots
-      __syncthreads();
-      if (tid == 0 && bulk)
-        for (int it = w1; it < min(items, w1 + slots); ++it) issue(it);
-    }
-  }
+  const bool ok = stage.pass1(tid, lane, warp);
   if (tok_lane) {  // the logits at the drafts (from L2, while others sum)
     const bool good = xtok >= 0 && xtok < V;
     sh.tok[lane] = xtok;
     sh.logit_x[lane] = good ? __ldg(row_ptr(lane) + xtok) : 0.f;
     sh.logit_x[K + lane] = good ? __ldg(row_ptr(K + 1 + lane) + xtok) : 0.f;
   }
-  __syncthreads();
-  if (tid < R2) {
-    ESum s{kNoExp, 0.f, 0.f};
-    for (int w = 0; w < kAWarps; ++w) s = esum_merge(s, sh.warp_s[w][tid]);
-    sh.slice_s[tid] = s;
-  }
+  stage.finish(tid);
   cluster.sync();  // #1: slice statistics visible cluster-wide
 
   // ---- normalisers and accept decisions, in warp 0 ----
-  // lane r < R2 holds row r's normaliser 2^e * S; decision i (lane i < K):
-  // u_i <= p_i(x)/q_i(x) = 2^d * S_q / S_p with
-  // d = (a - c) log2e - (E_p - E_q) (the same fp32 log2 e as the sums'
-  // terms), split as 2^k * 2^frac with a - c and its product with log2 e
-  // carried as unevaluated pairs (error-free transformations)
   if (warp == 0) {
-    int e = kNoExp;
-    float S = 0.f;
-    if (lane < R2) {
-      ESum o[NC];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        o[c] = cluster.map_shared_rank(&sh, c)->slice_s[lane];
-        e = max(e, o[c].e);
-      }
-      float hi = 0.f, lo = 0.f;
-#pragma unroll
-      for (int c = 0; c < NC; ++c)
-        if (o[c].e != kNoExp) {
-          const float f = pow2i(o[c].e - e);  // exact
-          pair_add(hi, lo, o[c].hi * f, o[c].lo * f);
-        }
-      S = hi + lo;
-      sh.row_e[lane] = e;
-      sh.row_s[lane] = S;
-    }
+    int e;
+    float S;
+    row_normalisers<NC>(cluster, sh.st, R2, lane, e, S);
     const int eq = __shfl_sync(0xffffffffu, e, min(lane + K + 1, 31));
     const float Sq = __shfl_sync(0xffffffffu, S, min(lane + K + 1, 31));
     bool bad_i = false, acc_i = true;
     if (lane < K) {
       const int x = sh.tok[lane];
       bad_i = x < 0 || x >= V;
-      const float a = sh.logit_x[lane], c = sh.logit_x[K + lane];
-      const float s = a - c;
-      const float bv = s - a;
-      const float err = (a - (s - bv)) + (-c - bv);
-      const float xh = s * kL2E;
-      const float xl = fmaf(s, kL2E, -xh) + err * kL2E;
-      const float kf = floorf(xh);
-      const float m = exp2f((xh - kf) + xl) * (Sq / S);
-      const float k = kf - ((float)e - (float)eq);
-      const float ratio = ldexpf(m, (int)fmaxf(fminf(k, 400.f), -400.f));
-      acc_i = p.uniforms[(size_t)b * (K + 1) + lane] <= ratio;  // q(x) = 0: +inf
+      const float ratio =
+          accept_ratio(sh.logit_x[lane], sh.logit_x[K + lane], e, S, eq, Sq);
+      acc_i = p.uniforms[(size_t)b * (K + 1) + lane] <= ratio;
     }
     const unsigned bad_mask = __ballot_sync(0xffffffffu, bad_i);
     const unsigned rej_mask = __ballot_sync(0xffffffffu, !acc_i) & ((1u << K) - 1u);
@@ -317,134 +552,31 @@ __global__ void __launch_bounds__(kAThreads, 3)
   const int j = bad ? K : sh.accept_upto;
   const float uK = p.uniforms[(size_t)b * (K + 1) + K];
 
-  // ---- pass 2: residual (or bonus) weights, their scan and the draw ----
+  // ---- the draw: residual max(0, p_j - q_j), or the bonus from p_K ----
   // thread t owns slice elements [t*per, t*per + per); per odd, so the
-  // threads' walks through shared memory fall in different banks.  Masses
-  // and prefix sums are compensated fp32 pairs throughout.
+  // threads' walks through shared memory fall in different banks
   const int per = ((n + kAThreads - 1) / kAThreads) | 1;
   const int e0 = min(n, tid * per), e1 = min(n, e0 + per);
-  const bool resident = np == 1 && slots >= R2;
-  bool arrived = false;  // this thread has arrived at the exit barrier
-  for (int attempt = 0; attempt < 2 && !bad; ++attempt) {
+  bool arrived = false;  // this CTA has arrived at the exit barrier
+  for (int attempt = 0; attempt < 2 && !bad && !arrived; ++attempt) {
     const bool residual = (j < K) && attempt == 0;
     const int rt = j;          // target row j (j == K: the bonus row)
     const int rd = K + 1 + j;  // draft row j (residual only)
-    const float *xt = resident ? xs + (size_t)rt * psz : row_ptr(rt) + s0;
-    const float *xd = resident ? xs + (size_t)rd * psz : row_ptr(rd) + s0;
-    const float et = (float)sh.row_e[rt];
-    const float it_ = 1.f / sh.row_s[rt];
-    const float ed = residual ? (float)sh.row_e[rd] : 0.f;
-    const float id_ = residual ? 1.f / sh.row_s[rd] : 0.f;
-    // visit(e, w) sees this thread's run in token order; false stops it
-    auto for_run = [&](auto visit) {
-#pragma unroll 4
-      for (int e = e0; e < e1; ++e) {
-        float w = ex2(fmaf(xt[e], kL2E, -et)) * it_;
-        if (residual) w = fmaxf(w - ex2(fmaf(xd[e], kL2E, -ed)) * id_, 0.f);
-        if (!visit(e, w)) return;
-      }
+    const float *xt = stage.row(rt);
+    const float *xd = stage.row(residual ? rd : rt);
+    const float et = (float)sh.st.row_e[rt];
+    const float it_ = 1.f / sh.st.row_s[rt];
+    const float ed = residual ? (float)sh.st.row_e[rd] : 0.f;
+    const float id_ = residual ? 1.f / sh.st.row_s[rd] : 0.f;
+    auto weight = [&](int e) {
+      float w = ex2(fmaf(xt[e], kL2E, -et)) * it_;
+      if (residual) w = fmaxf(w - ex2(fmaf(xd[e], kL2E, -ed)) * id_, 0.f);
+      return w;
     };
-    float hi = 0.f, lo = 0.f;  // my run's mass
-    int my_last = -1;          // my last slice index with w > 0
-    for_run([&](int e, float w) {
-      if (w > 0.f) my_last = e;
-      kahan_add(hi, lo, w);
-      return true;
-    });
-    // this slice's mass and last positive token; the inclusive warp scan
-    // of the run masses is kept for the draw
-    float ih = hi, il = lo;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float oh = __shfl_up_sync(0xffffffffu, ih, off);
-      const float ol = __shfl_up_sync(0xffffffffu, il, off);
-      if (lane >= off) pair_add(ih, il, oh, ol);
-    }
-    int lst = my_last;
-#pragma unroll
-    for (int off = 16; off; off >>= 1)
-      lst = max(lst, __shfl_xor_sync(0xffffffffu, lst, off));
-    if (lane == 31) {
-      sh.red_hi[warp] = ih;
-      sh.red_lo[warp] = il;
-    }
-    if (lane == 0) sh.red_i[warp] = lst;
-    __syncthreads();
-    if (tid == 0) {
-      float h2 = 0.f, l2 = 0.f;
-      int l = -1;
-      for (int w = 0; w < kAWarps; ++w) {
-        pair_add(h2, l2, sh.red_hi[w], sh.red_lo[w]);
-        l = max(l, sh.red_i[w]);
-      }
-      sh.mass_hi = h2;
-      sh.mass_lo = l2;
-      sh.last = l < 0 ? -1 : s0 + l;
-    }
-    cluster.sync();  // slice masses visible cluster-wide
-    // cumulative masses in CTA order: the same operations in every CTA
-    float Ph = 0.f, Pl = 0.f, loh = 0.f, lol = 0.f, hih = 0.f, hil = 0.f;
-    int last_tok = -1;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const AcceptShared *o = cluster.map_shared_rank(&sh, c);
-      const float mh = o->mass_hi, ml = o->mass_lo;
-      const int lt = o->last;
-      if (c == crank) { loh = Ph; lol = Pl; }
-      pair_add(Ph, Pl, mh, ml);
-      if (c == crank) { hih = Ph; hil = Pl; }
-      if (lt >= 0) last_tok = lt;
-    }
-    if (Ph > 0.f) {
-      cluster_arrive();  // no further reads of other CTAs' shared memory
-      arrived = true;
-      // draw: the smallest x with C(x) > T, T = u_K * W
-      float Th = uK * Ph;
-      float Tl = fmaf(uK, Ph, -Th) + uK * Pl;
-      const bool mine_cta = sh.mass_hi > 0.f && !pair_less(Th, Tl, loh, lol) &&
-                            pair_less(Th, Tl, hih, hil);  // CTA-uniform
-      if (mine_cta) {
-        pair_add(Th, Tl, -loh, -lol);  // T within this slice
-        // exclusive prefix of my run: the warp scan, shifted, plus the
-        // earlier warps' totals
-        float xh = __shfl_up_sync(0xffffffffu, ih, 1);
-        float xl = __shfl_up_sync(0xffffffffu, il, 1);
-        if (lane == 0) xh = xl = 0.f;
-        for (int w = 0; w < warp; ++w) pair_add(xh, xl, sh.red_hi[w], sh.red_lo[w]);
-        float nh = xh, nl = xl;  // ... and its inclusive end
-        pair_add(nh, nl, hi, lo);
-        if (tid == 0) sh.sel_t = -1;
-        __syncthreads();
-        if (hi > 0.f && !pair_less(Th, Tl, xh, xl) && pair_less(Th, Tl, nh, nl))
-          sh.sel_t = tid;
-        __syncthreads();
-        if (sh.sel_t < 0) {
-          // rounding left T outside every run: this slice's last token
-          if (tid == 0) p.out_tokens[(size_t)b * (K + 1) + j] = sh.last;
-        } else if (tid == sh.sel_t) {
-          // the run once more, to the first token whose prefix passes T
-          pair_add(Th, Tl, -xh, -xl);  // T within this run
-          float h2 = 0.f, l2 = 0.f;
-          int found = -1, lastpos = -1;
-          for_run([&](int e, float w) {
-            if (w > 0.f) lastpos = e;
-            kahan_add(h2, l2, w);
-            if (w > 0.f && pair_less(Th, Tl, h2, l2)) {
-              found = e;
-              return false;
-            }
-            return true;
-          });
-          if (found < 0) found = lastpos;  // rounding: stay inside this run
-          p.out_tokens[(size_t)b * (K + 1) + j] = s0 + found;
-        }
-      }
-      if (!pair_less(Th, Tl, Ph, Pl) && !mine_cta && crank == NC - 1 && tid == 0)
-        p.out_tokens[(size_t)b * (K + 1) + j] = last_tok;  // rounded past the end
-      break;
-    }
-    // zero residual mass (impossible in exact arithmetic): draw from p_j
-    cluster.sync();
+    // a zero residual (impossible in exact arithmetic) falls back to p_j
+    arrived = draw_token<NC>(cluster, sh.ds, weight, e0, e1, uK, s0, crank,
+                             tid, lane, warp,
+                             p.out_tokens + (size_t)b * (K + 1) + j);
   }
 
   // ---- accepted drafts, padding and the count (rank 0) ----
@@ -466,6 +598,182 @@ __global__ void __launch_bounds__(kAThreads, 3)
   cluster_wait();
 }
 
+// ---- draft tree: spec_accept_tree ----
+template <int NC>
+__global__ void __launch_bounds__(kAThreads, 3)
+    spec_accept_tree_kernel(const AcceptTreeParams p, int chunk, int psz,
+                            int np, int slots, int bulk) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  const int b = blockIdx.x / NC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = p.num_nodes, V = p.vocab;
+  __shared__ TreeShared sh;
+  extern __shared__ __align__(16) float xs[];
+
+  const int s0 = min(V, crank * chunk);
+  const int n = min(V, s0 + chunk) - s0;  // slice length (may be 0)
+  const float *tl = p.target_logits + (size_t)b * N * V;
+  const float *dl = p.draft_logits + (size_t)b * N * V;
+
+  // the tree: warp 0 reads parents and tokens, checks them, and lists the
+  // rows to stage -- the target rows of all nodes (0 .. N-1), then the
+  // draft rows of the inner nodes (the rows their children came from)
+  if (warp == 0) {
+    int pa = -1, tk = -1;
+    if (lane < N) {
+      pa = p.parents[(size_t)b * N + lane];
+      tk = p.node_tokens[(size_t)b * N + lane];
+    }
+    const bool bad_l =
+        lane < N && (lane == 0 ? pa != -1
+                               : (pa < 0 || pa >= lane || tk < 0 || tk >= V));
+    const unsigned bad_mask = __ballot_sync(0xffffffffu, bad_l);
+    unsigned inner = 0;  // nodes with a child
+    for (int c = 1; c < N; ++c) {
+      const int pc = __shfl_sync(0xffffffffu, pa, c);
+      if (pc >= 0 && pc < c) inner |= 1u << pc;
+    }
+    if (lane < N) {
+      sh.par[lane] = pa;
+      sh.tok[lane] = tk;
+      const bool in = (inner >> lane) & 1u;
+      const int r = N + __popc(inner & ((1u << lane) - 1u));
+      sh.drow[lane] = in ? r : -1;
+      if (in) sh.rowsrc[r] = lane;
+    }
+    if (lane == 0) {
+      sh.bad = bad_mask != 0;
+      sh.R = N + __popc(inner);
+    }
+  }
+  __syncthreads();
+  const int R = sh.R;
+  const bool bad = sh.bad != 0;
+  const int *rowsrc = sh.rowsrc;
+  auto row_ptr = [=](int r) -> const float * {
+    return r < N ? tl + (size_t)r * V : dl + (size_t)rowsrc[r] * V;
+  };
+  const SliceStage<decltype(row_ptr)> stage{row_ptr, R, s0, n, psz, np,
+                                            slots, bulk, xs, &sh.st};
+  stage.begin(tid);
+  __syncthreads();  // barriers initialised
+
+  const bool ok = stage.pass1(tid, lane, warp);
+  // the logits of each node's token in its parent's rows (last warp)
+  if (warp == kAWarps - 1 && lane >= 1 && lane < N && !bad) {
+    const int pa = sh.par[lane], x = sh.tok[lane];
+    sh.lx_t[lane] = __ldg(tl + (size_t)pa * V + x);
+    sh.lx_d[lane] = __ldg(dl + (size_t)pa * V + x);
+  }
+  stage.finish(tid);
+  cluster.sync();  // slice statistics visible cluster-wide
+  if (warp == 0) {
+    int e;
+    float S;
+    row_normalisers<NC>(cluster, sh.st, R, lane, e, S);
+  }
+  __syncthreads();
+
+  const int per = ((n + kAThreads - 1) / kAThreads) | 1;
+  const int e0 = min(n, tid * per), e1 = min(n, e0 + per);
+  bool arrived = false;
+  int n_acc = 0;
+  if (!bad) {
+    int cur = 0, k = 0, parity = 0;
+    const float *xt = nullptr, *xd = nullptr;
+    float et = 0.f, it_ = 0.f, ed = 0.f, id_ = 0.f;
+    // r_k of the current node, its q in `q` (meaningful at an inner node):
+    // r_0 = p, r_j = max(0, r_{j-1} - q) / Z_j
+    auto rk = [&](int e, float &q) {
+      float r = ex2(fmaf(xt[e], kL2E, -et)) * it_;
+      q = ex2(fmaf(xd[e], kL2E, -ed)) * id_;
+      for (int jj = 0; jj < k; ++jj) r = fmaxf(r - q, 0.f) * sh.zinv[jj];
+      return r;
+    };
+    for (;;) {
+      const int rd = sh.drow[cur];
+      xt = stage.row(cur);
+      xd = stage.row(rd >= 0 ? rd : cur);
+      et = (float)sh.st.row_e[cur];
+      it_ = 1.f / sh.st.row_s[cur];
+      ed = rd >= 0 ? (float)sh.st.row_e[rd] : 0.f;
+      id_ = rd >= 0 ? 1.f / sh.st.row_s[rd] : 0.f;
+      k = 0;
+      int next = -1;
+      for (int c = cur + 1; c < N && rd >= 0; ++c) {  // CTA-uniform
+        if (sh.par[c] != cur) continue;
+        // r_k(x) / q(x) = max(0, r_{k-1}(x)/q(x) - 1) / Z_k, from p/q
+        float ratio = accept_ratio(sh.lx_t[c], sh.lx_d[c], sh.st.row_e[cur],
+                                   sh.st.row_s[cur], sh.st.row_e[rd],
+                                   sh.st.row_s[rd]);
+        for (int jj = 0; jj < k; ++jj)
+          ratio = fmaxf(ratio - 1.f, 0.f) * sh.zinv[jj];
+        if (p.uniforms[(size_t)b * N + c] <= ratio) {
+          next = c;
+          break;
+        }
+        // rejected: the residual's mass Z = sum max(0, r_k - q)
+        float zh, zl;
+        cluster_sum<NC>(
+            cluster, sh.ds,
+            [&](int e) {
+              float q;
+              const float r = rk(e, q);
+              return fmaxf(r - q, 0.f);
+            },
+            e0, e1, tid, lane, warp, parity, zh, zl);
+        parity ^= 1;
+        if (zh > 0.f) {  // else (impossible in exact arithmetic) keep r_k
+          __syncthreads();  // zinv[k] is not being read
+          if (tid == 0) sh.zinv[k] = 1.f / (zh + zl);
+          __syncthreads();
+          ++k;
+        }
+      }
+      if (next < 0) break;
+      if (tid == 0) sh.path[n_acc] = next;
+      ++n_acc;
+      cur = next;
+    }
+    // one token from r_k of the last node (p itself at a leaf)
+    int32_t *dst = p.out_tokens + (size_t)b * N + n_acc;
+    const float u0 = p.uniforms[(size_t)b * N];
+    for (int attempt = 0; attempt < 2 && !arrived; ++attempt) {
+      if (attempt == 1) k = 0;  // zero mass by rounding: fall back to p
+      arrived = draw_token<NC>(
+          cluster, sh.ds,
+          [&](int e) {
+            float q;
+            return rk(e, q);
+          },
+          e0, e1, u0, s0, crank, tid, lane, warp, dst);
+    }
+  }
+
+  // ---- accepted path, padding and the count (rank 0) ----
+  if (crank == 0 && tid == 0) {
+    int32_t *out = p.out_tokens + (size_t)b * N;
+    int32_t *nodes = p.out_nodes + (size_t)b * N;
+    if (bad) {
+      for (int k = 0; k < N; ++k) out[k] = nodes[k] = -1;
+      p.n_accepted[b] = -1;
+      atomicOr(&g_status_accept, (unsigned)SVP_DEV_BAD_TOKEN);
+    } else {
+      for (int k = 0; k < n_acc; ++k) {
+        out[k] = sh.tok[sh.path[k]];
+        nodes[k] = sh.path[k];
+      }
+      for (int k = n_acc; k < N; ++k) nodes[k] = -1;
+      for (int k = n_acc + 1; k < N; ++k) out[k] = -1;
+      p.n_accepted[b] = n_acc;
+    }
+  }
+  if (!ok && tid == 0) atomicOr(&g_status_accept, (unsigned)SVP_DEV_TIMEOUT);
+  if (!arrived) cluster_arrive();
+  cluster_wait();
+}
+
 namespace {
 
 struct AcceptPlan {
@@ -474,27 +782,26 @@ struct AcceptPlan {
 };
 
 template <int NC>
-AcceptPlan accept_plan(const AcceptParams &p) {
-  AcceptPlan a;
-  a.chunk = (p.vocab + NC - 1) / NC;
-  a.chunk = (a.chunk + 3) & ~3;  // whole 16-byte groups per slice
-  a.psz = std::min(a.chunk, kStageBytes / 4);
-  a.np = (a.chunk + a.psz - 1) / a.psz;
-  const int items = (2 * p.num_draft + 1) * a.np;
-  a.slots = std::min(std::min(items, kMaxSlots), kStageBytes / (a.psz * 4));
-  const bool aligned = (reinterpret_cast<uintptr_t>(p.target_logits) % 16 == 0) &&
-                       (reinterpret_cast<uintptr_t>(p.draft_logits) % 16 == 0);
-  a.bulk = aligned && (p.vocab % 4 == 0);
-  a.smem = (size_t)a.slots * a.psz * sizeof(float);
-  return a;
+AcceptPlan accept_plan(int vocab, int rows, const float *a, const float *b) {
+  AcceptPlan pl;
+  pl.chunk = (vocab + NC - 1) / NC;
+  pl.chunk = (pl.chunk + 3) & ~3;  // whole 16-byte groups per slice
+  pl.psz = std::min(pl.chunk, kStageBytes / 4);
+  pl.np = (pl.chunk + pl.psz - 1) / pl.psz;
+  const int items = rows * pl.np;
+  pl.slots = std::min(std::min(items, kMaxSlots), kStageBytes / (pl.psz * 4));
+  const bool aligned = (reinterpret_cast<uintptr_t>(a) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(b) % 16 == 0);
+  pl.bulk = aligned && (vocab % 4 == 0);
+  pl.smem = (size_t)pl.slots * pl.psz * sizeof(float);
+  return pl;
 }
 
 template <int NC>
-cudaLaunchConfig_t accept_config(const AcceptParams &p, size_t smem,
-                                 cudaStream_t stream,
+cudaLaunchConfig_t accept_config(int batch, size_t smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.batch * NC), 1, 1);
+  cfg.gridDim = dim3((unsigned)(batch * NC), 1, 1);
   cfg.blockDim = dim3(kAThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -507,69 +814,90 @@ cudaLaunchConfig_t accept_config(const AcceptParams &p, size_t smem,
   return cfg;
 }
 
-template <int NC>
-cudaError_t prepare_kernel() {  // idempotent
-  static std::atomic<bool> done{false};
+template <class Kern>
+cudaError_t prepare_kernel(Kern kern, int nc, std::atomic<bool> &done) {
   if (done.load(std::memory_order_acquire)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(
-      spec_accept_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      kStageBytes);
-  if (e == cudaSuccess && NC > 8)
-    e = cudaFuncSetAttribute(spec_accept_kernel<NC>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBytes);
+  if (e == cudaSuccess && nc > 8)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done.store(true, std::memory_order_release);
   return e;
 }
 
-template <int NC>
-cudaError_t launch_nc(const AcceptParams &p, const AcceptPlan &a,
-                      cudaStream_t stream) {
-  cudaError_t e = prepare_kernel<NC>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = accept_config<NC>(p, a.smem, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, spec_accept_kernel<NC>, p, a.chunk, a.psz, a.np,
-                         a.slots, a.bulk);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-// How many 16-CTA clusters of the kernel with `smem` bytes of staging are
+// How many 16-CTA clusters of `kern` with `smem` bytes of staging are
 // resident at once on the current device (0 if none); cached.
-int max_clusters16(size_t smem) {
-  struct Entry { int dev; size_t smem; int n; };
+template <class Kern>
+int max_clusters16(Kern kern, std::atomic<bool> &prepared, size_t smem) {
+  struct Entry { const void *kern; int dev; size_t smem; int n; };
   static std::mutex mu;
-  static Entry cache[16];
+  static Entry cache[32];
   static int used = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
-    if (cache[i].dev == dev && cache[i].smem == smem) return cache[i].n;
+    if (cache[i].kern == (const void *)kern && cache[i].dev == dev &&
+        cache[i].smem == smem)
+      return cache[i].n;
   int n = 0;
-  if (prepare_kernel<16>() == cudaSuccess) {
-    AcceptParams dummy = {};
-    dummy.batch = 1;
+  if (prepare_kernel(kern, 16, prepared) == cudaSuccess) {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = accept_config<16>(dummy, smem, nullptr, attr);
-    if (cudaOccupancyMaxActiveClusters(&n, spec_accept_kernel<16>, &cfg) !=
-        cudaSuccess)
-      n = 0;
+    cudaLaunchConfig_t cfg = accept_config<16>(1, smem, nullptr, attr);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();  // a refused query leaves 8-CTA clusters
-  if (used < 16) cache[used++] = Entry{dev, smem, n};
+  if (used < 32) cache[used++] = Entry{(const void *)kern, dev, smem, n};
   return n;
+}
+
+std::atomic<bool> g_prep_lin8{false}, g_prep_lin16{false};
+std::atomic<bool> g_prep_tree8{false}, g_prep_tree16{false};
+
+template <int NC, class Kern, class Params>
+cudaError_t launch_accept(Kern kern, std::atomic<bool> &prepared,
+                          const Params &p, int batch, const AcceptPlan &pl,
+                          cudaStream_t stream) {
+  cudaError_t e = prepare_kernel(kern, NC, prepared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = accept_config<NC>(batch, pl.smem, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, kern, p, pl.chunk, pl.psz, pl.np, pl.slots,
+                         pl.bulk);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
+// 16-CTA clusters when the whole batch is resident at once (twice the SMs
+// per sequence, half the slice each); otherwise 8-CTA clusters.
 cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
-  // 16-CTA clusters when the whole batch is resident at once (twice the
-  // SMs per sequence, half the slice each); otherwise 8-CTA clusters
-  const AcceptPlan a16 = accept_plan<16>(p);
-  if (p.batch <= max_clusters16(a16.smem)) return launch_nc<16>(p, a16, stream);
-  return launch_nc<8>(p, accept_plan<8>(p), stream);
+  const int rows = 2 * p.num_draft + 1;
+  const AcceptPlan a16 =
+      accept_plan<16>(p.vocab, rows, p.target_logits, p.draft_logits);
+  if (p.batch <= max_clusters16(spec_accept_kernel<16>, g_prep_lin16, a16.smem))
+    return launch_accept<16>(spec_accept_kernel<16>, g_prep_lin16, p, p.batch,
+                             a16, stream);
+  return launch_accept<8>(
+      spec_accept_kernel<8>, g_prep_lin8, p, p.batch,
+      accept_plan<8>(p.vocab, rows, p.target_logits, p.draft_logits), stream);
+}
+
+cudaError_t launch_spec_accept_tree(const AcceptTreeParams &p,
+                                    cudaStream_t stream) {
+  if (p.batch == 0) return cudaSuccess;
+  const int rows = 2 * p.num_nodes - 1;  // the most a tree can need
+  const AcceptPlan a16 =
+      accept_plan<16>(p.vocab, rows, p.target_logits, p.draft_logits);
+  if (p.batch <= max_clusters16(spec_accept_tree_kernel<16>, g_prep_tree16,
+                                a16.smem))
+    return launch_accept<16>(spec_accept_tree_kernel<16>, g_prep_tree16, p,
+                             p.batch, a16, stream);
+  return launch_accept<8>(
+      spec_accept_tree_kernel<8>, g_prep_tree8, p, p.batch,
+      accept_plan<8>(p.vocab, rows, p.target_logits, p.draft_logits), stream);
 }
 
 cudaError_t read_status_accept(cudaStream_t s, unsigned *flags) {

@@ -241,11 +241,14 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len, int n_sink,
   return plan.ws_total;
 }
 
-int paged_decode_attention(const svp_dims *dims, const void *q,
-                           const void *k_cache, const void *v_cache,
-                           const int32_t *block_table, const int32_t *seq_lens,
-                           int q_len, int n_sink, int window, float scale,
-                           void *out, float *lse, cudaStream_t stream) {
+// The attention call behind both entry points; tree_mask (device, [batch,
+// q_len] uint32 ancestor bits) replaces the causal block when not null.
+static int attention_call(const svp_dims *dims, const void *q,
+                          const void *k_cache, const void *v_cache,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          int q_len, int n_sink, int window,
+                          const uint32_t *tree_mask, float scale, void *out,
+                          float *lse, cudaStream_t stream) {
   t_last_launches = 0;
   int st = check_attention_args(dims, q_len, n_sink, window, scale);
   if (st != SVP_OK) return st;
@@ -309,6 +312,7 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
     p.min_pages = plan.min_pages;
     p.seg_items = plan.seg_items;
     p.qscale = scale * 1.4426950408889634f;
+    p.tree_mask = tree_mask ? tree_mask + (size_t)b0 * q_len : nullptr;
     AttnPlan sub = plan;
     if (nb != bl) {
       plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
@@ -330,6 +334,31 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
   }
   t_last_launches = launches;
   return SVP_OK;
+}
+
+int paged_decode_attention(const svp_dims *dims, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window, float scale,
+                           void *out, float *lse, cudaStream_t stream) {
+  return attention_call(dims, q, k_cache, v_cache, block_table, seq_lens,
+                        q_len, n_sink, window, nullptr, scale, out, lse,
+                        stream);
+}
+
+int paged_tree_attention(const svp_dims *dims, const void *q,
+                         const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         int q_len, const uint32_t *tree_mask, float scale,
+                         void *out, float *lse, cudaStream_t stream) {
+  t_last_launches = 0;
+  const int st = check_attention_args(dims, q_len, 0, 0, scale);
+  if (st != SVP_OK) return st;
+  if (dims->batch == 0) return SVP_OK;
+  if (!tree_mask || reinterpret_cast<uintptr_t>(tree_mask) % 4 != 0)
+    return SVP_ERR_INVALID_ARG;
+  return attention_call(dims, q, k_cache, v_cache, block_table, seq_lens,
+                        q_len, 0, 0, tree_mask, scale, out, lse, stream);
 }
 
 int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
@@ -388,6 +417,37 @@ int spec_accept(int batch, int num_draft, int vocab,
   p.num_draft = num_draft;
   p.vocab = vocab;
   if (launch_spec_accept(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
+  t_last_launches = 1;
+  return SVP_OK;
+}
+
+int spec_accept_tree(int batch, int num_nodes, int vocab,
+                     const float *target_logits, const float *draft_logits,
+                     const int32_t *parents, const int32_t *node_tokens,
+                     const float *uniforms, int32_t *out_tokens,
+                     int32_t *out_nodes, int32_t *n_accepted,
+                     cudaStream_t stream) {
+  t_last_launches = 0;
+  if (batch < 0 || num_nodes < 1 || vocab < 2) return SVP_ERR_INVALID_ARG;
+  if (num_nodes > kMaxNodes || batch > kMaxBatch) return SVP_ERR_UNSUPPORTED;
+  if ((long long)vocab > 8LL * 40000) return SVP_ERR_UNSUPPORTED;
+  if (batch == 0) return SVP_OK;
+  if (!target_logits || !draft_logits || !parents || !node_tokens ||
+      !uniforms || !out_tokens || !out_nodes || !n_accepted)
+    return SVP_ERR_INVALID_ARG;
+  AcceptTreeParams p;
+  p.target_logits = target_logits;
+  p.draft_logits = draft_logits;
+  p.parents = parents;
+  p.node_tokens = node_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_nodes = out_nodes;
+  p.n_accepted = n_accepted;
+  p.batch = batch;
+  p.num_nodes = num_nodes;
+  p.vocab = vocab;
+  if (launch_spec_accept_tree(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
   t_last_launches = 1;
   return SVP_OK;
 }

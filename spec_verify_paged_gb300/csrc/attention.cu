@@ -194,7 +194,8 @@ __device__ __forceinline__ void process_page_fma(
     const T *__restrict__ kp, const T *__restrict__ vp,
     const float (&q)[RB][D / 32], float (&o)[RB][D / 32], float (&m)[RB],
     float (&l)[RB], float *pbuf /* [RB][16] of this warp */, int lane, int j0,
-    bool all_visible, const int (&t)[RB], int n_sink, int window) {
+    bool all_visible, const int (&t)[RB], const uint32_t (&tm)[RB], int base,
+    int n_sink, int window) {
   constexpr int VEC = D / 32;
   float kf[kBlockSize][VEC];
 #pragma unroll
@@ -243,12 +244,8 @@ __device__ __forceinline__ void process_page_fma(
     }
     float s = v[0] + __shfl_xor_sync(kFull, v[0], 1);
 
-    if (!all_visible) {
-      const int tr = t[r];
-      const bool vis = (jkey <= tr) &&
-                       (window == 0 || jkey < n_sink || jkey > tr - window);
-      s = vis ? s : -INFINITY;
-    }
+    if (!all_visible)
+      s = key_visible(jkey, t[r], tm[r], base, n_sink, window) ? s : -INFINITY;
     float pm = s;
     pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 2));
     pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 4));
@@ -329,7 +326,7 @@ __device__ __forceinline__ void process_page_mma(
     const uint32_t (&kb)[D / 16][4], const uint32_t (&vb)[D / 16][4],
     const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4], float (&m)[2],
     float (&lp)[2], int lane, int j0, bool all_visible, const int (&t)[2],
-    int n_sink, int window, float qscale) {
+    const uint32_t (&tm)[2], int base, int n_sink, int window, float qscale) {
   const int tq = lane & 3;
   // S = Q K^T : two n8 tiles (keys 0-7, 8-15), k over D, accumulated in two
   // independent chains (even / odd k steps) to halve the dependent depth
@@ -357,10 +354,8 @@ __device__ __forceinline__ void process_page_mma(
       float v = s[nt][e] * qscale;
       if (!all_visible) {
         const int j = j0 + nt * 8 + 2 * tq + (e & 1);
-        const int tr = t[e >> 1];
-        const bool vis = (j <= tr) &&
-                         (window == 0 || j < n_sink || j > tr - window);
-        v = vis ? v : -INFINITY;
+        v = key_visible(j, t[e >> 1], tm[e >> 1], base, n_sink, window)
+                ? v : -INFINITY;
       }
       s[nt][e] = v;
       mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -621,6 +616,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           t_max = max(t_max, tt);
         }
       }
+      // a page is visible to every row without checks if it ends by the
+      // first row's position (with a tree: before the tree's nodes)
+      if (p.tree_mask) t_min = min(t_min, t0 - 1);
 
       if constexpr (MMA) {
         // ---- tensor-core path: 16 rows, lane rows g and g+8 ----
@@ -629,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float o[D / 8][4];
         float m[2] = {-INFINITY, -INFINITY}, lp[2] = {0.f, 0.f};
         int t[2] = {-1, -1};
+        uint32_t tm[2] = {0u, 0u};
         // Q fragments straight from global memory: rows past the unit's
         // last row read row 0 of the group and are masked to zero, so all
         // loads are unconditional and issue back to back.
@@ -646,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D);
           qmask[r] = valid ? 0xffffffffu : 0u;
           t[r] = valid ? t0 + i : -1;
+          tm[r] = row_tree_bits(p, b, i);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
             process_page_mma<D>(kb, vb, qa, o, m, lp, lane, j0, all_vis, t,
-                                p.n_sink, p.window, p.qscale);
+                                tm, t0, p.n_sink, p.window, p.qscale);
           } else {
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
@@ -726,9 +726,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- CUDA-core path ----
         float q[RB][VEC], o[RB][VEC], m[RB], l[RB];
         int t[RB];
+        uint32_t tm[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
           const int gr = rg * RB + r;
+          tm[r] = 0u;
           m[r] = -INFINITY;
           l[r] = 0.f;
 #pragma unroll
@@ -744,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
             t[r] = t0 + i;
+            tm[r] = row_tree_bits(p, b, i);
           }
         }
         for (int k = first; k < ui.n_pages; k += NSTREAM) {
@@ -772,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             process_page_fma<T, D, RB>(
                 reinterpret_cast<const T *>(sm.kv[s][0]),
                 reinterpret_cast<const T *>(sm.kv[s][1]), q, o, m, l, pbuf,
-                lane, j0, all_vis, t, p.n_sink, p.window);
+                lane, j0, all_vis, t, tm, t0, p.n_sink, p.window);
           }
           if (lane == 0) mbar_arrive(&sm.empty[s]);
         }

@@ -716,11 +716,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             nhi = lim < N ? (int)lim : N;
           }
         }
-        const bool all_vis = __all_sync(kFull, nlo <= 0 && nhi >= N);
+        // a draft tree: node key j = t0 + k is seen by the rows whose node
+        // has bit k set (columns past the last row count as seeing it)
+        uint32_t cb = ~0u;
+        if (p.tree_mask && in_union && j >= t0) {
+          const int k = j - t0;
+          cb = 0u;
+          int i = row0 / p.group, rem = row0 - i * p.group;
+          for (int n = 0; n < N; ++n) {
+            const uint32_t bits = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
+            cb |= ((bits >> k) & 1u) << n;
+            if (++rem == p.group) { rem = 0; ++i; }
+          }
+        }
+        const bool all_vis = __all_sync(kFull, nlo <= 0 && nhi >= N && cb == ~0u);
 #pragma unroll
         for (int n = 0; n < N; ++n) {
           const float x = sv[n] * p.qscale;
-          sv[n] = (all_vis || (n >= nlo && n < nhi)) ? x : -INFINITY;
+          sv[n] = (all_vis || (n >= nlo && n < nhi && ((cb >> n) & 1u)))
+                      ? x : -INFINITY;
         }
 
         // ---- column max over the tile's 128 keys ----

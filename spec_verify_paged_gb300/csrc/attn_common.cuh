@@ -82,6 +82,26 @@ __device__ __forceinline__ void visible_pages(int L, int q_len, int n_sink,
   n_pages = na + (nblk - bs);
 }
 
+// Whether key j is visible to a query at position t whose node in a draft
+// tree has ancestor bits tm (pages: "How speculative decoding doubles LLM
+// speed", step 2 -- causal inside the draft -- and section "Modern
+// architecture variants" -- SpecInfer's tree mask; the StreamingLLM page,
+// section "The StreamingLLM solution" -- sinks and window).  base is the
+// position of the first of the q_len new rows: keys before it are the
+// cached prefix; key base + k is node k, visible iff bit k of tm is set.
+// Without a tree tm is all ones and the test is the causal block.
+__device__ __forceinline__ bool key_visible(int j, int t, uint32_t tm, int base,
+                                            int n_sink, int window) {
+  return j <= t && (j < base || ((tm >> ((j - base) & 31)) & 1u) != 0) &&
+         (window == 0 || j < n_sink || j > t - window);
+}
+
+// Ancestor bits of query position i of sequence b (all ones without a tree).
+__device__ __forceinline__ uint32_t row_tree_bits(const AttnParams &p, int b,
+                                                  int i) {
+  return p.tree_mask ? __ldg(p.tree_mask + (size_t)b * p.q_len + i) : ~0u;
+}
+
 // Logical block of the pidx-th visible page.
 __device__ __forceinline__ int logical_block(const UnitInfo &ui, int pidx) {
   return pidx < ui.n_a ? pidx : ui.b_start + (pidx - ui.n_a);

@@ -13,6 +13,7 @@ constexpr int kBlockSize = 16;     // tokens per KV page
 constexpr int kMaxQLen = 16;
 constexpr int kMaxBatch = 65535;
 constexpr int kMaxDraft = 15;
+constexpr int kMaxNodes = 16;    // draft-tree nodes (= the verify rows)
 
 // One paged_decode_attention launch.
 struct AttnParams {
@@ -37,6 +38,7 @@ struct AttnParams {
   int min_pages;       // fewest items a CTA's slice may hold
   int seg_items;       // items that stand for a segment's fixed cost
   float qscale;        // scale * log2(e)
+  const uint32_t *tree_mask;  // [batch, q_len] ancestor bits, or null
 };
 
 struct AttnPlan {
@@ -107,6 +109,20 @@ struct AcceptParams {
   int batch, num_draft, vocab;
 };
 cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream);
+
+struct AcceptTreeParams {
+  const float *target_logits;  // [batch, N, vocab]
+  const float *draft_logits;   // [batch, N, vocab]
+  const int32_t *parents;      // [batch, N]
+  const int32_t *node_tokens;  // [batch, N]
+  const float *uniforms;       // [batch, N]
+  int32_t *out_tokens;         // [batch, N]
+  int32_t *out_nodes;          // [batch, N]
+  int32_t *n_accepted;         // [batch]
+  int batch, num_nodes, vocab;
+};
+cudaError_t launch_spec_accept_tree(const AcceptTreeParams &p,
+                                    cudaStream_t stream);
 
 // Device status words (one per translation unit): read-and-clear.
 cudaError_t read_status_attention(cudaStream_t s, unsigned *flags);

@@ -84,6 +84,18 @@ def test_attention_null_pointers(lib):
                                       0.1, P, None, None) == -1
 
 
+def test_tree_attention_needs_a_mask(lib):
+    d = _dims()
+    assert lib.paged_tree_attention(ctypes.byref(d), P, P, P, P, P, 3, None,
+                                    0.1, P, P, None) == -1
+    # misaligned mask pointer
+    assert lib.paged_tree_attention(ctypes.byref(d), P, P, P, P, P, 3, 0x1002,
+                                    0.1, P, P, None) == -1
+    # q_len beyond the tree limit
+    assert lib.paged_tree_attention(ctypes.byref(d), P, P, P, P, P, 17, P, 0.1,
+                                    P, P, None) == -2
+
+
 def test_attention_empty_batch_is_a_no_op(lib):
     d = _dims(batch=0)
     assert lib.paged_decode_attention(ctypes.byref(d), None, None, None, None,
@@ -122,6 +134,22 @@ def test_workspace_size_grows_with_work(lib):
 ])
 def test_accept_rejects_bad_sizes(lib, args, expect):
     assert lib.spec_accept(*args, P, P, P, P, P, P, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((-1, 4, 100), -1), ((2, 0, 100), -1), ((2, 4, 1), -1),
+    ((2, 17, 100), -2), ((70000, 4, 100), -2), ((2, 4, 400000), -2),
+])
+def test_accept_tree_rejects_bad_sizes(lib, args, expect):
+    assert lib.spec_accept_tree(*args, *([P] * 8), None) == expect
+
+
+def test_accept_tree_null_pointer_and_empty_batch(lib):
+    ptrs = [P] * 8
+    ptrs[3] = None  # uniforms
+    assert lib.spec_accept_tree(2, 4, 100, *ptrs, None) == -1
+    assert lib.spec_accept_tree(0, 4, 100, *([None] * 8), None) == 0
+    assert lib.svp_last_launch_count() == 0
 
 
 def test_accept_null_pointer(lib):
