@@ -10,7 +10,9 @@ the new query rows over every cached row (decode-7b: 32 sequences, 32/32
 heads, head_dim 128, context U[512, 4096], bf16 16-token pages in a shuffled
 block table); on the verify workloads (q_len > 1) the step ends with
 spec_accept of the q_len - 1 drafts per sequence over a 32,000-token
-vocabulary (its time is reported as `accept_us`).  After the warm-up the
+vocabulary (its time is reported as `accept_us`); the tree-verify workload
+(a 15-node binary draft tree per sequence) runs paged_tree_attention and
+spec_accept_tree instead.  After the warm-up the
 step is captured as CUDA graphs and the timed loop replays them, so the
 host's launch overhead does not pace the GPU.  `value` is query tokens per
 second over the whole job; the KV-read bandwidth of the attention call and
@@ -248,9 +250,16 @@ def oracle_sample(wl, n_seqs, start=0):
     seqs = [(start + i) % B for i in range(n_seqs)]
     rows = np.concatenate([np.arange(b * per, (b + 1) * per) for b in seqs])
     t = time.perf_counter()
-    oracle.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_table,
-                           wl.seq_lens, wl.q_len, wl.cfg.n_sink, wl.cfg.window,
-                           wl.scale, rows=rows.astype(np.int64))
+    if wl.tree_mask is not None:
+        oracle.paged_tree_attention(wl.q, wl.k_cache, wl.v_cache,
+                                    wl.block_table, wl.seq_lens, wl.q_len,
+                                    wl.tree_mask, wl.scale,
+                                    rows=rows.astype(np.int64))
+    else:
+        oracle.paged_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_table,
+                               wl.seq_lens, wl.q_len, wl.cfg.n_sink,
+                               wl.cfg.window, wl.scale,
+                               rows=rows.astype(np.int64))
     return time.perf_counter() - t, n_seqs * wl.q_len
 
 
@@ -287,6 +296,9 @@ def workload_config(wl, split_pages=None):
          "kv_bytes_per_step": tr["kv_bytes"], "seed": cfg.seed,
          "l2": "no flush: each step reads %.2f GB of KV, > 129 MB L2"
                % (tr["kv_bytes"] / 1e9)}
+    if cfg.tree_depth > 0:
+        c["draft_tree"] = {"shape": "complete binary", "depth": cfg.tree_depth,
+                           "nodes": cfg.q_len}
     if split_pages is not None:
         c["split_pages"] = split_pages
     return c, tr
@@ -334,9 +346,25 @@ def run_ours(args):
                       dtype=torch.float32, device=dev)
     # verify workloads (q_len > 1) end with the acceptance step on K =
     # q_len - 1 drafts per sequence, vocab 32,000 (the acceptance workload's
-    # recipe, same seed as the attention inputs)
+    # recipe, same seed as the attention inputs); a draft tree ends with the
+    # tree acceptance over its nodes
+    tree = cfg.tree_depth > 0
+    tm = to_dev(wl.tree_mask.view(np.int32), dev) if tree else None
     acc = None
-    if cfg.q_len > 1:
+    if tree:
+        awl = W.make_tree_accept(batch=cfg.batch, depth=cfg.tree_depth,
+                                 vocab=W.TREE_ACCEPT_CONFIG["vocab"],
+                                 seed=cfg.seed)
+        acc_in = [to_dev(x, dev) for x in (awl.target_logits, awl.draft_logits,
+                                           awl.parents, awl.node_tokens,
+                                           awl.uniforms)]
+        acc_out = tuple(torch.empty(shape, dtype=torch.int32, device=dev)
+                        for shape in ((cfg.batch, cfg.q_len),
+                                      (cfg.batch, cfg.q_len), (cfg.batch,)))
+        acc = (acc_in, acc_out)
+        conf["accept"] = {"batch": cfg.batch, "tree_nodes": cfg.q_len,
+                          "vocab": W.TREE_ACCEPT_CONFIG["vocab"]}
+    elif cfg.q_len > 1:
         awl = W.make_accept(batch=cfg.batch, num_draft=cfg.q_len - 1,
                             vocab=W.ACCEPT_CONFIG["vocab"], seed=cfg.seed)
         acc_in = [to_dev(x, dev) for x in (awl.target_logits, awl.draft_logits,
@@ -349,13 +377,30 @@ def run_ours(args):
                           "vocab": W.ACCEPT_CONFIG["vocab"]}
     stream = torch.cuda.current_stream(dev)
     scale = float(wl.scale)
-    kw = dict(q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
-              scale=scale, out=out, lse=lse, split_pages=args.split_pages,
-              kernel_path=args.kernel_path)
     launches = [0]
 
+    def attn_call(q_, bt_, sl_, out_, lse_, tm_=None):
+        if tree:
+            svp.paged_tree_attention(q_, kc, vc, bt_, sl_, tm_, scale=scale,
+                                     out=out_, lse=lse_,
+                                     split_pages=args.split_pages,
+                                     kernel_path=args.kernel_path)
+        else:
+            svp.paged_decode_attention(
+                q_, kc, vc, bt_, sl_, q_len=cfg.q_len, n_sink=cfg.n_sink,
+                window=cfg.window, scale=scale, out=out_, lse=lse_,
+                split_pages=args.split_pages, kernel_path=args.kernel_path)
+
+    def accept_with(inputs, outputs):
+        if tree:
+            svp.spec_accept_tree(*inputs, out_tokens=outputs[0],
+                                 out_nodes=outputs[1], n_accepted=outputs[2])
+        else:
+            svp.spec_accept(*inputs, out_tokens=outputs[0],
+                            n_accepted=outputs[1])
+
     def accept_call():
-        svp.spec_accept(*acc[0], out_tokens=acc[1][0], n_accepted=acc[1][1])
+        accept_with(acc[0], acc[1])
         return svp.last_launch_count()
 
     def step(ev=None):
@@ -363,7 +408,7 @@ def run_ours(args):
         n = svp.last_launch_count()
         if ev is not None:
             ev[0].record(stream)
-        svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
+        attn_call(q, bt, sl, out, lse, tm)
         n += svp.last_launch_count()
         if ev is not None:
             ev[1].record(stream)
@@ -391,7 +436,7 @@ def run_ours(args):
             svp.kv_append(kn, vn, kc, vc, bt, sl)
         n_app = svp.last_launch_count()
         with torch.cuda.graph(g_attn):
-            svp.paged_decode_attention(q, kc, vc, bt, sl, **kw)
+            attn_call(q, bt, sl, out, lse, tm)
         n_attn = svp.last_launch_count()
         n_acc = 0
         if acc is not None:
@@ -451,31 +496,32 @@ def run_ours(args):
     # one device-to-host copy that the host waits for every step.
     in_parts = [("q", q), ("k_new", kn), ("v_new", vn), ("block_table", bt),
                 ("seq_lens", sl)]
+    if tree:
+        in_parts.append(("tree_mask", tm))
+    acc_names = (("target_logits", "draft_logits", "parents", "node_tokens",
+                  "uniforms") if tree else
+                 ("target_logits", "draft_logits", "draft_tokens", "uniforms"))
     if acc is not None:
-        in_parts += list(zip(("target_logits", "draft_logits", "draft_tokens",
-                              "uniforms"), acc[0]))
+        in_parts += list(zip(acc_names, acc[0]))
     h_in, d_in, d_views = pack_buffers(in_parts, dev)
     for name, t in in_parts:
         host_view(h_in, d_views[name]).copy_(t.cpu())
     out_parts = [("out", out), ("lse", lse)]
+    res_names = (("out_tokens", "out_nodes", "n_accepted") if tree else
+                 ("out_tokens", "n_accepted"))
     if acc is not None:
-        out_parts += list(zip(("out_tokens", "n_accepted"), acc[1]))
+        out_parts += list(zip(res_names, acc[1]))
     h_res, d_res, r_views = pack_buffers(out_parts, dev)
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         svp.kv_append(d_views["k_new"], d_views["v_new"], kc, vc,
                       d_views["block_table"], d_views["seq_lens"])
-        svp.paged_decode_attention(
-            d_views["q"], kc, vc, d_views["block_table"], d_views["seq_lens"],
-            q_len=cfg.q_len, n_sink=cfg.n_sink, window=cfg.window,
-            scale=scale, out=r_views["out"], lse=r_views["lse"],
-            split_pages=args.split_pages, kernel_path=args.kernel_path)
+        attn_call(d_views["q"], d_views["block_table"], d_views["seq_lens"],
+                  r_views["out"], r_views["lse"], d_views.get("tree_mask"))
         if acc is not None:
-            svp.spec_accept(d_views["target_logits"], d_views["draft_logits"],
-                            d_views["draft_tokens"], d_views["uniforms"],
-                            out_tokens=r_views["out_tokens"],
-                            n_accepted=r_views["n_accepted"])
+            accept_with([d_views[k] for k in acc_names],
+                        [r_views[k] for k in res_names])
         h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(args.warmup):
