@@ -74,6 +74,10 @@ def _load():
             lib.oracle_spec_accept_tree.argtypes = (
                 [i32] * 3 + [vp] * 10 + [ctypes.c_double])
             lib.oracle_spec_accept_tree.restype = i32
+            lib.oracle_spec_accept_ex.argtypes = (
+                [i32] * 3 + [vp] * 4 + [ctypes.c_double, vp, i32, vp, vp, vp,
+                                        ctypes.c_double])
+            lib.oracle_spec_accept_ex.restype = i32
             _lib = lib
     return _lib
 
@@ -269,3 +273,34 @@ def spec_accept_tree(target_logits, draft_logits, parents, node_tokens,
         raise ValueError(f"oracle_spec_accept_tree failed with status {st}")
     return {"out_tokens": out, "out_nodes": nodes, "n_accepted": nacc,
             "near_boundary": near, "residual_fallback": fb}
+
+
+def spec_accept_ex(target_logits, draft_logits, draft_tokens, uniforms,
+                   temperature=1.0, allowed=None, greedy=False,
+                   eps=BOUNDARY_EPS):
+    """spec_accept with the verify epilogue (see oracle.h): temperature,
+    allowed [B, K+1, ceil(V/32)] uint32 token masks (or None), greedy.
+    Returns dict(out_tokens, n_accepted, near_boundary)."""
+    lib = _load()
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    assert draft_logits.shape == (B, K, V)
+    assert draft_tokens.shape == (B, K) and uniforms.shape == (B, K + 1)
+    tl = _c(target_logits, np.float32)
+    dl = _c(draft_logits, np.float32)
+    dt = _c(draft_tokens, np.int32)
+    un = _c(uniforms, np.float32)
+    al = None
+    if allowed is not None:
+        al = _c(allowed, np.uint32)
+        assert al.shape == (B, K + 1, (V + 31) // 32)
+    out = np.full((B, K + 1), -1, np.int32)
+    nacc = np.zeros((B,), np.int32)
+    near = np.zeros((B,), np.int32)
+    st = lib.oracle_spec_accept_ex(B, K, V, _ptr(tl), _ptr(dl), _ptr(dt),
+                                   _ptr(un), float(temperature), _ptr(al),
+                                   int(bool(greedy)), _ptr(out), _ptr(nacc),
+                                   _ptr(near), float(eps))
+    if st != 0:
+        raise ValueError(f"oracle_spec_accept_ex failed with status {st}")
+    return {"out_tokens": out, "n_accepted": nacc, "near_boundary": near}

@@ -19,6 +19,10 @@
  *  [SL]  "How StreamingLLM stabilizes million-token streams via attention
  *        sinks" (dothoosh.com): sections "The softmax problem",
  *        "Why sliding windows fail", "The StreamingLLM solution".
+ *  [MD]  "How Moondream cut VLM inference latency by 35% via pipelined
+ *        decoding" (dothoosh.com): section "Mechanism one: ping-pong slots"
+ *        and "Mechanism two: forward first, then sample" (constrained
+ *        decoding sets disallowed tokens' logits to -inf before sampling).
  *  [SP]  "Speculative decoding: how AI models get faster without getting
  *        bigger" (aioapex.com): sections "What speculative decoding does" and
  *        "Real-world adoption" (tree speculation, longest accepted path).
@@ -543,5 +547,129 @@ int oracle_spec_accept_tree(int batch, int num_nodes, int vocab,
     if (residual_fallback) residual_fallback[b] = fallback;
   }
   free(r); free(qd);
+  return status;
+}
+
+/* ---- the verify epilogue: temperature, constrained decoding, greedy ----
+ * [SD] "Deployment limits": sampling temperature T (the distributions are
+ * softmax(logits / T) for both models); [MD] section "Mechanism two:
+ * forward first, then sample" (constrained decoding): tokens the grammar
+ * does not allow get logit -inf
+ * before sampling; greedy verification accepts a draft iff it is the
+ * target's most likely token.  Readings: mask row i applies to target row
+ * i and draft row i; a draft token the mask excludes has p(x) = 0 and is
+ * rejected; greedy ties go to the smallest token index. */
+
+/* softmax of one logit row at temperature T over the allowed tokens
+ * (allowed == NULL: all); excluded tokens get probability 0. */
+static void softmax_row_ex(const float *logits, int vocab, double inv_t,
+                           const uint32_t *allowed, double *p) {
+  double m = -INFINITY;
+  for (int x = 0; x < vocab; ++x) {
+    if (allowed && !((allowed[x >> 5] >> (x & 31)) & 1u)) continue;
+    const double v = (double)logits[x] * inv_t;
+    if (v > m) m = v;
+  }
+  double z = 0.0;
+  for (int x = 0; x < vocab; ++x) {
+    if (allowed && !((allowed[x >> 5] >> (x & 31)) & 1u)) {
+      p[x] = 0.0;
+      continue;
+    }
+    p[x] = exp((double)logits[x] * inv_t - m);
+    z += p[x];
+  }
+  for (int x = 0; x < vocab; ++x) p[x] /= z;
+}
+
+/* most likely allowed token of a logit row, smallest index on ties */
+static int argmax_row(const float *logits, int vocab, const uint32_t *allowed) {
+  int best = -1;
+  for (int x = 0; x < vocab; ++x) {
+    if (allowed && !((allowed[x >> 5] >> (x & 31)) & 1u)) continue;
+    if (best < 0 || logits[x] > logits[best]) best = x;
+  }
+  return best;
+}
+
+int oracle_spec_accept_ex(int batch, int num_draft, int vocab,
+                          const float *target_logits,
+                          const float *draft_logits,
+                          const int32_t *draft_tokens, const float *uniforms,
+                          double temperature, const uint32_t *allowed,
+                          int greedy, int32_t *out_tokens,
+                          int32_t *n_accepted, int32_t *near_boundary,
+                          double eps) {
+  if (batch < 0 || num_draft < 1 || vocab < 2) return -1;
+  if (!greedy && !(temperature > 0.0)) return -1;
+  const int K = num_draft;
+  const int words = (vocab + 31) / 32;
+  const double inv_t = greedy ? 1.0 : 1.0 / temperature;
+  double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *w = (double *)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !qd || !w) { free(p); free(qd); free(w); return -1; }
+  int status = 0;
+  for (int b = 0; b < batch && status == 0; ++b) {
+    int32_t *emit = out_tokens + (size_t)b * (K + 1);
+    const float *u = uniforms + (size_t)b * (K + 1);
+    int near = 0, n_out = 0, j = K;
+    for (int k = 0; k <= K; ++k) emit[k] = -1;
+    for (int i = 0; i < K; ++i) {
+      const int x = draft_tokens[(size_t)b * K + i];
+      if (x < 0 || x >= vocab) status = -4;
+    }
+    if (status) break;
+    for (int i = 0; i < K; ++i) {
+      const int x = draft_tokens[(size_t)b * K + i];
+      const float *tl = target_logits + ((size_t)b * (K + 1) + i) * vocab;
+      const float *dl = draft_logits + ((size_t)b * K + i) * vocab;
+      const uint32_t *al =
+          allowed ? allowed + ((size_t)b * (K + 1) + i) * words : NULL;
+      const int ok_x = !al || ((al[x >> 5] >> (x & 31)) & 1u);
+      if (greedy) {
+        if (ok_x && x == argmax_row(tl, vocab, al)) {
+          emit[n_out++] = x;
+          continue;
+        }
+        emit[n_out++] = argmax_row(tl, vocab, al);
+        j = i;
+        break;
+      }
+      softmax_row_ex(tl, vocab, inv_t, al, p);
+      softmax_row_ex(dl, vocab, inv_t, al, qd);
+      const double r = (double)u[i];
+      const double ratio = !ok_x ? 0.0 : (qd[x] > 0.0) ? p[x] / qd[x] : INFINITY;
+      if (ok_x && fabs(r - ratio) < eps) near = 1;
+      if (ok_x && r <= ratio) {
+        emit[n_out++] = x;
+        continue;
+      }
+      double mass = 0.0;
+      for (int y = 0; y < vocab; ++y) {
+        w[y] = (p[y] - qd[y] > 0.0) ? p[y] - qd[y] : 0.0;
+        mass += w[y];
+      }
+      if (mass == 0.0)
+        for (int y = 0; y < vocab; ++y) w[y] = p[y];
+      emit[n_out++] = inverse_cdf(w, vocab, (double)u[K], eps, &near);
+      j = i;
+      break;
+    }
+    if (j == K) { /* every draft accepted: the bonus from the last row */
+      const float *tl = target_logits + ((size_t)b * (K + 1) + K) * vocab;
+      const uint32_t *al =
+          allowed ? allowed + ((size_t)b * (K + 1) + K) * words : NULL;
+      if (greedy) {
+        emit[n_out++] = argmax_row(tl, vocab, al);
+      } else {
+        softmax_row_ex(tl, vocab, inv_t, al, p);
+        emit[n_out++] = inverse_cdf(p, vocab, (double)u[K], eps, &near);
+      }
+    }
+    n_accepted[b] = j;
+    if (near_boundary) near_boundary[b] = near;
+  }
+  free(p); free(qd); free(w);
   return status;
 }

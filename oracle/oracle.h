@@ -96,6 +96,23 @@ int oracle_spec_accept(int batch, int num_draft, int vocab,
                        int32_t *near_boundary, int32_t *residual_fallback,
                        double eps);
 
+/* spec_accept with the verify epilogue: both distributions at temperature
+ * T (softmax(logits / T)); allowed (may be NULL) [batch, K+1, (vocab+31)/32]
+ * uint32 bit masks of the tokens position i may emit (row i applies to
+ * target row i and draft row i; an excluded draft token is rejected); with
+ * greedy != 0 a draft is accepted iff it is the most likely allowed target
+ * token (smallest index on ties), the replacement or bonus is that token,
+ * and temperature and uniforms are not used.  Returns as oracle_spec_accept
+ * (-1 also for temperature <= 0 without greedy). */
+int oracle_spec_accept_ex(int batch, int num_draft, int vocab,
+                          const float *target_logits,
+                          const float *draft_logits,
+                          const int32_t *draft_tokens, const float *uniforms,
+                          double temperature, const uint32_t *allowed,
+                          int greedy, int32_t *out_tokens,
+                          int32_t *n_accepted, int32_t *near_boundary,
+                          double eps);
+
 /* Tree acceptance (draft tree of num_nodes nodes; node 0 is the root, the
  * last token already accepted; parents[c] < c for c >= 1, parents[0] = -1).
  *   target_logits [batch, N, vocab]: row i = target distribution after node i
