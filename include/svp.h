@@ -260,6 +260,41 @@ int spec_accept(int batch, int num_draft, int vocab,
                 const int32_t *draft_tokens, const float *uniforms,
                 int32_t *out_tokens, int32_t *n_accepted, cudaStream_t stream);
 
+/* The verify epilogue for spec_accept (pages: "How speculative decoding
+ * doubles LLM speed", section "Deployment limits" -- sampling temperature;
+ * "How Moondream cut VLM inference latency by 35% via pipelined decoding",
+ * section "Mechanism two: forward first, then sample" -- constrained
+ * decoding sets the logits of disallowed tokens to -inf before sampling).
+ *   temperature  > 0: p = softmax(target / T), q = softmax(draft / T)
+ *                (1 = the logits as given); ignored with greedy
+ *   allowed      NULL, or DEVICE [batch, num_draft+1, (vocab+31)/32] uint32,
+ *                4-byte aligned: bit x%32 of word x/32 of row (b, i) set iff
+ *                position i may emit token x; row i restricts target row i
+ *                and draft row i (disallowed logits read as -inf).  A draft
+ *                token the row excludes is rejected.  Every row must allow
+ *                at least one token.
+ *   greedy       0: rejection sampling; 1: argmax verification -- draft i
+ *                is accepted iff it is the most likely allowed token of
+ *                target row i (smallest index on ties), and the first
+ *                mismatch (or the bonus position) emits that token;
+ *                uniforms are not read. */
+typedef struct {
+  float temperature;
+  const uint32_t *allowed;
+  int greedy;
+} svp_accept_opts;
+
+/* spec_accept with the verify epilogue above applied inside the kernel
+ * (opts == NULL: temperature 1, no mask, sampling -- exactly spec_accept).
+ * Same layouts, outputs and errors as spec_accept, plus
+ * SVP_ERR_INVALID_ARG for temperature <= 0 or non-finite without greedy,
+ * or a misaligned mask. */
+int spec_accept_ex(int batch, int num_draft, int vocab,
+                   const float *target_logits, const float *draft_logits,
+                   const int32_t *draft_tokens, const float *uniforms,
+                   const svp_accept_opts *opts, int32_t *out_tokens,
+                   int32_t *n_accepted, cudaStream_t stream);
+
 /* Tree acceptance (pages: "How speculative decoding doubles LLM speed",
  * sections "Modern architecture variants" -- SpecInfer's draft tree -- and
  * step 3 (sampling); "Speculative decoding: how AI models get faster without

@@ -26,7 +26,7 @@ DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
             "paged_tree_attention",
             "paged_decode_workspace_size",
-            "kv_append", "spec_accept", "spec_accept_tree",
+            "kv_append", "spec_accept", "spec_accept_ex", "spec_accept_tree",
             "svp_read_device_status",
             "svp_status_string", "svp_last_launch_count")
 
@@ -41,6 +41,11 @@ class SvpDims(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t),
                 ("split_pages", ctypes.c_int),
                 ("kernel_path", ctypes.c_int)]
+
+
+class SvpAcceptOpts(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("allowed", ctypes.c_void_p),
+                ("greedy", ctypes.c_int)]
 
 
 class SvpError(RuntimeError):
@@ -82,6 +87,10 @@ def load_library(path: str = LIB_PATH):
         lib.kv_append.restype = i32
         lib.spec_accept.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.spec_accept.restype = i32
+        lib.spec_accept_ex.argtypes = ([i32, i32, i32] + [vp] * 4 +
+                                       [ctypes.POINTER(SvpAcceptOpts)] +
+                                       [vp] * 3)
+        lib.spec_accept_ex.restype = i32
         lib.spec_accept_tree.argtypes = [i32, i32, i32] + [vp] * 9
         lib.spec_accept_tree.restype = i32
         lib.svp_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -261,9 +270,12 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens,
 
 
 def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
-                out_tokens=None, n_accepted=None, stream=None):
-    """Speculative acceptance (include/svp.h: spec_accept).  Returns
-    (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+                out_tokens=None, n_accepted=None, stream=None,
+                temperature=1.0, allowed=None, greedy=False):
+    """Speculative acceptance (include/svp.h: spec_accept; with a
+    temperature other than 1, an `allowed` token mask (int32/uint32
+    [B, K+1, ceil(V/32)] on the GPU) or greedy=True: spec_accept_ex).
+    Returns (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
     lib = load_library()
     for t, n in ((target_logits, "target_logits"),
                  (draft_logits, "draft_logits"), (draft_tokens, "draft_tokens"),
@@ -283,11 +295,27 @@ def spec_accept(target_logits, draft_logits, draft_tokens, uniforms,
         out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
     if n_accepted is None:
         n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
-    st = lib.spec_accept(B, K, V, target_logits.data_ptr(),
-                         draft_logits.data_ptr(), draft_tokens.data_ptr(),
-                         uniforms.data_ptr(), out_tokens.data_ptr(),
-                         n_accepted.data_ptr(), _stream_handle(stream, dev))
-    _check("spec_accept", st)
+    if temperature == 1.0 and allowed is None and not greedy:
+        st = lib.spec_accept(B, K, V, target_logits.data_ptr(),
+                             draft_logits.data_ptr(), draft_tokens.data_ptr(),
+                             uniforms.data_ptr(), out_tokens.data_ptr(),
+                             n_accepted.data_ptr(), _stream_handle(stream, dev))
+        _check("spec_accept", st)
+        return out_tokens, n_accepted
+    if allowed is not None:
+        _cuda_contig(allowed, "allowed")
+        _need(tuple(allowed.shape) == (B, K + 1, (V + 31) // 32) and
+              allowed.element_size() == 4,
+              "allowed must be 32-bit [B, K+1, ceil(V/32)]")
+    opts = SvpAcceptOpts(float(temperature),
+                         None if allowed is None else allowed.data_ptr(),
+                         int(bool(greedy)))
+    st = lib.spec_accept_ex(B, K, V, target_logits.data_ptr(),
+                            draft_logits.data_ptr(), draft_tokens.data_ptr(),
+                            uniforms.data_ptr(), ctypes.byref(opts),
+                            out_tokens.data_ptr(), n_accepted.data_ptr(),
+                            _stream_handle(stream, dev))
+    _check("spec_accept_ex", st)
     return out_tokens, n_accepted
 
 

@@ -119,22 +119,52 @@ __device__ __forceinline__ ESum esum_merge(ESum a, ESum b) {
 }
 
 // p(x) / q(x) for logits a (target) and c (draft) and row normalisers
-// 2^ep * Sp, 2^eq * Sq: 2^d * Sq / Sp with d = (a - c) log2e - (ep - eq)
-// (the same fp32 log2 e as the sums' terms), split as 2^k * 2^frac with
-// a - c and its product with log2 e carried as unevaluated pairs
-// (error-free transformations).  q(x) = 0 gives +inf.
+// 2^ep * Sp, 2^eq * Sq: 2^d * Sq / Sp with d = (a - c) sc - (ep - eq),
+// sc = log2(e) / temperature (the same fp32 scale as the sums' terms),
+// split as 2^k * 2^frac with a - c and its product with sc carried as
+// unevaluated pairs (error-free transformations).  q(x) = 0 gives +inf.
 __device__ __forceinline__ float accept_ratio(float a, float c, int ep,
-                                              float Sp, int eq, float Sq) {
+                                              float Sp, int eq, float Sq,
+                                              float sc) {
   const float s = a - c;
   const float bv = s - a;
   const float err = (a - (s - bv)) + (-c - bv);
-  const float xh = s * kL2E;
-  const float xl = fmaf(s, kL2E, -xh) + err * kL2E;
+  const float xh = s * sc;
+  const float xl = fmaf(s, sc, -xh) + err * sc;
   const float kf = floorf(xh);
   const float m = exp2f((xh - kf) + xl) * (Sq / Sp);
   const float k = kf - ((float)ep - (float)eq);
   return ldexpf(m, (int)fmaxf(fminf(k, 400.f), -400.f));
 }
+
+// Per-element filters applied to staged logits (4 tokens from `tok`, a
+// multiple of 4, of staged row r): none, or the constrained-decoding mask
+// (disallowed tokens become -inf).
+struct NoFilter {
+  static constexpr bool kActive = false;
+  __device__ void operator()(int, int, float4 &) const {}
+  __device__ bool allows(int, int) const { return true; }
+};
+struct TokenMask {
+  static constexpr bool kActive = true;
+  const uint32_t *base;  // [batch, K+1, words] for this call
+  int words, K, b;
+  // mask row of staged row r: target row r <= K, draft row r - K - 1
+  __device__ const uint32_t *row(int r) const {
+    const int pos = r <= K ? r : r - K - 1;
+    return base + ((size_t)b * (K + 1) + pos) * words;
+  }
+  __device__ void operator()(int r, int tok, float4 &v) const {
+    const uint32_t bits = __ldg(row(r) + (tok >> 5)) >> (tok & 31);
+    if (!(bits & 1u)) v.x = -INFINITY;
+    if (!(bits & 2u)) v.y = -INFINITY;
+    if (!(bits & 4u)) v.z = -INFINITY;
+    if (!(bits & 8u)) v.w = -INFINITY;
+  }
+  __device__ bool allows(int r, int tok) const {
+    return (__ldg(row(r) + (tok >> 5)) >> (tok & 31)) & 1u;
+  }
+};
 
 // Slice statistics of every staged row (read cluster-wide).
 struct StageShared {
@@ -161,12 +191,14 @@ struct DrawShared {
 // rows) thread 0 moves items with 1-D bulk copies, a wave of `slots` at a
 // time; otherwise all threads copy with plain loads.  When every row is one
 // piece and has a slot, the rows stay resident after pass 1.
-template <class RowPtr>
+template <class RowPtr, class Filter = NoFilter, bool ARGMAX = false>
 struct SliceStage {
   RowPtr row_ptr;
   int R, s0, n, psz, np, slots, bulk;
   float *xs;
   StageShared *st;
+  Filter filter;
+  float sc;  // log2(e) / temperature
 
   __device__ int items() const { return R * np; }
   __device__ int piece_len(int pc) const { return min(psz, n - pc * psz); }
@@ -200,14 +232,23 @@ struct SliceStage {
   }
 
   // Pass 1: one warp per staged piece, in waves of `slots` pieces: a sweep
-  // for the piece's maximum fixes E = ceil(max * log2 e), a second sweep
-  // sums exp2(x * log2 e - E); the warp's partial sums per row (warp_s) are
-  // merged by exact power-of-two scaling.  Returns false if a wait timed
-  // out.  finish() then forms slice_s.
+  // for the piece's maximum fixes E = ceil(max * sc), a second sweep sums
+  // exp2(x * sc - E); the warp's partial sums per row (warp_s) are merged by
+  // exact power-of-two scaling.  A filter rewrites the staged values on the
+  // first sweep.  In ARGMAX mode the warp keeps the piece's largest value
+  // and its smallest token index instead (as ESum{index, value, 0}).
+  // Returns false if a wait timed out.  finish() then forms slice_s.
+  __device__ static ESum empty() {
+    return ARGMAX ? ESum{INT_MAX, -INFINITY, 0.f} : ESum{kNoExp, 0.f, 0.f};
+  }
+  __device__ static ESum merge(ESum a, ESum b) {
+    if (!ARGMAX) return esum_merge(a, b);
+    return (b.hi > a.hi || (b.hi == a.hi && b.e < a.e)) ? b : a;
+  }
   __device__ bool pass1(int tid, int lane, int warp) const {
     bool ok = true;
     if (lane == 0)
-      for (int r = 0; r < R; ++r) st->warp_s[warp][r] = ESum{kNoExp, 0.f, 0.f};
+      for (int r = 0; r < R; ++r) st->warp_s[warp][r] = empty();
     for (int w0 = 0; w0 < items(); w0 += slots) {
       const int w1 = min(items(), w0 + slots);
       if (!bulk) {  // plain loads into the wave's slots
@@ -226,28 +267,55 @@ struct SliceStage {
         const int len = piece_len(pc);
         if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
         if (len <= 0) continue;
-        const float4 *x4 =
-            reinterpret_cast<const float4 *>(xs + (size_t)(it - w0) * psz);
+        float4 *x4 = reinterpret_cast<float4 *>(xs + (size_t)(it - w0) * psz);
         const int ng = (len + 3) >> 2;
+        const int tok0 = s0 + pc * psz;  // token of the piece's first element
+        if (ARGMAX) {
+          float bv = -INFINITY;
+          int bi = INT_MAX;
+#pragma unroll 4
+          for (int g = lane; g < ng; g += 32) {
+            float4 v = x4[g];
+            if (Filter::kActive) filter(r, tok0 + 4 * g, v);
+            const int t = tok0 + 4 * g;  // first of 4: ties keep the lowest
+            if (v.x > bv) { bv = v.x; bi = t; }
+            if (v.y > bv) { bv = v.y; bi = t + 1; }
+            if (v.z > bv) { bv = v.z; bi = t + 2; }
+            if (v.w > bv) { bv = v.w; bi = t + 3; }
+          }
+#pragma unroll
+          for (int off = 16; off; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+          }
+          if (lane == 0)
+            st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{bi, bv, 0.f});
+          continue;
+        }
         float m = -INFINITY;
 #pragma unroll 4
         for (int g = lane; g < ng; g += 32) {
-          const float4 v = x4[g];
+          float4 v = x4[g];
+          if (Filter::kActive) {
+            filter(r, tok0 + 4 * g, v);
+            x4[g] = v;  // the filtered row is what later reads see
+          }
           m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
         }
 #pragma unroll
         for (int off = 16; off; off >>= 1)
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (!(m > -INFINITY)) continue;  // nothing but -inf (warp-uniform)
-        const int e = (int)ceilf(fminf(m * kL2E, 1.0e9f));
+        const int e = (int)ceilf(fminf(m * sc, 1.0e9f));
         const float eb = (float)e;
         float hi = 0.f, lo = 0.f;
 #pragma unroll 4
         for (int g = lane; g < ng; g += 32) {
           const float4 v = x4[g];
           const float t =
-              (ex2(fmaf(v.x, kL2E, -eb)) + ex2(fmaf(v.y, kL2E, -eb))) +
-              (ex2(fmaf(v.z, kL2E, -eb)) + ex2(fmaf(v.w, kL2E, -eb)));
+              (ex2(fmaf(v.x, sc, -eb)) + ex2(fmaf(v.y, sc, -eb))) +
+              (ex2(fmaf(v.z, sc, -eb)) + ex2(fmaf(v.w, sc, -eb)));
           kahan_add(hi, lo, t);
         }
 #pragma unroll
@@ -257,9 +325,12 @@ struct SliceStage {
           pair_add(hi, lo, oh, ol);
         }
         if (lane == 0)
-          st->warp_s[warp][r] = esum_merge(st->warp_s[warp][r], ESum{e, hi, lo});
+          st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{e, hi, lo});
       }
       if (w1 < items()) {  // ring: the next wave into the same slots
+        // filtered values were written back through the generic proxy;
+        // order them before the bulk copies that overwrite the slots
+        if (Filter::kActive) fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0 && bulk)
           for (int it = w1; it < min(items(), w1 + slots); ++it) issue(it);
@@ -271,8 +342,8 @@ struct SliceStage {
   __device__ void finish(int tid) const {
     __syncthreads();
     if (tid < R) {
-      ESum s{kNoExp, 0.f, 0.f};
-      for (int w = 0; w < kAWarps; ++w) s = esum_merge(s, st->warp_s[w][tid]);
+      ESum s = empty();
+      for (int w = 0; w < kAWarps; ++w) s = merge(s, st->warp_s[w][tid]);
       st->slice_s[tid] = s;
     }
   }
@@ -486,8 +557,8 @@ struct TreeShared {
 
 }  // namespace
 
-// ---- linear draft: spec_accept ----
-template <int NC>
+// ---- linear draft: spec_accept (Filter: NoFilter or TokenMask) ----
+template <int NC, class Filter>
 __global__ void __launch_bounds__(kAThreads, 3)
     spec_accept_kernel(const AcceptParams p, int chunk, int psz, int np,
                        int slots, int bulk) {
@@ -507,8 +578,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
     return r <= K ? p.target_logits + ((size_t)b * (K + 1) + r) * V
                   : p.draft_logits + ((size_t)b * K + (r - K - 1)) * V;
   };
-  const SliceStage<decltype(row_ptr)> stage{row_ptr, R2, s0, n, psz, np,
-                                            slots, bulk, xs, &sh.st};
+  Filter filter;
+  if constexpr (Filter::kActive) filter = Filter{p.allowed, p.words, K, b};
+  const float sc = p.sc;
+  const SliceStage<decltype(row_ptr), Filter> stage{
+      row_ptr, R2, s0, n, psz, np, slots, bulk, xs, &sh.st, filter, sc};
   stage.begin(tid);
   // the draft tokens, read by the last warp (it has the fewest pieces)
   const bool tok_lane = warp == kAWarps - 1 && lane < K;
@@ -536,9 +610,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
     if (lane < K) {
       const int x = sh.tok[lane];
       bad_i = x < 0 || x >= V;
-      const float ratio =
-          accept_ratio(sh.logit_x[lane], sh.logit_x[K + lane], e, S, eq, Sq);
+      const float ratio = accept_ratio(sh.logit_x[lane], sh.logit_x[K + lane],
+                                       e, S, eq, Sq, sc);
       acc_i = p.uniforms[(size_t)b * (K + 1) + lane] <= ratio;
+      // a token the mask excludes has p(x) = 0: rejected
+      if (Filter::kActive && !bad_i && !filter.allows(lane, x)) acc_i = false;
     }
     const unsigned bad_mask = __ballot_sync(0xffffffffu, bad_i);
     const unsigned rej_mask = __ballot_sync(0xffffffffu, !acc_i) & ((1u << K) - 1u);
@@ -569,8 +645,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
     const float ed = residual ? (float)sh.st.row_e[rd] : 0.f;
     const float id_ = residual ? 1.f / sh.st.row_s[rd] : 0.f;
     auto weight = [&](int e) {
-      float w = ex2(fmaf(xt[e], kL2E, -et)) * it_;
-      if (residual) w = fmaxf(w - ex2(fmaf(xd[e], kL2E, -ed)) * id_, 0.f);
+      float w = ex2(fmaf(xt[e], sc, -et)) * it_;
+      if (residual) w = fmaxf(w - ex2(fmaf(xd[e], sc, -ed)) * id_, 0.f);
+      if (Filter::kActive && !filter.allows(rt, s0 + e)) w = 0.f;
       return w;
     };
     // a zero residual (impossible in exact arithmetic) falls back to p_j
@@ -596,6 +673,79 @@ __global__ void __launch_bounds__(kAThreads, 3)
   // no CTA leaves while its shared memory may be read
   if (!arrived) cluster_arrive();
   cluster_wait();
+}
+
+// ---- linear draft, greedy verification (Filter: NoFilter or TokenMask) --
+// A draft is accepted iff it is the target row's most likely allowed token
+// (smallest index on ties); the first mismatch, or the bonus position,
+// emits that token.  Only the K+1 target rows are read.
+template <int NC, class Filter>
+__global__ void __launch_bounds__(kAThreads, 3)
+    spec_accept_greedy_kernel(const AcceptParams p, int chunk, int psz,
+                              int np, int slots, int bulk) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+  const int b = blockIdx.x / NC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.num_draft, V = p.vocab, R = K + 1;
+  __shared__ AcceptShared sh;
+  extern __shared__ __align__(16) float xs[];
+
+  const int s0 = min(V, crank * chunk);
+  const int n = min(V, s0 + chunk) - s0;
+  auto row_ptr = [=](int r) -> const float * {
+    return p.target_logits + ((size_t)b * (K + 1) + r) * V;
+  };
+  Filter filter;
+  if constexpr (Filter::kActive) filter = Filter{p.allowed, p.words, K, b};
+  const SliceStage<decltype(row_ptr), Filter, true> stage{
+      row_ptr, R, s0, n, psz, np, slots, bulk, xs, &sh.st, filter, kL2E};
+  stage.begin(tid);
+  const bool tok_lane = warp == kAWarps - 1 && lane < K;
+  const int xtok = tok_lane ? p.draft_tokens[(size_t)b * K + lane] : 0;
+  __syncthreads();  // barriers initialised
+  const bool ok = stage.pass1(tid, lane, warp);
+  if (tok_lane) sh.tok[lane] = xtok;
+  stage.finish(tid);
+  cluster.sync();  // slice maxima visible cluster-wide
+
+  if (warp == 0 && crank == 0) {
+    // lane r <= K: the row's best (value, token) over the NC slices
+    int best = -1;
+    if (lane < R) {
+      ESum m{INT_MAX, -INFINITY, 0.f};
+      for (int c = 0; c < NC; ++c) {
+        const ESum o = cluster.map_shared_rank(&sh.st, c)->slice_s[lane];
+        if (o.hi > m.hi || (o.hi == m.hi && o.e < m.e)) m = o;
+      }
+      best = m.e == INT_MAX ? -1 : m.e;  // no allowed token: -1
+    }
+    bool bad_i = false, acc_i = true;
+    if (lane < K) {
+      const int x = sh.tok[lane];
+      bad_i = x < 0 || x >= V;
+      acc_i = x == best;
+    }
+    const unsigned bad_mask = __ballot_sync(0xffffffffu, bad_i);
+    const unsigned rej_mask = __ballot_sync(0xffffffffu, !acc_i) & ((1u << K) - 1u);
+    const int j = rej_mask ? __ffs(rej_mask) - 1 : K;
+    const int best_j = __shfl_sync(0xffffffffu, best, j);
+    int32_t *out = p.out_tokens + (size_t)b * (K + 1);
+    if (bad_mask) {
+      if (lane <= K) out[lane] = -1;
+      if (lane == 0) {
+        p.n_accepted[b] = -1;
+        atomicOr(&g_status_accept, (unsigned)SVP_DEV_BAD_TOKEN);
+      }
+    } else {
+      if (lane < j) out[lane] = sh.tok[lane];
+      if (lane == j) out[lane] = best_j;
+      if (lane > j && lane <= K) out[lane] = -1;
+      if (lane == 0) p.n_accepted[b] = j;
+    }
+  }
+  if (!ok && tid == 0) atomicOr(&g_status_accept, (unsigned)SVP_DEV_TIMEOUT);
+  cluster.sync();  // no CTA leaves while its shared memory may be read
 }
 
 // ---- draft tree: spec_accept_tree ----
@@ -654,8 +804,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
   auto row_ptr = [=](int r) -> const float * {
     return r < N ? tl + (size_t)r * V : dl + (size_t)rowsrc[r] * V;
   };
-  const SliceStage<decltype(row_ptr)> stage{row_ptr, R, s0, n, psz, np,
-                                            slots, bulk, xs, &sh.st};
+  const SliceStage<decltype(row_ptr)> stage{
+      row_ptr, R, s0, n, psz, np, slots, bulk, xs, &sh.st, NoFilter{}, kL2E};
   stage.begin(tid);
   __syncthreads();  // barriers initialised
 
@@ -706,7 +856,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
         // r_k(x) / q(x) = max(0, r_{k-1}(x)/q(x) - 1) / Z_k, from p/q
         float ratio = accept_ratio(sh.lx_t[c], sh.lx_d[c], sh.st.row_e[cur],
                                    sh.st.row_s[cur], sh.st.row_e[rd],
-                                   sh.st.row_s[rd]);
+                                   sh.st.row_s[rd], kL2E);
         for (int jj = 0; jj < k; ++jj)
           ratio = fmaxf(ratio - 1.f, 0.f) * sh.zinv[jj];
         if (p.uniforms[(size_t)b * N + c] <= ratio) {
@@ -872,17 +1022,43 @@ cudaError_t launch_accept(Kern kern, std::atomic<bool> &prepared,
 
 // 16-CTA clusters when the whole batch is resident at once (twice the SMs
 // per sequence, half the slice each); otherwise 8-CTA clusters.
-cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream) {
-  if (p.batch == 0) return cudaSuccess;
-  const int rows = 2 * p.num_draft + 1;
+template <class K16, class K8>
+cudaError_t launch_linear(K16 k16, std::atomic<bool> &prep16, K8 k8,
+                          std::atomic<bool> &prep8, const AcceptParams &p,
+                          int rows) {
   const AcceptPlan a16 =
       accept_plan<16>(p.vocab, rows, p.target_logits, p.draft_logits);
-  if (p.batch <= max_clusters16(spec_accept_kernel<16>, g_prep_lin16, a16.smem))
-    return launch_accept<16>(spec_accept_kernel<16>, g_prep_lin16, p, p.batch,
-                             a16, stream);
+  if (p.batch <= max_clusters16(k16, prep16, a16.smem))
+    return launch_accept<16>(k16, prep16, p, p.batch, a16, p.stream);
   return launch_accept<8>(
-      spec_accept_kernel<8>, g_prep_lin8, p, p.batch,
-      accept_plan<8>(p.vocab, rows, p.target_logits, p.draft_logits), stream);
+      k8, prep8, p, p.batch,
+      accept_plan<8>(p.vocab, rows, p.target_logits, p.draft_logits), p.stream);
+}
+
+std::atomic<bool> g_prep_var[6][2];  // masked / greedy variants, by NC
+
+cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream) {
+  if (p.batch == 0) return cudaSuccess;
+  AcceptParams q = p;
+  q.stream = stream;
+  const int rows = 2 * p.num_draft + 1;
+  if (p.greedy) {
+    if (p.allowed)
+      return launch_linear(spec_accept_greedy_kernel<16, TokenMask>,
+                           g_prep_var[0][1],
+                           spec_accept_greedy_kernel<8, TokenMask>,
+                           g_prep_var[0][0], q, p.num_draft + 1);
+    return launch_linear(spec_accept_greedy_kernel<16, NoFilter>,
+                         g_prep_var[1][1],
+                         spec_accept_greedy_kernel<8, NoFilter>,
+                         g_prep_var[1][0], q, p.num_draft + 1);
+  }
+  if (p.allowed)
+    return launch_linear(spec_accept_kernel<16, TokenMask>, g_prep_var[2][1],
+                         spec_accept_kernel<8, TokenMask>, g_prep_var[2][0], q,
+                         rows);
+  return launch_linear(spec_accept_kernel<16, NoFilter>, g_prep_lin16,
+                       spec_accept_kernel<8, NoFilter>, g_prep_lin8, q, rows);
 }
 
 cudaError_t launch_spec_accept_tree(const AcceptTreeParams &p,

@@ -393,15 +393,22 @@ int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
   return SVP_OK;
 }
 
-int spec_accept(int batch, int num_draft, int vocab,
-                const float *target_logits, const float *draft_logits,
-                const int32_t *draft_tokens, const float *uniforms,
-                int32_t *out_tokens, int32_t *n_accepted,
-                cudaStream_t stream) {
+int spec_accept_ex(int batch, int num_draft, int vocab,
+                   const float *target_logits, const float *draft_logits,
+                   const int32_t *draft_tokens, const float *uniforms,
+                   const svp_accept_opts *opts, int32_t *out_tokens,
+                   int32_t *n_accepted, cudaStream_t stream) {
   t_last_launches = 0;
   if (batch < 0 || num_draft < 1 || vocab < 2) return SVP_ERR_INVALID_ARG;
   if (num_draft > kMaxDraft || batch > kMaxBatch) return SVP_ERR_UNSUPPORTED;
   if ((long long)vocab > 8LL * 40000) return SVP_ERR_UNSUPPORTED;
+  const float temperature = opts ? opts->temperature : 1.0f;
+  const bool greedy = opts && opts->greedy;
+  if (!greedy && !(std::isfinite(temperature) && temperature > 0.f))
+    return SVP_ERR_INVALID_ARG;
+  const uint32_t *allowed = opts ? opts->allowed : nullptr;
+  if (allowed && reinterpret_cast<uintptr_t>(allowed) % 4 != 0)
+    return SVP_ERR_INVALID_ARG;
   if (batch == 0) return SVP_OK;
   if (!target_logits || !draft_logits || !draft_tokens || !uniforms ||
       !out_tokens || !n_accepted)
@@ -416,9 +423,24 @@ int spec_accept(int batch, int num_draft, int vocab,
   p.batch = batch;
   p.num_draft = num_draft;
   p.vocab = vocab;
+  p.sc = 1.4426950408889634f / (greedy ? 1.0f : temperature);
+  p.allowed = allowed;
+  p.words = (vocab + 31) / 32;
+  p.greedy = greedy ? 1 : 0;
+  p.stream = stream;
   if (launch_spec_accept(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
   t_last_launches = 1;
   return SVP_OK;
+}
+
+int spec_accept(int batch, int num_draft, int vocab,
+                const float *target_logits, const float *draft_logits,
+                const int32_t *draft_tokens, const float *uniforms,
+                int32_t *out_tokens, int32_t *n_accepted,
+                cudaStream_t stream) {
+  return spec_accept_ex(batch, num_draft, vocab, target_logits, draft_logits,
+                        draft_tokens, uniforms, nullptr, out_tokens,
+                        n_accepted, stream);
 }
 
 int spec_accept_tree(int batch, int num_nodes, int vocab,

@@ -107,6 +107,11 @@ struct AcceptParams {
   int32_t *out_tokens;
   int32_t *n_accepted;
   int batch, num_draft, vocab;
+  float sc;                  // log2(e) / temperature
+  const uint32_t *allowed;   // [batch, K+1, words] token masks, or null
+  int words;                 // (vocab + 31) / 32
+  int greedy;                // argmax verification
+  cudaStream_t stream;       // set by the launcher
 };
 cudaError_t launch_spec_accept(const AcceptParams &p, cudaStream_t stream);
 

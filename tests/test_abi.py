@@ -152,6 +152,24 @@ def test_accept_tree_null_pointer_and_empty_batch(lib):
     assert lib.svp_last_launch_count() == 0
 
 
+def test_accept_ex_checks_its_options(lib):
+    from spec_verify_paged_gb300.binding import SvpAcceptOpts
+    bad_t = SvpAcceptOpts(0.0, None, 0)
+    assert lib.spec_accept_ex(2, 4, 100, P, P, P, P, ctypes.byref(bad_t), P, P,
+                              None) == -1
+    nan_t = SvpAcceptOpts(float("nan"), None, 0)
+    assert lib.spec_accept_ex(2, 4, 100, P, P, P, P, ctypes.byref(nan_t), P, P,
+                              None) == -1
+    odd_mask = SvpAcceptOpts(1.0, 0x1002, 0)
+    assert lib.spec_accept_ex(2, 4, 100, P, P, P, P, ctypes.byref(odd_mask), P,
+                              P, None) == -1
+    # greedy ignores the temperature; an empty batch launches nothing
+    greedy = SvpAcceptOpts(0.0, None, 1)
+    assert lib.spec_accept_ex(0, 4, 100, P, P, P, P, ctypes.byref(greedy), P,
+                              P, None) == 0
+    assert lib.spec_accept_ex(2, 16, 100, P, P, P, P, None, P, P, None) == -2
+
+
 def test_accept_null_pointer(lib):
     assert lib.spec_accept(2, 4, 100, P, None, P, P, P, P, None) == -1
     assert lib.spec_accept(0, 4, 100, None, None, None, None, None, None,
