@@ -280,6 +280,10 @@ def cpu_baseline(wl, budget_s=10.0, max_passes=20):
                       f"fp64, one thread), {total_t:.1f} s"}
 
 
+def tokens_per_step_of(cfg):
+    return cfg.batch * cfg.q_len
+
+
 def workload_config(wl, split_pages=None):
     cfg = wl.cfg
     tr = A.attention_traffic(wl.seq_lens, cfg.q_len, cfg.num_q_heads,
@@ -351,6 +355,7 @@ def run_ours(args):
     tree = cfg.tree_depth > 0
     tm = to_dev(wl.tree_mask.view(np.int32), dev) if tree else None
     acc = None
+    acc_opts = {}
     if tree:
         awl = W.make_tree_accept(batch=cfg.batch, depth=cfg.tree_depth,
                                  vocab=W.TREE_ACCEPT_CONFIG["vocab"],
@@ -375,6 +380,26 @@ def run_ours(args):
         acc = (acc_in, acc_out)
         conf["accept"] = {"batch": cfg.batch, "num_draft": cfg.q_len - 1,
                           "vocab": W.ACCEPT_CONFIG["vocab"]}
+        # the verify epilogue: temperature, token mask, greedy
+        acc_opts = {}
+        if args.temperature != 1.0:
+            acc_opts["temperature"] = args.temperature
+        if args.greedy:
+            acc_opts["greedy"] = True
+        if args.allowed_density > 0:
+            V = W.ACCEPT_CONFIG["vocab"]
+            mrng = np.random.default_rng(cfg.seed + 7)
+            allowed = mrng.random((cfg.batch, cfg.q_len, V)) < args.allowed_density
+            allowed[..., 0] = True
+            words = (V + 31) // 32
+            pad = np.zeros((cfg.batch, cfg.q_len, words * 32), bool)
+            pad[..., :V] = allowed
+            bits = np.packbits(pad, axis=-1, bitorder="little").view(np.int32)
+            acc_opts["allowed"] = to_dev(np.ascontiguousarray(bits), dev)
+        if acc_opts:
+            conf["accept"]["epilogue"] = {
+                "temperature": args.temperature, "greedy": bool(args.greedy),
+                "allowed_density": args.allowed_density}
     stream = torch.cuda.current_stream(dev)
     scale = float(wl.scale)
     launches = [0]
@@ -391,13 +416,14 @@ def run_ours(args):
                 window=cfg.window, scale=scale, out=out_, lse=lse_,
                 split_pages=args.split_pages, kernel_path=args.kernel_path)
 
-    def accept_with(inputs, outputs):
+    def accept_with(inputs, outputs, opts=None):
+        opts = acc_opts if opts is None else opts
         if tree:
             svp.spec_accept_tree(*inputs, out_tokens=outputs[0],
                                  out_nodes=outputs[1], n_accepted=outputs[2])
         else:
             svp.spec_accept(*inputs, out_tokens=outputs[0],
-                            n_accepted=outputs[1])
+                            n_accepted=outputs[1], **opts)
 
     def accept_call():
         accept_with(acc[0], acc[1])
@@ -503,6 +529,8 @@ def run_ours(args):
                  ("target_logits", "draft_logits", "draft_tokens", "uniforms"))
     if acc is not None:
         in_parts += list(zip(acc_names, acc[0]))
+    if "allowed" in acc_opts:  # a grammar mask arrives with every step
+        in_parts.append(("allowed", acc_opts["allowed"]))
     h_in, d_in, d_views = pack_buffers(in_parts, dev)
     for name, t in in_parts:
         host_view(h_in, d_views[name]).copy_(t.cpu())
@@ -520,8 +548,11 @@ def run_ours(args):
         attn_call(d_views["q"], d_views["block_table"], d_views["seq_lens"],
                   r_views["out"], r_views["lse"], d_views.get("tree_mask"))
         if acc is not None:
+            e2e_opts = dict(acc_opts)
+            if "allowed" in e2e_opts:
+                e2e_opts["allowed"] = d_views["allowed"]
             accept_with([d_views[k] for k in acc_names],
-                        [r_views[k] for k in res_names])
+                        [r_views[k] for k in res_names], e2e_opts)
         h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -538,6 +569,58 @@ def run_ours(args):
     e_ms = max_over_ranks(e_ms, world)
     h2d = sum(t.numel() * t.element_size() for _, t in in_parts)
     d2h = sum(t.numel() * t.element_size() for _, t in out_parts)
+
+    # ---- end to end through the graph-captured step (svp_step_*) ----
+    # Two ping-pong slots of pinned buffers; each launch replays the slot's
+    # graph (input copy, kv_append, attention, acceptance) and queues the
+    # result copy on the runner's copy stream; the host waits for a slot's
+    # result only when it reuses the slot, one step later.  The slots are
+    # filled once (the synthetic step's inputs do not change), so every
+    # replay still moves the full inputs and results across PCIe/C2C.
+    step_e2e = None
+    if world == 1 and not tree and not acc_opts:
+        run = svp.StepRunner(kc, vc, batch=cfg.batch,
+                             num_q_heads=cfg.num_q_heads, q_len=cfg.q_len,
+                             max_blocks_per_seq=wl.max_blocks_per_seq,
+                             n_sink=cfg.n_sink, window=cfg.window, scale=scale,
+                             num_draft=cfg.q_len - 1 if acc is not None else 0,
+                             vocab=W.ACCEPT_CONFIG["vocab"] if acc is not None else 0,
+                             split_pages=args.split_pages,
+                             kernel_path=args.kernel_path)
+        names = ["q", "k_new", "v_new", "block_table", "seq_lens"]
+        src = [q, kn, vn, bt, sl]
+        if acc is not None:
+            names += ["target_logits", "draft_logits", "draft_tokens", "uniforms"]
+            src += list(acc[0])
+        for slot in (0, 1):
+            for name, t in zip(names, src):
+                h = run.host(slot, name)
+                h[...] = (t.view(torch.int16).cpu().numpy().view(np.uint16)
+                          if t.dtype == torch.bfloat16 else t.cpu().numpy())
+        n_run = max(4, min(args.steps, 200))
+        for t in range(4):
+            if t >= 2:
+                run.wait(t % 2)
+            run.launch(t % 2)
+        run.wait(0)
+        run.wait(1)
+        r0 = time.perf_counter()
+        for t in range(n_run):
+            if t >= 2:
+                run.wait(t % 2)
+            run.launch(t % 2)
+        run.wait(0)
+        run.wait(1)
+        r_ms = (time.perf_counter() - r0) * 1e3 / n_run
+        step_bytes_in = sum(run.host(0, n).nbytes for n in names)
+        outs = ["out", "lse"] + (["out_tokens", "n_accepted"]
+                                 if acc is not None else [])
+        step_bytes_out = sum(run.host(0, n).nbytes for n in outs)
+        run.close()
+        step_e2e = {"value": round(tokens_per_step_of(cfg) / (r_ms / 1e3), 1),
+                    "unit": UNIT, "ms_per_step": round(r_ms, 4),
+                    "h2d_bytes_per_step": int(step_bytes_in),
+                    "d2h_bytes_per_step": int(step_bytes_out)}
 
     # ---- report ----
     kname, ksrc = attention_kernel(cfg, args.kernel_path)
@@ -565,6 +648,7 @@ def run_ours(args):
         "e2e": {"value": round(world * tokens_per_step / (e_ms / 1e3), 1),
                 "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
+        **({"e2e_step_runner": step_e2e} if step_e2e else {}),
         "gpu_launches": int(gpu_launches),
         **({"accept_us": round(sum(acc_ms) / len(acc_ms) * 1e3, 2)}
            if acc is not None else {}),
@@ -630,6 +714,14 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's sequence count (smaller "
                          "cases for profiling; reported in config)")
+    ap.add_argument("--temperature", type=float, default=1.0,
+                    help="verify workloads: sampling temperature of the "
+                         "accept step (spec_accept_ex)")
+    ap.add_argument("--allowed-density", type=float, default=0.0,
+                    help="verify workloads: constrained decoding, each "
+                         "token allowed with this probability (0: no mask)")
+    ap.add_argument("--greedy", action="store_true",
+                    help="verify workloads: greedy (argmax) verification")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time plain API calls instead of CUDA-graph replays")

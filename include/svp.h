@@ -335,6 +335,77 @@ int spec_accept_tree(int batch, int num_nodes, int vocab,
                      int32_t *out_nodes, int32_t *n_accepted,
                      cudaStream_t stream);
 
+/* ---- the graph-captured decode step ----------------------------------
+ * (page: "How Moondream cut VLM inference latency by 35% via pipelined
+ * decoding", sections "The problem: the GPU bubble" and "Mechanism one:
+ * ping-pong slots").  A runner owns two slots; each has pinned host buffers
+ * for the step's inputs and outputs and device copies of them, and one CUDA
+ * graph, captured at creation, that copies the slot's inputs to the device
+ * and runs kv_append (the q_len new rows), paged_decode_attention and, with
+ * num_draft > 0, spec_accept.  svp_step_launch replays a slot's graph on
+ * the runner's compute stream and queues the copy of its outputs back to
+ * the slot on a separate copy stream, ordered after an event recorded when
+ * that step's outputs are written -- so the next step (the other slot) can
+ * run while the copy is in flight.  The host fills one slot while the GPU
+ * works on the other.
+ * Protocol: write a slot's inputs only before its first launch or after
+ * svp_step_wait on it returned; read its outputs after svp_step_wait.
+ * Launching a slot again waits (on the device) for its previous result
+ * copy.  The caches are the caller's and are updated by every step, in
+ * launch order.  All memory is allocated at creation; launches allocate
+ * nothing. */
+typedef struct {
+  svp_dims dims;      /* shapes of the cache and the batch (workspace and
+                         split/path fields: as for paged_decode_attention;
+                         the runner allocates its own workspace) */
+  int q_len;          /* new rows per sequence: appended, then attending */
+  int n_sink, window; /* as for paged_decode_attention */
+  float scale;
+  void *k_cache;      /* DEVICE caches, caller-owned */
+  void *v_cache;
+  int num_draft;      /* 0: no acceptance step; else q_len - 1 */
+  int vocab;          /* vocabulary of the acceptance step */
+} svp_step_desc;
+
+/* Fields of a slot (pinned host memory; layouts as in the single calls). */
+typedef enum {
+  SVP_STEP_Q = 0,          /* in:  [batch, q_len, Hq, D] dtype          */
+  SVP_STEP_K_NEW,          /* in:  [batch, q_len, Hkv, D] dtype         */
+  SVP_STEP_V_NEW,          /* in:  [batch, q_len, Hkv, D] dtype         */
+  SVP_STEP_BLOCK_TABLE,    /* in:  [batch, max_blocks_per_seq] int32    */
+  SVP_STEP_SEQ_LENS,       /* in:  [batch] int32 (after the append)     */
+  SVP_STEP_TARGET_LOGITS,  /* in:  [batch, K+1, vocab] fp32             */
+  SVP_STEP_DRAFT_LOGITS,   /* in:  [batch, K, vocab] fp32               */
+  SVP_STEP_DRAFT_TOKENS,   /* in:  [batch, K] int32                     */
+  SVP_STEP_UNIFORMS,       /* in:  [batch, K+1] fp32                    */
+  SVP_STEP_OUT,            /* out: [batch, q_len, Hq, D] dtype          */
+  SVP_STEP_LSE,            /* out: [batch, q_len, Hq] fp32              */
+  SVP_STEP_OUT_TOKENS,     /* out: [batch, K+1] int32                   */
+  SVP_STEP_N_ACCEPTED,     /* out: [batch] int32                        */
+  SVP_STEP_NUM_FIELDS
+} svp_step_field;
+
+typedef struct svp_step svp_step;
+
+/* Allocates the runner (streams, workspace, both slots) and captures the
+ * two slot graphs.  Errors: SVP_ERR_INVALID_ARG for null pointers, sizes
+ * < 1 or num_draft not in {0, q_len - 1}; the errors of the single calls
+ * for their arguments; SVP_ERR_CUDA if an allocation or the capture fails. */
+int svp_step_create(const svp_step_desc *desc, svp_step **runner);
+/* Pinned host memory of one field of slot 0 or 1 and its size in bytes
+ * (*bytes may be NULL); NULL for a bad slot/field or an empty field. */
+void *svp_step_host_buffer(svp_step *runner, int slot, int field,
+                           size_t *bytes);
+/* Queues one step on the slot (asynchronous). */
+int svp_step_launch(svp_step *runner, int slot);
+/* Waits until the slot's last step has finished and its outputs are in the
+ * slot's host buffers. */
+int svp_step_wait(svp_step *runner, int slot);
+/* The runner's compute stream (for ordering other work after its steps). */
+cudaStream_t svp_step_stream(svp_step *runner);
+/* Waits for outstanding work and frees everything. */
+int svp_step_destroy(svp_step *runner);
+
 /* Synchronises `stream`, returns SVP_OK and stores in *flags the OR of the
  * SVP_DEV_* flags raised by kernels since the last read, then clears them.
  * flags may be NULL. */

@@ -6,6 +6,7 @@ include/svp.h); this package is its thin Python binding.  Importing it loads
 nothing; the first call loads the library and raises if it is not built.
 """
 from .binding import (  # noqa: F401
+    StepRunner,
     SvpError,
     kv_append,
     last_launch_count,

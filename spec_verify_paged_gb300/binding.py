@@ -13,6 +13,8 @@ import math
 import os
 import threading
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,6 +30,8 @@ EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
             "paged_decode_workspace_size",
             "kv_append", "spec_accept", "spec_accept_ex", "spec_accept_tree",
             "svp_read_device_status",
+            "svp_step_create", "svp_step_host_buffer", "svp_step_launch",
+            "svp_step_wait", "svp_step_stream", "svp_step_destroy",
             "svp_status_string", "svp_last_launch_count")
 
 
@@ -46,6 +50,19 @@ class SvpDims(ctypes.Structure):
 class SvpAcceptOpts(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("allowed", ctypes.c_void_p),
                 ("greedy", ctypes.c_int)]
+
+
+class SvpStepDesc(ctypes.Structure):
+    _fields_ = [("dims", SvpDims), ("q_len", ctypes.c_int),
+                ("n_sink", ctypes.c_int), ("window", ctypes.c_int),
+                ("scale", ctypes.c_float), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("num_draft", ctypes.c_int),
+                ("vocab", ctypes.c_int)]
+
+
+STEP_FIELDS = ("q", "k_new", "v_new", "block_table", "seq_lens",
+               "target_logits", "draft_logits", "draft_tokens", "uniforms",
+               "out", "lse", "out_tokens", "n_accepted")
 
 
 class SvpError(RuntimeError):
@@ -93,6 +110,19 @@ def load_library(path: str = LIB_PATH):
         lib.spec_accept_ex.restype = i32
         lib.spec_accept_tree.argtypes = [i32, i32, i32] + [vp] * 9
         lib.spec_accept_tree.restype = i32
+        lib.svp_step_create.argtypes = [ctypes.POINTER(SvpStepDesc),
+                                         ctypes.POINTER(vp)]
+        lib.svp_step_create.restype = i32
+        lib.svp_step_host_buffer.argtypes = [vp, i32, i32, ctypes.POINTER(sz)]
+        lib.svp_step_host_buffer.restype = vp
+        lib.svp_step_launch.argtypes = [vp, i32]
+        lib.svp_step_launch.restype = i32
+        lib.svp_step_wait.argtypes = [vp, i32]
+        lib.svp_step_wait.restype = i32
+        lib.svp_step_stream.argtypes = [vp]
+        lib.svp_step_stream.restype = vp
+        lib.svp_step_destroy.argtypes = [vp]
+        lib.svp_step_destroy.restype = i32
         lib.svp_read_device_status.argtypes = [vp, ctypes.POINTER(i32)]
         lib.svp_read_device_status.restype = i32
         lib.svp_status_string.argtypes = [i32]
@@ -368,3 +398,80 @@ def read_device_status(stream=None, device=None) -> int:
 def last_launch_count() -> int:
     """Kernels launched by the last successful library call on this thread."""
     return int(load_library().svp_last_launch_count())
+
+
+class StepRunner:
+    """The graph-captured decode step (include/svp.h: svp_step_*): two
+    ping-pong slots of pinned host buffers, each replayed as one CUDA graph
+    (input copy, kv_append, attention, spec_accept) with its result copied
+    back on a separate stream.  host(slot, name) returns a numpy view of a
+    slot's pinned buffer (bf16 as uint16 bits)."""
+
+    def __init__(self, k_cache, v_cache, batch, num_q_heads, q_len,
+                 max_blocks_per_seq, n_sink=0, window=0, scale=None,
+                 num_draft=0, vocab=0, split_pages=0, kernel_path=PATH_AUTO):
+        lib = load_library()
+        _cuda_contig(k_cache, "k_cache")
+        _cuda_contig(v_cache, "v_cache")
+        nb, Hkv, bs, D = k_cache.shape
+        code = _dtype_code(k_cache)
+        dims = SvpDims(batch, num_q_heads, Hkv, D, bs, max_blocks_per_seq, nb,
+                       code, None, 0, split_pages, kernel_path)
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        desc = SvpStepDesc(dims, q_len, n_sink, window, float(scale),
+                           k_cache.data_ptr(), v_cache.data_ptr(), num_draft,
+                           vocab)
+        h = ctypes.c_void_p()
+        _check("svp_step_create", lib.svp_step_create(ctypes.byref(desc),
+                                                      ctypes.byref(h)))
+        self._lib, self._h = lib, h
+        self._keep = (k_cache, v_cache)
+        ed = np.uint16 if code == SVP_BF16 else np.float32
+        B, Q, K, V = batch, q_len, num_draft, vocab
+        self._spec = {
+            "q": (ed, (B, Q, num_q_heads, D)), "k_new": (ed, (B, Q, Hkv, D)),
+            "v_new": (ed, (B, Q, Hkv, D)),
+            "block_table": (np.int32, (B, max_blocks_per_seq)),
+            "seq_lens": (np.int32, (B,)),
+            "target_logits": (np.float32, (B, K + 1, V)),
+            "draft_logits": (np.float32, (B, K, V)),
+            "draft_tokens": (np.int32, (B, K)),
+            "uniforms": (np.float32, (B, K + 1)),
+            "out": (ed, (B, Q, num_q_heads, D)),
+            "lse": (np.float32, (B, Q, num_q_heads)),
+            "out_tokens": (np.int32, (B, K + 1)),
+            "n_accepted": (np.int32, (B,)),
+        }
+        self._views = {}
+
+    def host(self, slot, name):
+        key = (slot, name)
+        if key not in self._views:
+            n = ctypes.c_size_t()
+            ptr = self._lib.svp_step_host_buffer(self._h, slot,
+                                                 STEP_FIELDS.index(name),
+                                                 ctypes.byref(n))
+            _need(ptr is not None, f"slot {slot} has no field {name}")
+            raw = (ctypes.c_uint8 * n.value).from_address(ptr)
+            dt, shape = self._spec[name]
+            self._views[key] = np.frombuffer(raw, dtype=dt).reshape(shape)
+        return self._views[key]
+
+    def launch(self, slot):
+        _check("svp_step_launch", self._lib.svp_step_launch(self._h, slot))
+
+    def wait(self, slot):
+        _check("svp_step_wait", self._lib.svp_step_wait(self._h, slot))
+
+    def close(self):
+        if self._h:
+            self._views.clear()
+            _check("svp_step_destroy", self._lib.svp_step_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

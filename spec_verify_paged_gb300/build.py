@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsvp.so")
 SOURCES = ["attention.cu", "attention_tc.cu", "accept.cu", "kv_append.cu",
-           "api.cu", "noalloc.cu"]
+           "api.cu", "noalloc.cu", "step.cu"]
 HEADERS = [os.path.join(CSRC, h)
            for h in ("ptx.cuh", "svp_internal.h", "attn_common.cuh")] + [
     os.path.join(INCLUDE, "svp.h")]

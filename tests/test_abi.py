@@ -170,6 +170,18 @@ def test_accept_ex_checks_its_options(lib):
     assert lib.spec_accept_ex(2, 16, 100, P, P, P, P, None, P, P, None) == -2
 
 
+def test_step_runner_rejects_bad_descriptions(lib):
+    from spec_verify_paged_gb300.binding import SvpStepDesc
+    h = ctypes.c_void_p()
+    assert lib.svp_step_create(None, ctypes.byref(h)) == -1
+    d = SvpStepDesc(_dims(batch=0), 5, 0, 0, 0.1, P, P, 4, 100)
+    assert lib.svp_step_create(ctypes.byref(d), ctypes.byref(h)) == -1
+    d = SvpStepDesc(_dims(), 5, 0, 0, 0.1, P, P, 3, 100)   # K != q_len - 1
+    assert lib.svp_step_create(ctypes.byref(d), ctypes.byref(h)) == -1
+    assert lib.svp_step_launch(None, 0) == -1
+    assert lib.svp_step_host_buffer(None, 0, 0, None) is None
+
+
 def test_accept_null_pointer(lib):
     assert lib.spec_accept(2, 4, 100, P, None, P, P, P, P, None) == -1
     assert lib.spec_accept(0, 4, 100, None, None, None, None, None, None,
