@@ -78,6 +78,17 @@ def _load():
                 [i32] * 3 + [vp] * 4 + [ctypes.c_double, vp, i32, vp, vp, vp,
                                         ctypes.c_double])
             lib.oracle_spec_accept_ex.restype = i32
+            lib.oracle_paged_attention_fp8.argtypes = (
+                [i32] * 7 + [vp] * 3 + [ctypes.c_double] * 2 + [vp] * 2 +
+                [i32, i32, i32, f32, vp, i64, vp, vp])
+            lib.oracle_paged_attention_fp8.restype = i32
+            lib.oracle_e4m3_decode.argtypes = [vp, ctypes.c_long, vp]
+            lib.oracle_e4m3_decode.restype = i32
+            lib.oracle_e4m3_encode.argtypes = [vp, ctypes.c_long, f32, vp]
+            lib.oracle_e4m3_encode.restype = i32
+            lib.oracle_kv_append_fp8.argtypes = ([i32] * 6 + [vp] * 4 +
+                                                 [f32, f32, vp, vp, i32])
+            lib.oracle_kv_append_fp8.restype = i32
             _lib = lib
     return _lib
 
@@ -304,3 +315,78 @@ def spec_accept_ex(target_logits, draft_logits, draft_tokens, uniforms,
     if st != 0:
         raise ValueError(f"oracle_spec_accept_ex failed with status {st}")
     return {"out_tokens": out, "n_accepted": nacc, "near_boundary": near}
+
+
+def e4m3_decode(codes):
+    """Values of FP8 E4M3 codes (uint8 array) as float64."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    lib.oracle_e4m3_decode(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x, scale=1.0):
+    """E4M3 codes of float32 x / scale (nearest, ties to even, saturating)."""
+    lib = _load()
+    a = _c(x, np.float32)
+    out = np.empty(a.shape, np.uint8)
+    if lib.oracle_e4m3_encode(_ptr(a), a.size, float(scale), _ptr(out)) != 0:
+        raise ValueError("scale must be positive")
+    return out
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table,
+                        seq_lens, q_len, n_sink=0, window=0, scale=None,
+                        rows=None):
+    """Exact attention over FP8 E4M3 caches (uint8 codes; values scaled by
+    k_scale / v_scale) with bf16 q (uint16 bits), in fp64."""
+    lib = _load()
+    B, ql, Hq, D = q.shape
+    assert ql == q_len and q.dtype == np.uint16
+    nb, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    q = _c(q, np.uint16)
+    kc = _c(k_cache, np.uint8)
+    vc = _c(v_cache, np.uint8)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    if rows is None:
+        out = np.zeros((B, q_len, Hq, D), np.float64)
+        lse = np.zeros((B, q_len, Hq), np.float64)
+        r, n = None, 0
+    else:
+        r = _c(rows, np.int64)
+        out = np.zeros((r.size, D), np.float64)
+        lse = np.zeros((r.size,), np.float64)
+        n = r.size
+    st = lib.oracle_paged_attention_fp8(
+        B, Hq, Hkv, D, bs, bt.shape[1], nb, _ptr(q), _ptr(kc), _ptr(vc),
+        float(k_scale), float(v_scale), _ptr(bt), _ptr(sl), q_len, n_sink,
+        window, float(scale), _ptr(r), n, _ptr(out), _ptr(lse))
+    if st != 0:
+        raise ValueError(f"oracle_paged_attention_fp8 failed with status {st}")
+    return out, lse
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                  block_table, seq_lens):
+    """Quantise bf16 k_new / v_new into copies of FP8 caches."""
+    lib = _load()
+    B, n_new, Hkv, D = k_new.shape
+    nb, Hkv2, bs, D2 = k_cache.shape
+    assert Hkv2 == Hkv and D2 == D and k_cache.dtype == np.uint8
+    kc = np.array(k_cache, copy=True, order="C")
+    vc = np.array(v_cache, copy=True, order="C")
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    bt = _c(block_table, np.int32)
+    sl = _c(seq_lens, np.int32)
+    st = lib.oracle_kv_append_fp8(B, Hkv, D, bs, bt.shape[1], nb, _ptr(kn),
+                                  _ptr(vn), _ptr(kc), _ptr(vc), float(k_scale),
+                                  float(v_scale), _ptr(bt), _ptr(sl), n_new)
+    if st != 0:
+        raise ValueError(f"oracle_kv_append_fp8 failed with status {st}")
+    return kc, vc

@@ -44,8 +44,55 @@
 
 /* ---- element access: the stored bits widened to fp64 ------------------ */
 
+/* ---- FP8 E4M3 (the OCP 8-bit float: 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 = NaN), the format behind the
+ * "--kv-cache-dtype fp8" option the KV-cache lesson names ([KV] "Practical
+ * use") and the KV quantisation [SL] lists ("The KV cache memory
+ * bottleneck").  Decoding follows the definition; encoding takes the
+ * nearest finite value, ties to the even code, saturating at +-448. ---- */
+
+static double e4m3_value(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);        /* subnormal */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+static uint8_t e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;       /* saturate */
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {         /* every finite magnitude */
+    const double d = fabs(e4m3_value((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, long n, double *out) {
+  for (long i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+  return 0;
+}
+
+int oracle_e4m3_encode(const float *x, long n, float scale, uint8_t *out) {
+  if (!(scale > 0.0f)) return -1;
+  for (long i = 0; i < n; ++i) out[i] = e4m3_encode((double)(x[i] / scale));
+  return 0;
+}
+
 static double widen(const void *base, size_t idx, int dtype) {
   if (dtype == 0) return (double)((const float *)base)[idx];
+  if (dtype == 2) return e4m3_value(((const uint8_t *)base)[idx]);
   /* bfloat16: the upper 16 bits of an IEEE fp32 pattern. */
   uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
   float f;
@@ -92,7 +139,7 @@ static int check_sizes(int batch, int num_q_heads, int num_kv_heads,
                        int window) {
   if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
       block_size < 1 || max_blocks < 0 || num_blocks < 0 || q_len < 1 ||
-      n_sink < 0 || window < 0 || (dtype != 0 && dtype != 1))
+      n_sink < 0 || window < 0 || dtype < 0 || dtype > 2)
     return -1;
   if (num_q_heads % num_kv_heads != 0) return -1;
   return 0;
@@ -101,9 +148,12 @@ static int check_sizes(int batch, int num_q_heads, int num_kv_heads,
 /* ---- exact attention: [KV] "FlashAttention" (S = QK^T, P = softmax(S),
  * O = PV) and [SL] "The softmax problem" (softmax(QK^T/sqrt(d))V) -------- */
 
+/* q in `dtype` (fp32 or bf16); the caches in kv_dtype (the same, or 2 = FP8
+ * E4M3 codes whose values are scaled by k_scale / v_scale). */
 static int attention_rows(int batch, int num_q_heads, int num_kv_heads,
                           int head_dim, int block_size, int max_blocks_per_seq,
-                          int num_blocks, int dtype, const void *q,
+                          int num_blocks, int dtype, int kv_dtype,
+                          double k_scale, double v_scale, const void *q,
                           const void *k_cache, const void *v_cache,
                           const int32_t *block_table, const int32_t *seq_lens,
                           int q_len, int n_sink, int window,
@@ -165,7 +215,7 @@ static int attention_rows(int batch, int num_q_heads, int num_kv_heads,
       double dot = 0.0;
       for (int d = 0; d < head_dim; ++d)
         dot += widen(q, (size_t)row * head_dim + d, dtype) *
-               widen(k_cache, (size_t)off + d, dtype);
+               (k_scale * widen(k_cache, (size_t)off + d, kv_dtype));
       s[nv] = sc * dot;
       koff[nv] = off;
       ++nv;
@@ -185,7 +235,7 @@ static int attention_rows(int batch, int num_q_heads, int num_kv_heads,
     for (long k = 0; k < nv; ++k) {
       double p = exp(s[k] - m) / z;
       for (int d = 0; d < head_dim; ++d)
-        o[d] += p * widen(v_cache, (size_t)koff[k] + d, dtype);
+        o[d] += p * (v_scale * widen(v_cache, (size_t)koff[k] + d, kv_dtype));
     }
     lse[n] = m + log(z);
   }
@@ -202,10 +252,28 @@ int oracle_paged_attention(int batch, int num_q_heads, int num_kv_heads,
                            int q_len, int n_sink, int window, float scale,
                            const int64_t *rows, int64_t n_rows, double *out,
                            double *lse) {
+  if (dtype == 2) return -1; /* q is fp32 or bf16 */
   return attention_rows(batch, num_q_heads, num_kv_heads, head_dim,
-                        block_size, max_blocks_per_seq, num_blocks, dtype, q,
-                        k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
-                        window, NULL, scale, rows, n_rows, out, lse);
+                        block_size, max_blocks_per_seq, num_blocks, dtype,
+                        dtype, 1.0, 1.0, q, k_cache, v_cache, block_table,
+                        seq_lens, q_len, n_sink, window, NULL, scale, rows,
+                        n_rows, out, lse);
+}
+
+int oracle_paged_attention_fp8(int batch, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks,
+                               const void *q, const void *k_cache,
+                               const void *v_cache, double k_scale,
+                               double v_scale, const int32_t *block_table,
+                               const int32_t *seq_lens, int q_len, int n_sink,
+                               int window, float scale, const int64_t *rows,
+                               int64_t n_rows, double *out, double *lse) {
+  return attention_rows(batch, num_q_heads, num_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, 1, 2,
+                        k_scale, v_scale, q, k_cache, v_cache, block_table,
+                        seq_lens, q_len, n_sink, window, NULL, scale, rows,
+                        n_rows, out, lse);
 }
 
 int oracle_paged_tree_attention(int batch, int num_q_heads, int num_kv_heads,
@@ -218,11 +286,12 @@ int oracle_paged_tree_attention(int batch, int num_q_heads, int num_kv_heads,
                                 const uint32_t *tree_mask, float scale,
                                 const int64_t *rows, int64_t n_rows,
                                 double *out, double *lse) {
-  if (!tree_mask) return -1;
+  if (!tree_mask || dtype == 2) return -1;
   return attention_rows(batch, num_q_heads, num_kv_heads, head_dim,
-                        block_size, max_blocks_per_seq, num_blocks, dtype, q,
-                        k_cache, v_cache, block_table, seq_lens, q_len, 0, 0,
-                        tree_mask, scale, rows, n_rows, out, lse);
+                        block_size, max_blocks_per_seq, num_blocks, dtype,
+                        dtype, 1.0, 1.0, q, k_cache, v_cache, block_table,
+                        seq_lens, q_len, 0, 0, tree_mask, scale, rows, n_rows,
+                        out, lse);
 }
 
 /* ---- tiled variant: [KV] "FlashAttention -- the tiling trick" and
@@ -358,6 +427,40 @@ int oracle_kv_append(int batch, int num_kv_heads, int head_dim, int block_size,
                (const char *)k_new + src, row_bytes);
         memcpy((char *)v_cache + (size_t)off * elem_bytes,
                (const char *)v_new + src, row_bytes);
+      }
+    }
+  }
+  return 0;
+}
+
+/* FP8 append: the new rows arrive in bf16; each value x is stored as the
+ * E4M3 code of the fp32 quotient x / scale (k_scale for K, v_scale for V),
+ * nearest, ties to even, saturated at +-448. */
+int oracle_kv_append_fp8(int batch, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq,
+                         int num_blocks, const uint16_t *k_new,
+                         const uint16_t *v_new, uint8_t *k_cache,
+                         uint8_t *v_cache, float k_scale, float v_scale,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         int n_new) {
+  if (batch < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 ||
+      n_new < 0 || !(k_scale > 0.0f) || !(v_scale > 0.0f))
+    return -1;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens[b] < n_new) return -1;
+    for (int k = 0; k < n_new; ++k) {
+      long pos = (long)seq_lens[b] - n_new + k;
+      for (int g = 0; g < num_kv_heads; ++g) {
+        long off = kv_offset(block_table, max_blocks_per_seq, b, pos,
+                             block_size, num_kv_heads, g, head_dim, num_blocks);
+        if (off < 0) return -2;
+        size_t src = ((((size_t)b * n_new + k) * num_kv_heads) + g) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+          const float kx = (float)widen(k_new, src + d, 1);
+          const float vx = (float)widen(v_new, src + d, 1);
+          k_cache[off + d] = e4m3_encode((double)(kx / k_scale));
+          v_cache[off + d] = e4m3_encode((double)(vx / v_scale));
+        }
       }
     }
   }

@@ -55,6 +55,36 @@ int oracle_paged_tree_attention(int batch, int num_q_heads, int num_kv_heads,
                                 const int64_t *rows, int64_t n_rows,
                                 double *out, double *lse);
 
+/* The same definition over an FP8 cache: q in bf16, k_cache / v_cache E4M3
+ * codes (1 byte per element, same layout), value = code's value * k_scale
+ * (or v_scale).  Same returns as oracle_paged_attention. */
+int oracle_paged_attention_fp8(int batch, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks,
+                               const void *q, const void *k_cache,
+                               const void *v_cache, double k_scale,
+                               double v_scale, const int32_t *block_table,
+                               const int32_t *seq_lens, int q_len, int n_sink,
+                               int window, float scale, const int64_t *rows,
+                               int64_t n_rows, double *out, double *lse);
+
+/* FP8 E4M3 codes: decode (values, NaN for the NaN codes); encode
+ * x / scale (fp32 division) to the nearest code, ties to even, saturating
+ * at +-448.  Return 0 (-1 for scale <= 0). */
+int oracle_e4m3_decode(const uint8_t *codes, long n, double *out);
+int oracle_e4m3_encode(const float *x, long n, float scale, uint8_t *out);
+
+/* KV append into FP8 caches: k_new / v_new bf16 [batch, n_new, Hkv, D];
+ * each value stored as the E4M3 code of value / scale.  Returns as
+ * oracle_kv_append. */
+int oracle_kv_append_fp8(int batch, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq,
+                         int num_blocks, const uint16_t *k_new,
+                         const uint16_t *v_new, uint8_t *k_cache,
+                         uint8_t *v_cache, float k_scale, float v_scale,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         int n_new);
+
 /* The same quantity computed the tiled way: the visible keys of each row are
  * cut into n_splits contiguous parts, each part is folded in `tile`-key
  * blocks with a running (max, sum, accumulator), and the parts are merged by

@@ -69,8 +69,43 @@ def _normals(rng: np.random.Generator, shape, dtype: str, chunk=1 << 24):
     return out.reshape(shape)
 
 
+FP8_SCALE = 2.0 ** -5        # k_scale = v_scale of the FP8 workloads
+FP8_NAN = np.uint8(0x7F)      # E4M3 NaN code
+
+
+def _fp8_codes(x: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes of fp32 values / scale, via torch's float8_e4m3fn cast
+    (data preparation: the synthetic cache contents)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32) / np.float32(scale))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _kv_values(rng: np.random.Generator, shape, dtype: str):
+    """Cache contents: N(0,1) draws stored as fp32, bf16 bits or, for
+    "fp8", E4M3 codes of value / FP8_SCALE."""
+    if dtype != "fp8":
+        return _normals(rng, shape, dtype)
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint8)
+    chunk = 1 << 24
+    for s0 in range(0, n, chunk):
+        e = min(n, s0 + chunk)
+        out[s0:e] = _fp8_codes(rng.standard_normal(e - s0, dtype=np.float32),
+                               FP8_SCALE)
+    return out.reshape(shape)
+
+
 def _nan_value(dtype: str):
+    if dtype == "fp8":
+        return FP8_NAN
     return np.float32(np.nan) if dtype == "f32" else BF16_NAN
+
+
+def io_dtype(dtype: str) -> str:
+    """Storage of q, out and new K/V rows: the cache's, except bf16 for an
+    FP8 cache."""
+    return "bf16" if dtype == "fp8" else dtype
 
 
 # --------------------------------------------------------------------------
@@ -85,7 +120,8 @@ class AttnConfig:
     num_kv_heads: int
     head_dim: int
     q_len: int
-    dtype: str                 # "f32" or "bf16"
+    dtype: str                 # cache: "f32", "bf16" or "fp8" (E4M3,
+                               # q / out / new rows in bf16)
     ctx_min: int               # seq_len range (including the q_len new rows)
     ctx_max: int
     n_sink: int = 0
@@ -110,6 +146,9 @@ CONFIGS = {
                                      sink_key_scale=4.0, seed=4),
     "long-context-128k": AttnConfig("long-context-128k", 4, 64, 8, 128, 1,
                                     "bf16", 131072, 131072, seed=5),
+    # the 7B decode shape over an FP8 E4M3 cache (half the KV bytes)
+    "decode-7b-fp8": AttnConfig("decode-7b-fp8", 32, 32, 32, 128, 1, "fp8",
+                                512, 4096, seed=2),
     "long-context-128k-verify": AttnConfig("long-context-128k-verify", 4, 64,
                                            8, 128, 4, "bf16", 131072, 131072,
                                            seed=5),
@@ -166,6 +205,9 @@ class AttnWorkload:
     v_new: Optional[np.ndarray] = None
     # [B, q_len] uint32 ancestor masks of a draft tree, or None (causal)
     tree_mask: Optional[np.ndarray] = None
+    # FP8 caches: value = code * scale (1.0 otherwise)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def q_len(self):
@@ -253,11 +295,11 @@ def make_attention(cfg: AttnConfig, seed: Optional[int] = None,
         else:
             table[b, :len(ids)] = ids
 
-    k_cache = _normals(rng, (num_blocks, Hkv, BLOCK_SIZE, D), cfg.dtype)
-    v_cache = _normals(rng, (num_blocks, Hkv, BLOCK_SIZE, D), cfg.dtype)
-    q = _normals(rng, (B, ql, Hq, D), cfg.dtype)
+    k_cache = _kv_values(rng, (num_blocks, Hkv, BLOCK_SIZE, D), cfg.dtype)
+    v_cache = _kv_values(rng, (num_blocks, Hkv, BLOCK_SIZE, D), cfg.dtype)
+    q = _normals(rng, (B, ql, Hq, D), io_dtype(cfg.dtype))
 
-    if cfg.sink_key_scale != 1.0 and cfg.n_sink > 0:
+    if cfg.sink_key_scale != 1.0 and cfg.n_sink > 0 and cfg.dtype != "fp8":
         for b in range(B):
             for pos in range(min(cfg.n_sink, int(seq_lens[b]))):
                 blk = table[b, pos // BLOCK_SIZE]
@@ -291,8 +333,8 @@ def make_attention(cfg: AttnConfig, seed: Optional[int] = None,
 
     k_new = v_new = None
     if n_new > 0:
-        k_new = _normals(rng, (B, n_new, Hkv, D), cfg.dtype)
-        v_new = _normals(rng, (B, n_new, Hkv, D), cfg.dtype)
+        k_new = _normals(rng, (B, n_new, Hkv, D), io_dtype(cfg.dtype))
+        v_new = _normals(rng, (B, n_new, Hkv, D), io_dtype(cfg.dtype))
         nan = _nan_value(cfg.dtype)
         for b in range(B):
             L = int(seq_lens[b])
@@ -307,9 +349,10 @@ def make_attention(cfg: AttnConfig, seed: Optional[int] = None,
         par = binary_tree_parents(cfg.tree_depth)
         assert par.size == ql, "q_len must be the tree's node count"
         tree_mask = np.tile(tree_mask_from_parents(par), (B, 1))
+    ks = FP8_SCALE if cfg.dtype == "fp8" else 1.0
     return AttnWorkload(cfg, q, k_cache, v_cache, table,
                         seq_lens.astype(np.int32), scale, k_new, v_new,
-                        tree_mask)
+                        tree_mask, ks, ks)
 
 
 def small_config(name="small", batch=3, num_q_heads=8, num_kv_heads=2,
