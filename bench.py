@@ -250,7 +250,12 @@ def oracle_sample(wl, n_seqs, start=0):
     seqs = [(start + i) % B for i in range(n_seqs)]
     rows = np.concatenate([np.arange(b * per, (b + 1) * per) for b in seqs])
     t = time.perf_counter()
-    if wl.tree_mask is not None:
+    if wl.cfg.dtype == "fp8":
+        oracle.paged_attention_fp8(wl.q, wl.k_cache, wl.v_cache, wl.k_scale,
+                                   wl.v_scale, wl.block_table, wl.seq_lens,
+                                   wl.q_len, wl.cfg.n_sink, wl.cfg.window,
+                                   wl.scale, rows=rows.astype(np.int64))
+    elif wl.tree_mask is not None:
         oracle.paged_tree_attention(wl.q, wl.k_cache, wl.v_cache,
                                     wl.block_table, wl.seq_lens, wl.q_len,
                                     wl.tree_mask, wl.scale,
@@ -288,7 +293,8 @@ def workload_config(wl, split_pages=None):
     cfg = wl.cfg
     tr = A.attention_traffic(wl.seq_lens, cfg.q_len, cfg.num_q_heads,
                              cfg.num_kv_heads, cfg.head_dim,
-                             4 if cfg.dtype == "f32" else 2, cfg.n_sink,
+                             {"f32": 4, "bf16": 2, "fp8": 1}[cfg.dtype],
+                             cfg.n_sink,
                              cfg.window)
     c = {"workload": cfg.name, "batch": cfg.batch,
          "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
@@ -404,17 +410,21 @@ def run_ours(args):
     scale = float(wl.scale)
     launches = [0]
 
+    # an FP8 cache's scales (1 otherwise)
+    kv_scales = dict(k_scale=wl.k_scale, v_scale=wl.v_scale)
+
     def attn_call(q_, bt_, sl_, out_, lse_, tm_=None):
         if tree:
             svp.paged_tree_attention(q_, kc, vc, bt_, sl_, tm_, scale=scale,
                                      out=out_, lse=lse_,
                                      split_pages=args.split_pages,
-                                     kernel_path=args.kernel_path)
+                                     kernel_path=args.kernel_path, **kv_scales)
         else:
             svp.paged_decode_attention(
                 q_, kc, vc, bt_, sl_, q_len=cfg.q_len, n_sink=cfg.n_sink,
                 window=cfg.window, scale=scale, out=out_, lse=lse_,
-                split_pages=args.split_pages, kernel_path=args.kernel_path)
+                split_pages=args.split_pages, kernel_path=args.kernel_path,
+                **kv_scales)
 
     def accept_with(inputs, outputs, opts=None):
         opts = acc_opts if opts is None else opts
@@ -430,7 +440,7 @@ def run_ours(args):
         return svp.last_launch_count()
 
     def step(ev=None):
-        svp.kv_append(kn, vn, kc, vc, bt, sl)
+        svp.kv_append(kn, vn, kc, vc, bt, sl, **kv_scales)
         n = svp.last_launch_count()
         if ev is not None:
             ev[0].record(stream)
@@ -459,7 +469,7 @@ def run_ours(args):
         g_app, g_attn, g_acc = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
                                 torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_app):
-            svp.kv_append(kn, vn, kc, vc, bt, sl)
+            svp.kv_append(kn, vn, kc, vc, bt, sl, **kv_scales)
         n_app = svp.last_launch_count()
         with torch.cuda.graph(g_attn):
             attn_call(q, bt, sl, out, lse, tm)
@@ -544,7 +554,7 @@ def run_ours(args):
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
         svp.kv_append(d_views["k_new"], d_views["v_new"], kc, vc,
-                      d_views["block_table"], d_views["seq_lens"])
+                      d_views["block_table"], d_views["seq_lens"], **kv_scales)
         attn_call(d_views["q"], d_views["block_table"], d_views["seq_lens"],
                   r_views["out"], r_views["lse"], d_views.get("tree_mask"))
         if acc is not None:
@@ -586,7 +596,7 @@ def run_ours(args):
                              num_draft=cfg.q_len - 1 if acc is not None else 0,
                              vocab=W.ACCEPT_CONFIG["vocab"] if acc is not None else 0,
                              split_pages=args.split_pages,
-                             kernel_path=args.kernel_path)
+                             kernel_path=args.kernel_path, **kv_scales)
         names = ["q", "k_new", "v_new", "block_table", "seq_lens"]
         src = [q, kn, vn, bt, sl]
         if acc is not None:
@@ -634,7 +644,7 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8-e4m3 KV, bf16 q"}[cfg.dtype],
         "data": "synthetic (seeded N(0,1) Q/K/V, shuffled 16-token pages)",
         "config": conf,
         "kv_read_gbs": round(tr["kv_bytes"] * args.steps / (ms / 1e3) / 1e9, 1),

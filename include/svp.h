@@ -46,7 +46,12 @@ typedef enum {
   SVP_ERR_WORKSPACE = -4    /* caller workspace smaller than required    */
 } svp_status;
 
-typedef enum { SVP_F32 = 0, SVP_BF16 = 1 } svp_dtype;
+/* SVP_FP8_E4M3: the K/V caches hold FP8 E4M3 codes (OCP: 1 sign bit, 4
+ * exponent bits, bias 7, 3 mantissa bits; 1 byte per element), a value
+ * being code * dims->k_scale (K) or code * dims->v_scale (V); q, out and the
+ * new rows of kv_append are bf16 ("KV cache & Flash Attention", section
+ * "Practical use": an fp8 KV cache halves the bytes attention reads). */
+typedef enum { SVP_F32 = 0, SVP_BF16 = 1, SVP_FP8_E4M3 = 2 } svp_dtype;
 
 /* Flags returned by svp_read_device_status(). */
 enum {
@@ -58,6 +63,7 @@ enum {
 
 /* Shapes shared by kv_append and paged_decode_attention.
  *   q, out           [batch, q_len, num_q_heads, head_dim]        dtype
+ *                    (bf16 when dtype is SVP_FP8_E4M3)
  *   k_cache, v_cache [num_blocks, num_kv_heads, block_size, head_dim] dtype
  *                    (one head's page is one contiguous run)
  *   block_table      [batch, max_blocks_per_seq] int32; entry lb of row b
@@ -83,6 +89,8 @@ typedef struct {
   size_t workspace_bytes; /* size of `workspace`                           */
   int split_pages;        /* fewest pages per CTA slice; 0 = automatic (8) */
   int kernel_path;        /* svp_kernel_path; SVP_PATH_AUTO by default     */
+  float k_scale;          /* SVP_FP8_E4M3 caches: value = code * scale    */
+  float v_scale;          /* (finite, > 0); ignored for other dtypes      */
 } svp_dims;
 
 /* Which attention kernel variant runs.  AUTO picks tensor cores (bf16 only)
@@ -218,11 +226,14 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len,
                                    int n_sink, int window);
 
 /* KV append: writes the n_new new K/V rows of every sequence, k_new/v_new
- * [batch, n_new, num_kv_heads, head_dim] (dtype of dims), at logical
- * positions seq_lens[b]-n_new .. seq_lens[b]-1 of the paged caches, i.e.
- * page block_table[b][pos/16], row pos%16 (pages: "KV cache & Flash
- * Attention", sections "KV cache" and "PagedAttention").  seq_lens are the
- * lengths AFTER the append.  A pure byte copy.  Uses no workspace.
+ * [batch, n_new, num_kv_heads, head_dim] (dtype of dims; bf16 for an
+ * SVP_FP8_E4M3 cache), at logical positions seq_lens[b]-n_new ..
+ * seq_lens[b]-1 of the paged caches, i.e. page block_table[b][pos/16], row
+ * pos%16 (pages: "KV cache & Flash Attention", sections "KV cache" and
+ * "PagedAttention").  seq_lens are the lengths AFTER the append.  A byte
+ * copy; into an FP8 cache each value x is stored as the E4M3 code of the
+ * fp32 quotient x / k_scale (resp. v_scale), nearest with ties to even,
+ * saturating at +-448.  Uses no workspace.
  * Errors as for paged_decode_attention; n_new in [0, 64]. */
 int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
               void *k_cache, void *v_cache, const int32_t *block_table,

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libsvp.so")
 
 SVP_OK, SVP_ERR_INVALID_ARG, SVP_ERR_UNSUPPORTED, SVP_ERR_CUDA, SVP_ERR_WORKSPACE = (
     0, -1, -2, -3, -4)
-SVP_F32, SVP_BF16 = 0, 1
+SVP_F32, SVP_BF16, SVP_FP8_E4M3 = 0, 1, 2
 PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES, PATH_TCGEN05 = 0, 1, 2, 3
 DEV_BAD_BLOCK_ID, DEV_BAD_SEQ_LEN, DEV_BAD_TOKEN, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED = ("paged_decode_attention", "paged_decode_attention_noalloc",
@@ -44,7 +44,9 @@ class SvpDims(ctypes.Structure):
                 ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t),
                 ("split_pages", ctypes.c_int),
-                ("kernel_path", ctypes.c_int)]
+                ("kernel_path", ctypes.c_int),
+                ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 class SvpAcceptOpts(ctypes.Structure):
@@ -153,6 +155,20 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
 
 
+_FP8_TYPES = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+
+
+def _cache_code(k_cache, q_dtype):
+    """dtype code of a call: the cache's; an FP8 E4M3 cache (uint8 codes or
+    float8_e4m3fn) pairs with bf16 q / out / new rows."""
+    if k_cache.dtype in _FP8_TYPES:
+        _need(q_dtype == torch.bfloat16,
+              "an FP8 cache takes bf16 q, out and new rows")
+        return SVP_FP8_E4M3
+    _need(k_cache.dtype == q_dtype, "q and the caches must share a dtype")
+    return _dtype_code(k_cache)
+
+
 def _need(cond, what):
     if not cond:
         raise ValueError(what)
@@ -164,7 +180,7 @@ def _cuda_contig(t, name):
 
 
 def make_dims(q_shape, k_cache, block_table, dtype_code, workspace=None,
-              split_pages=0, kernel_path=0):
+              split_pages=0, kernel_path=0, k_scale=1.0, v_scale=1.0):
     B, _, Hq, D = q_shape
     nb, Hkv, bs, D2 = k_cache.shape
     d = SvpDims()
@@ -173,6 +189,8 @@ def make_dims(q_shape, k_cache, block_table, dtype_code, workspace=None,
     d.dtype = dtype_code
     d.split_pages = int(split_pages)
     d.kernel_path = int(kernel_path)
+    d.k_scale = float(k_scale)
+    d.v_scale = float(v_scale)
     if workspace is not None:
         d.workspace = ctypes.c_void_p(workspace.data_ptr())
         d.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -203,18 +221,21 @@ def workspace_for(dims: SvpDims, q_len: int, n_sink: int, window: int,
 def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens,
                            q_len=None, n_sink=0, window=0, scale=None,
                            out=None, lse=None, workspace=None, split_pages=0,
-                           kernel_path=PATH_AUTO, stream=None):
+                           kernel_path=PATH_AUTO, stream=None, k_scale=1.0,
+                           v_scale=1.0):
     """out [B, q_len, Hq, D] (q's dtype) and lse [B, q_len, Hq] fp32 of paged
-    decode/verify attention (include/svp.h: paged_decode_attention)."""
+    decode/verify attention (include/svp.h: paged_decode_attention).  FP8
+    E4M3 caches (uint8 codes or float8_e4m3fn) take bf16 q and their
+    k_scale / v_scale."""
     return _attention(q, k_cache, v_cache, block_table, seq_lens, q_len,
                       n_sink, window, None, scale, out, lse, workspace,
-                      split_pages, kernel_path, stream)
+                      split_pages, kernel_path, stream, k_scale, v_scale)
 
 
 def paged_tree_attention(q, k_cache, v_cache, block_table, seq_lens,
                          tree_mask, scale=None, out=None, lse=None,
                          workspace=None, split_pages=0, kernel_path=PATH_AUTO,
-                         stream=None):
+                         stream=None, k_scale=1.0, v_scale=1.0):
     """Draft-tree verify attention (include/svp.h: paged_tree_attention).
     tree_mask: int32 (or uint32) [B, q_len] on the GPU, bit k of entry
     (b, i) set iff node k is an ancestor of node i or i itself."""
@@ -224,19 +245,18 @@ def paged_tree_attention(q, k_cache, v_cache, block_table, seq_lens,
           "tree_mask must be int32/uint32 [B, q_len]")
     return _attention(q, k_cache, v_cache, block_table, seq_lens, None, 0, 0,
                       tree_mask, scale, out, lse, workspace, split_pages,
-                      kernel_path, stream)
+                      kernel_path, stream, k_scale, v_scale)
 
 
 def _attention(q, k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
                window, tree_mask, scale, out, lse, workspace, split_pages,
-               kernel_path, stream):
+               kernel_path, stream, k_scale=1.0, v_scale=1.0):
     lib = load_library()
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
                  (block_table, "block_table"), (seq_lens, "seq_lens")):
         _cuda_contig(t, n)
-    code = _dtype_code(q)
-    _need(k_cache.dtype == q.dtype and v_cache.dtype == q.dtype,
-          "q, k_cache and v_cache must share a dtype")
+    code = _cache_code(k_cache, q.dtype)
+    _need(v_cache.dtype == k_cache.dtype, "k_cache and v_cache must share a dtype")
     _need(k_cache.shape == v_cache.shape and k_cache.dim() == 4,
           "k_cache/v_cache must be [num_blocks, Hkv, block_size, D]")
     _need(block_table.dtype == torch.int32 and block_table.dim() == 2,
@@ -255,7 +275,7 @@ def _attention(q, k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
     _cuda_contig(out, "out")
     _cuda_contig(lse, "lse")
     dims = make_dims(q.shape, k_cache, block_table, code, None, split_pages,
-                     kernel_path)
+                     kernel_path, k_scale, v_scale)
     if workspace is None:
         workspace = workspace_for(dims, q_len, n_sink, window, q.device)
     if workspace is not None:
@@ -279,19 +299,21 @@ def _attention(q, k_cache, v_cache, block_table, seq_lens, q_len, n_sink,
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, block_table, seq_lens,
-              stream=None):
+              stream=None, k_scale=1.0, v_scale=1.0):
     """Scatter k_new/v_new [B, n_new, Hkv, D] into the paged caches in place
-    (include/svp.h: kv_append).  seq_lens are the lengths after the append."""
+    (include/svp.h: kv_append).  seq_lens are the lengths after the append.
+    Into FP8 caches the bf16 rows are quantised with k_scale / v_scale."""
     lib = load_library()
     for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
                  (v_cache, "v_cache"), (block_table, "block_table"),
                  (seq_lens, "seq_lens")):
         _cuda_contig(t, n)
-    code = _dtype_code(k_cache)
-    _need(k_new.dtype == k_cache.dtype and v_new.dtype == k_cache.dtype,
-          "k_new/v_new must have the cache dtype")
+    code = _cache_code(k_cache, k_new.dtype)
+    _need(v_new.dtype == k_new.dtype and v_cache.dtype == k_cache.dtype,
+          "k_new/v_new and k_cache/v_cache must pair up")
     B, n_new, Hkv, D = k_new.shape
-    dims = make_dims((B, n_new, Hkv, D), k_cache, block_table, code)
+    dims = make_dims((B, n_new, Hkv, D), k_cache, block_table, code,
+                     k_scale=k_scale, v_scale=v_scale)
     st = lib.kv_append(ctypes.byref(dims), k_new.data_ptr(), v_new.data_ptr(),
                        k_cache.data_ptr(), v_cache.data_ptr(),
                        block_table.data_ptr(), seq_lens.data_ptr(), int(n_new),
@@ -409,14 +431,17 @@ class StepRunner:
 
     def __init__(self, k_cache, v_cache, batch, num_q_heads, q_len,
                  max_blocks_per_seq, n_sink=0, window=0, scale=None,
-                 num_draft=0, vocab=0, split_pages=0, kernel_path=PATH_AUTO):
+                 num_draft=0, vocab=0, split_pages=0, kernel_path=PATH_AUTO,
+                 k_scale=1.0, v_scale=1.0):
         lib = load_library()
         _cuda_contig(k_cache, "k_cache")
         _cuda_contig(v_cache, "v_cache")
         nb, Hkv, bs, D = k_cache.shape
-        code = _dtype_code(k_cache)
+        code = (SVP_FP8_E4M3 if k_cache.dtype in _FP8_TYPES
+                else _dtype_code(k_cache))
         dims = SvpDims(batch, num_q_heads, Hkv, D, bs, max_blocks_per_seq, nb,
-                       code, None, 0, split_pages, kernel_path)
+                       code, None, 0, split_pages, kernel_path, k_scale,
+                       v_scale)
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         desc = SvpStepDesc(dims, q_len, n_sink, window, float(scale),
@@ -427,7 +452,7 @@ class StepRunner:
                                                       ctypes.byref(h)))
         self._lib, self._h = lib, h
         self._keep = (k_cache, v_cache)
-        ed = np.uint16 if code == SVP_BF16 else np.float32
+        ed = np.float32 if code == SVP_F32 else np.uint16
         B, Q, K, V = batch, q_len, num_draft, vocab
         self._spec = {
             "q": (ed, (B, Q, num_q_heads, D)), "k_new": (ed, (B, Q, Hkv, D)),

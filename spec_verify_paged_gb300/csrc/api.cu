@@ -75,7 +75,12 @@ static int check_dims(const svp_dims *d) {
       d->kernel_path > SVP_PATH_TCGEN05)
     return SVP_ERR_INVALID_ARG;
   if (d->num_q_heads % d->num_kv_heads != 0) return SVP_ERR_INVALID_ARG;
-  if (d->dtype != SVP_F32 && d->dtype != SVP_BF16) return SVP_ERR_INVALID_ARG;
+  if (d->dtype != SVP_F32 && d->dtype != SVP_BF16 && d->dtype != SVP_FP8_E4M3)
+    return SVP_ERR_INVALID_ARG;
+  if (d->dtype == SVP_FP8_E4M3 &&
+      !(std::isfinite(d->k_scale) && d->k_scale > 0.f &&
+        std::isfinite(d->v_scale) && d->v_scale > 0.f))
+    return SVP_ERR_INVALID_ARG;
   if (d->head_dim != 64 && d->head_dim != 128) return SVP_ERR_UNSUPPORTED;
   if (d->block_size != kBlockSize) return SVP_ERR_UNSUPPORTED;
   if (d->batch > kMaxBatch) return SVP_ERR_UNSUPPORTED;
@@ -279,8 +284,9 @@ static int attention_call(const svp_dims *dims, const void *q,
   // every CTA rewrites its split descriptor, so the workspace needs no
   // clearing between calls
   char *wp = static_cast<char *>(ws);
-  const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;
+  const size_t eb = dims->dtype == SVP_F32 ? 4 : 2;  // q / out (bf16 for FP8)
   const size_t row_elems = (size_t)dims->num_q_heads * dims->head_dim;
+  const bool fp8 = dims->dtype == SVP_FP8_E4M3;
   int launches = 0;
   for (int b0 = 0; b0 < dims->batch; b0 += bl) {
     const int nb = dims->batch - b0 < bl ? dims->batch - b0 : bl;
@@ -311,7 +317,10 @@ static int attention_call(const svp_dims *dims, const void *q,
     p.n_rg = plan.n_rg;
     p.min_pages = plan.min_pages;
     p.seg_items = plan.seg_items;
-    p.qscale = scale * 1.4426950408889634f;
+    // an FP8 cache's K scale folds into the query scale, its V scale
+    // multiplies the outputs
+    p.qscale = scale * 1.4426950408889634f * (fp8 ? dims->k_scale : 1.0f);
+    p.v_scale = fp8 ? dims->v_scale : 1.0f;
     p.tree_mask = tree_mask ? tree_mask + (size_t)b0 * q_len : nullptr;
     AttnPlan sub = plan;
     if (nb != bl) {
@@ -388,6 +397,9 @@ int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
   p.max_blocks = dims->max_blocks_per_seq;
   p.num_blocks = dims->num_blocks;
   p.elem_bytes = dims->dtype == SVP_F32 ? 4 : 2;
+  p.fp8 = dims->dtype == SVP_FP8_E4M3;
+  p.k_scale = p.fp8 ? dims->k_scale : 1.0f;
+  p.v_scale = p.fp8 ? dims->v_scale : 1.0f;
   if (launch_kv_append(p, stream) != cudaSuccess) return SVP_ERR_CUDA;
   t_last_launches = 1;
   return SVP_OK;

@@ -42,6 +42,8 @@
 //    the CTA drains its outstanding copies and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cmath>
 #include <cstdint>
@@ -93,6 +95,31 @@ struct Vec<uint16_t, 128> {
     f[3] = __uint_as_float(v.y & 0xffff0000u);
   }
 };
+
+// FP8 E4M3 pages: lane owns VEC codes, converted exactly (through half)
+template <>
+struct Vec<uint8_t, 64> {
+  __device__ static void load(const uint8_t *p, float (&f)[2]) {
+    const __nv_fp8x2_storage_t v = *reinterpret_cast<const uint16_t *>(p);
+    const float2 a = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(v, __NV_E4M3)));
+    f[0] = a.x; f[1] = a.y;
+  }
+};
+template <>
+struct Vec<uint8_t, 128> {
+  __device__ static void load(const uint8_t *p, float (&f)[4]) {
+    const uint32_t v = *reinterpret_cast<const uint32_t *>(p);
+    const float2 a = __half22float2(
+        __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3)));
+    const float2 c = __half22float2(
+        __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v >> 16), __NV_E4M3)));
+    f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
+  }
+};
+
+// element type of q and out: the cache's, bf16 bits for an FP8 cache
+template <typename T> struct QT { using type = T; };
+template <> struct QT<uint8_t> { using type = uint16_t; };
 
 template <typename T, int D>
 struct Cfg {
@@ -739,10 +766,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (gr < p.rows) {
             const int i = gr / p.group;
             const int h = g * p.group + gr % p.group;
-            const T *qp = static_cast<const T *>(p.q) +
-                          (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
-                          lane * VEC;
-            Vec<T, D>::load(qp, q[r]);
+            using TQ = typename QT<T>::type;
+            const TQ *qp = static_cast<const TQ *>(p.q) +
+                           (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
+                           lane * VEC;
+            Vec<TQ, D>::load(qp, q[r]);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
             t[r] = t0 + i;
@@ -851,12 +879,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           a.z = fmaf(f, v.z, a.z);
           a.w = fmaf(f, v.w, a.w);
         }
+        // an FP8 cache's V scale (1 otherwise) applies to every output
+        a.x *= p.v_scale;
+        a.y *= p.v_scale;
+        a.z *= p.v_scale;
+        a.w *= p.v_scale;
         const int gr = rg * RB + r;
         if (single) {
           const int i = gr / p.group;
           const int h = g * p.group + gr % p.group;
-          T *dst = static_cast<T *>(p.out) +
-                   (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D + d;
+          using TQ = typename QT<T>::type;
+          TQ *dst = static_cast<TQ *>(p.out) +
+                    (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D + d;
           store_out(dst + 0, a.x);
           store_out(dst + 1, a.y);
           store_out(dst + 2, a.z);
@@ -939,6 +973,18 @@ static cudaError_t launch_t(const AttnParams &p, int grid, cudaStream_t st) {
       } else {                                                        \
         if (RB == 16) CALL(uint16_t, 128, 16, true);                  \
         else CALL(uint16_t, 128, 32, true);                           \
+      }                                                               \
+    } else if (DTYPE == 2) {                                          \
+      if (HD == 64) {                                                 \
+        switch (RB) { case 1: CALL(uint8_t, 64, 1, false); break;     \
+                      case 2: CALL(uint8_t, 64, 2, false); break;     \
+                      case 4: CALL(uint8_t, 64, 4, false); break;     \
+                      default: CALL(uint8_t, 64, 8, false); }         \
+      } else {                                                        \
+        switch (RB) { case 1: CALL(uint8_t, 128, 1, false); break;    \
+                      case 2: CALL(uint8_t, 128, 2, false); break;    \
+                      case 4: CALL(uint8_t, 128, 4, false); break;    \
+                      default: CALL(uint8_t, 128, 8, false); }        \
       }                                                               \
     } else if (DTYPE == 0) {                                          \
       if (HD == 64) {                                                 \

@@ -5,7 +5,10 @@
 // block via the page table).  Row (b, k, g) of k_new/v_new goes to logical
 // position pos = seq_lens[b] - n_new + k, i.e. page block_table[b][pos/16],
 // row pos % 16, kv head g.  A byte copy: one warp moves one K row and one V
-// row with 16-byte vector accesses.
+// row with 16-byte vector accesses.  Into an FP8 E4M3 cache each bf16 value
+// x becomes the code of x / scale (round to nearest even, saturating).
+#include <cuda_fp8.h>
+
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -39,6 +42,42 @@ __global__ void __launch_bounds__(32 * kAppendWarps)
   const int phys = p.block_table[(size_t)b * p.max_blocks + pos / kBlockSize];
   if (phys < 0 || phys >= p.num_blocks) {
     if (lane == 0) atomicOr(&g_status_append, (unsigned)SVP_DEV_BAD_BLOCK_ID);
+    return;
+  }
+  if (p.fp8) {
+    // 8 bf16 values (16 bytes) in, 8 codes (8 bytes) out per lane step
+    const size_t dst = ((((size_t)phys * p.num_kv_heads + g) * kBlockSize) +
+                        pos % kBlockSize) * (size_t)p.head_dim;
+    const size_t src = (size_t)row * p.head_dim * 2;
+    for (int c = lane; c < p.head_dim / 8; c += 32) {
+      const uint4 kv = reinterpret_cast<const uint4 *>(
+          static_cast<const char *>(p.k_new) + src)[c];
+      const uint4 vv = reinterpret_cast<const uint4 *>(
+          static_cast<const char *>(p.v_new) + src)[c];
+      auto quant = [](uint4 w, float s) {
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t out[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t packed = 0;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t u = in[2 * h + t];
+            const float2 f = make_float2(__uint_as_float(u << 16) / s,
+                                         __uint_as_float(u & 0xffff0000u) / s);
+            packed |= (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE,
+                                                         __NV_E4M3)
+                      << (16 * t);
+          }
+          out[h] = packed;
+        }
+        return make_uint2(out[0], out[1]);
+      };
+      reinterpret_cast<uint2 *>(static_cast<char *>(p.k_cache) + dst)[c] =
+          quant(kv, p.k_scale);
+      reinterpret_cast<uint2 *>(static_cast<char *>(p.v_cache) + dst)[c] =
+          quant(vv, p.v_scale);
+    }
     return;
   }
   const size_t row_bytes = (size_t)p.head_dim * p.elem_bytes;

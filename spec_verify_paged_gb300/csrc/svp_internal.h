@@ -39,6 +39,7 @@ struct AttnParams {
   int seg_items;       // items that stand for a segment's fixed cost
   float qscale;        // scale * log2(e)
   const uint32_t *tree_mask;  // [batch, q_len] ancestor bits, or null
+  float v_scale;       // FP8 caches: V value = code * v_scale (else 1)
 };
 
 struct AttnPlan {
@@ -96,6 +97,8 @@ struct AppendParams {
   const int32_t *seq_lens;
   int batch, num_kv_heads, head_dim, n_new, max_blocks, num_blocks;
   int elem_bytes;
+  int fp8;                   // bf16 rows quantised into E4M3 caches
+  float k_scale, v_scale;
 };
 cudaError_t launch_kv_append(const AppendParams &p, cudaStream_t stream);
 

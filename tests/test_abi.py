@@ -96,6 +96,17 @@ def test_tree_attention_needs_a_mask(lib):
                                     P, P, None) == -2
 
 
+def test_fp8_cache_needs_positive_scales(lib):
+    d = _dims(dtype=2)                       # k_scale = v_scale = 0
+    assert lib.paged_decode_attention(ctypes.byref(d), P, P, P, P, P, 1, 0, 0,
+                                      0.1, P, P, None) == -1
+    assert lib.kv_append(ctypes.byref(d), P, P, P, P, P, P, 1, None) == -1
+    d = _dims(dtype=2, k_scale=float("inf"), v_scale=1.0)
+    assert lib.paged_decode_workspace_size(ctypes.byref(d), 1, 0, 0) == 0
+    d = _dims(dtype=2, k_scale=0.03, v_scale=0.03)
+    assert lib.paged_decode_workspace_size(ctypes.byref(d), 1, 0, 0) > 0
+
+
 def test_attention_empty_batch_is_a_no_op(lib):
     d = _dims(batch=0)
     assert lib.paged_decode_attention(ctypes.byref(d), None, None, None, None,
