@@ -189,8 +189,8 @@ struct DrawShared {
 // it = (row it / np, piece it % np), psz floats per piece, goes to slot
 // it % slots of the dynamic shared memory xs.  With bulk (16-byte aligned
 // rows) thread 0 moves items with 1-D bulk copies, a wave of `slots` at a
-// time; otherwise all threads copy with plain loads.  When every row is one
-// piece and has a slot, the rows stay resident after pass 1.
+// time; otherwise all threads copy with plain loads.  When every item has a
+// slot, the rows stay resident after pass 1.
 template <class RowPtr, class Filter = NoFilter, bool ARGMAX = false>
 struct SliceStage {
   RowPtr row_ptr;
@@ -202,10 +202,11 @@ struct SliceStage {
 
   __device__ int items() const { return R * np; }
   __device__ int piece_len(int pc) const { return min(psz, n - pc * psz); }
-  __device__ bool resident() const { return np == 1 && slots >= R; }
+  // every item has its own slot: row r's pieces are consecutive slots
+  __device__ bool resident() const { return slots >= items(); }
   // row r of the slice: shared memory when resident, else global memory
   __device__ const float *row(int r) const {
-    return resident() ? xs + (size_t)r * psz : row_ptr(r) + s0;
+    return resident() ? xs + (size_t)r * np * psz : row_ptr(r) + s0;
   }
 
   __device__ void issue(int it) const {  // thread 0, bulk mode
@@ -562,6 +563,9 @@ template <int NC, class Filter>
 __global__ void __launch_bounds__(kAThreads, 3)
     spec_accept_kernel(const AcceptParams p, int chunk, int psz, int np,
                        int slots, int bulk) {
+  // launched early (programmatic dependent launch): no global memory is
+  // touched before the previous kernel on the stream has completed
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int b = blockIdx.x / NC;
@@ -683,6 +687,9 @@ template <int NC, class Filter>
 __global__ void __launch_bounds__(kAThreads, 3)
     spec_accept_greedy_kernel(const AcceptParams p, int chunk, int psz,
                               int np, int slots, int bulk) {
+  // launched early (programmatic dependent launch): no global memory is
+  // touched before the previous kernel on the stream has completed
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int b = blockIdx.x / NC;
@@ -753,6 +760,9 @@ template <int NC>
 __global__ void __launch_bounds__(kAThreads, 3)
     spec_accept_tree_kernel(const AcceptTreeParams p, int chunk, int psz,
                             int np, int slots, int bulk) {
+  // launched early (programmatic dependent launch): no global memory is
+  // touched before the previous kernel on the stream has completed
+  pdl_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int b = blockIdx.x / NC;
@@ -936,6 +946,9 @@ AcceptPlan accept_plan(int vocab, int rows, const float *a, const float *b) {
   AcceptPlan pl;
   pl.chunk = (vocab + NC - 1) / NC;
   pl.chunk = (pl.chunk + 3) & ~3;  // whole 16-byte groups per slice
+  // whole rows per piece when they fit the staging budget (splitting rows
+  // to even out the warps' shares measured slower: more copies, waits and
+  // merges per row)
   pl.psz = std::min(pl.chunk, kStageBytes / 4);
   pl.np = (pl.chunk + pl.psz - 1) / pl.psz;
   const int items = rows * pl.np;
@@ -959,8 +972,10 @@ cudaLaunchConfig_t accept_config(int batch, size_t smem, cudaStream_t stream,
   attr[0].val.clusterDim.x = NC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -992,7 +1007,7 @@ int max_clusters16(Kern kern, std::atomic<bool> &prepared, size_t smem) {
       return cache[i].n;
   int n = 0;
   if (prepare_kernel(kern, 16, prepared) == cudaSuccess) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = accept_config<16>(1, smem, nullptr, attr);
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
@@ -1010,7 +1025,7 @@ cudaError_t launch_accept(Kern kern, std::atomic<bool> &prepared,
                           cudaStream_t stream) {
   cudaError_t e = prepare_kernel(kern, NC, prepared);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = accept_config<NC>(batch, pl.smem, stream, attr);
   e = cudaLaunchKernelEx(&cfg, kern, p, pl.chunk, pl.psz, pl.np, pl.slots,
                          pl.bulk);

@@ -248,6 +248,9 @@ constexpr int kMergeUnroll = 4;
 template <typename T, int D, int RB>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_splits_kernel(const AttnParams p) {
+  // the acceptance kernel that usually follows may be scheduled now; it
+  // reads nothing before this grid has completed
+  pdl_launch_dependents();
   pdl_wait();  // launched early: the attention grid must have finished
   const SplitDesc dsc = p.desc[blockIdx.x];
   if (!dsc.valid) return;

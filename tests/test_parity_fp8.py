@@ -108,3 +108,44 @@ def test_decode_7b_fp8_sampled(svp, oracle_mod):
                                      [0, cfg.batch * per - 1]])).astype(np.int64)
     ref = _oracle(oracle_mod, wl, rows=rows)
     _compare(got, ref, rows=rows)
+
+
+def test_fp8_cache_with_a_tree_mask(svp, oracle_mod):
+    """The draft-tree mask over an FP8 cache (CUDA-core path), against the
+    fp32 tree oracle run over the dequantised cache: every E4M3 value times
+    the power-of-two scale is exact in fp32, so both read the same keys and
+    values (the poisoned rows past each sequence are never visible)."""
+    import torch
+    depth = 2
+    n = (1 << (depth + 1)) - 1
+    cfg = W.small_config(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                         q_len=n, dtype="fp8", ctx_min=n + 1, ctx_max=300,
+                         seed=77)
+    wl = W.make_attention(cfg, n_new=n)
+    par = W.binary_tree_parents(depth)
+    mask = np.tile(W.tree_mask_from_parents(par), (3, 1))
+    kc, vc = to_dev(wl.k_cache), to_dev(wl.v_cache)
+    bt, sl = to_dev(wl.block_table), to_dev(wl.seq_lens)
+    svp.kv_append(to_dev(wl.k_new), to_dev(wl.v_new), kc, vc, bt, sl,
+                  k_scale=wl.k_scale, v_scale=wl.v_scale)
+    out, lse = svp.paged_tree_attention(
+        to_dev(wl.q), kc, vc, bt, sl, to_dev(mask.view(np.int32)),
+        scale=float(wl.scale), k_scale=wl.k_scale, v_scale=wl.v_scale)
+    torch.cuda.synchronize()
+    assert svp.read_device_status() == 0
+    got_o, got_l = out_as_f64(out), lse.cpu().numpy().astype(np.float64)
+    # reference: dequantise the appended cache into fp32 and run the fp32
+    # tree oracle over it (fp32 holds every E4M3 value times a power of two)
+    kq, vq = oracle_mod.kv_append_fp8(wl.k_new, wl.v_new, wl.k_cache,
+                                      wl.v_cache, wl.k_scale, wl.v_scale,
+                                      wl.block_table, wl.seq_lens)
+    kf = (oracle_mod.e4m3_decode(kq) * wl.k_scale).astype(np.float32)
+    vf = (oracle_mod.e4m3_decode(vq) * wl.v_scale).astype(np.float32)
+    kf = np.nan_to_num(kf, nan=0.0)
+    vf = np.nan_to_num(vf, nan=0.0)
+    qf = W.bf16_bits_to_f32(wl.q)
+    ref_o, ref_l = oracle_mod.paged_tree_attention(qf, kf, vf, wl.block_table,
+                                                   wl.seq_lens, n, mask,
+                                                   wl.scale)
+    assert np.abs(got_o - ref_o).max() <= 2e-2
+    assert np.abs(got_l - ref_l).max() <= 1e-3
