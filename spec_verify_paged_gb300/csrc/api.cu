@@ -136,9 +136,11 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   const bool mma = path == SVP_PATH_TENSOR_CORES;
   const bool tc = path == SVP_PATH_TCGEN05;
   // mma.sync: one m16 tile per warp, two warps share a page beyond 16 rows;
-  // tcgen05: the rows are the MMA's N (16 or 32)
-  int rb = (mma || tc) ? (rows <= 16 ? 16 : 32)
-                       : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  // tcgen05: the rows are the MMA's N (16 or 32), or two 32-row groups
+  // sharing each K/V tile beyond 32 rows
+  int rb = tc    ? (rows <= 16 ? 16 : rows <= 32 ? 32 : 64)
+           : mma ? (rows <= 16 ? 16 : 32)
+                 : rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
   const int n_rg = (rows + rb - 1) / rb;
   const int ctas = tc ? attention_tc_ctas_per_sm(rb, batch)
                       : attention_ctas_per_sm(dtype, head_dim, rb, mma, batch);

@@ -1053,6 +1053,7 @@ cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
     SVP_MERGE_RB(8)
     SVP_MERGE_RB(16)
     SVP_MERGE_RB(32)
+    SVP_MERGE_RB(64)
 #undef SVP_MERGE_RB
     default:
       return cudaErrorInvalidValue;

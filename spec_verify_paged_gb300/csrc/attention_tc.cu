@@ -76,11 +76,15 @@ constexpr int kTcThreads = 32 * (kSoftWarps + 2);
 constexpr int kPageTxBytes = 2 * 2 * kBoxBytes;  // K and V, two boxes each
 constexpr int kTcBatchCap = 1024;  // sequences per launch (prefix in smem)
 
-template <int N>
+// DUAL: a unit holds 2N rows (two row groups of N); both softmax groups
+// take every tile, one row group each, so each K/V tile is read once for
+// 2N rows.  Its second Q tile is paid for with a two-stage ring.
+template <int N, bool DUAL = false>
 struct TcSmem {
-  alignas(1024) unsigned char k[kStages][kTileBytes];
-  alignas(1024) unsigned char v[kStages][kTileBytes];
-  alignas(1024) unsigned char q[N * kD * 2];
+  static constexpr int ST = DUAL ? 2 : kStages;
+  alignas(1024) unsigned char k[ST][kTileBytes];
+  alignas(1024) unsigned char v[ST][kTileBytes];
+  alignas(1024) unsigned char q[(DUAL ? 2 : 1) * N * kD * 2];
   alignas(1024) unsigned char pb[kGroups][N * kTileKeys * 2];  // P per group
   alignas(16) float red_m[kGroups][4][N];
   alignas(16) float red_l[kGroups][4][N];
@@ -88,11 +92,13 @@ struct TcSmem {
   alignas(16) float alpha[kGroups][2][N];  // rescale of the state by a tile
   alignas(16) float xs_m[2][N], xs_l[2][N];  // group 1's state per segment
   alignas(16) float f0[N], f1[N];          // combine weights of the groups
-  alignas(16) float lse_st[N];             // a split partial's LSEs
+  alignas(16) float lse_st[kGroups][N];    // a split partial's LSEs
   UnitInfo unit[kUnitRing];
-  int stage_mask[kStages];  // bit k: page k of the tile was copied
-  uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[kGroups], p_full[kGroups], o_full[kGroups];
+  int stage_mask[ST];  // bit k: page k of the tile was copied
+  uint64_t full[ST], empty[ST];
+  // S ready: one barrier per group, or per group and S buffer (DUAL)
+  uint64_t s_full[kGroups * (DUAL ? 2 : 1)];
+  uint64_t p_full[kGroups], o_full[kGroups];
   uint64_t q_full, q_empty;
   uint64_t x_full[2], x_empty[2];  // group 1 -> group 0 state hand-over
   uint64_t stg_free;               // a segment's output left the P buffers
@@ -103,14 +109,16 @@ struct TcSmem {
   int prefix[1];  // [batch + 1], dynamic
 };
 
-template <int N>
+template <int N, bool DUAL = false>
 constexpr size_t tc_smem_bytes(int batch) {
-  return sizeof(TcSmem<N>) + sizeof(int) * (size_t)batch + 1024;
+  return sizeof(TcSmem<N, DUAL>) + sizeof(int) * (size_t)batch + 1024;
 }
 static_assert(tc_smem_bytes<32>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 32-row CTA");
 static_assert(tc_smem_bytes<16>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 16-row CTA");
+static_assert(tc_smem_bytes<32, true>(kTcBatchCap + 1) <= 227 * 1024,
+              "shared memory of a 64-row CTA");
 
 __device__ __forceinline__ void raise_tc(unsigned f) {
   atomicOr(&g_status_attn_tc, f);
@@ -320,14 +328,19 @@ struct TcMaps {
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
-template <int N>
+template <int N, bool DUAL>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_attention_tc_kernel(const AttnParams p,
                               const __grid_constant__ TcMaps tm) {
   extern __shared__ unsigned char smem_raw[];
-  TcSmem<N> &sm = *reinterpret_cast<TcSmem<N> *>(
+  using Smem = TcSmem<N, DUAL>;
+  Smem &sm = *reinterpret_cast<Smem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // S[group], O[group], X[2] (group 1's o handed to group 0), N columns each
+  constexpr int ST = Smem::ST;
+  constexpr int UR = DUAL ? 2 * N : N;  // rows of a unit
+  // S[group], O[group], X[2] (group 1's o handed to group 0), N columns
+  // each; DUAL: S[group][2] at (2 group + tile parity) N, O[group] at
+  // (4 + group) N
   constexpr uint32_t kTmemCols = 6 * N <= 128 ? 128 : 256;
   constexpr uint32_t kIdescS = idesc_bf16(kTileKeys, N, 0, 0);
   constexpr uint32_t kIdescO = idesc_bf16(kD, N, 1, 0);
@@ -338,12 +351,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int groups_per_seq = p.num_kv_heads * p.n_rg;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
+    for (int i = 0; i < (int)(sizeof(sm.s_full) / sizeof(uint64_t)); ++i)
+      mbar_init(&sm.s_full[i], 1);
     for (int gi = 0; gi < kGroups; ++gi) {
-      mbar_init(&sm.s_full[gi], 1);
       mbar_init(&sm.p_full[gi], 4);  // the group's warps
       mbar_init(&sm.o_full[gi], 1);
     }
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp < kSoftWarps) {
     // Q rows past a segment's valid rows are never copied: keep them zero
-    for (int i = tid; i < N * kD * 2 / 16; i += kSoftWarps * 32)
+    for (int i = tid; i < (int)sizeof(sm.q) / 16; i += kSoftWarps * 32)
       reinterpret_cast<uint4 *>(sm.q)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -436,15 +450,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool q_pending = true;
       auto issue_q = [&]() {
         q_issued = us;
-        const int vr = min(N, p.rows - seg.rg * N);
+        const int vr = min(UR, p.rows - seg.rg * UR);
         if (lane == 0) mbar_arrive_expect_tx(&sm.q_full, vr * kD * 2);
         __syncwarp();
-        if (lane < vr) {
-          const int gr = seg.rg * N + lane;
+        for (int r = lane; r < vr; r += 32) {
+          // row r of the unit: Q tile r / N (DUAL), row r % N of it
+          unsigned char *qt = sm.q + (r / N) * (N * kD * 2);
+          const int rr = r % N;
+          const int gr = seg.rg * UR + r;
           const int i = gr / p.group, h = seg.g * p.group + gr % p.group;
           const int y = (seg.b * p.q_len + i) * p.num_q_heads + h;
-          tma_load_2d(sm.q + lane * 128, &tm.q, 0, y, &sm.q_full);
-          tma_load_2d(sm.q + N * 128 + lane * 128, &tm.q, kBoxElems, y,
+          tma_load_2d(qt + rr * 128, &tm.q, 0, y, &sm.q_full);
+          tma_load_2d(qt + N * 128 + rr * 128, &tm.q, kBoxElems, y,
                       &sm.q_full);
         }
         q_pending = false;
@@ -479,9 +496,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const bool good = mine && ph >= 0 && ph < p.num_blocks;
           if (mine && !good) raise_tc(SVP_DEV_BAD_BLOCK_ID);
           const unsigned mask = __ballot_sync(kFull, good) & 0xffu;
-          const int s = c % kStages;
+          const int s = c % ST;
           if (lane == 0) {
-            if (!mbar_wait(&sm.empty[s], ((c / kStages) & 1) ^ 1)) {
+            if (!mbar_wait(&sm.empty[s], ((c / ST) & 1) ^ 1)) {
               ok = false;
             } else {
               sm.stage_mask[s] = (int)mask;
@@ -519,102 +536,202 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // give up: flag it, then wait (bounded) for copies still in flight
       raise_tc(SVP_DEV_TIMEOUT);
       sm.abort_flag = 1;
-      for (int k = max(0, c - kStages); k < c; ++k)
-        (void)mbar_wait(&sm.full[k % kStages], (k / kStages) & 1);
+      for (int k = max(0, c - ST); k < c; ++k)
+        (void)mbar_wait(&sm.full[k % ST], (k / ST) & 1);
       if (q_issued >= 0) (void)mbar_wait(&sm.q_full, q_issued & 1);
     }
   } else if (warp == kMmaWarp) {
     // ======================= MMA issuer (event driven) =======================
     if (lane == 0) {
-      bool ok = true;
-      int c_s = 0;    // next tile whose S is issued
-      int c_p = 0;    // next tile whose P V is issued
-      int p_obs = 0;  // tiles whose P is known to be written
-      int us = 0;     // segments taken from the ring
-      int left = 0, tau = 0, cur_pages = 0;
-      bool first = false, no_more = false;
-      int npg_ring[8];  // pages of tiles c_p .. c_s - 1 (at most 3)
-      uint64_t last = globaltimer();
-      while (true) {
-        bool prog = false;
-        // a new segment for the S side
-        if (left == 0 && !no_more &&
-            mbar_test(&sm.ufull[us % kUnitRing], (us / kUnitRing) & 1)) {
-          const UnitInfo ui = sm.unit[us % kUnitRing];
-          mbar_arrive(&sm.uempty[us % kUnitRing]);
-          ++us;
-          if (!ui.valid) {
-            no_more = true;
-          } else {
-            cur_pages = ui.n_pages;
-            left = (ui.n_pages + kTilePages - 1) / kTilePages;
-            tau = 0;
-            first = true;
+      if constexpr (DUAL) {
+        // both groups take every tile: S(c) of group gi goes to its buffer
+        // c & 1 once P(c-2) of gi was written; P V(c) of gi once P(c) of gi
+        // was written; the stage is released after the second P V
+        bool ok = true;
+        int c_s = 0;                 // next tile whose S is issued
+        int c_p[2] = {0, 0};         // next tile whose P V is issued, by group
+        int p_obs[2] = {0, 0};       // tiles whose P is known written, by group
+        int us = 0;
+        int left = 0, tau = 0, cur_pages = 0;
+        bool first = false, no_more = false;
+        int npg_ring[8];
+        uint64_t last = globaltimer();
+        while (true) {
+          bool prog = false;
+          if (left == 0 && !no_more &&
+              mbar_test(&sm.ufull[us % kUnitRing], (us / kUnitRing) & 1)) {
+            const UnitInfo ui = sm.unit[us % kUnitRing];
+            mbar_arrive(&sm.uempty[us % kUnitRing]);
+            ++us;
+            if (!ui.valid) {
+              no_more = true;
+            } else {
+              cur_pages = ui.n_pages;
+              left = (ui.n_pages + kTilePages - 1) / kTilePages;
+              tau = 0;
+              first = true;
+            }
+            prog = true;
           }
-          prog = true;
-        }
-        // S^T = K Q^T of tile c_s: its data is in, its group's S buffer was
-        // read (P of tile c_s - 2 written), its segment's Q is in
-        if (left > 0 && p_obs >= c_s - 1 &&
-            mbar_test(&sm.full[c_s % kStages], (c_s / kStages) & 1) &&
-            (!first || mbar_test(&sm.q_full, (us - 1) & 1))) {
-          tc_fence_after();
-          const int s = c_s % kStages, gi = c_s & 1;
-          const uint32_t ka = smem_u32(sm.k[s]), qa = smem_u32(sm.q);
+          if (left > 0 && p_obs[0] >= c_s - 1 && p_obs[1] >= c_s - 1 &&
+              mbar_test(&sm.full[c_s % ST], (c_s / ST) & 1) &&
+              (!first || mbar_test(&sm.q_full, (us - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t ka = smem_u32(sm.k[c_s % ST]);
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            // 16 head dims per k-step: 32 B inside the 128-B swizzled rows
-            const uint64_t a =
-                sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
-            const uint64_t b =
-                sw128_desc(qa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-            tc_mma(tmem + gi * N, a, b, kIdescS, ks > 0 ? 1u : 0u);
+            for (int gi = 0; gi < 2; ++gi) {
+              const uint32_t qa = smem_u32(sm.q + gi * (N * kD * 2));
+#pragma unroll
+              for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint64_t a =
+                    sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+                const uint64_t bq =
+                    sw128_desc(qa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma(tmem + (2 * gi + (c_s & 1)) * N, a, bq, kIdescS,
+                       ks > 0 ? 1u : 0u);
+              }
+              // a barrier per S buffer: S(c + 2) waits for P(c), so no
+              // phase completes twice before the group has seen it
+              tc_commit(&sm.s_full[2 * gi + (c_s & 1)]);
+            }
+            npg_ring[c_s & 7] = min(kTilePages, cur_pages - tau * kTilePages);
+            ++c_s;
+            ++tau;
+            --left;
+            first = false;
+            if (left == 0) tc_commit(&sm.q_empty);
+            prog = true;
           }
-          tc_commit(&sm.s_full[gi]);
-          npg_ring[c_s & 7] = min(kTilePages, cur_pages - tau * kTilePages);
-          ++c_s;
-          ++tau;
-          --left;
-          first = false;
-          // the segment's last S: its Q may be replaced once this completes
-          if (left == 0) tc_commit(&sm.q_empty);
-          prog = true;
-        }
-        if (p_obs < c_s && mbar_test(&sm.p_full[p_obs & 1], (p_obs >> 1) & 1)) {
-          ++p_obs;
-          prog = true;
-        }
-        // O_t^T = V^T P^T of tile c_p over its pages (16 keys per k-step);
-        // the group read the previous O of this buffer before writing P
-        if (c_p < p_obs) {
-          tc_fence_after();
-          const int s = c_p % kStages, gi = c_p & 1;
-          const uint32_t va = smem_u32(sm.v[s]), pa = smem_u32(sm.pb[gi]);
-          const int npg = npg_ring[c_p & 7];
-          for (int ks = 0; ks < npg; ++ks) {
-            // V as MN-major A: 64-dim halves kHalfBytes apart (leading byte
-            // offset), 8-key groups 1024 B apart (stride byte offset)
-            const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
-            const uint64_t b =
-                sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-            tc_mma(tmem + (2 + gi) * N, a, b, kIdescO, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi)
+            if (p_obs[gi] < c_s && mbar_test(&sm.p_full[gi], p_obs[gi] & 1)) {
+              ++p_obs[gi];
+              prog = true;
+            }
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            if (c_p[gi] < p_obs[gi]) {
+              tc_fence_after();
+              const int c = c_p[gi];
+              const uint32_t va = smem_u32(sm.v[c % ST]);
+              const uint32_t pa = smem_u32(sm.pb[gi]);
+              const int npg = npg_ring[c & 7];
+              for (int ks = 0; ks < npg; ++ks) {
+                const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
+                const uint64_t bp =
+                    sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma(tmem + (4 + gi) * N, a, bp, kIdescO, ks > 0 ? 1u : 0u);
+              }
+              tc_commit(&sm.o_full[gi]);
+              ++c_p[gi];
+              // the other group's P V of this tile was issued before
+              if (c_p[1 - gi] > c) tc_commit(&sm.empty[c % ST]);
+              prog = true;
+            }
           }
-          tc_commit(&sm.empty[s]);
-          tc_commit(&sm.o_full[gi]);
-          ++c_p;
-          prog = true;
+          if (no_more && left == 0 && c_p[0] == c_s && c_p[1] == c_s) break;
+          if (prog) {
+            last = globaltimer();
+          } else if (sm.abort_flag || globaltimer() - last > SVP_WAIT_NS) {
+            ok = false;
+            break;
+          }
         }
-        if (no_more && left == 0 && c_p == c_s) break;
-        if (prog) {
-          last = globaltimer();
-        } else if (sm.abort_flag || globaltimer() - last > SVP_WAIT_NS) {
-          ok = false;
-          break;
+        if (!ok) {
+          raise_tc(SVP_DEV_TIMEOUT);
+          sm.abort_flag = 1;
         }
-      }
-      if (!ok) {
-        raise_tc(SVP_DEV_TIMEOUT);
-        sm.abort_flag = 1;
+      } else {
+        bool ok = true;
+        int c_s = 0;    // next tile whose S is issued
+        int c_p = 0;    // next tile whose P V is issued
+        int p_obs = 0;  // tiles whose P is known to be written
+        int us = 0;     // segments taken from the ring
+        int left = 0, tau = 0, cur_pages = 0;
+        bool first = false, no_more = false;
+        int npg_ring[8];  // pages of tiles c_p .. c_s - 1 (at most 3)
+        uint64_t last = globaltimer();
+        while (true) {
+          bool prog = false;
+          // a new segment for the S side
+          if (left == 0 && !no_more &&
+              mbar_test(&sm.ufull[us % kUnitRing], (us / kUnitRing) & 1)) {
+            const UnitInfo ui = sm.unit[us % kUnitRing];
+            mbar_arrive(&sm.uempty[us % kUnitRing]);
+            ++us;
+            if (!ui.valid) {
+              no_more = true;
+            } else {
+              cur_pages = ui.n_pages;
+              left = (ui.n_pages + kTilePages - 1) / kTilePages;
+              tau = 0;
+              first = true;
+            }
+            prog = true;
+          }
+          // S^T = K Q^T of tile c_s: its data is in, its group's S buffer was
+          // read (P of tile c_s - 2 written), its segment's Q is in
+          if (left > 0 && p_obs >= c_s - 1 &&
+              mbar_test(&sm.full[c_s % ST], (c_s / ST) & 1) &&
+              (!first || mbar_test(&sm.q_full, (us - 1) & 1))) {
+            tc_fence_after();
+            const int s = c_s % ST, gi = c_s & 1;
+            const uint32_t ka = smem_u32(sm.k[s]), qa = smem_u32(sm.q);
+  #pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+              // 16 head dims per k-step: 32 B inside the 128-B swizzled rows
+              const uint64_t a =
+                  sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+              const uint64_t b =
+                  sw128_desc(qa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma(tmem + gi * N, a, b, kIdescS, ks > 0 ? 1u : 0u);
+            }
+            tc_commit(&sm.s_full[gi]);
+            npg_ring[c_s & 7] = min(kTilePages, cur_pages - tau * kTilePages);
+            ++c_s;
+            ++tau;
+            --left;
+            first = false;
+            // the segment's last S: its Q may be replaced once this completes
+            if (left == 0) tc_commit(&sm.q_empty);
+            prog = true;
+          }
+          if (p_obs < c_s && mbar_test(&sm.p_full[p_obs & 1], (p_obs >> 1) & 1)) {
+            ++p_obs;
+            prog = true;
+          }
+          // O_t^T = V^T P^T of tile c_p over its pages (16 keys per k-step);
+          // the group read the previous O of this buffer before writing P
+          if (c_p < p_obs) {
+            tc_fence_after();
+            const int s = c_p % ST, gi = c_p & 1;
+            const uint32_t va = smem_u32(sm.v[s]), pa = smem_u32(sm.pb[gi]);
+            const int npg = npg_ring[c_p & 7];
+            for (int ks = 0; ks < npg; ++ks) {
+              // V as MN-major A: 64-dim halves kHalfBytes apart (leading byte
+              // offset), 8-key groups 1024 B apart (stride byte offset)
+              const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
+              const uint64_t b =
+                  sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma(tmem + (2 + gi) * N, a, b, kIdescO, ks > 0 ? 1u : 0u);
+            }
+            tc_commit(&sm.empty[s]);
+            tc_commit(&sm.o_full[gi]);
+            ++c_p;
+            prog = true;
+          }
+          if (no_more && left == 0 && c_p == c_s) break;
+          if (prog) {
+            last = globaltimer();
+          } else if (sm.abort_flag || globaltimer() - last > SVP_WAIT_NS) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) {
+          raise_tc(SVP_DEV_TIMEOUT);
+          sm.abort_flag = 1;
+        }
       }
       // every MMA issued has completed before tensor memory is freed
       tc_commit(&sm.drain);
@@ -632,21 +749,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int gt = tid & 127;          // key of the tile (S), head dim (O)
     const int gbar = 1 + gi;
     const uint32_t lane_base = (uint32_t)(gw * 32) << 16;
-    const uint32_t tS = tmem + lane_base + gi * N;
-    const uint32_t tO = tmem + lane_base + (2 + gi) * N;
+    const uint32_t tO = tmem + lane_base + (DUAL ? 4 + gi : 2 + gi) * N;
+    // phase of this group's t-th tile on its per-group barriers: every tile
+    // (DUAL), else every other tile
+    auto ph = [](int t) -> uint32_t {
+      return DUAL ? (uint32_t)(t & 1) : (uint32_t)((t >> 1) & 1);
+    };
     int c0 = 0, us = 0;
     bool ok = true;
     // O of this group's tile t: wait, read, fold into o with alpha(t).
     // Returns a warp-uniform success flag.
     auto fold_o = [&](int t, float (&o)[N]) -> bool {
       const bool got =
-          __all_sync(kFull, mbar_wait(&sm.o_full[gi], (t >> 1) & 1));
+          __all_sync(kFull, mbar_wait(&sm.o_full[gi], ph(t)));
       tc_fence_after();
       float ov[N];
       tmem_ld<N>(tO, ov);
       tc_wait_ld();
       const float4 *al =
-          reinterpret_cast<const float4 *>(sm.alpha[gi][(t >> 1) & 1]);
+          reinterpret_cast<const float4 *>(sm.alpha[gi][ph(t)]);
 #pragma unroll
       for (int n4 = 0; n4 < N / 4; ++n4) {
         const float4 a = al[n4];
@@ -666,8 +787,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ui.valid) break;
       const int b = ui.b, g = ui.g, rg = ui.rg, L = ui.seq_len;
       const int t0 = L - p.q_len;
-      const int vrows = min(N, p.rows - rg * N);
-      const int row0 = rg * N;  // first global row of the group's N rows
+      // first global row of the group's N rows
+      const int row0 = DUAL ? rg * UR + gi * N : rg * N;
+      const int vrows = max(0, min(N, p.rows - row0));
 
       float o[N];
 #pragma unroll
@@ -676,12 +798,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
       int prev = -1;  // this group's previous tile in the segment
       const int tiles = (ui.n_pages + kTilePages - 1) / kTilePages;
-      for (int tau = (c0 & 1) == gi ? 0 : 1; tau < tiles; tau += 2) {
+      for (int tau = DUAL || (c0 & 1) == gi ? 0 : 1; tau < tiles;
+           tau += DUAL ? 1 : 2) {
         const int c = c0 + tau;
-        const int s = c % kStages;
-        bool got = mbar_wait(&sm.s_full[gi], (c >> 1) & 1);
-        got = got && mbar_wait(&sm.full[s], (c / kStages) & 1);
+        const int s = c % ST;
+        bool got = mbar_wait(&sm.s_full[DUAL ? 2 * gi + (c & 1) : gi],
+                             (c >> 1) & 1);
+        got = got && mbar_wait(&sm.full[s], (c / ST) & 1);
         tc_fence_after();
+        const uint32_t tS =
+            tmem + lane_base + (DUAL ? 2 * gi + (c & 1) : gi) * N;
         float sv[N];
         tmem_ld<N>(tS, sv);
         tc_wait_ld();
@@ -754,7 +880,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           alpha_prev = ex2(m_run - mu);  // 0 while nothing was visible
           m_run = m_new;
           sm.mu[gi][gt] = mu;
-          sm.alpha[gi][(c >> 1) & 1][gt] = alpha_prev;
+          sm.alpha[gi][ph(c)][gt] = alpha_prev;
         }
         named_bar(gbar, kGroupThreads);
 
@@ -777,7 +903,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (prev >= 0) ok = fold_o(prev, o) && ok;
         // group 0 stages the previous segment's output in both P buffers:
         // group 1 writes P again once the TMA engine has read it
-        if (gi == 1 && prev < 0 && us > 0)
+        if (!DUAL && gi == 1 && prev < 0 && us > 0)
           ok = __all_sync(kFull, mbar_wait(&sm.stg_free, (us - 1) & 1)) && ok;
         unsigned char *pbuf = sm.pb[gi];
 #pragma unroll
@@ -803,7 +929,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          (sm.red_l[gi][2][gt] + sm.red_l[gi][3][gt]));
       const int xk = us & 1;
       const uint32_t tX = tmem + lane_base + (4 + xk) * N;
-      if (gi == 1) {
+      if constexpr (DUAL) {
+        // ---- epilogue of this group's N rows: no hand-over; staged in the
+        // group's own P buffer, whose last P V has completed ----
+        const bool single = ui.f == ui.l;
+        const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
+        float *fw = gi == 0 ? sm.f0 : sm.f1;
+        if (gt < N) {
+          fw[gt] = l_run > 0.f ? 1.f / l_run : 0.f;
+          const float lse2 = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+          if (single) {
+            if (gt < vrows) {
+              const int gr = row0 + gt;
+              const int i = gr / p.group, h = g * p.group + gr % p.group;
+              p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
+            }
+          } else {
+            sm.lse_st[gi][gt] = lse2;
+          }
+        }
+        named_bar(gbar, kGroupThreads);
+        if (single) {
+          __nv_bfloat16 *stg16 = reinterpret_cast<__nv_bfloat16 *>(&sm.pb[gi][0]);
+#pragma unroll
+          for (int n = 0; n < N; ++n)
+            stg16[n * kD + gt] = __float2bfloat16_rn(o[n] * fw[n]);
+          fence_proxy_async_smem();
+          named_bar(gbar, kGroupThreads);
+          if (gt == 0) {
+            for (int n = 0; n < vrows;) {
+              const int gr = row0 + n, i = gr / p.group;
+              const int n_end = min(vrows, (i + 1) * p.group - row0);
+              const int h = g * p.group + gr % p.group;
+              bulk_s2g(static_cast<uint16_t *>(p.out) +
+                           (((size_t)b * p.q_len + i) * p.num_q_heads + h) * kD,
+                       stg16 + n * kD, (uint32_t)(n_end - n) * kD * 2);
+              n = n_end;
+            }
+            bulk_commit();
+            bulk_wait_read();
+          }
+        } else {
+          // fp32 rows of 128 dims in two 64-dim halves: [N][64] per pass,
+          // one 256-byte copy per row, issued by the row's thread
+          float *stg32 = reinterpret_cast<float *>(&sm.pb[gi][0]);
+          for (int hh = 0; hh < 2; ++hh) {
+            if ((gt >> 6) == hh) {
+#pragma unroll
+              for (int n = 0; n < N; ++n)
+                stg32[n * 64 + (gt & 63)] = o[n] * fw[n];
+            }
+            fence_proxy_async_smem();
+            named_bar(gbar, kGroupThreads);
+            if (gt < N) {
+              bulk_s2g(p.part_o + (pslot * UR + gi * N + gt) * kD + hh * 64,
+                       stg32 + gt * 64, 64 * 4);
+              if (hh == 0 && gt == 0)
+                bulk_s2g(p.part_lse + pslot * UR + gi * N, sm.lse_st[gi], N * 4);
+              bulk_commit();
+              bulk_wait_read();
+            }
+            named_bar(gbar, kGroupThreads);
+          }
+          if (gi == 0 && gt == 0) record_split(p, ui, blockIdx.x);
+        }
+        // fw and the P buffer are rewritten only after this barrier
+        named_bar(gbar, kGroupThreads);
+      } else if (gi == 1) {
         // ---- hand the state to group 0 (its copy of segment us - 2 must
         // have been taken) and go on with the next segment ----
         bool got = us < 2 || mbar_wait(&sm.x_empty[xk], ((us >> 1) - 1) & 1);
@@ -846,7 +1038,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               p.lse[((size_t)b * p.q_len + i) * p.num_q_heads + h] = lse2 * kLn2;
             }
           } else {
-            sm.lse_st[gt] = lse2;
+            sm.lse_st[0][gt] = lse2;
           }
         }
         // group 1's state is read: its slot may be reused
@@ -883,7 +1075,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           } else {
             bulk_s2g(p.part_o + pslot * N * kD, stg32, N * kD * 4);
-            bulk_s2g(p.part_lse + pslot * N, sm.lse_st, N * 4);
+            bulk_s2g(p.part_lse + pslot * N, sm.lse_st[0], N * 4);
             record_split(p, ui, blockIdx.x);
           }
           bulk_commit();
@@ -901,7 +1093,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       raise_tc(SVP_DEV_TIMEOUT);
       sm.abort_flag = 1;
     }
-    if (gi == 0 && gt == 0) bulk_wait();  // the output stores have landed
+    // the output stores have landed
+    if (DUAL ? gt < N : gi == 0 && gt == 0) bulk_wait();
   }
 
   // no warp leaves while others may use the barriers; tensor memory is
@@ -926,10 +1119,10 @@ static size_t tc_batch_bucket(int batch) {
   return (size_t)(batch + 255) / 256 * 256;
 }
 
-template <int N>
+template <int N, bool DUAL>
 static int prepare_tc(int batch) {
-  const size_t smem = tc_smem_bytes<N>((int)tc_batch_bucket(batch));
-  auto kern = paged_attention_tc_kernel<N>;
+  const size_t smem = tc_smem_bytes<N, DUAL>((int)tc_batch_bucket(batch));
+  auto kern = paged_attention_tc_kernel<N, DUAL>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   const auto key = std::make_tuple(dev, (const void *)kern, smem);
@@ -951,10 +1144,10 @@ static int prepare_tc(int batch) {
   return n;
 }
 
-template <int N>
+template <int N, bool DUAL>
 static cudaError_t launch_tc(const AttnParams &p, int grid, cudaStream_t st) {
-  if (prepare_tc<N>(p.batch) < 0) return cudaErrorInvalidValue;
-  const size_t smem = tc_smem_bytes<N>((int)tc_batch_bucket(p.batch));
+  if (prepare_tc<N, DUAL>(p.batch) < 0) return cudaErrorInvalidValue;
+  const size_t smem = tc_smem_bytes<N, DUAL>((int)tc_batch_bucket(p.batch));
   TcMaps tm;
   memset(&tm, 0, sizeof tm);
   if (!cached_map(&tm.k, 0, p.k_cache, p.num_blocks, p.num_kv_heads, kD) ||
@@ -962,24 +1155,27 @@ static cudaError_t launch_tc(const AttnParams &p, int grid, cudaStream_t st) {
       !cached_map(&tm.q, 1, p.q, (long long)p.batch * p.q_len * p.num_q_heads,
                   0, kD))
     return cudaErrorInvalidValue;
-  return launch_pdl(paged_attention_tc_kernel<N>, (unsigned)grid,
+  return launch_pdl(paged_attention_tc_kernel<N, DUAL>, (unsigned)grid,
                     (unsigned)kTcThreads, smem, st, p, tm);
 }
 
 int tc_batch_cap() { return kTcBatchCap; }
 
 int attention_tc_ctas_per_sm(int rb, int batch) {
-  const int n = rb == 16 ? prepare_tc<16>(batch) : prepare_tc<32>(batch);
+  const int n = rb == 16   ? prepare_tc<16, false>(batch)
+                : rb == 32 ? prepare_tc<32, false>(batch)
+                           : prepare_tc<32, true>(batch);
   return n > 0 ? n : 1;
 }
 
 cudaError_t launch_attention_tc(const AttnParams &p, int grid,
                                 cudaStream_t stream) {
-  if (p.head_dim != kD || (p.rb != 16 && p.rb != 32) ||
+  if (p.head_dim != kD || (p.rb != 16 && p.rb != 32 && p.rb != 64) ||
       p.batch > kTcBatchCap)
     return cudaErrorInvalidValue;
-  return p.rb == 16 ? launch_tc<16>(p, grid, stream)
-                    : launch_tc<32>(p, grid, stream);
+  return p.rb == 16   ? launch_tc<16, false>(p, grid, stream)
+         : p.rb == 32 ? launch_tc<32, false>(p, grid, stream)
+                      : launch_tc<32, true>(p, grid, stream);
 }
 
 cudaError_t read_status_attention_tc(cudaStream_t s, unsigned *flags) {

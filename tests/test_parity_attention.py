@@ -131,6 +131,33 @@ def test_split_counts_agree(svp, oracle_mod, sp, path):
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
 
 
+TWO_GROUPS = [
+    # (Hq, Hkv, q_len, n_sink, window, split_pages): rows = Hq / Hkv * q_len
+    (32, 8, 9, 0, 0, 0),     # 36 rows: the second group holds 4
+    (32, 8, 9, 0, 0, 2),     # the same, split across CTAs
+    (16, 1, 4, 0, 0, 1),     # exactly 64 rows, one page per split
+    (8, 1, 9, 0, 0, 3),      # 72 rows: the second unit's second group is empty
+    (32, 4, 6, 4, 37, 0),    # 48 rows under sinks + window
+    (8, 2, 16, 0, 0, 7),     # 64 rows of one query position per 4 heads
+]
+
+
+@pytest.mark.parametrize("path", [0, 3])
+@pytest.mark.parametrize("case", TWO_GROUPS,
+                         ids=[str(i) for i in range(len(TWO_GROUPS))])
+def test_tc_two_row_groups(svp, oracle_mod, case, path):
+    """More than 32 rows per KV head: the tcgen05 kernel takes 64-row units
+    whose two 32-row groups share every K/V tile; ragged and empty second
+    groups, splits and a sink/window mask."""
+    Hq, Hkv, q_len, n_sink, window, sp = case
+    cfg = W.small_config(batch=4, num_q_heads=Hq, num_kv_heads=Hkv,
+                         head_dim=128, q_len=q_len, ctx_min=q_len,
+                         ctx_max=900, seed=400 + Hq + q_len + sp)
+    wl = W.make_attention(cfg, n_new=min(q_len, 2))
+    got = _run_gpu(svp, wl, n_sink, window, split_pages=sp, kernel_path=path)
+    _compare(wl, got, _oracle(oracle_mod, wl, n_sink, window))
+
+
 @pytest.mark.parametrize("path,q_len,Hq", [(1, 1, 4), (2, 1, 4), (2, 3, 8),
                                            (3, 1, 4), (3, 3, 8)])
 def test_ring_layout_small(svp, oracle_mod, path, q_len, Hq):
