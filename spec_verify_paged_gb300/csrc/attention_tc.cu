@@ -748,6 +748,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int gw = warp & 3;           // warp in the group = TMEM lane quadrant
     const int gt = tid & 127;          // key of the tile (S), head dim (O)
     const int gbar = 1 + gi;
+    const float qmul = p.qscale > 0.f ? p.qscale : 1.f;
     const uint32_t lane_base = (uint32_t)(gw * 32) << 16;
     const uint32_t tO = tmem + lane_base + (DUAL ? 4 + gi : 2 + gi) * N;
     // phase of this group's t-th tile on its per-group barriers: every tile
@@ -812,55 +813,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld<N>(tS, sv);
         tc_wait_ld();
 
-        // ---- this thread's key ----
-        const int kslot = gt >> 4, r = gt & 15;
+        // S enters the exponent as fma(s, qmul, -mu): with a positive
+        // scale the max is taken over raw S and scaled once per column
+        // (rounding is monotonic, so that is the max of the scaled S);
+        // otherwise S is scaled here and qmul is 1
+        if (!(p.qscale > 0.f)) {
+#pragma unroll
+          for (int n = 0; n < N; ++n) sv[n] *= p.qscale;
+        }
+        // an interior tile: all eight pages copied (a shorter tile's empty
+        // slots hold stale keys), no window, every key at or before the
+        // first query position (before it, under a draft tree) -- all keys
+        // real and seen by every row
         const int npg = min(kTilePages, ui.n_pages - tau * kTilePages);
-        const bool loaded = ((sm.stage_mask[s] >> kslot) & 1) != 0;
-        const int j =
-            logical_block(ui, ui.page0 + tau * kTilePages + kslot) * kBlockSize + r;
-        // visible to some row of the call: holds real data
-        const bool in_union = loaded && j < L &&
-                              (p.window == 0 || j < p.n_sink || j > t0 - p.window);
-        if (got && kslot < npg && !in_union) {
-          // p = 0 here, but 0 * NaN left in unused cache rows is still NaN
+        const int smask = sm.stage_mask[s];
+        const int jlast =
+            logical_block(ui, ui.page0 + tau * kTilePages + npg - 1) * kBlockSize +
+            kBlockSize - 1;
+        const bool interior = p.window == 0 && npg == kTilePages &&
+                              smask == (1 << kTilePages) - 1 &&
+                              jlast <= t0 - (p.tree_mask ? 1 : 0);
+        if (!interior) {
+          // ---- this thread's key ----
+          const int kslot = gt >> 4, r = gt & 15;
+          const bool loaded = ((smask >> kslot) & 1) != 0;
+          const int j =
+              logical_block(ui, ui.page0 + tau * kTilePages + kslot) * kBlockSize + r;
+          // visible to some row of the call: holds real data
+          const bool in_union = loaded && j < L &&
+                                (p.window == 0 || j < p.n_sink || j > t0 - p.window);
+          if (got && kslot < npg && !in_union) {
+            // p = 0 here, but 0 * NaN left in unused cache rows is still NaN
 #pragma unroll
-          for (int bx = 0; bx < 2; ++bx)
+            for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4 *>(sm.v[s] + bx * kHalfBytes + gt * 128 +
-                                         ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        // rows n that see key j: n in [nlo, nhi); row n is query position
-        // i = (row0 + n) / group, at t0 + i
-        int nlo = 0, nhi = N;
-        if (!in_union) {
-          nlo = N;
-        } else {
-          if (j > t0) nlo = min(N, (j - t0) * p.group - row0);
-          if (p.window != 0 && j >= p.n_sink) {
-            const long long lim = (long long)(j + p.window - t0) * p.group - row0;
-            nhi = lim < N ? (int)lim : N;
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(sm.v[s] + bx * kHalfBytes + gt * 128 +
+                                           ch * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
-        }
-        // a draft tree: node key j = t0 + k is seen by the rows whose node
-        // has bit k set (columns past the last row count as seeing it)
-        uint32_t cb = ~0u;
-        if (p.tree_mask && in_union && j >= t0) {
-          const int k = j - t0;
-          cb = 0u;
-          int i = row0 / p.group, rem = row0 - i * p.group;
-          for (int n = 0; n < N; ++n) {
-            const uint32_t bits = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
-            cb |= ((bits >> k) & 1u) << n;
-            if (++rem == p.group) { rem = 0; ++i; }
+          // rows n that see key j: n in [nlo, nhi); row n is query position
+          // i = (row0 + n) / group, at t0 + i
+          int nlo = 0, nhi = N;
+          if (!in_union) {
+            nlo = N;
+          } else {
+            if (j > t0) nlo = min(N, (j - t0) * p.group - row0);
+            if (p.window != 0 && j >= p.n_sink) {
+              const long long lim = (long long)(j + p.window - t0) * p.group - row0;
+              nhi = lim < N ? (int)lim : N;
+            }
           }
-        }
-        const bool all_vis = __all_sync(kFull, nlo <= 0 && nhi >= N && cb == ~0u);
+          // a draft tree: node key j = t0 + k is seen by the rows whose node
+          // has bit k set (columns past the last row count as seeing it)
+          uint32_t cb = ~0u;
+          if (p.tree_mask && in_union && j >= t0) {
+            const int k = j - t0;
+            cb = 0u;
+            int i = row0 / p.group, rem = row0 - i * p.group;
+            for (int n = 0; n < N; ++n) {
+              const uint32_t bits = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
+              cb |= ((bits >> k) & 1u) << n;
+              if (++rem == p.group) { rem = 0; ++i; }
+            }
+          }
+          if (!__all_sync(kFull, nlo <= 0 && nhi >= N && cb == ~0u)) {
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const float x = sv[n] * p.qscale;
-          sv[n] = (all_vis || (n >= nlo && n < nhi && ((cb >> n) & 1u)))
-                      ? x : -INFINITY;
+            for (int n = 0; n < N; ++n)
+              sv[n] = (n >= nlo && n < nhi && ((cb >> n) & 1u)) ? sv[n]
+                                                                 : -INFINITY;
+          }
         }
 
         // ---- column max over the tile's 128 keys ----
@@ -869,7 +890,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = bar_and(gbar, kGroupThreads, ok && got);
         if (!ok) break;
         if (gt < N) {
-          const float mt = fmaxf(fmaxf(sm.red_m[gi][0][gt], sm.red_m[gi][1][gt]),
+          const float mt = qmul *
+                           fmaxf(fmaxf(sm.red_m[gi][0][gt], sm.red_m[gi][1][gt]),
                                  fmaxf(sm.red_m[gi][2][gt], sm.red_m[gi][3][gt]));
           if (prev >= 0)
             l_run = fmaf(l_run, alpha_prev,
@@ -890,10 +912,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int n4 = 0; n4 < N / 4; ++n4) {
             const float4 m4 = mu4[n4];
-            sv[4 * n4 + 0] = ex2(sv[4 * n4 + 0] - m4.x);
-            sv[4 * n4 + 1] = ex2(sv[4 * n4 + 1] - m4.y);
-            sv[4 * n4 + 2] = ex2(sv[4 * n4 + 2] - m4.z);
-            sv[4 * n4 + 3] = ex2(sv[4 * n4 + 3] - m4.w);
+            sv[4 * n4 + 0] = ex2(fmaf(sv[4 * n4 + 0], qmul, -m4.x));
+            sv[4 * n4 + 1] = ex2(fmaf(sv[4 * n4 + 1], qmul, -m4.y));
+            sv[4 * n4 + 2] = ex2(fmaf(sv[4 * n4 + 2], qmul, -m4.z));
+            sv[4 * n4 + 3] = ex2(fmaf(sv[4 * n4 + 3], qmul, -m4.w));
           }
         }
         const float cs = col_reduce<N, false>(sv, lane);

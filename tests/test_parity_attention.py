@@ -131,6 +131,20 @@ def test_split_counts_agree(svp, oracle_mod, sp, path):
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
 
 
+@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("scale", [0.0, -0.07, 0.3])
+def test_scale_sign(svp, oracle_mod, path, scale):
+    """A zero, negative or large softmax scale (the kernels take the max of
+    raw scores only for a positive scale)."""
+    cfg = W.small_config(batch=3, num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, q_len=3, ctx_min=3, ctx_max=700,
+                         seed=41)
+    wl = W.make_attention(cfg, n_new=2)
+    wl.scale = np.float32(scale)
+    got = _run_gpu(svp, wl, 0, 0, kernel_path=path)
+    _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
+
+
 TWO_GROUPS = [
     # (Hq, Hkv, q_len, n_sink, window, split_pages): rows = Hq / Hkv * q_len
     (32, 8, 9, 0, 0, 0),     # 36 rows: the second group holds 4
