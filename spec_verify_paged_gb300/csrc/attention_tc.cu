@@ -316,6 +316,88 @@ __device__ __forceinline__ uint32_t kmajor_off(int n, int k) {
                     ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2);
 }
 
+// S in the mma-fragment layout: a warp reads its 32 TMEM lanes (keys) as
+// two 16-lane halves of 8 J columns (query rows); thread t holds lanes t/4
+// and t/4 + 8 of each half, columns 8 i + 2 (t % 4) + {0, 1} of each chunk.
+template <int J>
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[4 * J]);
+
+template <>
+__device__ __forceinline__ void tmem_ld16<4>(uint32_t addr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,"
+      "%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(addr));
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld16<2>(uint32_t addr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(addr));
+}
+
+// Reduction of a row's values over the 32 keys of a warp: a thread holds
+// rows 8 j + 2 (t % 4) + e (already folded over its four keys); lanes of
+// equal t % 4 hold the other keys.  A transposing butterfly over lane bits
+// 4, 3, 2 leaves lane t with row row_of<J>(t) (J = 2: lanes t and t ^ 4
+// share one).
+template <int J, bool MAX>
+__device__ __forceinline__ float row_reduce(const float (&x)[J][2], int lane) {
+  static_assert(J == 2 || J == 4, "16 or 32 rows");
+  float v[2 * J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    v[2 * j] = x[j][0];
+    v[2 * j + 1] = x[j][1];
+  }
+#pragma unroll
+  for (int h = J, off = 16; h >= 1; h >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = upper ? v[i] : v[i + h];
+      const float keep = upper ? v[i + h] : v[i];
+      const float got = __shfl_xor_sync(kFull, send, off);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  if (J == 2) {
+    const float got = __shfl_xor_sync(kFull, v[0], 4);
+    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+  }
+  return v[0];
+}
+
+template <int J>
+__device__ __forceinline__ int row_of(int lane) {
+  const int v = J == 4 ? (lane >> 2) & 7 : (lane >> 3) & 3;
+  return 8 * (v >> 1) + 2 * (lane & 3) + (v & 1);
+}
+
+// Four 8x8 bf16 blocks, stored transposed: this thread's fragment r[i]
+// (rows 2 (t % 4) and 2 (t % 4) + 1 of key t / 4) lands in block i, whose
+// row t % 8 starts at `addr` of lane 8 i + t % 8.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr,
+                                                  const uint32_t (&r)[4]) {
+  asm volatile(
+      "stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
+          addr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // K and V caches as 2-D tensors of 16-row pages; Q as rows of 128 dims.
 struct TcMaps {
   CUtensorMap k;
@@ -809,17 +891,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t tS =
             tmem + lane_base + (DUAL ? 2 * gi + (c & 1) : gi) * N;
-        float sv[N];
-        tmem_ld<N>(tS, sv);
-        tc_wait_ld();
+        // S of the tile: key gw 32 + 8 q + lane / 4, query row
+        // 8 j + 2 (lane % 4) + e of the group's N rows
+        constexpr int J = N / 8;
+        float sv[4][J][2];
+        {
+          uint32_t r0[4 * J], r1[4 * J];
+          tmem_ld16<J>(tS, r0);
+          tmem_ld16<J>(tS + (16u << 16), r1);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              sv[0][j][e] = __uint_as_float(r0[4 * j + e]);
+              sv[1][j][e] = __uint_as_float(r0[4 * j + 2 + e]);
+              sv[2][j][e] = __uint_as_float(r1[4 * j + e]);
+              sv[3][j][e] = __uint_as_float(r1[4 * j + 2 + e]);
+            }
+        }
 
         // S enters the exponent as fma(s, qmul, -mu): with a positive
-        // scale the max is taken over raw S and scaled once per column
+        // scale the max is taken over raw S and scaled once per row
         // (rounding is monotonic, so that is the max of the scaled S);
         // otherwise S is scaled here and qmul is 1
         if (!(p.qscale > 0.f)) {
 #pragma unroll
-          for (int n = 0; n < N; ++n) sv[n] *= p.qscale;
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+              sv[q][j][0] *= p.qscale;
+              sv[q][j][1] *= p.qscale;
+            }
         }
         // an interior tile: all eight pages copied (a shorter tile's empty
         // slots hold stale keys), no window, every key at or before the
@@ -834,59 +937,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               smask == (1 << kTilePages) - 1 &&
                               jlast <= t0 - (p.tree_mask ? 1 : 0);
         if (!interior) {
-          // ---- this thread's key ----
-          const int kslot = gt >> 4, r = gt & 15;
-          const bool loaded = ((smask >> kslot) & 1) != 0;
-          const int j =
-              logical_block(ui, ui.page0 + tau * kTilePages + kslot) * kBlockSize + r;
-          // visible to some row of the call: holds real data
-          const bool in_union = loaded && j < L &&
-                                (p.window == 0 || j < p.n_sink || j > t0 - p.window);
-          if (got && kslot < npg && !in_union) {
-            // p = 0 here, but 0 * NaN left in unused cache rows is still NaN
+          // this thread's rows: query position and draft-tree ancestor bits
+          // (rows past the last query position count as seeing every key)
+          int pos[J][2];
+          uint32_t tb[J][2];
 #pragma unroll
-            for (int bx = 0; bx < 2; ++bx)
+          for (int j = 0; j < J; ++j)
 #pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(sm.v[s] + bx * kHalfBytes + gt * 128 +
-                                           ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          // rows n that see key j: n in [nlo, nhi); row n is query position
-          // i = (row0 + n) / group, at t0 + i
-          int nlo = 0, nhi = N;
-          if (!in_union) {
-            nlo = N;
-          } else {
-            if (j > t0) nlo = min(N, (j - t0) * p.group - row0);
-            if (p.window != 0 && j >= p.n_sink) {
-              const long long lim = (long long)(j + p.window - t0) * p.group - row0;
-              nhi = lim < N ? (int)lim : N;
+            for (int e = 0; e < 2; ++e) {
+              const int i = (row0 + 8 * j + 2 * (lane & 3) + e) / p.group;
+              pos[j][e] = t0 + i;
+              tb[j][e] = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
             }
-          }
-          // a draft tree: node key j = t0 + k is seen by the rows whose node
-          // has bit k set (columns past the last row count as seeing it)
-          uint32_t cb = ~0u;
-          if (p.tree_mask && in_union && j >= t0) {
-            const int k = j - t0;
-            cb = 0u;
-            int i = row0 / p.group, rem = row0 - i * p.group;
-            for (int n = 0; n < N; ++n) {
-              const uint32_t bits = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
-              cb |= ((bits >> k) & 1u) << n;
-              if (++rem == p.group) { rem = 0; ++i; }
-            }
-          }
-          if (!__all_sync(kFull, nlo <= 0 && nhi >= N && cb == ~0u)) {
 #pragma unroll
-            for (int n = 0; n < N; ++n)
-              sv[n] = (n >= nlo && n < nhi && ((cb >> n) & 1u)) ? sv[n]
-                                                                 : -INFINITY;
+          for (int q = 0; q < 4; ++q) {
+            const int kt = gw * 32 + 8 * q + (lane >> 2);  // key of the tile
+            const int kslot = kt >> 4, r = kt & 15;
+            const bool loaded = ((smask >> kslot) & 1) != 0;
+            const int jk =
+                logical_block(ui, ui.page0 + tau * kTilePages + kslot) * kBlockSize + r;
+            // visible to some row of the call: holds real data
+            const bool in_union = loaded && jk < L &&
+                                  (p.window == 0 || jk < p.n_sink || jk > t0 - p.window);
+            if (got && kslot < npg && !in_union) {
+              // p = 0 here, but 0 * NaN left in unused cache rows is still
+              // NaN: the key's four threads clear a quarter of its V row each
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int idx = (lane & 3) * 4 + c4;
+                *reinterpret_cast<uint4 *>(sm.v[s] + (idx >> 3) * kHalfBytes +
+                                           kt * 128 + (idx & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ps = pos[j][e];
+                const bool vis =
+                    in_union && jk <= ps &&
+                    (p.window == 0 || jk < p.n_sink || jk > ps - p.window) &&
+                    (jk < t0 || ((tb[j][e] >> ((jk - t0) & 31)) & 1u) != 0);
+                if (!vis) sv[q][j][e] = -INFINITY;
+              }
           }
         }
 
-        // ---- column max over the tile's 128 keys ----
-        const float cm = col_reduce<N, true>(sv, lane);
-        if (N == 32 || (lane & 1) == 0) sm.red_m[gi][gw][col_of<N>(lane)] = cm;
+        // ---- row max over the tile's 128 keys ----
+        {
+          float mx[J][2];
+#pragma unroll
+          for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              mx[j][e] = fmaxf(fmaxf(sv[0][j][e], sv[1][j][e]),
+                               fmaxf(sv[2][j][e], sv[3][j][e]));
+          const float cm = row_reduce<J, true>(mx, lane);
+          if (J == 4 || (lane & 4) == 0) sm.red_m[gi][gw][row_of<J>(lane)] = cm;
+        }
         ok = bar_and(gbar, kGroupThreads, ok && got);
         if (!ok) break;
         if (gt < N) {
@@ -906,20 +1015,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar(gbar, kGroupThreads);
 
-        // ---- p = exp2(s - mu) and the column sums ----
+        // ---- p = exp2(s - mu) and the row sums ----
         {
-          const float4 *mu4 = reinterpret_cast<const float4 *>(sm.mu[gi]);
+          float sm_[J][2];
 #pragma unroll
-          for (int n4 = 0; n4 < N / 4; ++n4) {
-            const float4 m4 = mu4[n4];
-            sv[4 * n4 + 0] = ex2(fmaf(sv[4 * n4 + 0], qmul, -m4.x));
-            sv[4 * n4 + 1] = ex2(fmaf(sv[4 * n4 + 1], qmul, -m4.y));
-            sv[4 * n4 + 2] = ex2(fmaf(sv[4 * n4 + 2], qmul, -m4.z));
-            sv[4 * n4 + 3] = ex2(fmaf(sv[4 * n4 + 3], qmul, -m4.w));
+          for (int j = 0; j < J; ++j) {
+            const float2 m2 = *reinterpret_cast<const float2 *>(
+                &sm.mu[gi][8 * j + 2 * (lane & 3)]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              sv[q][j][0] = ex2(fmaf(sv[q][j][0], qmul, -m2.x));
+              sv[q][j][1] = ex2(fmaf(sv[q][j][1], qmul, -m2.y));
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              sm_[j][e] = (sv[0][j][e] + sv[1][j][e]) + (sv[2][j][e] + sv[3][j][e]);
           }
+          const float cs = row_reduce<J, false>(sm_, lane);
+          if (J == 4 || (lane & 4) == 0) sm.red_l[gi][gw][row_of<J>(lane)] = cs;
         }
-        const float cs = col_reduce<N, false>(sv, lane);
-        if (N == 32 || (lane & 1) == 0) sm.red_l[gi][gw][col_of<N>(lane)] = cs;
         // ---- the previous tile's O leaves the buffer before P is written:
         // its P V has then finished reading this group's P buffer too ----
         if (prev >= 0) ok = fold_o(prev, o) && ok;
@@ -927,11 +1041,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // group 1 writes P again once the TMA engine has read it
         if (!DUAL && gi == 1 && prev < 0 && us > 0)
           ok = __all_sync(kFull, mbar_wait(&sm.stg_free, (us - 1) & 1)) && ok;
-        unsigned char *pbuf = sm.pb[gi];
+        // P as bf16, K-major and swizzled: per 8-row block, four 8x8 blocks
+        // (keys gw 32 + 8 i ..) stored transposed
+        const uint32_t pbase = smem_u32(sm.pb[gi]);
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-          const __nv_bfloat16 h = __float2bfloat16_rn(sv[n]);
-          *reinterpret_cast<__nv_bfloat16 *>(pbuf + kmajor_off<N>(n, gt)) = h;
+        for (int j = 0; j < J; ++j) {
+          uint32_t fr[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) fr[q] = pack_bf16(sv[q][j][0], sv[q][j][1]);
+          stmatrix_x4_trans(
+              pbase + kmajor_off<N>(8 * j + (lane & 7), gw * 32 + 8 * (lane >> 3)),
+              fr);
         }
         fence_proxy_async_smem();  // P and zeroed V rows -> tensor core
         tc_fence_before();         // S and O reads done before they are rewritten
