@@ -237,28 +237,31 @@ __device__ __forceinline__ void record_split(const AttnParams &p,
   p.desc[cta] = d;
 }
 
-// Merge of split groups: CTA c finishes the group recorded in desc[c] (if
-// any) from the partials of CTAs c..l.  Each thread owns float4 slices of
+// Merge of split groups: CTAs c SPLIT .. c SPLIT + SPLIT - 1 finish the
+// group recorded in desc[c] (if any) from the partials of CTAs c..l, each
+// taking RB / SPLIT of its rows (a 64-row group's partials are too many
+// bytes for one SM to read quickly).  Each thread owns float4 slices of
 // a few rows and folds the splits in with an online log-sum-exp, kMergeUnroll
 // splits at a time: all their loads are issued together, so a typical group
 // (two to four splits) costs one memory round trip.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeUnroll = 4;
 
-template <typename T, int D, int RB>
+template <typename T, int D, int RB, int SPLIT>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_splits_kernel(const AttnParams p) {
   // the acceptance kernel that usually follows may be scheduled now; it
   // reads nothing before this grid has completed
   pdl_launch_dependents();
   pdl_wait();  // launched early: the attention grid must have finished
-  const SplitDesc dsc = p.desc[blockIdx.x];
+  const int f = blockIdx.x / SPLIT;
+  const int r0 = (blockIdx.x % SPLIT) * (RB / SPLIT);  // this CTA's rows
+  const SplitDesc dsc = p.desc[f];
   if (!dsc.valid) return;
   const int tid = threadIdx.x;
-  const int f = blockIdx.x;
   const int ns = dsc.l - f + 1;
   const int vrows = min(RB, p.rows - dsc.rg * RB);
-  constexpr int NE4 = RB * D / 4;  // float4 slices of the group's rows
+  constexpr int NE4 = RB / SPLIT * D / 4;  // float4 slices of the rows
   constexpr int EPT = (NE4 + kMergeThreads - 1) / kMergeThreads;
   const float4 *po4 = reinterpret_cast<const float4 *>(p.part_o);
   float m[EPT], w_sum[EPT];
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const int e4 = tid + k * kMergeThreads;
-      const int r = e4 / (D / 4), d4 = e4 % (D / 4);
+      const int r = r0 + e4 / (D / 4), d4 = e4 % (D / 4);
 #pragma unroll
       for (int j = 0; j < kMergeUnroll; ++j) {
         const int s = s0 + j;
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
     const int e4 = tid + k * kMergeThreads;
-    const int r = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
+    const int r = r0 + e4 / (D / 4), d = (e4 % (D / 4)) * 4;
     if (e4 >= NE4 || r >= vrows) continue;
     const float inv = w_sum[k] > 0.f ? 1.f / w_sum[k] : 0.f;
     const int gr = dsc.rg * RB + r;
