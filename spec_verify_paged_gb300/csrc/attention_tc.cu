@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // previous segment's last S MMA has read the old Q; tiles of this
       // segment are issued meanwhile
       bool q_pending = true;
+      const int seg_c0 = c;  // the segment's first tile
       auto issue_q = [&]() {
         q_issued = us;
         const int vr = min(UR, p.rows - seg.rg * UR);
@@ -563,9 +564,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int kend = min(k0 + kTableChunk, n_pages);
         for (int t0 = k0; t0 < kend; t0 += kTilePages) {
           if (q_pending) {
-            const bool r = __shfl_sync(
-                kFull, lane == 0 && mbar_test(&sm.q_empty, (us & 1) ^ 1), 0);
-            if (r) issue_q();
+            // the stage of tile c last held tile c - ST; if that tile is of
+            // this segment its S needs this Q, so the wait for the stage
+            // below could only end after it: wait for the old Q's last S
+            // (its release is a separate commit, and commits need not
+            // arrive in issue order)
+            const bool must = c - ST >= seg_c0;
+            bool r = false;
+            if (lane == 0)
+              r = must ? mbar_wait(&sm.q_empty, (us & 1) ^ 1)
+                       : mbar_test(&sm.q_empty, (us & 1) ^ 1);
+            r = __shfl_sync(kFull, r, 0);
+            if (r) {
+              issue_q();
+            } else if (must) {
+              ok = false;
+              break;
+            }
           }
           // tiles start at multiples of 8 pages of the segment; lane kk < 8
           // copies page t0 + kk, whose entry sits in lane (t0-k0)%32 + kk
