@@ -264,78 +264,82 @@ struct SliceStage {
         __syncthreads();
       }
       for (int it = w0 + warp; it < w1; it += kAWarps) {
-        const int r = it / np, pc = it - r * np;
-        const int len = piece_len(pc);
-        if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
-        if (len <= 0) continue;
-        float4 *x4 = reinterpret_cast<float4 *>(xs + (size_t)(it - w0) * psz);
-        const int ng = (len + 3) >> 2;
-        const int tok0 = s0 + pc * psz;  // token of the piece's first element
-        if (ARGMAX) {
-          float bv = -INFINITY;
-          int bi = INT_MAX;
-#pragma unroll 4
+        do {  // one pass: `break` ends the piece
+          const int r = it / np, pc = it - r * np;
+          const int len = piece_len(pc);
+          if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
+          if (len <= 0) break;
+          float4 *x4 = reinterpret_cast<float4 *>(xs + (size_t)(it - w0) * psz);
+          const int ng = (len + 3) >> 2;
+          const int tok0 = s0 + pc * psz;  // token of the piece's first element
+          if (ARGMAX) {
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+  #pragma unroll 4
+            for (int g = lane; g < ng; g += 32) {
+              float4 v = x4[g];
+              if (Filter::kActive) filter(r, tok0 + 4 * g, v);
+              const int t = tok0 + 4 * g;  // first of 4: ties keep the lowest
+              if (v.x > bv) { bv = v.x; bi = t; }
+              if (v.y > bv) { bv = v.y; bi = t + 1; }
+              if (v.z > bv) { bv = v.z; bi = t + 2; }
+              if (v.w > bv) { bv = v.w; bi = t + 3; }
+            }
+  #pragma unroll
+            for (int off = 16; off; off >>= 1) {
+              const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+              const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            if (lane == 0)
+              st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{bi, bv, 0.f});
+            break;
+          }
+          float m = -INFINITY;
+  #pragma unroll 4
           for (int g = lane; g < ng; g += 32) {
             float4 v = x4[g];
-            if (Filter::kActive) filter(r, tok0 + 4 * g, v);
-            const int t = tok0 + 4 * g;  // first of 4: ties keep the lowest
-            if (v.x > bv) { bv = v.x; bi = t; }
-            if (v.y > bv) { bv = v.y; bi = t + 1; }
-            if (v.z > bv) { bv = v.z; bi = t + 2; }
-            if (v.w > bv) { bv = v.w; bi = t + 3; }
+            if (Filter::kActive) {
+              filter(r, tok0 + 4 * g, v);
+              x4[g] = v;  // the filtered row is what later reads see
+            }
+            m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
           }
-#pragma unroll
+  #pragma unroll
+          for (int off = 16; off; off >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (!(m > -INFINITY)) break;  // nothing but -inf (warp-uniform)
+          const int e = (int)ceilf(fminf(m * sc, 1.0e9f));
+          const float eb = (float)e;
+          float hi = 0.f, lo = 0.f;
+  #pragma unroll 4
+          for (int g = lane; g < ng; g += 32) {
+            const float4 v = x4[g];
+            const float t =
+                (ex2(fmaf(v.x, sc, -eb)) + ex2(fmaf(v.y, sc, -eb))) +
+                (ex2(fmaf(v.z, sc, -eb)) + ex2(fmaf(v.w, sc, -eb)));
+            kahan_add(hi, lo, t);
+          }
+  #pragma unroll
           for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+            const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+            pair_add(hi, lo, oh, ol);
           }
           if (lane == 0)
-            st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{bi, bv, 0.f});
-          continue;
+            st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{e, hi, lo});
+        } while (false);
+        // bulk ring: only this warp read the slot in this wave, so the
+        // slot's piece of the next wave may be copied now (values a filter
+        // wrote back are ordered before the copy that overwrites them)
+        if (bulk && it + slots < items()) {
+          if (Filter::kActive) fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) issue(it + slots);
         }
-        float m = -INFINITY;
-#pragma unroll 4
-        for (int g = lane; g < ng; g += 32) {
-          float4 v = x4[g];
-          if (Filter::kActive) {
-            filter(r, tok0 + 4 * g, v);
-            x4[g] = v;  // the filtered row is what later reads see
-          }
-          m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if (!(m > -INFINITY)) continue;  // nothing but -inf (warp-uniform)
-        const int e = (int)ceilf(fminf(m * sc, 1.0e9f));
-        const float eb = (float)e;
-        float hi = 0.f, lo = 0.f;
-#pragma unroll 4
-        for (int g = lane; g < ng; g += 32) {
-          const float4 v = x4[g];
-          const float t =
-              (ex2(fmaf(v.x, sc, -eb)) + ex2(fmaf(v.y, sc, -eb))) +
-              (ex2(fmaf(v.z, sc, -eb)) + ex2(fmaf(v.w, sc, -eb)));
-          kahan_add(hi, lo, t);
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-          const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
-          const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
-          pair_add(hi, lo, oh, ol);
-        }
-        if (lane == 0)
-          st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{e, hi, lo});
       }
-      if (w1 < items()) {  // ring: the next wave into the same slots
-        // filtered values were written back through the generic proxy;
-        // order them before the bulk copies that overwrite the slots
-        if (Filter::kActive) fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0 && bulk)
-          for (int it = w1; it < min(items(), w1 + slots); ++it) issue(it);
-      }
+      // plain loads: every thread refills the slots of the next wave
+      if (!bulk && w1 < items()) __syncthreads();
     }
     return ok;
   }

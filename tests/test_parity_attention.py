@@ -323,3 +323,15 @@ def test_many_sequences_span_launches(svp, oracle_mod, path, batch):
     got = _run_gpu(svp, wl, 0, 0, split_pages=1, kernel_path=path)
     assert svp.last_launch_count() == 4  # two attention + two merge launches
     _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
+
+
+def test_many_sequences_span_launches_64_row_units(svp, oracle_mod):
+    """The same beyond one tcgen05 launch with 40 query rows per kv head:
+    64-row units, their split partials merged by two CTAs per group."""
+    cfg = W.small_config(batch=1030, num_q_heads=8, num_kv_heads=1,
+                         head_dim=128, q_len=5, ctx_min=5, ctx_max=60,
+                         seed=62)
+    wl = W.make_attention(cfg, n_new=2)
+    got = _run_gpu(svp, wl, 0, 0, split_pages=1, kernel_path=3)
+    assert svp.last_launch_count() == 4  # two attention + two merge launches
+    _compare(wl, got, _oracle(oracle_mod, wl, 0, 0))
