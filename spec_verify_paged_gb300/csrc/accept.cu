@@ -70,6 +70,27 @@ struct ESum {
   float hi, lo;
 };
 
+// Reads of another cluster CTA's shared memory: `mapa` gives the address
+// of this CTA's shared word `a` in CTA `rank`; the loads are issued back to
+// back and only their uses wait, so NC reads cost one round trip.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float pow2i(int k) {  // exact 2^k (0 below range)
   return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
 }
@@ -365,11 +386,16 @@ __device__ __forceinline__ void row_normalisers(cg::cluster_group &cluster,
   S = 0.f;
   if (lane < R) {
     ESum o[NC];
+    const uint32_t a0 = smem_u32(&st.slice_s[lane]);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      o[c] = cluster.map_shared_rank(&st, c)->slice_s[lane];
-      e = max(e, o[c].e);
+      const uint32_t a = cluster_map(a0, c);
+      o[c].e = ld_cluster_s32(a + offsetof(ESum, e));
+      o[c].hi = ld_cluster_f32(a + offsetof(ESum, hi));
+      o[c].lo = ld_cluster_f32(a + offsetof(ESum, lo));
     }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) e = max(e, o[c].e);
     float hi = 0.f, lo = 0.f;
 #pragma unroll
     for (int c = 0; c < NC; ++c)
@@ -414,10 +440,15 @@ __device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
   cluster.sync();
   h = 0.f;
   l = 0.f;
+  float zh[NC], zl[NC];
+  const uint32_t ah = smem_u32(&ds.zh[parity]), al = smem_u32(&ds.zl[parity]);
+#pragma unroll
   for (int c = 0; c < NC; ++c) {
-    const DrawShared *o = cluster.map_shared_rank(&ds, c);
-    pair_add(h, l, o->zh[parity], o->zl[parity]);
+    zh[c] = ld_cluster_f32(cluster_map(ah, c));
+    zl[c] = ld_cluster_f32(cluster_map(al, c));
   }
+#pragma unroll
+  for (int c = 0; c < NC; ++c) pair_add(h, l, zh[c], zl[c]);
 }
 
 // Inverse-CDF draw over weight(e) of every CTA's slice: the smallest token
@@ -477,11 +508,22 @@ __device__ bool draw_token(cg::cluster_group &cluster, DrawShared &ds,
   // cumulative masses in CTA order: the same operations in every CTA
   float Ph = 0.f, Pl = 0.f, loh = 0.f, lol = 0.f, hih = 0.f, hil = 0.f;
   int last_tok = -1;
+  float mh_[NC], ml_[NC];
+  int lt_[NC];
+  {
+    const uint32_t a0 = smem_u32(&ds);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const uint32_t a = cluster_map(a0, c);
+      mh_[c] = ld_cluster_f32(a + offsetof(DrawShared, mass_hi));
+      ml_[c] = ld_cluster_f32(a + offsetof(DrawShared, mass_lo));
+      lt_[c] = ld_cluster_s32(a + offsetof(DrawShared, last));
+    }
+  }
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    const DrawShared *o = cluster.map_shared_rank(&ds, c);
-    const float mh = o->mass_hi, ml = o->mass_lo;
-    const int lt = o->last;
+    const float mh = mh_[c], ml = ml_[c];
+    const int lt = lt_[c];
     if (c == crank) { loh = Ph; lol = Pl; }
     pair_add(Ph, Pl, mh, ml);
     if (c == crank) { hih = Ph; hil = Pl; }
@@ -541,6 +583,7 @@ struct AcceptShared {
   StageShared st;
   DrawShared ds;
   float logit_x[2 * kMaxDraft];  // target / draft logits at the drafts
+  float u[kMaxDraft + 1];        // the sequence's uniforms
   int tok[kMaxDraft];
   int accept_upto;
   int bad;
@@ -556,6 +599,7 @@ struct TreeShared {
   float lx_t[kMaxNodes];   // target / draft logits of node c's token in the
   float lx_d[kMaxNodes];   // rows of its parent
   float zinv[kMaxNodes];   // 1 / residual mass after each rejected child
+  float u[kMaxNodes];      // the sequence's uniforms
   int R;
   int bad;
 };
@@ -592,12 +636,16 @@ __global__ void __launch_bounds__(kAThreads, 3)
   const SliceStage<decltype(row_ptr), Filter> stage{
       row_ptr, R2, s0, n, psz, np, slots, bulk, xs, &sh.st, filter, sc};
   stage.begin(tid);
-  // the draft tokens, read by the last warp (it has the fewest pieces)
+  // the draft tokens and the uniforms, read by the last warp (it has the
+  // fewest pieces); they land while pass 1 runs
   const bool tok_lane = warp == kAWarps - 1 && lane < K;
   const int xtok = tok_lane ? p.draft_tokens[(size_t)b * K + lane] : 0;
+  const bool u_lane = warp == kAWarps - 1 && lane <= K;
+  const float uval = u_lane ? p.uniforms[(size_t)b * (K + 1) + lane] : 0.f;
   __syncthreads();  // barriers initialised
 
   const bool ok = stage.pass1(tid, lane, warp);
+  if (u_lane) sh.u[lane] = uval;
   if (tok_lane) {  // the logits at the drafts (from L2, while others sum)
     const bool good = xtok >= 0 && xtok < V;
     sh.tok[lane] = xtok;
@@ -620,7 +668,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
       bad_i = x < 0 || x >= V;
       const float ratio = accept_ratio(sh.logit_x[lane], sh.logit_x[K + lane],
                                        e, S, eq, Sq, sc);
-      acc_i = p.uniforms[(size_t)b * (K + 1) + lane] <= ratio;
+      acc_i = sh.u[lane] <= ratio;
       // a token the mask excludes has p(x) = 0: rejected
       if (Filter::kActive && !bad_i && !filter.allows(lane, x)) acc_i = false;
     }
@@ -634,7 +682,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
   __syncthreads();
   const bool bad = sh.bad != 0;
   const int j = bad ? K : sh.accept_upto;
-  const float uK = p.uniforms[(size_t)b * (K + 1) + K];
+  const float uK = sh.u[K];
 
   // ---- the draw: residual max(0, p_j - q_j), or the bonus from p_K ----
   // thread t owns slice elements [t*per, t*per + per); per odd, so the
@@ -725,10 +773,18 @@ __global__ void __launch_bounds__(kAThreads, 3)
     int best = -1;
     if (lane < R) {
       ESum m{INT_MAX, -INFINITY, 0.f};
+      int oe[NC];
+      float oh[NC];
+      const uint32_t a0 = smem_u32(&sh.st.slice_s[lane]);
+#pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const ESum o = cluster.map_shared_rank(&sh.st, c)->slice_s[lane];
-        if (o.hi > m.hi || (o.hi == m.hi && o.e < m.e)) m = o;
+        const uint32_t a = cluster_map(a0, c);
+        oe[c] = ld_cluster_s32(a + offsetof(ESum, e));
+        oh[c] = ld_cluster_f32(a + offsetof(ESum, hi));
       }
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (oh[c] > m.hi || (oh[c] == m.hi && oe[c] < m.e)) m = ESum{oe[c], oh[c], 0.f};
       best = m.e == INT_MAX ? -1 : m.e;  // no allowed token: -1
     }
     bool bad_i = false, acc_i = true;
@@ -785,9 +841,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
   // draft rows of the inner nodes (the rows their children came from)
   if (warp == 0) {
     int pa = -1, tk = -1;
+    float uv = 0.f;
     if (lane < N) {
       pa = p.parents[(size_t)b * N + lane];
       tk = p.node_tokens[(size_t)b * N + lane];
+      uv = p.uniforms[(size_t)b * N + lane];
     }
     const bool bad_l =
         lane < N && (lane == 0 ? pa != -1
@@ -801,6 +859,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
     if (lane < N) {
       sh.par[lane] = pa;
       sh.tok[lane] = tk;
+      sh.u[lane] = uv;
       const bool in = (inner >> lane) & 1u;
       const int r = N + __popc(inner & ((1u << lane) - 1u));
       sh.drow[lane] = in ? r : -1;
@@ -873,7 +932,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                                    sh.st.row_s[rd], kL2E);
         for (int jj = 0; jj < k; ++jj)
           ratio = fmaxf(ratio - 1.f, 0.f) * sh.zinv[jj];
-        if (p.uniforms[(size_t)b * N + c] <= ratio) {
+        if (sh.u[c] <= ratio) {
           next = c;
           break;
         }
@@ -902,7 +961,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
     }
     // one token from r_k of the last node (p itself at a leaf)
     int32_t *dst = p.out_tokens + (size_t)b * N + n_acc;
-    const float u0 = p.uniforms[(size_t)b * N];
+    const float u0 = sh.u[0];
     for (int attempt = 0; attempt < 2 && !arrived; ++attempt) {
       if (attempt == 1) k = 0;  // zero mass by rounding: fall back to p
       arrived = draw_token<NC>(
