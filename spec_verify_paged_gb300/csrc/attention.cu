@@ -1036,8 +1036,8 @@ bool tensor_maps_available() { return encode_fn() != nullptr; }
 cudaError_t launch_merge(const AttnParams &p, int dtype, int grid,
                          cudaStream_t stream) {
 #define SVP_MERGE(T, D, RB)                                            \
-  e = launch_pdl(merge_splits_kernel<T, D, RB, (RB > 32 ? 2 : 1)>,      \
-                 (unsigned)grid * (RB > 32 ? 2u : 1u),                  \
+  e = launch_pdl(merge_splits_kernel<T, D, RB, (RB >= 32 ? RB / 16 : 1)>, \
+                 (unsigned)grid * (RB >= 32 ? RB / 16u : 1u),           \
                  (unsigned)kMergeThreads, 0, stream, p)
   const bool f32 = dtype == 0;
   const int D = p.head_dim;

@@ -239,8 +239,8 @@ __device__ __forceinline__ void record_split(const AttnParams &p,
 
 // Merge of split groups: CTAs c SPLIT .. c SPLIT + SPLIT - 1 finish the
 // group recorded in desc[c] (if any) from the partials of CTAs c..l, each
-// taking RB / SPLIT of its rows (a 64-row group's partials are too many
-// bytes for one SM to read quickly).  Each thread owns float4 slices of
+// taking RB / SPLIT of its rows (one SM reading all the partials of a 32-
+// or 64-row group is slower than several reading 16 rows each).  Each thread owns float4 slices of
 // a few rows and folds the splits in with an online log-sum-exp, kMergeUnroll
 // splits at a time: all their loads are issued together, so a typical group
 // (two to four splits) costs one memory round trip.
