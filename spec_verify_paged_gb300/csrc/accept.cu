@@ -70,9 +70,17 @@ struct ESum {
   float hi, lo;
 };
 
+// A slice's ESum as other cluster CTAs read it: one 16-byte record, one
+// vector load per CTA.
+struct alignas(16) ESum4 {
+  int e;
+  float hi, lo, pad;
+};
+
 // Reads of another cluster CTA's shared memory: `mapa` gives the address
 // of this CTA's shared word `a` in CTA `rank`; the loads are issued back to
-// back and only their uses wait, so NC reads cost one round trip.
+// back and only their uses wait, and each reads a whole record (vector
+// loads: the request count, not the bytes, sets their cost).
 __device__ __forceinline__ uint32_t cluster_map(uint32_t a, int rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
@@ -80,14 +88,20 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t a, int rank) {
                : "r"(a), "r"(rank));
   return r;
 }
-__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t a) {  // 16-B aligned
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
   return v;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+__device__ __forceinline__ float2 ld_cluster_v2f(uint32_t a) {  // 8-B aligned
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];"
+               : "=f"(v.x), "=f"(v.y)
+               : "r"(a)
+               : "memory");
   return v;
 }
 
@@ -190,21 +204,27 @@ struct TokenMask {
 // Slice statistics of every staged row (read cluster-wide).
 struct StageShared {
   ESum warp_s[kAWarps][kMaxRows];  // pass 1: per-warp partials
-  ESum slice_s[kMaxRows];          // this CTA's slice
+  ESum4 slice_s[kMaxRows];         // this CTA's slice
   int row_e[kMaxRows];             // row normaliser 2^row_e * row_s
   float row_s[kMaxRows];
   uint64_t full[kMaxSlots];        // staging slots' arrival barriers
 };
 
 // Exchange state of cluster-wide sums and draws (read cluster-wide).
-struct DrawShared {
+struct alignas(16) DrawShared {
   float mass_hi, mass_lo;  // draw: this slice's total weight
   int last;                // draw: its last token of positive weight
-  float zh[2], zl[2];      // cluster sums, by parity of the sum
+  float pad0;              // (the four words above: one 16-byte record)
+  float zs[2][2];          // cluster sums (hi, lo), by parity of the sum
   float red_hi[kAWarps], red_lo[kAWarps];
   int red_i[kAWarps];
   int sel_t;
 };
+static_assert(offsetof(DrawShared, mass_hi) == 0 &&
+                  offsetof(DrawShared, mass_lo) == 4 &&
+                  offsetof(DrawShared, last) == 8 &&
+                  offsetof(DrawShared, zs) % 8 == 0,
+              "the records other CTAs read with vector loads");
 
 // Staging of this CTA's slice [s0, s0 + n) of rows 0 .. R-1: item
 // it = (row it / np, piece it % np), psz floats per piece, goes to slot
@@ -370,7 +390,7 @@ struct SliceStage {
     if (tid < R) {
       ESum s = empty();
       for (int w = 0; w < kAWarps; ++w) s = merge(s, st->warp_s[w][tid]);
-      st->slice_s[tid] = s;
+      st->slice_s[tid] = ESum4{s.e, s.hi, s.lo, 0.f};
     }
   }
 };
@@ -389,10 +409,8 @@ __device__ __forceinline__ void row_normalisers(cg::cluster_group &cluster,
     const uint32_t a0 = smem_u32(&st.slice_s[lane]);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      const uint32_t a = cluster_map(a0, c);
-      o[c].e = ld_cluster_s32(a + offsetof(ESum, e));
-      o[c].hi = ld_cluster_f32(a + offsetof(ESum, hi));
-      o[c].lo = ld_cluster_f32(a + offsetof(ESum, lo));
+      const uint4 v = ld_cluster_v4(cluster_map(a0, c));
+      o[c] = ESum{(int)v.x, __uint_as_float(v.y), __uint_as_float(v.z)};
     }
 #pragma unroll
     for (int c = 0; c < NC; ++c) e = max(e, o[c].e);
@@ -434,21 +452,18 @@ __device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
   if (tid == 0) {
     float h2 = 0.f, l2 = 0.f;
     for (int w = 0; w < kAWarps; ++w) pair_add(h2, l2, ds.red_hi[w], ds.red_lo[w]);
-    ds.zh[parity] = h2;
-    ds.zl[parity] = l2;
+    ds.zs[parity][0] = h2;
+    ds.zs[parity][1] = l2;
   }
   cluster.sync();
   h = 0.f;
   l = 0.f;
-  float zh[NC], zl[NC];
-  const uint32_t ah = smem_u32(&ds.zh[parity]), al = smem_u32(&ds.zl[parity]);
+  float2 z[NC];
+  const uint32_t az = smem_u32(&ds.zs[parity][0]);
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    zh[c] = ld_cluster_f32(cluster_map(ah, c));
-    zl[c] = ld_cluster_f32(cluster_map(al, c));
-  }
+  for (int c = 0; c < NC; ++c) z[c] = ld_cluster_v2f(cluster_map(az, c));
 #pragma unroll
-  for (int c = 0; c < NC; ++c) pair_add(h, l, zh[c], zl[c]);
+  for (int c = 0; c < NC; ++c) pair_add(h, l, z[c].x, z[c].y);
 }
 
 // Inverse-CDF draw over weight(e) of every CTA's slice: the smallest token
@@ -511,13 +526,13 @@ __device__ bool draw_token(cg::cluster_group &cluster, DrawShared &ds,
   float mh_[NC], ml_[NC];
   int lt_[NC];
   {
-    const uint32_t a0 = smem_u32(&ds);
+    const uint32_t a0 = smem_u32(&ds);  // mass_hi, mass_lo, last, pad
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-      const uint32_t a = cluster_map(a0, c);
-      mh_[c] = ld_cluster_f32(a + offsetof(DrawShared, mass_hi));
-      ml_[c] = ld_cluster_f32(a + offsetof(DrawShared, mass_lo));
-      lt_[c] = ld_cluster_s32(a + offsetof(DrawShared, last));
+      const uint4 v = ld_cluster_v4(cluster_map(a0, c));
+      mh_[c] = __uint_as_float(v.x);
+      ml_[c] = __uint_as_float(v.y);
+      lt_[c] = (int)v.z;
     }
   }
 #pragma unroll
@@ -778,9 +793,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
       const uint32_t a0 = smem_u32(&sh.st.slice_s[lane]);
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
-        const uint32_t a = cluster_map(a0, c);
-        oe[c] = ld_cluster_s32(a + offsetof(ESum, e));
-        oh[c] = ld_cluster_f32(a + offsetof(ESum, hi));
+        const uint4 v = ld_cluster_v4(cluster_map(a0, c));
+        oe[c] = (int)v.x;
+        oh[c] = __uint_as_float(v.y);
       }
 #pragma unroll
       for (int c = 0; c < NC; ++c)
