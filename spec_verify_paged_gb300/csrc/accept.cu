@@ -432,9 +432,9 @@ __device__ __forceinline__ void row_normalisers(cg::cluster_group &cluster,
 // between consecutive sums so a slot is rewritten only after a barrier.
 template <int NC, class Weight>
 __device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
-                            const Weight &weight, int e0, int e1, int tid,
-                            int lane, int warp, int parity, float &h,
-                            float &l) {
+                            uint4 *scratch, const Weight &weight, int e0,
+                            int e1, int tid, int lane, int warp, int parity,
+                            float &h, float &l) {
   float hi = 0.f, lo = 0.f;
 #pragma unroll 4
   for (int e = e0; e < e1; ++e) kahan_add(hi, lo, weight(e));
@@ -458,12 +458,15 @@ __device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
   cluster.sync();
   h = 0.f;
   l = 0.f;
-  float2 z[NC];
-  const uint32_t az = smem_u32(&ds.zs[parity][0]);
+  // warp 0 reads the NC pairs (one remote load per lane) for the block
+  if (warp == 0 && lane < NC) {
+    const float2 z = ld_cluster_v2f(cluster_map(smem_u32(&ds.zs[parity][0]), lane));
+    scratch[lane] = make_uint4(__float_as_uint(z.x), __float_as_uint(z.y), 0u, 0u);
+  }
+  __syncthreads();
 #pragma unroll
-  for (int c = 0; c < NC; ++c) z[c] = ld_cluster_v2f(cluster_map(az, c));
-#pragma unroll
-  for (int c = 0; c < NC; ++c) pair_add(h, l, z[c].x, z[c].y);
+  for (int c = 0; c < NC; ++c)
+    pair_add(h, l, __uint_as_float(scratch[c].x), __uint_as_float(scratch[c].y));
 }
 
 // Inverse-CDF draw over weight(e) of every CTA's slice: the smallest token
@@ -473,9 +476,9 @@ __device__ void cluster_sum(cg::cluster_group &cluster, DrawShared &ds,
 // the exit barrier (no further reads of other CTAs' shared memory).
 template <int NC, class Weight>
 __device__ bool draw_token(cg::cluster_group &cluster, DrawShared &ds,
-                           const Weight &weight, int e0, int e1, float u,
-                           int s0, int crank, int tid, int lane, int warp,
-                           int32_t *dst) {
+                           uint4 *scratch, const Weight &weight, int e0,
+                           int e1, float u, int s0, int crank, int tid,
+                           int lane, int warp, int32_t *dst) {
   // visit(e, w) sees this thread's run in token order; false stops it
   auto for_run = [&](auto visit) {
 #pragma unroll 4
@@ -523,22 +526,16 @@ __device__ bool draw_token(cg::cluster_group &cluster, DrawShared &ds,
   // cumulative masses in CTA order: the same operations in every CTA
   float Ph = 0.f, Pl = 0.f, loh = 0.f, lol = 0.f, hih = 0.f, hil = 0.f;
   int last_tok = -1;
-  float mh_[NC], ml_[NC];
-  int lt_[NC];
-  {
-    const uint32_t a0 = smem_u32(&ds);  // mass_hi, mass_lo, last, pad
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const uint4 v = ld_cluster_v4(cluster_map(a0, c));
-      mh_[c] = __uint_as_float(v.x);
-      ml_[c] = __uint_as_float(v.y);
-      lt_[c] = (int)v.z;
-    }
-  }
+  // warp 0 reads the NC records (mass_hi, mass_lo, last: one remote load
+  // per lane) for the block
+  if (warp == 0 && lane < NC)
+    scratch[lane] = ld_cluster_v4(cluster_map(smem_u32(&ds), lane));
+  __syncthreads();
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    const float mh = mh_[c], ml = ml_[c];
-    const int lt = lt_[c];
+    const uint4 v = scratch[c];
+    const float mh = __uint_as_float(v.x), ml = __uint_as_float(v.y);
+    const int lt = (int)v.z;
     if (c == crank) { loh = Ph; lol = Pl; }
     pair_add(Ph, Pl, mh, ml);
     if (c == crank) { hih = Ph; hil = Pl; }
@@ -702,6 +699,10 @@ __global__ void __launch_bounds__(kAThreads, 3)
   // ---- the draw: residual max(0, p_j - q_j), or the bonus from p_K ----
   // thread t owns slice elements [t*per, t*per + per); per odd, so the
   // threads' walks through shared memory fall in different banks
+  // scratch for the records other cluster CTAs expose: the pass-1 partials,
+  // consumed by finish()
+  uint4 *scratch = reinterpret_cast<uint4 *>(&sh.st.warp_s[0][0]);
+  static_assert(sizeof(sh.st.warp_s) >= 16 * sizeof(uint4), "scratch");
   const int per = ((n + kAThreads - 1) / kAThreads) | 1;
   const int e0 = min(n, tid * per), e1 = min(n, e0 + per);
   bool arrived = false;  // this CTA has arrived at the exit barrier
@@ -722,7 +723,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
       return w;
     };
     // a zero residual (impossible in exact arithmetic) falls back to p_j
-    arrived = draw_token<NC>(cluster, sh.ds, weight, e0, e1, uK, s0, crank,
+    arrived = draw_token<NC>(cluster, sh.ds, scratch, weight, e0, e1, uK, s0, crank,
                              tid, lane, warp,
                              p.out_tokens + (size_t)b * (K + 1) + j);
   }
@@ -913,6 +914,10 @@ __global__ void __launch_bounds__(kAThreads, 3)
   }
   __syncthreads();
 
+  // scratch for the records other cluster CTAs expose: the pass-1 partials,
+  // consumed by finish()
+  uint4 *scratch = reinterpret_cast<uint4 *>(&sh.st.warp_s[0][0]);
+  static_assert(sizeof(sh.st.warp_s) >= 16 * sizeof(uint4), "scratch");
   const int per = ((n + kAThreads - 1) / kAThreads) | 1;
   const int e0 = min(n, tid * per), e1 = min(n, e0 + per);
   bool arrived = false;
@@ -954,7 +959,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
         // rejected: the residual's mass Z = sum max(0, r_k - q)
         float zh, zl;
         cluster_sum<NC>(
-            cluster, sh.ds,
+            cluster, sh.ds, scratch,
             [&](int e) {
               float q;
               const float r = rk(e, q);
@@ -980,7 +985,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
     for (int attempt = 0; attempt < 2 && !arrived; ++attempt) {
       if (attempt == 1) k = 0;  // zero mass by rounding: fall back to p
       arrived = draw_token<NC>(
-          cluster, sh.ds,
+          cluster, sh.ds, scratch,
           [&](int e) {
             float q;
             return rk(e, q);
