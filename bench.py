@@ -613,25 +613,40 @@ def run_ours(args):
     # filled once (the synthetic step's inputs do not change), so every
     # replay still moves the full inputs and results across PCIe/C2C.
     step_e2e = None
-    if world == 1 and not tree and not acc_opts:
+    if world == 1:
+        ropts = {}
+        if tree:
+            ropts = dict(tree_nodes=cfg.q_len, vocab=W.TREE_ACCEPT_CONFIG["vocab"])
+        elif acc is not None:
+            ropts = dict(num_draft=cfg.q_len - 1, vocab=W.ACCEPT_CONFIG["vocab"],
+                         temperature=acc_opts.get("temperature", 1.0),
+                         greedy=acc_opts.get("greedy", False),
+                         use_mask="allowed" in acc_opts)
         run = svp.StepRunner(kc, vc, batch=cfg.batch,
                              num_q_heads=cfg.num_q_heads, q_len=cfg.q_len,
                              max_blocks_per_seq=wl.max_blocks_per_seq,
                              n_sink=cfg.n_sink, window=cfg.window, scale=scale,
-                             num_draft=cfg.q_len - 1 if acc is not None else 0,
-                             vocab=W.ACCEPT_CONFIG["vocab"] if acc is not None else 0,
                              split_pages=args.split_pages,
-                             kernel_path=args.kernel_path, **kv_scales)
+                             kernel_path=args.kernel_path, **kv_scales, **ropts)
         names = ["q", "k_new", "v_new", "block_table", "seq_lens"]
         src = [q, kn, vn, bt, sl]
-        if acc is not None:
+        if tree:
+            names += ["tree_mask", "target_logits", "draft_logits", "parents",
+                      "node_tokens", "uniforms"]
+            src += [tm] + list(acc[0])
+        elif acc is not None:
             names += ["target_logits", "draft_logits", "draft_tokens", "uniforms"]
             src += list(acc[0])
+            if "allowed" in acc_opts:
+                names.append("allowed")
+                src.append(acc_opts["allowed"])
         for slot in (0, 1):
             for name, t in zip(names, src):
                 h = run.host(slot, name)
-                h[...] = (t.view(torch.int16).cpu().numpy().view(np.uint16)
-                          if t.dtype == torch.bfloat16 else t.cpu().numpy())
+                a = (t.view(torch.int16).cpu().numpy().view(np.uint16)
+                     if t.dtype == torch.bfloat16 else t.cpu().numpy())
+                h[...] = a.view(h.dtype) if a.dtype.itemsize == h.dtype.itemsize \
+                    and a.dtype.kind != h.dtype.kind else a
         n_run = max(4, min(args.steps, 200))
         for t in range(4):
             if t >= 2:
@@ -649,7 +664,8 @@ def run_ours(args):
         r_ms = (time.perf_counter() - r0) * 1e3 / n_run
         step_bytes_in = sum(run.host(0, n).nbytes for n in names)
         outs = ["out", "lse"] + (["out_tokens", "n_accepted"]
-                                 if acc is not None else [])
+                                 if acc is not None else []) + (
+                                     ["out_nodes"] if tree else [])
         step_bytes_out = sum(run.host(0, n).nbytes for n in outs)
         run.close()
         step_e2e = {"value": round(tokens_per_step_of(cfg) / (r_ms / 1e3), 1),
@@ -684,9 +700,9 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "kernel": kname,
                      "traffic": kernel_traffic(kname, ksrc, cfg.name)},
-        # end to end: through the graph-captured step (svp_step_*) where it
-        # applies, else the plain calls; both copy each step's inputs from
-        # pinned host memory and read its results back
+        # end to end: through the graph-captured step (svp_step_*) on one GPU,
+        # else the plain calls; both copy each step's inputs from pinned
+        # host memory and read its results back
         "e2e": (dict(step_e2e, path="graph-captured step (svp_step)")
                 if step_e2e else plain_e2e),
         **({"e2e_plain_calls": plain_e2e} if step_e2e else {}),

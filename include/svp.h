@@ -353,7 +353,9 @@ int spec_accept_tree(int batch, int num_nodes, int vocab,
  * for the step's inputs and outputs and device copies of them, and one CUDA
  * graph, captured at creation, that copies the slot's inputs to the device
  * and runs kv_append (the q_len new rows), paged_decode_attention and, with
- * num_draft > 0, spec_accept.  svp_step_launch replays a slot's graph on
+ * num_draft > 0, spec_accept (spec_accept_ex with epilogue options) -- or,
+ * for a draft tree (tree_nodes > 0), paged_tree_attention and
+ * spec_accept_tree.  svp_step_launch replays a slot's graph on
  * the runner's compute stream and queues the copy of its outputs back to
  * the slot on a separate copy stream, ordered after an event recorded when
  * that step's outputs are written -- so the next step (the other slot) can
@@ -374,11 +376,23 @@ typedef struct {
   float scale;
   void *k_cache;      /* DEVICE caches, caller-owned */
   void *v_cache;
-  int num_draft;      /* 0: no acceptance step; else q_len - 1 */
+  int num_draft;      /* 0: no acceptance step or a tree; else q_len - 1 */
   int vocab;          /* vocabulary of the acceptance step */
+  /* the verify epilogue of a draft chain (num_draft > 0), as
+     svp_accept_opts: temperature (0 is read as 1), greedy, and with
+     use_mask != 0 the token mask from the slot's SVP_STEP_ALLOWED field */
+  float temperature;
+  int greedy;
+  int use_mask;
+  /* a draft tree instead of a chain: tree_nodes = q_len (<= 16) nodes,
+     num_draft 0, no sinks or window, no epilogue options; the slot then
+     takes SVP_STEP_TREE_MASK, SVP_STEP_PARENTS, SVP_STEP_NODE_TOKENS and
+     N-row logits and uniforms, and returns SVP_STEP_OUT_NODES */
+  int tree_nodes;
 } svp_step_desc;
 
-/* Fields of a slot (pinned host memory; layouts as in the single calls). */
+/* Fields of a slot (pinned host memory; layouts as in the single calls;
+ * N = tree_nodes for a tree, where K+1 and K rows read N). */
 typedef enum {
   SVP_STEP_Q = 0,          /* in:  [batch, q_len, Hq, D] dtype          */
   SVP_STEP_K_NEW,          /* in:  [batch, q_len, Hkv, D] dtype         */
@@ -387,12 +401,18 @@ typedef enum {
   SVP_STEP_SEQ_LENS,       /* in:  [batch] int32 (after the append)     */
   SVP_STEP_TARGET_LOGITS,  /* in:  [batch, K+1, vocab] fp32             */
   SVP_STEP_DRAFT_LOGITS,   /* in:  [batch, K, vocab] fp32               */
-  SVP_STEP_DRAFT_TOKENS,   /* in:  [batch, K] int32                     */
+  SVP_STEP_DRAFT_TOKENS,   /* in:  [batch, K] int32 (chain)             */
   SVP_STEP_UNIFORMS,       /* in:  [batch, K+1] fp32                    */
   SVP_STEP_OUT,            /* out: [batch, q_len, Hq, D] dtype          */
   SVP_STEP_LSE,            /* out: [batch, q_len, Hq] fp32              */
   SVP_STEP_OUT_TOKENS,     /* out: [batch, K+1] int32                   */
   SVP_STEP_N_ACCEPTED,     /* out: [batch] int32                        */
+  SVP_STEP_ALLOWED,        /* in:  [batch, K+1, ceil(vocab/32)] uint32
+                                   (chain with use_mask)                 */
+  SVP_STEP_TREE_MASK,      /* in:  [batch, N] uint32 (tree)             */
+  SVP_STEP_PARENTS,        /* in:  [batch, N] int32 (tree)              */
+  SVP_STEP_NODE_TOKENS,    /* in:  [batch, N] int32 (tree)              */
+  SVP_STEP_OUT_NODES,      /* out: [batch, N] int32 (tree)              */
   SVP_STEP_NUM_FIELDS
 } svp_step_field;
 
@@ -400,8 +420,11 @@ typedef struct svp_step svp_step;
 
 /* Allocates the runner (streams, workspace, both slots) and captures the
  * two slot graphs.  Errors: SVP_ERR_INVALID_ARG for null pointers, sizes
- * < 1 or num_draft not in {0, q_len - 1}; the errors of the single calls
- * for their arguments; SVP_ERR_CUDA if an allocation or the capture fails. */
+ * < 1, num_draft not in {0, q_len - 1}, epilogue options without drafts,
+ * or a tree with tree_nodes != q_len, drafts, sinks, a window or epilogue
+ * options; SVP_ERR_UNSUPPORTED for more than 16 tree nodes; the errors of
+ * the single calls for their arguments; SVP_ERR_CUDA if an allocation or
+ * the capture fails. */
 int svp_step_create(const svp_step_desc *desc, svp_step **runner);
 /* Pinned host memory of one field of slot 0 or 1 and its size in bytes
  * (*bytes may be NULL); NULL for a bad slot/field or an empty field. */

@@ -59,12 +59,15 @@ class SvpStepDesc(ctypes.Structure):
                 ("n_sink", ctypes.c_int), ("window", ctypes.c_int),
                 ("scale", ctypes.c_float), ("k_cache", ctypes.c_void_p),
                 ("v_cache", ctypes.c_void_p), ("num_draft", ctypes.c_int),
-                ("vocab", ctypes.c_int)]
+                ("vocab", ctypes.c_int), ("temperature", ctypes.c_float),
+                ("greedy", ctypes.c_int), ("use_mask", ctypes.c_int),
+                ("tree_nodes", ctypes.c_int)]
 
 
 STEP_FIELDS = ("q", "k_new", "v_new", "block_table", "seq_lens",
                "target_logits", "draft_logits", "draft_tokens", "uniforms",
-               "out", "lse", "out_tokens", "n_accepted")
+               "out", "lse", "out_tokens", "n_accepted", "allowed",
+               "tree_mask", "parents", "node_tokens", "out_nodes")
 
 
 class SvpError(RuntimeError):
@@ -425,14 +428,18 @@ def last_launch_count() -> int:
 class StepRunner:
     """The graph-captured decode step (include/svp.h: svp_step_*): two
     ping-pong slots of pinned host buffers, each replayed as one CUDA graph
-    (input copy, kv_append, attention, spec_accept) with its result copied
+    (input copy, kv_append, attention, acceptance) with its result copied
     back on a separate stream.  host(slot, name) returns a numpy view of a
-    slot's pinned buffer (bf16 as uint16 bits)."""
+    slot's pinned buffer (bf16 as uint16 bits).  Draft chains take the
+    verify epilogue options (temperature, greedy, use_mask: the token mask
+    in field "allowed"); tree_nodes > 0 makes the step a draft-tree verify
+    (fields "tree_mask", "parents", "node_tokens"; result "out_nodes")."""
 
     def __init__(self, k_cache, v_cache, batch, num_q_heads, q_len,
                  max_blocks_per_seq, n_sink=0, window=0, scale=None,
                  num_draft=0, vocab=0, split_pages=0, kernel_path=PATH_AUTO,
-                 k_scale=1.0, v_scale=1.0):
+                 k_scale=1.0, v_scale=1.0, temperature=1.0, greedy=False,
+                 use_mask=False, tree_nodes=0):
         lib = load_library()
         _cuda_contig(k_cache, "k_cache")
         _cuda_contig(v_cache, "v_cache")
@@ -446,27 +453,35 @@ class StepRunner:
             scale = 1.0 / math.sqrt(D)
         desc = SvpStepDesc(dims, q_len, n_sink, window, float(scale),
                            k_cache.data_ptr(), v_cache.data_ptr(), num_draft,
-                           vocab)
+                           vocab, float(temperature), int(bool(greedy)),
+                           int(bool(use_mask)), int(tree_nodes))
         h = ctypes.c_void_p()
         _check("svp_step_create", lib.svp_step_create(ctypes.byref(desc),
                                                       ctypes.byref(h)))
         self._lib, self._h = lib, h
         self._keep = (k_cache, v_cache)
         ed = np.float32 if code == SVP_F32 else np.uint16
-        B, Q, K, V = batch, q_len, num_draft, vocab
+        B, Q, K, V, N = batch, q_len, num_draft, vocab, tree_nodes
+        rt = N if N else K + 1   # target rows, uniforms, output tokens
+        rd = N if N else K       # draft rows
         self._spec = {
             "q": (ed, (B, Q, num_q_heads, D)), "k_new": (ed, (B, Q, Hkv, D)),
             "v_new": (ed, (B, Q, Hkv, D)),
             "block_table": (np.int32, (B, max_blocks_per_seq)),
             "seq_lens": (np.int32, (B,)),
-            "target_logits": (np.float32, (B, K + 1, V)),
-            "draft_logits": (np.float32, (B, K, V)),
+            "target_logits": (np.float32, (B, rt, V)),
+            "draft_logits": (np.float32, (B, rd, V)),
             "draft_tokens": (np.int32, (B, K)),
-            "uniforms": (np.float32, (B, K + 1)),
+            "uniforms": (np.float32, (B, rt)),
             "out": (ed, (B, Q, num_q_heads, D)),
             "lse": (np.float32, (B, Q, num_q_heads)),
-            "out_tokens": (np.int32, (B, K + 1)),
+            "out_tokens": (np.int32, (B, rt)),
             "n_accepted": (np.int32, (B,)),
+            "allowed": (np.uint32, (B, K + 1, (V + 31) // 32)),
+            "tree_mask": (np.uint32, (B, N)),
+            "parents": (np.int32, (B, N)),
+            "node_tokens": (np.int32, (B, N)),
+            "out_nodes": (np.int32, (B, N)),
         }
         self._views = {}
 

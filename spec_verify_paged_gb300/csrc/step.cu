@@ -45,7 +45,10 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-bool is_input(int f) { return f < SVP_STEP_OUT; }
+bool is_input(int f) {
+  return f < SVP_STEP_OUT ||
+         (f >= SVP_STEP_ALLOWED && f <= SVP_STEP_NODE_TOKENS);
+}
 
 void release(svp_step *s) {
   for (auto &sl : s->slot) {
@@ -64,8 +67,8 @@ void release(svp_step *s) {
 }
 
 // Captures slot i's step on the compute stream: the input copy from the
-// pinned slot, then kv_append, attention and (with drafts) spec_accept on
-// the slot's device buffers.
+// pinned slot, then kv_append, attention and (with drafts or a tree) the
+// acceptance step on the slot's device buffers.
 int capture_slot(svp_step *s, int i) {
   svp_step::Slot &sl = s->slot[i];
   const svp_step_desc &d = s->desc;
@@ -86,20 +89,43 @@ int capture_slot(svp_step *s, int i) {
     st = kv_append(&dims, in(SVP_STEP_K_NEW), in(SVP_STEP_V_NEW), d.k_cache,
                    d.v_cache, (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
                    (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, s->compute);
-  if (st == SVP_OK)
+  const bool tree = d.tree_nodes > 0;
+  if (st == SVP_OK && tree)
+    st = paged_tree_attention(
+        &dims, in(SVP_STEP_Q), d.k_cache, d.v_cache,
+        (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
+        (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len,
+        (const uint32_t *)in(SVP_STEP_TREE_MASK), d.scale, out(SVP_STEP_OUT),
+        (float *)out(SVP_STEP_LSE), s->compute);
+  else if (st == SVP_OK)
     st = paged_decode_attention(
         &dims, in(SVP_STEP_Q), d.k_cache, d.v_cache,
         (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
         (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, d.n_sink, d.window,
         d.scale, out(SVP_STEP_OUT), (float *)out(SVP_STEP_LSE), s->compute);
-  if (st == SVP_OK && d.num_draft > 0)
-    st = spec_accept(d.dims.batch, d.num_draft, d.vocab,
-                     (const float *)in(SVP_STEP_TARGET_LOGITS),
-                     (const float *)in(SVP_STEP_DRAFT_LOGITS),
-                     (const int32_t *)in(SVP_STEP_DRAFT_TOKENS),
-                     (const float *)in(SVP_STEP_UNIFORMS),
-                     (int32_t *)out(SVP_STEP_OUT_TOKENS),
-                     (int32_t *)out(SVP_STEP_N_ACCEPTED), s->compute);
+  if (st == SVP_OK && tree) {
+    st = spec_accept_tree(d.dims.batch, d.tree_nodes, d.vocab,
+                          (const float *)in(SVP_STEP_TARGET_LOGITS),
+                          (const float *)in(SVP_STEP_DRAFT_LOGITS),
+                          (const int32_t *)in(SVP_STEP_PARENTS),
+                          (const int32_t *)in(SVP_STEP_NODE_TOKENS),
+                          (const float *)in(SVP_STEP_UNIFORMS),
+                          (int32_t *)out(SVP_STEP_OUT_TOKENS),
+                          (int32_t *)out(SVP_STEP_OUT_NODES),
+                          (int32_t *)out(SVP_STEP_N_ACCEPTED), s->compute);
+  } else if (st == SVP_OK && d.num_draft > 0) {
+    svp_accept_opts o;
+    o.temperature = d.temperature > 0.f ? d.temperature : 1.f;
+    o.allowed = d.use_mask ? (const uint32_t *)in(SVP_STEP_ALLOWED) : nullptr;
+    o.greedy = d.greedy;
+    st = spec_accept_ex(d.dims.batch, d.num_draft, d.vocab,
+                        (const float *)in(SVP_STEP_TARGET_LOGITS),
+                        (const float *)in(SVP_STEP_DRAFT_LOGITS),
+                        (const int32_t *)in(SVP_STEP_DRAFT_TOKENS),
+                        (const float *)in(SVP_STEP_UNIFORMS), &o,
+                        (int32_t *)out(SVP_STEP_OUT_TOKENS),
+                        (int32_t *)out(SVP_STEP_N_ACCEPTED), s->compute);
+  }
   const cudaError_t e = cudaStreamEndCapture(s->compute, &graph);
   if (st != SVP_OK) {
     if (graph) cudaGraphDestroy(graph);
@@ -127,6 +153,16 @@ int svp_step_create(const svp_step_desc *desc, svp_step **out) {
   if (desc->num_draft > 0 && (desc->num_draft != desc->q_len - 1 ||
                               desc->vocab < 2))
     return SVP_ERR_INVALID_ARG;
+  const bool opts = desc->greedy || desc->use_mask ||
+                    (desc->temperature > 0.f && desc->temperature != 1.f);
+  if (desc->temperature < 0.f || (opts && desc->num_draft == 0))
+    return SVP_ERR_INVALID_ARG;
+  if (desc->tree_nodes < 0 ||
+      (desc->tree_nodes > 0 &&
+       (desc->tree_nodes != desc->q_len || desc->num_draft != 0 || opts ||
+        desc->n_sink != 0 || desc->window != 0 || desc->vocab < 2)))
+    return SVP_ERR_INVALID_ARG;
+  if (desc->tree_nodes > svp::kMaxNodes) return SVP_ERR_UNSUPPORTED;
   const size_t ws = paged_decode_workspace_size(&dm, desc->q_len,
                                                 desc->n_sink, desc->window);
   if (ws == 0) return SVP_ERR_INVALID_ARG;
@@ -138,19 +174,28 @@ int svp_step_create(const svp_step_desc *desc, svp_step **out) {
   const size_t B = (size_t)dm.batch, Q = (size_t)desc->q_len;
   const size_t eb = dm.dtype == SVP_F32 ? 4 : 2;
   const size_t K = (size_t)desc->num_draft, V = (size_t)desc->vocab;
+  const size_t N = (size_t)desc->tree_nodes;
+  const size_t rows_t = N ? N : (K ? K + 1 : 0);  // target rows, uniforms
+  const size_t rows_d = N ? N : K;                // draft rows
   s->bytes[SVP_STEP_Q] = B * Q * dm.num_q_heads * dm.head_dim * eb;
   s->bytes[SVP_STEP_K_NEW] = B * Q * dm.num_kv_heads * dm.head_dim * eb;
   s->bytes[SVP_STEP_V_NEW] = s->bytes[SVP_STEP_K_NEW];
   s->bytes[SVP_STEP_BLOCK_TABLE] = B * dm.max_blocks_per_seq * 4;
   s->bytes[SVP_STEP_SEQ_LENS] = B * 4;
-  s->bytes[SVP_STEP_TARGET_LOGITS] = K ? B * (K + 1) * V * 4 : 0;
-  s->bytes[SVP_STEP_DRAFT_LOGITS] = B * K * V * 4;
+  s->bytes[SVP_STEP_TARGET_LOGITS] = B * rows_t * V * 4;
+  s->bytes[SVP_STEP_DRAFT_LOGITS] = B * rows_d * V * 4;
   s->bytes[SVP_STEP_DRAFT_TOKENS] = B * K * 4;
-  s->bytes[SVP_STEP_UNIFORMS] = K ? B * (K + 1) * 4 : 0;
+  s->bytes[SVP_STEP_UNIFORMS] = B * rows_t * 4;
   s->bytes[SVP_STEP_OUT] = s->bytes[SVP_STEP_Q];
   s->bytes[SVP_STEP_LSE] = B * Q * dm.num_q_heads * 4;
-  s->bytes[SVP_STEP_OUT_TOKENS] = K ? B * (K + 1) * 4 : 0;
-  s->bytes[SVP_STEP_N_ACCEPTED] = K ? B * 4 : 0;
+  s->bytes[SVP_STEP_OUT_TOKENS] = B * rows_t * 4;
+  s->bytes[SVP_STEP_N_ACCEPTED] = rows_t ? B * 4 : 0;
+  s->bytes[SVP_STEP_ALLOWED] =
+      desc->use_mask ? B * (K + 1) * ((V + 31) / 32) * 4 : 0;
+  s->bytes[SVP_STEP_TREE_MASK] = B * N * 4;
+  s->bytes[SVP_STEP_PARENTS] = B * N * 4;
+  s->bytes[SVP_STEP_NODE_TOKENS] = B * N * 4;
+  s->bytes[SVP_STEP_OUT_NODES] = B * N * 4;
   for (int f = 0; f < SVP_STEP_NUM_FIELDS; ++f) {
     size_t &total = is_input(f) ? s->in_bytes : s->out_bytes;
     s->off[f] = total;

@@ -95,3 +95,131 @@ def test_step_runner_matches_plain_calls(svp, q_len, num_draft):
     assert torch.equal(vc1.view(torch.int16), vc2.view(torch.int16))
     run.close()
     assert svp.read_device_status() == 0
+
+
+def _run_steps(run, inputs, fields_out):
+    """Feeds `inputs` through the two slots (one step ahead) and returns each
+    step's outputs."""
+    got = []
+
+    def collect(slot):
+        run.wait(slot)
+        got.append({k: run.host(slot, k).copy() for k in fields_out})
+
+    steps = len(inputs)
+    for t in range(steps):
+        slot = t % 2
+        if t >= 2:
+            collect(slot)
+        for name, arr in inputs[t].items():
+            run.host(slot, name)[...] = arr
+        run.launch(slot)
+    for t in range(max(0, steps - 2), steps):
+        collect(t % 2)
+    return got
+
+
+def test_step_runner_tree_matches_plain_calls(svp):
+    """A draft-tree step (tree attention + tree acceptance) through the
+    runner equals the same steps made with plain calls."""
+    import torch
+    N = 7
+    par = W.binary_tree_parents(2)
+    cfg = W.small_config(batch=3, num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, q_len=N, dtype="bf16", ctx_min=N + 30,
+                         ctx_max=400, seed=131)
+    wl = W.make_attention(cfg, n_new=N)
+    V = 1500
+    rng = np.random.default_rng(8)
+    inputs = []
+    for t in range(4):
+        a = W.make_tree_accept(batch=3, vocab=V, seed=400 + t, parents=par)
+        inputs.append({
+            "q": W._normals(rng, wl.q.shape, "bf16"),
+            "k_new": W._normals(rng, wl.k_new.shape, "bf16"),
+            "v_new": W._normals(rng, wl.v_new.shape, "bf16"),
+            "block_table": wl.block_table, "seq_lens": wl.seq_lens,
+            "tree_mask": W.tree_mask_from_parents(a.parents),
+            "target_logits": a.target_logits, "draft_logits": a.draft_logits,
+            "parents": a.parents, "node_tokens": a.node_tokens,
+            "uniforms": a.uniforms})
+    kc1, vc1 = to_dev(wl.k_cache), to_dev(wl.v_cache)
+    kc2, vc2 = to_dev(wl.k_cache), to_dev(wl.v_cache)
+    run = svp.StepRunner(kc1, vc1, batch=3, num_q_heads=16, q_len=N,
+                         max_blocks_per_seq=wl.max_blocks_per_seq,
+                         scale=float(wl.scale), vocab=V, tree_nodes=N)
+    outs = ("out", "lse", "out_tokens", "out_nodes", "n_accepted")
+    got = _run_steps(run, inputs, outs)
+    for t, d in enumerate(inputs):
+        bt, sl = to_dev(d["block_table"]), to_dev(d["seq_lens"])
+        svp.kv_append(to_dev(d["k_new"]), to_dev(d["v_new"]), kc2, vc2, bt, sl)
+        out, lse = svp.paged_tree_attention(
+            to_dev(d["q"]), kc2, vc2, bt, sl,
+            to_dev(d["tree_mask"].view(np.int32)), scale=float(wl.scale))
+        toks, nodes, nacc = svp.spec_accept_tree(
+            to_dev(d["target_logits"]), to_dev(d["draft_logits"]),
+            to_dev(d["parents"]), to_dev(d["node_tokens"]),
+            to_dev(d["uniforms"]))
+        ref = {"out": out.view(torch.int16).cpu().numpy().view(np.uint16),
+               "lse": lse.cpu().numpy(), "out_tokens": toks.cpu().numpy(),
+               "out_nodes": nodes.cpu().numpy(), "n_accepted": nacc.cpu().numpy()}
+        for k in outs:
+            assert np.array_equal(got[t][k], ref[k]), (t, k)
+    torch.cuda.synchronize()
+    assert torch.equal(kc1.view(torch.int16), kc2.view(torch.int16))
+    run.close()
+    assert svp.read_device_status() == 0
+
+
+@pytest.mark.parametrize("opts", [dict(temperature=0.7, use_mask=True),
+                                  dict(greedy=True), dict(temperature=1.6)])
+def test_step_runner_epilogue_matches_plain_calls(svp, opts):
+    """The verify epilogue (temperature, token mask, greedy) through the
+    runner equals spec_accept with the same options."""
+    import torch
+    K, V = 4, 3000
+    cfg = W.small_config(batch=4, num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, q_len=K + 1, dtype="bf16", ctx_min=40,
+                         ctx_max=300, seed=141)
+    wl = W.make_attention(cfg, n_new=K + 1)
+    rng = np.random.default_rng(9)
+    words = (V + 31) // 32
+    inputs = []
+    for t in range(4):
+        a = W.make_accept(batch=4, num_draft=K, vocab=V, seed=500 + t)
+        d = {"q": W._normals(rng, wl.q.shape, "bf16"),
+             "k_new": W._normals(rng, wl.k_new.shape, "bf16"),
+             "v_new": W._normals(rng, wl.v_new.shape, "bf16"),
+             "block_table": wl.block_table, "seq_lens": wl.seq_lens,
+             "target_logits": a.target_logits, "draft_logits": a.draft_logits,
+             "draft_tokens": a.draft_tokens, "uniforms": a.uniforms}
+        if opts.get("use_mask"):
+            d["allowed"] = rng.integers(0, 2**32, size=(4, K + 1, words),
+                                        dtype=np.uint64).astype(np.uint32)
+            d["allowed"][..., 0] |= 1   # token 0 always allowed
+        inputs.append(d)
+    kc1, vc1 = to_dev(wl.k_cache), to_dev(wl.v_cache)
+    kc2, vc2 = to_dev(wl.k_cache), to_dev(wl.v_cache)
+    run = svp.StepRunner(kc1, vc1, batch=4, num_q_heads=16, q_len=K + 1,
+                         max_blocks_per_seq=wl.max_blocks_per_seq,
+                         scale=float(wl.scale), num_draft=K, vocab=V, **opts)
+    outs = ("out", "out_tokens", "n_accepted")
+    got = _run_steps(run, inputs, outs)
+    for t, d in enumerate(inputs):
+        bt, sl = to_dev(d["block_table"]), to_dev(d["seq_lens"])
+        svp.kv_append(to_dev(d["k_new"]), to_dev(d["v_new"]), kc2, vc2, bt, sl)
+        out, _ = svp.paged_decode_attention(to_dev(d["q"]), kc2, vc2, bt, sl,
+                                            q_len=K + 1, scale=float(wl.scale))
+        allowed = (to_dev(d["allowed"].view(np.int32))
+                   if "allowed" in d else None)
+        toks, nacc = svp.spec_accept(
+            to_dev(d["target_logits"]), to_dev(d["draft_logits"]),
+            to_dev(d["draft_tokens"]), to_dev(d["uniforms"]),
+            temperature=opts.get("temperature", 1.0), allowed=allowed,
+            greedy=opts.get("greedy", False))
+        ref = {"out": out.view(torch.int16).cpu().numpy().view(np.uint16),
+               "out_tokens": toks.cpu().numpy(), "n_accepted": nacc.cpu().numpy()}
+        for k in outs:
+            assert np.array_equal(got[t][k], ref[k]), (t, k)
+    run.close()
+    assert svp.read_device_status() == 0
