@@ -275,38 +275,6 @@ __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Column reduction over the 32 keys (lanes) of a warp: each lane holds N
-// columns; a transposing butterfly halves the columns each step, so lane l
-// ends with column col_of(l) of the warp's max (or sum) after N-1 shuffles.
-template <int N>
-__device__ __forceinline__ int col_of(int lane) {
-  return N == 32 ? lane : lane >> 1;
-}
-
-template <int N, bool MAX>
-__device__ __forceinline__ float col_reduce(const float (&x)[N], int lane) {
-  static_assert(N == 16 || N == 32, "16 or 32 columns");
-  float v[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = x[i];
-#pragma unroll
-  for (int h = N / 2, off = 16; h >= 1; h >>= 1, off >>= 1) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-      const float send = upper ? v[i] : v[i + h];
-      const float keep = upper ? v[i + h] : v[i];
-      const float got = __shfl_xor_sync(kFull, send, off);
-      v[i] = MAX ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  if (N == 16) {  // lanes l and l ^ 1 hold halves of the same column
-    const float got = __shfl_xor_sync(kFull, v[0], 1);
-    v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
-  }
-  return v[0];
-}
-
 // Byte offset of element (row n, column k) of an [N rows x 128 columns]
 // bf16 operand in the K-major 128-byte-swizzled layout: two 64-column
 // halves, each [N][128 B], 16-byte chunks XOR-ed with the row mod 8.
