@@ -193,6 +193,31 @@ def test_step_runner_rejects_bad_descriptions(lib):
     assert lib.svp_step_host_buffer(None, 0, 0, None) is None
 
 
+@pytest.mark.parametrize("q_len,n_sink,window,num_draft,temp,greedy,mask,tree,expect", [
+    (1, 0, 0, 0, 1.0, 1, 0, 0, -1),     # greedy without drafts
+    (1, 0, 0, 0, 0.7, 0, 0, 0, -1),     # a temperature without drafts
+    (5, 0, 0, 4, -0.5, 0, 0, 0, -1),    # negative temperature
+    (7, 0, 0, 6, 1.0, 0, 0, 7, -1),     # a tree with chain drafts
+    (7, 0, 0, 0, 1.0, 0, 0, 5, -1),     # tree_nodes != q_len
+    (7, 0, 16, 0, 1.0, 0, 0, 7, -1),    # a tree under a window
+    (7, 4, 0, 0, 1.0, 0, 0, 7, -1),     # a tree with sinks
+    (7, 0, 0, 0, 1.0, 1, 0, 7, -1),     # a tree with epilogue options
+    (7, 0, 0, 0, 1.0, 0, 1, 7, -1),
+    (17, 0, 0, 0, 1.0, 0, 0, 17, -2),   # more nodes than the kernels take
+])
+def test_step_runner_checks_epilogue_and_tree_options(lib, q_len, n_sink, window,
+                                                      num_draft, temp, greedy,
+                                                      mask, tree, expect):
+    """Epilogue options need draft chains; a draft tree needs tree_nodes =
+    q_len, no chain drafts, sinks, window or options; all checked before
+    anything touches the GPU."""
+    from spec_verify_paged_gb300.binding import SvpStepDesc
+    h = ctypes.c_void_p()
+    d = SvpStepDesc(_dims(), q_len, n_sink, window, 0.1, P, P, num_draft, 100,
+                    temp, greedy, mask, tree)
+    assert lib.svp_step_create(ctypes.byref(d), ctypes.byref(h)) == expect
+
+
 def test_accept_null_pointer(lib):
     assert lib.spec_accept(2, 4, 100, P, None, P, P, P, P, None) == -1
     assert lib.spec_accept(0, 4, 100, None, None, None, None, None, None,
