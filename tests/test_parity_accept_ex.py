@@ -121,3 +121,15 @@ def test_greedy(svp, oracle_mod, masked, V):
                             greedy_hits=0.8)
     nacc = _check(svp, oracle_mod, wl, allowed, greedy=True)
     assert len(np.unique(nacc)) >= 3
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_token_mask_with_a_staging_ring(svp, oracle_mod, greedy):
+    """15 drafts over vocab 32,000: 31 rows (16 for greedy) of 2,000-token
+    slices do not fit the 72 KB staging area, so pass 1 streams them through
+    a ring of slots refilled piece by piece while the mask rewrites staged
+    values; tokens and counts match the oracle."""
+    wl, allowed = _workload(8, 15, 32000, 96 + int(greedy), T=0.9, density=0.6,
+                            greedy_hits=0.9 if greedy else 0.0)
+    _check(svp, oracle_mod, wl, allowed, T=0.9 if not greedy else 1.0,
+           greedy=greedy)
