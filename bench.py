@@ -38,6 +38,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -86,19 +87,31 @@ def attention_kernel(cfg, kernel_path):
     return "paged_attention_kernel", "attention.cu"
 
 
+def code_hash(path):
+    """sha256 prefix of a source's code: `//` comments and blank lines
+    removed, so an edit of comments alone leaves it unchanged."""
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def kernel_traffic(kernel, src, workload):
     """dram bytes per launch from the committed ncu summary of this kernel
-    on this workload, if it was taken on the current source; else None."""
+    on this workload, if it was taken on the current code; else None."""
     prof = os.path.join(ROOT, "profiles", f"ncu_{kernel}_{workload}.md")
     if not os.path.exists(prof):
         return None
-    sha = hashlib.sha256(open(os.path.join(CSRC, src), "rb").read()).hexdigest()[:16]
+    sha = code_hash(os.path.join(CSRC, src))
     vals = {}
     for line in open(prof):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get(f"{src} sha256 prefix") != sha:
+            quoted = re.findall(r"`([^`]*)`", v)
+            vals[k.strip()] = quoted[0] if quoted else v.strip()
+    if vals.get(f"{src} code sha256 prefix") != sha:
         return None
     try:
         return int(vals["dram bytes per launch"])

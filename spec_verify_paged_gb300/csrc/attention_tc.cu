@@ -17,23 +17,27 @@
 //   O_t^T [128 d x N]   = V_tile^T [128 d x 128 keys] . P^T  A = V, MN-major
 // so a 20-row verify group costs a 32-column MMA instead of a 128-row one,
 // and both K and V feed the tensor core straight from the TMA-written
-// 128-byte-swizzled tiles.  Accumulators live in tensor memory (TMEM):
-// two S buffers and two O buffers of N columns, double-buffered by tile.
+// 128-byte-swizzled tiles.  Accumulators live in tensor memory (TMEM).
+// A unit is N = 16 or 32 rows of a kv head; beyond 32 rows it is 64 rows
+// in two 32-row groups (DUAL), so each K/V tile is read once for all 64.
 //
 // Warp roles (320 threads, one CTA per SM):
-//   warps 0-7  softmax and epilogue, as two groups of four warps that take
-//              alternate tiles (group = tile parity), so one group's
-//              shuffles, exponentials and barriers overlap the other's.
-//              Thread k of a group reads TMEM lane k: key k of the tile for
-//              S, head dim k for O.  Column statistics (row max and sum
-//              over the tile's keys) use a transposing warp butterfly and a
+//   warps 0-7  softmax and epilogue, as two groups of four warps.  One row
+//              group per unit: the groups take alternate tiles (group =
+//              tile parity), so one group's shuffles, exponentials and
+//              barriers overlap the other's; their states merge by
+//              log-sum-exp at the end of a segment.  DUAL: both groups take
+//              every tile, one 32-row group each, with S double-buffered.
+//              S is read in the mma-fragment layout (a thread holds four
+//              keys of eight rows): row max and sum fold over the four keys
+//              in registers, then a short transposing butterfly and a
 //              four-warp exchange in shared memory; P goes back to shared
-//              memory as bf16 in the MMA's swizzled layout.  Each group
-//              folds its tiles' O into registers (o = o * alpha + O_t) and
-//              keeps its own running max and sum; the two states are merged
-//              by log-sum-exp at the end of a segment.
+//              memory as bf16 in the MMA's swizzled layout through
+//              transposing stmatrix stores.  Interior tiles (every key real
+//              and seen by every row) skip per-key masking.  Each group
+//              folds its tiles' O into registers (o = o * alpha + O_t).
 //   warp 8     producer: block table, 2-D TMA copies of 8 pages' K and V
-//              into a 3-stage ring.
+//              into a 3-stage ring (2 stages for DUAL units).
 //   warp 9     one thread issues tcgen05.mma / tcgen05.commit, event
 //              driven: S of a tile as soon as its data and S buffer are
 //              free, P V as soon as its P is written, so stages go back to
@@ -811,7 +815,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // its own and writes the segment out.
     const int gi = warp >> 2;          // group: tiles of this parity
     const int gw = warp & 3;           // warp in the group = TMEM lane quadrant
-    const int gt = tid & 127;          // key of the tile (S), head dim (O)
+    const int gt = tid & 127;          // head dim of O; row of the stats
     const int gbar = 1 + gi;
     const float qmul = p.qscale > 0.f ? p.qscale : 1.f;
     const uint32_t lane_base = (uint32_t)(gw * 32) << 16;
@@ -860,7 +864,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float o[N];
 #pragma unroll
       for (int n = 0; n < N; ++n) o[n] = 0.f;
-      // running statistics of column gt (thread gt < N of the group)
+      // running statistics of row gt (thread gt < N of the group)
       float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
       int prev = -1;  // this group's previous tile in the segment
       const int tiles = (ui.n_pages + kTilePages - 1) / kTilePages;
@@ -1045,7 +1049,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---- the group's last tile (a warp whose last fold failed skips it;
       // the vote below makes the outcome the group's) ----
       if (ok && prev >= 0) ok = fold_o(prev, o);
-      // (also makes the last tile's column sums visible)
+      // (also makes the last tile's row sums visible)
       ok = bar_and(gbar, kGroupThreads, ok);
       if (!ok) break;
       if (gt < N && prev >= 0)
