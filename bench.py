@@ -292,6 +292,7 @@ def cpu_baseline(wl, budget_s=10.0, max_passes=20):
         total_tok += tok
         n += 1
     return {"value": total_tok / total_t, "unit": UNIT, "cores": 1,
+            "host_cpus": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{n} sequence passes over the {wl.cfg.batch} sequences "
                       f"of {wl.cfg.name} (all {wl.cfg.num_q_heads} heads, "
@@ -762,6 +763,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": conf,
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
+                         "host_cpus": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT,
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
