@@ -466,6 +466,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int MT = MMA ? RB / 16 : 1;
   constexpr int RW = MMA ? 16 : RB;
   constexpr int NSTREAM = kConsumerWarps / MT;
+  // A stage's previous page (c - STAGES) must belong to the same stream as
+  // page c: that stream has then waited for it, so its wait for page c is
+  // at most one phase ahead of the stage's full barrier.  Otherwise the
+  // parity wait can pass two phases early, on a copy still in flight.
+  static_assert(STAGES % NSTREAM == 0, "ring depth: a multiple of the streams");
   Smem<T, D, RB, RW> &sm = *reinterpret_cast<Smem<T, D, RB, RW> *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
