@@ -84,3 +84,32 @@ def test_warmup_floor():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_code_hash_ignores_comments_and_traffic_lookup(tmp_path, monkeypatch):
+    """A comment-only edit keeps a source's code hash (so a committed ncu
+    summary stays valid); a code edit changes it (so the traffic figure is
+    dropped)."""
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("int f() {  // one\n  return 1;\n}\n")
+    h0 = bench.code_hash(str(src))
+    src.write_text("// a new header comment\nint f() {  // two\n\n  return 1;\n}\n")
+    assert bench.code_hash(str(src)) == h0
+    src.write_text("int f() {\n  return 2;\n}\n")
+    assert bench.code_hash(str(src)) != h0
+    # a summary line with the file hash appended still parses
+    root = tmp_path / "root"
+    (root / "profiles").mkdir(parents=True)
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (csrc / "k.cu").write_text("int f() {\n  return 2;\n}\n")
+    h = bench.code_hash(str(csrc / "k.cu"))
+    (root / "profiles" / "ncu_kern_wl.md").write_text(
+        f"- k.cu code sha256 prefix: `{h}` (file `0123`)\n"
+        "- dram bytes per launch: `12345`\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    monkeypatch.setattr(bench, "CSRC", str(csrc))
+    assert bench.kernel_traffic("kern", "k.cu", "wl") == 12345
+    (csrc / "k.cu").write_text("int f() {\n  return 3;\n}\n")
+    assert bench.kernel_traffic("kern", "k.cu", "wl") is None
