@@ -78,6 +78,13 @@ def _load():
                 [i32] * 3 + [vp] * 4 + [ctypes.c_double, vp, i32, vp, vp, vp,
                                         ctypes.c_double])
             lib.oracle_spec_accept_ex.restype = i32
+            lib.oracle_spec_accept_valid.argtypes = (
+                [i32] * 3 + [vp] * 4 + [ctypes.c_double] + [vp] * 4 +
+                [i32, ctypes.c_double])
+            lib.oracle_spec_accept_valid.restype = i32
+            lib.oracle_spec_accept_tree_valid.argtypes = (
+                [i32] * 3 + [vp] * 7 + [i32, i32, ctypes.c_double])
+            lib.oracle_spec_accept_tree_valid.restype = i32
             lib.oracle_paged_attention_fp8.argtypes = (
                 [i32] * 7 + [vp] * 3 + [ctypes.c_double] * 2 + [vp] * 2 +
                 [i32, i32, i32, f32, vp, i64, vp, vp])
@@ -315,6 +322,86 @@ def spec_accept_ex(target_logits, draft_logits, draft_tokens, uniforms,
     if st != 0:
         raise ValueError(f"oracle_spec_accept_ex failed with status {st}")
     return {"out_tokens": out, "n_accepted": nacc, "near_boundary": near}
+
+
+MAX_CAND = 16
+
+
+def spec_accept_valid(target_logits, draft_logits, draft_tokens, uniforms,
+                      temperature=1.0, allowed=None, eps=BOUNDARY_EPS,
+                      max_cand=MAX_CAND):
+    """The outcomes the linear rule can reach when every comparison within
+    eps of its boundary may go either way (see oracle.h).
+
+    Returns dict(path_valid [B, K+1] bool: entry j < K = "first rejection at
+    j", entry K = "all accepted"; cand [B, K+1, max_cand] int32 (-1 padded);
+    n_cand [B, K+1])."""
+    lib = _load()
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    assert draft_logits.shape == (B, K, V)
+    assert draft_tokens.shape == (B, K) and uniforms.shape == (B, K + 1)
+    tl = _c(target_logits, np.float32)
+    dl = _c(draft_logits, np.float32)
+    dt = _c(draft_tokens, np.int32)
+    un = _c(uniforms, np.float32)
+    al = None
+    if allowed is not None:
+        al = _c(allowed, np.uint32)
+        assert al.shape == (B, K + 1, (V + 31) // 32)
+    pv = np.zeros((B, K + 1), np.int32)
+    cand = np.full((B, K + 1, max_cand), -1, np.int32)
+    ncand = np.zeros((B, K + 1), np.int32)
+    st = lib.oracle_spec_accept_valid(B, K, V, _ptr(tl), _ptr(dl), _ptr(dt),
+                                      _ptr(un), float(temperature), _ptr(al),
+                                      _ptr(pv), _ptr(cand), _ptr(ncand),
+                                      int(max_cand), float(eps))
+    if st != 0:
+        raise ValueError(f"oracle_spec_accept_valid failed with status {st}")
+    return {"path_valid": pv.astype(bool), "cand": cand, "n_cand": ncand}
+
+
+def spec_accept_tree_valid(target_logits, draft_logits, parents, node_tokens,
+                           uniforms, eps=BOUNDARY_EPS, max_out=64,
+                           max_cand=MAX_CAND):
+    """The outcomes the tree walk can reach when every comparison within eps
+    of its boundary may go either way (see oracle.h).
+
+    Returns a list (one per sequence) of outcomes, each a dict(nodes: tuple
+    of accepted nodes, n_accepted, cand: tuple of candidate tokens of the
+    final draw, n_cand)."""
+    lib = _load()
+    B, N, V = target_logits.shape
+    assert draft_logits.shape == (B, N, V)
+    assert parents.shape == (B, N) and node_tokens.shape == (B, N)
+    assert uniforms.shape == (B, N)
+    tl = _c(target_logits, np.float32)
+    dl = _c(draft_logits, np.float32)
+    pa = _c(parents, np.int32)
+    tk = _c(node_tokens, np.int32)
+    un = _c(uniforms, np.float32)
+    stride = N + 2 + max_cand
+    rows = np.full((B, max_out, stride), -1, np.int32)
+    nout = np.zeros((B,), np.int32)
+    st = lib.oracle_spec_accept_tree_valid(B, N, V, _ptr(tl), _ptr(dl),
+                                           _ptr(pa), _ptr(tk), _ptr(un),
+                                           _ptr(rows), _ptr(nout),
+                                           int(max_out), int(max_cand),
+                                           float(eps))
+    if st != 0:
+        raise ValueError(f"oracle_spec_accept_tree_valid failed with status {st}")
+    res = []
+    for b in range(B):
+        outs = []
+        for o in range(min(int(nout[b]), max_out)):
+            r = rows[b, o]
+            n = int(r[N])
+            nc = int(r[N + 1])
+            outs.append({"nodes": tuple(int(v) for v in r[:n]),
+                         "n_accepted": n, "n_cand": nc,
+                         "cand": tuple(int(v) for v in r[N + 2:N + 2 + min(nc, max_cand)])})
+        res.append({"outcomes": outs, "n_outcomes": int(nout[b])})
+    return res
 
 
 def e4m3_decode(codes):

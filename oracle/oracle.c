@@ -776,3 +776,223 @@ int oracle_spec_accept_ex(int batch, int num_draft, int vocab,
   free(p); free(qd); free(w);
   return status;
 }
+
+/* ---- outcomes that are valid near a decision boundary ----------------
+ * The acceptance rule ([SD] step 3) is a chain of comparisons: u_i against
+ * p(x)/q(x), and u*W against running sums of the draw's weights.  In exact
+ * arithmetic each has one answer; an implementation in another precision
+ * may take the other side of a comparison that lies within eps of its
+ * boundary (the band within which decisions are not compared exactly).
+ * The functions below list every outcome the literal rule can reach when
+ * each comparison within eps of its boundary may go either way, and every
+ * other comparison goes as in exact arithmetic.  With eps = 0 the set is
+ * the single outcome of the rule. */
+
+/* Tokens a draw from weights w with uniform u may return when the running
+ * sums within eps*W of u*W may compare either way: every x of positive
+ * weight whose interval [C(x-1), C(x)) meets the band [u*W - eps*W,
+ * u*W + eps*W], plus the last token of positive weight when u*W is at or
+ * past the total (the rule's fallback).  Writes at most max_cand tokens to
+ * cand (in token order) and returns how many there are (which may exceed
+ * max_cand). */
+static int draw_candidates(const double *w, int vocab, double u, double eps,
+                           int32_t *cand, int max_cand) {
+  double total = 0.0;
+  for (int x = 0; x < vocab; ++x) total += w[x];
+  const double target = u * total;
+  const double lo = target - eps * total, hi = target + eps * total;
+  int n = 0, last_pos = -1, last_added = -1, reached = 0;
+  double c = 0.0;
+  for (int x = 0; x < vocab; ++x) {
+    const double prev = c;
+    c += w[x];
+    if (c > target) reached = 1;
+    if (!(w[x] > 0.0)) continue;
+    last_pos = x;
+    if (prev <= hi && c > lo) {
+      if (n < max_cand) cand[n] = x;
+      ++n;
+      last_added = x;
+    }
+  }
+  if (!reached && last_pos >= 0 && last_added != last_pos) {
+    if (n < max_cand) cand[n] = last_pos;
+    ++n;
+  }
+  return n;
+}
+
+int oracle_spec_accept_valid(int batch, int num_draft, int vocab,
+                             const float *target_logits,
+                             const float *draft_logits,
+                             const int32_t *draft_tokens,
+                             const float *uniforms, double temperature,
+                             const uint32_t *allowed, int32_t *path_valid,
+                             int32_t *cand, int32_t *n_cand, int max_cand,
+                             double eps) {
+  if (batch < 0 || num_draft < 1 || vocab < 2 || max_cand < 1) return -1;
+  if (!(temperature > 0.0) || eps < 0.0) return -1;
+  const int K = num_draft;
+  const int words = (vocab + 31) / 32;
+  const double inv_t = 1.0 / temperature;
+  double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)vocab);
+  double *w = (double *)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !qd || !w) { free(p); free(qd); free(w); return -1; }
+  int status = 0;
+  for (int b = 0; b < batch && status == 0; ++b) {
+    const float *u = uniforms + (size_t)b * (K + 1);
+    int32_t *pv = path_valid + (size_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) {
+      pv[j] = 0;
+      n_cand[(size_t)b * (K + 1) + j] = 0;
+      for (int c = 0; c < max_cand; ++c)
+        cand[((size_t)b * (K + 1) + j) * max_cand + c] = -1;
+    }
+    for (int i = 0; i < K; ++i) {
+      const int x = draft_tokens[(size_t)b * K + i];
+      if (x < 0 || x >= vocab) status = -4;
+    }
+    if (status) break;
+    /* path j < K: drafts 0..j-1 accepted, draft j rejected, one draw from
+     * the residual of row j; path K: all accepted, the bonus draw from
+     * row K.  Walk the drafts while "accepted" stays a valid answer. */
+    for (int j = 0; j <= K; ++j) {
+      const float *tl = target_logits + ((size_t)b * (K + 1) + j) * vocab;
+      const uint32_t *al =
+          allowed ? allowed + ((size_t)b * (K + 1) + j) * words : NULL;
+      const size_t slot = (size_t)b * (K + 1) + j;
+      softmax_row_ex(tl, vocab, inv_t, al, p);
+      if (j == K) { /* every draft accepted */
+        pv[j] = 1;
+        n_cand[slot] = draw_candidates(p, vocab, (double)u[K], eps,
+                                       cand + slot * max_cand, max_cand);
+        break;
+      }
+      const int x = draft_tokens[(size_t)b * K + j];
+      const float *dl = draft_logits + ((size_t)b * K + j) * vocab;
+      softmax_row_ex(dl, vocab, inv_t, al, qd);
+      const int ok_x = !al || ((al[x >> 5] >> (x & 31)) & 1u);
+      const double r = (double)u[j];
+      const double ratio = !ok_x ? 0.0 : (qd[x] > 0.0) ? p[x] / qd[x] : INFINITY;
+      const int near = ok_x && fabs(r - ratio) < eps;
+      const int can_accept = ok_x && (r <= ratio || near);
+      const int can_reject = !ok_x || r > ratio || near;
+      if (can_reject) {
+        double mass = 0.0;
+        for (int y = 0; y < vocab; ++y) {
+          w[y] = (p[y] - qd[y] > 0.0) ? p[y] - qd[y] : 0.0;
+          mass += w[y];
+        }
+        if (mass == 0.0)
+          for (int y = 0; y < vocab; ++y) w[y] = p[y];
+        pv[j] = 1;
+        n_cand[slot] = draw_candidates(w, vocab, (double)u[K], eps,
+                                       cand + slot * max_cand, max_cand);
+      }
+      if (!can_accept) break;
+    }
+  }
+  free(p); free(qd); free(w);
+  return status;
+}
+
+/* Tree walk with both answers at every accept test within eps of its
+ * boundary: a depth-first enumeration of the literal walk of
+ * oracle_spec_accept_tree.  Each outcome is one row of `outcomes`:
+ * [N entries: the accepted nodes in order, -1 padded] [n_accepted]
+ * [n_cand] [max_cand candidate tokens of the final draw, -1 padded]. */
+typedef struct {
+  int N, vocab, max_out, max_cand, n_out;
+  double eps;
+  const float *tl, *dl, *u;
+  const int32_t *par, *tok;
+  double *scratch; /* 2 * vocab doubles per depth */
+  int32_t *rows;
+  int32_t path[64];
+} tree_enum;
+
+static void tree_enum_emit(tree_enum *e, int depth, const double *r) {
+  const int stride = e->N + 2 + e->max_cand;
+  int32_t tmp[1];
+  if (e->n_out < e->max_out) {
+    int32_t *row = e->rows + (size_t)e->n_out * stride;
+    for (int k = 0; k < e->N; ++k) row[k] = k < depth ? e->path[k] : -1;
+    row[e->N] = depth;
+    for (int c = 0; c < e->max_cand; ++c) row[e->N + 2 + c] = -1;
+    row[e->N + 1] = draw_candidates(r, e->vocab, (double)e->u[0], e->eps,
+                                    row + e->N + 2, e->max_cand);
+  } else {
+    (void)draw_candidates(r, e->vocab, (double)e->u[0], e->eps, tmp, 1);
+  }
+  ++e->n_out;
+}
+
+static void tree_enum_node(tree_enum *e, int cur, int depth) {
+  const int V = e->vocab;
+  double *r = e->scratch + (size_t)2 * depth * V;
+  double *qd = r + V;
+  softmax_row(e->tl + (size_t)cur * V, V, r);
+  softmax_row(e->dl + (size_t)cur * V, V, qd);
+  for (int c = cur + 1; c < e->N; ++c) {
+    if (e->par[c] != cur) continue;
+    const int x = e->tok[c];
+    const double ur = (double)e->u[c];
+    const double ratio = (qd[x] > 0.0) ? r[x] / qd[x] : INFINITY;
+    const int near = fabs(ur - ratio) < e->eps;
+    if (ur <= ratio || near) { /* accepting child c is a valid answer */
+      e->path[depth] = c;
+      tree_enum_node(e, c, depth + 1);
+    }
+    if (!(ur > ratio || near)) return; /* rejecting it is not */
+    double mass = 0.0;
+    for (int y = 0; y < V; ++y)
+      mass += (r[y] - qd[y] > 0.0) ? r[y] - qd[y] : 0.0;
+    if (mass == 0.0) continue; /* the walk keeps r (see above) */
+    for (int y = 0; y < V; ++y)
+      r[y] = ((r[y] - qd[y] > 0.0) ? r[y] - qd[y] : 0.0) / mass;
+  }
+  tree_enum_emit(e, depth, r); /* no child accepted: draw from r */
+}
+
+int oracle_spec_accept_tree_valid(int batch, int num_nodes, int vocab,
+                                  const float *target_logits,
+                                  const float *draft_logits,
+                                  const int32_t *parents,
+                                  const int32_t *node_tokens,
+                                  const float *uniforms, int32_t *outcomes,
+                                  int32_t *n_outcomes, int max_out,
+                                  int max_cand, double eps) {
+  if (batch < 0 || num_nodes < 1 || num_nodes > 64 || vocab < 2 ||
+      max_out < 1 || max_cand < 1 || eps < 0.0)
+    return -1;
+  const int N = num_nodes;
+  double *scratch =
+      (double *)malloc(sizeof(double) * 2 * (size_t)vocab * (size_t)(N + 1));
+  if (!scratch) return -1;
+  int status = 0;
+  const int stride = N + 2 + max_cand;
+  for (int b = 0; b < batch && status == 0; ++b) {
+    const int32_t *par = parents + (size_t)b * N;
+    const int32_t *tok = node_tokens + (size_t)b * N;
+    if (par[0] != -1) status = -1;
+    for (int c = 1; c < N; ++c) {
+      if (par[c] < 0 || par[c] >= c) status = -1;
+      if (tok[c] < 0 || tok[c] >= vocab) status = status ? status : -4;
+    }
+    if (status) break;
+    tree_enum e;
+    e.N = N; e.vocab = vocab; e.max_out = max_out; e.max_cand = max_cand;
+    e.n_out = 0; e.eps = eps;
+    e.tl = target_logits + (size_t)b * N * vocab;
+    e.dl = draft_logits + (size_t)b * N * vocab;
+    e.u = uniforms + (size_t)b * N;
+    e.par = par; e.tok = tok; e.scratch = scratch;
+    e.rows = outcomes + (size_t)b * max_out * stride;
+    for (int k = 0; k < max_out * stride; ++k) e.rows[k] = -1;
+    tree_enum_node(&e, 0, 0);
+    n_outcomes[b] = e.n_out;
+  }
+  free(scratch);
+  return status;
+}

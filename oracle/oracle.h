@@ -168,6 +168,42 @@ int oracle_spec_accept_tree(int batch, int num_nodes, int vocab,
                             int32_t *n_accepted, int32_t *near_boundary,
                             int32_t *residual_fallback, double eps);
 
+/* The outcomes the acceptance rule can reach when every comparison that
+ * lies within eps of its boundary may go either way (accept test:
+ * |u_i - p(x)/q(x)| < eps; draw: running sums within eps*W of u*W), every
+ * other comparison going as in exact arithmetic.  With eps = 0 this is the
+ * single outcome of the rule.
+ *
+ * Linear rule (temperature and allowed as for oracle_spec_accept_ex, no
+ * greedy): path_valid [batch, K+1]: entry j < K is 1 iff "drafts 0..j-1
+ * accepted, draft j rejected" is reachable, entry K iff "all accepted" is;
+ * cand [batch, K+1, max_cand] (-1 padded) and n_cand [batch, K+1]: the
+ * tokens the draw on that path may return (n_cand may exceed max_cand).
+ * Returns as oracle_spec_accept_ex. */
+int oracle_spec_accept_valid(int batch, int num_draft, int vocab,
+                             const float *target_logits,
+                             const float *draft_logits,
+                             const int32_t *draft_tokens,
+                             const float *uniforms, double temperature,
+                             const uint32_t *allowed, int32_t *path_valid,
+                             int32_t *cand, int32_t *n_cand, int max_cand,
+                             double eps);
+
+/* Tree walk (arguments as oracle_spec_accept_tree; num_nodes <= 64):
+ * outcomes [batch, max_out, N + 2 + max_cand]: each reachable outcome as
+ * [accepted nodes in order, -1 padded (N)] [n_accepted] [n_cand]
+ * [candidate tokens of the final draw, -1 padded (max_cand)];
+ * n_outcomes [batch] (may exceed max_out: only the first max_out rows are
+ * written).  Returns as oracle_spec_accept_tree. */
+int oracle_spec_accept_tree_valid(int batch, int num_nodes, int vocab,
+                                  const float *target_logits,
+                                  const float *draft_logits,
+                                  const int32_t *parents,
+                                  const int32_t *node_tokens,
+                                  const float *uniforms, int32_t *outcomes,
+                                  int32_t *n_outcomes, int max_out,
+                                  int max_cand, double eps);
+
 #ifdef __cplusplus
 }
 #endif

@@ -71,3 +71,103 @@ def to_host(t):
 def out_as_f64(t):
     """GPU attention output widened to float64."""
     return widen(to_host(t))
+
+
+def accept_in_valid_set(out_tokens, n_accepted, draft_tokens, valid):
+    """Per sequence: True iff (out_tokens, n_accepted) is one of the outcomes
+    in the oracle's valid set (oracle.spec_accept_valid): a reachable path j,
+    the first j draft tokens copied, the drawn token among that path's
+    candidates, then -1 padding."""
+    B, K1 = out_tokens.shape
+    ok = np.zeros(B, bool)
+    for b in range(B):
+        j = int(n_accepted[b])
+        if j < 0 or j >= K1 or not valid["path_valid"][b, j]:
+            continue
+        if not np.array_equal(out_tokens[b, :j], draft_tokens[b, :j]):
+            continue
+        n = int(valid["n_cand"][b, j])
+        if n > valid["cand"].shape[2]:
+            continue          # more candidates than listed: undecidable here
+        if int(out_tokens[b, j]) not in set(valid["cand"][b, j, :n].tolist()):
+            continue
+        if np.any(out_tokens[b, j + 1:] != -1):
+            continue
+        ok[b] = True
+    return ok
+
+
+def tree_accept_in_valid_set(out_tokens, out_nodes, n_accepted, node_tokens,
+                             valid):
+    """Per sequence: True iff the tree outcome (accepted nodes, their tokens,
+    the drawn token, -1 padding) is one of the oracle's valid outcomes
+    (oracle.spec_accept_tree_valid)."""
+    B, N = out_tokens.shape
+    ok = np.zeros(B, bool)
+    for b in range(B):
+        if valid[b]["n_outcomes"] > len(valid[b]["outcomes"]):
+            continue
+        k = int(n_accepted[b])
+        if k < 0 or k >= N:
+            continue
+        nodes = tuple(int(x) for x in out_nodes[b, :k])
+        if any(n < 0 or n >= N for n in nodes):
+            continue
+        if not np.array_equal(out_tokens[b, :k], node_tokens[b, list(nodes)]):
+            continue
+        if np.any(out_nodes[b, k:] != -1) or np.any(out_tokens[b, k + 1:] != -1):
+            continue
+        tok = int(out_tokens[b, k])
+        ok[b] = any(o["nodes"] == nodes and o["n_cand"] == len(o["cand"])
+                    and tok in o["cand"] for o in valid[b]["outcomes"])
+    return ok
+
+
+def compare_accept(toks, nacc, ref, valid, draft_tokens, label="spec_accept"):
+    """GPU acceptance against the oracle: sequences the oracle does not flag
+    must match its outcome exactly; flagged ones (a decision within the band
+    of its boundary) must be one of the oracle's valid outcomes.  Returns
+    (flagged, flagged and identical to the oracle's own outcome)."""
+    near = ref["near_boundary"] != 0
+    exact = ((nacc == ref["n_accepted"]) &
+             (toks == ref["out_tokens"]).all(axis=1))
+    bad_exact = np.nonzero(~near & ~exact)[0]
+    inset = accept_in_valid_set(toks, nacc, draft_tokens, valid)
+    bad_set = np.nonzero(near & ~inset)[0]
+    assert bad_exact.size == 0, (
+        f"[{label}] {bad_exact.size} unflagged sequences differ: "
+        f"{bad_exact[:8].tolist()}")
+    assert bad_set.size == 0, (
+        f"[{label}] {bad_set.size} flagged sequences outside the valid set: "
+        f"{bad_set[:8].tolist()}")
+    # every sequence is in the valid set (the unflagged ones trivially)
+    assert inset.all()
+    nf = int(near.sum())
+    print(f"[{label}] {len(nacc)} sequences: {len(nacc) - nf} identical, "
+          f"{nf} flagged near a boundary and inside the valid set "
+          f"({int((near & exact).sum())} of them identical)")
+    return nf, int((near & exact).sum())
+
+
+def compare_tree_accept(toks, nodes, nacc, ref, valid, node_tokens,
+                        label="spec_accept_tree"):
+    """As compare_accept, for tree acceptance."""
+    near = ref["near_boundary"] != 0
+    exact = ((nacc == ref["n_accepted"]) &
+             (toks == ref["out_tokens"]).all(axis=1) &
+             (nodes == ref["out_nodes"]).all(axis=1))
+    bad_exact = np.nonzero(~near & ~exact)[0]
+    inset = tree_accept_in_valid_set(toks, nodes, nacc, node_tokens, valid)
+    bad_set = np.nonzero(near & ~inset)[0]
+    assert bad_exact.size == 0, (
+        f"[{label}] {bad_exact.size} unflagged sequences differ: "
+        f"{bad_exact[:8].tolist()}")
+    assert bad_set.size == 0, (
+        f"[{label}] {bad_set.size} flagged sequences outside the valid set: "
+        f"{bad_set[:8].tolist()}")
+    assert inset.all()
+    nf = int(near.sum())
+    print(f"[{label}] {len(nacc)} sequences: {len(nacc) - nf} identical, "
+          f"{nf} flagged near a boundary and inside the valid set "
+          f"({int((near & exact).sum())} of them identical)")
+    return nf, int((near & exact).sum())
