@@ -1,12 +1,14 @@
 """GPU spec_accept vs the fp64 oracle.
 
-Accept counts and output tokens must be identical given the same uniforms,
-except for sequences where the oracle reports a decision within 1e-6 of its
-boundary (those are counted and reported, not compared)."""
+Accept counts and output tokens must be identical given the same uniforms.
+Where the oracle reports a decision within 1e-6 of its boundary, either
+answer of that comparison is correct: the GPU outcome must then be one of
+the outcomes the oracle lists as reachable (oracle.spec_accept_valid).
+Flagged sequences are counted and reported."""
 import numpy as np
 import pytest
 
-from helpers import to_dev
+from helpers import compare_accept, to_dev
 from spec_verify_paged_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -34,24 +36,16 @@ def _gpu(svp, wl):
 
 def _check(svp, oracle_mod, wl, max_boundary_frac=0.15):
     """Exact agreement on every sequence whose decisions all lie farther
-    than 1e-6 from their boundary.  The excluded share is reported: for the
-    inverse-CDF draw it is about 2e-6 x (tokens of positive weight), i.e. a
-    few percent at vocab 32000, so it is only bounded loosely."""
+    than 1e-6 from their boundary; valid-set membership on the others.  The
+    flagged share is about 2e-6 x (tokens of positive weight) for the draw,
+    i.e. a few percent at vocab 32000, and is only bounded loosely."""
     toks, nacc = _gpu(svp, wl)
     ref = oracle_mod.spec_accept(wl.target_logits, wl.draft_logits,
                                  wl.draft_tokens, wl.uniforms)
-    ok = ref["near_boundary"] == 0
-    n_boundary = int((~ok).sum())
-    bad_acc = np.nonzero(nacc[ok] != ref["n_accepted"][ok])[0]
-    bad_tok = np.nonzero((toks[ok] != ref["out_tokens"][ok]).any(axis=1))[0]
-    assert bad_acc.size == 0 and bad_tok.size == 0, (
-        f"{bad_acc.size} count / {bad_tok.size} token mismatches "
-        f"({n_boundary} boundary draws excluded)")
-    # the accept counts themselves are compared on all but accept-boundary
-    # cases; the boundary share stays small
-    assert n_boundary <= max(2, max_boundary_frac * len(ok)), n_boundary
-    print(f"[spec_accept] {len(ok)} sequences, {n_boundary} near a boundary "
-          f"(excluded), {len(ok) - n_boundary} identical")
+    valid = oracle_mod.spec_accept_valid(wl.target_logits, wl.draft_logits,
+                                         wl.draft_tokens, wl.uniforms)
+    n_boundary, _ = compare_accept(toks, nacc, ref, valid, wl.draft_tokens)
+    assert n_boundary <= max(2, max_boundary_frac * len(nacc)), n_boundary
     assert svp.read_device_status() == 0
     return n_boundary, nacc
 

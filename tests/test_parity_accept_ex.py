@@ -1,11 +1,13 @@
 """GPU verify epilogue (temperature, token mask, greedy) vs the fp64 oracle.
 
-Sampling: tokens and counts identical except for sequences whose decisions
-the oracle places within 1e-6 of a boundary.  Greedy: identical."""
+Sampling: tokens and counts identical, except that where the oracle places a
+decision within 1e-6 of its boundary the GPU outcome must be one of the
+outcomes the oracle lists as reachable when such comparisons may go either
+way (oracle.spec_accept_valid).  Greedy: identical."""
 import numpy as np
 import pytest
 
-from helpers import to_dev
+from helpers import compare_accept, to_dev
 from spec_verify_paged_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -68,11 +70,16 @@ def _check(svp, oracle_mod, wl, allowed, T=1.0, greedy=False,
     ref = oracle_mod.spec_accept_ex(wl.target_logits, wl.draft_logits,
                                     wl.draft_tokens, wl.uniforms,
                                     temperature=T, allowed=bits, greedy=greedy)
-    ok = ref["near_boundary"] == 0 if not greedy else np.ones(len(nacc), bool)
-    bad = np.nonzero((nacc[ok] != ref["n_accepted"][ok]) |
-                     (toks[ok] != ref["out_tokens"][ok]).any(axis=1))[0]
-    assert bad.size == 0, f"{bad.size} mismatches ({(~ok).sum()} excluded)"
-    assert (~ok).sum() <= max(2, max_boundary_frac * len(ok))
+    if greedy:  # no boundary: argmax ties go to the smallest index
+        assert np.array_equal(nacc, ref["n_accepted"])
+        assert np.array_equal(toks, ref["out_tokens"])
+    else:
+        valid = oracle_mod.spec_accept_valid(
+            wl.target_logits, wl.draft_logits, wl.draft_tokens, wl.uniforms,
+            temperature=T, allowed=bits)
+        nb, _ = compare_accept(toks, nacc, ref, valid, wl.draft_tokens,
+                               label="spec_accept_ex")
+        assert nb <= max(2, max_boundary_frac * len(nacc))
     assert svp.read_device_status() == 0
     if allowed is not None:  # every emitted token is allowed at its position
         B, K1 = toks.shape

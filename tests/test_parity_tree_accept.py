@@ -1,12 +1,14 @@
 """GPU tree acceptance vs the fp64 oracle.
 
 Accepted paths, their nodes and the drawn tokens must be identical given the
-same uniforms, except for sequences where the oracle reports a decision
-within 1e-6 of its boundary (counted, not compared)."""
+same uniforms.  Where the oracle reports a decision within 1e-6 of its
+boundary, the GPU outcome must be one of the outcomes the oracle lists as
+reachable when such comparisons may go either way
+(oracle.spec_accept_tree_valid); those sequences are counted."""
 import numpy as np
 import pytest
 
-from helpers import to_dev
+from helpers import compare_tree_accept, to_dev
 from spec_verify_paged_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -36,15 +38,12 @@ def _check(svp, oracle_mod, wl, max_boundary_frac=0.15):
     toks, nodes, nacc = _gpu(svp, wl)
     ref = oracle_mod.spec_accept_tree(wl.target_logits, wl.draft_logits,
                                       wl.parents, wl.node_tokens, wl.uniforms)
-    ok = ref["near_boundary"] == 0
-    nb = int((~ok).sum())
-    bad = np.nonzero((nacc[ok] != ref["n_accepted"][ok]) |
-                     (toks[ok] != ref["out_tokens"][ok]).any(axis=1) |
-                     (nodes[ok] != ref["out_nodes"][ok]).any(axis=1))[0]
-    assert bad.size == 0, f"{bad.size} mismatching sequences ({nb} excluded)"
-    assert nb <= max(2, max_boundary_frac * len(ok)), nb
+    valid = oracle_mod.spec_accept_tree_valid(wl.target_logits,
+                                              wl.draft_logits, wl.parents,
+                                              wl.node_tokens, wl.uniforms)
+    nb, _ = compare_tree_accept(toks, nodes, nacc, ref, valid, wl.node_tokens)
+    assert nb <= max(2, max_boundary_frac * len(nacc)), nb
     assert svp.read_device_status() == 0
-    print(f"[spec_accept_tree] {len(ok)} sequences, {nb} near a boundary")
     return nacc
 
 

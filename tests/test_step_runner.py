@@ -1,11 +1,47 @@
 """The graph-captured decode step (two ping-pong slots, one CUDA graph per
 slot, result copies on a separate stream) against the same steps made with
-plain calls: outputs, tokens and the final caches must be bit-identical."""
+plain calls: outputs, tokens and the final caches must be bit-identical.
+Each step's results, read from the runner's host slots, are also checked
+against the fp64 oracle run step by step on its own copy of the caches
+(append, attention at the attention tolerances, acceptance exact or inside
+the oracle's valid set near a decision boundary)."""
 import numpy as np
 import pytest
 
-from helpers import to_dev
+from helpers import compare_accept, compare_tree_accept, to_dev, widen
 from spec_verify_paged_gb300 import workloads as W
+
+ATOL, LSE_TOL = 2e-2, 1e-3   # bf16 KV
+
+
+class _OracleSteps:
+    """The oracle's view of a run of steps: its own caches, appended to by
+    oracle.kv_append, read by oracle.paged_attention."""
+
+    def __init__(self, oracle_mod, wl):
+        self.o = oracle_mod
+        self.kc, self.vc = wl.k_cache.copy(), wl.v_cache.copy()
+        self.scale = wl.scale
+
+    def attention(self, d, q_len, tree_mask=None):
+        self.kc, self.vc = self.o.kv_append(d["k_new"], d["v_new"], self.kc,
+                                            self.vc, d["block_table"],
+                                            d["seq_lens"])
+        if tree_mask is not None:
+            return self.o.paged_tree_attention(
+                d["q"], self.kc, self.vc, d["block_table"], d["seq_lens"],
+                q_len, tree_mask, self.scale)
+        return self.o.paged_attention(d["q"], self.kc, self.vc,
+                                      d["block_table"], d["seq_lens"], q_len,
+                                      0, 0, self.scale)
+
+
+def _check_attention(got, out_ref, lse_ref):
+    err = np.abs(widen(got["out"]) - out_ref).max()
+    assert err <= ATOL, err
+    if "lse" in got:
+        lerr = np.abs(got["lse"].astype(np.float64) - lse_ref).max()
+        assert lerr <= LSE_TOL, lerr
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +58,7 @@ def svp():
 
 
 @pytest.mark.parametrize("q_len,num_draft", [(5, 4), (1, 0)])
-def test_step_runner_matches_plain_calls(svp, q_len, num_draft):
+def test_step_runner_matches_plain_calls(svp, oracle_mod, q_len, num_draft):
     import torch
     cfg = W.small_config(batch=4, num_q_heads=16, num_kv_heads=4,
                          head_dim=128, q_len=q_len, dtype="bf16", ctx_min=40,
@@ -95,6 +131,22 @@ def test_step_runner_matches_plain_calls(svp, q_len, num_draft):
     assert torch.equal(vc1.view(torch.int16), vc2.view(torch.int16))
     run.close()
     assert svp.read_device_status() == 0
+    # the runner's host-slot results against the oracle, step by step
+    ora = _OracleSteps(oracle_mod, wl)
+    for t, d in enumerate(inputs):
+        out_ref, lse_ref = ora.attention(d, q_len)
+        _check_attention(got[t], out_ref, lse_ref)
+        if num_draft:
+            ref = oracle_mod.spec_accept(d["target_logits"], d["draft_logits"],
+                                         d["draft_tokens"], d["uniforms"])
+            valid = oracle_mod.spec_accept_valid(
+                d["target_logits"], d["draft_logits"], d["draft_tokens"],
+                d["uniforms"])
+            compare_accept(got[t]["out_tokens"], got[t]["n_accepted"], ref,
+                           valid, d["draft_tokens"], label=f"runner step {t}")
+    # and the runner's cache after the last step holds the oracle's appends
+    assert np.array_equal(kc1.view(torch.int16).cpu().numpy().view(np.uint16),
+                          ora.kc)
 
 
 def _run_steps(run, inputs, fields_out):
@@ -119,7 +171,7 @@ def _run_steps(run, inputs, fields_out):
     return got
 
 
-def test_step_runner_tree_matches_plain_calls(svp):
+def test_step_runner_tree_matches_plain_calls(svp, oracle_mod):
     """A draft-tree step (tree attention + tree acceptance) through the
     runner equals the same steps made with plain calls."""
     import torch
@@ -169,11 +221,24 @@ def test_step_runner_tree_matches_plain_calls(svp):
     assert torch.equal(kc1.view(torch.int16), kc2.view(torch.int16))
     run.close()
     assert svp.read_device_status() == 0
+    ora = _OracleSteps(oracle_mod, wl)
+    for t, d in enumerate(inputs):
+        out_ref, lse_ref = ora.attention(d, N, tree_mask=d["tree_mask"])
+        _check_attention(got[t], out_ref, lse_ref)
+        ref = oracle_mod.spec_accept_tree(d["target_logits"], d["draft_logits"],
+                                          d["parents"], d["node_tokens"],
+                                          d["uniforms"])
+        valid = oracle_mod.spec_accept_tree_valid(
+            d["target_logits"], d["draft_logits"], d["parents"],
+            d["node_tokens"], d["uniforms"])
+        compare_tree_accept(got[t]["out_tokens"], got[t]["out_nodes"],
+                            got[t]["n_accepted"], ref, valid, d["node_tokens"],
+                            label=f"runner tree step {t}")
 
 
 @pytest.mark.parametrize("opts", [dict(temperature=0.7, use_mask=True),
                                   dict(greedy=True), dict(temperature=1.6)])
-def test_step_runner_epilogue_matches_plain_calls(svp, opts):
+def test_step_runner_epilogue_matches_plain_calls(svp, oracle_mod, opts):
     """The verify epilogue (temperature, token mask, greedy) through the
     runner equals spec_accept with the same options."""
     import torch
@@ -223,3 +288,23 @@ def test_step_runner_epilogue_matches_plain_calls(svp, opts):
             assert np.array_equal(got[t][k], ref[k]), (t, k)
     run.close()
     assert svp.read_device_status() == 0
+    ora = _OracleSteps(oracle_mod, wl)
+    T = opts.get("temperature", 1.0)
+    greedy = opts.get("greedy", False)
+    for t, d in enumerate(inputs):
+        out_ref, lse_ref = ora.attention(d, K + 1)
+        _check_attention(got[t], out_ref, lse_ref)
+        allowed = d.get("allowed")
+        ref = oracle_mod.spec_accept_ex(d["target_logits"], d["draft_logits"],
+                                        d["draft_tokens"], d["uniforms"],
+                                        temperature=T, allowed=allowed,
+                                        greedy=greedy)
+        if greedy:
+            assert np.array_equal(got[t]["out_tokens"], ref["out_tokens"])
+            assert np.array_equal(got[t]["n_accepted"], ref["n_accepted"])
+            continue
+        valid = oracle_mod.spec_accept_valid(
+            d["target_logits"], d["draft_logits"], d["draft_tokens"],
+            d["uniforms"], temperature=T, allowed=allowed)
+        compare_accept(got[t]["out_tokens"], got[t]["n_accepted"], ref, valid,
+                       d["draft_tokens"], label=f"runner epilogue step {t}")

@@ -3,14 +3,15 @@ cannot allocate device memory (code running under CUDA-graph capture,
 plug-ins whose host owns every allocation, loops where cudaMalloc would
 synchronise the device).  Its split-K scratch is a fixed array inside the
 library, so this test calls it through the C ABI with raw device pointers
-and checks it against the allocating entry point, twice in a row (the
-array keeps the previous call's contents).  Kept in a file collected last."""
+and checks it against the allocating entry point and against the fp64
+oracle, twice in a row (the array keeps the previous call's contents).
+Kept in a file collected last."""
 import ctypes
 
 import numpy as np
 import pytest
 
-from helpers import to_dev
+from helpers import out_as_f64, to_dev
 from spec_verify_paged_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -45,7 +46,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=["decode", "verify", "fp32"])
-def test_noalloc_matches_allocating_call_twice(lib, case):
+def test_noalloc_matches_allocating_call_twice(lib, oracle_mod, case):
     import torch
     import spec_verify_paged_gb300 as svp
     from spec_verify_paged_gb300 import binding
@@ -60,6 +61,9 @@ def test_noalloc_matches_allocating_call_twice(lib, case):
         q, kc, vc, bt, sl, q_len=wl.q_len, n_sink=n_sink, window=window,
         scale=float(wl.scale), split_pages=sp, kernel_path=path)
     torch.cuda.synchronize()
+    o_ref, l_ref = oracle_mod.paged_attention(
+        wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.seq_lens, wl.q_len,
+        n_sink, window, wl.scale)
     dims = binding.make_dims(q.shape, kc, bt, binding._dtype_code(q), None,
                              sp, path)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -76,6 +80,11 @@ def test_noalloc_matches_allocating_call_twice(lib, case):
         lerr = (lse - ref_lse).abs().max().item()
         assert err <= TOL[cfg.dtype], (call, err)
         assert lerr <= LSE_TOL, (call, lerr)
+        # and against the oracle itself
+        oerr = np.abs(out_as_f64(out) - o_ref).max()
+        olerr = np.abs(lse.cpu().numpy().astype(np.float64) - l_ref).max()
+        assert oerr <= TOL[cfg.dtype], (call, oerr)
+        assert olerr <= LSE_TOL, (call, olerr)
     assert svp.read_device_status() == 0
 
 
