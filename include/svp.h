@@ -201,7 +201,10 @@ int paged_tree_attention(const svp_dims *dims, const void *q,
  * passes q, the caches, block_table, seq_lens, out and lse.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device, with that device current);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is
+ *     cached for the life of the CUDA context: after cudaDeviceReset the
+ *     cached address is stale, so do not use this entry point across a
+ *     device reset.
  *   - Every call shares the one array and leaves its contents behind;
  *     nothing in it needs to start at zero (every launch rewrites the
  *     split records it reads), so calls in sequence on one stream are
@@ -234,7 +237,9 @@ size_t paged_decode_workspace_size(const svp_dims *dims, int q_len,
  * copy; into an FP8 cache each value x is stored as the E4M3 code of the
  * fp32 quotient x / k_scale (resp. v_scale), nearest with ties to even,
  * saturating at +-448.  Uses no workspace.
- * Errors as for paged_decode_attention; n_new in [0, 64]. */
+ * Errors as for paged_decode_attention; n_new in [0, 64]; k_new, v_new,
+ * k_cache and v_cache must be 16-byte aligned (else SVP_ERR_INVALID_ARG,
+ * before any launch). */
 int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
               void *k_cache, void *v_cache, const int32_t *block_table,
               const int32_t *seq_lens, int n_new, cudaStream_t stream);

@@ -385,6 +385,12 @@ int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
     return SVP_ERR_INVALID_ARG;
   if (dims->num_blocks == 0 || dims->max_blocks_per_seq == 0)
     return SVP_ERR_INVALID_ARG;
+  // rows move as 16-byte (8-byte for FP8 codes) vectors: reject unaligned
+  // pointers here rather than fault on the device
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+       reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) % 16 != 0)
+    return SVP_ERR_INVALID_ARG;
   AppendParams p;
   p.k_new = k_new;
   p.v_new = v_new;

@@ -11,9 +11,15 @@
 //
 // The array lives in every GPU that loads the library, from module load
 // until process exit.  Every call shares it, and it keeps the last call's
-// contents.  Nothing in it must start at zero: the split counters carry a
-// per-launch tag, so counts left by earlier launches read as zero.  Calls
-// that overlap on the GPU race on it.
+// contents.  Nothing in it must start at zero: every attention launch
+// rewrites the split descriptor of each of its CTAs before the merge kernel
+// reads any of them, and it writes them only after its grid-dependency
+// wait, i.e. after the previous kernel on the stream (the previous call's
+// merge) has finished, so the next call on the same stream cannot
+// overwrite descriptors or partials the previous merge still reads.
+// Calls that overlap on the GPU (other streams, other host threads) race
+// on it.  The device address of the array is looked up once per device and
+// cached for the life of the process's CUDA context.
 #include <mutex>
 
 #include "svp.h"

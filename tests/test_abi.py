@@ -234,6 +234,34 @@ def test_append_rejects_bad_arguments(lib):
     assert lib.kv_append(ctypes.byref(d), P, P, P, P, P, P, 0, None) == 0
 
 
+@pytest.mark.parametrize("which", range(4))
+def test_append_rejects_unaligned_rows(lib, which):
+    """The append moves rows as 16-byte vectors: a pointer that is not
+    16-byte aligned (an offset view) is refused on the host, before any
+    launch, instead of faulting on the device."""
+    d = _dims()
+    ptrs = [P, P, P, P]
+    ptrs[which] = ctypes.c_void_p(P.value + 2)
+    assert lib.kv_append(ctypes.byref(d), *ptrs, P, P, 1, None) == -1
+    assert lib.svp_last_launch_count() == 0
+
+
+def test_noalloc_fallback_splits_need_no_more_scratch(lib):
+    """The no-alloc entry point retries a plan that does not fit its fixed
+    array with 64 and then 128 pages per CTA; those plans never need more
+    scratch than the automatic one (fewer or equal partial slots)."""
+    for kw in (dict(), dict(batch=4096, max_blocks_per_seq=8192),
+               dict(batch=64, num_q_heads=64, num_kv_heads=8,
+                    max_blocks_per_seq=8192)):
+        base = lib.paged_decode_workspace_size(ctypes.byref(_dims(**kw)), 1, 0, 0)
+        assert base > 0
+        for pps in (64, 128):
+            d = _dims(**kw)
+            d.split_pages = pps
+            n = lib.paged_decode_workspace_size(ctypes.byref(d), 1, 0, 0)
+            assert 0 < n <= base, (kw, pps, n, base)
+
+
 def test_status_strings(lib):
     assert lib.svp_status_string(0) == b"SVP_OK"
     assert lib.svp_status_string(-4) == b"SVP_ERR_WORKSPACE"

@@ -120,7 +120,7 @@ def test_parity_sweep(svp, oracle_mod, case, path):
 
 
 @pytest.mark.parametrize("path", [1, 2, 3])
-@pytest.mark.parametrize("sp", [1, 2, 7, 128])
+@pytest.mark.parametrize("sp", [1, 2, 7, 64, 128])
 def test_split_counts_agree(svp, oracle_mod, sp, path):
     """The same inputs under different split sizes (1 page per split up to
     128) all match the oracle: the log-sum-exp merge is exact."""
