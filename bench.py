@@ -58,6 +58,7 @@ from spec_verify_paged_gb300 import workloads as W  # noqa: E402
 METRIC = ("decode-attention query-tokens/s and achieved KV-read HBM GB/s "
           "(% of GB300 peak)")
 UNIT = "query-tokens/s"
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s HBM roofline of a GB300
 CSRC = os.path.join(ROOT, "spec_verify_paged_gb300", "csrc")
 
 
@@ -253,9 +254,24 @@ def max_over_ranks(value: float, world: int) -> float:
 # CPU oracle timing (cpu_baseline and --impl reference)
 # --------------------------------------------------------------------------
 
-def oracle_sample(wl, n_seqs, start=0):
+def accept_inputs(cfg):
+    """The acceptance step's inputs of a verify workload (K = q_len - 1
+    drafts, vocab 32,000, same seed as the attention inputs), a draft tree's
+    for the tree workload, None for plain decode."""
+    if cfg.tree_depth > 0:
+        return W.make_tree_accept(batch=cfg.batch, depth=cfg.tree_depth,
+                                  vocab=W.TREE_ACCEPT_CONFIG["vocab"],
+                                  seed=cfg.seed)
+    if cfg.q_len > 1:
+        return W.make_accept(batch=cfg.batch, num_draft=cfg.q_len - 1,
+                             vocab=W.ACCEPT_CONFIG["vocab"], seed=cfg.seed)
+    return None
+
+
+def oracle_sample(wl, n_seqs, start=0, awl=None):
     """Run the fp64 oracle on n_seqs sequences of the workload (all heads,
-    all query rows); returns (seconds, query tokens)."""
+    all query rows, and the acceptance of those sequences when awl is
+    given); returns (seconds, query tokens)."""
     import oracle
     oracle.build()
     B = wl.cfg.batch
@@ -278,32 +294,91 @@ def oracle_sample(wl, n_seqs, start=0):
                                wl.seq_lens, wl.q_len, wl.cfg.n_sink,
                                wl.cfg.window, wl.scale,
                                rows=rows.astype(np.int64))
+    if awl is not None:
+        s = np.array(seqs)
+        if wl.cfg.tree_depth > 0:
+            oracle.spec_accept_tree(awl.target_logits[s], awl.draft_logits[s],
+                                    awl.parents[s], awl.node_tokens[s],
+                                    awl.uniforms[s])
+        else:
+            oracle.spec_accept(awl.target_logits[s], awl.draft_logits[s],
+                               awl.draft_tokens[s], awl.uniforms[s])
     return time.perf_counter() - t, n_seqs * wl.q_len
 
 
-def cpu_baseline(wl, budget_s=10.0, max_passes=20):
+def cpu_baseline(wl, awl=None, budget_s=10.0, max_passes=20):
     """The oracle as it stands, single-threaded, on whole sequences of the
     workload (cycling through them) until about budget_s seconds of CPU
-    work."""
+    work (at least one sequence)."""
     total_t, total_tok, n = 0.0, 0, 0
-    while total_t < budget_s and n < max_passes * wl.cfg.batch:
-        dt, tok = oracle_sample(wl, 1, start=n)
+    while (n == 0 or total_t < budget_s) and n < max_passes * wl.cfg.batch:
+        dt, tok = oracle_sample(wl, 1, start=n, awl=awl)
         total_t += dt
         total_tok += tok
         n += 1
+    what = "attention" + (" and acceptance" if awl is not None else "")
     return {"value": total_tok / total_t, "unit": UNIT, "cores": 1,
             "host_cpus": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{n} sequence passes over the {wl.cfg.batch} sequences "
-                      f"of {wl.cfg.name} (all {wl.cfg.num_q_heads} heads, "
-                      f"fp64, one thread), {total_t:.1f} s"}
+                      f"of {wl.cfg.name} ({what}, all {wl.cfg.num_q_heads} "
+                      f"heads, fp64, one thread), {total_t:.1f} s"}
+
+
+def accept_boundary(cfg, awl, toks, nodes, nacc):
+    """The fp64 oracle's view of the acceptance step the GPU just made (part
+    of the CPU-baseline leg): how many sequences have a decision within 1e-6
+    of its boundary, and whether every GPU outcome is the oracle's or, for
+    a flagged sequence, one of the outcomes the oracle lists as valid."""
+    import oracle
+    oracle.build()
+    t = time.perf_counter()
+    if cfg.tree_depth > 0:
+        ref = oracle.spec_accept_tree(awl.target_logits, awl.draft_logits,
+                                      awl.parents, awl.node_tokens,
+                                      awl.uniforms)
+        valid = oracle.spec_accept_tree_valid(
+            awl.target_logits, awl.draft_logits, awl.parents,
+            awl.node_tokens, awl.uniforms)
+        same = ((nacc == ref["n_accepted"]) &
+                (toks == ref["out_tokens"]).all(1) &
+                (nodes == ref["out_nodes"]).all(1))
+        inset = []
+        for b in range(cfg.batch):
+            k = int(nacc[b])
+            path = tuple(int(x) for x in nodes[b, :max(k, 0)])
+            inset.append(any(o["nodes"] == path and int(toks[b, k]) in o["cand"]
+                             for o in valid[b]["outcomes"]) if k >= 0 else False)
+    else:
+        ref = oracle.spec_accept(awl.target_logits, awl.draft_logits,
+                                 awl.draft_tokens, awl.uniforms)
+        valid = oracle.spec_accept_valid(awl.target_logits, awl.draft_logits,
+                                         awl.draft_tokens, awl.uniforms)
+        same = ((nacc == ref["n_accepted"]) &
+                (toks == ref["out_tokens"]).all(1))
+        inset = []
+        for b in range(cfg.batch):
+            j = int(nacc[b])
+            ok = 0 <= j < toks.shape[1] and bool(valid["path_valid"][b, j])
+            ok = ok and np.array_equal(toks[b, :j], awl.draft_tokens[b, :j])
+            ok = ok and int(toks[b, j]) in valid["cand"][b, j].tolist()
+            inset.append(ok)
+    near = ref["near_boundary"] != 0
+    return {"sequences": int(cfg.batch), "boundary_draws": int(near.sum()),
+            "identical_to_oracle": int(same.sum()),
+            "flagged_inside_valid_set": int((near & np.array(inset)).sum()),
+            "unflagged_mismatches": int((~near & ~same).sum()),
+            "oracle_n_accepted_hist": np.bincount(
+                ref["n_accepted"], minlength=toks.shape[1]).tolist(),
+            "oracle_s": round(time.perf_counter() - t, 3)}
 
 
 def tokens_per_step_of(cfg):
     return cfg.batch * cfg.q_len
 
 
-def workload_config(wl, split_pages=None):
+def workload_config(wl, args=None):
+    """The `config` object of a bench line; both arms emit the same one."""
     cfg = wl.cfg
     tr = A.attention_traffic(wl.seq_lens, cfg.q_len, cfg.num_q_heads,
                              cfg.num_kv_heads, cfg.head_dim,
@@ -318,19 +393,329 @@ def workload_config(wl, split_pages=None):
                      if cfg.ctx_min != cfg.ctx_max else cfg.ctx_min),
          "n_sink": cfg.n_sink, "window": cfg.window,
          "kv_bytes_per_step": tr["kv_bytes"], "seed": cfg.seed,
-         "l2": "no flush: each step reads %.2f GB of KV, > 129 MB L2"
-               % (tr["kv_bytes"] / 1e9)}
+         "l2": ("no flush: each step reads %.2f GB of KV, > 129 MB L2"
+                % (tr["kv_bytes"] / 1e9)) if tr["kv_bytes"] > 129e6 else
+               ("no flush: the %.1f MB of KV stay L2-resident (a latency-bound "
+                "case)" % (tr["kv_bytes"] / 1e6))}
     if cfg.tree_depth > 0:
         c["draft_tree"] = {"shape": "complete binary", "depth": cfg.tree_depth,
                            "nodes": cfg.q_len}
-    if split_pages is not None:
-        c["split_pages"] = split_pages
+        c["accept"] = {"batch": cfg.batch, "tree_nodes": cfg.q_len,
+                       "vocab": W.TREE_ACCEPT_CONFIG["vocab"]}
+    elif cfg.q_len > 1:
+        c["accept"] = {"batch": cfg.batch, "num_draft": cfg.q_len - 1,
+                       "vocab": W.ACCEPT_CONFIG["vocab"]}
+        if args is not None and (args.temperature != 1.0 or args.greedy or
+                                 args.allowed_density > 0):
+            c["accept"]["epilogue"] = {
+                "temperature": args.temperature, "greedy": bool(args.greedy),
+                "allowed_density": args.allowed_density}
+    if args is not None and args.split_pages:
+        c["split_pages"] = args.split_pages
+    if args is not None and args.kernel_path:
+        c["kernel_path"] = {1: "cuda_cores", 2: "tensor_cores",
+                            3: "tcgen05"}[args.kernel_path]
     return c, tr
 
 
 # --------------------------------------------------------------------------
 # the GPU arm
 # --------------------------------------------------------------------------
+
+class GpuCase:
+    """One workload resident on the device: its step as plain library calls
+    and as CUDA graphs (the whole step, and each phase on its own)."""
+
+    def __init__(self, svp, cfg, args, dev):
+        import torch
+        self.svp, self.cfg, self.args, self.dev = svp, cfg, args, dev
+        wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
+        self.wl = wl
+        self.conf, self.tr = workload_config(wl, args)
+        self.q = to_dev(wl.q, dev)
+        self.kc, self.vc = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
+        self.bt, self.sl = to_dev(wl.block_table, dev), to_dev(wl.seq_lens, dev)
+        self.kn, self.vn = to_dev(wl.k_new, dev), to_dev(wl.v_new, dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((cfg.batch, cfg.q_len, cfg.num_q_heads),
+                               dtype=torch.float32, device=dev)
+        self.tree = cfg.tree_depth > 0
+        self.tm = (to_dev(wl.tree_mask.view(np.int32), dev) if self.tree
+                   else None)
+        self.awl = accept_inputs(cfg)
+        self.acc = None
+        self.acc_opts = {}
+        if self.tree:
+            a = self.awl
+            acc_in = [to_dev(x, dev) for x in (a.target_logits, a.draft_logits,
+                                               a.parents, a.node_tokens,
+                                               a.uniforms)]
+            acc_out = tuple(torch.empty(shape, dtype=torch.int32, device=dev)
+                            for shape in ((cfg.batch, cfg.q_len),
+                                          (cfg.batch, cfg.q_len), (cfg.batch,)))
+            self.acc = (acc_in, acc_out)
+        elif self.awl is not None:
+            a = self.awl
+            acc_in = [to_dev(x, dev) for x in (a.target_logits, a.draft_logits,
+                                               a.draft_tokens, a.uniforms)]
+            acc_out = (torch.empty((cfg.batch, cfg.q_len), dtype=torch.int32,
+                                   device=dev),
+                       torch.empty((cfg.batch,), dtype=torch.int32, device=dev))
+            self.acc = (acc_in, acc_out)
+            # the verify epilogue: temperature, token mask, greedy
+            if args.temperature != 1.0:
+                self.acc_opts["temperature"] = args.temperature
+            if args.greedy:
+                self.acc_opts["greedy"] = True
+            if args.allowed_density > 0:
+                V = W.ACCEPT_CONFIG["vocab"]
+                mrng = np.random.default_rng(cfg.seed + 7)
+                allowed = mrng.random((cfg.batch, cfg.q_len, V)) < args.allowed_density
+                allowed[..., 0] = True
+                words = (V + 31) // 32
+                pad = np.zeros((cfg.batch, cfg.q_len, words * 32), bool)
+                pad[..., :V] = allowed
+                bits = np.packbits(pad, axis=-1, bitorder="little").view(np.int32)
+                self.acc_opts["allowed"] = to_dev(np.ascontiguousarray(bits), dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.scale = float(wl.scale)
+        # an FP8 cache's scales (1 otherwise)
+        self.kv_scales = dict(k_scale=wl.k_scale, v_scale=wl.v_scale)
+        self.launches = 0
+        self.graphs = None
+
+    # -- the library calls of one step --
+    def attn_call(self, q_, bt_, sl_, out_, lse_, tm_=None):
+        a, cfg = self.args, self.cfg
+        if self.tree:
+            self.svp.paged_tree_attention(
+                q_, self.kc, self.vc, bt_, sl_, tm_, scale=self.scale,
+                out=out_, lse=lse_, split_pages=a.split_pages,
+                kernel_path=a.kernel_path, **self.kv_scales)
+        else:
+            self.svp.paged_decode_attention(
+                q_, self.kc, self.vc, bt_, sl_, q_len=cfg.q_len,
+                n_sink=cfg.n_sink, window=cfg.window, scale=self.scale,
+                out=out_, lse=lse_, split_pages=a.split_pages,
+                kernel_path=a.kernel_path, **self.kv_scales)
+
+    def accept_with(self, inputs, outputs, opts=None):
+        opts = self.acc_opts if opts is None else opts
+        if self.tree:
+            self.svp.spec_accept_tree(*inputs, out_tokens=outputs[0],
+                                      out_nodes=outputs[1],
+                                      n_accepted=outputs[2])
+        else:
+            self.svp.spec_accept(*inputs, out_tokens=outputs[0],
+                                 n_accepted=outputs[1], **opts)
+
+    def append_call(self):
+        self.svp.kv_append(self.kn, self.vn, self.kc, self.vc, self.bt,
+                           self.sl, **self.kv_scales)
+
+    def plain_step(self, ev=None):
+        svp = self.svp
+        self.append_call()
+        n = svp.last_launch_count()
+        if ev is not None:
+            ev[0].record(self.stream)
+        self.attn_call(self.q, self.bt, self.sl, self.out, self.lse, self.tm)
+        n += svp.last_launch_count()
+        if ev is not None:
+            ev[1].record(self.stream)
+        if self.acc is not None:
+            self.accept_with(self.acc[0], self.acc[1])
+            n += svp.last_launch_count()
+            if ev is not None:
+                ev[2].record(self.stream)
+        self.launches += n
+
+    # -- CUDA graphs: the whole step, and each phase on its own --
+    def capture(self):
+        """The library keeps no per-call state, so a replay does exactly the
+        work of a call.  Inside one graph each kernel is a programmatic
+        dependent launch of the one before."""
+        import torch
+        svp = self.svp
+        g_step, g_app, g_attn, g_acc = (torch.cuda.CUDAGraph(),
+                                        torch.cuda.CUDAGraph(),
+                                        torch.cuda.CUDAGraph(),
+                                        torch.cuda.CUDAGraph())
+        with torch.cuda.graph(g_app):
+            self.append_call()
+        n_app = svp.last_launch_count()
+        with torch.cuda.graph(g_attn):
+            self.attn_call(self.q, self.bt, self.sl, self.out, self.lse,
+                           self.tm)
+        n_attn = svp.last_launch_count()
+        n_acc = 0
+        if self.acc is not None:
+            with torch.cuda.graph(g_acc):
+                self.accept_with(self.acc[0], self.acc[1])
+            n_acc = svp.last_launch_count()
+        with torch.cuda.graph(g_step):
+            self.append_call()
+            self.attn_call(self.q, self.bt, self.sl, self.out, self.lse,
+                           self.tm)
+            if self.acc is not None:
+                self.accept_with(self.acc[0], self.acc[1])
+        torch.cuda.synchronize(self.dev)
+        self.graphs = (g_step, g_app, g_attn, g_acc if self.acc else None)
+        self.n_launch = (n_app, n_attn, n_acc)
+
+    def whole_step(self):
+        self.graphs[0].replay()
+        self.launches += sum(self.n_launch)
+
+    def phase_step(self, ev):
+        _, g_app, g_attn, g_acc = self.graphs
+        g_app.replay()
+        ev[0].record(self.stream)
+        g_attn.replay()
+        ev[1].record(self.stream)
+        if g_acc is not None:
+            g_acc.replay()
+            ev[2].record(self.stream)
+        self.launches += sum(self.n_launch)
+
+    def measure(self, steps, sampler, world=1, use_graph=True):
+        """Times `steps` steps (graph replays of the whole step, or plain
+        calls), then the phases in a second loop of `steps` per-phase
+        replays; returns the raw figures."""
+        import torch
+        import torch.distributed as dist
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+              for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        self.launches = 0
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        t0 = time.time()
+        start.record(self.stream)
+        for i in range(steps):
+            if use_graph:
+                self.whole_step()
+            else:
+                self.plain_step(ev[i])
+        end.record(self.stream)
+        if use_graph:  # the phase times, in a second timed loop
+            for i in range(steps):
+                self.phase_step(ev[i])
+        torch.cuda.synchronize(self.dev)
+        t1 = time.time()
+        if world > 1:
+            dist.barrier()
+        ms = start.elapsed_time(end)
+        attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        acc_ms = ([e[1].elapsed_time(e[2]) for e in ev]
+                  if self.acc is not None else None)
+        return {"ms": ms, "attn_ms": attn_ms, "acc_ms": acc_ms,
+                "launches": self.launches, "t0": t0, "t1": t1}
+
+    def accept_results(self):
+        """(tokens, nodes or None, n_accepted) of the last acceptance call."""
+        if self.acc is None:
+            return None
+        outs = [t.cpu().numpy() for t in self.acc[1]]
+        if self.tree:
+            return outs[0], outs[1], outs[2]
+        return outs[0], None, outs[1]
+
+    def free(self):
+        import torch
+        for k in list(self.__dict__):
+            if k not in ("cfg", "conf", "tr", "args"):
+                setattr(self, k, None)
+        torch.cuda.empty_cache()
+
+
+def roofline_of(case, attn_avg_s):
+    cfg = case.cfg
+    kname, ksrc = attention_kernel(cfg, case.args.kernel_path)
+    peak, peak_kind = measured_peaks()
+    achieved = case.tr["kv_bytes"] / attn_avg_s / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "frac_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "peak_source": f"{peak_kind} HBM copy bandwidth (frac); "
+                           f"frac_8tbs against the nominal 8 TB/s",
+            "kernel": kname,
+            "traffic": kernel_traffic(kname, ksrc, cfg.name)}
+
+
+def accept_summary(case):
+    """The acceptance step's own output: the n_accepted histogram of the
+    batch (path length for a draft tree)."""
+    r = case.accept_results()
+    if r is None:
+        return None
+    toks, nodes, nacc = r
+    return {"n_accepted_hist": np.bincount(np.maximum(nacc, 0),
+                                           minlength=case.cfg.q_len).tolist(),
+            "mean_accepted": round(float(nacc.mean()), 3),
+            "tokens_per_sequence": round(float(nacc.mean()) + 1.0, 3)}
+
+
+def measure_other_workload(svp, name, args, dev):
+    """One entry of the `workloads` object: the workload's step replayed as
+    one CUDA graph long enough for the clock sampler (>= 0.3 s, >= 50
+    steps), its phase times, roofline fractions, clocks, acceptance
+    histogram and, on the CPU-baseline leg, the oracle's rate and its view
+    of the acceptance step."""
+    import torch
+    cfg = W.CONFIGS[name]
+    case = GpuCase(svp, cfg, args, dev)
+    for _ in range(args.warmup):
+        case.plain_step()
+    torch.cuda.synchronize(dev)
+    assert svp.read_device_status() == 0, f"{name}: device status flags raised"
+    case.capture()
+    for _ in range(3):
+        case.whole_step()
+        case.phase_step([torch.cuda.Event() for _ in range(3)])
+    # size the timed loop from a short probe
+    probe = case.measure(10, None)
+    per_step_s = max(probe["ms"] / 10 / 1e3, 1e-6)
+    steps = int(min(20000, max(50, math.ceil(0.3 / per_step_s))))
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    m = case.measure(steps, sampler)
+    time.sleep(0.1)
+    sampler.stop()
+    attn_avg_s = sum(m["attn_ms"]) / len(m["attn_ms"]) / 1e3
+    roof = roofline_of(case, attn_avg_s)
+    e = {"config": case.conf, "steps": steps,
+         "ms_per_step": round(m["ms"] / steps, 5),
+         "value": round(tokens_per_step_of(cfg) * steps / (m["ms"] / 1e3), 1),
+         "unit": UNIT,
+         "attention_us": round(attn_avg_s * 1e6, 2),
+         "kv_bytes": int(case.tr["kv_bytes"]),
+         "kv_read_gbs": roof["achieved"],
+         "frac": roof["frac"], "frac_8tbs": roof["frac_8tbs"],
+         "kernel": roof["kernel"], "traffic": roof["traffic"],
+         "gpu_launches": int(m["launches"]),
+         "clocks": sampler.summary(m["t0"], m["t1"])}
+    if m["acc_ms"] is not None:
+        e["accept_us"] = round(sum(m["acc_ms"]) / len(m["acc_ms"]) * 1e3, 2)
+        e["accept"] = accept_summary(case)
+    if not args.no_cpu_baseline:
+        e["cpu_baseline"] = cpu_baseline(case.wl, case.awl, budget_s=2.0)
+        if case.acc is not None:
+            toks, nodes, nacc = case.accept_results()
+            e["cpu_baseline"]["accept_check"] = accept_boundary(
+                cfg, case.awl, toks, nodes, nacc)
+    case.free()
+    return e
+
+
+OTHER_WORKLOADS = ("long-context-128k", "long-context-128k-verify",
+                   "verify-gqa", "stream-sink-window", "tiny-decode",
+                   "decode-7b-fp8", "tree-verify")
+
 
 def run_ours(args):
     import torch
@@ -353,217 +738,47 @@ def run_ours(args):
     cfg = W.CONFIGS[args.workload]
     if args.batch:
         cfg = dataclasses.replace(cfg, batch=args.batch)
-    wl = W.make_attention(cfg, n_new=cfg.q_len, poison=False)
-    conf, tr = workload_config(wl, args.split_pages or None)
-    if args.kernel_path:
-        conf["kernel_path"] = {1: "cuda_cores", 2: "tensor_cores",
-                               3: "tcgen05"}[args.kernel_path]
-    conf["timing"] = ("plain calls" if args.no_graph else
-                      "one CUDA graph per step (append, attention, acceptance "
-                      "as programmatic dependent launches); phase times from a "
-                      "second timed loop of per-phase graphs")
-
-    q = to_dev(wl.q, dev)
-    kc, vc = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
-    bt, sl = to_dev(wl.block_table, dev), to_dev(wl.seq_lens, dev)
-    kn, vn = to_dev(wl.k_new, dev), to_dev(wl.v_new, dev)
-    out = torch.empty_like(q)
-    lse = torch.empty((cfg.batch, cfg.q_len, cfg.num_q_heads),
-                      dtype=torch.float32, device=dev)
-    # verify workloads (q_len > 1) end with the acceptance step on K =
-    # q_len - 1 drafts per sequence, vocab 32,000 (the acceptance workload's
-    # recipe, same seed as the attention inputs); a draft tree ends with the
-    # tree acceptance over its nodes
-    tree = cfg.tree_depth > 0
-    tm = to_dev(wl.tree_mask.view(np.int32), dev) if tree else None
-    acc = None
-    acc_opts = {}
-    if tree:
-        awl = W.make_tree_accept(batch=cfg.batch, depth=cfg.tree_depth,
-                                 vocab=W.TREE_ACCEPT_CONFIG["vocab"],
-                                 seed=cfg.seed)
-        acc_in = [to_dev(x, dev) for x in (awl.target_logits, awl.draft_logits,
-                                           awl.parents, awl.node_tokens,
-                                           awl.uniforms)]
-        acc_out = tuple(torch.empty(shape, dtype=torch.int32, device=dev)
-                        for shape in ((cfg.batch, cfg.q_len),
-                                      (cfg.batch, cfg.q_len), (cfg.batch,)))
-        acc = (acc_in, acc_out)
-        conf["accept"] = {"batch": cfg.batch, "tree_nodes": cfg.q_len,
-                          "vocab": W.TREE_ACCEPT_CONFIG["vocab"]}
-    elif cfg.q_len > 1:
-        awl = W.make_accept(batch=cfg.batch, num_draft=cfg.q_len - 1,
-                            vocab=W.ACCEPT_CONFIG["vocab"], seed=cfg.seed)
-        acc_in = [to_dev(x, dev) for x in (awl.target_logits, awl.draft_logits,
-                                           awl.draft_tokens, awl.uniforms)]
-        acc_out = (torch.empty((cfg.batch, cfg.q_len), dtype=torch.int32,
-                               device=dev),
-                   torch.empty((cfg.batch,), dtype=torch.int32, device=dev))
-        acc = (acc_in, acc_out)
-        conf["accept"] = {"batch": cfg.batch, "num_draft": cfg.q_len - 1,
-                          "vocab": W.ACCEPT_CONFIG["vocab"]}
-        # the verify epilogue: temperature, token mask, greedy
-        acc_opts = {}
-        if args.temperature != 1.0:
-            acc_opts["temperature"] = args.temperature
-        if args.greedy:
-            acc_opts["greedy"] = True
-        if args.allowed_density > 0:
-            V = W.ACCEPT_CONFIG["vocab"]
-            mrng = np.random.default_rng(cfg.seed + 7)
-            allowed = mrng.random((cfg.batch, cfg.q_len, V)) < args.allowed_density
-            allowed[..., 0] = True
-            words = (V + 31) // 32
-            pad = np.zeros((cfg.batch, cfg.q_len, words * 32), bool)
-            pad[..., :V] = allowed
-            bits = np.packbits(pad, axis=-1, bitorder="little").view(np.int32)
-            acc_opts["allowed"] = to_dev(np.ascontiguousarray(bits), dev)
-        if acc_opts:
-            conf["accept"]["epilogue"] = {
-                "temperature": args.temperature, "greedy": bool(args.greedy),
-                "allowed_density": args.allowed_density}
-    stream = torch.cuda.current_stream(dev)
-    scale = float(wl.scale)
-    launches = [0]
-
-    # an FP8 cache's scales (1 otherwise)
-    kv_scales = dict(k_scale=wl.k_scale, v_scale=wl.v_scale)
-
-    def attn_call(q_, bt_, sl_, out_, lse_, tm_=None):
-        if tree:
-            svp.paged_tree_attention(q_, kc, vc, bt_, sl_, tm_, scale=scale,
-                                     out=out_, lse=lse_,
-                                     split_pages=args.split_pages,
-                                     kernel_path=args.kernel_path, **kv_scales)
-        else:
-            svp.paged_decode_attention(
-                q_, kc, vc, bt_, sl_, q_len=cfg.q_len, n_sink=cfg.n_sink,
-                window=cfg.window, scale=scale, out=out_, lse=lse_,
-                split_pages=args.split_pages, kernel_path=args.kernel_path,
-                **kv_scales)
-
-    def accept_with(inputs, outputs, opts=None):
-        opts = acc_opts if opts is None else opts
-        if tree:
-            svp.spec_accept_tree(*inputs, out_tokens=outputs[0],
-                                 out_nodes=outputs[1], n_accepted=outputs[2])
-        else:
-            svp.spec_accept(*inputs, out_tokens=outputs[0],
-                            n_accepted=outputs[1], **opts)
-
-    def accept_call():
-        accept_with(acc[0], acc[1])
-        return svp.last_launch_count()
-
-    def step(ev=None):
-        svp.kv_append(kn, vn, kc, vc, bt, sl, **kv_scales)
-        n = svp.last_launch_count()
-        if ev is not None:
-            ev[0].record(stream)
-        attn_call(q, bt, sl, out, lse, tm)
-        n += svp.last_launch_count()
-        if ev is not None:
-            ev[1].record(stream)
-        if acc is not None:
-            n += accept_call()
-            if ev is not None:
-                ev[2].record(stream)
-        launches[0] += n
+    case = GpuCase(svp, cfg, args, dev)
+    conf, tr = case.conf, case.tr
+    if args.batch:
+        conf["batch_override"] = args.batch
+    timing = ("plain calls" if args.no_graph else
+              "one CUDA graph per step (append, attention, acceptance as "
+              "programmatic dependent launches); phase times from a second "
+              "timed loop of per-phase graphs")
 
     for _ in range(args.warmup):
-        step()
+        case.plain_step()
     torch.cuda.synchronize(dev)
     assert svp.read_device_status() == 0, "device status flags raised"
 
-    # The timed loop replays the step as one CUDA graph captured once here
-    # (KV append, attention, acceptance: the library launches each kernel as
-    # a programmatic dependent of the one before, so inside one graph each
-    # launch overlaps the previous kernel's tail): a step of tens of
-    # microseconds would otherwise be paced by the host's Python and launch
-    # overhead, not by the GPU.  The library keeps no per-call state, so a
-    # replay does exactly the work of a call.  The phase times (attention
-    # call, acceptance call) come from a second timed loop that replays each
-    # phase as its own graph with CUDA events between them.  The end-to-end
-    # figure below still goes through the plain public calls every step.
-    g_step = None
+    # The timed loop replays the step as one CUDA graph captured once here:
+    # a step of tens of microseconds would otherwise be paced by the host's
+    # Python and launch overhead, not by the GPU.  The phase times
+    # (attention call, acceptance call) come from a second timed loop that
+    # replays each phase as its own graph with CUDA events between them.
     if not args.no_graph:
-        g_step, g_app, g_attn, g_acc = (torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph())
-        with torch.cuda.graph(g_app):
-            svp.kv_append(kn, vn, kc, vc, bt, sl, **kv_scales)
-        n_app = svp.last_launch_count()
-        with torch.cuda.graph(g_attn):
-            attn_call(q, bt, sl, out, lse, tm)
-        n_attn = svp.last_launch_count()
-        n_acc = 0
-        if acc is not None:
-            with torch.cuda.graph(g_acc):
-                n_acc = accept_call()
-        with torch.cuda.graph(g_step):
-            svp.kv_append(kn, vn, kc, vc, bt, sl, **kv_scales)
-            attn_call(q, bt, sl, out, lse, tm)
-            if acc is not None:
-                accept_call()
-        torch.cuda.synchronize(dev)
-
-        def whole_step():
-            g_step.replay()
-            launches[0] += n_app + n_attn + n_acc
-
-        def step(ev=None):  # noqa: F811 -- the replayed form of the step
-            g_app.replay()
-            if ev is not None:
-                ev[0].record(stream)
-            g_attn.replay()
-            if ev is not None:
-                ev[1].record(stream)
-            if acc is not None:
-                g_acc.replay()
-                if ev is not None:
-                    ev[2].record(stream)
-            launches[0] += n_app + n_attn + n_acc
-
+        case.capture()
         for _ in range(3):
-            step()
-            whole_step()
+            case.phase_step([torch.cuda.Event() for _ in range(3)])
+            case.whole_step()
         torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)  # let the sampler start producing lines
-    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
-               for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches[0] = 0
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        if g_step is not None:
-            whole_step()
-        else:
-            step(attn_ev[i])
-    end.record(stream)
-    if g_step is not None:  # the phase times, in a second timed loop
-        for i in range(args.steps):
-            step(attn_ev[i])
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    if world > 1:
-        dist.barrier()
-    gpu_launches = launches[0]
-    ms = start.elapsed_time(end)
-    attn_ms = [e[0].elapsed_time(e[1]) for e in attn_ev]
-    acc_ms = ([e[1].elapsed_time(e[2]) for e in attn_ev] if acc is not None
-              else None)
+    m = case.measure(args.steps, sampler, world, use_graph=not args.no_graph)
     time.sleep(0.1)
     sampler.stop()
-    clocks = sampler.summary(t0, t1)
+    clocks = sampler.summary(m["t0"], m["t1"])
+    ms = m["ms"]
     ms_max = max_over_ranks(ms, world)
+    gpu_launches = m["launches"]
+    q, kc, vc, bt, sl = case.q, case.kc, case.vc, case.bt, case.sl
+    kn, vn, tm, acc, acc_opts = case.kn, case.vn, case.tm, case.acc, case.acc_opts
+    tree, stream, scale = case.tree, case.stream, case.scale
+    out, lse, kv_scales = case.out, case.lse, case.kv_scales
+    acc_stats = accept_summary(case)
 
     # ---- end to end through the public calls, host buffers ----
     # The step's inputs (q, new K/V rows, block table, lengths) travel in one
@@ -594,14 +809,15 @@ def run_ours(args):
         d_in.copy_(h_in, non_blocking=True)
         svp.kv_append(d_views["k_new"], d_views["v_new"], kc, vc,
                       d_views["block_table"], d_views["seq_lens"], **kv_scales)
-        attn_call(d_views["q"], d_views["block_table"], d_views["seq_lens"],
-                  r_views["out"], r_views["lse"], d_views.get("tree_mask"))
+        case.attn_call(d_views["q"], d_views["block_table"],
+                       d_views["seq_lens"], r_views["out"], r_views["lse"],
+                       d_views.get("tree_mask"))
         if acc is not None:
             e2e_opts = dict(acc_opts)
             if "allowed" in e2e_opts:
                 e2e_opts["allowed"] = d_views["allowed"]
-            accept_with([d_views[k] for k in acc_names],
-                        [r_views[k] for k in res_names], e2e_opts)
+            case.accept_with([d_views[k] for k in acc_names],
+                             [r_views[k] for k in res_names], e2e_opts)
         h_res.copy_(d_res, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -625,7 +841,7 @@ def run_ours(args):
     # result copy on the runner's copy stream; the host waits for a slot's
     # result only when it reuses the slot, one step later.  The slots are
     # filled once (the synthetic step's inputs do not change), so every
-    # replay still moves the full inputs and results across PCIe/C2C.
+    # replay still moves the full inputs and results across the host link.
     step_e2e = None
     if world == 1:
         ropts = {}
@@ -638,7 +854,7 @@ def run_ours(args):
                          use_mask="allowed" in acc_opts)
         run = svp.StepRunner(kc, vc, batch=cfg.batch,
                              num_q_heads=cfg.num_q_heads, q_len=cfg.q_len,
-                             max_blocks_per_seq=wl.max_blocks_per_seq,
+                             max_blocks_per_seq=case.wl.max_blocks_per_seq,
                              n_sink=cfg.n_sink, window=cfg.window, scale=scale,
                              split_pages=args.split_pages,
                              kernel_path=args.kernel_path, **kv_scales, **ropts)
@@ -688,12 +904,10 @@ def run_ours(args):
                     "d2h_bytes_per_step": int(step_bytes_out)}
 
     # ---- report ----
-    kname, ksrc = attention_kernel(cfg, args.kernel_path)
     tokens_per_step = cfg.batch * cfg.q_len
     value = world * tokens_per_step * args.steps / (ms_max / 1e3)
-    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
-    peak, peak_kind = measured_peaks()
-    achieved = tr["kv_bytes"] / attn_avg_s / 1e9
+    attn_avg_s = sum(m["attn_ms"]) / len(m["attn_ms"]) / 1e3
+    roof = roofline_of(case, attn_avg_s)
     plain_e2e = {"value": round(world * tokens_per_step / (e_ms / 1e3), 1),
                  "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                  "d2h_bytes_per_step": int(d2h),
@@ -706,14 +920,10 @@ def run_ours(args):
         "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "fp8-e4m3 KV, bf16 q"}[cfg.dtype],
         "data": "synthetic (seeded N(0,1) Q/K/V, shuffled 16-token pages)",
         "config": conf,
+        "timing": timing,
         "kv_read_gbs": round(tr["kv_bytes"] * args.steps / (ms / 1e3) / 1e9, 1),
         "attention_us": round(attn_avg_s * 1e6, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "kernel": kname,
-                     "traffic": kernel_traffic(kname, ksrc, cfg.name)},
+        "roofline": roof,
         # end to end: through the graph-captured step (svp_step_*) on one GPU,
         # else the plain calls; both copy each step's inputs from pinned
         # host memory and read its results back
@@ -721,12 +931,29 @@ def run_ours(args):
                 if step_e2e else plain_e2e),
         **({"e2e_plain_calls": plain_e2e} if step_e2e else {}),
         "gpu_launches": int(gpu_launches),
-        **({"accept_us": round(sum(acc_ms) / len(acc_ms) * 1e3, 2)}
+        **({"accept_us": round(sum(m["acc_ms"]) / len(m["acc_ms"]) * 1e3, 2),
+            "accept": acc_stats}
            if acc is not None else {}),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(case.wl, case.awl)
+        if acc is not None:
+            toks, nodes, nacc = case.accept_results()
+            line["cpu_baseline"]["accept_check"] = accept_boundary(
+                cfg, case.awl, toks, nodes, nacc)
+    case.free()
+    del q, kc, vc, bt, sl, kn, vn, tm, acc, acc_opts, out, lse
+    del h_in, d_in, d_views, h_res, d_res, r_views
+    torch.cuda.empty_cache()
+    # every other workload at one GPU, same build, same process
+    if world == 1 and not args.no_workloads and not args.batch:
+        others = {}
+        for name in OTHER_WORKLOADS:
+            if name == cfg.name:
+                continue
+            others[name] = measure_other_workload(svp, name, args, dev)
+        line["workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -743,18 +970,21 @@ def run_reference(args):
         return
     cfg = W.CONFIGS[args.workload]
     wl = W.make_attention(cfg, poison=False)
-    conf, _ = workload_config(wl)
+    awl = accept_inputs(cfg)
+    conf, _ = workload_config(wl, args)
     seqs_per_step = 1
     for i in range(args.warmup):
-        oracle_sample(wl, seqs_per_step, start=i)
+        oracle_sample(wl, seqs_per_step, start=i, awl=awl)
     t_tot, tok = 0.0, 0
     for i in range(args.steps):
-        dt, n = oracle_sample(wl, seqs_per_step, start=args.warmup + i)
+        dt, n = oracle_sample(wl, seqs_per_step, start=args.warmup + i, awl=awl)
         t_tot += dt
         tok += n
     value = tok / t_tot
     sample = (f"each step: {seqs_per_step} of {cfg.batch} sequences of "
-              f"{cfg.name}, all heads, fp64 oracle, one thread")
+              f"{cfg.name}, all heads" +
+              (", with its acceptance" if awl is not None else "") +
+              ", fp64 oracle, one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3),
         "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -762,6 +992,7 @@ def run_reference(args):
         "ms_per_step": round(t_tot * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": conf,
+        "timing": "host wall clock around each oracle call",
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
                          "host_cpus": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
@@ -795,6 +1026,9 @@ def main(argv=None):
     ap.add_argument("--greedy", action="store_true",
                     help="verify workloads: greedy (argmax) verification")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure the named workload only (no `workloads` "
+                         "object with the other configurations)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time plain API calls instead of CUDA-graph replays")
     args = ap.parse_args(argv)
