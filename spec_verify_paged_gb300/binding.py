@@ -80,12 +80,19 @@ _lock = threading.Lock()
 _lib = None
 
 
+_variants = {}
+
+
 def load_library(path: str = LIB_PATH):
-    """Load libsvp.so (raises if it has not been built)."""
+    """Load libsvp.so (raises if it has not been built).  Another path loads
+    a separately built copy of the library (its own kernels and device
+    state), e.g. a test build."""
     global _lib
     with _lock:
-        if _lib is not None:
+        if path == LIB_PATH and _lib is not None:
             return _lib
+        if path in _variants:
+            return _variants[path]
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: build it with "
@@ -134,7 +141,10 @@ def load_library(path: str = LIB_PATH):
         lib.svp_status_string.restype = ctypes.c_char_p
         lib.svp_last_launch_count.argtypes = []
         lib.svp_last_launch_count.restype = i32
-        _lib = lib
+        if path == LIB_PATH:
+            _lib = lib
+        else:
+            _variants[path] = lib
         return lib
 
 

@@ -61,6 +61,38 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, force: bool = False) -> str:
+    """A separately named copy of the library (libsvp_<name>.so beside
+    libsvp.so) compiled with extra preprocessor definitions, e.g. the test
+    build whose producers stall so that the bounded waits run out."""
+    lib = os.path.join(PKG, f"libsvp_{name}.so")
+    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS
+    if (not force and os.path.exists(lib) and
+            all(os.path.getmtime(d) <= os.path.getmtime(lib) for d in deps)):
+        return lib
+    out_dir = os.path.join(BUILD_DIR, name)
+    os.makedirs(out_dir, exist_ok=True)
+    extra = [f"-D{d}" for d in defines]
+
+    def one(src):
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [NVCC] + FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(one, SOURCES))
+    tmp = lib + f".tmp{os.getpid()}"
+    r = subprocess.run([NVCC] + ARCH + ["-shared", "-o", tmp] + objs,
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv)
     print(LIB)

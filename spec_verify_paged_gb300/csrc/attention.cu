@@ -149,6 +149,9 @@ struct Smem {
   uint64_t full[C::STAGES], empty[C::STAGES];
   uint64_t ufull[kUnitRing], uempty[kUnitRing];
   uint64_t epi;                                    // consumer-only barrier
+#ifdef SVP_TEST_STALL_AFTER
+  uint64_t stall;  // test builds: a barrier nothing arrives on
+#endif
   int abort_flag;
   int total_pages;                                 // flattened pages
   int n_ctas;                                      // CTAs sharing them
@@ -490,6 +493,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&sm.uempty[u], 1);
     }
     mbar_init(&sm.epi, kConsumerWarps);
+#ifdef SVP_TEST_STALL_AFTER
+    mbar_init(&sm.stall, 1);
+#endif
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -566,6 +572,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int k = k0 + k4 * 32 + kk;
             if (k >= n_pages) break;
             const int ph = __shfl_sync(kFull, phys[k4], kk);
+#ifdef SVP_TEST_STALL_AFTER
+            // test builds only: the producer stops after a few pages and
+            // waits on a barrier nothing arrives on, so every role's wait
+            // runs out and takes its timeout path
+            if (c == SVP_TEST_STALL_AFTER) {
+              if (lane == 0) ok = mbar_wait(&sm.stall, 0);
+              ok = __shfl_sync(kFull, ok, 0);
+              if (!ok) break;
+            }
+#endif
             if (lane == 0) {
               const int s = c % STAGES;
               if (!mbar_wait(&sm.empty[s], ((c / STAGES) & 1) ^ 1)) {
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         raise_flag(SVP_DEV_TIMEOUT);
         sm.abort_flag = 1;
         for (int k = max(0, c - STAGES); k < c; ++k)
-          (void)mbar_wait(&sm.full[k % STAGES], (k / STAGES) & 1);
+          (void)mbar_wait_drain(&sm.full[k % STAGES], (k / STAGES) & 1);
       }
     }
   } else {

@@ -108,6 +108,9 @@ struct TcSmem {
   uint64_t stg_free;               // a segment's output left the P buffers
   uint64_t ufull[kUnitRing], uempty[kUnitRing];
   uint64_t drain;
+#ifdef SVP_TEST_STALL_AFTER
+  uint64_t stall;  // test builds: a barrier nothing arrives on
+#endif
   uint32_t tmem_base;
   int abort_flag, total_pages, n_ctas;
   int prefix[1];  // [batch + 1], dynamic
@@ -427,6 +430,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(&sm.stg_free, 1);      // group 0's storing thread
     mbar_init(&sm.drain, 1);
+#ifdef SVP_TEST_STALL_AFTER
+    mbar_init(&sm.stall, 1);
+#endif
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -561,6 +567,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int src = k4 == 0 ? phys[0] : k4 == 1 ? phys[1]
                         : k4 == 2 ? phys[2] : phys[3];
           const int ph = __shfl_sync(kFull, src, ((t0 - k0) & 31) + (lane & 7));
+#ifdef SVP_TEST_STALL_AFTER
+          // test builds only: the producer stops after a few tiles and waits
+          // on a barrier nothing arrives on, so every role's wait runs out
+          if (c == SVP_TEST_STALL_AFTER) {
+            bool r = false;
+            if (lane == 0) r = mbar_wait(&sm.stall, 0);
+            if (!__shfl_sync(kFull, r, 0)) {
+              ok = false;
+              break;
+            }
+          }
+#endif
           const bool mine = lane < npg;
           const bool good = mine && ph >= 0 && ph < p.num_blocks;
           if (mine && !good) raise_tc(SVP_DEV_BAD_BLOCK_ID);
@@ -606,8 +624,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       raise_tc(SVP_DEV_TIMEOUT);
       sm.abort_flag = 1;
       for (int k = max(0, c - ST); k < c; ++k)
-        (void)mbar_wait(&sm.full[k % ST], (k / ST) & 1);
-      if (q_issued >= 0) (void)mbar_wait(&sm.q_full, q_issued & 1);
+        (void)mbar_wait_drain(&sm.full[k % ST], (k / ST) & 1);
+      if (q_issued >= 0) (void)mbar_wait_drain(&sm.q_full, q_issued & 1);
     }
   } else if (warp == kMmaWarp) {
     // ======================= MMA issuer (event driven) =======================
@@ -804,7 +822,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // every MMA issued has completed before tensor memory is freed
       tc_commit(&sm.drain);
-      (void)mbar_wait(&sm.drain, 0);
+      (void)mbar_wait_drain(&sm.drain, 0);
     }
     __syncwarp();
   } else {

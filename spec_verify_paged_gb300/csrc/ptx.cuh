@@ -10,6 +10,12 @@
 #ifndef SVP_WAIT_NS
 #define SVP_WAIT_NS 2000000000ull  // 2 s
 #endif
+// Limit of the waits a role makes after it gave up (for the copies and
+// MMAs it started, before the CTA exits).  Kept long even where a build
+// shortens the pipeline waits above, so no CTA leaves with work in flight.
+#ifndef SVP_DRAIN_WAIT_NS
+#define SVP_DRAIN_WAIT_NS 2000000000ull  // 2 s
+#endif
 
 namespace svp {
 
@@ -78,6 +84,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer() - start > SVP_WAIT_NS) return false;
+  }
+}
+
+// mbar_wait with the drain limit (see SVP_DRAIN_WAIT_NS).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar,
+                                                uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = globaltimer();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - start > SVP_DRAIN_WAIT_NS) return false;
   }
 }
 
