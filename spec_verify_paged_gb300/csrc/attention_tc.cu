@@ -27,7 +27,10 @@
 //              tile parity), so one group's shuffles, exponentials and
 //              barriers overlap the other's; their states merge by
 //              log-sum-exp at the end of a segment.  DUAL: both groups take
-//              every tile, one 32-row group each, with S double-buffered.
+//              every tile, one 32-row group each, with S double-buffered;
+//              each group's P, and at a segment's end its staged output,
+//              go into the tile's K buffer (read by then), so the ring
+//              keeps three stages beside the second Q tile.
 //              S is read in the mma-fragment layout (a thread holds four
 //              keys of eight rows): row max and sum fold over the four keys
 //              in registers, then a short transposing butterfly and a
@@ -37,7 +40,7 @@
 //              and seen by every row) skip per-key masking.  Each group
 //              folds its tiles' O into registers (o = o * alpha + O_t).
 //   warp 8     producer: block table, 2-D TMA copies of 8 pages' K and V
-//              into a 3-stage ring (2 stages for DUAL units).
+//              into a 3-stage ring.
 //   warp 9     one thread issues tcgen05.mma / tcgen05.commit, event
 //              driven: S of a tile as soon as its data and S buffer are
 //              free, P V as soon as its P is written, so stages go back to
@@ -82,14 +85,17 @@ constexpr int kTcBatchCap = 1024;  // sequences per launch (prefix in smem)
 
 // DUAL: a unit holds 2N rows (two row groups of N); both softmax groups
 // take every tile, one row group each, so each K/V tile is read once for
-// 2N rows.  Its second Q tile is paid for with a two-stage ring.
+// 2N rows.  Its second Q tile is paid for by keeping P (and a segment's
+// staged output) in the stage's K tile, which both groups' S MMAs have
+// finished reading by then: no separate P buffers.
 template <int N, bool DUAL = false>
 struct TcSmem {
-  static constexpr int ST = DUAL ? 2 : kStages;
+  static constexpr int ST = kStages;
+  static constexpr int PB = N * kTileKeys * 2;  // one group's P tile (bf16)
   alignas(1024) unsigned char k[ST][kTileBytes];
   alignas(1024) unsigned char v[ST][kTileBytes];
   alignas(1024) unsigned char q[(DUAL ? 2 : 1) * N * kD * 2];
-  alignas(1024) unsigned char pb[kGroups][N * kTileKeys * 2];  // P per group
+  alignas(1024) unsigned char pb[kGroups][DUAL ? 16 : PB];  // P per group
   alignas(16) float red_m[kGroups][4][N];
   alignas(16) float red_l[kGroups][4][N];
   alignas(16) float mu[kGroups][N];        // the max a tile's p was taken at
@@ -100,8 +106,9 @@ struct TcSmem {
   UnitInfo unit[kUnitRing];
   int stage_mask[ST];  // bit k: page k of the tile was copied
   uint64_t full[ST], empty[ST];
-  // S ready: one barrier per group, or per group and S buffer (DUAL)
-  uint64_t s_full[kGroups * (DUAL ? 2 : 1)];
+  // S ready: one barrier per group, or per S buffer parity (DUAL: both
+  // groups' S MMAs of a tile, one commit)
+  uint64_t s_full[2];
   uint64_t p_full[kGroups], o_full[kGroups];
   uint64_t q_full, q_empty;
   uint64_t x_full[2], x_empty[2];  // group 1 -> group 0 state hand-over
@@ -126,6 +133,8 @@ static_assert(tc_smem_bytes<16>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 16-row CTA");
 static_assert(tc_smem_bytes<32, true>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 64-row CTA");
+static_assert(TcSmem<32, true>::PB * kGroups <= kTileBytes,
+              "both groups' P tiles fit one K tile");
 
 __device__ __forceinline__ void raise_tc(unsigned f) {
   atomicOr(&g_status_attn_tc, f);
@@ -410,7 +419,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      // DUAL: one commit after each group's P V, or, for a segment's last
+      // tile, each group's arrival once its staged output has been read
+      mbar_init(&sm.empty[s], DUAL ? 2 : 1);
     }
     for (int i = 0; i < (int)(sizeof(sm.s_full) / sizeof(uint64_t)); ++i)
       mbar_init(&sm.s_full[i], 1);
@@ -631,9 +642,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ======================= MMA issuer (event driven) =======================
     if (lane == 0) {
       if constexpr (DUAL) {
-        // both groups take every tile: S(c) of group gi goes to its buffer
-        // c & 1 once P(c-2) of gi was written; P V(c) of gi once P(c) of gi
-        // was written; the stage is released after the second P V
+        // both groups take every tile: S(c) of both groups (buffers c & 1)
+        // once P(c-2) of both was written, one commit; P V(c) of gi once
+        // P(c) of gi was written, reading gi's P from stage c's K tile;
+        // a commit to the stage's empty barrier after each P V, except on a
+        // segment's last tile, whose stage the groups release after their
+        // outputs staged there have been read
         bool ok = true;
         int c_s = 0;                 // next tile whose S is issued
         int c_p[2] = {0, 0};         // next tile whose P V is issued, by group
@@ -642,6 +656,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int left = 0, tau = 0, cur_pages = 0;
         bool first = false, no_more = false;
         int npg_ring[8];
+        bool last_ring[8];
         uint64_t last = globaltimer();
         while (true) {
           bool prog = false;
@@ -677,11 +692,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_mma(tmem + (2 * gi + (c_s & 1)) * N, a, bq, kIdescS,
                        ks > 0 ? 1u : 0u);
               }
-              // a barrier per S buffer: S(c + 2) waits for P(c), so no
-              // phase completes twice before the group has seen it
-              tc_commit(&sm.s_full[2 * gi + (c_s & 1)]);
             }
+            // one commit for both groups: when it arrives, K of the tile is
+            // no longer read and may take P; S(c + 2) waits for both P(c),
+            // so no phase completes twice before both groups have seen it
+            tc_commit(&sm.s_full[c_s & 1]);
             npg_ring[c_s & 7] = min(kTilePages, cur_pages - tau * kTilePages);
+            last_ring[c_s & 7] = left == 1;
             ++c_s;
             ++tau;
             --left;
@@ -701,7 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc_fence_after();
               const int c = c_p[gi];
               const uint32_t va = smem_u32(sm.v[c % ST]);
-              const uint32_t pa = smem_u32(sm.pb[gi]);
+              const uint32_t pa = smem_u32(sm.k[c % ST]) + gi * Smem::PB;
               const int npg = npg_ring[c & 7];
               for (int ks = 0; ks < npg; ++ks) {
                 const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
@@ -710,9 +727,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_mma(tmem + (4 + gi) * N, a, bp, kIdescO, ks > 0 ? 1u : 0u);
               }
               tc_commit(&sm.o_full[gi]);
+              if (!last_ring[c & 7]) tc_commit(&sm.empty[c % ST]);
               ++c_p[gi];
-              // the other group's P V of this tile was issued before
-              if (c_p[1 - gi] > c) tc_commit(&sm.empty[c % ST]);
               prog = true;
             }
           }
@@ -890,8 +906,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
            tau += DUAL ? 1 : 2) {
         const int c = c0 + tau;
         const int s = c % ST;
-        bool got = mbar_wait(&sm.s_full[DUAL ? 2 * gi + (c & 1) : gi],
-                             (c >> 1) & 1);
+        bool got = mbar_wait(&sm.s_full[DUAL ? (c & 1) : gi], (c >> 1) & 1);
         got = got && mbar_wait(&sm.full[s], (c / ST) & 1);
         tc_fence_after();
         const uint32_t tS =
@@ -1047,8 +1062,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!DUAL && gi == 1 && prev < 0 && us > 0)
           ok = __all_sync(kFull, mbar_wait(&sm.stg_free, (us - 1) & 1)) && ok;
         // P as bf16, K-major and swizzled: per 8-row block, four 8x8 blocks
-        // (keys gw 32 + 8 i ..) stored transposed
-        const uint32_t pbase = smem_u32(sm.pb[gi]);
+        // (keys gw 32 + 8 i ..) stored transposed.  DUAL: in this group's
+        // part of the stage's K tile, which both groups' S MMAs have read
+        const uint32_t pbase = DUAL ? smem_u32(sm.k[s]) + gi * Smem::PB
+                                    : smem_u32(sm.pb[gi]);
 #pragma unroll
         for (int j = 0; j < J; ++j) {
           uint32_t fr[4];
@@ -1078,7 +1095,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tX = tmem + lane_base + (4 + xk) * N;
       if constexpr (DUAL) {
         // ---- epilogue of this group's N rows: no hand-over; staged in the
-        // group's own P buffer, whose last P V has completed ----
+        // group's part of its last tile's K, where that tile's P was (its
+        // P V has completed: the fold above waited for it); the stage goes
+        // back to the producer once the stores have read it ----
+        unsigned char *stg = sm.k[prev % ST] + gi * Smem::PB;
         const bool single = ui.f == ui.l;
         const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
         float *fw = gi == 0 ? sm.f0 : sm.f1;
@@ -1097,7 +1117,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar(gbar, kGroupThreads);
         if (single) {
-          __nv_bfloat16 *stg16 = reinterpret_cast<__nv_bfloat16 *>(&sm.pb[gi][0]);
+          __nv_bfloat16 *stg16 = reinterpret_cast<__nv_bfloat16 *>(stg);
 #pragma unroll
           for (int n = 0; n < N; ++n)
             stg16[n * kD + gt] = __float2bfloat16_rn(o[n] * fw[n]);
@@ -1119,7 +1139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           // fp32 rows of 128 dims in two 64-dim halves: [N][64] per pass,
           // one 256-byte copy per row, issued by the row's thread
-          float *stg32 = reinterpret_cast<float *>(&sm.pb[gi][0]);
+          float *stg32 = reinterpret_cast<float *>(stg);
           for (int hh = 0; hh < 2; ++hh) {
             if ((gt >> 6) == hh) {
 #pragma unroll
@@ -1140,8 +1160,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (gi == 0 && gt == 0) record_split(p, ui, blockIdx.x);
         }
-        // fw and the P buffer are rewritten only after this barrier
+        // fw and the staging area are rewritten only after this barrier;
+        // then the last tile's stage may be refilled
         named_bar(gbar, kGroupThreads);
+        if (gt == 0) mbar_arrive(&sm.empty[prev % ST]);
       } else if (gi == 1) {
         // ---- hand the state to group 0 (its copy of segment us - 2 must
         // have been taken) and go on with the next segment ----

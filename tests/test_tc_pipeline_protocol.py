@@ -18,13 +18,26 @@ order of arrivals and waits, which side waits for what -- with:
 It checks that every run completes, that no wait sees a lapped phase, and
 that every buffer read sees the data of the tile it is meant for (the K/V
 stage, Q of the segment, the S and O accumulators, the P buffer).  Both
-modes are modelled: one row group per tile (two groups on alternate tiles,
-three stages, state handed from group 1 to group 0 at a segment's end) and
-two row groups (both groups on every tile, two stages, double-buffered S
-with one barrier per S buffer).  Two controls show the model finds the
-hazards the kernel avoids: one S barrier per group in the two-group mode
-laps, and issuing Q only when its release has been seen (without waiting
-for it before blocking on a stage of the same segment) deadlocks.
+modes are modelled:
+
+* one row group per tile: two groups on alternate tiles, three stages, P in
+  a buffer per group, state handed from group 1 to group 0 at a segment's
+  end;
+* two row groups: both groups on every tile, three stages, S
+  double-buffered per group with one barrier per S buffer parity committed
+  after both groups' S MMAs of a tile, each group's P written into the
+  stage's K tile (free once both S MMAs have completed), a segment's output
+  staged there too; a stage goes back to the producer after two arrivals:
+  a commit after each group's P V, or for a segment's last tile each
+  group's own arrival once its staged output has been read.
+
+Controls show the model finds the hazards the kernel avoids: a single S
+barrier for all tiles (instead of one per parity) laps, committing each
+group's S separately lets a group overwrite K while the other group's S
+MMA still reads it, releasing a segment's last stage right after its P V
+lets the producer overwrite the staged output, and issuing Q only when its
+release has been seen (without waiting for it before blocking on a stage
+of the same segment) deadlocks.
 """
 import random
 
@@ -64,13 +77,18 @@ def wait(bar, k):
         yield
 
 
-def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
+class Hazard(Exception):
+    pass
+
+
+def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
+        separate_s_commits=False, early_release=False):
     rnd = random.Random(seed)
-    ST = 2 if dual else 3
+    ST = 3
     segs = [rnd.randint(1, 7) for _ in range(rnd.randint(1, 6))]
     full = [Bar(f"full{s}", 1) for s in range(ST)]
-    empty = [Bar(f"empty{s}", 1) for s in range(ST)]
-    n_s = 4 if dual and not single_s_barrier else 2
+    empty = [Bar(f"empty{s}", 2 if dual else 1) for s in range(ST)]
+    n_s = 1 if single_s_barrier else 4 if separate_s_commits else 2
     s_full = [Bar(f"s_full{i}", 1) for i in range(n_s)]
     p_full = [Bar(f"p_full{g}", 4) for g in range(2)]
     o_full = [Bar(f"o_full{g}", 1) for g in range(2)]
@@ -83,6 +101,9 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
 
     unit = [None] * R
     stage = [None] * ST      # tile whose K/V a stage holds
+    # two row groups: what each group's part of a stage's K tile holds
+    # ("K" until a group writes P there, then ("P", tile), ("out", seg))
+    kpart = [[None, None] for _ in range(ST)]
     qbuf = [None]            # segment whose Q is in the Q buffer
     seg_of = {}              # tile -> segment
     sbuf, obuf, pbuf = {}, [None, None], [None, None]
@@ -91,12 +112,22 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
     commits = []             # commits whose MMAs are all complete
 
     def s_bar(g, c):
-        if dual and not single_s_barrier:
-            return s_full[2 * g + (c & 1)], c >> 1
-        return s_full[g], (c if dual else c >> 1)
+        if dual:
+            if single_s_barrier:
+                return s_full[0], c
+            if separate_s_commits:   # one barrier per group and S buffer
+                return s_full[2 * g + (c & 1)], c >> 1
+            return s_full[c & 1], c >> 1
+        return s_full[g], c >> 1
 
     def o_phase(t):
         return t if dual else t >> 1
+
+    def land(s, c):
+        if dual and "out" in [k[0] if k else None for k in kpart[s]]:
+            raise Hazard(f"copy into stage {s} over a staged output")
+        stage[s] = c
+        kpart[s] = ["K", "K"]
 
     def copy_engine():
         while True:
@@ -111,12 +142,19 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
             if pipe and pipe[0][0] != "commit" and rnd.random() < 0.5:
                 op = pipe.pop(0)
                 kind, g, c = op
-                assert stage[c % ST] == c, ("MMA reads stage", stage[c % ST], c)
+                s = c % ST
+                assert stage[s] == c, ("MMA reads stage", stage[s], c)
                 if kind == "S":
                     assert qbuf[0] == seg_of[c], ("S reads Q", qbuf[0], seg_of[c])
+                    if dual and kpart[s] != ["K", "K"]:
+                        raise Hazard(f"S({c}) reads K overwritten: {kpart[s]}")
                     sbuf[(g, c & 1) if dual else g] = c
                 else:
-                    assert pbuf[g] == c, ("P V reads P", pbuf[g], c)
+                    if dual:
+                        if kpart[s][g] != ("P", c):
+                            raise Hazard(f"P V({g},{c}) reads {kpart[s][g]}")
+                    else:
+                        assert pbuf[g] == c, ("P V reads P", pbuf[g], c)
                     obuf[g] = c
             while pipe and pipe[0][0] == "commit":
                 commits.append(pipe.pop(0)[1])
@@ -151,7 +189,7 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
                 if c >= ST:
                     yield from wait(empty[s], c // ST - 1)
                 seg_of[c] = us
-                copies.append((full[s], lambda s=s, c=c: stage.__setitem__(s, c)))
+                copies.append((full[s], lambda s=s, c=c: land(s, c)))
                 c += 1
                 yield
             if q_pending:
@@ -163,6 +201,7 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
         c_s = us = left = 0
         first = no_more = False
         c_p, p_obs = [0, 0], [0, 0]   # alternating mode uses index 0
+        last_tiles = set()            # tiles that end a segment
         while True:
             if left == 0 and not no_more and ufull[us % R].test((us // R) & 1):
                 nt = unit[us % R]
@@ -176,7 +215,15 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
                 else p_obs[0] >= c_s - 1
             if (left > 0 and ready and full[c_s % ST].test((c_s // ST) & 1)
                     and (not first or q_full.test((us - 1) & 1))):
-                for g in ((0, 1) if dual else (c_s & 1,)):
+                if dual:
+                    for g in (0, 1):
+                        pipe.append(("S", g, c_s))
+                        if separate_s_commits:
+                            pipe.append(("commit", s_bar(g, c_s)[0]))
+                    if not separate_s_commits:
+                        pipe.append(("commit", s_bar(0, c_s)[0]))
+                else:
+                    g = c_s & 1
                     pipe.append(("S", g, c_s))
                     pipe.append(("commit", s_bar(g, c_s)[0]))
                 c_s += 1
@@ -184,6 +231,7 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
                 first = False
                 if left == 0:
                     pipe.append(("commit", q_empty))
+                    last_tiles.add(c_s - 1)
             if dual:
                 for g in (0, 1):
                     if p_obs[g] < c_s and p_full[g].test(p_obs[g] & 1):
@@ -194,7 +242,9 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
                         pipe.append(("PV", g, c))
                         pipe.append(("commit", o_full[g]))
                         c_p[g] += 1
-                        if c_p[1 - g] > c:
+                        # a segment's last stage goes back from the groups,
+                        # once their staged outputs were read
+                        if c not in last_tiles or early_release:
                             pipe.append(("commit", empty[c % ST]))
                 if no_more and left == 0 and c_p[0] == c_s and c_p[1] == c_s:
                     return
@@ -235,14 +285,31 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4):
                     assert obuf[g] == prev, ("fold O", obuf[g], prev)
                 if not dual and g == 1 and prev < 0 and us > 0:
                     yield from wait(stg_free, us - 1)
-                pbuf[g] = c
+                if dual:
+                    kpart[c % ST][g] = ("P", c)
+                else:
+                    pbuf[g] = c
                 p_full[g].arrive()
                 prev = c
                 yield
             if prev >= 0:
                 yield from wait(o_full[g], o_phase(prev))
                 assert obuf[g] == prev
-            if not dual:
+            if dual:
+                # the group's output is staged in its part of the last
+                # tile's K, read by the bulk stores, then released
+                s = prev % ST
+                if w == 0:
+                    if stage[s] != prev:
+                        raise Hazard(f"staging in stage {s} now holding {stage[s]}")
+                    kpart[s][g] = ("out", us)
+                    yield
+                    if kpart[s][g] != ("out", us) or stage[s] != prev:
+                        raise Hazard(f"staged output of segment {us} overwritten")
+                    kpart[s][g] = ("done", us)
+                    if not early_release:
+                        empty[s].arrive()
+            else:
                 xk = us & 1
                 if g == 1:
                     if us >= 2:
@@ -282,14 +349,40 @@ def test_protocol_completes_without_laps_or_hazards(dual):
         run(seed, dual)
 
 
-def test_one_s_barrier_per_group_laps_with_two_row_groups():
-    """Control: with double-buffered S and one barrier per group, S(c + 1)
-    can complete before the group has waited for S(c)."""
+def test_one_s_barrier_for_all_tiles_laps_with_two_row_groups():
+    """Control: with double-buffered S and a single S barrier (instead of
+    one per buffer parity), S(c + 1) can complete before a group has waited
+    for S(c)."""
     failures = 0
     for seed in range(200):
         try:
             run(seed, True, single_s_barrier=True)
         except (Lap, Stuck):
+            failures += 1
+    assert failures > 0
+
+
+def test_separate_s_commits_let_p_overwrite_k_in_use():
+    """Control: with a commit after each group's S MMA, a group can see its
+    own S complete and write P into the stage's K tile while the other
+    group's S MMA still reads it."""
+    failures = 0
+    for seed in range(400):
+        try:
+            run(seed, True, separate_s_commits=True)
+        except Hazard:
+            failures += 1
+    assert failures > 0
+
+
+def test_releasing_a_segments_last_stage_early_overwrites_its_output():
+    """Control: handing a segment's last stage back right after its P V lets
+    the producer copy the next tile over the output staged there."""
+    failures = 0
+    for seed in range(400):
+        try:
+            run(seed, True, early_release=True)
+        except Hazard:
             failures += 1
     assert failures > 0
 
