@@ -102,7 +102,7 @@ typedef struct {
  *   TENSOR_CORES  warp-level mma.sync (bf16 in, fp32 accumulate).
  *   TCGEN05       fifth-generation tensor cores: tcgen05.mma with fp32
  *                 accumulators in tensor memory, keys as the 128-row M
- *                 dimension (bf16, head_dim 128, 1024 sequences per
+ *                 dimension (bf16, head_dim 128, 512 sequences per
  *                 kernel launch).
  * A forced tensor path on data it cannot take (fp32; head_dim 64 for
  * TCGEN05) is SVP_ERR_UNSUPPORTED. */
@@ -139,7 +139,7 @@ typedef enum {
  * no initialisation: each CTA rewrites the split record it owns in every
  * launch, and the merge kernel reads partials only where a record of the
  * same launch points.  Two kernel launches (attention, merge) per 4096
- * sequences (1024 on the TCGEN05 path).  With
+ * sequences (512 on the TCGEN05 path).  With
  * dims->workspace == NULL the library uses a buffer of its own per device,
  * (re)allocated inside the call when it is too small -- that first call is
  * then not capturable in a CUDA graph.  Calls that share a workspace must

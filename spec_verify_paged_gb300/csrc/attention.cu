@@ -153,16 +153,14 @@ struct Smem {
   uint64_t stall;  // test builds: a barrier nothing arrives on
 #endif
   int abort_flag;
-  int total_pages;                                 // flattened pages
-  int n_ctas;                                      // CTAs sharing them
-  int prefix[1];                                   // [batch + 1], dynamic
+  int prefix[1];  // [batch + 1] item prefix, then [batch] lengths: dynamic
 };
 
 template <typename T, int D, int RB, bool MMA>
 constexpr size_t smem_bytes(int batch) {
   // + 1024 so the ring can be aligned to 1024 bytes (the swizzle atom)
-  return sizeof(Smem<T, D, RB, MMA ? 16 : RB>) + sizeof(int) * (size_t)batch +
-         1024;
+  return sizeof(Smem<T, D, RB, MMA ? 16 : RB>) +
+         sizeof(int) * (2 * (size_t)batch + 1) + 1024;
 }
 
 __device__ __forceinline__ void raise_flag(unsigned f) {
@@ -499,31 +497,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm.abort_flag = 0;
     fence_mbar_init();
   }
+  __syncthreads();  // barriers initialised
   // launched early (programmatic dependent launch): nothing in global
   // memory is touched before the previous kernel on the stream is done
   pdl_wait();
-  if (tid == 0) p.desc[blockIdx.x].valid = 0;  // until a split group starts
-  if (warp == 0) {
-    // pages of every sequence, times its groups (kv heads x row groups)
-    const int run = build_prefix(p, sm.prefix, groups_per_seq, lane,
-                                 &g_status_attn);
-    if (lane == 0) {
-      sm.total_pages = run;
-      sm.n_ctas = working_ctas(run, p.min_pages);
-    }
+  if (tid == 0) {
+    p.desc[blockIdx.x].valid = 0;  // until a split group starts
+    pdl_launch_dependents();       // the merge may be scheduled
   }
-  __syncthreads();
-  if (tid == 0) pdl_launch_dependents();  // the merge may be scheduled
-  const int total_pages = sm.total_pages;
-  const int n_ctas = sm.n_ctas;
-  // this CTA's slice of the flattened (sequence, group, page) space
-  const int range_begin = slice_begin(blockIdx.x, total_pages, n_ctas);
-  const int range_end = blockIdx.x < n_ctas
-                            ? slice_begin(blockIdx.x + 1, total_pages, n_ctas)
-                            : total_pages;
 
   if (warp == kConsumerWarps) {
     // ======================= producer warp =======================
+    // pages of every sequence, times its groups (kv heads x row groups):
+    // only this warp walks the slices, so it builds the prefix itself
+    int *const seqlen = sm.prefix + p.batch + 1;
+    const int total_pages = build_prefix(p, sm.prefix, seqlen, groups_per_seq,
+                                         lane, &g_status_attn);
+    const int n_ctas = working_ctas(total_pages, p.min_pages);
+    // this CTA's slice of the flattened (sequence, group, page) space
+    const int range_begin = slice_begin(blockIdx.x, total_pages, n_ctas);
+    const int range_end = blockIdx.x < n_ctas
+                              ? slice_begin(blockIdx.x + 1, total_pages, n_ctas)
+                              : total_pages;
     int c = 0;   // pages issued so far
     int us = 0;  // segments published so far
     bool ok = true;
@@ -536,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!ok) break;
       const UnitInfo seg =
           pos < range_end
-              ? decode_segment(p, sm.prefix, groups_per_seq, pos, us == 0,
-                               range_end, total_pages, n_ctas)
+              ? decode_segment(p, sm.prefix, seqlen, groups_per_seq, pos,
+                               us == 0, range_end, total_pages, n_ctas)
               : UnitInfo{};
       if (!seg.valid) {
         if (lane == 0) {

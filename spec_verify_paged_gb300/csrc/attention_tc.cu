@@ -81,7 +81,7 @@ constexpr int kMmaWarp = kSoftWarps + 1;
 constexpr int kTcThreads = 32 * (kSoftWarps + 2);
 // named barriers (0 is __syncthreads): 1 + g for group g
 constexpr int kPageTxBytes = 2 * 2 * kBoxBytes;  // K and V, two boxes each
-constexpr int kTcBatchCap = 1024;  // sequences per launch (prefix in smem)
+constexpr int kTcBatchCap = 512;  // sequences per launch (prefix in smem)
 
 // DUAL: a unit holds 2N rows (two row groups of N); both softmax groups
 // take every tile, one row group each, so each K/V tile is read once for
@@ -119,13 +119,14 @@ struct TcSmem {
   uint64_t stall;  // test builds: a barrier nothing arrives on
 #endif
   uint32_t tmem_base;
-  int abort_flag, total_pages, n_ctas;
-  int prefix[1];  // [batch + 1], dynamic
+  int abort_flag;
+  int prefix[1];  // [batch + 1] item prefix, then [batch] lengths: dynamic
 };
 
 template <int N, bool DUAL = false>
 constexpr size_t tc_smem_bytes(int batch) {
-  return sizeof(TcSmem<N, DUAL>) + sizeof(int) * (size_t)batch + 1024;
+  return sizeof(TcSmem<N, DUAL>) + sizeof(int) * (2 * (size_t)batch + 1) +
+         1024;
 }
 static_assert(tc_smem_bytes<32>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 32-row CTA");
@@ -462,32 +463,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
                      : "memory");
   }
+  tc_fence_before();
+  __syncthreads();  // barriers initialised, tensor memory allocated
+  tc_fence_after();
   // launched early (programmatic dependent launch): nothing in global
   // memory is touched before the previous kernel on the stream is done
   pdl_wait();
-  if (tid == 0) p.desc[blockIdx.x].valid = 0;  // until a split group starts
-  if (warp == 0) {
-    const int run = build_prefix(p, sm.prefix, groups_per_seq, lane,
-                                 &g_status_attn_tc);
-    if (lane == 0) {
-      sm.total_pages = run;
-      sm.n_ctas = working_ctas(run, p.min_pages);
-    }
+  if (tid == 0) {
+    p.desc[blockIdx.x].valid = 0;  // until a split group starts
+    pdl_launch_dependents();       // the merge may be scheduled
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) pdl_launch_dependents();  // the merge may be scheduled
   const uint32_t tmem = sm.tmem_base;
-  const int total_pages = sm.total_pages;
-  const int n_ctas = sm.n_ctas;
-  const int range_begin = slice_begin(blockIdx.x, total_pages, n_ctas);
-  const int range_end = blockIdx.x < n_ctas
-                            ? slice_begin(blockIdx.x + 1, total_pages, n_ctas)
-                            : total_pages;
 
   if (warp == kProducerWarp) {
     // ======================= producer warp =======================
+    // only this warp walks the slices, so it builds the prefix itself
+    int *const seqlen = sm.prefix + p.batch + 1;
+    const int total_pages = build_prefix(p, sm.prefix, seqlen, groups_per_seq,
+                                         lane, &g_status_attn_tc);
+    const int n_ctas = working_ctas(total_pages, p.min_pages);
+    const int range_begin = slice_begin(blockIdx.x, total_pages, n_ctas);
+    const int range_end = blockIdx.x < n_ctas
+                              ? slice_begin(blockIdx.x + 1, total_pages, n_ctas)
+                              : total_pages;
     int c = 0;   // tiles issued so far
     int us = 0;  // segments published so far
     int q_issued = -1;  // last segment whose Q copies were issued
@@ -501,8 +499,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ok) break;
       const UnitInfo seg =
           pos < range_end
-              ? decode_segment(p, sm.prefix, groups_per_seq, pos, us == 0,
-                               range_end, total_pages, n_ctas)
+              ? decode_segment(p, sm.prefix, seqlen, groups_per_seq, pos,
+                               us == 0, range_end, total_pages, n_ctas)
               : UnitInfo{};
       if (!seg.valid) {
         if (lane == 0) {

@@ -135,12 +135,14 @@ __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &phase,
   return __all_sync(kFull, ok);
 }
 
-// Warp 0: prefix[b + 1] = items of sequences 0..b (visible pages x groups
-// per sequence); returns the total on lane 0.  A sequence whose length is
-// out of range contributes nothing and raises SVP_DEV_BAD_SEQ_LEN.
+// One warp: prefix[b + 1] = items of sequences 0..b (visible pages x
+// groups per sequence) and seqlen[b] = the sequence's length (both in
+// shared memory, so decoding a segment needs no global load); returns the
+// total in every lane.  A sequence whose length is out of range contributes
+// nothing and raises SVP_DEV_BAD_SEQ_LEN.
 __device__ __forceinline__ int build_prefix(const AttnParams &p, int *prefix,
-                                            int groups_per_seq, int lane,
-                                            unsigned *status) {
+                                            int *seqlen, int groups_per_seq,
+                                            int lane, unsigned *status) {
   int run = 0;
   if (lane == 0) prefix[0] = 0;
   for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -148,6 +150,7 @@ __device__ __forceinline__ int build_prefix(const AttnParams &p, int *prefix,
     int n = 0;
     if (b < p.batch) {
       const int L = p.seq_lens[b];
+      seqlen[b] = L;
       if (L < p.q_len || L > p.max_blocks * kBlockSize) {
         if (blockIdx.x == 0) atomicOr(status, (unsigned)SVP_DEV_BAD_SEQ_LEN);
       } else {
@@ -186,6 +189,7 @@ __device__ __forceinline__ int slice_begin(int cta, int total, int n_ctas) {
 // before (its partial goes to slot 0, any later one to slot 1).
 __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
                                                    const int *prefix,
+                                                   const int *seqlen,
                                                    int groups_per_seq, int pos,
                                                    bool first, int range_end,
                                                    int total, int n_ctas) {
@@ -212,7 +216,7 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   ui.f = (int)(((long long)(gfirst + 1) * n_ctas - 1) / total);
   ui.l = (int)(((long long)(gfirst + np) * n_ctas - 1) / total);
   ui.slot = first ? 0 : 1;
-  ui.seq_len = __ldg(p.seq_lens + b);
+  ui.seq_len = seqlen[b];
   int np_seq;
   visible_pages(ui.seq_len, p.q_len, p.n_sink, p.window, ui.n_a, ui.b_start,
                 np_seq);

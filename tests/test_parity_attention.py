@@ -310,9 +310,9 @@ def test_workspace_shared_across_shapes(svp, oracle_mod):
                  _oracle(oracle_mod, wl, 0, 0))
 
 
-@pytest.mark.parametrize("path,batch", [(1, 4100), (3, 1030)])
+@pytest.mark.parametrize("path,batch", [(1, 4100), (3, 520)])
 def test_many_sequences_span_launches(svp, oracle_mod, path, batch):
-    """More sequences than one launch takes (4096 on CUDA cores, 1024 on
+    """More sequences than one launch takes (4096 on CUDA cores, 512 on
     tcgen05): the call makes two attention launches on one workspace, each
     followed by its merge, with groups split over several CTAs in both;
     every output matches the oracle."""
@@ -328,7 +328,7 @@ def test_many_sequences_span_launches(svp, oracle_mod, path, batch):
 def test_many_sequences_span_launches_64_row_units(svp, oracle_mod):
     """The same beyond one tcgen05 launch with 40 query rows per kv head:
     64-row units, their split partials merged by two CTAs per group."""
-    cfg = W.small_config(batch=1030, num_q_heads=8, num_kv_heads=1,
+    cfg = W.small_config(batch=520, num_q_heads=8, num_kv_heads=1,
                          head_dim=128, q_len=5, ctx_min=5, ctx_max=60,
                          seed=62)
     wl = W.make_attention(cfg, n_new=2)
