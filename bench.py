@@ -530,62 +530,60 @@ class GpuCase:
                 ev[2].record(self.stream)
         self.launches += n
 
-    # -- CUDA graphs: the whole step, and each phase on its own --
+    # -- CUDA graphs: the whole step, and the step cut short --
     def capture(self):
         """The library keeps no per-call state, so a replay does exactly the
         work of a call.  Inside one graph each kernel is a programmatic
-        dependent launch of the one before."""
+        dependent launch of the one before.  Besides the whole step, two
+        prefixes of it are captured -- the append alone, and the append
+        with the attention call -- so that each phase's cost is measured as
+        what it adds to the step, with the same launches and overlaps as in
+        the step itself."""
         import torch
         svp = self.svp
-        g_step, g_app, g_attn, g_acc = (torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph(),
-                                        torch.cuda.CUDAGraph())
+        g_step, g_app, g_noacc = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                  torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_app):
             self.append_call()
         n_app = svp.last_launch_count()
-        with torch.cuda.graph(g_attn):
+        with torch.cuda.graph(g_noacc):
+            self.append_call()
             self.attn_call(self.q, self.bt, self.sl, self.out, self.lse,
                            self.tm)
         n_attn = svp.last_launch_count()
         n_acc = 0
-        if self.acc is not None:
-            with torch.cuda.graph(g_acc):
-                self.accept_with(self.acc[0], self.acc[1])
-            n_acc = svp.last_launch_count()
         with torch.cuda.graph(g_step):
             self.append_call()
             self.attn_call(self.q, self.bt, self.sl, self.out, self.lse,
                            self.tm)
             if self.acc is not None:
                 self.accept_with(self.acc[0], self.acc[1])
+                n_acc = svp.last_launch_count()
         torch.cuda.synchronize(self.dev)
-        self.graphs = (g_step, g_app, g_attn, g_acc if self.acc else None)
+        self.graphs = (g_step, g_app, g_noacc if self.acc is not None else None)
         self.n_launch = (n_app, n_attn, n_acc)
 
     def whole_step(self):
         self.graphs[0].replay()
         self.launches += sum(self.n_launch)
 
-    def phase_step(self, ev):
-        _, g_app, g_attn, g_acc = self.graphs
-        g_app.replay()
-        ev[0].record(self.stream)
-        g_attn.replay()
-        ev[1].record(self.stream)
-        if g_acc is not None:
-            g_acc.replay()
-            ev[2].record(self.stream)
-        self.launches += sum(self.n_launch)
+    def warm_graphs(self):
+        g_step, g_app, g_noacc = self.graphs
+        for g in (g_step, g_app, g_noacc):
+            if g is not None:
+                g.replay()
 
     def measure(self, steps, sampler, world=1, use_graph=True):
         """Times `steps` steps (graph replays of the whole step, or plain
-        calls), then the phases in a second loop of `steps` per-phase
-        replays; returns the raw figures."""
+        calls).  With graphs, two more timed loops replay the step's
+        prefixes (append alone; append and attention), `steps` times each:
+        attention = t(append + attention) - t(append), acceptance =
+        t(step) - t(append + attention), per step."""
         import torch
         import torch.distributed as dist
         ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
               for _ in range(steps)]
+        ep = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         self.launches = 0
@@ -600,17 +598,38 @@ class GpuCase:
             else:
                 self.plain_step(ev[i])
         end.record(self.stream)
-        if use_graph:  # the phase times, in a second timed loop
-            for i in range(steps):
-                self.phase_step(ev[i])
+        if use_graph:  # the step's prefixes, in two more timed loops
+            _, g_app, g_noacc = self.graphs
+            n_app, n_attn, _ = self.n_launch
+            ep[0].record(self.stream)
+            for _ in range(steps):
+                g_app.replay()
+            ep[1].record(self.stream)
+            if g_noacc is not None:
+                for _ in range(steps):
+                    g_noacc.replay()
+            ep[2].record(self.stream)
+            self.launches += steps * (n_app + (n_app + n_attn
+                                               if g_noacc is not None else 0))
         torch.cuda.synchronize(self.dev)
         t1 = time.time()
         if world > 1:
             dist.barrier()
         ms = start.elapsed_time(end)
-        attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
-        acc_ms = ([e[1].elapsed_time(e[2]) for e in ev]
-                  if self.acc is not None else None)
+        if use_graph:
+            t_app = ep[0].elapsed_time(ep[1]) / steps
+            t_step = ms / steps
+            if self.acc is not None:
+                t_noacc = ep[1].elapsed_time(ep[2]) / steps
+                attn_ms = [t_noacc - t_app]
+                acc_ms = [t_step - t_noacc]
+            else:
+                attn_ms = [t_step - t_app]
+                acc_ms = None
+        else:
+            attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
+            acc_ms = ([e[1].elapsed_time(e[2]) for e in ev]
+                      if self.acc is not None else None)
         return {"ms": ms, "attn_ms": attn_ms, "acc_ms": acc_ms,
                 "launches": self.launches, "t0": t0, "t1": t1}
 
@@ -674,8 +693,7 @@ def measure_other_workload(svp, name, args, dev):
     assert svp.read_device_status() == 0, f"{name}: device status flags raised"
     case.capture()
     for _ in range(3):
-        case.whole_step()
-        case.phase_step([torch.cuda.Event() for _ in range(3)])
+        case.warm_graphs()
     # size the timed loop from a short probe
     probe = case.measure(10, None)
     per_step_s = max(probe["ms"] / 10 / 1e3, 1e-6)
@@ -744,8 +762,9 @@ def run_ours(args):
         conf["batch_override"] = args.batch
     timing = ("plain calls" if args.no_graph else
               "one CUDA graph per step (append, attention, acceptance as "
-              "programmatic dependent launches); phase times from a second "
-              "timed loop of per-phase graphs")
+              "programmatic dependent launches); phase times are what each "
+              "phase adds to the step: two more timed loops replay the "
+              "step's prefixes (append; append + attention)")
 
     for _ in range(args.warmup):
         case.plain_step()
@@ -760,8 +779,7 @@ def run_ours(args):
     if not args.no_graph:
         case.capture()
         for _ in range(3):
-            case.phase_step([torch.cuda.Event() for _ in range(3)])
-            case.whole_step()
+            case.warm_graphs()
         torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local)

@@ -60,6 +60,10 @@ constexpr int kAWarps = kAThreads / 32;
 constexpr int kMaxRows = 2 * kMaxDraft + 1;  // also 2 * kMaxNodes - 1
 constexpr int kStageBytes = 72000;  // staged logits per CTA (3 CTAs per SM)
 constexpr int kMaxSlots = 32;
+#ifndef SVP_ACCEPT_PIECES
+#define SVP_ACCEPT_PIECES 1
+#endif
+constexpr int kAcceptPieces = SVP_ACCEPT_PIECES;
 constexpr float kL2E = 1.4426950408889634f;
 constexpr int kNoExp = INT_MIN / 4;  // reference exponent of an empty sum
 static_assert(2 * kMaxNodes - 1 <= kMaxRows, "tree rows exceed the row arrays");
@@ -209,6 +213,8 @@ struct StageShared {
   float row_s[kMaxRows];
   uint64_t full[kMaxSlots];        // staging slots' arrival barriers
 };
+// 16-byte records that fit in warp_s once pass 1 is over (gather scratch)
+constexpr int kGatherCap = (int)(sizeof(ESum) * kAWarps * kMaxRows / 16);
 
 // Exchange state of cluster-wide sums and draws (read cluster-wide).
 struct alignas(16) DrawShared {
@@ -263,13 +269,14 @@ struct SliceStage {
              (uint32_t)len * 4u, &st->full[s]);
   }
 
-  // Thread 0 initialises the slot barriers and issues the first wave; the
-  // caller synchronises the block before pass1.
+  // Thread 0 initialises the slot barriers; the caller synchronises the
+  // block before pass1, where each warp issues the copies of the first
+  // wave's pieces it will sum (one thread issuing them all was measured
+  // slower: the copies start one after another).
   __device__ void begin(int tid) const {
     if (tid == 0 && bulk) {
       for (int s = 0; s < slots; ++s) mbar_init(&st->full[s], 1);
       fence_mbar_init();
-      for (int it = 0; it < min(slots, items()); ++it) issue(it);
     }
   }
 
@@ -287,8 +294,74 @@ struct SliceStage {
     if (!ARGMAX) return esum_merge(a, b);
     return (b.hi > a.hi || (b.hi == a.hi && b.e < a.e)) ? b : a;
   }
+  // Max and exp-sum of float4 groups [g_lo, g_hi) of staged item `it`
+  // (slot pointer x4), merged into this warp's partial of its row.
+  __device__ void sum_groups(int it, float4 *x4, int g_lo, int g_hi,
+                             int lane, int warp) const {
+    const int r = it / np, pc = it - r * np;
+    const int tok0 = s0 + pc * psz;  // token of the piece's first element
+    if (ARGMAX) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll 4
+      for (int g = g_lo + lane; g < g_hi; g += 32) {
+        float4 v = x4[g];
+        if (Filter::kActive) filter(r, tok0 + 4 * g, v);
+        const int t = tok0 + 4 * g;  // first of 4: ties keep the lowest
+        if (v.x > bv) { bv = v.x; bi = t; }
+        if (v.y > bv) { bv = v.y; bi = t + 1; }
+        if (v.z > bv) { bv = v.z; bi = t + 2; }
+        if (v.w > bv) { bv = v.w; bi = t + 3; }
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0)
+        st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{bi, bv, 0.f});
+      return;
+    }
+    float m = -INFINITY;
+#pragma unroll 4
+    for (int g = g_lo + lane; g < g_hi; g += 32) {
+      float4 v = x4[g];
+      if (Filter::kActive) {
+        filter(r, tok0 + 4 * g, v);
+        x4[g] = v;  // the filtered row is what later reads see
+      }
+      m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (!(m > -INFINITY)) return;  // nothing but -inf (warp-uniform)
+    const int e = (int)ceilf(fminf(m * sc, 1.0e9f));
+    const float eb = (float)e;
+    float hi = 0.f, lo = 0.f;
+#pragma unroll 4
+    for (int g = g_lo + lane; g < g_hi; g += 32) {
+      const float4 v = x4[g];
+      const float t =
+          (ex2(fmaf(v.x, sc, -eb)) + ex2(fmaf(v.y, sc, -eb))) +
+          (ex2(fmaf(v.z, sc, -eb)) + ex2(fmaf(v.w, sc, -eb)));
+      kahan_add(hi, lo, t);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+      const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+      pair_add(hi, lo, oh, ol);
+    }
+    if (lane == 0)
+      st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{e, hi, lo});
+  }
+
   __device__ bool pass1(int tid, int lane, int warp) const {
     bool ok = true;
+    if (bulk && lane == 0)  // this warp's pieces of the first wave
+      for (int it = warp; it < min(slots, items()); it += kAWarps) issue(it);
     if (lane == 0)
       for (int r = 0; r < R; ++r) st->warp_s[warp][r] = empty();
     for (int w0 = 0; w0 < items(); w0 += slots) {
@@ -305,71 +378,11 @@ struct SliceStage {
         __syncthreads();
       }
       for (int it = w0 + warp; it < w1; it += kAWarps) {
-        do {  // one pass: `break` ends the piece
-          const int r = it / np, pc = it - r * np;
-          const int len = piece_len(pc);
-          if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
-          if (len <= 0) break;
-          float4 *x4 = reinterpret_cast<float4 *>(xs + (size_t)(it - w0) * psz);
-          const int ng = (len + 3) >> 2;
-          const int tok0 = s0 + pc * psz;  // token of the piece's first element
-          if (ARGMAX) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-  #pragma unroll 4
-            for (int g = lane; g < ng; g += 32) {
-              float4 v = x4[g];
-              if (Filter::kActive) filter(r, tok0 + 4 * g, v);
-              const int t = tok0 + 4 * g;  // first of 4: ties keep the lowest
-              if (v.x > bv) { bv = v.x; bi = t; }
-              if (v.y > bv) { bv = v.y; bi = t + 1; }
-              if (v.z > bv) { bv = v.z; bi = t + 2; }
-              if (v.w > bv) { bv = v.w; bi = t + 3; }
-            }
-  #pragma unroll
-            for (int off = 16; off; off >>= 1) {
-              const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-              const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if (lane == 0)
-              st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{bi, bv, 0.f});
-            break;
-          }
-          float m = -INFINITY;
-  #pragma unroll 4
-          for (int g = lane; g < ng; g += 32) {
-            float4 v = x4[g];
-            if (Filter::kActive) {
-              filter(r, tok0 + 4 * g, v);
-              x4[g] = v;  // the filtered row is what later reads see
-            }
-            m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-          }
-  #pragma unroll
-          for (int off = 16; off; off >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-          if (!(m > -INFINITY)) break;  // nothing but -inf (warp-uniform)
-          const int e = (int)ceilf(fminf(m * sc, 1.0e9f));
-          const float eb = (float)e;
-          float hi = 0.f, lo = 0.f;
-  #pragma unroll 4
-          for (int g = lane; g < ng; g += 32) {
-            const float4 v = x4[g];
-            const float t =
-                (ex2(fmaf(v.x, sc, -eb)) + ex2(fmaf(v.y, sc, -eb))) +
-                (ex2(fmaf(v.z, sc, -eb)) + ex2(fmaf(v.w, sc, -eb)));
-            kahan_add(hi, lo, t);
-          }
-  #pragma unroll
-          for (int off = 16; off; off >>= 1) {
-            const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
-            const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
-            pair_add(hi, lo, oh, ol);
-          }
-          if (lane == 0)
-            st->warp_s[warp][r] = merge(st->warp_s[warp][r], ESum{e, hi, lo});
-        } while (false);
+        const int len = piece_len(it % np);
+        if (bulk) ok = mbar_wait(&st->full[it - w0], (it / slots) & 1) && ok;
+        if (len > 0)
+          sum_groups(it, reinterpret_cast<float4 *>(xs + (size_t)(it - w0) * psz),
+                     0, (len + 3) >> 2, lane, warp);
         // bulk ring: only this warp read the slot in this wave, so the
         // slot's piece of the next wave may be copied now (values a filter
         // wrote back are ordered before the copy that overwrites them)
@@ -395,35 +408,44 @@ struct SliceStage {
   }
 };
 
-// Warp 0, after the cluster barrier that follows finish(): lane r < R
-// combines row r's slice statistics of all NC CTAs into its normaliser
-// 2^e * S (kept in registers and in row_e / row_s).
+// The whole block, after the cluster barrier that follows finish(): every
+// row's normaliser 2^e * S from the NC CTAs' slice statistics, kept in
+// row_e / row_s.  The remote records are gathered into `gath` by many
+// threads at once (one vector load each, a batch of rows at a time), then
+// warp 0, lane r, combines row r from shared memory: one lane issuing all
+// NC loads of its row was measured slower.  Ends with a block barrier.
 template <int NC>
-__device__ __forceinline__ void row_normalisers(cg::cluster_group &cluster,
-                                                StageShared &st, int R,
-                                                int lane, int &e, float &S) {
-  e = kNoExp;
-  S = 0.f;
-  if (lane < R) {
-    ESum o[NC];
-    const uint32_t a0 = smem_u32(&st.slice_s[lane]);
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const uint4 v = ld_cluster_v4(cluster_map(a0, c));
-      o[c] = ESum{(int)v.x, __uint_as_float(v.y), __uint_as_float(v.z)};
+__device__ void row_normalisers(StageShared &st, uint4 *gath, int gath_cap,
+                                int R, int tid, int lane, int warp) {
+  const int rows_per = max(1, gath_cap / NC);
+  for (int r0 = 0; r0 < R; r0 += rows_per) {
+    const int nr = min(rows_per, R - r0);
+    for (int i = tid; i < NC * nr; i += kAThreads) {
+      const int c = i / nr, r = r0 + (i - c * nr);
+      gath[i] = ld_cluster_v4(cluster_map(smem_u32(&st.slice_s[r]), c));
     }
+    __syncthreads();
+    if (warp == 0 && lane < nr) {
+      const int r = r0 + lane;
+      int e = kNoExp;
+      ESum o[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) e = max(e, o[c].e);
-    float hi = 0.f, lo = 0.f;
-#pragma unroll
-    for (int c = 0; c < NC; ++c)
-      if (o[c].e != kNoExp) {
-        const float f = pow2i(o[c].e - e);  // exact
-        pair_add(hi, lo, o[c].hi * f, o[c].lo * f);
+      for (int c = 0; c < NC; ++c) {
+        const uint4 v = gath[c * nr + lane];
+        o[c] = ESum{(int)v.x, __uint_as_float(v.y), __uint_as_float(v.z)};
+        e = max(e, o[c].e);
       }
-    S = hi + lo;
-    st.row_e[lane] = e;
-    st.row_s[lane] = S;
+      float hi = 0.f, lo = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (o[c].e != kNoExp) {
+          const float f = pow2i(o[c].e - e);  // exact
+          pair_add(hi, lo, o[c].hi * f, o[c].lo * f);
+        }
+      st.row_e[r] = e;
+      st.row_s[r] = hi + lo;
+    }
+    __syncthreads();
   }
 }
 
@@ -667,11 +689,12 @@ __global__ void __launch_bounds__(kAThreads, 3)
   stage.finish(tid);
   cluster.sync();  // #1: slice statistics visible cluster-wide
 
-  // ---- normalisers and accept decisions, in warp 0 ----
+  // ---- normalisers, then the accept decisions in warp 0 ----
+  row_normalisers<NC>(sh.st, reinterpret_cast<uint4 *>(&sh.st.warp_s[0][0]),
+                      kGatherCap, R2, tid, lane, warp);
   if (warp == 0) {
-    int e;
-    float S;
-    row_normalisers<NC>(cluster, sh.st, R2, lane, e, S);
+    const int e = lane < R2 ? sh.st.row_e[lane] : kNoExp;
+    const float S = lane < R2 ? sh.st.row_s[lane] : 0.f;
     const int eq = __shfl_sync(0xffffffffu, e, min(lane + K + 1, 31));
     const float Sq = __shfl_sync(0xffffffffu, S, min(lane + K + 1, 31));
     bool bad_i = false, acc_i = true;
@@ -907,12 +930,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
   }
   stage.finish(tid);
   cluster.sync();  // slice statistics visible cluster-wide
-  if (warp == 0) {
-    int e;
-    float S;
-    row_normalisers<NC>(cluster, sh.st, R, lane, e, S);
-  }
-  __syncthreads();
+  row_normalisers<NC>(sh.st, reinterpret_cast<uint4 *>(&sh.st.warp_s[0][0]),
+                      kGatherCap, R, tid, lane, warp);
 
   // scratch for the records other cluster CTAs expose: the pass-1 partials,
   // consumed by finish()
@@ -1029,10 +1048,13 @@ AcceptPlan accept_plan(int vocab, int rows, const float *a, const float *b) {
   AcceptPlan pl;
   pl.chunk = (vocab + NC - 1) / NC;
   pl.chunk = (pl.chunk + 3) & ~3;  // whole 16-byte groups per slice
-  // whole rows per piece when they fit the staging budget (splitting rows
-  // to even out the warps' shares measured slower: more copies, waits and
-  // merges per row)
-  pl.psz = std::min(pl.chunk, kStageBytes / 4);
+  // SVP_ACCEPT_PIECES pieces per row slice when they fit the staging
+  // budget and the slot count, else whole rows (or the budget).  Whole
+  // rows (1) measured fastest: each bulk copy has a fixed cost, and the
+  // waits and merges grow with the pieces
+  const int want = (((pl.chunk + kAcceptPieces - 1) / kAcceptPieces) + 3) & ~3;
+  pl.psz = std::min(rows * kAcceptPieces <= kMaxSlots ? want : pl.chunk,
+                    kStageBytes / 4);
   pl.np = (pl.chunk + pl.psz - 1) / pl.psz;
   const int items = rows * pl.np;
   pl.slots = std::min(std::min(items, kMaxSlots), kStageBytes / (pl.psz * 4));
