@@ -40,8 +40,11 @@ constexpr int kBoxElems = 64;        // 128-byte swizzle box: 64 bf16 columns
 constexpr int kBoxBytes = kBlockSize * 128;
 
 // One segment of a CTA's slice: pages [page0, page0 + n_pages) of group
-// (b, g, rg).  CTAs f..l own the group's pages; `slot` says whether this is
-// the CTA's first (0) or last (1) segment, which is where its partial goes.
+// (b, g, rg).  CTAs f..l own the group's pages; `slot` is where this CTA's
+// partial of a split group goes: 1 for the group's first CTA f (the group
+// is f's last segment), 0 for the others (it is their first segment), so
+// no two split groups share a CTA's slot and every partial's address is
+// known from f alone.
 struct UnitInfo {
   int b, g, rg, slot;
   int f, l, item0, page0;  // item0: flat item of page0
@@ -54,8 +57,8 @@ struct TensorMaps {
   CUtensorMap v;
 };
 
-// A split group whose first page this CTA owns: its partials sit in slot
-// f_slot of this CTA and slot 0 of CTAs blockIdx.x+1 .. l.
+// A split group whose first page this CTA owns: its partials sit in slot 1
+// of this CTA and slot 0 of CTAs blockIdx.x+1 .. l.
 struct SplitDesc {
   int valid, b, g, rg;
   int l, f_slot, pad0, pad1;
@@ -215,7 +218,8 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   // CTAs that own the group's first and last pages
   ui.f = (int)(((long long)(gfirst + 1) * n_ctas - 1) / total);
   ui.l = (int)(((long long)(gfirst + np) * n_ctas - 1) / total);
-  ui.slot = first ? 0 : 1;
+  ui.slot = (int)blockIdx.x == ui.f ? 1 : 0;
+  (void)first;
   ui.seq_len = seqlen[b];
   int np_seq;
   visible_pages(ui.seq_len, p.q_len, p.n_sink, p.window, ui.n_a, ui.b_start,
@@ -236,7 +240,7 @@ __device__ __forceinline__ void record_split(const AttnParams &p,
   d.g = ui.g;
   d.rg = ui.rg;
   d.l = ui.l;
-  d.f_slot = ui.slot;
+  d.f_slot = 1;
   d.pad0 = d.pad1 = 0;
   p.desc[cta] = d;
 }
@@ -244,10 +248,11 @@ __device__ __forceinline__ void record_split(const AttnParams &p,
 // Merge of split groups: CTAs c SPLIT .. c SPLIT + SPLIT - 1 finish the
 // group recorded in desc[c] (if any) from the partials of CTAs c..l, each
 // taking RB / SPLIT of its rows (one SM reading all the partials of a 32-
-// or 64-row group is slower than several reading 16 rows each).  Each thread owns float4 slices of
-// a few rows and folds the splits in with an online log-sum-exp, kMergeUnroll
-// splits at a time: all their loads are issued together, so a typical group
-// (two to four splits) costs one memory round trip.
+// or 64-row group is slower than several reading 16 rows each).  Each
+// thread owns float4 slices of a few rows and folds the splits in with an
+// online log-sum-exp.  The first two partials are loaded together with the
+// record (their addresses do not depend on it), the rest kMergeUnroll at a
+// time, so a two-way split costs one memory round trip.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeUnroll = 4;
 
@@ -259,26 +264,59 @@ __global__ void __launch_bounds__(kMergeThreads)
   pdl_launch_dependents();
   pdl_wait();  // launched early: the attention grid must have finished
   const int f = blockIdx.x / SPLIT;
+  const int n_attn = gridDim.x / SPLIT;  // CTAs of the attention grid
   const int r0 = (blockIdx.x % SPLIT) * (RB / SPLIT);  // this CTA's rows
-  const SplitDesc dsc = p.desc[f];
-  if (!dsc.valid) return;
   const int tid = threadIdx.x;
-  const int ns = dsc.l - f + 1;
-  const int vrows = min(RB, p.rows - dsc.rg * RB);
   constexpr int NE4 = RB / SPLIT * D / 4;  // float4 slices of the rows
   constexpr int EPT = (NE4 + kMergeThreads - 1) / kMergeThreads;
   const float4 *po4 = reinterpret_cast<const float4 *>(p.part_o);
+  // the partials of CTA f (slot 1) and CTA f + 1 (slot 0) -- every split
+  // group has both -- are loaded together with the split record, so the
+  // common two-way split costs one memory round trip
+  float ls[EPT][2];
+  float4 v[EPT][2];
+  const bool two = f + 1 < n_attn;
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) {
+    const int e4 = tid + k * kMergeThreads;
+    const int r = r0 + e4 / (D / 4), d4 = e4 % (D / 4);
+    ls[k][0] = ls[k][1] = -INFINITY;
+    v[k][0] = v[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e4 < NE4 && two) {
+      const size_t p0 = (size_t)(2 * f + 1), p1 = (size_t)(2 * (f + 1));
+      ls[k][0] = p.part_lse[p0 * RB + r];
+      v[k][0] = po4[(p0 * RB + r) * (D / 4) + d4];
+      ls[k][1] = p.part_lse[p1 * RB + r];
+      v[k][1] = po4[(p1 * RB + r) * (D / 4) + d4];
+    }
+  }
+  const SplitDesc dsc = p.desc[f];
+  if (!dsc.valid) return;
+  const int ns = dsc.l - f + 1;  // >= 2
+  const int vrows = min(RB, p.rows - dsc.rg * RB);
   float m[EPT], w_sum[EPT];
   float4 acc[EPT];
 #pragma unroll
   for (int k = 0; k < EPT; ++k) {
-    m[k] = -INFINITY;
+    // the first two splits
+    const float mn = fmaxf(ls[k][0], ls[k][1]);
+    m[k] = mn;
     w_sum[k] = 0.f;
     acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mn == -INFINITY) continue;  // nothing visible yet (or padding)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float w = ex2(ls[k][j] - mn);  // 0 for an empty split
+      w_sum[k] += w;
+      acc[k].x = fmaf(w, v[k][j].x, acc[k].x);
+      acc[k].y = fmaf(w, v[k][j].y, acc[k].y);
+      acc[k].z = fmaf(w, v[k][j].z, acc[k].z);
+      acc[k].w = fmaf(w, v[k][j].w, acc[k].w);
+    }
   }
-  for (int s0 = 0; s0 < ns; s0 += kMergeUnroll) {
-    float ls[EPT][kMergeUnroll];
-    float4 v[EPT][kMergeUnroll];
+  for (int s0 = 2; s0 < ns; s0 += kMergeUnroll) {
+    float lsx[EPT][kMergeUnroll];
+    float4 vx[EPT][kMergeUnroll];
 #pragma unroll
     for (int k = 0; k < EPT; ++k) {
       const int e4 = tid + k * kMergeThreads;
@@ -286,13 +324,12 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
       for (int j = 0; j < kMergeUnroll; ++j) {
         const int s = s0 + j;
-        ls[k][j] = -INFINITY;
-        v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lsx[k][j] = -INFINITY;
+        vx[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (e4 < NE4 && r < vrows && s < ns) {
-          // CTA f's partial sits in its f_slot; later CTAs' in slot 0
-          const size_t prow = (size_t)(2 * (f + s) + (s == 0 ? dsc.f_slot : 0));
-          ls[k][j] = p.part_lse[prow * RB + r];
-          v[k][j] = po4[(prow * RB + r) * (D / 4) + d4];
+          const size_t prow = (size_t)(2 * (f + s));  // slot 0 of CTA f + s
+          lsx[k][j] = p.part_lse[prow * RB + r];
+          vx[k][j] = po4[(prow * RB + r) * (D / 4) + d4];
         }
       }
     }
@@ -300,20 +337,20 @@ __global__ void __launch_bounds__(kMergeThreads)
     for (int k = 0; k < EPT; ++k) {
       float mn = m[k];
 #pragma unroll
-      for (int j = 0; j < kMergeUnroll; ++j) mn = fmaxf(mn, ls[k][j]);
-      if (mn == -INFINITY) continue;  // nothing visible yet (or padding)
+      for (int j = 0; j < kMergeUnroll; ++j) mn = fmaxf(mn, lsx[k][j]);
+      if (mn == -INFINITY) continue;
       const float sc = ex2(m[k] - mn);  // 0 while m[k] is -inf
       float4 a = acc[k];
       a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
       float ws = w_sum[k] * sc;
 #pragma unroll
       for (int j = 0; j < kMergeUnroll; ++j) {
-        const float w = ex2(ls[k][j] - mn);  // 0 for an empty split
+        const float w = ex2(lsx[k][j] - mn);
         ws += w;
-        a.x = fmaf(w, v[k][j].x, a.x);
-        a.y = fmaf(w, v[k][j].y, a.y);
-        a.z = fmaf(w, v[k][j].z, a.z);
-        a.w = fmaf(w, v[k][j].w, a.w);
+        a.x = fmaf(w, vx[k][j].x, a.x);
+        a.y = fmaf(w, vx[k][j].y, a.y);
+        a.z = fmaf(w, vx[k][j].z, a.z);
+        a.w = fmaf(w, vx[k][j].w, a.w);
       }
       acc[k] = a;
       w_sum[k] = ws;
