@@ -51,6 +51,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "attn_common.cuh"
 
@@ -325,6 +326,104 @@ __device__ __forceinline__ void process_page_fma(
 }
 
 // --------------------------------------------------------------------------
+// FP8 pages with one query row per kv head (head_dim 128): key per lane
+// --------------------------------------------------------------------------
+// d = a * b + c with a, b fp16 and c, d fp32: the product of two fp16 values
+// is exact in fp32, so this equals widening both and one fmaf.
+__device__ __forceinline__ float fma_h(float c, unsigned short a,
+                                       unsigned short b) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+// two E4M3 codes (low 16 bits) -> fp16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t w) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      (__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Lane l takes key l/2 of the page and half l%2 of its 128 dims: 64
+// fp16 x E4M3 products summed in fp32 with mixed-precision FMAs, then one
+// shuffle joins the halves -- no transposing reduction of 16 partial dot
+// products.  The four 16-code chunks of a half are visited in an order
+// rotated by the key (qr holds q's chunks in the same order), so the eight
+// lanes of a 16-byte load phase hit eight different bank groups.  P V: the
+// lane owns dims 4l..4l+3, p goes through shared memory as fp16.  q is the
+// row's bf16 values as fp16 (exact in fp16's normal range), unscaled; the
+// score is scaled once (qscale).
+__device__ __forceinline__ void process_page_fp8_k1(
+    const uint8_t *__restrict__ kp, const uint8_t *__restrict__ vp,
+    const uint32_t (&qr)[4][8], float (&o)[4], float &m, float &l,
+    uint16_t *pb16 /* [16] of this warp */, int lane, int j0,
+    bool all_visible, int t, uint32_t tm, int base, int n_sink, int window,
+    float qscale) {
+  const int key = lane >> 1, half = lane & 1;
+  const uint8_t *krow = kp + key * 128 + half * 64;
+  float acc = 0.f, acc2 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(krow + ((c + key) & 3) * 16);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k01 = e4m3x2_h2(wv[i]), k23 = e4m3x2_h2(wv[i] >> 16);
+      const uint32_t q01 = qr[c][2 * i], q23 = qr[c][2 * i + 1];
+      acc = fma_h(acc, (unsigned short)(k01 & 0xffffu), (unsigned short)(q01 & 0xffffu));
+      acc2 = fma_h(acc2, (unsigned short)(k01 >> 16), (unsigned short)(q01 >> 16));
+      acc = fma_h(acc, (unsigned short)(k23 & 0xffffu), (unsigned short)(q23 & 0xffffu));
+      acc2 = fma_h(acc2, (unsigned short)(k23 >> 16), (unsigned short)(q23 >> 16));
+    }
+  }
+  acc += acc2;
+  float sc = (acc + __shfl_xor_sync(kFull, acc, 1)) * qscale;
+  const int jkey = j0 + key;
+  if (!all_visible)
+    sc = key_visible(jkey, t, tm, base, n_sink, window) ? sc : -INFINITY;
+  float pm = sc;
+  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 2));
+  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
+  const float m_new = fmaxf(m, pm);
+  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+  const float pv = ex2(sc - m_use);
+  float ps = half ? 0.f : pv;  // each key once
+  ps += __shfl_xor_sync(kFull, ps, 2);
+  ps += __shfl_xor_sync(kFull, ps, 4);
+  ps += __shfl_xor_sync(kFull, ps, 8);
+  ps += __shfl_xor_sync(kFull, ps, 16);
+  if (m_new != m) {  // warp-uniform
+    const float alpha = ex2(m - m_use);
+    l *= alpha;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] *= alpha;
+    m = m_new;
+  }
+  l += ps;
+  if (!half) pb16[key] = __half_as_ushort(__float2half_rn(pv));
+  __syncwarp();
+#pragma unroll
+  for (int jq = 0; jq < kBlockSize; jq += 4) {
+    const uint2 p4 = *reinterpret_cast<const uint2 *>(pb16 + jq);
+    const unsigned short pj[4] = {(unsigned short)(p4.x & 0xffffu),
+                                  (unsigned short)(p4.x >> 16),
+                                  (unsigned short)(p4.y & 0xffffu),
+                                  (unsigned short)(p4.y >> 16)};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(vp + (jq + u) * 128 + lane * 4);
+      const uint32_t v01 = e4m3x2_h2(w), v23 = e4m3x2_h2(w >> 16);
+      o[0] = fma_h(o[0], (unsigned short)(v01 & 0xffffu), pj[u]);
+      o[1] = fma_h(o[1], (unsigned short)(v01 >> 16), pj[u]);
+      o[2] = fma_h(o[2], (unsigned short)(v23 & 0xffffu), pj[u]);
+      o[3] = fma_h(o[3], (unsigned short)(v23 >> 16), pj[u]);
+    }
+  }
+  __syncwarp();
+}
+
+// --------------------------------------------------------------------------
 // tensor-core consumer work on one page (16 query rows x 16 keys)
 // Lane layout of m16n8k16: g = lane/4 (rows g, g+8), t = lane%4.
 // --------------------------------------------------------------------------
@@ -454,8 +553,15 @@ __device__ __forceinline__ void zero_invalid_rows(unsigned char *vp, int lane,
 // --------------------------------------------------------------------------
 // the kernel
 // --------------------------------------------------------------------------
+// CTAs per SM the registers must allow: three for the single-row paths
+// (their shared-memory rings allow three), two otherwise
 template <typename T, int D, int RB, bool MMA>
-__global__ void __launch_bounds__(kThreads, 2)
+constexpr int min_ctas() {
+  return (!MMA && RB == 1) ? 3 : 2;
+}
+
+template <typename T, int D, int RB, bool MMA>
+__global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
     paged_attention_kernel(const AttnParams p,
                            const __grid_constant__ TensorMaps tm) {
   using C = Cfg<T, D>;
@@ -767,6 +873,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       } else {
         // ---- CUDA-core path ----
+        // FP8 pages, one row, head_dim 128: key per lane (see
+        // process_page_fp8_k1); q kept as fp16 of this lane's half
+        constexpr bool kKeyLane = std::is_same<T, uint8_t>::value && RB == 1 &&
+                                  D == 128;
+        uint32_t qr[4][8];
         float q[RB][VEC], o[RB][VEC], m[RB], l[RB];
         int t[RB];
         uint32_t tm[RB];
@@ -786,9 +897,32 @@ __global__ void __launch_bounds__(kThreads, 2)
             const TQ *qp = static_cast<const TQ *>(p.q) +
                            (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
                            lane * VEC;
-            Vec<TQ, D>::load(qp, q[r]);
+            if constexpr (kKeyLane) {
+              // dims half*64 + ((c + key) & 3)*16 .. +16 of the row, bf16
+              // -> fp16 pairs, in this lane's chunk order
+              const int key = lane >> 1, half = lane & 1;
+              const uint16_t *qrow = static_cast<const uint16_t *>(p.q) +
+                                     (((size_t)b * p.q_len + i) * p.num_q_heads + h) * D +
+                                     half * 64;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
+              for (int c = 0; c < 4; ++c) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    qrow + ((c + key) & 3) * 16);
+                const uint4 a = __ldg(src), b2 = __ldg(src + 1);
+                const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                  const float lo = __uint_as_float(w[k2] << 16);
+                  const float hi = __uint_as_float(w[k2] & 0xffff0000u);
+                  const __half2 hh = __floats2half2_rn(lo, hi);
+                  qr[c][k2] = *reinterpret_cast<const uint32_t *>(&hh);
+                }
+              }
+            } else {
+              Vec<TQ, D>::load(qp, q[r]);
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) q[r][e] *= p.qscale;
+            }
             t[r] = t0 + i;
             tm[r] = row_tree_bits(p, b, i);
           }
@@ -816,10 +950,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool all_vis = (j1 <= t_min) &&
                                  (p.window == 0 || j1 < p.n_sink ||
                                   j0 > t_max - p.window);
-            process_page_fma<T, D, RB>(
-                reinterpret_cast<const T *>(sm.kv[s][0]),
-                reinterpret_cast<const T *>(sm.kv[s][1]), q, o, m, l, pbuf,
-                lane, j0, all_vis, t, tm, t0, p.n_sink, p.window);
+            if constexpr (kKeyLane)
+              process_page_fp8_k1(
+                  reinterpret_cast<const uint8_t *>(sm.kv[s][0]),
+                  reinterpret_cast<const uint8_t *>(sm.kv[s][1]), qr,
+                  reinterpret_cast<float (&)[4]>(o[0]), m[0], l[0],
+                  reinterpret_cast<uint16_t *>(pbuf), lane, j0, all_vis,
+                  t[0], tm[0], t0, p.n_sink, p.window, p.qscale);
+            else
+              process_page_fma<T, D, RB>(
+                  reinterpret_cast<const T *>(sm.kv[s][0]),
+                  reinterpret_cast<const T *>(sm.kv[s][1]), q, o, m, l, pbuf,
+                  lane, j0, all_vis, t, tm, t0, p.n_sink, p.window);
           }
           if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
