@@ -667,55 +667,80 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
             phys[k4] = __ldg(p.block_table + (size_t)b * p.max_blocks + lb);
           }
         }
+        // Pages go out in batches, every step spread over the lanes: lane
+        // 0 waits for the next stage, lane i tests whether stage c + i is
+        // free too, the run of free stages from c is the batch; lane i arms
+        // stage c + i, and the batch's K and V copies are issued one per
+        // lane.  One thread doing all of it page by page cannot keep 2 KB
+        // FP8 pages coming: each barrier operation and copy it issues
+        // waits for the one before.
+        constexpr int CPP = MMA ? 2 * (D / kBoxElems) : 2;  // copies per page
+        constexpr int MAXB = (32 / CPP) < STAGES ? (32 / CPP) : STAGES;
+        const int part = lane % CPP;
 #pragma unroll
         for (int k4 = 0; k4 < kTableChunk / 32; ++k4) {
-          for (int kk = 0; kk < 32; ++kk) {
+          for (int kk = 0; kk < 32;) {
             const int k = k0 + k4 * 32 + kk;
             if (k >= n_pages) break;
-            const int ph = __shfl_sync(kFull, phys[k4], kk);
 #ifdef SVP_TEST_STALL_AFTER
             // test builds only: the producer stops after a few pages and
             // waits on a barrier nothing arrives on, so every role's wait
             // runs out and takes its timeout path
-            if (c == SVP_TEST_STALL_AFTER) {
+            if (c >= SVP_TEST_STALL_AFTER) {
               if (lane == 0) ok = mbar_wait(&sm.stall, 0);
               ok = __shfl_sync(kFull, ok, 0);
               if (!ok) break;
             }
 #endif
-            if (lane == 0) {
-              const int s = c % STAGES;
-              if (!mbar_wait(&sm.empty[s], ((c / STAGES) & 1) ^ 1)) {
-                ok = false;
-              } else if (ph < 0 || ph >= p.num_blocks) {
+            const int left = min(min(32 - kk, n_pages - k), MAXB);
+            // lane i: page c + i's block (arming), and the page of this
+            // lane's copy
+            const int ph_i = __shfl_sync(kFull, phys[k4], min(kk + lane, 31));
+            const int pg = lane / CPP;
+            const int ph_c = __shfl_sync(kFull, phys[k4], min(kk + pg, 31));
+            bool ready = false;
+            if (lane == 0)
+              ready = mbar_wait(&sm.empty[c % STAGES], ((c / STAGES) & 1) ^ 1);
+            ok = __shfl_sync(kFull, ready, 0);
+            if (!ok) break;
+            if (lane > 0 && lane < left)
+              ready = mbar_ready(&sm.empty[(c + lane) % STAGES],
+                                 (((c + lane) / STAGES) & 1) ^ 1);
+            const unsigned run = __ballot_sync(kFull, lane < left && ready);
+            const int n = __ffs(~run) - 1;  // stages c .. c + n - 1 are free
+            if (lane < n) {
+              const int s = (c + lane) % STAGES;
+              if (ph_i >= 0 && ph_i < p.num_blocks) {
+                sm.stage_ok[s] = 1;
+                mbar_arrive_expect_tx(&sm.full[s], 2 * C::PAGE_BYTES);
+              } else {
                 raise_flag(SVP_DEV_BAD_BLOCK_ID);
                 sm.stage_ok[s] = 0;
                 mbar_arrive(&sm.full[s]);
-              } else {
-                sm.stage_ok[s] = 1;
-                mbar_arrive_expect_tx(&sm.full[s], 2 * C::PAGE_BYTES);
-                if constexpr (MMA) {
-                  const int y = (ph * p.num_kv_heads + g) * kBlockSize;
-#pragma unroll
-                  for (int bx = 0; bx < D / kBoxElems; ++bx) {
-                    tma_load_2d(sm.kv[s][0] + bx * kBoxBytes, &tm.k,
-                                bx * kBoxElems, y, &sm.full[s]);
-                    tma_load_2d(sm.kv[s][1] + bx * kBoxBytes, &tm.v,
-                                bx * kBoxElems, y, &sm.full[s]);
-                  }
-                } else {
-                  const size_t off = (size_t)ph * p.num_kv_heads * C::PAGE_ELEMS +
-                                     head_off;
-                  bulk_g2s(sm.kv[s][0], static_cast<const T *>(p.k_cache) + off,
-                           C::PAGE_BYTES, &sm.full[s]);
-                  bulk_g2s(sm.kv[s][1], static_cast<const T *>(p.v_cache) + off,
-                           C::PAGE_BYTES, &sm.full[s]);
-                }
               }
             }
-            ok = __shfl_sync(kFull, ok, 0);
-            if (!ok) break;
-            ++c;
+            __syncwarp();
+            if (pg < n && ph_c >= 0 && ph_c < p.num_blocks) {
+              const int s = (c + pg) % STAGES;
+              if constexpr (MMA) {
+                const int y = (ph_c * p.num_kv_heads + g) * kBlockSize;
+                const int bx = part >> 1;
+                if (part & 1)
+                  tma_load_2d(sm.kv[s][1] + bx * kBoxBytes, &tm.v,
+                              bx * kBoxElems, y, &sm.full[s]);
+                else
+                  tma_load_2d(sm.kv[s][0] + bx * kBoxBytes, &tm.k,
+                              bx * kBoxElems, y, &sm.full[s]);
+              } else {
+                const size_t off = (size_t)ph_c * p.num_kv_heads * C::PAGE_ELEMS +
+                                   head_off;
+                bulk_g2s(sm.kv[s][part],
+                         static_cast<const T *>(part ? p.v_cache : p.k_cache) + off,
+                         C::PAGE_BYTES, &sm.full[s]);
+              }
+            }
+            c += n;
+            kk += n;
           }
           if (!ok) break;
         }

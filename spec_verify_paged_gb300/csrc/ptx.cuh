@@ -87,6 +87,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// Non-blocking: whether the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_ready(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // mbar_wait with the drain limit (see SVP_DRAIN_WAIT_NS).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar,
                                                 uint32_t parity) {
