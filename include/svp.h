@@ -356,16 +356,18 @@ int spec_accept_tree(int batch, int num_nodes, int vocab,
  * decoding", sections "The problem: the GPU bubble" and "Mechanism one:
  * ping-pong slots").  A runner owns two slots; each has pinned host buffers
  * for the step's inputs and outputs and device copies of them, and one CUDA
- * graph, captured at creation, that copies the slot's inputs to the device
- * and runs kv_append (the q_len new rows), paged_decode_attention and, with
- * num_draft > 0, spec_accept (spec_accept_ex with epilogue options) -- or,
- * for a draft tree (tree_nodes > 0), paged_tree_attention and
- * spec_accept_tree.  svp_step_launch replays a slot's graph on
- * the runner's compute stream and queues the copy of its outputs back to
- * the slot on a separate copy stream, ordered after an event recorded when
- * that step's outputs are written -- so the next step (the other slot) can
- * run while the copy is in flight.  The host fills one slot while the GPU
- * works on the other.
+ * graph, captured at creation, that runs kv_append (the q_len new rows),
+ * paged_decode_attention and, with num_draft > 0, spec_accept
+ * (spec_accept_ex with epilogue options) -- or, for a draft tree
+ * (tree_nodes > 0), paged_tree_attention and spec_accept_tree -- on the
+ * slot's device buffers.  svp_step_launch copies the slot's inputs to the
+ * device on an upload stream (once the slot's previous step has finished
+ * with them, so the upload overlaps the other slot's step), replays the
+ * slot's graph on the runner's compute stream after that copy, and queues
+ * the copy of its outputs back to the slot on a separate copy stream,
+ * ordered after an event recorded when that step's outputs are written --
+ * so the next step (the other slot) can run while the copy is in flight.
+ * The host fills one slot while the GPU works on the other.
  * Protocol: write a slot's inputs only before its first launch or after
  * svp_step_wait on it returned; read its outputs after svp_step_wait.
  * Launching a slot again waits (on the device) for its previous result

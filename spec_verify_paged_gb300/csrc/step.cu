@@ -10,7 +10,10 @@
 // while the GPU runs the other; the device-to-host copy of a step's result
 // runs on a separate copy stream, ordered after an event recorded when that
 // step's outputs are written (not after work queued behind it); a slot is
-// reused only once its result copy has completed.
+// reused only once its result copy has completed.  The slot's input copy
+// runs on an upload stream of its own, ordered only after the slot's
+// previous step has finished with its inputs, so the next step's upload
+// overlaps the current step's kernels.
 //
 // Host code only: the kernels are the library's own entry points, called
 // while the slot's graph is captured.
@@ -25,7 +28,7 @@
 
 struct svp_step {
   svp_step_desc desc;
-  cudaStream_t compute = nullptr, copy = nullptr;
+  cudaStream_t compute = nullptr, copy = nullptr, upload = nullptr;
   void *workspace = nullptr;
   size_t ws_bytes = 0;
   size_t off[SVP_STEP_NUM_FIELDS] = {};    // offsets in the input / output blocks
@@ -37,6 +40,7 @@ struct svp_step {
     cudaGraphExec_t exec = nullptr;
     cudaEvent_t done = nullptr;  // the step's outputs are written
     cudaEvent_t out = nullptr;   // its result copy has completed
+    cudaEvent_t in = nullptr;    // its input copy has completed
     bool launched = false;
   } slot[2];
 };
@@ -55,6 +59,7 @@ void release(svp_step *s) {
     if (sl.exec) cudaGraphExecDestroy(sl.exec);
     if (sl.done) cudaEventDestroy(sl.done);
     if (sl.out) cudaEventDestroy(sl.out);
+    if (sl.in) cudaEventDestroy(sl.in);
     if (sl.host_in) cudaFreeHost(sl.host_in);
     if (sl.host_out) cudaFreeHost(sl.host_out);
     if (sl.dev_in) cudaFree(sl.dev_in);
@@ -63,12 +68,13 @@ void release(svp_step *s) {
   if (s->workspace) cudaFree(s->workspace);
   if (s->compute) cudaStreamDestroy(s->compute);
   if (s->copy) cudaStreamDestroy(s->copy);
+  if (s->upload) cudaStreamDestroy(s->upload);
   delete s;
 }
 
-// Captures slot i's step on the compute stream: the input copy from the
-// pinned slot, then kv_append, attention and (with drafts or a tree) the
-// acceptance step on the slot's device buffers.
+// Captures slot i's step on the compute stream: kv_append, attention and
+// (with drafts or a tree) the acceptance step on the slot's device buffers
+// (the input copy from the pinned slot is issued at launch).
 int capture_slot(svp_step *s, int i) {
   svp_step::Slot &sl = s->slot[i];
   const svp_step_desc &d = s->desc;
@@ -81,12 +87,7 @@ int capture_slot(svp_step *s, int i) {
   if (cudaStreamBeginCapture(s->compute, cudaStreamCaptureModeRelaxed) !=
       cudaSuccess)
     return SVP_ERR_CUDA;
-  int st = SVP_OK;
-  if (cudaMemcpyAsync(sl.dev_in, sl.host_in, s->in_bytes,
-                      cudaMemcpyHostToDevice, s->compute) != cudaSuccess)
-    st = SVP_ERR_CUDA;
-  if (st == SVP_OK)
-    st = kv_append(&dims, in(SVP_STEP_K_NEW), in(SVP_STEP_V_NEW), d.k_cache,
+  int st = kv_append(&dims, in(SVP_STEP_K_NEW), in(SVP_STEP_V_NEW), d.k_cache,
                    d.v_cache, (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
                    (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, s->compute);
   const bool tree = d.tree_nodes > 0;
@@ -204,6 +205,7 @@ int svp_step_create(const svp_step_desc *desc, svp_step **out) {
   int st = SVP_OK;
   if (cudaStreamCreateWithFlags(&s->compute, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&s->upload, cudaStreamNonBlocking) != cudaSuccess ||
       cudaMalloc(&s->workspace, ws) != cudaSuccess)
     st = SVP_ERR_CUDA;
   for (int i = 0; i < 2 && st == SVP_OK; ++i) {
@@ -213,7 +215,8 @@ int svp_step_create(const svp_step_desc *desc, svp_step **out) {
         cudaMalloc((void **)&sl.dev_in, s->in_bytes) != cudaSuccess ||
         cudaMalloc((void **)&sl.dev_out, s->out_bytes) != cudaSuccess ||
         cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&sl.out, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&sl.out, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sl.in, cudaEventDisableTiming) != cudaSuccess) {
       st = SVP_ERR_CUDA;
       break;
     }
@@ -241,10 +244,19 @@ void *svp_step_host_buffer(svp_step *s, int slot, int field, size_t *bytes) {
 int svp_step_launch(svp_step *s, int slot) {
   if (!s || slot < 0 || slot > 1) return SVP_ERR_INVALID_ARG;
   svp_step::Slot &sl = s->slot[slot];
+  // the input copy: once the slot's previous step has finished with its
+  // inputs, on the upload stream, so it overlaps the other slot's kernels
+  if (sl.launched && cudaStreamWaitEvent(s->upload, sl.done, 0) != cudaSuccess)
+    return SVP_ERR_CUDA;
+  if (cudaMemcpyAsync(sl.dev_in, sl.host_in, s->in_bytes,
+                      cudaMemcpyHostToDevice, s->upload) != cudaSuccess ||
+      cudaEventRecord(sl.in, s->upload) != cudaSuccess)
+    return SVP_ERR_CUDA;
   // the slot's previous result must have left its device buffers
   if (sl.launched && cudaStreamWaitEvent(s->compute, sl.out, 0) != cudaSuccess)
     return SVP_ERR_CUDA;
-  if (cudaGraphLaunch(sl.exec, s->compute) != cudaSuccess ||
+  if (cudaStreamWaitEvent(s->compute, sl.in, 0) != cudaSuccess ||
+      cudaGraphLaunch(sl.exec, s->compute) != cudaSuccess ||
       cudaEventRecord(sl.done, s->compute) != cudaSuccess ||
       cudaStreamWaitEvent(s->copy, sl.done, 0) != cudaSuccess ||
       cudaMemcpyAsync(sl.host_out, sl.dev_out, s->out_bytes,
@@ -266,7 +278,8 @@ cudaStream_t svp_step_stream(svp_step *s) { return s ? s->compute : nullptr; }
 
 int svp_step_destroy(svp_step *s) {
   if (!s) return SVP_OK;
-  const bool ok = cudaStreamSynchronize(s->compute) == cudaSuccess &&
+  const bool ok = cudaStreamSynchronize(s->upload) == cudaSuccess &&
+                  cudaStreamSynchronize(s->compute) == cudaSuccess &&
                   cudaStreamSynchronize(s->copy) == cudaSuccess;
   release(s);
   return ok ? SVP_OK : SVP_ERR_CUDA;
