@@ -587,6 +587,12 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
   const int groups_per_seq = p.num_kv_heads * p.n_rg;
 
   // ---- set-up: barriers and the per-sequence unit prefix ----
+  if constexpr (MMA) {
+    if (tid == 32) {
+      prefetch_tensormap(&tm.k);
+      prefetch_tensormap(&tm.v);
+    }
+  }
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);

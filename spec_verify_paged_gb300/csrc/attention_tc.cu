@@ -19,7 +19,10 @@
 // and both K and V feed the tensor core straight from the TMA-written
 // 128-byte-swizzled tiles.  Accumulators live in tensor memory (TMEM).
 // A unit is N = 16 or 32 rows of a kv head; beyond 32 rows it is 64 rows
-// in two 32-row groups (DUAL), so each K/V tile is read once for all 64.
+// in two 32-row groups (DUAL), so each K/V tile is read once for all 64,
+// and the tensor core takes both groups in one 64-column MMA per k-step
+// (the A operand, K or V, is fetched from shared memory once per tile:
+// with 32-column MMAs that fetch, not the arithmetic, set the MMA time).
 //
 // Warp roles (320 threads, one CTA per SM):
 //   warps 0-7  softmax and epilogue, as two groups of four warps.  One row
@@ -28,9 +31,10 @@
 //              barriers overlap the other's; their states merge by
 //              log-sum-exp at the end of a segment.  DUAL: both groups take
 //              every tile, one 32-row group each, with S double-buffered;
-//              each group's P, and at a segment's end its staged output,
-//              go into the tile's K buffer (read by then), so the ring
-//              keeps three stages beside the second Q tile.
+//              the groups' P (rows 0-31 and 32-63 of one 64-row operand),
+//              and at a segment's end their staged outputs, go into the
+//              tile's K buffer (read by then), so the ring keeps three
+//              stages beside the 64-row Q tile.
 //              S is read in the mma-fragment layout (a thread holds four
 //              keys of eight rows): row max and sum fold over the four keys
 //              in registers, then a short transposing butterfly and a
@@ -85,15 +89,18 @@ constexpr int kTcBatchCap = 512;  // sequences per launch (prefix in smem)
 
 // DUAL: a unit holds 2N rows (two row groups of N); both softmax groups
 // take every tile, one row group each, so each K/V tile is read once for
-// 2N rows.  Its second Q tile is paid for by keeping P (and a segment's
-// staged output) in the stage's K tile, which both groups' S MMAs have
-// finished reading by then: no separate P buffers.
+// 2N rows.  Its 2N-row Q tile is paid for by keeping P (and a segment's
+// staged output) in the stage's K tile, which the tile's S MMAs have
+// finished reading by then: no separate P buffers.  Q and P are 2N-row
+// K-major operands (group g's rows at g N), so one MMA per k-step serves
+// both groups.
 template <int N, bool DUAL = false>
 struct TcSmem {
   static constexpr int ST = kStages;
   static constexpr int PB = N * kTileKeys * 2;  // one group's P tile (bf16)
   alignas(1024) unsigned char k[ST][kTileBytes];
   alignas(1024) unsigned char v[ST][kTileBytes];
+  // Q of a unit's rows: two 64-dim halves, each [rows][128 B] swizzled
   alignas(1024) unsigned char q[(DUAL ? 2 : 1) * N * kD * 2];
   alignas(1024) unsigned char pb[kGroups][DUAL ? 16 : PB];  // P per group
   alignas(16) float red_m[kGroups][4][N];
@@ -103,6 +110,7 @@ struct TcSmem {
   alignas(16) float xs_m[2][N], xs_l[2][N];  // group 1's state per segment
   alignas(16) float f0[N], f1[N];          // combine weights of the groups
   alignas(16) float lse_st[kGroups][N];    // a split partial's LSEs
+  uint32_t tbits[kGroups][N];  // draft-tree ancestor bits of the rows
   UnitInfo unit[kUnitRing];
   int stage_mask[ST];  // bit k: page k of the tile was copied
   uint64_t full[ST], empty[ST];
@@ -135,7 +143,9 @@ static_assert(tc_smem_bytes<16>(kTcBatchCap + 1) <= 227 * 1024,
 static_assert(tc_smem_bytes<32, true>(kTcBatchCap + 1) <= 227 * 1024,
               "shared memory of a 64-row CTA");
 static_assert(TcSmem<32, true>::PB * kGroups <= kTileBytes,
-              "both groups' P tiles fit one K tile");
+              "the 64-row P operand fits one K tile");
+static_assert(32 * kD * 4 * kGroups <= kTileBytes,
+              "both groups' fp32 output rows fit one K tile");
 
 __device__ __forceinline__ void raise_tc(unsigned f) {
   atomicOr(&g_status_attn_tc, f);
@@ -383,11 +393,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// K and V caches as 2-D tensors of 16-row pages; Q as rows of 128 dims.
+// K and V caches as 2-D tensors of 16-row pages; Q either as a 3-D tensor
+// whose box is a unit's rows (q_unit_box: whole GQA groups of a unit's
+// positions, or a whole unit of one position's heads) or as rows of 128
+// dims copied one per box.
 struct TcMaps {
   CUtensorMap k;
   CUtensorMap v;
   CUtensorMap q;
+  int q_unit_box;
 };
 
 }  // namespace
@@ -406,22 +420,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int ST = Smem::ST;
   constexpr int UR = DUAL ? 2 * N : N;  // rows of a unit
   // S[group], O[group], X[2] (group 1's o handed to group 0), N columns
-  // each; DUAL: S[group][2] at (2 group + tile parity) N, O[group] at
-  // (4 + group) N
+  // each; DUAL: S[tile parity] of both groups (2N columns, group g's at
+  // g N) at parity 2N, O of both groups at 4N (group g's at (4 + g) N)
   constexpr uint32_t kTmemCols = 6 * N <= 128 ? 128 : 256;
-  constexpr uint32_t kIdescS = idesc_bf16(kTileKeys, N, 0, 0);
-  constexpr uint32_t kIdescO = idesc_bf16(kD, N, 1, 0);
+  constexpr uint32_t kIdescS = idesc_bf16(kTileKeys, UR, 0, 0);
+  constexpr uint32_t kIdescO = idesc_bf16(kD, UR, 1, 0);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int groups_per_seq = p.num_kv_heads * p.n_rg;
 
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tensormap(&tm.q);
+    prefetch_tensormap(&tm.k);
+    prefetch_tensormap(&tm.v);
+  }
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(&sm.full[s], 1);
-      // DUAL: one commit after each group's P V, or, for a segment's last
-      // tile, each group's arrival once its staged output has been read
+      // DUAL: two commits after the tile's P V (one per group's share),
+      // or, for a segment's last tile, each group's arrival once its
+      // staged output has been read
       mbar_init(&sm.empty[s], DUAL ? 2 : 1);
     }
     for (int i = 0; i < (int)(sizeof(sm.s_full) / sizeof(uint64_t)); ++i)
@@ -520,19 +540,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int seg_c0 = c;  // the segment's first tile
       auto issue_q = [&]() {
         q_issued = us;
-        const int vr = min(UR, p.rows - seg.rg * UR);
-        if (lane == 0) mbar_arrive_expect_tx(&sm.q_full, vr * kD * 2);
-        __syncwarp();
-        for (int r = lane; r < vr; r += 32) {
-          // row r of the unit: Q tile r / N (DUAL), row r % N of it
-          unsigned char *qt = sm.q + (r / N) * (N * kD * 2);
-          const int rr = r % N;
-          const int gr = seg.rg * UR + r;
-          const int i = gr / p.group, h = seg.g * p.group + gr % p.group;
-          const int y = (seg.b * p.q_len + i) * p.num_q_heads + h;
-          tma_load_2d(qt + rr * 128, &tm.q, 0, y, &sm.q_full);
-          tma_load_2d(qt + N * 128 + rr * 128, &tm.q, kBoxElems, y,
-                      &sm.q_full);
+        if (tm.q_unit_box) {
+          // the unit's UR rows (row r = position r / group, head r % group
+          // from its first row) in one box per 64-dim half; rows past the
+          // valid ones hold other rows' queries (or zeros past the tensor)
+          // and are never written out.  One copy each instead of one per
+          // row: a warp issues bulk copies one at a time
+          if (lane == 0) {
+            const int gr0 = seg.rg * UR;
+            const int y = seg.g * p.group + gr0 % p.group;
+            const int z = seg.b * p.q_len + gr0 / p.group;
+            mbar_arrive_expect_tx(&sm.q_full, UR * kD * 2);
+            tma_load_3d(sm.q, &tm.q, 0, y, z, &sm.q_full);
+            tma_load_3d(sm.q + UR * 128, &tm.q, kBoxElems, y, z, &sm.q_full);
+          }
+          __syncwarp();
+        } else {
+          const int vr = min(UR, p.rows - seg.rg * UR);
+          if (lane == 0) mbar_arrive_expect_tx(&sm.q_full, vr * kD * 2);
+          __syncwarp();
+          for (int r = lane; r < vr; r += 32) {
+            // row r of the unit: 128 B in each 64-dim half of [UR][128 B]
+            const int gr = seg.rg * UR + r;
+            const int i = gr / p.group, h = seg.g * p.group + gr % p.group;
+            const int y = (seg.b * p.q_len + i) * p.num_q_heads + h;
+            tma_load_2d(sm.q + r * 128, &tm.q, 0, y, &sm.q_full);
+            tma_load_2d(sm.q + UR * 128 + r * 128, &tm.q, kBoxElems, y,
+                        &sm.q_full);
+          }
         }
         q_pending = false;
       };
@@ -640,15 +675,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ======================= MMA issuer (event driven) =======================
     if (lane == 0) {
       if constexpr (DUAL) {
-        // both groups take every tile: S(c) of both groups (buffers c & 1)
-        // once P(c-2) of both was written, one commit; P V(c) of gi once
-        // P(c) of gi was written, reading gi's P from stage c's K tile;
-        // a commit to the stage's empty barrier after each P V, except on a
+        // both groups take every tile, one 2N-column MMA per k-step for
+        // both: S(c) (buffer c & 1) once P(c-2) of both was written, one
+        // commit; P V(c) once P(c) of both was written, reading the P
+        // operand from stage c's K tile, then a commit to each group's O
+        // barrier and two to the stage's empty barrier, except on a
         // segment's last tile, whose stage the groups release after their
         // outputs staged there have been read
         bool ok = true;
         int c_s = 0;                 // next tile whose S is issued
-        int c_p[2] = {0, 0};         // next tile whose P V is issued, by group
+        int c_p = 0;                 // next tile whose P V is issued
         int p_obs[2] = {0, 0};       // tiles whose P is known written, by group
         int us = 0;
         int left = 0, tau = 0, cur_pages = 0;
@@ -678,18 +714,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               (!first || mbar_test(&sm.q_full, (us - 1) & 1))) {
             tc_fence_after();
             const uint32_t ka = smem_u32(sm.k[c_s % ST]);
+            const uint32_t qa = smem_u32(sm.q);
 #pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-              const uint32_t qa = smem_u32(sm.q + gi * (N * kD * 2));
-#pragma unroll
-              for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint64_t a =
-                    sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
-                const uint64_t bq =
-                    sw128_desc(qa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-                tc_mma(tmem + (2 * gi + (c_s & 1)) * N, a, bq, kIdescS,
-                       ks > 0 ? 1u : 0u);
-              }
+            for (int ks = 0; ks < kD / 16; ++ks) {
+              const uint64_t a =
+                  sw128_desc(ka + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
+              const uint64_t bq =
+                  sw128_desc(qa + (ks >> 2) * (UR * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma(tmem + (c_s & 1) * UR, a, bq, kIdescS, ks > 0 ? 1u : 0u);
             }
             // one commit for both groups: when it arrives, K of the tile is
             // no longer read and may take P; S(c + 2) waits for both P(c),
@@ -710,27 +742,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               ++p_obs[gi];
               prog = true;
             }
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            if (c_p[gi] < p_obs[gi]) {
-              tc_fence_after();
-              const int c = c_p[gi];
-              const uint32_t va = smem_u32(sm.v[c % ST]);
-              const uint32_t pa = smem_u32(sm.k[c % ST]) + gi * Smem::PB;
-              const int npg = npg_ring[c & 7];
-              for (int ks = 0; ks < npg; ++ks) {
-                const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
-                const uint64_t bp =
-                    sw128_desc(pa + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
-                tc_mma(tmem + (4 + gi) * N, a, bp, kIdescO, ks > 0 ? 1u : 0u);
-              }
-              tc_commit(&sm.o_full[gi]);
-              if (!last_ring[c & 7]) tc_commit(&sm.empty[c % ST]);
-              ++c_p[gi];
-              prog = true;
+          if (c_p < p_obs[0] && c_p < p_obs[1]) {
+            tc_fence_after();
+            const int c = c_p;
+            const uint32_t va = smem_u32(sm.v[c % ST]);
+            const uint32_t pa = smem_u32(sm.k[c % ST]);
+            const int npg = npg_ring[c & 7];
+            for (int ks = 0; ks < npg; ++ks) {
+              const uint64_t a = sw128_desc(va + ks * 2048, kHalfBytes, 1024);
+              const uint64_t bp =
+                  sw128_desc(pa + (ks >> 2) * (UR * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma(tmem + 4 * N, a, bp, kIdescO, ks > 0 ? 1u : 0u);
             }
+            tc_commit(&sm.o_full[0]);
+            tc_commit(&sm.o_full[1]);
+            if (!last_ring[c & 7]) {  // one arrival per group's share
+              tc_commit(&sm.empty[c % ST]);
+              tc_commit(&sm.empty[c % ST]);
+            }
+            ++c_p;
+            prog = true;
           }
-          if (no_more && left == 0 && c_p[0] == c_s && c_p[1] == c_s) break;
+          if (no_more && left == 0 && c_p == c_s) break;
           if (prog) {
             last = globaltimer();
           } else if (sm.abort_flag || globaltimer() - last > SVP_WAIT_NS) {
@@ -892,6 +925,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // first global row of the group's N rows
       const int row0 = DUAL ? rg * UR + gi * N : rg * N;
       const int vrows = max(0, min(N, p.rows - row0));
+      // the rows' draft-tree ancestor bits (all ones without a tree, or
+      // past the last query position), read here so that the masked tiles
+      // at the segment's end find them in shared memory
+      if (gt < N) {
+        const int i = (row0 + gt) / p.group;
+        sm.tbits[gi][gt] = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
+      }
+      named_bar(gbar, kGroupThreads);
 
       float o[N];
 #pragma unroll
@@ -908,7 +949,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         got = got && mbar_wait(&sm.full[s], (c / ST) & 1);
         tc_fence_after();
         const uint32_t tS =
-            tmem + lane_base + (DUAL ? 2 * gi + (c & 1) : gi) * N;
+            tmem + lane_base + (DUAL ? 2 * (c & 1) + gi : gi) * N;
         // S of the tile: key gw 32 + 8 q + lane / 4, query row
         // 8 j + 2 (lane % 4) + e of the group's N rows
         constexpr int J = N / 8;
@@ -963,9 +1004,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < J; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int i = (row0 + 8 * j + 2 * (lane & 3) + e) / p.group;
-              pos[j][e] = t0 + i;
-              tb[j][e] = i < p.q_len ? row_tree_bits(p, b, i) : ~0u;
+              const int r = 8 * j + 2 * (lane & 3) + e;
+              pos[j][e] = t0 + (row0 + r) / p.group;
+              tb[j][e] = sm.tbits[gi][r];
             }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -1052,25 +1093,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float cs = row_reduce<J, false>(sm_, lane);
           if (J == 4 || (lane & 4) == 0) sm.red_l[gi][gw][row_of<J>(lane)] = cs;
         }
-        // ---- the previous tile's O leaves the buffer before P is written:
-        // its P V has then finished reading this group's P buffer too ----
+        // ---- the previous tile's O leaves the buffer before P is written
+        // (the next P V overwrites it; without DUAL that P V has then also
+        // finished reading this group's P buffer) ----
         if (prev >= 0) ok = fold_o(prev, o) && ok;
         // group 0 stages the previous segment's output in both P buffers:
         // group 1 writes P again once the TMA engine has read it
         if (!DUAL && gi == 1 && prev < 0 && us > 0)
           ok = __all_sync(kFull, mbar_wait(&sm.stg_free, (us - 1) & 1)) && ok;
         // P as bf16, K-major and swizzled: per 8-row block, four 8x8 blocks
-        // (keys gw 32 + 8 i ..) stored transposed.  DUAL: in this group's
-        // part of the stage's K tile, which both groups' S MMAs have read
-        const uint32_t pbase = DUAL ? smem_u32(sm.k[s]) + gi * Smem::PB
-                                    : smem_u32(sm.pb[gi]);
+        // (keys gw 32 + 8 i ..) stored transposed.  DUAL: rows gi N .. of
+        // the 2N-row operand in the stage's K tile, which the tile's S MMAs
+        // have read
+        const uint32_t pbase = DUAL ? smem_u32(sm.k[s]) : smem_u32(sm.pb[gi]);
+        const int prow0 = DUAL ? gi * N : 0;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
           uint32_t fr[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) fr[q] = pack_bf16(sv[q][j][0], sv[q][j][1]);
           stmatrix_x4_trans(
-              pbase + kmajor_off<N>(8 * j + (lane & 7), gw * 32 + 8 * (lane >> 3)),
+              pbase + kmajor_off<UR>(prow0 + 8 * j + (lane & 7),
+                                     gw * 32 + 8 * (lane >> 3)),
               fr);
         }
         fence_proxy_async_smem();  // P and zeroed V rows -> tensor core
@@ -1092,11 +1136,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int xk = us & 1;
       const uint32_t tX = tmem + lane_base + (4 + xk) * N;
       if constexpr (DUAL) {
-        // ---- epilogue of this group's N rows: no hand-over; staged in the
-        // group's part of its last tile's K, where that tile's P was (its
-        // P V has completed: the fold above waited for it); the stage goes
-        // back to the producer once the stores have read it ----
-        unsigned char *stg = sm.k[prev % ST] + gi * Smem::PB;
+        // ---- epilogue of this group's N rows: no hand-over; staged in
+        // the group's half of its last tile's K, where that tile's P was
+        // (the tile's P V, which read both groups' P, has completed: the
+        // fold above waited for it), and written out by one bulk copy (a
+        // partial's rows are consecutive) or one per query position; the
+        // stage goes back to the producer once both groups' stores have
+        // read it ----
+        unsigned char *stg = sm.k[prev % ST] + gi * (kTileBytes / 2);
         const bool single = ui.f == ui.l;
         const size_t pslot = (size_t)(2 * blockIdx.x + ui.slot);
         float *fw = gi == 0 ? sm.f0 : sm.f1;
@@ -1135,28 +1182,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bulk_wait_read();
           }
         } else {
-          // fp32 rows of 128 dims in two 64-dim halves: [N][64] per pass,
-          // one 256-byte copy per row, issued by the row's thread
+          // fp32 rows [N][128]: the group's rows of this CTA's partial slot
           float *stg32 = reinterpret_cast<float *>(stg);
-          for (int hh = 0; hh < 2; ++hh) {
-            if ((gt >> 6) == hh) {
 #pragma unroll
-              for (int n = 0; n < N; ++n)
-                stg32[n * 64 + (gt & 63)] = o[n] * fw[n];
-            }
-            fence_proxy_async_smem();
-            named_bar(gbar, kGroupThreads);
-            if (gt < N) {
-              bulk_s2g(p.part_o + (pslot * UR + gi * N + gt) * kD + hh * 64,
-                       stg32 + gt * 64, 64 * 4);
-              if (hh == 0 && gt == 0)
-                bulk_s2g(p.part_lse + pslot * UR + gi * N, sm.lse_st[gi], N * 4);
-              bulk_commit();
-              bulk_wait_read();
-            }
-            named_bar(gbar, kGroupThreads);
+          for (int n = 0; n < N; ++n) stg32[n * kD + gt] = o[n] * fw[n];
+          fence_proxy_async_smem();
+          named_bar(gbar, kGroupThreads);
+          if (gt == 0) {
+            bulk_s2g(p.part_o + (pslot * UR + gi * N) * kD, stg32, N * kD * 4);
+            bulk_s2g(p.part_lse + pslot * UR + gi * N, sm.lse_st[gi], N * 4);
+            bulk_commit();
+            bulk_wait_read();
+            if (gi == 0) record_split(p, ui, blockIdx.x);
           }
-          if (gi == 0 && gt == 0) record_split(p, ui, blockIdx.x);
         }
         // fw and the staging area are rewritten only after this barrier;
         // then the last tile's stage may be refilled
@@ -1317,10 +1355,25 @@ static cudaError_t launch_tc(const AttnParams &p, int grid, cudaStream_t st) {
   const size_t smem = tc_smem_bytes<N, DUAL>((int)tc_batch_bucket(p.batch));
   TcMaps tm;
   memset(&tm, 0, sizeof tm);
+  // a unit's rows as one box: whole GQA groups of UR / group positions, or
+  // UR heads of one position (every unit then starts on a box boundary)
+  constexpr int UR = DUAL ? 2 * N : N;
+  const long long positions = (long long)p.batch * p.q_len;
+  int bh = 0, bp = 0;
+  if (p.group <= UR && UR % p.group == 0) {
+    bh = p.group;
+    bp = UR / p.group;
+  } else if (p.group > UR && p.group % UR == 0) {
+    bh = UR;
+    bp = 1;
+  }
+  tm.q_unit_box = bh > 0 && bp <= positions;
   if (!cached_map(&tm.k, 0, p.k_cache, p.num_blocks, p.num_kv_heads, kD) ||
       !cached_map(&tm.v, 0, p.v_cache, p.num_blocks, p.num_kv_heads, kD) ||
-      !cached_map(&tm.q, 1, p.q, (long long)p.batch * p.q_len * p.num_q_heads,
-                  0, kD))
+      !(tm.q_unit_box
+            ? cached_map(&tm.q, 2, p.q, positions, p.num_q_heads, kD,
+                         bh * 65536 + bp)
+            : cached_map(&tm.q, 1, p.q, positions * p.num_q_heads, 0, kD)))
     return cudaErrorInvalidValue;
   return launch_pdl(paged_attention_tc_kernel<N, DUAL>, (unsigned)grid,
                     (unsigned)kTcThreads, smem, st, p, tm);

@@ -116,6 +116,24 @@ __device__ __forceinline__ void store_out(uint16_t *p, float v) {
   *p = *reinterpret_cast<uint16_t *>(&h);
 }
 
+// Fetches a tensor map (a kernel parameter) into the TMA unit's cache ahead
+// of its first copy; it depends on no earlier kernel, so it may be issued
+// before the grid-dependency wait.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map,
+                                            int x, int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
                                             int x, int y, uint64_t *bar) {
   asm volatile(
@@ -174,6 +192,13 @@ __device__ __forceinline__ int build_prefix(const AttnParams &p, int *prefix,
   return run;
 }
 
+// x / c for the slice arithmetic below: the products there usually fit
+// 32 bits, and a 32-bit division is a few instructions where a 64-bit one
+// is a long software routine on the start-up path.
+__device__ __forceinline__ int div_u64(unsigned long long x, unsigned c) {
+  return (int)(x <= 0xffffffffull ? (unsigned)x / c : x / c);
+}
+
 // CTAs that share the items: each slice holds at least min_pages items.
 __device__ __forceinline__ int working_ctas(int total, int min_pages) {
   long long ce = total / (min_pages > 0 ? min_pages : 1);
@@ -183,7 +208,9 @@ __device__ __forceinline__ int working_ctas(int total, int min_pages) {
 }
 
 __device__ __forceinline__ int slice_begin(int cta, int total, int n_ctas) {
-  return cta < n_ctas ? (int)((long long)cta * total / n_ctas) : total;
+  return cta < n_ctas
+             ? div_u64((unsigned long long)cta * (unsigned)total, (unsigned)n_ctas)
+             : total;
 }
 
 // The first segment with pages at or after flat item `pos` of this CTA's
@@ -216,8 +243,10 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   ui.rg = gi - ui.g * p.n_rg;
   ui.n_pages = min(range_end - ui.item0, np - ui.page0);
   // CTAs that own the group's first and last pages
-  ui.f = (int)(((long long)(gfirst + 1) * n_ctas - 1) / total);
-  ui.l = (int)(((long long)(gfirst + np) * n_ctas - 1) / total);
+  ui.f = div_u64((unsigned long long)(gfirst + 1) * (unsigned)n_ctas - 1u,
+                 (unsigned)total);
+  ui.l = div_u64((unsigned long long)(gfirst + np) * (unsigned)n_ctas - 1u,
+                 (unsigned)total);
   ui.slot = (int)blockIdx.x == ui.f ? 1 : 0;
   (void)first;
   ui.seq_len = seqlen[b];
@@ -433,14 +462,35 @@ inline bool make_row_map(CUtensorMap *map, const void *base, long long rows,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q [positions = batch * q_len, Hq, d] as a 3-D bf16 tensor whose boxes
+// are 64 columns (128-byte swizzled) of bh consecutive heads at bp
+// consecutive positions: the rows of a query-row unit in one copy per
+// 64-column half (they land as [bp][bh] rows of 128 bytes).
+inline bool make_q_map(CUtensorMap *map, const void *base, long long positions,
+                       int hq, int d, int bh, int bp) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || positions <= 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq,
+                              (cuuint64_t)positions};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kBoxElems, (cuuint32_t)bh,
+                             (cuuint32_t)bp};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Encoded tensor maps of recent calls, keyed by everything they encode
 // (kind 0: make_kv_map(base, a = num_blocks, b = hkv, d); kind 1:
-// make_row_map(base, a = rows, d)), so repeated calls on the same buffers
+// make_row_map(base, a = rows, d); kind 2: make_q_map(base, a = positions,
+// b = hq, d, e = bh * 65536 + bp)), so repeated calls on the same buffers
 // skip the driver's encoder.
 inline bool cached_map(CUtensorMap *map, int kind, const void *base,
-                       long long a, int b, int d) {
+                       long long a, int b, int d, int e = 0) {
   struct Entry {
-    int kind, b, d;
+    int kind, b, d, e;
     const void *base;
     long long a;
     CUtensorMap map;
@@ -452,24 +502,27 @@ inline bool cached_map(CUtensorMap *map, int kind, const void *base,
   {
     std::lock_guard<std::mutex> lk(mu);
     for (int i = 0; i < filled; ++i) {
-      const Entry &e = cache[i];
-      if (e.kind == kind && e.base == base && e.a == a && e.b == b && e.d == d) {
-        *map = e.map;
+      const Entry &en = cache[i];
+      if (en.kind == kind && en.base == base && en.a == a && en.b == b &&
+          en.d == d && en.e == e) {
+        *map = en.map;
         return true;
       }
     }
   }
-  const bool ok = kind == 0 ? make_kv_map(map, base, (int)a, b, d)
-                            : make_row_map(map, base, a, d);
+  const bool ok = kind == 0   ? make_kv_map(map, base, (int)a, b, d)
+                  : kind == 1 ? make_row_map(map, base, a, d)
+                              : make_q_map(map, base, a, b, d, e >> 16, e & 0xFFFF);
   if (!ok) return false;
   std::lock_guard<std::mutex> lk(mu);
-  Entry &e = cache[next];
-  e.kind = kind;
-  e.b = b;
-  e.d = d;
-  e.base = base;
-  e.a = a;
-  e.map = *map;
+  Entry &en = cache[next];
+  en.kind = kind;
+  en.b = b;
+  en.d = d;
+  en.e = e;
+  en.base = base;
+  en.a = a;
+  en.map = *map;
   next = (next + 1) % kEntries;
   if (filled < kEntries) ++filled;
   return true;

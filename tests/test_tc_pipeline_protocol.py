@@ -23,21 +23,26 @@ modes are modelled:
 * one row group per tile: two groups on alternate tiles, three stages, P in
   a buffer per group, state handed from group 1 to group 0 at a segment's
   end;
-* two row groups: both groups on every tile, three stages, S
-  double-buffered per group with one barrier per S buffer parity committed
-  after both groups' S MMAs of a tile, each group's P written into the
-  stage's K tile (free once both S MMAs have completed), a segment's output
-  staged there too; a stage goes back to the producer after two arrivals:
-  a commit after each group's P V, or for a segment's last tile each
-  group's own arrival once its staged output has been read.
+* two row groups: both groups on every tile, three stages, one S MMA per
+  tile for both groups into a double-buffered S with one barrier per S
+  buffer parity, each group's P written into the stage's K tile (free once
+  the S MMA has completed) as rows of one operand shared by both groups, a
+  segment's output staged there too (over both groups' P); one P V per
+  tile for both groups, issued once both groups' P are written, followed
+  by a commit to each group's O barrier and, except on a segment's last
+  tile, two commits to the stage's empty barrier; a segment's last stage
+  goes back to the producer on each group's own arrival once its staged
+  output has been read.
 
 Controls show the model finds the hazards the kernel avoids: a single S
-barrier for all tiles (instead of one per parity) laps, committing each
-group's S separately lets a group overwrite K while the other group's S
-MMA still reads it, releasing a segment's last stage right after its P V
-lets the producer overwrite the staged output, and issuing Q only when its
-release has been seen (without waiting for it before blocking on a stage
-of the same segment) deadlocks.
+barrier for all tiles (instead of one per parity) laps, separate S MMAs
+with a commit each let a group overwrite K while the other group's S MMA
+still reads it, releasing a segment's last stage right after its P V lets
+the producer overwrite the staged output, issuing the shared P V once one
+group's P is written reads the other group's rows before they are (or its
+O before it is folded), and
+issuing Q only when its release has been seen (without waiting for it
+before blocking on a stage of the same segment) deadlocks.
 """
 import random
 
@@ -82,7 +87,7 @@ class Hazard(Exception):
 
 
 def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
-        separate_s_commits=False, early_release=False):
+        separate_s_commits=False, early_release=False, pv_on_one_p=False):
     rnd = random.Random(seed)
     ST = 3
     segs = [rnd.randint(1, 7) for _ in range(rnd.randint(1, 6))]
@@ -148,13 +153,14 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
                     assert qbuf[0] == seg_of[c], ("S reads Q", qbuf[0], seg_of[c])
                     if dual and kpart[s] != ["K", "K"]:
                         raise Hazard(f"S({c}) reads K overwritten: {kpart[s]}")
-                    sbuf[(g, c & 1) if dual else g] = c
+                    for gg in ((0, 1) if g is None else (g,)):
+                        sbuf[(gg, c & 1) if dual else gg] = c
+                elif g is None:  # both groups' P V: one operand of both P
+                    if kpart[s] != [("P", c), ("P", c)]:
+                        raise Hazard(f"P V({c}) reads {kpart[s]}")
+                    obuf[0] = obuf[1] = c
                 else:
-                    if dual:
-                        if kpart[s][g] != ("P", c):
-                            raise Hazard(f"P V({g},{c}) reads {kpart[s][g]}")
-                    else:
-                        assert pbuf[g] == c, ("P V reads P", pbuf[g], c)
+                    assert pbuf[g] == c, ("P V reads P", pbuf[g], c)
                     obuf[g] = c
             while pipe and pipe[0][0] == "commit":
                 commits.append(pipe.pop(0)[1])
@@ -215,13 +221,13 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
                 else p_obs[0] >= c_s - 1
             if (left > 0 and ready and full[c_s % ST].test((c_s // ST) & 1)
                     and (not first or q_full.test((us - 1) & 1))):
-                if dual:
+                if dual and separate_s_commits:
                     for g in (0, 1):
                         pipe.append(("S", g, c_s))
-                        if separate_s_commits:
-                            pipe.append(("commit", s_bar(g, c_s)[0]))
-                    if not separate_s_commits:
-                        pipe.append(("commit", s_bar(0, c_s)[0]))
+                        pipe.append(("commit", s_bar(g, c_s)[0]))
+                elif dual:
+                    pipe.append(("S", None, c_s))
+                    pipe.append(("commit", s_bar(0, c_s)[0]))
                 else:
                     g = c_s & 1
                     pipe.append(("S", g, c_s))
@@ -236,17 +242,18 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
                 for g in (0, 1):
                     if p_obs[g] < c_s and p_full[g].test(p_obs[g] & 1):
                         p_obs[g] += 1
-                for g in (0, 1):
-                    if c_p[g] < p_obs[g]:
-                        c = c_p[g]
-                        pipe.append(("PV", g, c))
-                        pipe.append(("commit", o_full[g]))
-                        c_p[g] += 1
-                        # a segment's last stage goes back from the groups,
-                        # once their staged outputs were read
-                        if c not in last_tiles or early_release:
-                            pipe.append(("commit", empty[c % ST]))
-                if no_more and left == 0 and c_p[0] == c_s and c_p[1] == c_s:
+                if c_p[0] < p_obs[0] and (pv_on_one_p or c_p[0] < p_obs[1]):
+                    c = c_p[0]
+                    pipe.append(("PV", None, c))
+                    pipe.append(("commit", o_full[0]))
+                    pipe.append(("commit", o_full[1]))
+                    c_p[0] += 1
+                    # a segment's last stage goes back from the groups, once
+                    # their staged outputs were read
+                    if c not in last_tiles or early_release:
+                        pipe.append(("commit", empty[c % ST]))
+                        pipe.append(("commit", empty[c % ST]))
+                if no_more and left == 0 and c_p[0] == c_s:
                     return
             else:
                 k = p_obs[0]
@@ -296,13 +303,16 @@ def run(seed, dual, single_s_barrier=False, lazy_q_only=False, R=4,
                 yield from wait(o_full[g], o_phase(prev))
                 assert obuf[g] == prev
             if dual:
-                # the group's output is staged in its part of the last
-                # tile's K, read by the bulk stores, then released
+                # the group's output is staged in the last tile's K (over
+                # rows of both groups' P), read by the bulk stores, then
+                # released
                 s = prev % ST
                 if w == 0:
                     if stage[s] != prev:
                         raise Hazard(f"staging in stage {s} now holding {stage[s]}")
                     kpart[s][g] = ("out", us)
+                    kpart[s][1 - g] = ("out", us) if kpart[s][1 - g] == ("P", prev) \
+                        else kpart[s][1 - g]
                     yield
                     if kpart[s][g] != ("out", us) or stage[s] != prev:
                         raise Hazard(f"staged output of segment {us} overwritten")
@@ -383,6 +393,20 @@ def test_releasing_a_segments_last_stage_early_overwrites_its_output():
         try:
             run(seed, True, early_release=True)
         except Hazard:
+            failures += 1
+    assert failures > 0
+
+
+def test_shared_p_v_issued_on_one_groups_p_reads_unwritten_rows():
+    """Control: the P V that serves both groups issued as soon as group 0's
+    P is written reads group 1's rows before group 1 has written them, or
+    overwrites group 1's O before group 1 has folded it (its O barrier then
+    laps, or its arrivals run ahead of its waits)."""
+    failures = 0
+    for seed in range(400):
+        try:
+            run(seed, True, pv_on_one_p=True)
+        except (Hazard, AssertionError, Lap, Stuck):
             failures += 1
     assert failures > 0
 
