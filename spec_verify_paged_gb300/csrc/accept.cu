@@ -67,6 +67,7 @@ constexpr int kAcceptPieces = SVP_ACCEPT_PIECES;
 constexpr float kL2E = 1.4426950408889634f;
 constexpr int kNoExp = INT_MIN / 4;  // reference exponent of an empty sum
 static_assert(2 * kMaxNodes - 1 <= kMaxRows, "tree rows exceed the row arrays");
+static_assert(kMaxRows <= 127, "staged row indices are kept in bytes");
 
 // A sum of exp2 terms relative to 2^e, as a compensated fp32 pair.
 struct ESum {
@@ -237,7 +238,8 @@ static_assert(offsetof(DrawShared, mass_hi) == 0 &&
 // it % slots of the dynamic shared memory xs.  With bulk (16-byte aligned
 // rows) thread 0 moves items with 1-D bulk copies, a wave of `slots` at a
 // time; otherwise all threads copy with plain loads.  When every item has a
-// slot, the rows stay resident after pass 1.
+// slot, the rows stay resident after pass 1; with whole-row items the last
+// `slots` rows do (the ones a caller stages last).
 template <class RowPtr, class Filter = NoFilter, bool ARGMAX = false>
 struct SliceStage {
   RowPtr row_ptr;
@@ -251,9 +253,13 @@ struct SliceStage {
   __device__ int piece_len(int pc) const { return min(psz, n - pc * psz); }
   // every item has its own slot: row r's pieces are consecutive slots
   __device__ bool resident() const { return slots >= items(); }
-  // row r of the slice: shared memory when resident, else global memory
+  // row r of the slice: shared memory while a slot still holds it (every
+  // row when all are resident; with whole-row items, a row no later row
+  // has replaced), else global memory
   __device__ const float *row(int r) const {
-    return resident() ? xs + (size_t)r * np * psz : row_ptr(r) + s0;
+    if (resident()) return xs + (size_t)r * np * psz;
+    if (np == 1 && r + slots >= R) return xs + (size_t)(r % slots) * psz;
+    return row_ptr(r) + s0;
   }
 
   __device__ void issue(int it) const {  // thread 0, bulk mode
@@ -626,10 +632,15 @@ struct AcceptShared {
 struct TreeShared {
   StageShared st;
   DrawShared ds;
-  int par[kMaxNodes], tok[kMaxNodes];
-  int drow[kMaxNodes];     // staged draft row of an inner node, else -1
-  int rowsrc[kMaxRows];    // node whose draft row a staged row r >= N is
-  int path[kMaxNodes];     // accepted nodes
+  int tok[kMaxNodes];
+  // node and row indices fit a byte (the static shared memory stays small
+  // enough for three CTAs per SM)
+  int8_t par[kMaxNodes];
+  int8_t trow[kMaxNodes];    // staged target row of a node
+  int8_t drow[kMaxNodes];    // staged draft row of an inner node, else -1
+  int8_t lastc[kMaxNodes];   // a node's last child, else -1
+  int8_t rowsrc[kMaxRows];   // node whose target (r < N) or draft row r is
+  int8_t path[kMaxNodes];    // accepted nodes
   float lx_t[kMaxNodes];   // target / draft logits of node c's token in the
   float lx_d[kMaxNodes];   // rows of its parent
   float zinv[kMaxNodes];   // 1 / residual mass after each rejected child
@@ -876,8 +887,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
   const float *dl = p.draft_logits + (size_t)b * N * V;
 
   // the tree: warp 0 reads parents and tokens, checks them, and lists the
-  // rows to stage -- the target rows of all nodes (0 .. N-1), then the
-  // draft rows of the inner nodes (the rows their children came from)
+  // rows to stage -- the target rows of all nodes, then the draft rows of
+  // the inner nodes (the rows their children came from).  Leaves' target
+  // rows go first and inner nodes' rows in decreasing node order, so the
+  // rows that stay in shared memory after pass 1 (the last ones staged)
+  // are those the walk from the root reads first
   if (warp == 0) {
     int pa = -1, tk = -1;
     float uv = 0.f;
@@ -891,16 +905,26 @@ __global__ void __launch_bounds__(kAThreads, 3)
                                : (pa < 0 || pa >= lane || tk < 0 || tk >= V));
     const unsigned bad_mask = __ballot_sync(0xffffffffu, bad_l);
     unsigned inner = 0;  // nodes with a child
+    int lastc = -1;      // this lane's node's last child
     for (int c = 1; c < N; ++c) {
       const int pc = __shfl_sync(0xffffffffu, pa, c);
       if (pc >= 0 && pc < c) inner |= 1u << pc;
+      if (pc == lane) lastc = c;
     }
     if (lane < N) {
       sh.par[lane] = pa;
       sh.tok[lane] = tk;
       sh.u[lane] = uv;
+      sh.lastc[lane] = lastc;
       const bool in = (inner >> lane) & 1u;
-      const int r = N + __popc(inner & ((1u << lane) - 1u));
+      const unsigned below = (1u << lane) - 1u;      // nodes before this one
+      const unsigned above = ~((2u << lane) - 1u);   // nodes after it
+      const unsigned leaves = ((1u << N) - 1u) & ~inner;
+      const int tr = in ? __popc(leaves) + __popc(inner & above)
+                        : __popc(leaves & below);
+      sh.trow[lane] = tr;
+      sh.rowsrc[tr] = lane;
+      const int r = N + __popc(inner & above);
       sh.drow[lane] = in ? r : -1;
       if (in) sh.rowsrc[r] = lane;
     }
@@ -912,9 +936,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
   __syncthreads();
   const int R = sh.R;
   const bool bad = sh.bad != 0;
-  const int *rowsrc = sh.rowsrc;
+  const int8_t *rowsrc = sh.rowsrc;
   auto row_ptr = [=](int r) -> const float * {
-    return r < N ? tl + (size_t)r * V : dl + (size_t)rowsrc[r] * V;
+    return (r < N ? tl : dl) + (size_t)rowsrc[r] * V;
   };
   const SliceStage<decltype(row_ptr)> stage{
       row_ptr, R, s0, n, psz, np, slots, bulk, xs, &sh.st, NoFilter{}, kL2E};
@@ -953,12 +977,16 @@ __global__ void __launch_bounds__(kAThreads, 3)
       for (int jj = 0; jj < k; ++jj) r = fmaxf(r - q, 0.f) * sh.zinv[jj];
       return r;
     };
+    // a node's last child rejected: the draw weighs max(0, r_k - q)
+    // unnormalised (the draw takes its own total), so its mass Z, a
+    // cluster-wide sum, is not formed
+    bool lazy = false;
     for (;;) {
-      const int rd = sh.drow[cur];
-      xt = stage.row(cur);
-      xd = stage.row(rd >= 0 ? rd : cur);
-      et = (float)sh.st.row_e[cur];
-      it_ = 1.f / sh.st.row_s[cur];
+      const int rt = sh.trow[cur], rd = sh.drow[cur];
+      xt = stage.row(rt);
+      xd = stage.row(rd >= 0 ? rd : rt);
+      et = (float)sh.st.row_e[rt];
+      it_ = 1.f / sh.st.row_s[rt];
       ed = rd >= 0 ? (float)sh.st.row_e[rd] : 0.f;
       id_ = rd >= 0 ? 1.f / sh.st.row_s[rd] : 0.f;
       k = 0;
@@ -966,8 +994,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
       for (int c = cur + 1; c < N && rd >= 0; ++c) {  // CTA-uniform
         if (sh.par[c] != cur) continue;
         // r_k(x) / q(x) = max(0, r_{k-1}(x)/q(x) - 1) / Z_k, from p/q
-        float ratio = accept_ratio(sh.lx_t[c], sh.lx_d[c], sh.st.row_e[cur],
-                                   sh.st.row_s[cur], sh.st.row_e[rd],
+        float ratio = accept_ratio(sh.lx_t[c], sh.lx_d[c], sh.st.row_e[rt],
+                                   sh.st.row_s[rt], sh.st.row_e[rd],
                                    sh.st.row_s[rd], kL2E);
         for (int jj = 0; jj < k; ++jj)
           ratio = fmaxf(ratio - 1.f, 0.f) * sh.zinv[jj];
@@ -976,16 +1004,19 @@ __global__ void __launch_bounds__(kAThreads, 3)
           break;
         }
         // rejected: the residual's mass Z = sum max(0, r_k - q)
-        float zh, zl;
-        cluster_sum<NC>(
-            cluster, sh.ds, scratch,
-            [&](int e) {
-              float q;
-              const float r = rk(e, q);
-              return fmaxf(r - q, 0.f);
-            },
-            e0, e1, tid, lane, warp, parity, zh, zl);
-        parity ^= 1;
+        float zh = 1.f, zl = 0.f;
+        lazy = c == sh.lastc[cur];
+        if (!lazy) {
+          cluster_sum<NC>(
+              cluster, sh.ds, scratch,
+              [&](int e) {
+                float q;
+                const float r = rk(e, q);
+                return fmaxf(r - q, 0.f);
+              },
+              e0, e1, tid, lane, warp, parity, zh, zl);
+          parity ^= 1;
+        }
         if (zh > 0.f) {  // else (impossible in exact arithmetic) keep r_k
           __syncthreads();  // zinv[k] is not being read
           if (tid == 0) sh.zinv[k] = 1.f / (zh + zl);
@@ -998,11 +1029,15 @@ __global__ void __launch_bounds__(kAThreads, 3)
       ++n_acc;
       cur = next;
     }
-    // one token from r_k of the last node (p itself at a leaf)
+    // one token from r_k of the last node (p itself at a leaf); a zero
+    // mass by rounding falls back to r_{k-1} (when r_k's mass was not
+    // formed: where a zero Z would have left it), then to p
     int32_t *dst = p.out_tokens + (size_t)b * N + n_acc;
     const float u0 = sh.u[0];
-    for (int attempt = 0; attempt < 2 && !arrived; ++attempt) {
-      if (attempt == 1) k = 0;  // zero mass by rounding: fall back to p
+    const int tries[3] = {k, lazy ? k - 1 : -1, 0};
+    for (int t = 0; t < 3 && !arrived; ++t) {
+      if (tries[t] < 0 || (t == 2 && tries[1] == 0)) continue;
+      k = tries[t];
       arrived = draw_token<NC>(
           cluster, sh.ds, scratch,
           [&](int e) {
