@@ -255,7 +255,7 @@ static int attention_call(const svp_dims *dims, const void *q,
                           const int32_t *block_table, const int32_t *seq_lens,
                           int q_len, int n_sink, int window,
                           const uint32_t *tree_mask, float scale, void *out,
-                          float *lse, cudaStream_t stream) {
+                          float *lse, cudaStream_t stream, int early = 0) {
   t_last_launches = 0;
   int st = check_attention_args(dims, q_len, n_sink, window, scale);
   if (st != SVP_OK) return st;
@@ -324,6 +324,9 @@ static int attention_call(const svp_dims *dims, const void *q,
     p.qscale = scale * 1.4426950408889634f * (fp8 ? dims->k_scale : 1.0f);
     p.v_scale = fp8 ? dims->v_scale : 1.0f;
     p.tree_mask = tree_mask ? tree_mask + (size_t)b0 * q_len : nullptr;
+    // only the first launch follows the append: a later one follows the
+    // previous launch's merge, which reads the workspace it would reset
+    p.early = early && b0 == 0;
     AttnPlan sub = plan;
     if (nb != bl) {
       plan_attention(nb, dims->num_q_heads, dims->num_kv_heads,
@@ -357,11 +360,11 @@ int paged_decode_attention(const svp_dims *dims, const void *q,
                         stream);
 }
 
-int paged_tree_attention(const svp_dims *dims, const void *q,
-                         const void *k_cache, const void *v_cache,
-                         const int32_t *block_table, const int32_t *seq_lens,
-                         int q_len, const uint32_t *tree_mask, float scale,
-                         void *out, float *lse, cudaStream_t stream) {
+static int tree_call(const svp_dims *dims, const void *q, const void *k_cache,
+                     const void *v_cache, const int32_t *block_table,
+                     const int32_t *seq_lens, int q_len,
+                     const uint32_t *tree_mask, float scale, void *out,
+                     float *lse, cudaStream_t stream, int early) {
   t_last_launches = 0;
   const int st = check_attention_args(dims, q_len, 0, 0, scale);
   if (st != SVP_OK) return st;
@@ -369,7 +372,16 @@ int paged_tree_attention(const svp_dims *dims, const void *q,
   if (!tree_mask || reinterpret_cast<uintptr_t>(tree_mask) % 4 != 0)
     return SVP_ERR_INVALID_ARG;
   return attention_call(dims, q, k_cache, v_cache, block_table, seq_lens,
-                        q_len, 0, 0, tree_mask, scale, out, lse, stream);
+                        q_len, 0, 0, tree_mask, scale, out, lse, stream, early);
+}
+
+int paged_tree_attention(const svp_dims *dims, const void *q,
+                         const void *k_cache, const void *v_cache,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         int q_len, const uint32_t *tree_mask, float scale,
+                         void *out, float *lse, cudaStream_t stream) {
+  return tree_call(dims, q, k_cache, v_cache, block_table, seq_lens, q_len,
+                   tree_mask, scale, out, lse, stream, 0);
 }
 
 int kv_append(const svp_dims *dims, const void *k_new, const void *v_new,
@@ -505,3 +517,21 @@ int svp_read_device_status(cudaStream_t stream, int *flags) {
 }
 
 }  // extern "C"
+
+namespace svp {
+
+int attention_after_append(const svp_dims *dims, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window,
+                           const uint32_t *tree_mask, float scale, void *out,
+                           float *lse, cudaStream_t stream) {
+  if (tree_mask)
+    return tree_call(dims, q, k_cache, v_cache, block_table, seq_lens, q_len,
+                     tree_mask, scale, out, lse, stream, 1);
+  return attention_call(dims, q, k_cache, v_cache, block_table, seq_lens,
+                        q_len, n_sink, window, nullptr, scale, out, lse, stream,
+                        1);
+}
+
+}  // namespace svp

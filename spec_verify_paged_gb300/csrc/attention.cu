@@ -611,8 +611,11 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
   }
   __syncthreads();  // barriers initialised
   // launched early (programmatic dependent launch): nothing in global
-  // memory is touched before the previous kernel on the stream is done
-  pdl_wait();
+  // memory is touched before the previous kernel on the stream is done --
+  // or, right behind the append of the newest positions (p.early), nothing
+  // but the pages holding them (the producer waits before the first batch
+  // with such a page, the consumers before their first output)
+  if (!p.early) pdl_wait();
   if (tid == 0) {
     p.desc[blockIdx.x].valid = 0;  // until a split group starts
     pdl_launch_dependents();       // the merge may be scheduled
@@ -633,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
                               : total_pages;
     int c = 0;   // pages issued so far
     int us = 0;  // segments published so far
+    bool waited = !p.early;  // the grid-dependency wait is behind us
     bool ok = true;
     int pos = range_begin;
     while (true) {
@@ -699,6 +703,14 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
             }
 #endif
             const int left = min(min(32 - kk, n_pages - k), MAXB);
+            if (!waited) {
+              const int pl = page0 + k + left - 1;  // the batch's last page
+              const int lb = pl < na ? pl : bs + (pl - na);
+              if ((lb + 1) * kBlockSize > seg.seq_len - p.q_len) {
+                pdl_wait();  // it may hold some of the appended positions
+                waited = true;
+              }
+            }
             // lane i: page c + i's block (arming), and the page of this
             // lane's copy
             const int ph_i = __shfl_sync(kFull, phys[k4], min(kk + lane, 31));
@@ -1011,6 +1023,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
       c += ui.n_pages;
 
       // ---- epilogue: merge the 4 warps' states ----
+      if (p.early) pdl_wait();  // outputs are written from here on
       if (!epi_sync(sm, epi_phase, lane) || aborted) {
         if (lane == 0) { raise_flag(SVP_DEV_TIMEOUT); sm.abort_flag = 1; }
         break;

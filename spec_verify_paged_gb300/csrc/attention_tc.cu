@@ -487,8 +487,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();  // barriers initialised, tensor memory allocated
   tc_fence_after();
   // launched early (programmatic dependent launch): nothing in global
-  // memory is touched before the previous kernel on the stream is done
-  pdl_wait();
+  // memory is touched before the previous kernel on the stream is done --
+  // or, right behind the append of the newest positions (p.early), nothing
+  // but the pages holding them (the producer waits before the first such
+  // tile, the softmax groups before their first output)
+  if (!p.early) pdl_wait();
   if (tid == 0) {
     p.desc[blockIdx.x].valid = 0;  // until a split group starts
     pdl_launch_dependents();       // the merge may be scheduled
@@ -509,6 +512,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int c = 0;   // tiles issued so far
     int us = 0;  // segments published so far
     int q_issued = -1;  // last segment whose Q copies were issued
+    bool waited = !p.early;  // the grid-dependency wait is behind us
     bool ok = true;
     int pos = range_begin;
     while (true) {
@@ -607,6 +611,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // tiles start at multiples of 8 pages of the segment; lane kk < 8
           // copies page t0 + kk, whose entry sits in lane (t0-k0)%32 + kk
           const int npg = min(kTilePages, n_pages - t0);
+          if (!waited &&
+              (logical_block(seg, seg.page0 + t0 + npg - 1) + 1) * kBlockSize >
+                  seg.seq_len - p.q_len) {
+            pdl_wait();  // the tile holds some of the appended positions
+            waited = true;
+          }
           const int k4 = (t0 - k0) >> 5;
           const int src = k4 == 0 ? phys[0] : k4 == 1 ? phys[1]
                         : k4 == 2 ? phys[2] : phys[3];
@@ -1123,6 +1133,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(&sm.p_full[gi]);
         prev = c;
       }
+      if (p.early) pdl_wait();  // outputs are written from here on
       // ---- the group's last tile (a warp whose last fold failed skips it;
       // the vote below makes the outcome the group's) ----
       if (ok && prev >= 0) ok = fold_o(prev, o);

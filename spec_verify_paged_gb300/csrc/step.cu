@@ -91,19 +91,16 @@ int capture_slot(svp_step *s, int i) {
                    d.v_cache, (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
                    (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, s->compute);
   const bool tree = d.tree_nodes > 0;
-  if (st == SVP_OK && tree)
-    st = paged_tree_attention(
+  // attention right behind the append of its q_len newest positions: it
+  // reads the prefix pages while the append runs
+  if (st == SVP_OK)
+    st = svp::attention_after_append(
         &dims, in(SVP_STEP_Q), d.k_cache, d.v_cache,
         (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
-        (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len,
-        (const uint32_t *)in(SVP_STEP_TREE_MASK), d.scale, out(SVP_STEP_OUT),
-        (float *)out(SVP_STEP_LSE), s->compute);
-  else if (st == SVP_OK)
-    st = paged_decode_attention(
-        &dims, in(SVP_STEP_Q), d.k_cache, d.v_cache,
-        (const int32_t *)in(SVP_STEP_BLOCK_TABLE),
-        (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, d.n_sink, d.window,
-        d.scale, out(SVP_STEP_OUT), (float *)out(SVP_STEP_LSE), s->compute);
+        (const int32_t *)in(SVP_STEP_SEQ_LENS), d.q_len, tree ? 0 : d.n_sink,
+        tree ? 0 : d.window,
+        tree ? (const uint32_t *)in(SVP_STEP_TREE_MASK) : nullptr, d.scale,
+        out(SVP_STEP_OUT), (float *)out(SVP_STEP_LSE), s->compute);
   if (st == SVP_OK && tree) {
     st = spec_accept_tree(d.dims.batch, d.tree_nodes, d.vocab,
                           (const float *)in(SVP_STEP_TARGET_LOGITS),

@@ -40,6 +40,13 @@ struct AttnParams {
   float qscale;        // scale * log2(e)
   const uint32_t *tree_mask;  // [batch, q_len] ancestor bits, or null
   float v_scale;       // FP8 caches: V value = code * v_scale (else 1)
+  // 1: the previous kernel on the stream appended the q_len newest
+  // positions of these sequences and wrote nothing else this call reads,
+  // and every other input was written before it started.  The kernel then
+  // reads everything but the pages holding those positions before its
+  // grid-dependency wait, and waits before the first such page and before
+  // its first write.  0: it waits before touching global memory.
+  int early;
 };
 
 struct AttnPlan {
@@ -49,6 +56,16 @@ struct AttnPlan {
   int batch_cap;       // sequences per launch
   size_t ws_head, ws_desc, ws_part_o, ws_part_lse, ws_total;
 };
+
+// paged_decode_attention (tree_mask null) or paged_tree_attention launched
+// right after kv_append of the q_len newest positions on the same stream
+// (the fused step): the prefix pages are read while the append runs.
+int attention_after_append(const svp_dims *dims, const void *q,
+                           const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           int q_len, int n_sink, int window,
+                           const uint32_t *tree_mask, float scale, void *out,
+                           float *lse, cudaStream_t stream);
 
 // Fills the plan (no CUDA launches).  dtype 0 = f32, 1 = bf16.  Returns 0 or
 // a negative svp_status.
