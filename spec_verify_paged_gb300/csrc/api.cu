@@ -3,6 +3,7 @@
 // contract of every entry point are in include/svp.h.
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -317,7 +318,10 @@ static int attention_call(const svp_dims *dims, const void *q,
     p.rows = p.group * q_len;
     p.rb = plan.rb;
     p.n_rg = plan.n_rg;
-    p.min_pages = plan.min_pages;
+    // tcgen05: items are 8-page tiles (a slice's minimum in tiles)
+    p.ppi = plan.tc ? kTilePagesTc : 1;
+    p.min_pages = plan.tc ? std::max(1, plan.min_pages / kTilePagesTc)
+                          : plan.min_pages;
     p.seg_items = plan.seg_items;
     // an FP8 cache's K scale folds into the query scale, its V scale
     // multiplies the outputs

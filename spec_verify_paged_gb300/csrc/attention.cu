@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, (min_ctas<T, D, RB, MMA>()))
         }
       }
       if (!ok) break;
-      pos = seg.item0 + seg.n_pages;
+      pos = seg.item0 + (seg.n_pages + p.ppi - 1) / p.ppi;
       ++us;
     }
     if (!ok) {

@@ -74,6 +74,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTilePages = 8;
 constexpr int kTileKeys = kTilePages * kBlockSize;  // the MMA's M
+static_assert(kTilePages == kTilePagesTc, "stream-K items are the kernel's tiles");
 constexpr int kHalfBytes = kTileKeys * 128;  // 64 columns x 128 keys, bf16
 constexpr int kTileBytes = 2 * kHalfBytes;   // one K (or V) tile: 32 KB
 constexpr int kStages = 3;
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok) issue_q();
       }
       if (!ok) break;
-      pos = seg.item0 + seg.n_pages;
+      pos = seg.item0 + (seg.n_pages + p.ppi - 1) / p.ppi;
       ++us;
     }
     if (!ok && lane == 0) {

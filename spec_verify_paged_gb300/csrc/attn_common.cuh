@@ -156,8 +156,9 @@ __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &phase,
   return __all_sync(kFull, ok);
 }
 
-// One warp: prefix[b + 1] = items of sequences 0..b (visible pages x
-// groups per sequence) and seqlen[b] = the sequence's length (both in
+// One warp: prefix[b + 1] = items of sequences 0..b (per group: its
+// visible pages in items of p.ppi pages, plus p.seg_items; times the groups
+// per sequence) and seqlen[b] = the sequence's length (both in
 // shared memory, so decoding a segment needs no global load); returns the
 // total in every lane.  A sequence whose length is out of range contributes
 // nothing and raises SVP_DEV_BAD_SEQ_LEN.
@@ -177,7 +178,7 @@ __device__ __forceinline__ int build_prefix(const AttnParams &p, int *prefix,
       } else {
         int na, bs, np;
         visible_pages(L, p.q_len, p.n_sink, p.window, na, bs, np);
-        n = (np + p.seg_items) * groups_per_seq;
+        n = ((np + p.ppi - 1) / p.ppi + p.seg_items) * groups_per_seq;
       }
     }
     int incl = n;
@@ -215,8 +216,10 @@ __device__ __forceinline__ int slice_begin(int cta, int total, int n_ctas) {
 
 // The first segment with pages at or after flat item `pos` of this CTA's
 // slice (valid = 0 if the rest of the slice holds none); the next segment
-// starts at item0 + n_pages.  `first`: no segment of this slice came
-// before (its partial goes to slot 0, any later one to slot 1).
+// starts at item0 + ceil(n_pages / p.ppi).  An item is p.ppi pages of a
+// group (its last item possibly fewer), so a segment starts on an item
+// boundary of its group.  `first`: no segment of this slice came before
+// (its partial goes to slot 0, any later one to slot 1).
 __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
                                                    const int *prefix,
                                                    const int *seqlen,
@@ -230,29 +233,30 @@ __device__ __forceinline__ UnitInfo decode_segment(const AttnParams &p,
   }
   UnitInfo ui;
   const int b = lo;
-  const int per = (prefix[b + 1] - prefix[b]) / groups_per_seq;  // np + X
-  const int np = per - p.seg_items;
+  const int per = (prefix[b + 1] - prefix[b]) / groups_per_seq;  // nt + X
+  const int nt = per - p.seg_items;       // a group's page items
   const int qoff = pos - prefix[b];
   const int gi = qoff / per;              // group within the sequence
   const int off = qoff - gi * per;        // item within the group
-  const int gfirst = prefix[b] + gi * per + p.seg_items;  // its first page
-  ui.page0 = off < p.seg_items ? 0 : off - p.seg_items;
-  ui.item0 = gfirst + ui.page0;
+  const int gfirst = prefix[b] + gi * per + p.seg_items;  // its first page item
+  const int t0 = off < p.seg_items ? 0 : off - p.seg_items;
+  ui.seq_len = seqlen[b];
+  int np;
+  visible_pages(ui.seq_len, p.q_len, p.n_sink, p.window, ui.n_a, ui.b_start,
+                np);
+  ui.page0 = t0 * p.ppi;
+  ui.item0 = gfirst + t0;
   ui.b = b;
   ui.g = gi / p.n_rg;
   ui.rg = gi - ui.g * p.n_rg;
-  ui.n_pages = min(range_end - ui.item0, np - ui.page0);
-  // CTAs that own the group's first and last pages
+  ui.n_pages = min(min(range_end - ui.item0, nt - t0) * p.ppi, np - ui.page0);
+  // CTAs that own the group's first and last items
   ui.f = div_u64((unsigned long long)(gfirst + 1) * (unsigned)n_ctas - 1u,
                  (unsigned)total);
-  ui.l = div_u64((unsigned long long)(gfirst + np) * (unsigned)n_ctas - 1u,
+  ui.l = div_u64((unsigned long long)(gfirst + nt) * (unsigned)n_ctas - 1u,
                  (unsigned)total);
   ui.slot = (int)blockIdx.x == ui.f ? 1 : 0;
   (void)first;
-  ui.seq_len = seqlen[b];
-  int np_seq;
-  visible_pages(ui.seq_len, p.q_len, p.n_sink, p.window, ui.n_a, ui.b_start,
-                np_seq);
   ui.pad0 = ui.pad1 = ui.pad2 = 0;
   ui.valid = ui.n_pages > 0;
   return ui;

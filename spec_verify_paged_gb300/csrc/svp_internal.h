@@ -37,6 +37,8 @@ struct AttnParams {
   int n_rg;            // ceil(rows / rb)
   int min_pages;       // fewest items a CTA's slice may hold
   int seg_items;       // items that stand for a segment's fixed cost
+  int ppi;             // pages per item: 1, or the tcgen05 kernel's tile
+                       // (slices then split groups at tile boundaries)
   float qscale;        // scale * log2(e)
   const uint32_t *tree_mask;  // [batch, q_len] ancestor bits, or null
   float v_scale;       // FP8 caches: V value = code * v_scale (else 1)
@@ -74,9 +76,11 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                    int window, int split_pages, int kernel_path, int num_sms,
                    long long num_blocks, AttnPlan *plan);
 
-// Pages' worth of time a segment's fixed cost takes on the tcgen05 kernel
-// (epilogue, partial tiles at its ends): the stream-K split counts it.
-constexpr int kSegItemsTc = 12;
+// The tcgen05 kernel's stream-K items are 8-page tiles; a segment's fixed
+// cost (the masked last tile, epilogue, next Q) takes about two tiles'
+// time: the split counts it.
+constexpr int kTilePagesTc = 8;
+constexpr int kSegItemsTc = 2;
 
 // Query rows per kv head (GQA group x q_len) from which the automatic path
 // choice uses tensor cores (bf16 only): tcgen05 for head_dim 128, warp-level
