@@ -160,7 +160,7 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
   plan->tc = tc;
   plan->batch_cap = tc ? tc_batch_cap() : kBatchPerLaunch;
   plan->min_pages = min_pages;
-  plan->seg_items = tc ? kSegItemsTc : 0;
+  plan->seg_items = tc ? kSegItemsTc : kSegItemsCc;
   plan->grid = (int)grid;
   plan->ctas_per_sm = ctas;
   plan->ws_head = 256;
@@ -199,7 +199,7 @@ static int plan_call(const svp_dims *d, int q_len, int n_sink, int window,
   if (path < 0) return path;
   const int cap = path == SVP_PATH_TCGEN05 ? tc_batch_cap() : kBatchPerLaunch;
   const int bl = batch_per_launch(d, q_len, n_sink, window, cap,
-                                  path == SVP_PATH_TCGEN05 ? kSegItemsTc : 0);
+                                  path == SVP_PATH_TCGEN05 ? kSegItemsTc : kSegItemsCc);
   const int st = plan_attention(bl, d->num_q_heads, d->num_kv_heads,
                                 d->head_dim, d->dtype, d->max_blocks_per_seq,
                                 q_len, n_sink, window, d->split_pages, path,

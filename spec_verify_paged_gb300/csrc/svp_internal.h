@@ -81,6 +81,10 @@ int plan_attention(int batch, int num_q_heads, int num_kv_heads, int head_dim,
 // time: the split counts it.
 constexpr int kTilePagesTc = 8;
 constexpr int kSegItemsTc = 2;
+// The CUDA-core kernel's items are pages; a segment's epilogue (the four
+// warps' states merged through shared memory, the rows written out) is
+// counted as this many pages.
+constexpr int kSegItemsCc = 12;
 
 // Query rows per kv head (GQA group x q_len) from which the automatic path
 // choice uses tensor cores (bf16 only): tcgen05 for head_dim 128, warp-level
