@@ -132,9 +132,11 @@ typedef enum {
  * q_len: 1 (decode) .. 16 (verify of q_len-1 drafts + bonus position).
  * Work: every CTA of one persistent launch takes an equal slice of all
  * visible pages of all (sequence, kv head) groups (at least
- * dims->split_pages pages each); a group that spans several slices is
- * finished by a second kernel, launched as a programmatic dependent of the
- * first, which merges the slices' partial results by log-sum-exp.
+ * dims->split_pages pages each; each group also counts a few pages' worth
+ * for its fixed cost, and the TCGEN05 path slices in 8-page tiles); a
+ * group that spans several slices is finished by a second kernel, launched
+ * as a programmatic dependent of the first, which merges the slices'
+ * partial results by log-sum-exp.
  * Workspace: paged_decode_workspace_size() bytes, passed in dims; it needs
  * no initialisation: each CTA rewrites the split record it owns in every
  * launch, and the merge kernel reads partials only where a record of the
