@@ -82,6 +82,8 @@ SWEEP = [
     ("bf16", 128, 4, 4, 3, 3, 300, 20, 5, 2),     # sinks span 2 pages
     ("f32", 64, 2, 2, 2, 2, 200, 0, 1, 0),        # window 1: own key only
     ("bf16", 128, 8, 8, 1, 1, 64, 100, 8, 0),     # n_sink beyond the length
+    ("bf16", 128, 12, 4, 3, 3, 300, 0, 0, 0),     # GQA group 3: Q row by row
+    ("bf16", 128, 128, 1, 1, 1, 200, 0, 0, 0),    # group 128: two 64-row units
 ]
 
 
